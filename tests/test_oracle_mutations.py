@@ -1,0 +1,141 @@
+"""Planted mistakes: each test swaps one oracle function for a plausibly wrong version
+(on the CPU, inside the oracle only) and checks that at least one pin then fails."""
+import numpy as np
+import pytest
+
+import oracle as O
+import oracle.kvq_oracle as K
+import tests.test_oracle_pins as P
+
+
+def _fails(fn, *args, **kw):
+    try:
+        fn(*args, **kw)
+    except (AssertionError, IndexError, ValueError):
+        return True
+    return False
+
+
+def test_rope_sign_flip_is_caught(monkeypatch, golden_dir):
+    orig = K.rope
+    monkeypatch.setattr(K, "rope", lambda x, pos, theta=10000.0: orig(x, -np.asarray(pos), theta))
+    monkeypatch.setattr(O, "rope", K.rope)
+    assert _fails(P.test_rope_norm_identity_and_relative_position, golden_dir)
+
+
+def test_rope_rotate_half_layout_is_caught(monkeypatch, golden_dir):
+    def rotate_half(x, positions, theta=10000.0):
+        x = np.asarray(x, np.float64)
+        ang = K.rope_angles(positions, theta, x.shape[-1])
+        c, s = np.cos(ang), np.sin(ang)
+        x0, x1 = x[..., :64], x[..., 64:]
+        return np.concatenate([c * x0 - s * x1, s * x0 + c * x1], axis=-1)
+    monkeypatch.setattr(K, "rope", rotate_half)
+    monkeypatch.setattr(O, "rope", rotate_half)
+    assert _fails(P.test_rope_norm_identity_and_relative_position, golden_dir)
+
+
+def test_rtn_axis_swap_in_cache_is_caught(monkeypatch):
+    orig = K.rtn_quantize
+    monkeypatch.setattr(K, "rtn_quantize", lambda x, bits, axis: orig(x, bits, 1 - axis))
+    assert _fails(P.test_cache_decode_equals_plain_attention_on_lossless_inputs, "rtn", 1, False)
+
+
+def test_rtn_floor_instead_of_rint_is_caught(monkeypatch):
+    def enc(x, s16, z16, bits):
+        t = np.float32(x) / s16.astype(np.float32) - z16.astype(np.float32)
+        return np.clip(np.floor(t), 0, 2 ** bits - 1).astype(np.uint8)
+    monkeypatch.setattr(K, "rtn_encode", enc)
+    assert _fails(P.test_rtn_error_bound, 2, 0)
+
+
+def test_missing_sqrt_d_is_caught(monkeypatch):
+    def att(q, Kx, V):
+        s = np.asarray(q, np.float64) @ np.asarray(Kx, np.float64).T
+        p = np.exp(s - s.max(axis=-1, keepdims=True))
+        return (p @ V) / p.sum(axis=-1, keepdims=True)
+    monkeypatch.setattr(K, "attention", att)
+    monkeypatch.setattr(O, "attention", att)
+    assert _fails(P.test_attention_brute_force, 127)
+
+
+def test_argmin_last_index_tie_is_caught(monkeypatch):
+    def enc(t, cb):
+        d = np.abs(np.float32(t)[..., None] - np.float32(cb))
+        return (len(cb) - 1 - np.argmin(d[..., ::-1], axis=-1)).astype(np.uint8)
+    monkeypatch.setattr(K, "nuq_encode", enc)
+    monkeypatch.setattr(O, "nuq_encode", enc)
+    assert _fails(P.test_nuq_argmin_equals_brute_force)
+
+
+def test_pack_msb_first_is_caught(monkeypatch, golden_dir):
+    def pack(codes, bits):
+        n = 32 // bits
+        W = -(-128 // n)
+        out = np.zeros(np.shape(codes)[:-1] + (W,), np.uint64)
+        for i in range(128):
+            out[..., i // n] |= np.asarray(codes)[..., i].astype(np.uint64) << np.uint64(bits * (n - 1 - i % n))
+        return out.astype(np.uint32)
+    monkeypatch.setattr(K, "pack_rows", pack)
+    monkeypatch.setattr(O, "pack_rows", pack)
+    assert _fails(P.test_3bit_layout_printed_words, golden_dir)
+
+
+def test_varn_column_only_is_caught(monkeypatch):
+    def varn_cols(X, iters=8):
+        Y = np.array(X, np.float64)
+        lc = np.zeros(Y.shape[1])
+        for _ in range(iters):
+            sc = Y.std(axis=0)
+            Y /= sc
+            lc += np.log(sc)
+        return Y, np.ones(Y.shape[0]), np.exp(lc)
+    monkeypatch.setattr(K, "varn", varn_cols)
+    monkeypatch.setattr(O, "varn", varn_cols)
+    assert _fails(P.test_varn_recomposition_and_stds)
+
+
+def test_hadamard_unnormalised_is_caught(monkeypatch):
+    monkeypatch.setattr(K, "fwht", lambda x: np.asarray(x, np.float64) @ K.hadamard(x.shape[-1]))
+    monkeypatch.setattr(O, "fwht", K.fwht)
+    assert _fails(P.test_hadamard_sylvester_and_orthogonality)
+
+
+def test_int4_asymmetric_clamp_is_caught(monkeypatch):
+    orig = K.int4_quantize
+    def q8(x):
+        q, s = orig(x)
+        return np.where(q == -7, -8, q).astype(np.int8), s
+    monkeypatch.setattr(K, "int4_quantize", q8)
+    monkeypatch.setattr(O, "int4_quantize", q8)
+    assert _fails(P.test_int4_codes_range_and_bound)
+
+
+def test_outlier_tie_break_reversed_is_caught(monkeypatch):
+    def mask_rev(x, n_out):
+        mag = (np.asarray(x, np.float32).astype(np.float16).view(np.uint16) & 0x7FFF).ravel()
+        idx = np.arange(mag.size)
+        order = np.lexsort((-idx, -mag.astype(np.int64)))
+        m = np.zeros(mag.size, bool)
+        m[order[:n_out]] = True
+        return m.reshape(np.shape(x))
+    monkeypatch.setattr(K, "outlier_mask", mask_rev)
+    monkeypatch.setattr(O, "outlier_mask", mask_rev)
+    assert _fails(P.test_outlier_selection_planted_and_ties)
+
+
+def test_gqa_mapping_interleaved_is_caught(monkeypatch):
+    orig = K.OracleCache.decode
+    def dec(self, q, tail_k=None, tail_v=None, only_heads=None):
+        G = self.n_q_heads // self.n_kv_heads
+        qq = np.asarray(q).copy()
+        if G > 1:       # read KV head j % H_kv instead of j // G
+            idx = np.array([(j % self.n_kv_heads) * G + (j // self.n_kv_heads) for j in range(self.n_q_heads)])
+            qq = qq[:, idx]
+            out = orig(self, qq, tail_k, tail_v, only_heads)
+            res = np.empty_like(out)
+            res[:, idx] = out
+            return res
+        return orig(self, q, tail_k, tail_v, only_heads)
+    monkeypatch.setattr(K.OracleCache, "decode", dec)
+    assert _fails(P.test_cache_decode_equals_plain_attention_on_lossless_inputs, "rtn", 4, False)

@@ -1,0 +1,513 @@
+"""Pins of the CPU oracle against what the pages and mathematics fix (no GPU).
+
+Each test ties an oracle function to something other than itself: a value the pages
+print (tests/golden/*.json), a closed form, an invariant, a library routine, or brute
+force on tiny inputs.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+import scipy.stats
+
+import oracle as O
+import workloads as WL
+
+
+def _golden(golden_dir, name):
+    with open(os.path.join(golden_dir, name)) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ KV-cache size formula
+
+def test_kv_cache_size_formula_matches_printed_values(golden_dir):
+    g = _golden(golden_dir, "kv_cache_sizes.json")
+    for c in g["cases"]:
+        got = O.kv_cache_bytes(c["layers"], c["heads"], c["head_dim"], c["elem_bytes"],
+                               c["batch"], c["seq_len"])
+        assert abs(got - c["printed_bytes"]) <= c["tolerance_rel"] * c["printed_bytes"] + 0.5, c["cite"]
+    # LLaMA-7B at 128K is exactly 64 GiB
+    assert O.kv_cache_bytes(32, 32, 128, 2, 1, 131072) == 64 * 2 ** 30
+
+
+# ------------------------------------------------------------------ packing layout
+
+def test_3bit_layout_printed_words(golden_dir):
+    g = _golden(golden_dir, "kvquant_3bit_layout.json")
+    assert O.codes_per_word(3) == g["codes_per_word"]
+    for c in g["cases"]:
+        row = np.zeros(128, np.uint8)
+        row[:10] = c["codes"]
+        words = O.pack_rows(row[None, :], 3)[0]
+        assert int(words[0]) == c["word"], c["cite"]
+        assert int(words[0]) >> 30 == 0
+    assert 128 * 3 == g["bits_per_128_channel_key"]["value"]
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_pack_roundtrip_and_unused_bits(bits):
+    rng = np.random.default_rng(bits)
+    codes = rng.integers(0, 2 ** bits, size=(64, 128)).astype(np.uint8)
+    words = O.pack_rows(codes, bits)
+    n = 32 // bits
+    assert words.shape == (64, -(-128 // n))
+    assert np.array_equal(O.unpack_rows(words, bits), codes)
+    used = n * bits
+    if used < 32:
+        assert np.all((words >> np.uint32(used)) == 0)
+    # the last word of a 3-bit row holds codes 120..127 only
+    if bits == 3:
+        assert np.all((words[:, 12] >> np.uint32(24)) == 0)
+    # field i of word w is code w*n + i: check one element by direct bit reading
+    assert ((int(words[5, 1]) >> (bits * 2)) & ((1 << bits) - 1)) == codes[5, n + 2]
+
+
+# ------------------------------------------------------------------ uniform RTN
+
+def test_scale_examples_per_token_vs_per_channel(golden_dir):
+    g = _golden(golden_dir, "kvquant_scale_examples.json")
+    bits = g["per_token"]["bits"]
+    rng = np.random.default_rng(0)
+    x = rng.uniform(-1, 1, size=(128, 128)).astype(np.float32)
+    x[0, :] = -1.0
+    x[1, :] = 1.0                           # every channel spans exactly [-1, 1]
+    oc, oc2 = 7, 8
+    x[:, oc] = np.where(np.arange(128) % 2 == 0, 15.0, -15.0)   # |K_{t,c'}| = 15
+    x[:, oc2] = -x[:, oc]                  # each token spans [-15, 15]: range 30 as on the page
+    x = WL.round_f16(x)
+    _, s_tok, _ = O.rtn_quantize(x, bits, axis=1)
+    _, s_ch, _ = O.rtn_quantize(x, bits, axis=0)
+    s_tok = s_tok.astype(np.float64)
+    s_ch = s_ch.astype(np.float64)
+    assert np.all(np.abs(s_tok - g["per_token"]["approx"]) <= g["per_token"]["tolerance_abs"])
+    normal = np.delete(s_ch, [oc, oc2])
+    assert np.all(np.abs(normal - g["per_channel_normal"]["approx"]) <= g["per_channel_normal"]["tolerance_abs"])
+    for c in (oc, oc2):
+        assert abs(s_ch[c] - g["per_channel_outlier"]["approx"]) <= g["per_channel_outlier"]["tolerance_abs"]
+
+
+def _rtn_bound_check(x, codes, s16, z16, bits, axis):
+    xh = O.rtn_dequant(codes, s16, z16, axis)
+    s = s16.astype(np.float64)
+    z = z16.astype(np.float64)
+    if axis == 0:
+        s, z = s[None, :], z[None, :]
+        mn = x.min(axis=0)[None, :].astype(np.float64)
+    else:
+        s, z = s[:, None], z[:, None]
+        mn = x.min(axis=1)[:, None].astype(np.float64)
+    err = np.abs(x.astype(np.float64) - xh)
+    t = x.astype(np.float64) / s - z
+    eps = 2.0 ** -22 * (np.abs(x / s) + np.abs(z) + 1.0)
+    unclamped = (np.rint(t) >= 0) & (np.rint(t) <= 2 ** bits - 1)
+    # |x - x_dq| <= s/2 on every element that was not clamped (rounding of fp32 steps aside)
+    sb = np.broadcast_to(s, x.shape)
+    assert np.all(err[unclamped] <= sb[unclamped] * (0.5 + eps[unclamped]))
+    # clamping only comes from fp16 rounding of the zero point: error <= s/2 + s*|z16 - min/s|
+    zerr = np.abs(z - mn / s)
+    bound = s * (0.5 + zerr + eps + 2.0 ** -10 * (2 ** bits))
+    assert np.all(err <= bound)
+    return unclamped
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+@pytest.mark.parametrize("axis", [0, 1])
+def test_rtn_error_bound(bits, axis):
+    w = WL.WORKLOADS[5]
+    for blk in range(3):
+        x = WL.tile(w, 0, 3, blk, WL.KIND_K)       # includes x12 outlier channels
+        codes, s16, z16 = O.rtn_quantize(x, bits, axis)
+        assert codes.max() <= 2 ** bits - 1
+        _rtn_bound_check(x, codes, s16, z16, bits, axis)
+        # the extremes of each group are reproduced to within s/2
+        xh = O.rtn_dequant(codes, s16, z16, axis)
+        am = np.argmax(x, axis=axis)
+        if axis == 0:
+            assert np.all(np.abs(xh[am, np.arange(128)] - x[am, np.arange(128)]) <= s16.astype(float) * 0.5 + 1e-6)
+
+
+def test_rtn_constant_group_is_exact():
+    x = np.full((128, 128), 0.75, np.float32)
+    codes, s16, z16 = O.rtn_quantize(x, 2, 0)
+    assert np.all(s16 == 1.0) and np.all(codes == 0)
+    assert np.array_equal(O.rtn_dequant(codes, s16, z16, 0), x.astype(np.float64))
+
+
+def test_rtn_grid_inputs_are_lossless():
+    # values on the grid {min + k*s}, s a power of two, are reproduced exactly
+    rng = np.random.default_rng(1)
+    q = rng.integers(0, 4, size=(128, 128))
+    q[0, :], q[1, :] = 0, 3
+    x = (q.astype(np.float32) - 2.0) * np.float32(0.25)
+    codes, s16, z16 = O.rtn_quantize(x, 2, 0)
+    assert np.array_equal(O.rtn_dequant(codes, s16, z16, 0), x.astype(np.float64))
+
+
+# ------------------------------------------------------------------ int4 absmax
+
+def test_int4_codes_range_and_bound():
+    w = WL.WORKLOADS[4]
+    for blk in range(3):
+        x = WL.tile(w, 1, 2, blk, WL.KIND_V)
+        q, s16 = O.int4_quantize(x)
+        assert q.min() >= -7 and q.max() <= 7
+        s = s16.astype(np.float64)
+        a = np.abs(x).max(axis=1)
+        # the element with |x| = absmax maps to +-7
+        for t in range(128):
+            j = int(np.argmax(np.abs(x[t])))
+            assert abs(int(q[t, j])) == 7
+        err = np.abs(x.astype(np.float64) - O.int4_dequant(q, s16))
+        assert np.all(err <= (s * 0.5 * (1 + 2.0 ** -10))[:, None])
+        # fp16 scale is absmax/7 rounded once
+        assert np.all(np.abs(s - a / 7.0) <= np.abs(a / 7.0) * 2.0 ** -11)
+        nib = O.int4_nibbles(q)
+        assert nib.max() <= 15 and np.array_equal(O.int4_from_nibbles(nib), q)
+
+
+def test_int4_zero_block_and_lossless_grid():
+    x = np.zeros((128, 128), np.float32)
+    q, s16 = O.int4_quantize(x)
+    assert np.all(q == 0) and np.all(s16 == 0)
+    rng = np.random.default_rng(2)
+    q0 = rng.integers(-7, 8, size=(128, 128))
+    q0[:, 5] = 7
+    x = (q0 * 0.125).astype(np.float32)         # scale = 7*0.125/7 = 0.125 exactly
+    q, s16 = O.int4_quantize(x)
+    assert np.array_equal(q, q0) and np.all(s16 == 0.125)
+    # two's complement nibble of -1 is 0xF, of -7 is 0x9
+    assert O.int4_nibbles(np.array([-1, -7, 7, 0]))[:4].tolist() == [15, 9, 7, 0]
+
+
+# ------------------------------------------------------------------ nuq (KVQuant)
+
+def test_worked_example_normalise_and_argmin(golden_dir):
+    g = _golden(golden_dir, "kvquant_worked_example.json")
+    cb = np.array(g["codebook_channel_15"]["values"], np.float32)
+    for key in ("channel_15", "channel_0"):
+        c = g[key]
+        t = O.nuq_normalise(np.float32(c["k"]), np.float16(c["s"]), np.float16(c["z"]))
+        assert abs(float(t) - c["k_norm"]) < 2e-3, c["cite"]
+        assert int(O.nuq_encode(np.array([t]), cb)[0]) == c["index"], c["cite"]
+    for key in ("outlier_channel_7", "channel_0_not_outlier"):
+        c = g[key]
+        dense, sparse = O.threshold_split(np.array([c["k"]]), np.array([c["tau"]]))
+        assert (sparse[0] != 0) == c["is_outlier"], c["cite"]
+        assert dense[0] == (0.0 if c["is_outlier"] else c["k"])
+
+
+def test_codebook_is_scaled_normal_quantiles():
+    cb = O.nuq_codebook(3).astype(np.float64)
+    ref = scipy.stats.norm.ppf((np.arange(8) + 0.5) / 8)
+    ref = ref / ref[-1]
+    assert np.allclose(cb, ref, rtol=0, atol=1e-7)
+    assert cb[0] == -1.0 and cb[-1] == 1.0
+    assert np.all(np.diff(cb) > 0) and np.allclose(cb, -cb[::-1])
+
+
+def test_nuq_argmin_equals_brute_force():
+    rng = np.random.default_rng(3)
+    cb = O.nuq_codebook(3)
+    mids = (cb[:-1].astype(np.float64) + cb[1:]) / 2
+    t = np.concatenate([rng.uniform(-1, 1, 500), mids, cb.astype(np.float64), [-1.0, 1.0, 0.0]]).astype(np.float32)
+    got = O.nuq_encode(t, cb)
+    for i, v in enumerate(t):
+        best, bj = None, None
+        for j, c in enumerate(cb):
+            d = abs(np.float32(v) - np.float32(c))
+            if best is None or d < best:
+                best, bj = d, j
+        assert got[i] == bj
+
+
+def test_outlier_selection_planted_and_ties():
+    rng = np.random.default_rng(4)
+    x = rng.uniform(-1, 1, size=(128, 128)).astype(np.float32)
+    flat = rng.choice(128 * 128, size=164, replace=False)
+    x.ravel()[flat] = rng.uniform(5, 9, size=164) * rng.choice([-1, 1], size=164)
+    x = WL.round_f16(x)
+    m = O.outlier_mask(x, 164)
+    assert set(np.flatnonzero(m)) == set(flat)
+    # ties on |x|: 200 entries of equal magnitude -> the 164 with the lowest flat index
+    y = np.zeros((128, 128), np.float32)
+    pos = np.sort(rng.choice(128 * 128, size=200, replace=False))
+    y.ravel()[pos] = np.where(rng.random(200) < 0.5, -3.0, 3.0)
+    m = O.outlier_mask(y, 164)
+    assert set(np.flatnonzero(m)) == set(pos[:164])
+
+
+def test_nuq_quantize_csr_and_bound():
+    w = WL.WORKLOADS[2]
+    cb = O.nuq_codebook(3)
+    for kind, axis in ((WL.KIND_K, 0), (WL.KIND_V, 1)):
+        x = WL.tile(w, 0, 7, 3, kind)
+        r = O.nuq_quantize(x, cb, axis, 164)
+        rp, col, val = r["row_ptr"].astype(int), r["col"].astype(int), r["val"]
+        assert rp[0] == 0 and rp[-1] == 164 and np.all(np.diff(rp) >= 0)
+        for t in range(128):
+            cs = col[rp[t]:rp[t + 1]]
+            assert np.all(np.diff(cs) > 0)
+            for j, c in enumerate(cs):
+                assert r["mask"][t, c]
+                assert val[rp[t] + j] == np.float16(x[t, c]).view(np.uint16)   # bit-exact fp16
+        # the outliers are the 164 largest magnitudes
+        thr = np.sort(np.abs(x).ravel())[-164]
+        assert np.all(np.abs(x[r["mask"]]) >= thr) and np.all(np.abs(x[~r["mask"]]) <= thr)
+        xh = O.nuq_dequant(r["codes"], r["s16"], r["zp16"], cb, axis, r["row_ptr"], r["col"], r["val"])
+        s = r["s16"].astype(np.float64)
+        s = s[None, :] if axis == 0 else s[:, None]
+        gap = np.max(np.diff(cb.astype(np.float64))) / 2
+        err = np.abs(xh - x)
+        dense_ok = ~r["mask"]
+        sb = np.broadcast_to(s, x.shape)
+        assert np.all(err[dense_ok] <= (sb * (gap + 2.0 ** -9))[dense_ok])
+        # at an outlier the error is the quantisation error of a dense zero
+        t0 = O.nuq_normalise(np.zeros_like(x), r["s16"][None, :] if axis == 0 else r["s16"][:, None],
+                             r["zp16"][None, :] if axis == 0 else r["zp16"][:, None])
+        e0 = np.abs(t0.astype(np.float64) - cb.astype(np.float64)[O.nuq_encode(t0, cb)]) * sb
+        zp = r["zp16"].astype(np.float64)
+        zp = zp[None, :] if axis == 0 else zp[:, None]
+        clampx = np.abs(np.broadcast_to(zp, x.shape)) - sb
+        lim = e0 + np.maximum(clampx, 0) + 1e-6
+        assert np.all(err[r["mask"]] <= lim[r["mask"]])
+
+
+def test_nuq_lossless_on_codebook_grid():
+    cb = np.array([-1, -0.75, -0.5, -0.25, 0.25, 0.5, 0.75, 1.0], np.float32)
+    rng = np.random.default_rng(5)
+    q = rng.integers(0, 8, size=(128, 128))
+    q[0, :], q[1, :] = 0, 7
+    x = (cb[q] * 0.5 + 0.25).astype(np.float32)            # s = 0.5, zp = 0.25 per channel
+    x[10, 20] = 40.0                                       # one planted outlier, stored exactly
+    r = O.nuq_quantize(x, cb, 0, 1)
+    xh = O.nuq_dequant(r["codes"], r["s16"], r["zp16"], cb, 0, r["row_ptr"], r["col"], r["val"])
+    dense0 = cb[r["codes"][10, 20]] * 0.5 + 0.25          # dense zero quantised, then += 40
+    assert xh[10, 20] == pytest.approx(40.0 + dense0)
+    xh[10, 20] = x[10, 20]
+    assert np.array_equal(xh, x.astype(np.float64))
+
+
+# ------------------------------------------------------------------ RoPE
+
+def test_rope_norm_identity_and_relative_position(golden_dir):
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((300, 128))
+    pos = rng.integers(0, 1 << 20, size=300)
+    y = O.rope(x, pos)
+    assert np.allclose(np.linalg.norm(y, axis=1), np.linalg.norm(x, axis=1), rtol=1e-12, atol=0)
+    assert np.array_equal(O.rope(x[:5], np.zeros(5)), x[:5])
+    # (R_m q) . (R_n k) = q . (R_{n-m} k)
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    for m, n in ((3, 10), (1000, 77), (123456, 654321)):
+        lhs = O.rope(q[None], [m])[0] @ O.rope(k[None], [n])[0]
+        rhs = q @ O.rope(k[None], [n - m])[0]
+        assert lhs == pytest.approx(rhs, rel=1e-9, abs=1e-9)
+    # orientation of the printed matrix: (1, 0) at angle phi goes to (cos phi, sin phi)
+    e = np.zeros((1, 128))
+    e[0, 0] = 1.0
+    y = O.rope(e, [1])                    # theta_0 = 1 rad
+    assert y[0, 0] == pytest.approx(math.cos(1.0)) and y[0, 1] == pytest.approx(math.sin(1.0))
+    # lowest frequency pair i = 63: theta^(-126/128)
+    e = np.zeros((1, 128))
+    e[0, 126] = 1.0
+    y = O.rope(e, [1000])
+    ang = 1000 * 10000.0 ** (-126 / 128)
+    assert y[0, 126] == pytest.approx(math.cos(ang)) and y[0, 127] == pytest.approx(math.sin(ang))
+
+
+def test_rope_variance_example(golden_dir):
+    g = _golden(golden_dir, "rope_variance_example.json")
+    rng = np.random.default_rng(7)
+    n = 200000
+    x = np.zeros((n, 128))
+    x[:, 0] = rng.standard_normal(n) * math.sqrt(g["var_channel0"])
+    x[:, 1] = rng.standard_normal(n) * math.sqrt(g["var_channel1"])
+    y = O.rope(x, rng.integers(0, 100000, size=n))
+    v = y[:, 0].var()
+    assert abs(v - g["post_rope_var"]) <= g["tolerance_rel"] * g["post_rope_var"]
+    assert abs(math.sqrt(v) - g["post_rope_std_approx"]) < 0.2
+
+
+# ------------------------------------------------------------------ KVarN
+
+def test_hadamard_sylvester_and_orthogonality():
+    H = O.hadamard(128)
+    assert np.array_equal(H, scipy.linalg.hadamard(128))
+    assert np.array_equal(H @ H.T, 128 * np.eye(128))
+    x = np.random.default_rng(8).standard_normal((16, 128))
+    assert np.allclose(O.fwht(O.fwht(x)), x, rtol=0, atol=1e-12)
+    # integer inputs: H (H x) = 128 x exactly
+    xi = np.random.default_rng(9).integers(-50, 50, size=(4, 128)).astype(np.float64)
+    assert np.array_equal((xi @ H) @ H, 128 * xi)
+    # unit vector e_0 spreads evenly: every output is 1/sqrt(128)
+    e = np.zeros((1, 128))
+    e[0, 0] = 1
+    assert np.allclose(O.fwht(e), 1 / math.sqrt(128))
+
+
+def test_varn_recomposition_and_stds():
+    w = WL.WORKLOADS[3]
+    x = O.fwht(WL.tile(w, 2, 1, 0, WL.KIND_K))
+    Y, r, c = O.varn(x, 8)
+    assert np.allclose(r[:, None] * Y * c[None, :], x, rtol=1e-12, atol=1e-12)
+    assert np.allclose(Y.std(axis=1), 1.0, atol=1e-12)          # rows normalised last
+    assert np.max(np.abs(Y.std(axis=0) - 1.0)) < 0.05           # columns near 1 after 8 rounds
+    Y0, r0, c0 = O.varn(x, 0)
+    assert np.array_equal(Y0, x) and np.all(r0 == 1) and np.all(c0 == 1)
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_varn_reduces_to_rtn_without_hadamard_and_iterations(kind):
+    w = WL.WORKLOADS[3]
+    x = WL.tile(w, 0, 0, 1, kind)
+    v = O.varn_quantize(x, 2, kind, iters=0, use_hadamard=False)
+    codes, s16, z16 = O.rtn_quantize(x, 2, 0 if kind == 0 else 1)
+    assert np.array_equal(v["codes"], codes)
+    assert np.array_equal(v["s16"], s16) and np.array_equal(v["z16"], z16)
+    assert np.all(v["s1"] == 1)
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_varn_reconstruction_bound(kind):
+    w = WL.WORKLOADS[3]
+    x = WL.tile(w, 1, 5, 2, kind)
+    v = O.varn_quantize(x, 2, kind, 8, True)
+    xh_H = O.varn_dequant(v["codes"], v["s16"], v["z16"], v["s1"], kind)
+    # Hadamard-domain error = s1 * RTN error on Z, plus the fp16 rounding of s1
+    Z = v["Z"]
+    zh = O.rtn_dequant(v["codes"], v["s16"], v["z16"], v["axis"])
+    s = v["s16"].astype(np.float64)
+    s = s[None, :] if kind == 0 else s[:, None]
+    assert np.all(np.abs(Z - zh) <= s * (0.5 + 2e-3) + 1e-6)
+    s1 = v["s1"].astype(np.float64)
+    true_s1 = v["r"] if kind == 0 else v["c"]
+    assert np.all(np.abs(s1 - true_s1) <= true_s1 * 2.0 ** -11)
+    X = O.fwht(x)
+    ref = (Z * true_s1[:, None]) if kind == 0 else (Z * true_s1[None, :])
+    assert np.allclose(ref, X, rtol=1e-10, atol=1e-10)
+    # norm/direction identity on the reconstruction
+    xh = O.fwht(xh_H)
+    em, ed = O.norm_direction_errors(x, xh)
+    tot = ((x.astype(np.float64) - xh) ** 2).sum(axis=1)
+    assert np.allclose(em + ed, tot, rtol=1e-9, atol=1e-12)
+
+
+def test_norm_direction_decomposition_closed_forms():
+    K = np.array([[3.0, 4.0]])
+    assert O.norm_direction_errors(K, 2 * K)[0][0] == pytest.approx(25.0)   # scaled copy: norm error only
+    assert O.norm_direction_errors(K, 2 * K)[1][0] == pytest.approx(0.0, abs=1e-12)
+    e = O.norm_direction_errors(np.array([[1.0, 0.0]]), np.array([[0.0, 1.0]]))
+    assert e[0][0] == pytest.approx(0.0) and e[1][0] == pytest.approx(2.0)   # rotation: direction only
+
+
+# ------------------------------------------------------------------ attention
+
+def _brute_attention(q, K, V):
+    out = []
+    for qi in q:
+        s = [sum(float(qi[c]) * float(k[c]) for c in range(len(qi))) / math.sqrt(len(qi)) for k in K]
+        m = max(s)
+        e = [math.exp(v - m) for v in s]
+        z = sum(e)
+        out.append([sum(e[n] * float(V[n][c]) for n in range(len(K))) / z for c in range(len(qi))])
+    return np.array(out)
+
+
+@pytest.mark.parametrize("L", [1, 127, 128, 129, 255])
+def test_attention_brute_force(L):
+    rng = np.random.default_rng(L)
+    q = rng.standard_normal((2, 16)) * 2
+    K = rng.standard_normal((L, 16)) * 2
+    V = rng.standard_normal((L, 16))
+    assert np.allclose(O.attention(q, K, V), _brute_attention(q, K, V), rtol=1e-12, atol=1e-12)
+
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(11)
+    q = rng.standard_normal((3, 128))
+    V = rng.standard_normal((1, 128))
+    assert np.array_equal(O.attention(q, rng.standard_normal((1, 128)), V), np.repeat(V, 3, axis=0))
+    V = rng.standard_normal((50, 128))
+    K = np.repeat(rng.standard_normal((1, 128)), 50, axis=0)
+    assert np.allclose(O.attention(q, K, V), V.mean(axis=0)[None, :], rtol=0, atol=1e-12)
+
+
+def _lossless_cache_inputs(method, B, H, n_blocks, rng, cb=None):
+    """Inputs the quantizer reproduces exactly: every group (a key channel, a value token;
+    a token for int4) lies on its own dyadic grid with its extremes present. Group scales
+    differ, so grouping along the wrong axis would not be lossless."""
+    K = np.empty((B, H, n_blocks * 128, 128), np.float32)
+    V = np.empty_like(K)
+    ch = (2.0 ** (np.arange(128) % 3 - 2))[None, :]           # per-channel scales 1/4, 1/2, 1
+    tok = (2.0 ** (np.arange(128) % 4 - 3))[:, None]          # per-token scales 1/8 .. 1
+    for b in range(B):
+        for h in range(H):
+            for blk in range(n_blocks):
+                sl = slice(blk * 128, (blk + 1) * 128)
+                if method == "rtn":            # 2-bit grid, per channel (K) / per token (V)
+                    qk = rng.integers(0, 4, (128, 128)); qk[0], qk[1] = 0, 3
+                    qv = rng.integers(0, 4, (128, 128)); qv[:, 0], qv[:, 1] = 0, 3
+                    K[b, h, sl] = (qk - 1.5) * ch
+                    V[b, h, sl] = (qv - 2.0) * tok
+                elif method == "int4":         # per token for both
+                    qk = rng.integers(-7, 8, (128, 128)); qk[:, 3] = -7
+                    qv = rng.integers(-7, 8, (128, 128)); qv[:, 9] = 7
+                    K[b, h, sl] = qk * 0.125 * tok
+                    V[b, h, sl] = qv * 0.0625 * tok[::-1]
+                else:                          # nuq with a dyadic codebook, no outliers
+                    qk = rng.integers(0, 8, (128, 128)); qk[0], qk[1] = 0, 7
+                    qv = rng.integers(0, 8, (128, 128)); qv[:, 0], qv[:, 1] = 0, 7
+                    K[b, h, sl] = cb[qk] * ch + 0.25 * ch
+                    V[b, h, sl] = cb[qv] * tok - 0.5 * tok
+    return K, V
+
+
+@pytest.mark.parametrize("method,G,pre_rope", [("rtn", 1, False), ("rtn", 4, False),
+                                               ("int4", 4, False), ("nuq", 1, True), ("nuq", 2, False)])
+def test_cache_decode_equals_plain_attention_on_lossless_inputs(method, G, pre_rope):
+    """On inputs the quantizer reproduces exactly, decode over the packed cache must equal
+    plain fp64 attention over the raw K/V (RoPE at absolute positions for pre-RoPE keys),
+    including the fp tail and the GQA head mapping."""
+    rng = np.random.default_rng(12)
+    B, H, nb = 2, 2, 3
+    cb = np.array([-1, -0.75, -0.5, -0.25, 0.25, 0.5, 0.75, 1.0], np.float32)
+    bits = {"rtn": 2, "int4": 4, "nuq": 3}[method]
+    cache = O.OracleCache(method, bits, B, H, H * G, pre_rope=pre_rope, outlier_frac=0.0,
+                          codebook=cb if method == "nuq" else None)
+    K, V = _lossless_cache_inputs(method, B, H, nb, rng, cb)
+    cache.append(K[:, :, :256], V[:, :, :256])
+    cache.append(K[:, :, 256:], V[:, :, 256:])
+    q = rng.standard_normal((B, H * G, 128))
+    tk = rng.standard_normal((B, H, 5, 128))
+    tv = rng.standard_normal((B, H, 5, 128))
+    got = cache.decode(q, tk, tv)
+    for b in range(B):
+        for j in range(H * G):
+            h = j // G
+            Kf = np.concatenate([K[b, h], tk[b, h]]).astype(np.float64)
+            if pre_rope:
+                Kf = O.rope(Kf, np.arange(Kf.shape[0]))
+            Vf = np.concatenate([V[b, h], tv[b, h]]).astype(np.float64)
+            ref = O.attention(q[b, j][None], Kf, Vf)[0]
+            assert np.allclose(got[b, j], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_varn_cache_decode_matches_dequantised_attention():
+    """KVarN decode works in the Hadamard domain (q -> Hq, o -> H o); the result equals
+    attention over the input-domain reconstruction, because H/sqrt(128) is orthonormal."""
+    w = WL.WORKLOADS[3].scaled(batch=1, n_kv_heads=2, n_q_heads=4, ctx=256)
+    cache = O.OracleCache.for_workload(w)
+    K, V = WL.blocks(w, 0, 2)
+    cache.append(K, V)
+    q = WL.query(w)
+    tk, tv = WL.tail(w, 3)
+    got = cache.decode(q, tk, tv)
+    for j in range(4):
+        h = j // 2
+        Kd = np.concatenate([cache.dequant(0, h, 0, "input"), tk[0, h]])
+        Vd = np.concatenate([cache.dequant(0, h, 1, "input"), tv[0, h]])
+        assert np.allclose(got[0, j], O.attention(q[0, j][None], Kd, Vd)[0], rtol=1e-10, atol=1e-10)
