@@ -1,0 +1,455 @@
+"""Benchmark: decode attention over the packed low-bit KV cache, plus block append.
+
+One timed step = one block period of streaming decode on the configured workload: 128 decode
+calls (kvq_decode_attn) over the full packed cache with the fp tail growing 0..127 tokens,
+then one kvq_append_block that quantizes the 128-token block the tail formed. value = packed
+cache bytes the 128 decodes read (codes + fp16 metadata + CSR: the algorithmic count) / step
+time, in GB/s. Decodes rotate over enough copies of the cache that every decode reads data
+that is not in L2 (the copies together exceed 3x L2).
+
+Default workload: LLaMA-7B-shaped MHA layer (32 heads x 128), batch 1, context 32768, nuq3
+keys (pre-RoPE, per channel) / values (per token), 8-entry per-head N(0,1)-quantile codebook,
+1% fp16 outliers in CSR. --config selects another workload (1..5).
+
+--impl reference times the CPU oracle (test infrastructure) on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as WL  # noqa: E402
+
+L2_BYTES = 126.5 * 2 ** 20
+DECODES_PER_STEP = 128
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.idx = gpu_id
+        self.p = None
+        self.path = os.path.join("/tmp", f"kvq_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except Exception:
+                self.p.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.p is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), float(parts[3]) if parts[3] not in ("[N/A]", "N/A") else 0.0,
+                             parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i, v in enumerate(r[3]) if v.lower() == "active"})
+        loaded = [r for r in rows if r[2] > 200] or rows
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _gen_device(w, torch, dev, shape, kind, seed):
+    """Large synthetic inputs drawn on the device (performance runs only; parity tests use the
+    seeded numpy generators)."""
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000003 * seed + 17 * kind + w.cfg_id)
+    if kind == 0 and w.k_dist == "student_t3":
+        z = torch.randn(shape, generator=g, device=dev)
+        chi = torch.randn((3,) + tuple(shape), generator=g, device=dev).pow(2).sum(0) / 3
+        x = z / chi.sqrt()
+    else:
+        x = torch.randn(shape, generator=g, device=dev)
+    if kind == 0 and w.k_outlier_channels:
+        x[..., list(w.k_outlier_channels)] *= w.k_outlier_gain
+    return x.to(torch.float16 if w.dtype == "f16" else torch.bfloat16)
+
+
+def _inputs(w, torch, dev, rank):
+    """Prefill K/V for the whole context, the tail block and the decode query, resident on the device."""
+    nb = w.n_blocks
+    shape = (w.batch, w.n_kv_heads, nb * 128, 128)
+    dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
+    n_elem = 2 * math.prod(shape)
+    if n_elem * 4 <= 2 * 2 ** 30:   # seeded numpy generators (same as the tests)
+        K, V = WL.blocks(w, 0, nb, seed=rank)
+        to = lambda x: torch.from_numpy(WL.to_storage(x, w.dtype).view(np.int16)).to(dev).view(dt)
+        Kd, Vd = to(K), to(V)
+        tk, tv = WL.tail(w, 127, seed=rank)
+        q = WL.query(w, seed=rank)
+        return Kd, Vd, to(tk), to(tv), to(q), "numpy"
+    Kd = _gen_device(w, torch, dev, shape, 0, rank)
+    Vd = _gen_device(w, torch, dev, shape, 1, rank)
+    tshape = (w.batch, w.n_kv_heads, 127, 128)
+    tk = _gen_device(w, torch, dev, tshape, 0, rank + 7)
+    tv = _gen_device(w, torch, dev, tshape, 1, rank + 7)
+    q = _gen_device(w, torch, dev, (w.batch, w.n_q_heads, 128), 1, rank + 11)
+    return Kd, Vd, tk, tv, q, "torch-device"
+
+
+def run_kvq(args):
+    import torch
+    import bit_kv_cache_block_gb300 as K
+    import __graft_entry__
+    rank, world, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if rank == 0:
+        __graft_entry__.build()
+    if world > 1:
+        torch.distributed.barrier()
+    K._lib.lib()
+    w = WL.WORKLOADS[args.config]
+    nb = w.n_blocks
+    cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, nb + 1, w.dtype, w.pre_rope,
+                        w.rope_theta, w.outlier_frac, w.varn_iters, True)
+    lay = K.kvq_layout(cfg)
+    cb = None
+    if w.method == "nuq":
+        from statistics import NormalDist
+        inv = NormalDist().inv_cdf
+        n = 2 ** w.bits
+        vals = [inv((j + 0.5) / n) / inv((n - 0.5) / n) for j in range(n)]
+        cb = torch.tensor([vals] * w.n_kv_heads, dtype=torch.float32)
+    cache_bytes = K.kvq_decode_bytes(cfg, nb)
+    n_copies = max(1, math.ceil(3 * L2_BYTES / max(1, int(lay.records_bytes))))
+    caches = [K.KVCache(cfg, cb, device=dev)]
+    Kd, Vd, tk, tv, q, gen = _inputs(w, torch, dev, rank)
+    caches[0].append(Kd, Vd)
+    del Kd, Vd
+    for _ in range(n_copies - 1):
+        c = K.KVCache(cfg, cb, device=dev)
+        c.base.copy_(caches[0].base)
+        K.kvq_truncate(c.cache, 0)
+        c.cache.n_blocks = nb
+        caches.append(c)
+    out = torch.empty(w.batch, w.n_q_heads, 128, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    tail_k = tk.contiguous()
+    tail_v = tv.contiguous()
+    # tail prefixes for n_tail = 1..127 as contiguous views ([B][H][n][128] each)
+    tails = [None] + [(tail_k[:, :, :j].contiguous(), tail_v[:, :, :j].contiguous()) for j in range(1, 128)]
+    blk_k = torch.cat([tail_k, tail_k[:, :, :1]], dim=2).contiguous()   # the block the tail completes
+    blk_v = torch.cat([tail_v, tail_v[:, :, :1]], dim=2).contiguous()
+    ws = caches[0].workspace
+
+    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(DECODES_PER_STEP)]
+    ev_app = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+
+    def step(i, timed):
+        for d in range(DECODES_PER_STEP):
+            c = caches[(i * DECODES_PER_STEP + d) % n_copies]
+            nt = d
+            tkk, tvv = (tails[nt] if nt else (None, None))
+            if timed:
+                ev_dec[d][0].record(stream)
+            K.kvq_decode_attn(c.cache, q, tkk, tvv, nt, out, ws, stream)
+            if timed:
+                ev_dec[d][1].record(stream)
+        c = caches[i % n_copies]
+        if timed:
+            ev_app[0].record(stream)
+        c.append(blk_k, blk_v, stream=stream)
+        if timed:
+            ev_app[1].record(stream)
+        K.kvq_truncate(c.cache, nb)
+
+    for i in range(args.warmup):
+        step(i, False)
+    torch.cuda.synchronize()
+    dec_ms, app_ms = [], []
+    if world > 1:
+        torch.distributed.barrier()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+    except Exception:
+        gpu_id = str(local)
+    with Clocks(gpu_id) as clk:
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i, True)
+            torch.cuda.synchronize()   # read the per-decode events of this step
+            dec_ms.extend(a.elapsed_time(b) for a, b in ev_dec)
+            app_ms.append(ev_app[0].elapsed_time(ev_app[1]))
+        t1.record(stream)
+        torch.cuda.synchronize()
+    total_ms = t0.elapsed_time(t1)
+    status = max(int(c.status.item()) for c in caches)
+    if status != 0:
+        raise RuntimeError(f"device status {status} ({K.kvq_status_str(status)})")
+    step_ms = (sum(dec_ms) + sum(app_ms)) / args.steps
+    if world > 1:
+        tt = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(tt.item())
+    dec_bytes_step = cache_bytes * DECODES_PER_STEP
+    value = world * dec_bytes_step / (step_ms * 1e-3) / 1e9
+    dec_avg_us = 1e3 * statistics.mean(dec_ms)
+    dec0_us = 1e3 * statistics.mean(dec_ms[d] for d in range(len(dec_ms)) if d % DECODES_PER_STEP == 0)
+    app_us = 1e3 * statistics.mean(app_ms)
+    peak, peak_kind = _peaks()
+    achieved = cache_bytes / (dec0_us * 1e-6) / 1e9   # decode call with an empty tail
+    res = {
+        "metric": "quantized decode-attn packed-KV GB/s (% of 8 TB/s HBM), us/step; append tokens/s",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": {"rtn": "u%d codes, fp32 accumulate" % w.bits, "nuq": "u3 codes + fp16 csr, fp32 accumulate",
+                  "varn": "u2 codes, fp32 accumulate", "int4": "s4 codes, fp32 accumulate"}[w.method],
+        "data": f"synthetic ({gen}, seeded)",
+        "config": {"workload": w.name, "method": w.method, "bits": w.bits, "batch": w.batch,
+                   "n_kv_heads": w.n_kv_heads, "n_q_heads": w.n_q_heads, "context": w.ctx,
+                   "decodes_per_step": DECODES_PER_STEP, "tail_tokens": "0..127",
+                   "packed_bytes_per_decode": cache_bytes, "cache_copies": n_copies,
+                   "l2": f"{n_copies} cache copies rotated ({n_copies * int(lay.records_bytes) / 2**20:.0f} MiB > 3x L2)",
+                   "parallelism": f"replicas x{world}"},
+        "pct_of_8TBs": round(100 * value / 8000, 2),
+        "decode_us": round(dec_avg_us, 3),
+        "decode_us_empty_tail": round(dec0_us, 3),
+        "append_us_per_block": round(app_us, 3),
+        "append_tokens_per_s": round(w.batch * 128 / (app_us * 1e-6), 1),
+        "wall_ms_timed_region": round(total_ms, 3),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "decode_kernel + combine_kernel (kvq_decode_attn, empty tail)",
+                     "peak_source": f"{peak_kind} hbm_gbs"},
+        "gpu_launches": args.steps * (2 * DECODES_PER_STEP + 1),
+        "clocks": clk.summary(),
+    }
+    if args.e2e:
+        res["e2e"] = run_e2e(args, K, torch, dev, caches, cfg, w, nb, q, tail_k, tail_v, cache_bytes)
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_heads)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return res if rank == 0 else None
+
+
+def run_e2e(args, K, torch, dev, caches, cfg, w, nb, q, tail_k, tail_v, cache_bytes):
+    """Same step through the C ABI from pinned host buffers: every decode uploads its query
+    and the new tail token, and downloads its output; the block append reads the tail that
+    was uploaded token by token."""
+    stream = torch.cuda.current_stream()
+    hq = q.cpu().pin_memory()
+    htk = tail_k.cpu().pin_memory()
+    htv = tail_v.cpu().pin_memory()
+    hout = torch.empty((DECODES_PER_STEP, w.batch, w.n_q_heads, 128), dtype=torch.float32).pin_memory()
+    dq = torch.empty_like(q)
+    dtk = torch.empty((w.batch, w.n_kv_heads, 128, 128), dtype=tail_k.dtype, device=dev)
+    dtv = torch.empty_like(dtk)
+    out = torch.empty(w.batch, w.n_q_heads, 128, dtype=torch.float32, device=dev)
+    ws = caches[0].workspace
+    n_copies = len(caches)
+    h2d = d2h = 0
+
+    def step(i):
+        nonlocal h2d, d2h
+        h2d = d2h = 0
+        for d in range(DECODES_PER_STEP):
+            dq.copy_(hq, non_blocking=True)
+            h2d += hq.numel() * hq.element_size()
+            if d > 0:
+                dtk[:, :, d - 1].copy_(htk[:, :, d - 1], non_blocking=True)
+                dtv[:, :, d - 1].copy_(htv[:, :, d - 1], non_blocking=True)
+                h2d += 2 * htk[:, :, 0].numel() * htk.element_size()
+            c = caches[(i * DECODES_PER_STEP + d) % n_copies]
+            tk_ = dtk[:, :, :d].contiguous() if d else None
+            tv_ = dtv[:, :, :d].contiguous() if d else None
+            K.kvq_decode_attn(c.cache, dq, tk_, tv_, d, out, ws, stream)
+            hout[d].copy_(out, non_blocking=True)
+            d2h += out.numel() * 4
+        dtk[:, :, 127].copy_(htk[:, :, 0], non_blocking=True)
+        dtv[:, :, 127].copy_(htv[:, :, 0], non_blocking=True)
+        c = caches[i % n_copies]
+        c.append(dtk, dtv, stream=stream)
+        K.kvq_truncate(c.cache, nb)
+        torch.cuda.synchronize()
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    return {"value": round(cache_bytes * DECODES_PER_STEP / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "wall clock per step, host buffers pinned, copies inside the timed region"}
+
+
+def _oracle_sample(w, heads, seed=0):
+    """Oracle append (timed) and decode (timed) for a few (b, h) of the workload."""
+    import oracle as O
+    oc = O.OracleCache.for_workload(w)
+    t_app = 0.0
+    for blk in range(w.n_blocks):
+        K = np.empty((w.batch, w.n_kv_heads, 128, 128), np.float32)
+        V = np.empty_like(K)
+        for (b, h) in heads:
+            K[b, h] = WL.tile(w, b, h, blk, 0, seed)
+            V[b, h] = WL.tile(w, b, h, blk, 1, seed)
+        t = time.perf_counter()
+        oc.append(K, V, only_heads=set(heads))
+        t_app += time.perf_counter() - t
+    q = WL.query(w, seed=seed)
+    t = time.perf_counter()
+    oc.decode(q, only_heads=set(heads))
+    t_dec = time.perf_counter() - t
+    return t_app, t_dec
+
+
+def cpu_baseline(w, n_heads):
+    """The oracle (as it stands, single process) on a bounded sample: n_heads (b, h) pairs of
+    the workload, every block of their context."""
+    heads = [(0, h) for h in range(min(n_heads, w.n_kv_heads))]
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import sys, json; sys.path.insert(0, %r); import bench, workloads as WL; "
+            "w = WL.WORKLOADS[%d]; a, d = bench._oracle_sample(w, %r); print(json.dumps([a, d]))"
+            % (ROOT, w.cfg_id, heads))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
+    t_app, t_dec = json.loads(r.stdout.strip().splitlines()[-1])
+    import bit_kv_cache_block_gb300 as K
+    cfg = K.make_config(w.method, w.bits, 1, 1, w.group, w.n_blocks, w.dtype, w.pre_rope, w.rope_theta,
+                        w.outlier_frac, w.varn_iters, True)
+    per_head = K.kvq_decode_bytes(cfg, w.n_blocks)
+    nbytes = per_head * len(heads)
+    return {"value": round(nbytes / t_dec / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{len(heads)} of {w.batch * w.n_kv_heads} (batch, KV head) pairs, all {w.n_blocks} blocks; "
+                      f"decode {t_dec:.2f} s, append {t_app:.2f} s",
+            "append_tokens_per_s": round(len(heads) * w.n_blocks * 128 / t_app, 1),
+            "cpu": _cpu_model()}
+
+
+def _cpu_model():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return os.uname().machine
+
+
+def run_reference(args):
+    rank, world, local = _dist()
+    if rank != 0:
+        return None
+    w = WL.WORKLOADS[args.config]
+    heads = [(0, 0)]
+    # bound the whole run to a few minutes of CPU work: fewer blocks per step for long runs
+    n_sample = w.n_blocks if args.steps + args.warmup <= 25 else \
+        max(16, w.n_blocks * 25 // (args.steps + args.warmup))
+    ws = w.scaled(ctx=128 * min(w.n_blocks, n_sample))
+    per = []
+    for i in range(args.warmup + args.steps):
+        t_app, t_dec = _oracle_sample(ws, heads, seed=i % 2)
+        if i >= args.warmup:
+            per.append(t_dec)
+    nbytes = _decode_bytes_per_head(ws)
+    ms = 1e3 * statistics.mean(per)
+    v = nbytes / (ms * 1e-3) / 1e9
+    return {"impl": "reference", "metric": "quantized decode-attn packed-KV GB/s (% of 8 TB/s HBM), us/step; append tokens/s",
+            "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64 (oracle)", "data": "synthetic (numpy, seeded)",
+            "config": {"workload": w.name, "sample": f"1 (batch, KV head) pair, {ws.n_blocks} blocks, per step"},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"decode of 1 (batch, KV head) pair over {ws.n_blocks} blocks per step"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _decode_bytes_per_head(w):
+    """Algorithmic packed bytes of one (b, h) over the context (same count as kvq_decode_bytes)."""
+    W = -(-128 // (32 // w.bits))
+    meta = {"rtn": 2, "nuq": 2, "varn": 3, "int4": 1}[w.method] * 256
+    csr = 0
+    if w.method == "nuq":
+        n = math.ceil(float(np.float32(w.outlier_frac)) * 16384)
+        csr = 3 * n + 258 if n else 0
+    return 2 * (128 * W * 4 + meta + csr) * w.n_blocks
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--cpu-sample-heads", type=int, default=2)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    res = run_reference(args) if args.impl == "reference" else run_kvq(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

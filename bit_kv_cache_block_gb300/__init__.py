@@ -1,0 +1,185 @@
+"""bit_kv_cache_block_gb300: low-bit KV-cache quantization in 128-token blocks and decode
+attention over the packed cache, as hand-written CUDA kernels for sm_103a behind a C ABI
+(include/kvq.h, libkvq.so).
+
+This module is the thin Python binding: the functions carry the C names and only marshal
+arguments (torch tensors -> device pointers, the current torch stream -> cudaStream_t).
+Every step of the path runs in the library's kernels; there is no Python or CPU fallback.
+PyTorch only provides device memory and streams.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+from . import _lib
+from ._lib import (KVQ_BF16, KVQ_F16, KVQ_INT4, KVQ_NUQ, KVQ_OK, KVQ_RTN, KVQ_VARN, KVQError, METHODS,
+                   kvq_cache, kvq_config, kvq_layout_t)
+
+__all__ = ["make_config", "kvq_layout", "kvq_dense_kv_bytes", "kvq_cache_init", "kvq_append_block",
+           "kvq_truncate", "kvq_reset", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
+           "kvq_decode_attn", "kvq_dequant", "kvq_status_str", "KVCache", "KVQError", "kvq_config",
+           "kvq_layout_t", "kvq_cache", "lib_path"]
+
+
+def lib_path() -> str:
+    return _lib.LIB_PATH
+
+
+def make_config(method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: int, max_blocks: int,
+                in_dtype: str = "f16", pre_rope: bool = False, rope_theta: float = 10000.0,
+                outlier_frac: float = 0.01, varn_iters: int = 8, hadamard: bool = True) -> kvq_config:
+    c = kvq_config()
+    c.method = METHODS[method] if isinstance(method, str) else int(method)
+    c.bits, c.batch, c.n_kv_heads, c.n_q_heads = bits, batch, n_kv_heads, n_q_heads
+    c.head_dim, c.block, c.max_blocks = 128, 128, max_blocks
+    c.in_dtype = KVQ_BF16 if in_dtype == "bf16" else KVQ_F16
+    c.pre_rope = int(bool(pre_rope))
+    c.rope_theta = float(rope_theta)
+    c.outlier_frac = float(outlier_frac)
+    c.varn_iters = int(varn_iters)
+    c.hadamard = int(bool(hadamard))
+    return c
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return C.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if hasattr(stream, "cuda_stream"):
+        return C.c_void_p(stream.cuda_stream)
+    return C.c_void_p(int(stream))
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return C.c_void_p(t)
+    if not t.is_cuda:
+        raise ValueError("device tensor expected")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return C.c_void_p(t.data_ptr())
+
+
+def kvq_status_str(s: int) -> str:
+    return _lib.status_str(s)
+
+
+def kvq_dense_kv_bytes(n_layers, n_heads, head_dim, elem_bytes, batch, seq_len) -> int:
+    return int(_lib.lib().kvq_dense_kv_bytes(n_layers, n_heads, head_dim, elem_bytes, batch, seq_len))
+
+
+def kvq_layout(cfg: kvq_config) -> kvq_layout_t:
+    out = kvq_layout_t()
+    _lib.check(_lib.lib().kvq_layout(C.byref(cfg), C.byref(out)), "kvq_layout")
+    return out
+
+
+def kvq_cache_init(cfg: kvq_config, base, codebook, status, stream=None) -> kvq_cache:
+    """base: uint8 device tensor of >= layout.total_bytes; codebook: fp32 [H_kv][2^bits] (NUQ) or
+    None; status: int32 device tensor of 1 element."""
+    cache = kvq_cache()
+    _lib.check(_lib.lib().kvq_cache_init(C.byref(cache), C.byref(cfg), _ptr(base), base.numel() * base.element_size(),
+                                         _ptr(codebook), _ptr(status), _stream(stream)), "kvq_cache_init")
+    return cache
+
+
+def kvq_append_block(cache: kvq_cache, k, v, dbg_varn_scales=None, stream=None) -> None:
+    """k, v: device [B][H_kv][n*128][128] in the cache's input dtype."""
+    n = k.shape[2] // 128
+    if tuple(k.shape) != tuple(v.shape) or k.shape[2] % 128 != 0:
+        raise ValueError("k and v must have the same shape [B][H_kv][n*128][128]")
+    _lib.check(_lib.lib().kvq_append_block(C.byref(cache), _ptr(k), _ptr(v), n, _ptr(dbg_varn_scales),
+                                           _stream(stream)), "kvq_append_block")
+
+
+def kvq_truncate(cache: kvq_cache, n_blocks: int) -> None:
+    _lib.check(_lib.lib().kvq_truncate(C.byref(cache), int(n_blocks)), "kvq_truncate")
+
+
+def kvq_reset(cache: kvq_cache) -> None:
+    _lib.check(_lib.lib().kvq_reset(C.byref(cache)), "kvq_reset")
+
+
+def kvq_decode_splits(cfg: kvq_config, n_blocks: int) -> int:
+    return int(_lib.lib().kvq_decode_splits(C.byref(cfg), int(n_blocks)))
+
+
+def kvq_decode_workspace_bytes(cfg: kvq_config, n_blocks: int) -> int:
+    out = C.c_size_t()
+    _lib.check(_lib.lib().kvq_decode_workspace_bytes(C.byref(cfg), int(n_blocks), C.byref(out)),
+               "kvq_decode_workspace_bytes")
+    return int(out.value)
+
+
+def kvq_decode_bytes(cfg: kvq_config, n_blocks: int) -> int:
+    return int(_lib.lib().kvq_decode_bytes(C.byref(cfg), int(n_blocks)))
+
+
+def kvq_decode_attn(cache: kvq_cache, q, tail_k, tail_v, n_tail: int, out, workspace, stream=None) -> None:
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _lib.check(_lib.lib().kvq_decode_attn(C.byref(cache), _ptr(q), _ptr(tail_k), _ptr(tail_v), int(n_tail),
+                                          _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)),
+               "kvq_decode_attn")
+
+
+def kvq_dequant(cache: kvq_cache, first_block: int, n_blocks: int, domain: int, out_k, out_v, stream=None) -> None:
+    _lib.check(_lib.lib().kvq_dequant(C.byref(cache), int(first_block), int(n_blocks), int(domain), _ptr(out_k),
+                                      _ptr(out_v), _stream(stream)), "kvq_dequant")
+
+
+class KVCache:
+    """Convenience owner of the device buffers of one cache (allocated by PyTorch) plus the
+    decode workspace; every call goes through the C ABI above."""
+
+    def __init__(self, cfg: kvq_config, codebook=None, device="cuda", stream=None):
+        import torch
+        self.cfg = cfg
+        self.layout = kvq_layout(cfg)
+        self.device = torch.device(device)
+        self.base = torch.empty(int(self.layout.total_bytes), dtype=torch.uint8, device=self.device)
+        self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.codebook = None if codebook is None else codebook.to(self.device, torch.float32).contiguous()
+        self.cache = kvq_cache_init(cfg, self.base, self.codebook, self.status, stream)
+        self.workspace = torch.empty(max(16, kvq_decode_workspace_bytes(cfg, cfg.max_blocks)),
+                                     dtype=torch.uint8, device=self.device)
+
+    @property
+    def n_blocks(self) -> int:
+        return int(self.cache.n_blocks)
+
+    def append(self, k, v, dbg_varn_scales=None, stream=None):
+        kvq_append_block(self.cache, k, v, dbg_varn_scales, stream)
+
+    def truncate(self, n_blocks: int):
+        kvq_truncate(self.cache, n_blocks)
+
+    def decode(self, q, tail_k=None, tail_v=None, out=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty(q.shape[0], q.shape[1], 128, dtype=torch.float32, device=self.device)
+        n_tail = 0 if tail_k is None else int(tail_k.shape[2])
+        need = kvq_decode_workspace_bytes(self.cfg, self.n_blocks)
+        if self.workspace.numel() < need:
+            self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
+        kvq_decode_attn(self.cache, q, tail_k if n_tail else None, tail_v if n_tail else None, n_tail, out,
+                        self.workspace, stream)
+        return out
+
+    def dequant(self, first_block: int, n_blocks: int, domain: int = 0, stream=None):
+        import torch
+        shape = (self.cfg.batch, self.cfg.n_kv_heads, n_blocks * 128, 128)
+        ok = torch.empty(shape, dtype=torch.float32, device=self.device)
+        ov = torch.empty(shape, dtype=torch.float32, device=self.device)
+        kvq_dequant(self.cache, first_block, n_blocks, domain, ok, ov, stream)
+        return ok, ov
+
+    def device_status(self) -> int:
+        return int(self.status.item())
+
+    def record_view(self):
+        """The records as a uint8 tensor [B][H_kv][max_blocks][record_bytes] (for checking)."""
+        c = self.cfg
+        n = c.batch * c.n_kv_heads * c.max_blocks * int(self.layout.record_bytes)
+        return self.base[:n].view(c.batch, c.n_kv_heads, c.max_blocks, int(self.layout.record_bytes))

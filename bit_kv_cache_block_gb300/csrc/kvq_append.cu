@@ -1,0 +1,418 @@
+// Append: quantize new 128-token blocks of K and V into packed cache records.
+//
+// One CTA of 256 threads per tile (b, h, block, K|V). The tile is staged once from HBM into
+// shared memory as fp32 (128 x 129, padded rows), then:
+//   RTN  : per-group min/max -> fp16 s, z -> q = clamp(rne(x/s - z)) -> pack
+//          ([KVN] preliminaries, KIVI representation (K_q + z) * s; [KVQ] §1.2, §3.1)
+//   VARN : FWHT-128 on each token row, Sinkhorn-style variance normalisation (columns, then
+//          rows, repeated), merge of the scales, RTN, second scale s1 ([KVN] method steps 1-4)
+//   INT4 : per-token absmax/7 -> fp16 scale -> q = clamp(rne(x/s), -8, 7) -> nibbles
+//          ([TQ] §2.1, §4.2 quantize_kv_block)
+//   NUQ  : exact top-n |x| selection (radix select on the fp16 magnitude, ties to the lower
+//          flat index) -> CSR; centre/half-range of the non-outliers -> nearest codebook entry
+//          ([KVQ] §3.3-3.4, §3.8 Algorithm 1 steps 1-4)
+// Every step that decides a code or a stored fp16 value uses single IEEE fp32 operations
+// (explicit _rn intrinsics, no contraction) in a fixed order, so the records are bit-exact
+// with a plain restatement of the definitions.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+constexpr int AP_THREADS = 256;
+constexpr int XS = 129;  // padded row stride of the fp32 tile in shared memory
+
+struct AppendArgs {
+  Geo g;
+  const uint16_t* k;
+  const uint16_t* v;
+  int n_new;
+  int blk0;
+  uint8_t* base;
+  const float* codebook;
+  float* dbg;
+  int* status;
+  int varn_iters;
+  int hadamard;
+};
+
+struct AppendSmem {
+  float x[T * XS];
+  uint8_t codes[T * D];
+  float gs[T], gz[T], gs1[T];     // per-group scale / zero (fp32 copies of the fp16 values)
+  float racc[T], cacc[T];         // VarN token / channel scales
+  uint32_t mask[TILE / 32];       // NUQ outlier bitmap, flat index t*128 + c
+  int hist[256];
+  int scan[16];
+  int sel[4];
+  float cb[16];
+};
+
+__device__ __forceinline__ int block_excl_scan(int v, int* sh, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) sh[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int s = lane < AP_THREADS / 32 ? sh[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    if (lane < AP_THREADS / 32) sh[lane] = s;
+  }
+  __syncthreads();
+  int excl = x - v + (wid > 0 ? sh[wid - 1] : 0);
+  if (total) *total = sh[AP_THREADS / 32 - 1];
+  __syncthreads();
+  return excl;
+}
+
+// Element j (0..63) of half `half` of group `gi`: axis 0 = per channel (group = channel,
+// elements over tokens), axis 1 = per token.
+__device__ __forceinline__ int gidx(int axis, int gi, int half, int j) {
+  int e = half * 64 + j;
+  return axis == 0 ? e * XS + gi : gi * XS + e;
+}
+
+// RTN of the tile in sm->x along `axis`: fills gs/gz and the fp16 meta (s at m16[0..127],
+// z at m16[128..255]) and sm->codes.
+__device__ void rtn_tile(AppendSmem* sm, int axis, int bits, uint16_t* m16) {
+  const int tid = threadIdx.x, gi = tid >> 1, half = tid & 1;
+  float mx = -INFINITY, mn = INFINITY;
+  for (int j = 0; j < 64; ++j) {
+    float v = sm->x[gidx(axis, gi, half, j)];
+    mx = fmaxf(mx, v);
+    mn = fminf(mn, v);
+  }
+  mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+  if (half == 0) {
+    float s32 = __fdiv_rn(__fsub_rn(mx, mn), (float)((1 << bits) - 1));
+    uint16_t s16 = f2h_rn(s32);
+    if ((s16 & 0x7fff) == 0) s16 = 0x3c00;  // a zero scale becomes 1
+    float sf = h2f(s16);
+    uint16_t z16 = f2h_rn(__fdiv_rn(mn, sf));
+    sm->gs[gi] = sf;
+    sm->gz[gi] = h2f(z16);
+    m16[gi] = s16;
+    m16[T + gi] = z16;
+  }
+  __syncthreads();
+  const float qmax = (float)((1 << bits) - 1);
+  for (int e = tid; e < TILE; e += AP_THREADS) {
+    int t = e >> 7, c = e & 127;
+    int gg = axis == 0 ? c : t;
+    float q = rintf(__fsub_rn(__fdiv_rn(sm->x[t * XS + c], sm->gs[gg]), sm->gz[gg]));
+    q = fminf(fmaxf(q, 0.0f), qmax);
+    sm->codes[e] = (uint8_t)q;
+  }
+  __syncthreads();
+}
+
+// Pack sm->codes rows into words: code i of a row at bits [b*(i%n)+b-1 : b*(i%n)] of word i/n.
+__device__ void pack_tile(const AppendSmem* sm, int bits, uint32_t* dst) {
+  const int n = 32 / bits, W = (D + n - 1) / n;
+  for (int it = threadIdx.x; it < T * W; it += AP_THREADS) {
+    int t = it / W, w = it - t * W;
+    uint32_t word = 0;
+    for (int j = 0; j < n; ++j) {
+      int c = w * n + j;
+      if (c < D) word |= (uint32_t)(sm->codes[t * D + c] & ((1u << bits) - 1)) << (bits * j);
+    }
+    dst[it] = word;
+  }
+}
+
+// In-place FWHT of every row (Sylvester order), then scaling by 1/sqrt(128).
+__device__ void fwht_rows(AppendSmem* sm) {
+  const int tid = threadIdx.x;
+  for (int hh = 1; hh < D; hh <<= 1) {
+    for (int it = tid; it < T * (D / 2); it += AP_THREADS) {
+      int t = it >> 6, j = it & 63;
+      int i0 = (j / hh) * (2 * hh) + (j % hh);
+      float a = sm->x[t * XS + i0], b = sm->x[t * XS + i0 + hh];
+      sm->x[t * XS + i0] = __fadd_rn(a, b);
+      sm->x[t * XS + i0 + hh] = __fsub_rn(a, b);
+    }
+    __syncthreads();
+  }
+  const float inv = 0.08838834764831845f;  // 1/sqrt(128)
+  for (int e = tid; e < TILE; e += AP_THREADS) {
+    int t = e >> 7, c = e & 127;
+    sm->x[t * XS + c] = __fmul_rn(sm->x[t * XS + c], inv);
+  }
+  __syncthreads();
+}
+
+// Population std of each group along `axis`, divide the group by it, multiply the
+// accumulated scale. Two threads per group, four partial sums each.
+__device__ void varn_axis(AppendSmem* sm, int axis, float* acc) {
+  const int tid = threadIdx.x, gi = tid >> 1, half = tid & 1;
+  float p[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < 64; ++j) p[j & 3] += sm->x[gidx(axis, gi, half, j)];
+  float s = (p[0] + p[1]) + (p[2] + p[3]);
+  s += __shfl_xor_sync(0xffffffffu, s, 1);
+  const float mean = s * (1.0f / 128.0f);
+  float r[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < 64; ++j) {
+    float d = sm->x[gidx(axis, gi, half, j)] - mean;
+    r[j & 3] = fmaf(d, d, r[j & 3]);
+  }
+  float ss = (r[0] + r[1]) + (r[2] + r[3]);
+  ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+  const float sigma = sqrtf(ss * (1.0f / 128.0f));
+  if (sigma > 0.0f) {
+    for (int j = 0; j < 64; ++j) {
+      int id = gidx(axis, gi, half, j);
+      sm->x[id] = sm->x[id] / sigma;
+    }
+    if (half == 0) acc[gi] *= sigma;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  AppendSmem* sm = reinterpret_cast<AppendSmem*>(smem_raw);
+  const Geo& g = a.g;
+  const int tid = threadIdx.x;
+  const int blk_src = blockIdx.x, h = blockIdx.y, b = blockIdx.z >> 1, kind = blockIdx.z & 1;
+  const int blk = a.blk0 + blk_src;
+  if (blk >= g.max_blocks) {  // host checks capacity; keep the kernel safe regardless
+    if (tid == 0) report(a.status, KVQ_ERR_CAPACITY);
+    return;
+  }
+
+  // ---- stage the tile (one read of HBM), fp32
+  const uint16_t* src = (kind ? a.v : a.k) +
+                        (((uint64_t)b * g.H + h) * (uint64_t)a.n_new * T + (uint64_t)blk_src * T) * D;
+  for (int i = tid; i < TILE / 8; i += AP_THREADS) {
+    uint4 u = reinterpret_cast<const uint4*>(src)[i];
+    int e = i * 8, t = e >> 7, c = e & 127;
+    const uint16_t* hv = reinterpret_cast<const uint16_t*>(&u);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sm->x[t * XS + c + j] = in_bits_to_f32(hv[j], g.in_bf16);
+  }
+  if (tid < T) {
+    sm->racc[tid] = 1.0f;
+    sm->cacc[tid] = 1.0f;
+  }
+  __syncthreads();
+
+  uint8_t* rec = a.base + record_index(g, b, h, blk) * g.rec_bytes;
+  uint32_t* codes_dst = reinterpret_cast<uint32_t*>(rec + g.codes_off[kind]);
+  uint16_t* m16 = reinterpret_cast<uint16_t*>(rec + g.meta_off[kind]);
+  const int axis = kind == 0 ? 0 : 1;  // keys per channel, values per token
+
+  if (g.method == KVQ_RTN) {
+    rtn_tile(sm, axis, g.bits, m16);
+  } else if (g.method == KVQ_VARN) {
+    if (a.hadamard) fwht_rows(sm);
+    for (int it = 0; it < a.varn_iters; ++it) {
+      varn_axis(sm, 0, sm->cacc);   // columns (channels) first
+      varn_axis(sm, 1, sm->racc);   // then rows (tokens)
+    }
+    // keys: Z = Y diag(c), s1 = r; values: Z = diag(r) Y, s1 = c
+    for (int e = tid; e < TILE; e += AP_THREADS) {
+      int t = e >> 7, c = e & 127;
+      float sc = kind == 0 ? sm->cacc[c] : sm->racc[t];
+      sm->x[t * XS + c] = __fmul_rn(sm->x[t * XS + c], sc);
+    }
+    __syncthreads();
+    if (tid < T) {
+      float s1 = kind == 0 ? sm->racc[tid] : sm->cacc[tid];
+      m16[2 * T + tid] = f2h_rn(s1);
+      if (a.dbg) {
+        float* d = a.dbg + ((((uint64_t)b * g.H + h) * a.n_new + blk_src) * 2 + kind) * 2 * T;
+        d[tid] = sm->racc[tid];
+        d[T + tid] = sm->cacc[tid];
+      }
+    }
+    rtn_tile(sm, axis, g.bits, m16);
+  } else if (g.method == KVQ_INT4) {
+    const int gi = tid >> 1, half = tid & 1;
+    float am = 0.0f;
+    for (int j = 0; j < 64; ++j) am = fmaxf(am, fabsf(sm->x[gi * XS + half * 64 + j]));
+    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    if (half == 0) {
+      float s32 = fminf(__fdiv_rn(am, 7.0f), 65504.0f);
+      uint16_t s16 = f2h_rn(s32);
+      sm->gs[gi] = h2f(s16);
+      m16[gi] = s16;
+    }
+    __syncthreads();
+    for (int e = tid; e < TILE; e += AP_THREADS) {
+      int t = e >> 7, c = e & 127;
+      float sf = sm->gs[t];
+      int q = 0;
+      if (sf != 0.0f) {
+        float qf = rintf(__fdiv_rn(sm->x[t * XS + c], sf));
+        q = (int)fminf(fmaxf(qf, -8.0f), 7.0f);
+      }
+      sm->codes[e] = (uint8_t)(q & 0xF);
+    }
+    __syncthreads();
+  } else {  // KVQ_NUQ
+    const int ncb = 1 << g.bits;
+    if (tid < ncb) sm->cb[tid] = a.codebook[h * ncb + tid];
+    for (int i = tid; i < TILE / 32; i += AP_THREADS) sm->mask[i] = 0u;
+    uint8_t* csr = rec + g.csr_off[kind];
+    const int n_out = g.n_out;
+    __syncthreads();
+    if (n_out > 0) {
+      // pass 1: histogram of the high 8 bits of the 15-bit fp16 magnitude
+      sm->hist[tid] = 0;
+      __syncthreads();
+      const int e0 = tid * 64;  // this thread's chunk of flat indices (half a row)
+      const int t0 = e0 >> 7, c0 = e0 & 127;
+      for (int j = 0; j < 64; ++j) {
+        int mag = f2h_rn(sm->x[t0 * XS + c0 + j]) & 0x7fff;
+        atomicAdd(&sm->hist[mag >> 7], 1);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int cum = 0, bin = 255;
+        for (; bin > 0; --bin) {
+          if (cum + sm->hist[bin] >= n_out) break;
+          cum += sm->hist[bin];
+        }
+        sm->sel[0] = bin;
+        sm->sel[1] = cum;  // count strictly above this bin
+      }
+      __syncthreads();
+      const int bin1 = sm->sel[0];
+      sm->hist[tid] = 0;
+      __syncthreads();
+      for (int j = 0; j < 64; ++j) {
+        int mag = f2h_rn(sm->x[t0 * XS + c0 + j]) & 0x7fff;
+        if ((mag >> 7) == bin1) atomicAdd(&sm->hist[mag & 0x7f], 1);
+      }
+      __syncthreads();
+      if (tid == 0) {
+        int cum = sm->sel[1], lo = 127;
+        for (; lo > 0; --lo) {
+          if (cum + sm->hist[lo] >= n_out) break;
+          cum += sm->hist[lo];
+        }
+        sm->sel[2] = (bin1 << 7) | lo;  // threshold magnitude
+        sm->sel[3] = n_out - cum;       // how many entries equal to the threshold are taken
+      }
+      __syncthreads();
+      const int thr = sm->sel[2], need_eq = sm->sel[3];
+      int n_eq = 0;
+      for (int j = 0; j < 64; ++j) n_eq += (f2h_rn(sm->x[t0 * XS + c0 + j]) & 0x7fff) == thr;
+      int eq_rank = block_excl_scan(n_eq, sm->scan, nullptr);
+      uint64_t selbits = 0;
+      for (int j = 0; j < 64; ++j) {
+        int mag = f2h_rn(sm->x[t0 * XS + c0 + j]) & 0x7fff;
+        bool s = mag > thr;
+        if (mag == thr) {
+          s = eq_rank < need_eq;
+          ++eq_rank;
+        }
+        if (s) selbits |= 1ull << j;
+      }
+      const int n_sel = __popcll(selbits);
+      int pos = block_excl_scan(n_sel, sm->scan, nullptr);
+      uint16_t* val = reinterpret_cast<uint16_t*>(csr);
+      uint16_t* row_ptr = reinterpret_cast<uint16_t*>(csr + 2 * n_out);
+      uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
+      if ((tid & 1) == 0) row_ptr[t0] = (uint16_t)pos;
+      if (tid == 0) row_ptr[T] = (uint16_t)n_out;
+      sm->mask[e0 >> 5] = (uint32_t)selbits;
+      sm->mask[(e0 >> 5) + 1] = (uint32_t)(selbits >> 32);
+      for (int j = 0; j < 64; ++j) {
+        if (selbits >> j & 1) {
+          if (pos < n_out) {
+            val[pos] = f2h_rn(sm->x[t0 * XS + c0 + j]);
+            col[pos] = (uint8_t)(c0 + j);
+          } else {
+            report(a.status, KVQ_ERR_INVALID_ARG);
+          }
+          ++pos;
+        }
+      }
+      // zero the padding of the CSR region so that records are deterministic
+      const int used = 3 * n_out + 2 * (T + 1);
+      const int total = (int)round16((uint64_t)used);
+      for (int i = used + tid; i < total; i += AP_THREADS) csr[i] = 0;
+      __syncthreads();
+    }
+    // centre / half-range of the non-outlier entries of each group
+    {
+      const int gi = tid >> 1, half = tid & 1;
+      float mx = -INFINITY, mn = INFINITY;
+      for (int j = 0; j < 64; ++j) {
+        int e = axis == 0 ? (half * 64 + j) * D + gi : gi * D + half * 64 + j;
+        if (sm->mask[e >> 5] >> (e & 31) & 1) continue;
+        float v = sm->x[gidx(axis, gi, half, j)];
+        mx = fmaxf(mx, v);
+        mn = fminf(mn, v);
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
+      if (half == 0) {
+        uint16_t s16 = 0, zp16 = 0;
+        if (mx != -INFINITY) {
+          zp16 = f2h_rn(__fdiv_rn(__fadd_rn(mx, mn), 2.0f));
+          s16 = f2h_rn(__fdiv_rn(__fsub_rn(mx, mn), 2.0f));
+        }
+        sm->gs[gi] = h2f(s16);
+        sm->gz[gi] = h2f(zp16);
+        m16[gi] = s16;
+        m16[T + gi] = zp16;
+      }
+    }
+    __syncthreads();
+    for (int e = tid; e < TILE; e += AP_THREADS) {
+      int t = e >> 7, c = e & 127;
+      int gg = axis == 0 ? c : t;
+      bool outl = sm->mask[e >> 5] >> (e & 31) & 1;
+      float xd = outl ? 0.0f : sm->x[t * XS + c];
+      float sf = sm->gs[gg];
+      float tv = 0.0f;
+      if (sf != 0.0f) tv = fminf(fmaxf(__fdiv_rn(__fsub_rn(xd, sm->gz[gg]), sf), -1.0f), 1.0f);
+      int best = 0;
+      float bd = fabsf(__fsub_rn(tv, sm->cb[0]));
+      for (int j = 1; j < ncb; ++j) {
+        float d = fabsf(__fsub_rn(tv, sm->cb[j]));
+        if (d < bd) {
+          bd = d;
+          best = j;
+        }
+      }
+      sm->codes[e] = (uint8_t)best;
+    }
+    __syncthreads();
+  }
+  pack_tile(sm, g.bits, codes_dst);
+}
+
+size_t append_smem_bytes() { return sizeof(AppendSmem); }
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
+  const size_t smem = sizeof(AppendSmem);
+  cudaError_t e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.n_new, a.g.H, a.g.B * 2);
+  append_kernel<<<grid, AP_THREADS, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq
+
+// C++ entry used by the API translation unit.
+cudaError_t kvq_launch_append(const kvq::Geo& g, const uint16_t* k, const uint16_t* v, int n_new, int blk0,
+                              uint8_t* base, const float* codebook, float* dbg, int* status, int varn_iters,
+                              int hadamard, cudaStream_t st) {
+  kvq::AppendArgs a;
+  a.g = g; a.k = k; a.v = v; a.n_new = n_new; a.blk0 = blk0; a.base = base; a.codebook = codebook;
+  a.dbg = dbg; a.status = status; a.varn_iters = varn_iters; a.hadamard = hadamard;
+  return kvq::launch_append(a, st);
+}

@@ -1,0 +1,485 @@
+// Decode attention over the packed cache: split-K flash-decode plus a combine kernel.
+//
+// decode_kernel: grid (n_split, H_kv, B), 128 threads. A CTA owns a contiguous range of
+// blocks of one (b, h) and all G = H_q/H_kv query heads that share it. Whole block records
+// (K tile + V tile: codes, fp16 metadata, CSR) stream from HBM into a 3-stage shared-memory
+// ring by 1-D bulk copies (cp.async.bulk, completion on an mbarrier; every wait is bounded).
+// Per block:
+//   K phase (thread = token): unpack, dequantise in registers ((q+z)*s, C[q]*s+zp, q*s, times
+//     s1), add the CSR outliers, rotate pre-RoPE keys at their absolute position, dot with the
+//     G queries ([KVQ] §3.7 key matvec steps 1-6, Algorithm 1 dequantisation).
+//   online softmax over the block's 128 scores (running max and sum per head, base 2).
+//   V phase (thread = channel): unpack, dequantise, weighted sum with the probabilities
+//     ([KVQ] §3.7 value matvec; [KVN] step 5 with s1; [TQ] §5.2: dequantise inside attention).
+// No dequantised value is written to memory. Each CTA writes (m, l, o[128]) per query head.
+//
+// combine_kernel: grid (H_q, B), 128 threads: merges the splits, applies the inverse FWHT for
+// KVarN caches, attends the fp tail (< 128 tokens, RoPE'd at its positions for pre-RoPE
+// caches) and writes out = o / l.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+constexpr int DC_THREADS = 128;
+constexpr int NSTAGE = 3;
+constexpr float LOG2E_RSQRT_D = 1.4426950408889634f * 0.08838834764831845f;  // log2(e)/sqrt(128)
+
+struct DecodeArgs {
+  Geo g;
+  const uint8_t* base;
+  const float* codebook;
+  const uint16_t* q;
+  int n_blocks;
+  int n_split;
+  float* ws_m;
+  float* ws_l;
+  float* ws_o;
+  int* status;
+  int hadamard;
+};
+
+struct CombineArgs {
+  Geo g;
+  const uint8_t* base;
+  const uint16_t* q;
+  const uint16_t* tail_k;
+  const uint16_t* tail_v;
+  int n_tail;
+  int n_blocks;
+  int n_split;
+  const float* ws_m;
+  const float* ws_l;
+  const float* ws_o;
+  float* out;
+  int hadamard;
+};
+
+// 1/sqrt(128)-scaled FWHT of `n` rows of 128 fp32 values in shared memory (row stride 128).
+__device__ void smem_fwht(float* x, int n) {
+  for (int hh = 1; hh < D; hh <<= 1) {
+    for (int it = threadIdx.x; it < n * (D / 2); it += blockDim.x) {
+      int r = it >> 6, j = it & 63;
+      int i0 = (j / hh) * (2 * hh) + (j % hh);
+      float a = x[r * D + i0], b = x[r * D + i0 + hh];
+      x[r * D + i0] = a + b;
+      x[r * D + i0 + hh] = a - b;
+    }
+    __syncthreads();
+  }
+  for (int it = threadIdx.x; it < n * D; it += blockDim.x) x[it] *= 0.08838834764831845f;
+  __syncthreads();
+}
+
+template <int GMAX>
+struct DecSmem {
+  float qraw[GMAX][D];    // query (Hadamard domain for KVarN)
+  float qs[GMAX][D];      // query used by the K phase (rotated by the block's base angle if pre-RoPE)
+  float pv[GMAX][T];      // probabilities times the per-token value scale
+  float osp[GMAX][D];     // NUQ value outliers weighted by p
+  float red[2][GMAX][DC_THREADS / 32];
+  float cb[16];
+  uint64_t bar[NSTAGE];
+};
+
+template <int METHOD, int GMAX>
+__global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const Geo& g = a.g;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int G = g.G;
+  const int rec = (int)g.rec_bytes;
+  uint8_t* stages = smem_raw;
+  DecSmem<GMAX>* sm = reinterpret_cast<DecSmem<GMAX>*>(smem_raw + NSTAGE * rec);
+
+  const int nb = a.n_blocks;
+  const int blk_begin = (int)((long long)nb * split / a.n_split);
+  const int blk_end = (int)((long long)nb * (split + 1) / a.n_split);
+  const int n_my = blk_end - blk_begin;
+  const uint8_t* rec0 = a.base + record_index(g, b, h, 0) * g.rec_bytes;
+
+  if (tid == 0) {
+    for (int s = 0; s < NSTAGE; ++s) mbar_init(&sm->bar[s], 1);
+    fence_mbar_init();
+    fence_proxy_async();
+    for (int s = 0; s < NSTAGE && s < n_my; ++s) {
+      mbar_arrive_expect_tx(&sm->bar[s], (uint32_t)rec);
+      bulk_g2s(stages + s * rec, rec0 + (uint64_t)(blk_begin + s) * g.rec_bytes, (uint32_t)rec, &sm->bar[s]);
+    }
+  }
+  // queries of this KV head's group
+  for (int i = tid; i < G * D; i += DC_THREADS) {
+    int gg = i >> 7, c = i & 127;
+    sm->qraw[gg][c] = load_in(a.q + ((uint64_t)b * g.Hq + h * G + gg) * D + c, g.in_bf16);
+  }
+  if (METHOD == KVQ_NUQ && tid < (1 << g.bits)) sm->cb[tid] = a.codebook[h * (1 << g.bits) + tid];
+  __syncthreads();
+  if (METHOD == KVQ_VARN && a.hadamard) smem_fwht(&sm->qraw[0][0], G);
+  if (!g.pre_rope) {
+    for (int i = tid; i < G * D; i += DC_THREADS) sm->qs[i >> 7][i & 127] = sm->qraw[i >> 7][i & 127];
+  }
+  __syncthreads();
+
+  const int bits = g.bits, W = g.W, nw = 32 / bits;
+  const uint32_t cmask = (1u << bits) - 1u;
+  const float2* rope_blk = reinterpret_cast<const float2*>(a.base + g.rope_off);
+  const float2* rope_off = rope_blk + (size_t)(g.max_blocks + 1) * 64;
+
+  float m_run[GMAX], l_run[GMAX], o[GMAX];
+#pragma unroll
+  for (int k = 0; k < GMAX; ++k) {
+    m_run[k] = -INFINITY;
+    l_run[k] = 0.0f;
+    o[k] = 0.0f;
+  }
+
+  bool ok = true;
+  int failed_at = n_my;
+  for (int i = 0; i < n_my; ++i) {
+    const int s = i % NSTAGE;
+    const int blk = blk_begin + i;
+    const bool got = mbar_wait_bounded(&sm->bar[s], (uint32_t)((i / NSTAGE) & 1), a.status);
+    if (__syncthreads_or(!got)) {  // every thread leaves together
+      ok = false;
+      failed_at = i;
+      break;
+    }
+    const uint8_t* st = stages + s * rec;
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + g.codes_off[0]);
+    const uint16_t* km = reinterpret_cast<const uint16_t*>(st + g.meta_off[0]);
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + g.codes_off[1]);
+    const uint16_t* vm = reinterpret_cast<const uint16_t*>(st + g.meta_off[1]);
+
+    if (g.pre_rope) {  // q0 = R(n0)^T q, n0 = blk*128
+      for (int it = tid; it < G * 64; it += DC_THREADS) {
+        int gg = it >> 6, p = it & 63;
+        float2 cs = rope_blk[(size_t)blk * 64 + p];
+        float x0 = sm->qraw[gg][2 * p], x1 = sm->qraw[gg][2 * p + 1];
+        sm->qs[gg][2 * p] = cs.x * x0 + cs.y * x1;
+        sm->qs[gg][2 * p + 1] = -cs.y * x0 + cs.x * x1;
+      }
+    }
+    if (METHOD == KVQ_NUQ) {
+#pragma unroll
+      for (int k = 0; k < GMAX; ++k)
+        if (k < G) sm->osp[k][tid] = 0.0f;
+    }
+    __syncthreads();
+
+    // ---------------- K phase: thread = token t
+    const int t = tid;
+    float acc[GMAX];
+#pragma unroll
+    for (int k = 0; k < GMAX; ++k) acc[k] = 0.0f;
+    for (int w = 0; w < W; ++w) {
+      const uint32_t word = kc[t * W + w];
+      for (int j = 0; j < nw; j += 2) {
+        const int c = w * nw + j;
+        if (c >= D) break;
+        const uint32_t c0 = (word >> (bits * j)) & cmask, c1 = (word >> (bits * (j + 1))) & cmask;
+        float k0, k1;
+        if (METHOD == KVQ_RTN || METHOD == KVQ_VARN) {
+          k0 = ((float)c0 + h2f(km[T + c])) * h2f(km[c]);
+          k1 = ((float)c1 + h2f(km[T + c + 1])) * h2f(km[c + 1]);
+        } else if (METHOD == KVQ_INT4) {
+          k0 = (float)((int)(c0 << 28) >> 28);
+          k1 = (float)((int)(c1 << 28) >> 28);
+        } else {
+          k0 = sm->cb[c0] * h2f(km[c]) + h2f(km[T + c]);
+          k1 = sm->cb[c1] * h2f(km[c + 1]) + h2f(km[T + c + 1]);
+        }
+        if (g.pre_rope) {
+          float2 cs = rope_off[t * 64 + (c >> 1)];
+          float r0 = cs.x * k0 - cs.y * k1, r1 = cs.y * k0 + cs.x * k1;
+          k0 = r0;
+          k1 = r1;
+        }
+#pragma unroll
+        for (int k = 0; k < GMAX; ++k)
+          if (k < G) acc[k] += sm->qs[k][c] * k0 + sm->qs[k][c + 1] * k1;
+      }
+    }
+    if (METHOD == KVQ_NUQ && g.n_out > 0) {
+      const uint8_t* csr = st + g.csr_off[0];
+      const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
+      const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * g.n_out);
+      const uint8_t* col = csr + 2 * g.n_out + 2 * (T + 1);
+      const int j1 = min((int)rp[t + 1], g.n_out);
+      for (int j = min((int)rp[t], g.n_out); j < j1; ++j) {
+        const int c = col[j] & (D - 1);
+        const float v = h2f(val[j]);
+        if (g.pre_rope) {
+          float2 cs = rope_off[t * 64 + (c >> 1)];
+#pragma unroll
+          for (int k = 0; k < GMAX; ++k) {
+            if (k < G) {
+              float a0 = sm->qs[k][c & ~1], a1 = sm->qs[k][c | 1];
+              float qq = (c & 1) ? (-cs.y * a0 + cs.x * a1) : (cs.x * a0 + cs.y * a1);
+              acc[k] += v * qq;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < GMAX; ++k)
+            if (k < G) acc[k] += v * sm->qs[k][c];
+        }
+      }
+    }
+    float tscale = LOG2E_RSQRT_D;
+    if (METHOD == KVQ_INT4) tscale *= h2f(km[t]);
+    if (METHOD == KVQ_VARN) tscale *= h2f(km[2 * T + t]);
+
+    // ---------------- online softmax (base 2)
+    float s2[GMAX];
+#pragma unroll
+    for (int k = 0; k < GMAX; ++k) {
+      s2[k] = acc[k] * tscale;
+      float mx = s2[k];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      if (lane == 0 && k < G) sm->red[0][k][warp] = mx;
+    }
+    __syncthreads();
+    float alpha[GMAX];
+#pragma unroll
+    for (int k = 0; k < GMAX; ++k) {
+      if (k < G) {
+        float mb = fmaxf(fmaxf(sm->red[0][k][0], sm->red[0][k][1]), fmaxf(sm->red[0][k][2], sm->red[0][k][3]));
+        float mn = fmaxf(m_run[k], mb);
+        alpha[k] = exp2f(m_run[k] - mn);
+        m_run[k] = mn;
+        float p = exp2f(s2[k] - mn);
+        float ps = p;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+        if (lane == 0) sm->red[1][k][warp] = ps;
+        float vs = 1.0f;
+        if (METHOD != KVQ_NUQ) vs = h2f(vm[t]);  // per-token value scale folded into p
+        sm->pv[k][t] = p * vs;
+      } else {
+        alpha[k] = 1.0f;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < GMAX; ++k)
+      if (k < G)
+        l_run[k] = l_run[k] * alpha[k] +
+                   ((sm->red[1][k][0] + sm->red[1][k][1]) + (sm->red[1][k][2] + sm->red[1][k][3]));
+
+    if (METHOD == KVQ_NUQ && g.n_out > 0) {  // value outliers of row t, weighted by p
+      const uint8_t* csr = st + g.csr_off[1];
+      const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
+      const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * g.n_out);
+      const uint8_t* col = csr + 2 * g.n_out + 2 * (T + 1);
+      const int j1 = min((int)rp[t + 1], g.n_out);
+      for (int j = min((int)rp[t], g.n_out); j < j1; ++j) {
+        const int c = col[j] & (D - 1);
+        const float v = h2f(val[j]);
+#pragma unroll
+        for (int k = 0; k < GMAX; ++k)
+          if (k < G) atomicAdd(&sm->osp[k][c], sm->pv[k][t] * v);
+      }
+      __syncthreads();
+    }
+
+    // ---------------- V phase: thread = channel c
+    {
+      const int c = tid;
+      const int wc = c / nw, sh = bits * (c - wc * nw);
+      float bs[GMAX];
+#pragma unroll
+      for (int k = 0; k < GMAX; ++k) bs[k] = 0.0f;
+      for (int tt = 0; tt < T; ++tt) {
+        const uint32_t code = (vc[tt * W + wc] >> sh) & cmask;
+        float val;
+        if (METHOD == KVQ_RTN || METHOD == KVQ_VARN) {
+          val = (float)code + h2f(vm[T + tt]);
+        } else if (METHOD == KVQ_INT4) {
+          val = (float)((int)(code << 28) >> 28);
+        } else {
+          val = sm->cb[code] * h2f(vm[tt]) + h2f(vm[T + tt]);
+        }
+#pragma unroll
+        for (int k = 0; k < GMAX; ++k)
+          if (k < G) bs[k] += sm->pv[k][tt] * val;
+      }
+      float s1c = 1.0f;
+      if (METHOD == KVQ_VARN) s1c = h2f(vm[2 * T + c]);
+#pragma unroll
+      for (int k = 0; k < GMAX; ++k) {
+        if (k < G) {
+          float add = bs[k];
+          if (METHOD == KVQ_NUQ) add += sm->osp[k][c];
+          o[k] = o[k] * alpha[k] + add * s1c;
+        }
+      }
+    }
+    __syncthreads();  // every thread is done with stage s
+    if (tid == 0 && i + NSTAGE < n_my) {
+      fence_proxy_async();
+      mbar_arrive_expect_tx(&sm->bar[s], (uint32_t)rec);
+      bulk_g2s(stages + s * rec, rec0 + (uint64_t)(blk + NSTAGE) * g.rec_bytes, (uint32_t)rec, &sm->bar[s]);
+    }
+  }
+
+  if (!ok) {
+    // a wait gave up: wait (bounded) for the copies still in flight before the CTA exits
+    if (tid == 0) {
+      for (int j = failed_at; j < n_my && j < failed_at + NSTAGE; ++j)
+        mbar_wait_bounded(&sm->bar[j % NSTAGE], (uint32_t)((j / NSTAGE) & 1), nullptr, 200000000LL);
+    }
+    __syncthreads();
+    return;
+  }
+#pragma unroll
+  for (int k = 0; k < GMAX; ++k) {
+    if (k < G) {
+      const uint64_t row = ((uint64_t)b * g.Hq + h * G + k) * a.n_split + split;
+      a.ws_o[row * D + tid] = o[k];
+      if (tid == 0) {
+        a.ws_m[row] = m_run[k];
+        a.ws_l[row] = l_run[k];
+      }
+    }
+  }
+}
+
+__global__ void __launch_bounds__(DC_THREADS) combine_kernel(CombineArgs a) {
+  __shared__ float ob[D];
+  __shared__ float qv[D];
+  __shared__ float sc[T];
+  __shared__ float red[DC_THREADS / 32];
+  const Geo& g = a.g;
+  const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
+  const int hq = blockIdx.x, b = blockIdx.y, h = hq / g.G;
+  const uint64_t row0 = ((uint64_t)b * g.Hq + hq) * a.n_split;
+
+  float M = -INFINITY;
+  for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, a.ws_m[row0 + s]);
+  float L = 0.0f, O = 0.0f;
+  for (int s = 0; s < a.n_split; ++s) {
+    float f = exp2f(a.ws_m[row0 + s] - M);
+    L += a.ws_l[row0 + s] * f;
+    O += a.ws_o[(row0 + s) * D + c] * f;
+  }
+  if (g.method == KVQ_VARN && a.hadamard && a.n_split > 0) {
+    ob[c] = O;
+    __syncthreads();
+    smem_fwht(ob, 1);
+    O = ob[c];
+  }
+  if (a.n_tail > 0) {
+    const float2* rope_blk = reinterpret_cast<const float2*>(a.base + g.rope_off);
+    const float2* rope_off = rope_blk + (size_t)(g.max_blocks + 1) * 64;
+    float qc = load_in(a.q + ((uint64_t)b * g.Hq + hq) * D + c, g.in_bf16);
+    qv[c] = qc;
+    __syncthreads();
+    if (g.pre_rope) {  // q0 = R(n0)^T q with n0 = n_blocks*128
+      const int p = c >> 1;
+      float2 cs = rope_blk[(size_t)a.n_blocks * 64 + p];
+      float x0 = qv[2 * p], x1 = qv[2 * p + 1];
+      qc = (c & 1) ? (-cs.y * x0 + cs.x * x1) : (cs.x * x0 + cs.y * x1);
+    }
+    __syncthreads();
+    qv[c] = qc;
+    __syncthreads();
+    const uint16_t* tk = a.tail_k + ((uint64_t)b * g.H + h) * a.n_tail * D;
+    const uint16_t* tv = a.tail_v + ((uint64_t)b * g.H + h) * a.n_tail * D;
+    float mine = -INFINITY;
+    if (c < a.n_tail) {
+      float acc = 0.0f;
+      for (int p = 0; p < 64; ++p) {
+        float k0 = load_in(tk + (uint64_t)c * D + 2 * p, g.in_bf16);
+        float k1 = load_in(tk + (uint64_t)c * D + 2 * p + 1, g.in_bf16);
+        if (g.pre_rope) {
+          float2 cs = rope_off[c * 64 + p];
+          float r0 = cs.x * k0 - cs.y * k1, r1 = cs.y * k0 + cs.x * k1;
+          k0 = r0;
+          k1 = r1;
+        }
+        acc += qv[2 * p] * k0 + qv[2 * p + 1] * k1;
+      }
+      mine = acc * LOG2E_RSQRT_D;
+      sc[c] = mine;
+    }
+    float mx = mine;
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    const float Mn = fmaxf(M, fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])));
+    const float f = exp2f(M - Mn);
+    L *= f;
+    O *= f;
+    __syncthreads();
+    float pl = 0.0f;
+    if (c < a.n_tail) {
+      pl = exp2f(sc[c] - Mn);
+      sc[c] = pl;
+    }
+    for (int off = 16; off > 0; off >>= 1) pl += __shfl_xor_sync(0xffffffffu, pl, off);
+    if (lane == 0) red[warp] = pl;
+    __syncthreads();
+    L += (red[0] + red[1]) + (red[2] + red[3]);
+    for (int j = 0; j < a.n_tail; ++j) O += sc[j] * load_in(tv + (uint64_t)j * D + c, g.in_bf16);
+  }
+  a.out[((uint64_t)b * g.Hq + hq) * D + c] = O / L;
+}
+
+template <int METHOD, int GMAX>
+cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
+  size_t smem = (size_t)NSTAGE * a.g.rec_bytes + sizeof(DecSmem<GMAX>);
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<METHOD, GMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.n_split, a.g.H, a.g.B);
+  decode_kernel<METHOD, GMAX><<<grid, DC_THREADS, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <int METHOD>
+cudaError_t launch_decode_m(const DecodeArgs& a, cudaStream_t st) {
+  const int G = a.g.G;
+  if (G <= 1) return launch_decode_t<METHOD, 1>(a, st);
+  if (G <= 2) return launch_decode_t<METHOD, 2>(a, st);
+  if (G <= 4) return launch_decode_t<METHOD, 4>(a, st);
+  if (G <= 8) return launch_decode_t<METHOD, 8>(a, st);
+  return launch_decode_t<METHOD, 16>(a, st);
+}
+
+}  // namespace kvq
+
+cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const float* codebook, const uint16_t* q,
+                              const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, int n_blocks,
+                              int n_split, float* ws, float* out, int* status, int hadamard, cudaStream_t st) {
+  using namespace kvq;
+  const uint64_t rows = (uint64_t)g.B * g.Hq * n_split;
+  float* ws_m = ws;
+  float* ws_l = ws + rows;
+  float* ws_o = ws + 2 * rows + ((4 - (2 * rows) % 4) % 4);  // keep o 16-byte aligned
+  if (n_blocks > 0) {
+    DecodeArgs a;
+    a.g = g; a.base = base; a.codebook = codebook; a.q = q; a.n_blocks = n_blocks; a.n_split = n_split;
+    a.ws_m = ws_m; a.ws_l = ws_l; a.ws_o = ws_o; a.status = status; a.hadamard = hadamard;
+    cudaError_t e;
+    switch (g.method) {
+      case KVQ_RTN: e = launch_decode_m<KVQ_RTN>(a, st); break;
+      case KVQ_NUQ: e = launch_decode_m<KVQ_NUQ>(a, st); break;
+      case KVQ_VARN: e = launch_decode_m<KVQ_VARN>(a, st); break;
+      default: e = launch_decode_m<KVQ_INT4>(a, st); break;
+    }
+    if (e != cudaSuccess) return e;
+  }
+  CombineArgs c;
+  c.g = g; c.base = base; c.q = q; c.tail_k = tail_k; c.tail_v = tail_v; c.n_tail = n_tail;
+  c.n_blocks = n_blocks; c.n_split = n_blocks > 0 ? n_split : 0; c.ws_m = ws_m; c.ws_l = ws_l; c.ws_o = ws_o;
+  c.out = out; c.hadamard = hadamard;
+  dim3 grid(g.Hq, g.B);
+  combine_kernel<<<grid, DC_THREADS, 0, st>>>(c);
+  return cudaGetLastError();
+}
+
+size_t kvq_decode_ws_floats(const kvq::Geo& g, int n_split) {
+  const uint64_t rows = (uint64_t)g.B * g.Hq * n_split;
+  return 2 * rows + 4 + rows * kvq::D;
+}

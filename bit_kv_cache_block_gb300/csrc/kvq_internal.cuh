@@ -1,0 +1,151 @@
+// Internal definitions shared by the translation units of libkvq (not installed).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+constexpr int T = 128;      // tokens per block
+constexpr int D = 128;      // head dim
+constexpr int TILE = T * D; // elements per tile
+
+__host__ __device__ constexpr int codes_per_word(int bits) { return 32 / bits; }
+__host__ __device__ constexpr int words_per_row(int bits) {
+  return (D + codes_per_word(bits) - 1) / codes_per_word(bits);
+}
+__host__ __device__ constexpr uint64_t round16(uint64_t x) { return (x + 15) & ~uint64_t(15); }
+
+// Number of fp16 vectors of 128 in a tile's metadata region.
+__host__ __device__ inline int meta_vectors(int method) {
+  switch (method) {
+    case KVQ_RTN: return 2;    // s, z
+    case KVQ_NUQ: return 2;    // s, zp
+    case KVQ_VARN: return 3;   // s, z, s1
+    default: return 1;         // INT4: s
+  }
+}
+
+// Outliers per tile: ceil(frac * 16384) with frac taken as the stored fp32 value.
+inline int n_outliers_for(float frac) {
+  if (!(frac > 0.0f)) return 0;
+  double n = (double)frac * (double)TILE;
+  long long c = (long long)n;
+  if ((double)c < n) ++c;
+  if (c > TILE) c = TILE;
+  return (int)c;
+}
+
+inline uint64_t csr_bytes_for(int n_out) {
+  if (n_out == 0) return 0;
+  return round16((uint64_t)n_out * 2 + (uint64_t)(T + 1) * 2 + (uint64_t)n_out);
+}
+
+// Parameters every kernel needs, passed by value.
+struct Geo {
+  int method, bits, B, H, Hq, G, max_blocks, in_bf16, pre_rope, n_out, W;
+  uint64_t rec_bytes;
+  uint32_t codes_off[2], meta_off[2], csr_off[2];
+  uint64_t rope_off;
+};
+
+inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
+  Geo g;
+  g.method = c.method; g.bits = c.bits; g.B = c.batch; g.H = c.n_kv_heads; g.Hq = c.n_q_heads;
+  g.G = c.n_q_heads / c.n_kv_heads; g.max_blocks = c.max_blocks; g.in_bf16 = c.in_dtype == KVQ_BF16;
+  g.pre_rope = c.pre_rope; g.n_out = l.n_outliers; g.W = l.words_per_row; g.rec_bytes = l.record_bytes;
+  for (int k = 0; k < 2; ++k) {
+    g.codes_off[k] = (uint32_t)l.codes_off[k];
+    g.meta_off[k] = (uint32_t)l.meta_off[k];
+    g.csr_off[k] = (uint32_t)l.csr_off[k];
+  }
+  g.rope_off = l.rope_off;
+  return g;
+}
+
+__host__ __device__ inline uint64_t record_index(const Geo& g, int b, int h, int blk) {
+  return ((uint64_t)b * g.H + h) * g.max_blocks + blk;
+}
+
+// ----------------------------------------------------------------- device helpers
+
+__device__ __forceinline__ float load_in(const uint16_t* p, int bf16) {
+  uint16_t u = *p;
+  return bf16 ? __bfloat162float(__ushort_as_bfloat16(u)) : __half2float(__ushort_as_half(u));
+}
+
+__device__ __forceinline__ float in_bits_to_f32(uint16_t u, int bf16) {
+  return bf16 ? __bfloat162float(__ushort_as_bfloat16(u)) : __half2float(__ushort_as_half(u));
+}
+
+__device__ __forceinline__ float h2f(uint16_t u) { return __half2float(__ushort_as_half(u)); }
+__device__ __forceinline__ uint16_t f2h_rn(float x) { return __half_as_ushort(__float2half_rn(x)); }
+
+// First device-side error wins.
+__device__ __forceinline__ void report(int* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+// 1-D bulk copy global -> shared, completion counted on an mbarrier (bytes: multiple of 16,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for phase `parity` of an mbarrier for at most ~`max_cycles` SM clocks. Returns false
+// (and records KVQ_ERR_TIMEOUT) when the wait gives up.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status,
+                                                  long long max_cycles = 2000000000LL) {
+  if (mbar_try_wait(bar, parity)) return true;
+  long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (clock64() - t0 > max_cycles) {
+      report(status, KVQ_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+}  // namespace kvq

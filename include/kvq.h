@@ -1,0 +1,213 @@
+/*
+ * kvq.h - C ABI of libkvq: low-bit KV-cache quantization in 128-token blocks and
+ * decode attention that reads the packed cache directly (sm_103a, one GPU).
+ *
+ * Sources (cited by page and section):
+ *   [KVQ] "KVQuant: Towards 10 Million Context Length LLM Inference with KV Cache
+ *         Quantization" reading notes (zhongzhuzhou.org).
+ *   [KVN] "KVarN: Variance-Normalized KV-Cache Quantization Mitigates Error Accumulation
+ *         in Reasoning Tasks" summary (paper.rainbus.top).
+ *   [TQ]  TurboQuant KV-cache reproduction blog (pwwt.cn).
+ *
+ * Conventions shared by every call
+ *   - All tensors live in device memory owned by the caller; the library allocates
+ *     nothing (no cudaMalloc, no host buffers beyond its arguments).
+ *   - Calls are asynchronous on the given stream. The returned kvq_status covers argument
+ *     checks and launch errors only. Errors found on the device (a bounded wait that gave
+ *     up, an index out of range) are written to the caller's device status word
+ *     (kvq_cache.dev_status, first error wins); read it after a synchronize.
+ *   - Pointers passed to the library must be 16-byte aligned; the cache base must be
+ *     128-byte aligned. Violations return KVQ_ERR_ALIGNMENT and launch nothing.
+ *   - head_dim and block are both 128. A "tile" is one (batch b, KV head h, block) slab
+ *     of 128 tokens x 128 channels of K or of V.
+ *   - K, V, q and tail inputs are in cfg.in_dtype (fp16 or bf16), contiguous, layout
+ *     given per call. Outputs are fp32.
+ *   - Nothing here falls back to the CPU: without a usable CUDA device every call that
+ *     launches work returns KVQ_ERR_CUDA.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KVQ_FORMAT_VERSION 1u
+#define KVQ_BLOCK 128
+#define KVQ_HEAD_DIM 128
+#define KVQ_MAX_GROUP 16      /* n_q_heads / n_kv_heads supported by decode */
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,   /* a NULL pointer, a size out of range, an inconsistent config */
+  KVQ_ERR_UNSUPPORTED = 2,   /* a valid but unimplemented combination (e.g. INT4 with bits != 4) */
+  KVQ_ERR_CAPACITY = 3,      /* an append past cfg.max_blocks, or a buffer smaller than needed */
+  KVQ_ERR_ALIGNMENT = 4,     /* a pointer that breaks the alignment rules above */
+  KVQ_ERR_CUDA = 5,          /* a CUDA runtime error (launch failure, no device) */
+  KVQ_ERR_TIMEOUT = 6        /* device side: a bounded wait gave up (written to dev_status) */
+} kvq_status;
+
+/* Quantization method of a cache (fixed for its lifetime). */
+typedef enum {
+  KVQ_RTN = 0,   /* KIVI-style asymmetric round-to-nearest: keys per channel over the 128 tokens
+                    of a block, values per token over the 128 channels; x_dq = (q + z) * s
+                    ([KVN] preliminaries; [KVQ] §1.2, §3.1). bits 2..4. */
+  KVQ_NUQ = 1,   /* KVQuant: per-channel keys (optionally pre-RoPE) and per-token values normalised
+                    to [-1, 1] by the non-outlier centre/half-range, nearest entry of a per-KV-head
+                    2^bits codebook, and the ceil(outlier_frac * 16384) largest-|x| entries of each
+                    tile kept in fp16 as CSR ([KVQ] §3.2-3.4, §3.8 Algorithm 1). bits 2..4. */
+  KVQ_VARN = 2,  /* KVarN: FWHT-128 on channels, Sinkhorn-style variance normalisation, RTN
+                    (keys per channel, values per token) and a second fp16 scale s1 (keys: per
+                    token, values: per channel); x_dq = (q + z) * s * s1 ([KVN] method steps 1-5).
+                    bits 2..4. */
+  KVQ_INT4 = 3   /* TurboQuant-style symmetric int4 absmax: one fp16 scale per token's 128
+                    channels, q = clamp(rne(x/s), -8, 7) stored as two's complement nibbles
+                    ([TQ] §2.1, §4.2). bits must be 4. */
+} kvq_method;
+
+typedef enum { KVQ_F16 = 0, KVQ_BF16 = 1 } kvq_dtype;
+
+/* Cache configuration. All fields are read by kvq_layout / kvq_cache_init. */
+typedef struct {
+  int32_t method;        /* kvq_method */
+  int32_t bits;          /* code width: 2, 3 or 4 (INT4: 4) */
+  int32_t batch;         /* B >= 1 */
+  int32_t n_kv_heads;    /* H_kv >= 1 */
+  int32_t n_q_heads;     /* H_q, a multiple of H_kv, H_q / H_kv <= KVQ_MAX_GROUP */
+  int32_t head_dim;      /* must be 128 */
+  int32_t block;         /* must be 128 */
+  int32_t max_blocks;    /* capacity per (b, h) in blocks of 128 tokens, >= 1 */
+  int32_t in_dtype;      /* kvq_dtype of K, V, q and the tail */
+  int32_t pre_rope;      /* NUQ only: keys are stored before RoPE; decode rotates them at their
+                            absolute position after dequantisation ([KVQ] §3.2). 0 otherwise. */
+  double rope_theta;     /* RoPE base (10000): angle of channel pair i at position n is
+                            n * theta^(-2i/128) ([KVQ] §1.3) */
+  float outlier_frac;    /* NUQ: fraction of each tile kept as fp16 outliers (0.01); 0 disables */
+  int32_t varn_iters;    /* VARN: variance-normalisation iterations (8); 0..64 */
+  int32_t hadamard;      /* VARN: 1 applies the FWHT-128 (the decode transforms q and o too) */
+} kvq_config;
+
+/* Byte layout of a cache, from kvq_layout. One record per (b, h, block), at
+ *   base + ((b * n_kv_heads + h) * max_blocks + block) * record_bytes,
+ * holding the K tile then the V tile; every region starts 16-byte aligned:
+ *   codes : 128 rows (tokens) x words_per_row uint32; code i of a row at bits
+ *           [b*(i%n)+b-1 : b*(i%n)] of word i/n, n = floor(32/b), unused high bits zero
+ *           ([KVQ] §9.3 3-bit layout, generalised)
+ *   meta  : fp16 vectors of 128. RTN and VARN: s, z (keys: per channel; values: per token),
+ *           VARN adds s1 (keys: per token; values: per channel). NUQ: s (half-range),
+ *           zp (centre). INT4: s (per token).
+ *   csr   : NUQ only: val fp16[n_outliers], row_ptr uint16[129] (row = token),
+ *           col uint8[n_outliers] (channel), zero padded.
+ * After the records, for pre-RoPE caches: a table of (cos, sin) fp32 pairs of
+ * block*128*theta_i for block = 0..max_blocks, then of t*theta_i for t = 0..127 (64 pairs each),
+ * written by kvq_cache_init. */
+typedef struct {
+  uint64_t record_bytes;
+  uint64_t codes_off[2], codes_bytes[2];   /* [0] = K, [1] = V, offsets within a record */
+  uint64_t meta_off[2], meta_bytes[2];
+  uint64_t csr_off[2], csr_bytes[2];
+  uint64_t records_bytes;                  /* B * H_kv * max_blocks * record_bytes */
+  uint64_t rope_off, rope_bytes;           /* from base; rope_bytes = 0 without pre-RoPE keys */
+  uint64_t total_bytes;                    /* bytes the caller must provide at base */
+  int32_t words_per_row;
+  int32_t n_outliers;                      /* NUQ: outliers per tile; 0 otherwise */
+  uint32_t format_version;                 /* KVQ_FORMAT_VERSION */
+  int32_t reserved;
+} kvq_layout_t;
+
+/* A cache handle: plain data owned by the caller. kvq_cache_init fills it. */
+typedef struct {
+  kvq_config cfg;
+  kvq_layout_t lay;
+  void* base;              /* device, lay.total_bytes, caller-owned */
+  const float* codebook;   /* device fp32 [n_kv_heads][2^bits], NUQ only (else NULL), caller-owned */
+  int32_t* dev_status;     /* device int32, caller-owned; 0 = no device-side error */
+  int32_t n_blocks;        /* blocks appended so far, per (b, h) */
+  int32_t device;          /* CUDA device ordinal the cache was initialised on */
+} kvq_cache;
+
+/* Human-readable name of a status code (static string). */
+const char* kvq_status_str(kvq_status s);
+
+/* Dense KV-cache size 2*n*h*d*e*b*l bytes ([KVQ] §1.1; [TQ] §1.1). Pure. */
+uint64_t kvq_dense_kv_bytes(int64_t n_layers, int64_t n_heads, int64_t head_dim,
+                            int64_t elem_bytes, int64_t batch, int64_t seq_len);
+
+/* Checks cfg and computes its layout. Host only, pure; *out is written only on KVQ_OK. */
+kvq_status kvq_layout(const kvq_config* cfg, kvq_layout_t* out);
+
+/* Binds caller memory to a cache: checks cfg, the size (bytes >= lay.total_bytes) and the
+ * alignment, records the pointers and sets n_blocks = 0. For pre-RoPE caches it launches one
+ * kernel on `stream` that writes the RoPE tables (fp64 angles rounded to fp32). It also sets
+ * *dev_status = 0 on `stream`. codebook: NUQ only, device fp32 [n_kv_heads][2^bits], read by
+ * every append and decode (keep it alive and unchanged). No allocation. */
+kvq_status kvq_cache_init(kvq_cache* cache, const kvq_config* cfg, void* dev_base, size_t bytes,
+                          const float* dev_codebook, int32_t* dev_status, cudaStream_t stream);
+
+/* Quantizes n_blocks new blocks of 128 tokens for every (b, h) and stores them at block
+ * positions cache->n_blocks .. cache->n_blocks + n_blocks - 1; on success cache->n_blocks
+ * grows by n_blocks ([KVQ] §3.8 Algorithm 1 inference steps 1-4; [KVN] method steps 1-4;
+ * [TQ] §4.2 quantize_kv_block).
+ *   k, v            : device [B][H_kv][n_blocks*128][128] in cfg.in_dtype (pre-RoPE keys for
+ *                     pre-RoPE caches). Partial blocks are not accepted: fewer than 128 new
+ *                     tokens stay in the caller's fp tail.
+ *   dbg_varn_scales : VARN only, nullable: device fp32 [B][H_kv][n_blocks][2 (K, V)][2 (r, c)][128]
+ *                     receives the unrounded VarN token scales r and channel scales c.
+ * Returns KVQ_ERR_CAPACITY (nothing written) if cache->n_blocks + n_blocks > max_blocks. */
+kvq_status kvq_append_block(kvq_cache* cache, const void* k, const void* v, int32_t n_blocks,
+                            float* dbg_varn_scales, cudaStream_t stream);
+
+/* Drops the newest blocks: sets cache->n_blocks = n_blocks (0 <= n_blocks <= current).
+ * Host only; the dropped records are overwritten by later appends. */
+kvq_status kvq_truncate(kvq_cache* cache, int32_t n_blocks);
+
+/* kvq_truncate(cache, 0). */
+kvq_status kvq_reset(kvq_cache* cache);
+
+/* Number of sequence splits the decode uses for n_blocks cached blocks (a pure function of
+ * the config and n_blocks). */
+int32_t kvq_decode_splits(const kvq_config* cfg, int32_t n_blocks);
+
+/* Device workspace kvq_decode_attn needs for n_blocks cached blocks, in bytes. Pure. */
+kvq_status kvq_decode_workspace_bytes(const kvq_config* cfg, int32_t n_blocks, size_t* out);
+
+/* Packed-cache bytes one decode step reads for n_blocks blocks per (b, h): code words plus
+ * metadata plus CSR records, K and V (the algorithmic byte count of the decode). Pure. */
+uint64_t kvq_decode_bytes(const kvq_config* cfg, int32_t n_blocks);
+
+/* Decode attention of one new query per head over the packed cache plus an fp tail
+ * ([KVQ] §3.7 fused matvec kernels and Algorithm 1 dequantisation; [TQ] §5.2 fused dequant
+ * inside attention): out = softmax(q . k_n / sqrt(128)) weighted sum of v_n over the n_blocks*128
+ * cached tokens then the n_tail tail tokens, where k_n and v_n are dequantised in registers
+ * (never written to memory), pre-RoPE keys are rotated at their absolute position n, and KVarN
+ * caches are read in the Hadamard domain (q is transformed, the output transformed back).
+ * Query head j attends with KV head j / (H_q / H_kv).
+ *   q        : device [B][H_q][128] in cfg.in_dtype (already position-encoded for pre-RoPE caches)
+ *   tail_k/v : device [B][H_kv][n_tail][128] in cfg.in_dtype, tokens at positions
+ *              n_blocks*128 + j (pre-RoPE keys are rotated there); NULL when n_tail == 0
+ *   n_tail   : 0..127
+ *   out      : device fp32 [B][H_q][128]
+ *   workspace: device scratch of at least kvq_decode_workspace_bytes(cfg, n_blocks) bytes
+ * At least one token must be attended (n_blocks > 0 or n_tail > 0). */
+kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const void* tail_k,
+                           const void* tail_v, int32_t n_tail, float* out, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/* Dequantises blocks [first_block, first_block + n_blocks) of every (b, h) to fp32, for
+ * checking only (never on the decode path: [TQ] §4.2 and §5.2 warn that materialising costs
+ * more than it saves).
+ *   domain 0: the stored representation (pre-RoPE keys un-rotated, KVarN in the Hadamard domain)
+ *   domain 1: the input domain (inverse Hadamard for KVarN; same as 0 otherwise)
+ *   out_k, out_v: device fp32 [B][H_kv][n_blocks*128][128]; either may be NULL to skip. */
+kvq_status kvq_dequant(const kvq_cache* cache, int32_t first_block, int32_t n_blocks,
+                       int32_t domain, float* out_k, float* out_v, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

@@ -1,0 +1,119 @@
+"""Helpers shared by the tests: build a device cache for a workload, upload seeded inputs,
+read the device records back through the layout, compare them with the oracle's records."""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle as O
+import workloads as WL
+
+T, D = 128, 128
+
+
+def torch_mod():
+    import torch
+    return torch
+
+
+def cfg_for(w: WL.Workload, max_blocks=None, batch=None):
+    import bit_kv_cache_block_gb300 as K
+    return K.make_config(w.method, w.bits, batch or w.batch, w.n_kv_heads, w.n_q_heads,
+                         max_blocks or w.n_blocks, in_dtype=w.dtype, pre_rope=w.pre_rope,
+                         rope_theta=w.rope_theta, outlier_frac=w.outlier_frac, varn_iters=w.varn_iters,
+                         hadamard=True)
+
+
+def codebook_for(w: WL.Workload):
+    if w.method != "nuq":
+        return None
+    return np.broadcast_to(O.nuq_codebook(w.bits), (w.n_kv_heads, 2 ** w.bits)).copy()
+
+
+def to_device(x: np.ndarray, dtype: str, device="cuda"):
+    """float32 values (exactly representable in dtype) -> device tensor of that dtype."""
+    torch = torch_mod()
+    bits = WL.to_storage(np.ascontiguousarray(x), dtype)
+    t = torch.from_numpy(bits.view(np.int16).copy()).to(device)
+    return t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
+
+
+def new_cache(w: WL.Workload, max_blocks=None, batch=None):
+    import bit_kv_cache_block_gb300 as K
+    torch = torch_mod()
+    cb = codebook_for(w)
+    return K.KVCache(cfg_for(w, max_blocks, batch), None if cb is None else torch.from_numpy(cb))
+
+
+def records_np(cache) -> np.ndarray:
+    return cache.record_view().cpu().numpy()
+
+
+def tile_fields(rec: np.ndarray, lay, kind: int, method: str, bits: int) -> dict:
+    """Decode one record's K (kind 0) or V (kind 1) regions into arrays."""
+    W = lay.words_per_row
+    co, cb = int(lay.codes_off[kind]), int(lay.codes_bytes[kind])
+    mo, mb = int(lay.meta_off[kind]), int(lay.meta_bytes[kind])
+    out = dict(words=rec[co:co + cb].view(np.uint32).reshape(T, W).copy())
+    meta = rec[mo:mo + mb].view(np.uint16).reshape(-1, T)
+    out["s16"] = meta[0].view(np.float16).copy()
+    if method in ("rtn", "varn"):
+        out["z16"] = meta[1].view(np.float16).copy()
+    if method == "varn":
+        out["s1"] = meta[2].view(np.float16).copy()
+    if method == "nuq":
+        out["zp16"] = meta[1].view(np.float16).copy()
+        n = int(lay.n_outliers)
+        if n:
+            so = int(lay.csr_off[kind])
+            csr = rec[so:so + int(lay.csr_bytes[kind])]
+            out["val"] = csr[:2 * n].view(np.uint16).copy()
+            out["row_ptr"] = csr[2 * n:2 * n + 2 * (T + 1)].view(np.uint16).copy()
+            out["col"] = csr[2 * n + 2 * (T + 1):3 * n + 2 * (T + 1)].copy()
+            out["csr_pad"] = csr[3 * n + 2 * (T + 1):].copy()
+    return out
+
+
+def serialize_tile(rec: np.ndarray, lay, kind: int, otile: dict, method: str) -> None:
+    """Write an oracle tile record into the byte layout (for feeding oracle planes to the GPU)."""
+    co, mo = int(lay.codes_off[kind]), int(lay.meta_off[kind])
+    words = np.ascontiguousarray(otile["words"], np.uint32)
+    rec[co:co + words.nbytes] = words.view(np.uint8).ravel()
+    vecs = [otile["s16"]]
+    if method in ("rtn", "varn"):
+        vecs.append(otile["z16"])
+    if method == "varn":
+        vecs.append(otile["s1"])
+    if method == "nuq":
+        vecs.append(otile["zp16"])
+    meta = np.stack([np.asarray(v, np.float16) for v in vecs]).view(np.uint8).ravel()
+    rec[mo:mo + meta.size] = meta
+    n = int(lay.n_outliers)
+    if method == "nuq" and n:
+        so = int(lay.csr_off[kind])
+        rec[so:so + 2 * n] = np.asarray(otile["val"], np.uint16).view(np.uint8)
+        rec[so + 2 * n:so + 2 * n + 2 * (T + 1)] = np.asarray(otile["row_ptr"], np.uint16).view(np.uint8)
+        rec[so + 2 * n + 2 * (T + 1):so + 3 * n + 2 * (T + 1)] = np.asarray(otile["col"], np.uint8)
+
+
+def f16_bits(x) -> np.ndarray:
+    return np.asarray(x, np.float16).view(np.uint16)
+
+
+def near_f16_midpoint(v: np.ndarray, rel: float = 1e-5) -> np.ndarray:
+    """True where a positive/negative value lies within rel of a rounding midpoint of fp16."""
+    v = np.asarray(v, np.float64)
+    h = v.astype(np.float16)
+    hf = h.astype(np.float64)
+    up = np.nextafter(h, np.float16(np.inf)).astype(np.float64)
+    dn = np.nextafter(h, np.float16(-np.inf)).astype(np.float64)
+    other = np.where(hf <= v, up, dn)
+    mid = (hf + other) / 2
+    return np.abs(v - mid) <= rel * np.maximum(np.abs(v), 1e-30)
+
+
+def ulp_apart(a16: np.ndarray, b16: np.ndarray) -> np.ndarray:
+    """|ordinal(a) - ordinal(b)| for fp16 arrays (works across zero)."""
+    def ordn(x):
+        u = np.asarray(x, np.float16).view(np.uint16).astype(np.int32)
+        return np.where(u & 0x8000, -(u & 0x7fff), u)
+    return np.abs(ordn(a16) - ordn(b16))

@@ -1,0 +1,178 @@
+"""The C ABI without a GPU: the library loads, exports every entry point include/kvq.h
+declares, the ctypes structs match the C layout, and the host-only logic (layouts, sizes,
+argument checks) behaves as documented. No compute call runs here."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as WL
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def K():
+    import __graft_entry__
+    __graft_entry__.build()
+    import bit_kv_cache_block_gb300 as K
+    return K
+
+
+def _header_functions():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(K):
+    declared = _header_functions()
+    assert set(declared) == set(K._lib.EXPORTS)
+    lib = K._lib.lib()
+    for name in declared:
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", K.lib_path()], capture_output=True, text=True).stdout
+    for name in declared:
+        assert re.search(rf"\bT {name}$", out, re.M), f"{name} not exported"
+
+
+def test_struct_layout_matches_c(K, tmp_path):
+    prog = tmp_path / "sizes.c"
+    prog.write_text(r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "kvq.h"
+int main(void) {
+  printf("%zu %zu %zu\n", sizeof(kvq_config), sizeof(kvq_layout_t), sizeof(kvq_cache));
+  printf("%zu %zu %zu %zu\n", offsetof(kvq_config, rope_theta), offsetof(kvq_config, outlier_frac),
+         offsetof(kvq_config, hadamard), offsetof(kvq_layout_t, total_bytes));
+  printf("%zu %zu %zu %zu\n", offsetof(kvq_cache, lay), offsetof(kvq_cache, base), offsetof(kvq_cache, n_blocks),
+         offsetof(kvq_cache, device));
+  return 0;
+}
+''')
+    exe = tmp_path / "sizes"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), "-I", "/usr/local/cuda/include",
+                    str(prog), "-o", str(exe)], check=True)
+    vals = [int(x) for x in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split()]
+    L = K._lib
+    py = [C.sizeof(L.kvq_config), C.sizeof(L.kvq_layout_t), C.sizeof(L.kvq_cache),
+          L.kvq_config.rope_theta.offset, L.kvq_config.outlier_frac.offset, L.kvq_config.hadamard.offset,
+          L.kvq_layout_t.total_bytes.offset, L.kvq_cache.lay.offset, L.kvq_cache.base.offset,
+          L.kvq_cache.n_blocks.offset, L.kvq_cache.device.offset]
+    assert vals == py
+
+
+def test_dense_kv_bytes_matches_oracle(K):
+    for args in [(32, 32, 128, 2, 1, 131072), (32, 8, 128, 2, 16, 8192), (80, 8, 128, 2, 3, 12345)]:
+        assert K.kvq_dense_kv_bytes(*args) == O.kv_cache_bytes(*args)
+
+
+def _cfg(K, wid, **kw):
+    w = WL.WORKLOADS[wid].scaled(**kw)
+    return K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, w.n_blocks, w.dtype, w.pre_rope,
+                         w.rope_theta, w.outlier_frac, w.varn_iters, True)
+
+
+# algorithmic packed bytes per decode step at the full workloads (codes + fp16 metadata + CSR)
+EXPECTED_DECODE_BYTES = {1: 278528, 2: 129728512, 3: 79691776, 4: 1107296256, 5: 2415919104}
+EXPECTED_RECORD_BYTES = {1: 2 * (8192 + 512), 2: 2 * (6656 + 512 + 752), 3: 2 * (4096 + 768),
+                         4: 2 * (8192 + 256), 5: 2 * (4096 + 512)}
+
+
+@pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
+def test_layout_and_decode_bytes(K, wid):
+    cfg = _cfg(K, wid)
+    lay = K.kvq_layout(cfg)
+    w = WL.WORKLOADS[wid]
+    assert lay.record_bytes == EXPECTED_RECORD_BYTES[wid]
+    assert lay.words_per_row == -(-128 // (32 // w.bits))
+    assert lay.format_version == 1
+    for k in range(2):
+        assert lay.codes_off[k] % 16 == 0 and lay.meta_off[k] % 16 == 0 and lay.csr_off[k] % 16 == 0
+    assert lay.records_bytes == w.batch * w.n_kv_heads * w.n_blocks * lay.record_bytes
+    assert lay.total_bytes >= lay.records_bytes
+    if w.pre_rope:
+        assert lay.rope_off % 128 == 0 and lay.rope_bytes == (w.n_blocks + 1 + 128) * 64 * 8
+    if w.method == "nuq":
+        assert lay.n_outliers == O.n_outliers(w.outlier_frac) == 164
+    assert K.kvq_decode_bytes(cfg, w.n_blocks) == EXPECTED_DECODE_BYTES[wid]
+    S = K.kvq_decode_splits(cfg, w.n_blocks)
+    assert 1 <= S <= w.n_blocks
+    assert K.kvq_decode_workspace_bytes(cfg, w.n_blocks) >= 4 * (w.batch * w.n_q_heads * S * 130)
+
+
+def test_config_checks(K):
+    L = K._lib
+    bad = [dict(head_dim=64), dict(block=64), dict(bits=5), dict(bits=1), dict(n_q_heads=33),
+           dict(n_q_heads=8 * 17), dict(max_blocks=0), dict(batch=0), dict(in_dtype=7), dict(method=9)]
+    for b in bad:
+        cfg = _cfg(K, 4)
+        for k, v in b.items():
+            setattr(cfg, k, v)
+        with pytest.raises(K.KVQError):
+            K.kvq_layout(cfg)
+    cfg = _cfg(K, 4)
+    cfg.bits = 3                      # int4 is 4-bit only
+    with pytest.raises(K.KVQError) as e:
+        K.kvq_layout(cfg)
+    assert e.value.status == L.KVQ_ERR_UNSUPPORTED
+    cfg = _cfg(K, 1)
+    cfg.pre_rope = 1                  # pre-RoPE keys only with nuq
+    with pytest.raises(K.KVQError) as e:
+        K.kvq_layout(cfg)
+    assert e.value.status == L.KVQ_ERR_UNSUPPORTED
+
+
+def test_host_argument_checks_launch_nothing(K):
+    """Argument errors are caught on the host before any CUDA call (works without a GPU)."""
+    L = K._lib
+    lib = L.lib()
+    cfg = _cfg(K, 1)
+    lay = K.kvq_layout(cfg)
+    cache = L.kvq_cache()
+    # misaligned base / too small / missing status
+    st = lib.kvq_cache_init(C.byref(cache), C.byref(cfg), C.c_void_p(0x1001), lay.total_bytes, None,
+                            C.c_void_p(0x2000), None)
+    assert st == L.KVQ_ERR_ALIGNMENT
+    st = lib.kvq_cache_init(C.byref(cache), C.byref(cfg), C.c_void_p(0x1000), lay.total_bytes - 1, None,
+                            C.c_void_p(0x2000), None)
+    assert st == L.KVQ_ERR_CAPACITY
+    st = lib.kvq_cache_init(C.byref(cache), C.byref(cfg), C.c_void_p(0x1000), lay.total_bytes, None, None, None)
+    assert st == L.KVQ_ERR_INVALID_ARG
+    ncfg = _cfg(K, 2)
+    nlay = K.kvq_layout(ncfg)
+    st = lib.kvq_cache_init(C.byref(cache), C.byref(ncfg), C.c_void_p(0x1000), nlay.total_bytes, None,
+                            C.c_void_p(0x2000), None)
+    assert st == L.KVQ_ERR_INVALID_ARG            # nuq needs a codebook
+    # a hand-built (never initialised on a device) cache for the append/decode checks
+    cache.cfg = cfg
+    cache.lay = lay
+    cache.base = 0x100000
+    cache.n_blocks = cfg.max_blocks
+    assert lib.kvq_append_block(C.byref(cache), C.c_void_p(0x1000), C.c_void_p(0x2000), 1, None, None) \
+        == L.KVQ_ERR_CAPACITY
+    cache.n_blocks = 0
+    assert lib.kvq_append_block(C.byref(cache), C.c_void_p(0x1008), C.c_void_p(0x2000), 1, None, None) \
+        == L.KVQ_ERR_ALIGNMENT
+    assert lib.kvq_append_block(C.byref(cache), None, C.c_void_p(0x2000), 1, None, None) == L.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_append_block(C.byref(cache), C.c_void_p(0x1000), C.c_void_p(0x2000), 0, None, None) \
+        == L.KVQ_ERR_INVALID_ARG
+    q, out, ws = C.c_void_p(0x1000), C.c_void_p(0x3000), C.c_void_p(0x5000)
+    assert lib.kvq_decode_attn(C.byref(cache), q, None, None, 0, out, ws, 1 << 20, None) == L.KVQ_ERR_INVALID_ARG
+    cache.n_blocks = 4
+    assert lib.kvq_decode_attn(C.byref(cache), q, None, None, 128, out, ws, 1 << 20, None) == L.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_decode_attn(C.byref(cache), q, None, None, 3, out, ws, 1 << 20, None) == L.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_decode_attn(C.byref(cache), q, None, None, 0, out, ws, 16, None) == L.KVQ_ERR_CAPACITY
+    assert lib.kvq_decode_attn(C.byref(cache), C.c_void_p(0x1004), None, None, 0, out, ws, 1 << 20, None) \
+        == L.KVQ_ERR_ALIGNMENT
+    assert lib.kvq_dequant(C.byref(cache), 3, 2, 0, out, None, None) == L.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_dequant(C.byref(cache), 0, 1, 2, out, None, None) == L.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_truncate(C.byref(cache), 5) == L.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_truncate(C.byref(cache), 2) == L.KVQ_OK and cache.n_blocks == 2
+    assert lib.kvq_reset(C.byref(cache)) == L.KVQ_OK and cache.n_blocks == 0
+    assert K.kvq_status_str(L.KVQ_ERR_TIMEOUT) == "device wait timed out"
