@@ -17,7 +17,7 @@ from ._lib import (KVQ_BF16, KVQ_F16, KVQ_INT4, KVQ_NUQ, KVQ_OK, KVQ_RTN, KVQ_VA
 
 __all__ = ["make_config", "kvq_layout", "kvq_dense_kv_bytes", "kvq_cache_init", "kvq_append_block",
            "kvq_truncate", "kvq_reset", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
-           "kvq_decode_attn", "kvq_dequant", "kvq_status_str", "KVCache", "KVQError", "kvq_config",
+           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_dequant", "kvq_status_str", "KVCache", "KVQError", "kvq_config",
            "kvq_layout_t", "kvq_cache", "lib_path"]
 
 
@@ -122,6 +122,15 @@ def kvq_decode_attn(cache: kvq_cache, q, tail_k, tail_v, n_tail: int, out, works
     _lib.check(_lib.lib().kvq_decode_attn(C.byref(cache), _ptr(q), _ptr(tail_k), _ptr(tail_v), int(n_tail),
                                           _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)),
                "kvq_decode_attn")
+
+
+def kvq_decode_attn_static(cache: kvq_cache, q, tail_k, tail_v, n_tail: int, out, stream=None) -> None:
+    """kvq_decode_attn with the library's own fixed scratch instead of a caller workspace, for
+    callers that cannot allocate device memory. Calls that may overlap on the GPU share that
+    scratch and race; the first call on a device looks up its address (no allocation)."""
+    _lib.check(_lib.lib().kvq_decode_attn_static(C.byref(cache), _ptr(q), _ptr(tail_k), _ptr(tail_v),
+                                                 int(n_tail), _ptr(out), _stream(stream)),
+               "kvq_decode_attn_static")
 
 
 def kvq_dequant(cache: kvq_cache, first_block: int, n_blocks: int, domain: int, out_k, out_v, stream=None) -> None:

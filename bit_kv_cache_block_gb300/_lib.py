@@ -16,12 +16,13 @@ KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY, KVQ_ERR_ALIG
 KVQ_RTN, KVQ_NUQ, KVQ_VARN, KVQ_INT4 = range(4)
 KVQ_F16, KVQ_BF16 = 0, 1
 KVQ_FORMAT_VERSION = 1
+KVQ_STATIC_WORKSPACE_BYTES = 8 << 20
 METHODS = {"rtn": KVQ_RTN, "nuq": KVQ_NUQ, "varn": KVQ_VARN, "int4": KVQ_INT4}
 
 # every entry point declared in include/kvq.h
 EXPORTS = ["kvq_status_str", "kvq_dense_kv_bytes", "kvq_layout", "kvq_cache_init", "kvq_append_block",
            "kvq_truncate", "kvq_reset", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
-           "kvq_decode_attn", "kvq_dequant"]
+           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_dequant"]
 
 
 class kvq_config(C.Structure):
@@ -81,6 +82,8 @@ def lib() -> C.CDLL:
     L.kvq_decode_bytes.argtypes = [P(kvq_config), i32]
     L.kvq_decode_attn.restype = C.c_int
     L.kvq_decode_attn.argtypes = [P(kvq_cache), vp, vp, vp, i32, vp, vp, sz, vp]
+    L.kvq_decode_attn_static.restype = C.c_int
+    L.kvq_decode_attn_static.argtypes = [P(kvq_cache), vp, vp, vp, i32, vp, vp]
     L.kvq_dequant.restype = C.c_int
     L.kvq_dequant.argtypes = [P(kvq_cache), i32, i32, i32, vp, vp, vp]
     _lib = L

@@ -13,6 +13,7 @@ size_t kvq_decode_ws_floats(const kvq::Geo& g, int n_split);
 cudaError_t kvq_launch_dequant(const kvq::Geo& g, const uint8_t* base, const float* codebook, int first, int n,
                                int domain, int hadamard, float* out_k, float* out_v, cudaStream_t st);
 cudaError_t kvq_launch_rope_init(float2* tab, int max_blocks, double theta, cudaStream_t st);
+cudaError_t kvq_static_workspace(float** ptr, size_t* n_floats);
 
 namespace {
 
@@ -226,6 +227,38 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const void* ta
                              static_cast<const uint16_t*>(tail_v), n_tail, nb, S, static_cast<float*>(workspace),
                              out, cache->dev_status, hadamard_of(cache->cfg), stream);
   });
+}
+
+kvq_status kvq_decode_attn_static(const kvq_cache* cache, const void* q, const void* tail_k, const void* tail_v,
+                                  int32_t n_tail, float* out, cudaStream_t stream) {
+  if (!cache || !cache->base || !q || !out) return KVQ_ERR_INVALID_ARG;
+  if (check_config(&cache->cfg) != KVQ_OK) return KVQ_ERR_INVALID_ARG;
+  if (n_tail < 0 || n_tail >= KVQ_BLOCK) return KVQ_ERR_INVALID_ARG;
+  if (n_tail > 0 && (!tail_k || !tail_v)) return KVQ_ERR_INVALID_ARG;
+  const int nb = cache->n_blocks;
+  if (nb + n_tail == 0) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16)) return KVQ_ERR_ALIGNMENT;
+  if (n_tail > 0 && (!aligned(tail_k, 16) || !aligned(tail_v, 16))) return KVQ_ERR_ALIGNMENT;
+  const kvq::Geo g = kvq::make_geo(cache->cfg, cache->lay);
+  const int S = kvq_decode_splits(&cache->cfg, nb);
+  const size_t need = kvq_decode_ws_floats(g, S) * sizeof(float);
+  if (need > KVQ_STATIC_WORKSPACE_BYTES) return KVQ_ERR_CAPACITY;
+  kvq_status cap = KVQ_OK;
+  kvq_status s = on_device(cache->device, [&]() -> cudaError_t {
+    float* ws = nullptr;
+    size_t n_floats = 0;
+    cudaError_t e = kvq_static_workspace(&ws, &n_floats);
+    if (e != cudaSuccess) return e;
+    if (need > n_floats * sizeof(float)) {
+      cap = KVQ_ERR_CAPACITY;
+      return cudaSuccess;
+    }
+    return kvq_launch_decode(g, static_cast<const uint8_t*>(cache->base), cache->codebook,
+                             static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(tail_k),
+                             static_cast<const uint16_t*>(tail_v), n_tail, nb, S, ws, out, cache->dev_status,
+                             hadamard_of(cache->cfg), stream);
+  });
+  return s != KVQ_OK ? s : cap;
 }
 
 kvq_status kvq_dequant(const kvq_cache* cache, int32_t first_block, int32_t n_blocks, int32_t domain, float* out_k,

@@ -483,3 +483,39 @@ size_t kvq_decode_ws_floats(const kvq::Geo& g, int n_split) {
   const uint64_t rows = (uint64_t)g.B * g.Hq * n_split;
   return 2 * rows + 4 + rows * kvq::D;
 }
+
+// ------------------------------------------------------------------ library-owned decode scratch
+//
+// kvq_decode_attn_static runs the same decode as kvq_decode_attn but keeps the split partials in
+// this file-scope device array instead of a caller buffer. The array exists once per GPU that
+// loads the library and lives until the process exits. Host code must not pass its name to a
+// kernel (on the host it is only a stand-in); kvq_static_workspace() looks up its device
+// address with cudaGetSymbolAddress, once per device, with that device current.
+#include <mutex>
+
+namespace {
+constexpr size_t kStaticWsFloats = (size_t)KVQ_STATIC_WORKSPACE_BYTES / sizeof(float);
+static __device__ __align__(256) float g_decode_scratch[kStaticWsFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[kMaxDevices] = {};
+}  // namespace
+
+// Device address of the scratch array on the current device (looked up on first use).
+cudaError_t kvq_static_workspace(float** ptr, size_t* n_floats) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return e;
+    g_scratch_ptr[dev] = static_cast<float*>(p);
+  }
+  *ptr = g_scratch_ptr[dev];
+  *n_floats = kStaticWsFloats;
+  return cudaSuccess;
+}

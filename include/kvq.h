@@ -197,6 +197,28 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const void* ta
                            const void* tail_v, int32_t n_tail, float* out, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
 
+/* Size of the decode scratch that the library itself holds for kvq_decode_attn_static:
+ * one copy per GPU that loads the library, kept until the process exits. */
+#define KVQ_STATIC_WORKSPACE_BYTES (8u << 20)
+
+/* kvq_decode_attn without a workspace argument, for callers that cannot allocate device
+ * memory or hand the library a scratch buffer. Examples: an engine whose whole device memory
+ * pool is owned by another allocator, or a latency-critical loop where a cudaMalloc (which
+ * may synchronise the device) is not acceptable. The pages have no counterpart: this is a
+ * deployment convenience, not part of the method.
+ *
+ * Same arguments, results and checks as kvq_decode_attn, minus the workspace. The split
+ * partials go to a fixed device array of KVQ_STATIC_WORKSPACE_BYTES inside the library; a
+ * decode that would need more (see kvq_decode_workspace_bytes) returns KVQ_ERR_CAPACITY and
+ * launches nothing. No memory is allocated on any call: the first call on a device looks up
+ * the array's device address (make that first call before any stream capture), later calls
+ * reuse it. Nothing in the array needs to start at zero: every call writes each partial
+ * before reading it. All calls on a device share the one array and it keeps the last call's
+ * contents, so calls that may overlap on the GPU (other streams, other host threads) race
+ * and give wrong results: order them on one stream or synchronise between them. */
+kvq_status kvq_decode_attn_static(const kvq_cache* cache, const void* q, const void* tail_k,
+                                  const void* tail_v, int32_t n_tail, float* out, cudaStream_t stream);
+
 /* Dequantises blocks [first_block, first_block + n_blocks) of every (b, h) to fp32, for
  * checking only (never on the decode path: [TQ] §4.2 and §5.2 warn that materialising costs
  * more than it saves).
