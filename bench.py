@@ -158,6 +158,8 @@ def run_kvq(args):
         torch.distributed.barrier()
     K._lib.lib()
     w = WL.WORKLOADS[args.config]
+    if args.ctx:
+        w = w.scaled(ctx=args.ctx)
     nb = w.n_blocks
     cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, nb + 1, w.dtype, w.pre_rope,
                         w.rope_theta, w.outlier_frac, w.varn_iters, True)
@@ -191,64 +193,76 @@ def run_kvq(args):
     blk_v = torch.cat([tail_v, tail_v[:, :, :1]], dim=2).contiguous()
     ws = caches[0].workspace
 
-    ev_dec = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(DECODES_PER_STEP)]
-    ev_app = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    R_DEC, R_APP = 32, 8
 
-    def step(i, timed):
+    def step_ops(st):
         for d in range(DECODES_PER_STEP):
-            c = caches[(i * DECODES_PER_STEP + d) % n_copies]
-            nt = d
-            tkk, tvv = (tails[nt] if nt else (None, None))
-            if timed:
-                ev_dec[d][0].record(stream)
-            K.kvq_decode_attn(c.cache, q, tkk, tvv, nt, out, ws, stream)
-            if timed:
-                ev_dec[d][1].record(stream)
-        c = caches[i % n_copies]
-        if timed:
-            ev_app[0].record(stream)
-        c.append(blk_k, blk_v, stream=stream)
-        if timed:
-            ev_app[1].record(stream)
-        K.kvq_truncate(c.cache, nb)
+            c = caches[d % n_copies]
+            tkk, tvv = (tails[d] if d else (None, None))
+            K.kvq_decode_attn(c.cache, q, tkk, tvv, d, out, ws, st)
+        caches[0].append(blk_k, blk_v, stream=st)
+        K.kvq_truncate(caches[0].cache, nb)
 
-    for i in range(args.warmup):
-        step(i, False)
-    torch.cuda.synchronize()
-    dec_ms, app_ms = [], []
-    if world > 1:
-        torch.distributed.barrier()
-    try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
-    except Exception:
-        gpu_id = str(local)
-    with Clocks(gpu_id) as clk:
-        torch.cuda.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(stream)
-        for i in range(args.steps):
-            step(args.warmup + i, True)
-            torch.cuda.synchronize()   # read the per-decode events of this step
-            dec_ms.extend(a.elapsed_time(b) for a, b in ev_dec)
-            app_ms.append(ev_app[0].elapsed_time(ev_app[1]))
-        t1.record(stream)
-        torch.cuda.synchronize()
-    total_ms = t0.elapsed_time(t1)
+    def dec_ops(st):
+        for d in range(R_DEC):
+            K.kvq_decode_attn(caches[d % n_copies].cache, q, None, None, 0, out, ws, st)
+
+    def app_ops(st):
+        for _ in range(R_APP):
+            caches[0].append(blk_k, blk_v, stream=st)
+            K.kvq_truncate(caches[0].cache, nb)
+
+    cap = torch.cuda.Stream(device=dev)
+    cap.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(cap):
+        for _ in range(args.warmup):       # eager warm-up (also settles every launch attribute)
+            step_ops(cap)
+            dec_ops(cap)
+            app_ops(cap)
+        cap.synchronize()
+        graphs = {}
+        for name, fn in (("step", step_ops), ("dec", dec_ops), ("app", app_ops)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=cap):
+                fn(cap)
+            graphs[name] = g
+        for g in graphs.values():           # warm replays
+            g.replay()
+        cap.synchronize()
+
+        def timed(g, reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(cap)
+            for _ in range(reps):
+                g.replay()
+            e1.record(cap)
+            e1.synchronize()
+            return e0.elapsed_time(e1) / reps
+
+        if world > 1:
+            torch.distributed.barrier()
+        try:
+            gpu_id = "GPU-" + str(torch.cuda.get_device_properties(local).uuid)
+        except Exception:
+            gpu_id = str(local)
+        with Clocks(gpu_id) as clk:
+            torch.cuda.synchronize()
+            step_ms = timed(graphs["step"], args.steps)
+            torch.cuda.synchronize()
+        dec0_us = 1e3 * timed(graphs["dec"], 3) / R_DEC
+        app_us = 1e3 * timed(graphs["app"], 3) / R_APP
+    total_ms = step_ms * args.steps
     status = max(int(c.status.item()) for c in caches)
     if status != 0:
         raise RuntimeError(f"device status {status} ({K.kvq_status_str(status)})")
-    step_ms = (sum(dec_ms) + sum(app_ms)) / args.steps
     if world > 1:
         tt = torch.tensor([step_ms], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         step_ms = float(tt.item())
     dec_bytes_step = cache_bytes * DECODES_PER_STEP
     value = world * dec_bytes_step / (step_ms * 1e-3) / 1e9
-    dec_avg_us = 1e3 * statistics.mean(dec_ms)
-    dec0_us = 1e3 * statistics.mean(dec_ms[d] for d in range(len(dec_ms)) if d % DECODES_PER_STEP == 0)
-    app_us = 1e3 * statistics.mean(app_ms)
+    dec_avg_us = (1e3 * step_ms - app_us) / DECODES_PER_STEP
     peak, peak_kind = _peaks()
     achieved = cache_bytes / (dec0_us * 1e-6) / 1e9   # decode call with an empty tail
     res = {
@@ -269,12 +283,16 @@ def run_kvq(args):
         "decode_us_empty_tail": round(dec0_us, 3),
         "append_us_per_block": round(app_us, 3),
         "append_tokens_per_s": round(w.batch * 128 / (app_us * 1e-6), 1),
-        "wall_ms_timed_region": round(total_ms, 3),
+        "timed_region_ms": round(total_ms, 3),
+        "timing": "CUDA graph replays, CUDA events on the launching stream",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
-                     "kernel": "decode_kernel + combine_kernel (kvq_decode_attn, empty tail)",
+                     "kernel": ("decode_mma_kernel" if (w.method in ("rtn", "varn", "int4") and w.bits in (2, 4)
+                                                        and w.group <= 4) else "decode_kernel")
+                               + " + combine_kernel (kvq_decode_attn, empty tail)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "gpu_launches": args.steps * (2 * DECODES_PER_STEP + 1),
+        "roofline_decodes": R_DEC,
         "clocks": clk.summary(),
     }
     if args.e2e:
@@ -437,13 +455,14 @@ def _decode_bytes_per_head(w):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--cpu-sample-heads", type=int, default=2)
+    ap.add_argument("--ctx", type=int, default=0, help="override the context length (tokens, multiple of 128)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     res = run_reference(args) if args.impl == "reference" else run_kvq(args)

@@ -9,7 +9,7 @@ cudaError_t kvq_launch_append(const kvq::Geo& g, const uint16_t* k, const uint16
 cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const float* codebook, const uint16_t* q,
                               const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, int n_blocks,
                               int n_split, float* ws, float* out, int* status, int hadamard, cudaStream_t st);
-size_t kvq_decode_ws_floats(const kvq::Geo& g, int n_split);
+size_t kvq_decode_ws_floats(const kvq::Geo& g, int n_blocks, int v1_splits);
 cudaError_t kvq_launch_dequant(const kvq::Geo& g, const uint8_t* base, const float* codebook, int first, int n,
                                int domain, int hadamard, float* out_k, float* out_v, cudaStream_t st);
 cudaError_t kvq_launch_rope_init(float2* tab, int max_blocks, double theta, cudaStream_t st);
@@ -187,7 +187,7 @@ kvq_status kvq_decode_workspace_bytes(const kvq_config* cfg, int32_t n_blocks, s
   if (s != KVQ_OK) return s;
   if (!out || n_blocks < 0) return KVQ_ERR_INVALID_ARG;
   const kvq::Geo g = kvq::make_geo(*cfg, l);
-  *out = kvq_decode_ws_floats(g, kvq_decode_splits(cfg, n_blocks)) * sizeof(float);
+  *out = kvq_decode_ws_floats(g, n_blocks, kvq_decode_splits(cfg, n_blocks)) * sizeof(float);
   return KVQ_OK;
 }
 
@@ -215,7 +215,7 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const void* ta
   if (n_tail > 0 && (!aligned(tail_k, 16) || !aligned(tail_v, 16))) return KVQ_ERR_ALIGNMENT;
   const kvq::Geo g = kvq::make_geo(cache->cfg, cache->lay);
   const int S = kvq_decode_splits(&cache->cfg, nb);
-  const size_t need = kvq_decode_ws_floats(g, S) * sizeof(float);
+  const size_t need = kvq_decode_ws_floats(g, nb, S) * sizeof(float);
   if (nb > 0) {
     if (!workspace) return KVQ_ERR_INVALID_ARG;
     if (workspace_bytes < need) return KVQ_ERR_CAPACITY;
@@ -241,7 +241,7 @@ kvq_status kvq_decode_attn_static(const kvq_cache* cache, const void* q, const v
   if (n_tail > 0 && (!aligned(tail_k, 16) || !aligned(tail_v, 16))) return KVQ_ERR_ALIGNMENT;
   const kvq::Geo g = kvq::make_geo(cache->cfg, cache->lay);
   const int S = kvq_decode_splits(&cache->cfg, nb);
-  const size_t need = kvq_decode_ws_floats(g, S) * sizeof(float);
+  const size_t need = kvq_decode_ws_floats(g, nb, S) * sizeof(float);
   if (need > KVQ_STATIC_WORKSPACE_BYTES) return KVQ_ERR_CAPACITY;
   kvq_status cap = KVQ_OK;
   kvq_status s = on_device(cache->device, [&]() -> cudaError_t {

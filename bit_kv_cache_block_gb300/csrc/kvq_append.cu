@@ -115,15 +115,20 @@ __device__ void rtn_tile(AppendSmem* sm, int axis, int bits, uint16_t* m16) {
   __syncthreads();
 }
 
-// Pack sm->codes rows into words: code i of a row at bits [b*(i%n)+b-1 : b*(i%n)] of word i/n.
-__device__ void pack_tile(const AppendSmem* sm, int bits, uint32_t* dst) {
+// Pack sm->codes (token-major, [t][c]) into words: code i of a row at bits
+// [b*(i%n)+b-1 : b*(i%n)] of word i/n. Key tiles: one row per token (its 128 channel codes).
+// Value tiles (transpose = true): one row per channel (its codes for the 128 tokens).
+__device__ void pack_tile(const AppendSmem* sm, int bits, bool transpose, uint32_t* dst) {
   const int n = 32 / bits, W = (D + n - 1) / n;
   for (int it = threadIdx.x; it < T * W; it += AP_THREADS) {
-    int t = it / W, w = it - t * W;
+    int r = it / W, w = it - r * W;
     uint32_t word = 0;
     for (int j = 0; j < n; ++j) {
-      int c = w * n + j;
-      if (c < D) word |= (uint32_t)(sm->codes[t * D + c] & ((1u << bits) - 1)) << (bits * j);
+      int i = w * n + j;
+      if (i < D) {
+        uint32_t code = transpose ? sm->codes[i * D + r] : sm->codes[r * D + i];
+        word |= (code & ((1u << bits) - 1)) << (bits * j);
+      }
     }
     dst[it] = word;
   }
@@ -391,14 +396,14 @@ __global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
     }
     __syncthreads();
   }
-  pack_tile(sm, g.bits, codes_dst);
+  pack_tile(sm, g.bits, kind == 1, codes_dst);
 }
 
 size_t append_smem_bytes() { return sizeof(AppendSmem); }
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t st) {
   const size_t smem = sizeof(AppendSmem);
-  cudaError_t e = cudaFuncSetAttribute(append_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem_attr((const void*)append_kernel, (size_t)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_new, a.g.H, a.g.B * 2);
   append_kernel<<<grid, AP_THREADS, smem, st>>>(a);

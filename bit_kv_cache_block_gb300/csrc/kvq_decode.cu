@@ -46,7 +46,9 @@ struct CombineArgs {
   const uint16_t* tail_v;
   int n_tail;
   int n_blocks;
-  int n_split;
+  int n_split;          // partial rows per (b, query head)
+  long long ranges;     // > 0: partials come from the range-split tensor-core decode
+  long long total;      // B * H * n_blocks
   const float* ws_m;
   const float* ws_l;
   const float* ws_o;
@@ -283,15 +285,15 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
       __syncthreads();
     }
 
-    // ---------------- V phase: thread = channel c
+    // ---------------- V phase: thread = channel c (value rows are channels)
     {
       const int c = tid;
-      const int wc = c / nw, sh = bits * (c - wc * nw);
       float bs[GMAX];
 #pragma unroll
       for (int k = 0; k < GMAX; ++k) bs[k] = 0.0f;
       for (int tt = 0; tt < T; ++tt) {
-        const uint32_t code = (vc[tt * W + wc] >> sh) & cmask;
+        const int wt = tt / nw;
+        const uint32_t code = (vc[c * W + wt] >> (bits * (tt - wt * nw))) & cmask;
         float val;
         if (METHOD == KVQ_RTN || METHOD == KVQ_VARN) {
           val = (float)code + h2f(vm[T + tt]);
@@ -354,16 +356,24 @@ __global__ void __launch_bounds__(DC_THREADS) combine_kernel(CombineArgs a) {
   const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
   const int hq = blockIdx.x, b = blockIdx.y, h = hq / g.G;
   const uint64_t row0 = ((uint64_t)b * g.Hq + hq) * a.n_split;
+  int n_part = a.n_split;
+  if (a.ranges > 0 && a.n_blocks > 0) {  // the ranges that hold blocks of this (b, h)
+    const long long u = (long long)b * g.H + h;
+    const long long r0 = ((u * a.n_blocks + 1) * a.ranges - 1) / a.total;
+    const long long r1 = (((u + 1) * a.n_blocks) * a.ranges - 1) / a.total;
+    n_part = (int)(r1 - r0 + 1);
+    if (n_part > a.n_split) n_part = a.n_split;
+  }
 
   float M = -INFINITY;
-  for (int s = 0; s < a.n_split; ++s) M = fmaxf(M, a.ws_m[row0 + s]);
+  for (int s = 0; s < n_part; ++s) M = fmaxf(M, a.ws_m[row0 + s]);
   float L = 0.0f, O = 0.0f;
-  for (int s = 0; s < a.n_split; ++s) {
+  for (int s = 0; s < n_part; ++s) {
     float f = exp2f(a.ws_m[row0 + s] - M);
     L += a.ws_l[row0 + s] * f;
     O += a.ws_o[(row0 + s) * D + c] * f;
   }
-  if (g.method == KVQ_VARN && a.hadamard && a.n_split > 0) {
+  if (g.method == KVQ_VARN && a.hadamard && n_part > 0) {
     ob[c] = O;
     __syncthreads();
     smem_fwht(ob, 1);
@@ -429,8 +439,7 @@ __global__ void __launch_bounds__(DC_THREADS) combine_kernel(CombineArgs a) {
 template <int METHOD, int GMAX>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
   size_t smem = (size_t)NSTAGE * a.g.rec_bytes + sizeof(DecSmem<GMAX>);
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<METHOD, GMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)smem);
+  cudaError_t e = ensure_smem_attr((const void*)decode_kernel<METHOD, GMAX>, (size_t)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_split, a.g.H, a.g.B);
   decode_kernel<METHOD, GMAX><<<grid, DC_THREADS, smem, st>>>(a);
@@ -449,38 +458,77 @@ cudaError_t launch_decode_m(const DecodeArgs& a, cudaStream_t st) {
 
 }  // namespace kvq
 
+long long kvq_mma_ranges(const kvq::Geo& g);
+long long kvq_mma_slots(const kvq::Geo& g, int n_blocks, long long ranges);
+cudaError_t kvq_launch_decode_mma(const kvq::Geo& g, const uint8_t* base, const uint16_t* q, int n_blocks,
+                                  long long ranges, long long slots, float* ws_m, float* ws_l, float* ws_o,
+                                  int* status, int hadamard, cudaStream_t st);
+int32_t kvq_decode_splits(const kvq_config* cfg, int32_t n_blocks);
+
+namespace {
+// Which decode runs for this geometry on the current device, and how many partial rows per
+// (b, query head) it writes.
+struct DecodePlan {
+  long long ranges;  // > 0: tensor-core decode over this many warp ranges
+  long long rows;    // partial rows per (b, query head)
+};
+
+DecodePlan plan_decode(const kvq::Geo& g, int n_blocks, int v1_splits) {
+  DecodePlan p{0, v1_splits};
+  if (n_blocks <= 0) return DecodePlan{0, 0};
+  long long ranges = kvq_mma_ranges(g);
+  const long long total = (long long)g.B * g.H * n_blocks;
+  if (ranges > total) ranges = total;  // every range holds at least one block
+  if (ranges > 0 && total < (1LL << 62) / ranges) {
+    p.ranges = ranges;
+    p.rows = kvq_mma_slots(g, n_blocks, ranges);
+  }
+  return p;
+}
+}  // namespace
+
 cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const float* codebook, const uint16_t* q,
                               const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, int n_blocks,
                               int n_split, float* ws, float* out, int* status, int hadamard, cudaStream_t st) {
   using namespace kvq;
-  const uint64_t rows = (uint64_t)g.B * g.Hq * n_split;
+  const DecodePlan plan = plan_decode(g, n_blocks, n_split);
+  const uint64_t rows = (uint64_t)g.B * g.Hq * plan.rows;
   float* ws_m = ws;
   float* ws_l = ws + rows;
   float* ws_o = ws + 2 * rows + ((4 - (2 * rows) % 4) % 4);  // keep o 16-byte aligned
   if (n_blocks > 0) {
-    DecodeArgs a;
-    a.g = g; a.base = base; a.codebook = codebook; a.q = q; a.n_blocks = n_blocks; a.n_split = n_split;
-    a.ws_m = ws_m; a.ws_l = ws_l; a.ws_o = ws_o; a.status = status; a.hadamard = hadamard;
     cudaError_t e;
-    switch (g.method) {
-      case KVQ_RTN: e = launch_decode_m<KVQ_RTN>(a, st); break;
-      case KVQ_NUQ: e = launch_decode_m<KVQ_NUQ>(a, st); break;
-      case KVQ_VARN: e = launch_decode_m<KVQ_VARN>(a, st); break;
-      default: e = launch_decode_m<KVQ_INT4>(a, st); break;
+    if (plan.ranges > 0) {
+      e = kvq_launch_decode_mma(g, base, q, n_blocks, plan.ranges, plan.rows, ws_m, ws_l, ws_o, status, hadamard,
+                                st);
+    } else {
+      DecodeArgs a;
+      a.g = g; a.base = base; a.codebook = codebook; a.q = q; a.n_blocks = n_blocks; a.n_split = n_split;
+      a.ws_m = ws_m; a.ws_l = ws_l; a.ws_o = ws_o; a.status = status; a.hadamard = hadamard;
+      switch (g.method) {
+        case KVQ_RTN: e = launch_decode_m<KVQ_RTN>(a, st); break;
+        case KVQ_NUQ: e = launch_decode_m<KVQ_NUQ>(a, st); break;
+        case KVQ_VARN: e = launch_decode_m<KVQ_VARN>(a, st); break;
+        default: e = launch_decode_m<KVQ_INT4>(a, st); break;
+      }
     }
     if (e != cudaSuccess) return e;
   }
   CombineArgs c;
   c.g = g; c.base = base; c.q = q; c.tail_k = tail_k; c.tail_v = tail_v; c.n_tail = n_tail;
-  c.n_blocks = n_blocks; c.n_split = n_blocks > 0 ? n_split : 0; c.ws_m = ws_m; c.ws_l = ws_l; c.ws_o = ws_o;
-  c.out = out; c.hadamard = hadamard;
+  c.n_blocks = n_blocks; c.n_split = (int)plan.rows; c.ranges = plan.ranges;
+  c.total = (long long)g.B * g.H * n_blocks;
+  c.ws_m = ws_m; c.ws_l = ws_l; c.ws_o = ws_o; c.out = out; c.hadamard = hadamard;
   dim3 grid(g.Hq, g.B);
   combine_kernel<<<grid, DC_THREADS, 0, st>>>(c);
   return cudaGetLastError();
 }
 
-size_t kvq_decode_ws_floats(const kvq::Geo& g, int n_split) {
-  const uint64_t rows = (uint64_t)g.B * g.Hq * n_split;
+// Workspace floats the decode of n_blocks blocks needs on the current device (v1_splits: the
+// split count of the CUDA-core decode).
+size_t kvq_decode_ws_floats(const kvq::Geo& g, int n_blocks, int v1_splits) {
+  const DecodePlan plan = plan_decode(g, n_blocks, v1_splits);
+  const uint64_t rows = (uint64_t)g.B * g.Hq * plan.rows;
   return 2 * rows + 4 + rows * kvq::D;
 }
 

@@ -1,0 +1,670 @@
+// Decode attention over the packed cache on the tensor cores (linear codes: RTN, KVarN, int4;
+// 2- and 4-bit codes; up to 4 query heads per KV head).
+//
+// Work split. The (b, h, block) sequence of the whole batch is cut into one contiguous range
+// per resident warp (persistent: one wave, equal ranges). A warp streams its blocks through
+// its own ring of shared-memory stages with 1-D bulk copies (cp.async.bulk, mbarrier
+// completion, bounded waits) and keeps a flash-decode state (running max, sum and output)
+// per query head. When its range crosses from one (b, h) to the next, it writes a partial
+// (m, l, o[128]) for the finished segment; the combine kernel merges the partials.
+//
+// Contractions. Both products run as mma.sync m16n8k16 (fp16 in, fp32 accumulate):
+//   scores   S[token][col] = K_codes[token][channel] . Bq[channel][col]
+//   outputs  O[channel][col] = V_codes[channel][token] . Bp[token][col]      (V tiles are
+//            stored one row per channel, so both A operands are adjacent codes of a row)
+// A operands are the packed codes themselves, masked in place into fp16 subnormals: a 2-bit
+// code at bits [2p, 2p+1] of a 16-bit half becomes the exact value code * 4^p * 2^-24 (p <= 4;
+// the upper positions are shifted down first), a 4-bit code code * 16^p * 2^-24; int4 codes
+// are biased by 8 with one xor. One LOP3 yields two operands, about half an instruction per
+// element. The power of two of each position is divided out of the matching B entry.
+// B columns are (query head, hi/lo): the per-channel key scales (RTN/KVarN, [KVN]
+// preliminaries (K_q + z) * s) are folded into q, and the per-token value scales into the
+// probabilities, each split into a high and a low fp16 half so the products keep about 22
+// bits; a per-block power of two keeps them in range. Zero points enter as one scalar per
+// head and block. The softmax (base 2, running max) runs on the score fragments in
+// registers ([KVQ] §3.7 fused matvec kernels; [TQ] §5.2 dequantisation inside attention).
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace mmadec {
+
+constexpr int GQ = 4;  // query heads per KV head on this path: 8 MMA columns = 4 heads x (hi, lo)
+constexpr float LOG2E_RSQRT_D = 1.4426950408889634f * 0.08838834764831845f;
+
+struct Args {
+  Geo g;
+  const uint8_t* base;
+  const uint16_t* q;
+  int nb;                 // cached blocks per (b, h)
+  long long total;        // B * H * nb
+  int n_ranges;           // warps in the grid
+  int n_slots;            // partial slots per (b, h, query head)
+  float* ws_m;
+  float* ws_l;
+  float* ws_o;
+  int* status;
+  int hadamard;
+};
+
+struct WarpSmem {
+  float q[GQ][D];         // queries of the current (b, h) (Hadamard domain for KVarN)
+  uint32_t frag[32 * 16]; // B fragments staged per lane (score product, then value product)
+  uint64_t bar[4];
+};
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Operand register `qr` of a packed word: two codes (positions qr and qr + n/2 of the word)
+// as fp16 subnormals.
+template <int BITS, bool BIAS8>
+__device__ __forceinline__ uint32_t operand(uint32_t w, int qr) {
+  if (BITS == 2) {
+    return qr <= 4 ? (w & (0x00030003u << (2 * qr))) : ((w >> 10) & (0x00030003u << (2 * (qr - 5))));
+  } else {
+    const uint32_t m = (qr & 1) ? 0x00f000f0u : 0x000f000fu;
+    uint32_t v = (qr < 2 ? w : (w >> 8)) & m;
+    if (BIAS8) v ^= (qr & 1) ? 0x00800080u : 0x00080008u;
+    return v;
+  }
+}
+
+// Where code index i (0..127) of a row sits in the B fragments: lane group tq (0..3), B
+// register (0..15: 2 per k-step) and half, and 1/(power of two of its operand position).
+template <int BITS>
+__device__ __forceinline__ void position(int i, int& tq, int& reg, int& half, float& inv_f) {
+  if (BITS == 2) {
+    const int wd = i >> 4, p = i & 15, qr = p & 7;
+    tq = wd >> 1;
+    half = p >> 3;
+    reg = 2 * ((wd & 1) * 4 + (qr >> 1)) + (qr & 1);
+    const int e = qr <= 4 ? 2 * qr : 2 * (qr - 5);
+    inv_f = __int_as_float((127 - e) << 23);
+  } else {
+    const int wd = i >> 3, p = i & 7, qr = p & 3;
+    tq = wd >> 2;
+    half = p >> 2;
+    reg = 2 * ((wd & 3) * 2 + (qr >> 1)) + (qr & 1);
+    inv_f = (qr & 1) ? 0.0625f : 1.0f;
+  }
+}
+
+__device__ __forceinline__ void put_half(uint32_t* frag, int lane_dst, int reg, int half, __half v) {
+  reinterpret_cast<__half*>(frag + lane_dst * 16 + reg)[half] = v;
+}
+
+// hi/lo fp16 split of x: hi = fp16(x), lo = fp16(x - hi).
+__device__ __forceinline__ void split_hl(float x, __half& hi, __half& lo) {
+  hi = __float2half_rn(x);
+  lo = __float2half_rn(x - __half2float(hi));
+}
+
+// 2^e for the exponent that keeps max|v| * 2^e below 2^14 (0 for an all-zero block).
+__device__ __forceinline__ int range_exp(float mx) {
+  if (!(mx > 0.0f)) return 0;
+  int e;
+  frexpf(mx, &e);  // mx = m * 2^e, m in [0.5, 1)
+  int s = 14 - e;
+  return s > 100 ? 100 : (s < -100 ? -100 : s);
+}
+
+__device__ __forceinline__ float exp2i(int e) { return ldexpf(1.0f, e); }
+
+__device__ __forceinline__ float warp_max_tq(float v) {  // over lanes with the same lane & 3
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+}
+__device__ __forceinline__ float warp_sum_tq(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  return v + __shfl_xor_sync(0xffffffffu, v, 16);
+}
+__device__ __forceinline__ float warp_max_all(float v) {
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum_all(float v) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Range containing block x of the flattened (b, h, block) sequence: range r holds
+// [floor(r*total/N), floor((r+1)*total/N)).
+__host__ __device__ inline long long range_of(long long x, long long total, long long N) {
+  return ((x + 1) * N - 1) / total;
+}
+
+// acc[mt] += (rows 16mt+gq and 16mt+gq+8 of a 128-row code tile) . B, for the 8 m-tiles of the
+// tile; the k-step loop is outermost so that consecutive MMAs use independent accumulators.
+template <int BITS, bool BIAS8>
+__device__ __forceinline__ void tile_mma(float (&acc)[8][4], const uint32_t* codes, int gq, int tq,
+                                         const uint32_t (&b)[16]) {
+  if (BITS == 2) {
+    uint2 w0[8], w1[8];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+      w0[mt] = *reinterpret_cast<const uint2*>(codes + (16 * mt + gq) * 8 + 2 * tq);
+      w1[mt] = *reinterpret_cast<const uint2*>(codes + (16 * mt + gq + 8) * 8 + 2 * tq);
+    }
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int qr = 2 * (ks & 3);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const uint32_t x0 = ks < 4 ? w0[mt].x : w0[mt].y, x1 = ks < 4 ? w1[mt].x : w1[mt].y;
+        mma16816(acc[mt], operand<2, BIAS8>(x0, qr), operand<2, BIAS8>(x1, qr), operand<2, BIAS8>(x0, qr + 1),
+                 operand<2, BIAS8>(x1, qr + 1), b[2 * ks], b[2 * ks + 1]);
+      }
+    }
+  } else {
+#pragma unroll
+    for (int hm = 0; hm < 2; ++hm) {  // 4 m-tiles at a time
+      uint4 w0[4], w1[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int mt = 4 * hm + m;
+        w0[m] = *reinterpret_cast<const uint4*>(codes + (16 * mt + gq) * 16 + 4 * tq);
+        w1[m] = *reinterpret_cast<const uint4*>(codes + (16 * mt + gq + 8) * 16 + 4 * tq);
+      }
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int qr = 2 * (ks & 1);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const uint32_t* p0 = &w0[m].x;
+          const uint32_t* p1 = &w1[m].x;
+          const uint32_t x0 = p0[ks >> 1], x1 = p1[ks >> 1];
+          mma16816(acc[4 * hm + m], operand<4, BIAS8>(x0, qr), operand<4, BIAS8>(x1, qr),
+                   operand<4, BIAS8>(x0, qr + 1), operand<4, BIAS8>(x1, qr + 1), b[2 * ks], b[2 * ks + 1]);
+        }
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void put_col(uint32_t* frag, int col, int off, __half v) {
+  reinterpret_cast<__half*>(frag)[col * 128 + off] = v;
+}
+
+// Half offset inside one staged B column of the code at row position x = 16*mt + gq + 8*hlf
+// (the positions a lane owns), and the power of two that lane's operands carry (both follow from
+// operand() and the fragment layout).
+template <int BITS>
+__device__ __forceinline__ int col_off(int mt, int gq, int hlf) {
+  return BITS == 2 ? 16 * mt + 2 * gq + hlf : 16 * mt + 8 * hlf + 2 * (gq & 3) + (gq >> 2);
+}
+template <int BITS>
+__device__ __forceinline__ float lane_inv_f(int gq) {
+  if (BITS == 2) {
+    const int e = gq <= 4 ? 2 * gq : 2 * (gq - 5);
+    return __int_as_float((127 - e) << 23);
+  }
+  return (gq & 1) ? 0.0625f : 1.0f;
+}
+
+// Reductions over the lanes that hold the same query head (8 row groups x the replicas).
+template <int GT>
+__device__ __forceinline__ float head_max(float v) {
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+  v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+  if (GT <= 2) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 2));
+  if (GT == 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 1));
+  return v;
+}
+template <int GT>
+__device__ __forceinline__ float head_sum(float v) {
+  v += __shfl_xor_sync(0xffffffffu, v, 4);
+  v += __shfl_xor_sync(0xffffffffu, v, 8);
+  v += __shfl_xor_sync(0xffffffffu, v, 16);
+  if (GT <= 2) v += __shfl_xor_sync(0xffffffffu, v, 2);
+  if (GT == 1) v += __shfl_xor_sync(0xffffffffu, v, 1);
+  return v;
+}
+
+// Stages the hi/lo halves of v (one value per position the lane owns) into columns 2h, 2h+1.
+template <int BITS, int NMT>
+__device__ __forceinline__ void stage_cols(uint32_t* frag, int h, int gq, int rho, int RP, const float (&v)[2 * NMT]) {
+  __half* col_hi = reinterpret_cast<__half*>(frag) + (2 * h) * 128;
+  __half* col_lo = col_hi + 128;
+#pragma unroll
+  for (int j = 0; j < NMT; ++j) {
+    const int mt = rho + RP * j;
+    __half h0, l0, h1, l1;
+    split_hl(v[2 * j], h0, l0);
+    split_hl(v[2 * j + 1], h1, l1);
+    if (BITS == 2) {  // the two positions of an m-tile are adjacent halves
+      const int o = col_off<2>(mt, gq, 0);
+      *reinterpret_cast<__half2*>(col_hi + o) = __halves2half2(h0, h1);
+      *reinterpret_cast<__half2*>(col_lo + o) = __halves2half2(l0, l1);
+    } else {
+      const int o0 = col_off<4>(mt, gq, 0), o1 = col_off<4>(mt, gq, 1);
+      col_hi[o0] = h0; col_lo[o0] = l0;
+      col_hi[o1] = h1; col_lo[o1] = l1;
+    }
+  }
+}
+
+// The lane's j-th own m-tile (mt = rho + RP*j) of an accumulator array, with static indices.
+template <int RP>
+__device__ __forceinline__ void pick_tile(const float (&acc)[8][4], int j, int rho, float (&c)[4]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    float v = acc[RP * j][k];
+#pragma unroll
+    for (int r = 1; r < RP; ++r) v = (rho == r) ? acc[r + RP * j][k] : v;
+    c[k] = v;
+  }
+}
+
+// Loads the lane's 16 B registers: lane (g', t') reads staged column g' mod 2G.
+__device__ __forceinline__ void load_frag(const uint32_t* frag, int lane, int G, uint32_t (&b)[16]) {
+  const int col = (lane >> 2) % (2 * G);
+  const uint4* src = reinterpret_cast<const uint4*>(frag + (col * 4 + (lane & 3)) * 16);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint4 v = src[k];
+    b[4 * k] = v.x; b[4 * k + 1] = v.y; b[4 * k + 2] = v.z; b[4 * k + 3] = v.w;
+  }
+}
+
+// GT: query heads per KV head this instantiation serves (1, 2 or 4; G = 3 runs on GT = 4). Each
+// head's B columns are replicated over the 4 column pairs (RP = 4/GT copies), so every lane holds
+// real scores and finishes 16/RP of the block's tokens.
+template <int METHOD, int BITS, int GT, int NW, int NS>
+__global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
+  constexpr bool BIAS8 = METHOD == KVQ_INT4;
+  constexpr int RP = 4 / GT;
+  constexpr int NMT = 8 / RP;  // m-tiles (16 rows) a lane finishes
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const Geo& g = a.g;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int G = g.G;
+  const int hl = tq % GT, rho = tq / GT;  // the lane's head and replica
+  const bool head_ok = hl < G;
+  const float inv_f = lane_inv_f<BITS>(gq);
+  const int rec = (int)g.rec_bytes;
+  uint8_t* stages = smem_raw + (size_t)warp * NS * rec;
+  WarpSmem* sw = reinterpret_cast<WarpSmem*>(smem_raw + (size_t)NW * NS * rec) + warp;
+
+  const long long R = (long long)blockIdx.x * NW + warp;
+  if (R >= a.n_ranges) return;  // the last CTA may carry warps beyond the range count
+  const long long x0 = R * a.total / a.n_ranges, x1 = (R + 1) * a.total / a.n_ranges;
+  const int n = (int)(x1 - x0);
+  if (n <= 0) return;
+
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&sw->bar[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  // (unit, block) of the block being processed and of the next one to prefetch
+  long long u = x0 / a.nb;
+  int blk = (int)(x0 - u * a.nb);
+  long long pu = u;
+  int pblk = blk;
+  auto rec_ptr = [&](long long uu, int bb) -> const uint8_t* {
+    return a.base + ((uint64_t)uu * g.max_blocks + (uint64_t)bb) * g.rec_bytes;
+  };
+  if (lane == 0) {
+    fence_proxy_async();
+    for (int s = 0; s < NS && s < n; ++s) {
+      mbar_arrive_expect_tx(&sw->bar[s], (uint32_t)rec);
+      bulk_g2s(stages + s * rec, rec_ptr(pu, pblk), (uint32_t)rec, &sw->bar[s]);
+      if (++pblk == a.nb) { pblk = 0; ++pu; }
+    }
+  }
+
+  float m_run = -INFINITY, l_run = 0.0f, zv = 0.0f;
+  float O[8][4];
+  int g1_cur = 0;
+  uint32_t bk[16], bv[16];
+  float zk = 0.0f, sumq = 0.0f;
+  int g0_fixed = 0;
+  long long cur_u = -1;
+  bool ok = true;
+  int failed_at = n;
+
+  auto flush = [&](long long uu) {
+    const long long b = uu / g.H, h = uu - b * g.H;
+    const long long slot = R - range_of(uu * a.nb, a.total, a.n_ranges);
+    if (rho == 0 && head_ok && slot >= 0 && slot < a.n_slots) {
+      const uint64_t row = ((uint64_t)(b * g.Hq + h * G + hl)) * a.n_slots + slot;
+      const float sc = (METHOD == KVQ_VARN) ? 1.0f : exp2i(24 - g1_cur);
+      const float add = (METHOD == KVQ_VARN) ? 0.0f : zv;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        a.ws_o[row * D + 16 * mt + gq] = (O[mt][0] + O[mt][1]) * sc + add;
+        a.ws_o[row * D + 16 * mt + gq + 8] = (O[mt][2] + O[mt][3]) * sc + add;
+      }
+      if (gq == 0) {
+        a.ws_m[row] = m_run;
+        a.ws_l[row] = l_run;
+      }
+    }
+  };
+
+  for (int i = 0; i < n; ++i) {
+    const int s_idx = i % NS;
+    if (u != cur_u) {
+      if (cur_u >= 0) flush(cur_u);
+      cur_u = u;
+      const long long b = u / g.H, h = u - b * g.H;
+      __syncwarp();
+      for (int e = lane; e < GQ * D; e += 32) {
+        const int hh = e >> 7, c = e & 127;
+        sw->q[hh][c] = hh < G ? load_in(a.q + ((uint64_t)(b * g.Hq + h * G + hh)) * D + c, g.in_bf16) : 0.0f;
+      }
+      __syncwarp();
+      if (METHOD == KVQ_VARN && a.hadamard) {  // q in the Hadamard domain
+        for (int hh = 0; hh < G; ++hh) {
+          float* v = sw->q[hh];
+          for (int st = 1; st < D; st <<= 1) {
+            for (int j = lane; j < D / 2; j += 32) {
+              const int i0 = (j / st) * (2 * st) + (j % st);
+              const float p0 = v[i0], p1 = v[i0 + st];
+              v[i0] = p0 + p1;
+              v[i0 + st] = p0 - p1;
+            }
+            __syncwarp();
+          }
+          for (int c = lane; c < D; c += 32) v[c] *= 0.08838834764831845f;
+          __syncwarp();
+        }
+      }
+      m_run = -INFINITY;
+      l_run = 0.0f;
+      zv = 0.0f;
+      g1_cur = 0;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.0f;
+      if (METHOD == KVQ_INT4) {  // int4 keys carry no per-channel scale: B is fixed per (b, h)
+        float mx = 0.0f, sq = 0.0f;
+        float v[2 * NMT];
+#pragma unroll
+        for (int j = 0; j < NMT; ++j)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const float qv = head_ok ? sw->q[hl][16 * (rho + RP * j) + gq + 8 * hf] : 0.0f;
+            v[2 * j + hf] = qv;
+            sq += qv;
+            mx = fmaxf(mx, fabsf(qv));
+          }
+        mx = warp_max_all(mx);
+        sumq = head_sum<GT>(sq);
+        g0_fixed = range_exp(mx);
+        const float sc = exp2i(g0_fixed) * inv_f;
+#pragma unroll
+        for (int k = 0; k < 2 * NMT; ++k) v[k] *= sc;
+        if (head_ok) stage_cols<BITS, NMT>(sw->frag, hl, gq, rho, RP, v);
+        __syncwarp();
+        load_frag(sw->frag, lane, G, bk);
+      }
+    }
+
+    // ---- wait for this block's record (bounded; all lanes leave together on failure)
+    const bool got = mbar_wait_bounded(&sw->bar[s_idx], (uint32_t)((i / NS) & 1), a.status);
+    if (__any_sync(0xffffffffu, !got)) {
+      ok = false;
+      failed_at = i;
+      break;
+    }
+    const uint8_t* st = stages + s_idx * rec;
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + g.codes_off[0]);
+    const uint16_t* km = reinterpret_cast<const uint16_t*>(st + g.meta_off[0]);
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + g.codes_off[1]);
+    const uint16_t* vm = reinterpret_cast<const uint16_t*>(st + g.meta_off[1]);
+
+    // ---- B fragments of the score product: q * s_channel (RTN, KVarN)
+    int g0 = g0_fixed;
+    if (METHOD != KVQ_INT4) {
+      float v[2 * NMT];
+      float mx = 0.0f, zp = 0.0f;
+#pragma unroll
+      for (int j = 0; j < NMT; ++j)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int c = 16 * (rho + RP * j) + gq + 8 * hf;
+          const float qs = head_ok ? sw->q[hl][c] * h2f(km[c]) : 0.0f;
+          v[2 * j + hf] = qs;
+          mx = fmaxf(mx, fabsf(qs));
+          zp = fmaf(qs, h2f(km[T + c]), zp);
+        }
+      mx = warp_max_all(mx);
+      zk = head_sum<GT>(zp);
+      g0 = range_exp(mx);
+      const float sc = exp2i(g0) * inv_f;
+#pragma unroll
+      for (int k = 0; k < 2 * NMT; ++k) v[k] *= sc;
+      __syncwarp();  // the staging buffer is free (last block's value fragments are loaded)
+      if (head_ok) stage_cols<BITS, NMT>(sw->frag, hl, gq, rho, RP, v);
+      __syncwarp();
+      load_frag(sw->frag, lane, G, bk);
+    }
+
+    // ---- scores: S = K . Bq  (8 m-tiles of 16 tokens x 8 k-steps of 16 channels)
+    float sc8[8][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) sc8[mt][0] = sc8[mt][1] = sc8[mt][2] = sc8[mt][3] = 0.0f;
+    tile_mma<BITS, BIAS8>(sc8, kc, gq, tq, bk);
+
+    // ---- finish the scores of the lane's tokens, online softmax (base 2)
+    const float ksc = exp2i(24 - g0);
+    float sv[2 * NMT];
+    float mloc = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < NMT; ++j) {
+      const int mt = rho + RP * j;
+      float c4[4];
+      pick_tile<RP>(sc8, j, rho, c4);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int tok = 16 * mt + gq + 8 * hf;
+        float v = (c4[2 * hf] + c4[2 * hf + 1]) * ksc;
+        if (METHOD == KVQ_INT4) v = (v - 8.0f * sumq) * h2f(km[tok]);
+        else v += zk;
+        if (METHOD == KVQ_VARN) v *= h2f(km[2 * T + tok]);
+        v *= LOG2E_RSQRT_D;
+        sv[2 * j + hf] = v;
+        mloc = fmaxf(mloc, v);
+      }
+    }
+    mloc = head_max<GT>(mloc);
+    const float m_new = fmaxf(m_run, mloc);
+    const float alpha = exp2f(m_run - m_new);
+    float lsum = 0.0f, zsum_blk = 0.0f, pmax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NMT; ++j) {
+      const int mt = rho + RP * j;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int tok = 16 * mt + gq + 8 * hf;
+        const float p = exp2f(sv[2 * j + hf] - m_new);
+        lsum += p;
+        const float pp = p * h2f(vm[tok]);  // per-token value scale folded into p
+        sv[2 * j + hf] = pp;
+        if (METHOD == KVQ_INT4) zsum_blk -= 8.0f * pp;
+        else zsum_blk = fmaf(pp, h2f(vm[T + tok]), zsum_blk);
+        pmax = fmaxf(pmax, pp);
+      }
+    }
+    lsum = head_sum<GT>(lsum);
+    zsum_blk = head_sum<GT>(zsum_blk);
+    l_run = l_run * alpha + lsum;
+    m_run = m_new;
+    const int g1 = range_exp(warp_max_all(head_ok ? pmax : 0.0f));
+
+    // ---- B fragments of the value product: p' (hi, lo) per head
+    {
+      const float sc = exp2i(g1) * inv_f;
+#pragma unroll
+      for (int k = 0; k < 2 * NMT; ++k) sv[k] *= sc;
+      __syncwarp();  // every lane has loaded its score fragments
+      if (head_ok) stage_cols<BITS, NMT>(sw->frag, hl, gq, rho, RP, sv);
+      __syncwarp();
+      load_frag(sw->frag, lane, G, bv);
+    }
+
+    // ---- outputs: O = V . Bp  (8 m-tiles of 16 channels x 8 k-steps of 16 tokens)
+    if (METHOD != KVQ_VARN) {
+      const float rs = alpha * exp2i(g1 - g1_cur);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        O[mt][0] *= rs; O[mt][1] *= rs; O[mt][2] *= rs; O[mt][3] *= rs;
+      }
+      zv = zv * alpha + zsum_blk;
+      g1_cur = g1;
+      tile_mma<BITS, BIAS8>(O, vc, gq, tq, bv);
+    } else {  // second scale s1 per channel: o_c += s1_c * (P.V_c + sum p' z)
+      float acc[8][4];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+      tile_mma<BITS, BIAS8>(acc, vc, gq, tq, bv);
+      const float usc = exp2i(24 - g1);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int r0 = 16 * mt + gq, r1 = r0 + 8;
+        const float s1a = h2f(vm[2 * T + r0]), s1b = h2f(vm[2 * T + r1]);
+        O[mt][0] = O[mt][0] * alpha + (acc[mt][0] * usc + zsum_blk) * s1a;
+        O[mt][1] = O[mt][1] * alpha + acc[mt][1] * usc * s1a;
+        O[mt][2] = O[mt][2] * alpha + (acc[mt][2] * usc + zsum_blk) * s1b;
+        O[mt][3] = O[mt][3] * alpha + acc[mt][3] * usc * s1b;
+      }
+    }
+
+    __syncwarp();  // every lane is done with this stage
+    if (lane == 0 && i + NS < n) {
+      fence_proxy_async();
+      mbar_arrive_expect_tx(&sw->bar[s_idx], (uint32_t)rec);
+      bulk_g2s(stages + s_idx * rec, rec_ptr(pu, pblk), (uint32_t)rec, &sw->bar[s_idx]);
+    }
+    if (++pblk == a.nb) { pblk = 0; ++pu; }
+    if (++blk == a.nb) { blk = 0; ++u; }
+  }
+
+  if (!ok) {
+    if (lane == 0) {
+      for (int j = failed_at; j < n && j < failed_at + NS; ++j)
+        mbar_wait_bounded(&sw->bar[j % NS], (uint32_t)((j / NS) & 1), nullptr, 200000000LL);
+    }
+    __syncwarp();
+    return;
+  }
+  if (cur_u >= 0) flush(cur_u);
+}
+
+struct Plan {
+  void (*fn)(Args);
+  int nw, ns;
+};
+
+template <int METHOD, int BITS, int GT>
+Plan plan_for() {
+  constexpr int NW = 4, NS = 2;
+  return Plan{decode_mma_kernel<METHOD, BITS, GT, NW, NS>, NW, NS};
+}
+
+template <int METHOD, int BITS>
+Plan plan_g(int G) {
+  if (G == 1) return plan_for<METHOD, BITS, 1>();
+  if (G == 2) return plan_for<METHOD, BITS, 2>();
+  return plan_for<METHOD, BITS, 4>();
+}
+
+bool supported(const Geo& g) {
+  if (g.G > GQ) return false;
+  if (g.bits != 2 && g.bits != 4) return false;
+  return g.method == KVQ_RTN || g.method == KVQ_VARN || g.method == KVQ_INT4;
+}
+
+Plan get_plan(const Geo& g) {
+  if (g.method == KVQ_RTN) return g.bits == 2 ? plan_g<KVQ_RTN, 2>(g.G) : plan_g<KVQ_RTN, 4>(g.G);
+  if (g.method == KVQ_VARN) return g.bits == 2 ? plan_g<KVQ_VARN, 2>(g.G) : plan_g<KVQ_VARN, 4>(g.G);
+  return plan_g<KVQ_INT4, 4>(g.G);
+}
+
+size_t smem_bytes(const Geo& g, const Plan& p) {
+  return (size_t)p.nw * p.ns * g.rec_bytes + (size_t)p.nw * sizeof(WarpSmem);
+}
+
+}  // namespace mmadec
+}  // namespace kvq
+
+// ------------------------------------------------------------------ host entry points
+
+namespace {
+struct OccCache {
+  int dev = -1;
+  void* fn = nullptr;
+  size_t smem = 0;
+  int ctas = 0;
+};
+thread_local OccCache t_occ[8];
+}  // namespace
+
+// Ranges (warps) the tensor-core decode uses on the current device for this geometry, or 0 if
+// the path does not apply. Without a usable device it assumes a 152-SM part with one CTA per SM.
+long long kvq_mma_ranges(const kvq::Geo& g) {
+  using namespace kvq::mmadec;
+  if (!supported(g)) return 0;
+  const Plan p = get_plan(g);
+  const size_t smem = smem_bytes(g, p);
+  if (smem > 227 * 1024) return 0;
+  int dev = 0, sms = 152, ctas = 1;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
+    OccCache* hit = nullptr;
+    for (auto& c : t_occ)
+      if (c.dev == dev && c.fn == (void*)p.fn && c.smem == smem) hit = &c;
+    if (!hit) {
+      cudaFuncSetAttribute(p.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      int occ = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p.fn, p.nw * 32, smem) != cudaSuccess || occ < 1)
+        occ = 1;
+      for (auto& c : t_occ)
+        if (c.fn == nullptr || &c == &t_occ[7]) {
+          c.dev = dev; c.fn = (void*)p.fn; c.smem = smem; c.ctas = occ;
+          hit = &c;
+          break;
+        }
+    }
+    ctas = hit->ctas;
+  } else {
+    cudaGetLastError();
+    sms = 152;
+  }
+  return (long long)sms * ctas * p.nw;
+}
+
+// Partial slots per (b, query head) for n_blocks blocks split into `ranges` ranges.
+long long kvq_mma_slots(const kvq::Geo& g, int n_blocks, long long ranges) {
+  const long long total = (long long)g.B * g.H * n_blocks;
+  if (total <= 0 || ranges <= 0) return 0;
+  long long p = (long long)(n_blocks - 1) * ranges / total + 2;
+  return p < n_blocks ? p : n_blocks;
+}
+
+cudaError_t kvq_launch_decode_mma(const kvq::Geo& g, const uint8_t* base, const uint16_t* q, int n_blocks,
+                                  long long ranges, long long slots, float* ws_m, float* ws_l, float* ws_o,
+                                  int* status, int hadamard, cudaStream_t st) {
+  using namespace kvq::mmadec;
+  const Plan p = get_plan(g);
+  const size_t smem = smem_bytes(g, p);
+  cudaError_t e = kvq::ensure_smem_attr((const void*)p.fn, (size_t)smem);
+  if (e != cudaSuccess) return e;
+  Args a;
+  a.g = g; a.base = base; a.q = q; a.nb = n_blocks; a.total = (long long)g.B * g.H * n_blocks;
+  a.n_ranges = (int)ranges; a.n_slots = (int)slots; a.ws_m = ws_m; a.ws_l = ws_l; a.ws_o = ws_o;
+  a.status = status; a.hadamard = hadamard;
+  const int grid = (int)((ranges + p.nw - 1) / p.nw);
+  p.fn<<<grid, p.nw * 32, smem, st>>>(a);
+  return cudaGetLastError();
+}

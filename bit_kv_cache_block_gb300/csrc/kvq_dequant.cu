@@ -33,7 +33,9 @@ __global__ void __launch_bounds__(DQ_THREADS) dequant_kernel(DequantArgs a) {
   const uint32_t cmask = (1u << bits) - 1u;
   float* row = xs + t * 129;
   for (int c = 0; c < D; ++c) {
-    const uint32_t q = (codes[t * W + c / nw] >> (bits * (c % nw))) & cmask;
+    // key rows are tokens, value rows are channels
+    const uint32_t q = kind == 0 ? (codes[t * W + c / nw] >> (bits * (c % nw))) & cmask
+                                 : (codes[c * W + t / nw] >> (bits * (t % nw))) & cmask;
     float v;
     if (g.method == KVQ_RTN || g.method == KVQ_VARN) {
       const int gi = kind == 0 ? c : t;
@@ -93,7 +95,7 @@ cudaError_t kvq_launch_dequant(const kvq::Geo& g, const uint8_t* base, const flo
   a.g = g; a.base = base; a.codebook = codebook; a.first = first; a.n = n; a.domain = domain;
   a.hadamard = hadamard; a.out_k = out_k; a.out_v = out_v;
   const int smem = kvq::T * 129 * (int)sizeof(float);
-  cudaError_t e = cudaFuncSetAttribute(kvq::dequant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaError_t e = kvq::ensure_smem_attr((const void*)kvq::dequant_kernel, (size_t)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(n, g.H, g.B * 2);
   kvq::dequant_kernel<<<grid, kvq::DQ_THREADS, smem, st>>>(a);

@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/kvq.h"
 
 namespace kvq {
@@ -69,6 +71,24 @@ inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
 
 __host__ __device__ inline uint64_t record_index(const Geo& g, int b, int h, int blk) {
   return ((uint64_t)b * g.H + h) * g.max_blocks + blk;
+}
+
+// Raises a kernel's dynamic shared-memory limit on the current device once (the setting is
+// cached per device and kernel), so repeated launches make no extra runtime calls.
+inline cudaError_t ensure_smem_attr(const void* fn, size_t smem) {
+  static std::mutex mu;
+  struct Entry { int dev; const void* fn; size_t smem; };
+  static Entry tab[128];
+  static int n = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (tab[i].dev == dev && tab[i].fn == fn && tab[i].smem >= smem) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e == cudaSuccess && n < 128) tab[n++] = Entry{dev, fn, smem};
+  return e;
 }
 
 // ----------------------------------------------------------------- device helpers

@@ -94,9 +94,10 @@ typedef struct {
 /* Byte layout of a cache, from kvq_layout. One record per (b, h, block), at
  *   base + ((b * n_kv_heads + h) * max_blocks + block) * record_bytes,
  * holding the K tile then the V tile; every region starts 16-byte aligned:
- *   codes : 128 rows (tokens) x words_per_row uint32; code i of a row at bits
+ *   codes : 128 rows x words_per_row uint32; code i of a row at bits
  *           [b*(i%n)+b-1 : b*(i%n)] of word i/n, n = floor(32/b), unused high bits zero
- *           ([KVQ] §9.3 3-bit layout, generalised)
+ *           ([KVQ] §9.3 3-bit layout, generalised). K tile: one row per token (its 128
+ *           channel codes). V tile: one row per channel (its codes for the 128 tokens).
  *   meta  : fp16 vectors of 128. RTN and VARN: s, z (keys: per channel; values: per token),
  *           VARN adds s1 (keys: per token; values: per channel). NUQ: s (half-range),
  *           zp (centre). INT4: s (per token).

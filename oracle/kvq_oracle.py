@@ -444,8 +444,9 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
 class OracleCache:
     """A packed cache kept as per-tile records plus the decode that reads it.
 
-    One record per (batch b, KV head h, block, kind): the packed code words, the fp16
-    metadata and, for nuq, the CSR outliers. decode() unpacks and dequantises every
+    One record per (batch b, KV head h, block, kind): the packed code words (key tiles one
+    row per token, value tiles one row per channel), the fp16 metadata and, for nuq, the CSR
+    outliers. decode() unpacks and dequantises every
     record in fp64 (RoPE at absolute positions for pre-RoPE keys; the Hadamard domain
     for KVarN, with the query transformed the same way and the output transformed back),
     appends the fp residual tail and evaluates softmax attention. Query head j reads KV
@@ -486,7 +487,9 @@ class OracleCache:
             rec = nuq_quantize(x, self.codebook[h], 0 if kind == KIND_K else 1, self.n_out)
         else:
             rec = varn_quantize(x, b, kind, self.varn_iters, self.use_hadamard)
-        rec["words"] = pack_rows(rec["codes"], b)
+        # keys: one row per token (its 128 channel codes); values: one row per channel (its
+        # codes for the 128 tokens of the block)
+        rec["words"] = pack_rows(rec["codes"] if kind == KIND_K else rec["codes"].T, b)
         return rec
 
     def append(self, K: np.ndarray, V: np.ndarray, only_heads=None):
@@ -509,6 +512,8 @@ class OracleCache:
         in the Hadamard domain); 'input': back in the input domain (inverse Hadamard for
         KVarN); 'attn': what attention reads (RoPE applied to pre-RoPE keys)."""
         codes = unpack_rows(rec["words"], self.bits)
+        if kind == KIND_V:
+            codes = codes.T
         m = self.method
         if m == "rtn":
             x = rtn_dequant(codes, rec["s16"], rec["z16"], 0 if kind == KIND_K else 1)
