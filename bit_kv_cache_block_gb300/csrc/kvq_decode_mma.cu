@@ -278,7 +278,9 @@ __device__ __forceinline__ void load_frag(const uint32_t* frag, int lane, int G,
 // GT: query heads per KV head this instantiation serves (1, 2 or 4; G = 3 runs on GT = 4). Each
 // head's B columns are replicated over the 4 column pairs (RP = 4/GT copies), so every lane holds
 // real scores and finishes 16/RP of the block's tokens.
-template <int METHOD, int BITS, int GT, int NW, int NS>
+// NW warps per CTA; NB shared-memory buffers per warp, each holding one half-record (the K tile
+// or the V tile of a block, with its metadata): the ring streams K(0), V(0), K(1), V(1), ...
+template <int METHOD, int BITS, int GT, int NW, int NB, bool WHOLE>
 __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
   constexpr bool BIAS8 = METHOD == KVQ_INT4;
   constexpr int RP = 4 / GT;
@@ -291,9 +293,11 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
   const int hl = tq % GT, rho = tq / GT;  // the lane's head and replica
   const bool head_ok = hl < G;
   const float inv_f = lane_inv_f<BITS>(gq);
-  const int rec = (int)g.rec_bytes;
-  uint8_t* stages = smem_raw + (size_t)warp * NS * rec;
-  WarpSmem* sw = reinterpret_cast<WarpSmem*>(smem_raw + (size_t)NW * NS * rec) + warp;
+  const int halfk = (int)g.codes_off[1];               // K half: K codes, K meta (, K csr)
+  const int halfv = (int)g.rec_bytes - halfk;          // V half
+  const int hb = WHOLE ? (int)g.rec_bytes : (halfk > halfv ? halfk : halfv);  // bytes per buffer
+  uint8_t* ring = smem_raw + (size_t)warp * NB * hb;
+  WarpSmem* sw = reinterpret_cast<WarpSmem*>(smem_raw + (size_t)NW * NB * hb) + warp;
 
   const long long R = (long long)blockIdx.x * NW + warp;
   if (R >= a.n_ranges) return;  // the last CTA may carry warps beyond the range count
@@ -302,25 +306,45 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
   if (n <= 0) return;
 
   if (lane == 0) {
-    for (int s = 0; s < NS; ++s) mbar_init(&sw->bar[s], 1);
+    for (int s = 0; s < NB; ++s) mbar_init(&sw->bar[s], 1);
     fence_mbar_init();
   }
   __syncwarp();
-  // (unit, block) of the block being processed and of the next one to prefetch
+  // (unit, block) being processed; lane 0 also tracks the next half-record to prefetch
   long long u = x0 / a.nb;
   int blk = (int)(x0 - u * a.nb);
-  long long pu = u;
-  int pblk = blk;
-  auto rec_ptr = [&](long long uu, int bb) -> const uint8_t* {
-    return a.base + ((uint64_t)uu * g.max_blocks + (uint64_t)bb) * g.rec_bytes;
+  const int n_units = WHOLE ? n : 2 * n;  // copies: whole records, or K and V halves
+  int pnext = 0, pbuf = 0, pblk = blk;  // next copy to issue, its buffer, its block
+  const uint8_t* psrc = a.base + ((uint64_t)u * g.max_blocks + (uint64_t)blk) * g.rec_bytes;
+  auto issue_next = [&]() {  // lane 0 only
+    if (pnext >= n_units) return;
+    const bool is_v = !WHOLE && (pnext & 1);
+    const uint32_t bytes = (uint32_t)(WHOLE ? (int)g.rec_bytes : (is_v ? halfv : halfk));
+    mbar_arrive_expect_tx(&sw->bar[pbuf], bytes);
+    bulk_g2s(ring + (size_t)pbuf * hb, psrc + (is_v ? halfk : 0), bytes, &sw->bar[pbuf]);
+    ++pnext;
+    if (++pbuf == NB) pbuf = 0;
+    if (WHOLE || is_v) {  // next block: the next record, or the first record of the next (b, h)
+      if (++pblk == a.nb) {
+        pblk = 0;
+        psrc += (uint64_t)(g.max_blocks - a.nb + 1) * g.rec_bytes;
+      } else {
+        psrc += g.rec_bytes;
+      }
+    }
+  };
+  int cbuf = 0;          // buffer of the next half-record to consume
+  uint32_t parity = 0;   // bit b: phase parity of buffer b's next completion
+  auto wait_next = [&](const uint8_t*& buf) -> bool {
+    const bool got = mbar_wait_bounded(&sw->bar[cbuf], (parity >> cbuf) & 1u, a.status);
+    buf = ring + (size_t)cbuf * hb;
+    parity ^= 1u << cbuf;
+    if (++cbuf == NB) cbuf = 0;
+    return got;
   };
   if (lane == 0) {
     fence_proxy_async();
-    for (int s = 0; s < NS && s < n; ++s) {
-      mbar_arrive_expect_tx(&sw->bar[s], (uint32_t)rec);
-      bulk_g2s(stages + s * rec, rec_ptr(pu, pblk), (uint32_t)rec, &sw->bar[s]);
-      if (++pblk == a.nb) { pblk = 0; ++pu; }
-    }
+    for (int s = 0; s < NB; ++s) issue_next();
   }
 
   float m_run = -INFINITY, l_run = 0.0f, zv = 0.0f;
@@ -353,7 +377,6 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
   };
 
   for (int i = 0; i < n; ++i) {
-    const int s_idx = i % NS;
     if (u != cur_u) {
       if (cur_u >= 0) flush(cur_u);
       cur_u = u;
@@ -410,18 +433,15 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
       }
     }
 
-    // ---- wait for this block's record (bounded; all lanes leave together on failure)
-    const bool got = mbar_wait_bounded(&sw->bar[s_idx], (uint32_t)((i / NS) & 1), a.status);
-    if (__any_sync(0xffffffffu, !got)) {
+    // ---- wait for this block's record or K half (bounded; all lanes leave together on failure)
+    const uint8_t* kbuf;
+    if (__any_sync(0xffffffffu, !wait_next(kbuf))) {
       ok = false;
-      failed_at = i;
+      failed_at = WHOLE ? i : 2 * i;
       break;
     }
-    const uint8_t* st = stages + s_idx * rec;
-    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + g.codes_off[0]);
-    const uint16_t* km = reinterpret_cast<const uint16_t*>(st + g.meta_off[0]);
-    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + g.codes_off[1]);
-    const uint16_t* vm = reinterpret_cast<const uint16_t*>(st + g.meta_off[1]);
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(kbuf + g.codes_off[0]);
+    const uint16_t* km = reinterpret_cast<const uint16_t*>(kbuf + g.meta_off[0]);
 
     // ---- B fragments of the score product: q * s_channel (RTN, KVarN)
     int g0 = g0_fixed;
@@ -477,6 +497,22 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
         mloc = fmaxf(mloc, v);
       }
     }
+    const uint8_t* vbuf = kbuf + halfk;
+    if (!WHOLE) {  // the K half is consumed: refill its buffer, then wait for the V half
+      __syncwarp();
+      if (lane == 0) {
+        fence_proxy_async();
+        issue_next();
+      }
+      if (__any_sync(0xffffffffu, !wait_next(vbuf))) {
+        ok = false;
+        failed_at = 2 * i + 1;
+        break;
+      }
+    }
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(vbuf);
+    const uint16_t* vm = reinterpret_cast<const uint16_t*>(vbuf + (g.meta_off[1] - g.codes_off[1]));
+
     mloc = head_max<GT>(mloc);
     const float m_new = fmaxf(m_run, mloc);
     const float alpha = exp2f(m_run - m_new);
@@ -540,20 +576,18 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
       }
     }
 
-    __syncwarp();  // every lane is done with this stage
-    if (lane == 0 && i + NS < n) {
+    __syncwarp();  // every lane is done with the record / V half: refill its buffer
+    if (lane == 0) {
       fence_proxy_async();
-      mbar_arrive_expect_tx(&sw->bar[s_idx], (uint32_t)rec);
-      bulk_g2s(stages + s_idx * rec, rec_ptr(pu, pblk), (uint32_t)rec, &sw->bar[s_idx]);
+      issue_next();
     }
-    if (++pblk == a.nb) { pblk = 0; ++pu; }
     if (++blk == a.nb) { blk = 0; ++u; }
   }
 
-  if (!ok) {
+  if (!ok) {  // drain the copies still in flight (bounded) before the warp exits
     if (lane == 0) {
-      for (int j = failed_at; j < n && j < failed_at + NS; ++j)
-        mbar_wait_bounded(&sw->bar[j % NS], (uint32_t)((j / NS) & 1), nullptr, 200000000LL);
+      for (int j = failed_at; j < pnext; ++j)
+        mbar_wait_bounded(&sw->bar[j % NB], (uint32_t)((j / NB) & 1), nullptr, 200000000LL);
     }
     __syncwarp();
     return;
@@ -563,13 +597,36 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
 
 struct Plan {
   void (*fn)(Args);
-  int nw, ns;
+  int nw, ns;  // warps per CTA, buffers per warp
+  bool whole;  // buffers hold whole records (else K and V halves)
 };
+
+// Warps per CTA and half-record buffers per warp (compile-time tuning; the defaults are the
+// measured best on GB300).
+#ifndef KVQ_MMA2_NW
+#define KVQ_MMA2_NW 4
+#endif
+#ifndef KVQ_MMA2_NB
+#define KVQ_MMA2_NB 2
+#endif
+#ifndef KVQ_MMA2_WHOLE
+#define KVQ_MMA2_WHOLE 1
+#endif
+#ifndef KVQ_MMA4_NW
+#define KVQ_MMA4_NW 5
+#endif
+#ifndef KVQ_MMA4_NB
+#define KVQ_MMA4_NB 2
+#endif
+#ifndef KVQ_MMA4_WHOLE
+#define KVQ_MMA4_WHOLE 0
+#endif
 
 template <int METHOD, int BITS, int GT>
 Plan plan_for() {
-  constexpr int NW = 4, NS = 2;
-  return Plan{decode_mma_kernel<METHOD, BITS, GT, NW, NS>, NW, NS};
+  constexpr int NW = BITS == 2 ? KVQ_MMA2_NW : KVQ_MMA4_NW, NB = BITS == 2 ? KVQ_MMA2_NB : KVQ_MMA4_NB;
+  constexpr bool WH = BITS == 2 ? KVQ_MMA2_WHOLE : KVQ_MMA4_WHOLE;
+  return Plan{decode_mma_kernel<METHOD, BITS, GT, NW, NB, WH>, NW, NB, WH};
 }
 
 template <int METHOD, int BITS>
@@ -592,7 +649,9 @@ Plan get_plan(const Geo& g) {
 }
 
 size_t smem_bytes(const Geo& g, const Plan& p) {
-  return (size_t)p.nw * p.ns * g.rec_bytes + (size_t)p.nw * sizeof(WarpSmem);
+  const uint64_t hk = g.codes_off[1], hv = g.rec_bytes - hk;
+  const uint64_t hb = p.whole ? g.rec_bytes : (hk > hv ? hk : hv);
+  return (size_t)p.nw * p.ns * hb + (size_t)p.nw * sizeof(WarpSmem);
 }
 
 }  // namespace mmadec
