@@ -443,7 +443,7 @@ def run_reference(args):
 
 def _decode_bytes_per_head(w):
     """Algorithmic packed bytes of one (b, h) over the context (same count as kvq_decode_bytes)."""
-    W = -(-128 // (32 // w.bits))
+    W = 12 if w.bits == 3 else -(-128 // (32 // w.bits))  # 3-bit tiles: 48 B per 128 codes
     meta = {"rtn": 2, "nuq": 2, "varn": 3, "int4": 1}[w.method] * 256
     csr = 0
     if w.method == "nuq":

@@ -15,7 +15,7 @@ KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY, KVQ_ERR_ALIG
     KVQ_ERR_TIMEOUT = range(7)
 KVQ_RTN, KVQ_NUQ, KVQ_VARN, KVQ_INT4 = range(4)
 KVQ_F16, KVQ_BF16 = 0, 1
-KVQ_FORMAT_VERSION = 1
+KVQ_FORMAT_VERSION = 2
 KVQ_STATIC_WORKSPACE_BYTES = 8 << 20
 METHODS = {"rtn": KVQ_RTN, "nuq": KVQ_NUQ, "varn": KVQ_VARN, "int4": KVQ_INT4}
 

@@ -115,10 +115,35 @@ __device__ void rtn_tile(AppendSmem* sm, int axis, int bits, uint16_t* m16) {
   __syncthreads();
 }
 
-// Pack sm->codes (token-major, [t][c]) into words: code i of a row at bits
-// [b*(i%n)+b-1 : b*(i%n)] of word i/n. Key tiles: one row per token (its 128 channel codes).
-// Value tiles (transpose = true): one row per channel (its codes for the 128 tokens).
+// Pack sm->codes (token-major, [t][c]) into words. 2 and 4 bits: code i of a row at bits
+// [b*(i%n)+b-1 : b*(i%n)] of word i/n; key tiles one row per token (its 128 channel codes),
+// value tiles (transpose = true) one row per channel (its codes for the 128 tokens).
+// 3 bits: the plane layout of tile3_slot (one thread per output word).
 __device__ void pack_tile(const AppendSmem* sm, int bits, bool transpose, uint32_t* dst) {
+  if (bits == 3) {
+    const int kind = transpose ? 1 : 0;
+    for (int wi = threadIdx.x; wi < TILE3_WORDS; wi += AP_THREADS) {
+      const int s = wi / 192, rem = wi - s * 192, grp = rem / 6, o = rem - grp * 6;
+      uint32_t word = 0;
+      for (int k = 0; k < 8; ++k) {
+        if (o < 4) {  // low-bit plane: nibble words 2o and 2o+1
+          for (int hf = 0; hf < 2; ++hf) {
+            int t, c;
+            tile3_code_at(kind, s, grp, 2 * o + hf, k, t, c);
+            word |= ((uint32_t)sm->codes[t * D + c] & 3u) << (4 * k + 2 * hf);
+          }
+        } else {      // high-bit plane: nibble words 4(o-4) .. 4(o-4)+3
+          for (int q = 0; q < 4; ++q) {
+            int t, c;
+            tile3_code_at(kind, s, grp, 4 * (o - 4) + q, k, t, c);
+            word |= (((uint32_t)sm->codes[t * D + c] >> 2) & 1u) << (4 * k + (q ^ 2));
+          }
+        }
+      }
+      dst[wi] = word;
+    }
+    return;
+  }
   const int n = 32 / bits, W = (D + n - 1) / n;
   for (int it = threadIdx.x; it < T * W; it += AP_THREADS) {
     int r = it / W, w = it - r * W;

@@ -173,12 +173,18 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
     float acc[GMAX];
 #pragma unroll
     for (int k = 0; k < GMAX; ++k) acc[k] = 0.0f;
-    for (int w = 0; w < W; ++w) {
-      const uint32_t word = kc[t * W + w];
-      for (int j = 0; j < nw; j += 2) {
-        const int c = w * nw + j;
-        if (c >= D) break;
-        const uint32_t c0 = (word >> (bits * j)) & cmask, c1 = (word >> (bits * (j + 1))) & cmask;
+    for (int c = 0; c < D; c += 2) {
+      {
+        uint32_t c0, c1;
+        if (bits == 3) {
+          c0 = tile3_code(kc, 0, t, c);
+          c1 = tile3_code(kc, 0, t, c + 1);
+        } else {  // n = 32/bits is even: a channel pair never straddles two words
+          const int w = c / nw, j = c - w * nw;
+          const uint32_t word = kc[t * W + w];
+          c0 = (word >> (bits * j)) & cmask;
+          c1 = (word >> (bits * (j + 1))) & cmask;
+        }
         float k0, k1;
         if (METHOD == KVQ_RTN || METHOD == KVQ_VARN) {
           k0 = ((float)c0 + h2f(km[T + c])) * h2f(km[c]);
@@ -293,7 +299,8 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
       for (int k = 0; k < GMAX; ++k) bs[k] = 0.0f;
       for (int tt = 0; tt < T; ++tt) {
         const int wt = tt / nw;
-        const uint32_t code = (vc[c * W + wt] >> (bits * (tt - wt * nw))) & cmask;
+        const uint32_t code =
+            bits == 3 ? tile3_code(vc, 1, tt, c) : (vc[c * W + wt] >> (bits * (tt - wt * nw))) & cmask;
         float val;
         if (METHOD == KVQ_RTN || METHOD == KVQ_VARN) {
           val = (float)code + h2f(vm[T + tt]);

@@ -18,7 +18,54 @@ constexpr int TILE = T * D; // elements per tile
 
 __host__ __device__ constexpr int codes_per_word(int bits) { return 32 / bits; }
 __host__ __device__ constexpr int words_per_row(int bits) {
-  return (D + codes_per_word(bits) - 1) / codes_per_word(bits);
+  return bits == 3 ? 12 : (D + codes_per_word(bits) - 1) / codes_per_word(bits);
+}
+
+// 3-bit tiles ([KVQ] §9.3: 48 bytes per 128 codes) keep each code's two low bits and its high
+// bit in separate planes, in the order the tensor-core decode's fragments read them. The tile
+// is 8 segments of 16 tokens; a segment is 32 groups of 6 words (one lane's codes); in a group,
+// slot k (0..7) of nibble word u (0..7) has its low bits in word u/2 at bit 4k + 2(u%2) and its
+// high bit in word 4 + u/4 at bit 4k + ((u%4) ^ 2).
+constexpr int TILE3_WORDS = 1536;
+
+// Token t and channel c of slot k of nibble word u in group grp of segment s.
+__host__ __device__ inline void tile3_code_at(int kind, int s, int grp, int u, int k, int& t, int& c) {
+  const int g = grp >> 2, tq = grp & 3;
+  if (kind == 0) {  // keys: group = (token t%8, channel pair class (c/2)%4)
+    t = 16 * s + g + 8 * ((k >> 1) & 1);
+    c = 8 * (2 * u + (k >> 2)) + 2 * tq + (k & 1);
+  } else {          // values: group = (channel c%8, token class t%4)
+    const int v = 2 * (k & 1) + (k >> 2);
+    t = 16 * s + tq + 4 * v;
+    c = 16 * u + g + 8 * ((k >> 1) & 1);
+  }
+}
+
+// Word indices and bit shifts of code (t, c): low bits at (lw, ls), high bit at (hw, hs).
+__host__ __device__ inline void tile3_slot(int kind, int t, int c, int& lw, int& ls, int& hw, int& hs) {
+  const int s = t >> 4, tl = t & 15;
+  int grp, u, k;
+  if (kind == 0) {
+    grp = 4 * (tl & 7) + ((c >> 1) & 3);
+    u = c >> 4;
+    k = 4 * ((c >> 3) & 1) + 2 * (tl >> 3) + (c & 1);
+  } else {
+    const int v = tl >> 2;
+    grp = 4 * (c & 7) + (tl & 3);
+    u = c >> 4;
+    k = 4 * (v & 1) + 2 * ((c >> 3) & 1) + (v >> 1);
+  }
+  const int base = s * 192 + grp * 6;
+  lw = base + (u >> 1);
+  ls = 4 * k + 2 * (u & 1);
+  hw = base + 4 + (u >> 2);
+  hs = 4 * k + ((u & 3) ^ 2);
+}
+
+__device__ __forceinline__ uint32_t tile3_code(const uint32_t* w, int kind, int t, int c) {
+  int lw, ls, hw, hs;
+  tile3_slot(kind, t, c, lw, ls, hw, hs);
+  return ((w[lw] >> ls) & 3u) | (((w[hw] >> hs) & 1u) << 2);
 }
 __host__ __device__ constexpr uint64_t round16(uint64_t x) { return (x + 15) & ~uint64_t(15); }
 

@@ -36,7 +36,7 @@
 extern "C" {
 #endif
 
-#define KVQ_FORMAT_VERSION 1u
+#define KVQ_FORMAT_VERSION 2u
 #define KVQ_BLOCK 128
 #define KVQ_HEAD_DIM 128
 #define KVQ_MAX_GROUP 16      /* n_q_heads / n_kv_heads supported by decode */
@@ -94,10 +94,20 @@ typedef struct {
 /* Byte layout of a cache, from kvq_layout. One record per (b, h, block), at
  *   base + ((b * n_kv_heads + h) * max_blocks + block) * record_bytes,
  * holding the K tile then the V tile; every region starts 16-byte aligned:
- *   codes : 128 rows x words_per_row uint32; code i of a row at bits
- *           [b*(i%n)+b-1 : b*(i%n)] of word i/n, n = floor(32/b), unused high bits zero
- *           ([KVQ] §9.3 3-bit layout, generalised). K tile: one row per token (its 128
- *           channel codes). V tile: one row per channel (its codes for the 128 tokens).
+ *   codes : 2- and 4-bit tiles: 128 rows x words_per_row uint32; code i of a row at bits
+ *           [b*(i%n)+b-1 : b*(i%n)] of word i/n, n = 32/b ([KVQ] §9.3 layout, generalised).
+ *           K tile: one row per token (its 128 channel codes). V tile: one row per channel
+ *           (its codes for the 128 tokens).
+ *           3-bit tiles: 1536 uint32 (48 bytes per 128 codes, the count of [KVQ] §9.3),
+ *           bit planes in matrix-fragment order. Segment s = t/16 (t = token in the block)
+ *           holds 32 groups of 6 words (group base word s*192 + 6*grp); in a group, slot k
+ *           (0..7) of nibble word u (0..7) keeps a code's two low bits in word u/2 at bit
+ *           4k + 2(u%2) and its high bit in word 4 + u/4 at bit 4k + {2,3,0,1}[u%4].
+ *           K tile, code (t, channel c): grp = 4(t%8) + (c/2)%4, u = c/16,
+ *             k = 4((c/8)%2) + 2((t%16)/8) + c%2.
+ *           V tile, code (t, c): grp = 4(c%8) + t%4, u = c/16,
+ *             k = 4(((t%16)/4)%2) + 2((c/8)%2) + (t%16)/8.
+ *           words_per_row is 12 for 3-bit caches (the tile holds 128 x 12 words).
  *   meta  : fp16 vectors of 128. RTN and VARN: s, z (keys: per channel; values: per token),
  *           VARN adds s1 (keys: per token; values: per channel). NUQ: s (half-range),
  *           zp (centre). INT4: s (per token).

@@ -122,6 +122,76 @@ def unpack_rows(words: np.ndarray, bits: int) -> np.ndarray:
     return out
 
 
+# 3-bit tiles. [KVQ] §9.3 counts 128 x 3 bits = 48 bytes per key vector, which ten codes per
+# 32-bit word (its bit example, 13 words = 52 bytes) cannot reach; a 3-bit tile here takes the
+# 48-byte count: 128 x 128 codes in 1536 words, with every code's two low bits and its high bit
+# in separate bit planes. The plane order follows the decode's matrix fragments: the tile is
+# cut into 8 segments of 16 tokens, each segment into 32 groups of 64 codes (6 words each),
+# and within a group the codes sit in 8 four-bit slots of 8 "nibble words" u (the low bits of
+# nibble word u in word u//2 at bit 4k + 2(u%2), its high bit in word 4 + u//4 at bit
+# 4k + (2, 3, 0, 1)[u%4], k = 0..7 the slot).
+TILE3_WORDS = 1536
+
+
+def tile3_slot(kind: int, t, c):
+    """Where code (token t, channel c) of a 3-bit tile lives: (low-bits word, its shift,
+    high-bit word, its shift). Keys: group 4*(t%8) + (c//2)%4 of segment t//16, nibble word
+    c//16, slot 4*((c//8)%2) + 2*((t%16)//8) + c%2. Values: group 4*(c%8) + t%4 of segment
+    t//16, nibble word c//16, slot 4*((t%16)//4 % 2) + 2*((c//8)%2) + (t%16)//8."""
+    t = np.asarray(t, np.int64)
+    c = np.asarray(c, np.int64)
+    s, tl = t >> 4, t & 15
+    if kind == KIND_K:
+        g, r = tl & 7, tl >> 3
+        tq, kg, j = (c >> 1) & 3, c >> 3, c & 1
+        u, k = kg >> 1, 4 * (kg & 1) + 2 * r + j
+    else:
+        tq, v = tl & 3, tl >> 2
+        g, r, mt = c & 7, (c >> 3) & 1, c >> 4
+        u, k = mt, 4 * (v & 1) + 2 * r + (v >> 1)
+    base = s * 192 + (4 * g + tq) * 6
+    hi_pos = np.array([2, 3, 0, 1])[u & 3]
+    return base + (u >> 1), 4 * k + 2 * (u & 1), base + 4 + (u >> 2), 4 * k + hi_pos
+
+
+def pack_tile3(codes: np.ndarray, kind: int) -> np.ndarray:
+    """3-bit codes [128 tokens][128 channels] -> uint32[1536] in the tile3 plane layout."""
+    codes = np.asarray(codes, np.uint64)
+    t, c = np.meshgrid(np.arange(T), np.arange(D), indexing="ij")
+    lw, ls, hw, hs = tile3_slot(kind, t.ravel(), c.ravel())
+    q = codes.ravel()
+    out = np.zeros(TILE3_WORDS, np.uint64)
+    np.bitwise_or.at(out, lw, (q & np.uint64(3)) << ls.astype(np.uint64))
+    np.bitwise_or.at(out, hw, ((q >> np.uint64(2)) & np.uint64(1)) << hs.astype(np.uint64))
+    return out.astype(np.uint32)
+
+
+def unpack_tile3(words: np.ndarray, kind: int) -> np.ndarray:
+    """Inverse of pack_tile3: uint32[1536] -> uint8 codes [128 tokens][128 channels]."""
+    w = np.asarray(words, np.uint64)
+    t, c = np.meshgrid(np.arange(T), np.arange(D), indexing="ij")
+    lw, ls, hw, hs = tile3_slot(kind, t.ravel(), c.ravel())
+    lo = (w[lw] >> ls.astype(np.uint64)) & np.uint64(3)
+    hi = (w[hw] >> hs.astype(np.uint64)) & np.uint64(1)
+    return (lo | (hi << np.uint64(2))).astype(np.uint8).reshape(T, D)
+
+
+def pack_tile(codes: np.ndarray, bits: int, kind: int) -> np.ndarray:
+    """Code words of one tile (codes [token][channel]): 3-bit tiles use the plane layout above;
+    2- and 4-bit key tiles hold one row per token, value tiles one row per channel."""
+    if bits == 3:
+        return pack_tile3(codes, kind)
+    return pack_rows(codes if kind == KIND_K else np.asarray(codes).T, bits)
+
+
+def unpack_tile(words: np.ndarray, bits: int, kind: int) -> np.ndarray:
+    """Inverse of pack_tile: codes [token][channel]."""
+    if bits == 3:
+        return unpack_tile3(words, kind)
+    codes = unpack_rows(words, bits)
+    return codes if kind == KIND_K else codes.T
+
+
 # =========================================================================== uniform RTN
 
 def rtn_meta(mx, mn, bits: int):
@@ -444,9 +514,8 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
 class OracleCache:
     """A packed cache kept as per-tile records plus the decode that reads it.
 
-    One record per (batch b, KV head h, block, kind): the packed code words (key tiles one
-    row per token, value tiles one row per channel), the fp16 metadata and, for nuq, the CSR
-    outliers. decode() unpacks and dequantises every
+    One record per (batch b, KV head h, block, kind): the packed code words (pack_tile), the
+    fp16 metadata and, for nuq, the CSR outliers. decode() unpacks and dequantises every
     record in fp64 (RoPE at absolute positions for pre-RoPE keys; the Hadamard domain
     for KVarN, with the query transformed the same way and the output transformed back),
     appends the fp residual tail and evaluates softmax attention. Query head j reads KV
@@ -487,9 +556,7 @@ class OracleCache:
             rec = nuq_quantize(x, self.codebook[h], 0 if kind == KIND_K else 1, self.n_out)
         else:
             rec = varn_quantize(x, b, kind, self.varn_iters, self.use_hadamard)
-        # keys: one row per token (its 128 channel codes); values: one row per channel (its
-        # codes for the 128 tokens of the block)
-        rec["words"] = pack_rows(rec["codes"] if kind == KIND_K else rec["codes"].T, b)
+        rec["words"] = pack_tile(rec["codes"], b, kind)
         return rec
 
     def append(self, K: np.ndarray, V: np.ndarray, only_heads=None):
@@ -511,9 +578,7 @@ class OracleCache:
         """domain 'stored': the quantised representation (pre-RoPE keys un-rotated, KVarN
         in the Hadamard domain); 'input': back in the input domain (inverse Hadamard for
         KVarN); 'attn': what attention reads (RoPE applied to pre-RoPE keys)."""
-        codes = unpack_rows(rec["words"], self.bits)
-        if kind == KIND_V:
-            codes = codes.T
+        codes = unpack_tile(rec["words"], self.bits, kind)
         m = self.method
         if m == "rtn":
             x = rtn_dequant(codes, rec["s16"], rec["z16"], 0 if kind == KIND_K else 1)

@@ -53,7 +53,8 @@ def tile_fields(rec: np.ndarray, lay, kind: int, method: str, bits: int) -> dict
     W = lay.words_per_row
     co, cb = int(lay.codes_off[kind]), int(lay.codes_bytes[kind])
     mo, mb = int(lay.meta_off[kind]), int(lay.meta_bytes[kind])
-    out = dict(words=rec[co:co + cb].view(np.uint32).reshape(T, W).copy())
+    words = rec[co:co + cb].view(np.uint32).copy()
+    out = dict(words=words if bits == 3 else words.reshape(T, W))
     meta = rec[mo:mo + mb].view(np.uint16).reshape(-1, T)
     out["s16"] = meta[0].view(np.float16).copy()
     if method in ("rtn", "varn"):

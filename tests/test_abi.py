@@ -79,8 +79,8 @@ def _cfg(K, wid, **kw):
 
 
 # algorithmic packed bytes per decode step at the full workloads (codes + fp16 metadata + CSR)
-EXPECTED_DECODE_BYTES = {1: 278528, 2: 129728512, 3: 79691776, 4: 1107296256, 5: 2415919104}
-EXPECTED_RECORD_BYTES = {1: 2 * (8192 + 512), 2: 2 * (6656 + 512 + 752), 3: 2 * (4096 + 768),
+EXPECTED_DECODE_BYTES = {1: 278528, 2: 121339904, 3: 79691776, 4: 1107296256, 5: 2415919104}
+EXPECTED_RECORD_BYTES = {1: 2 * (8192 + 512), 2: 2 * (6144 + 512 + 752), 3: 2 * (4096 + 768),
                          4: 2 * (8192 + 256), 5: 2 * (4096 + 512)}
 
 
@@ -90,8 +90,8 @@ def test_layout_and_decode_bytes(K, wid):
     lay = K.kvq_layout(cfg)
     w = WL.WORKLOADS[wid]
     assert lay.record_bytes == EXPECTED_RECORD_BYTES[wid]
-    assert lay.words_per_row == -(-128 // (32 // w.bits))
-    assert lay.format_version == 1
+    assert lay.words_per_row == (12 if w.bits == 3 else -(-128 // (32 // w.bits)))
+    assert lay.format_version == 2
     for k in range(2):
         assert lay.codes_off[k] % 16 == 0 and lay.meta_off[k] % 16 == 0 and lay.csr_off[k] % 16 == 0
     assert lay.records_bytes == w.batch * w.n_kv_heads * w.n_blocks * lay.record_bytes

@@ -117,9 +117,7 @@ def _varn_check_tile(got, exp, K_in, kind, dbg_rc):
     else:
         tt = Z32 / s[:, None] - z[:, None]
     e = np.clip(np.rint(tt), 0, 2 ** bits - 1)
-    codes = O.unpack_rows(got["words"], bits).astype(np.int64)
-    if kind == 1:      # value tiles are stored one row per channel
-        codes = codes.T
+    codes = O.unpack_tile(got["words"], bits, kind).astype(np.int64)
     diff = np.abs(codes - e)
     frac = np.abs(tt.astype(np.float64) - np.floor(tt.astype(np.float64)) - 0.5)
     near = frac <= 1e-5 * np.maximum(1.0, np.abs(tt))

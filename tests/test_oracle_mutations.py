@@ -81,6 +81,32 @@ def test_pack_msb_first_is_caught(monkeypatch, golden_dir):
     assert _fails(P.test_3bit_layout_printed_words, golden_dir)
 
 
+def test_tile3_swapped_high_bit_planes_are_caught(monkeypatch):
+    orig = K.tile3_slot
+
+    def slot(kind, t, c):
+        lw, ls, hw, hs = orig(kind, t, c)
+        u = np.asarray(c, np.int64) >> 4  # the nibble word, for keys and values alike
+        # high bits of nibble words 2 and 3 exchanged: still a valid permutation
+        return lw, ls, hw, np.where((u & 3) >= 2, hs ^ 1, hs)
+    monkeypatch.setattr(K, "tile3_slot", slot)
+    monkeypatch.setattr(O, "tile3_slot", slot)
+    assert _fails(P.test_tile3_slots_follow_the_documented_rule)
+
+
+def test_tile3_value_token_order_is_caught(monkeypatch):
+    orig = K.tile3_slot
+
+    def slot(kind, t, c):
+        if kind == K.KIND_V:  # tokens t and t^8 of each segment exchanged
+            t = np.asarray(t, np.int64) ^ 8
+        return orig(kind, t, c)
+    monkeypatch.setattr(K, "tile3_slot", slot)
+    monkeypatch.setattr(O, "tile3_slot", slot)
+    assert _fails(P.test_tile3_groups_hold_one_lanes_fragment_codes, 1) or \
+        _fails(P.test_tile3_slots_follow_the_documented_rule)
+
+
 def test_varn_column_only_is_caught(monkeypatch):
     def varn_cols(X, iters=8):
         Y = np.array(X, np.float64)

@@ -66,6 +66,72 @@ def test_pack_roundtrip_and_unused_bits(bits):
     assert ((int(words[5, 1]) >> (bits * 2)) & ((1 << bits) - 1)) == codes[5, n + 2]
 
 
+def test_tile3_size_bijection_and_roundtrip(golden_dir):
+    g = _golden(golden_dir, "kvquant_3bit_layout.json")
+    assert O.TILE3_WORDS * 4 == 128 * g["bytes_per_128_channel_key"]["value"]
+    t, c = np.meshgrid(np.arange(128), np.arange(128), indexing="ij")
+    rng = np.random.default_rng(3)
+    for kind in (O.KIND_K, O.KIND_V):
+        lw, ls, hw, hs = O.tile3_slot(kind, t.ravel(), c.ravel())
+        assert np.all((ls & 1) == 0) and np.all(ls <= 30) and np.all(hs <= 31)
+        bit_ids = np.concatenate([lw * 32 + ls, lw * 32 + ls + 1, hw * 32 + hs])
+        # every one of the 49152 bits of the tile holds exactly one bit of one code
+        assert np.array_equal(np.sort(bit_ids), np.arange(O.TILE3_WORDS * 32))
+        codes = rng.integers(0, 8, size=(128, 128)).astype(np.uint8)
+        words = O.pack_tile3(codes, kind)
+        assert words.dtype == np.uint32 and words.shape == (O.TILE3_WORDS,)
+        assert np.array_equal(O.unpack_tile3(words, kind), codes)
+        # a single code 5 = 0b101: low bits 01 at its low-bit slot, high bit at its high slot
+        one = np.zeros((128, 128), np.uint8)
+        one[77, 101] = 5
+        w = O.pack_tile3(one, kind)
+        lw1, ls1, hw1, hs1 = (int(x) for x in O.tile3_slot(kind, 77, 101))
+        exp = np.zeros(O.TILE3_WORDS, np.uint64)
+        exp[lw1] |= 1 << ls1
+        exp[hw1] |= 1 << hs1
+        assert np.array_equal(w.astype(np.uint64), exp)
+
+
+def test_tile3_slots_follow_the_documented_rule():
+    """Hand-evaluated positions from the rule in the layout's description."""
+    # key (t=9, c=13): segment 0, t%8=1, (t%16)//8=1, (c//2)%4=2, c//8=1, c%2=1
+    #   group 4*1+2=6 (word base 36), nibble word 13//16=0, slot 4*1+2*1+1=7
+    assert tuple(int(x) for x in O.tile3_slot(O.KIND_K, 9, 13)) == (36, 28, 40, 30)
+    # key (t=50, c=100): segment 3, t%16=2 -> g=2, r=0,
+    #   (c//2)%4=2, c//8=12, c%2=0: group 10 (base 3*192+60=636), nibble word 6, slot 0
+    #   low bits: word 636+3, shift 0; high bit: word 636+4+1, shift (2,3,0,1)[2] = 0
+    assert tuple(int(x) for x in O.tile3_slot(O.KIND_K, 50, 100)) == (639, 0, 641, 0)
+    # value (t=23, c=45): segment 1, t%16=7 -> t%4=3, (t%16)//4=1; c%8=5, (c//8)%2=1, c//16=2
+    #   group 4*5+3=23 (base 192+138=330), nibble word 2, slot 4*1+2*1+0=6
+    #   low bits: word 330+1, shift 24; high bit: word 330+4, shift 24+(2,3,0,1)[2]=24
+    assert tuple(int(x) for x in O.tile3_slot(O.KIND_V, 23, 45)) == (331, 24, 334, 24)
+
+
+@pytest.mark.parametrize("kind", [0, 1])
+def test_tile3_groups_hold_one_lanes_fragment_codes(kind):
+    """Group l = 4g + tq of segment s holds: keys, tokens 16s+g and 16s+g+8 at the 32
+    channels c with (c//2)%4 = tq; values, tokens 16s+tq+4v (v = 0..3) at the 16 channels
+    16m+g and 16m+g+8."""
+    t, c = np.meshgrid(np.arange(128), np.arange(128), indexing="ij")
+    lw, _, hw, _ = O.tile3_slot(kind, t, c)
+    grp = lw // 6
+    assert np.array_equal(grp, hw // 6)
+    for s in (0, 5):
+        for g in range(8):
+            for tq in range(4):
+                sel = grp == s * 32 + 4 * g + tq
+                if kind == O.KIND_K:
+                    exp = np.zeros((128, 128), bool)
+                    for r in (0, 1):
+                        exp[16 * s + g + 8 * r, [ch for ch in range(128) if (ch // 2) % 4 == tq]] = True
+                else:
+                    exp = np.zeros((128, 128), bool)
+                    for v in range(4):
+                        for m in range(8):
+                            exp[16 * s + tq + 4 * v, [16 * m + g, 16 * m + g + 8]] = True
+                assert np.array_equal(sel, exp)
+
+
 # ------------------------------------------------------------------ uniform RTN
 
 def test_scale_examples_per_token_vs_per_channel(golden_dir):
