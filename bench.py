@@ -287,9 +287,7 @@ def run_kvq(args):
         "timing": "CUDA graph replays, CUDA events on the launching stream",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
-                     "kernel": ("decode_mma_kernel" if (w.method in ("rtn", "varn", "int4") and w.bits in (2, 4)
-                                                        and w.group <= 4) else "decode_kernel")
-                               + " + combine_kernel (kvq_decode_attn, empty tail)",
+                     "kernel": _decode_kernel_name(w) + " + combine_kernel (kvq_decode_attn, empty tail)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "gpu_launches": args.steps * (2 * DECODES_PER_STEP + 1),
         "roofline_decodes": R_DEC,
@@ -439,6 +437,15 @@ def run_reference(args):
             "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                              "sample": f"decode of 1 (batch, KV head) pair over {ws.n_blocks} blocks per step"},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def _decode_kernel_name(w):
+    """The decode kernel the library picks for this workload (mirrors its dispatch rules)."""
+    if w.method == "nuq" and w.bits == 3 and w.group == 1 and w.pre_rope:
+        return "decode_nuq_kernel"
+    if w.method in ("rtn", "varn", "int4") and w.bits in (2, 4) and w.group <= 4:
+        return "decode_mma_kernel"
+    return "decode_kernel"
 
 
 def _decode_bytes_per_head(w):

@@ -466,6 +466,10 @@ cudaError_t launch_decode_m(const DecodeArgs& a, cudaStream_t st) {
 }  // namespace kvq
 
 long long kvq_mma_ranges(const kvq::Geo& g);
+long long kvq_nuq_ranges(const kvq::Geo& g);
+cudaError_t kvq_launch_decode_nuq(const kvq::Geo& g, const uint8_t* base, const float* codebook, const uint16_t* q,
+                                  int n_blocks, long long ranges, long long slots, float* ws_m, float* ws_l,
+                                  float* ws_o, int* status, cudaStream_t st);
 long long kvq_mma_slots(const kvq::Geo& g, int n_blocks, long long ranges);
 cudaError_t kvq_launch_decode_mma(const kvq::Geo& g, const uint8_t* base, const uint16_t* q, int n_blocks,
                                   long long ranges, long long slots, float* ws_m, float* ws_l, float* ws_o,
@@ -476,14 +480,17 @@ namespace {
 // Which decode runs for this geometry on the current device, and how many partial rows per
 // (b, query head) it writes.
 struct DecodePlan {
-  long long ranges;  // > 0: tensor-core decode over this many warp ranges
+  long long ranges;  // > 0: tensor-core decode over this many ranges (warps, or CTAs for nuq)
   long long rows;    // partial rows per (b, query head)
+  bool nuq;          // the 3-bit nuq pre-RoPE decode
 };
 
 DecodePlan plan_decode(const kvq::Geo& g, int n_blocks, int v1_splits) {
-  DecodePlan p{0, v1_splits};
-  if (n_blocks <= 0) return DecodePlan{0, 0};
-  long long ranges = kvq_mma_ranges(g);
+  DecodePlan p{0, v1_splits, false};
+  if (n_blocks <= 0) return DecodePlan{0, 0, false};
+  long long ranges = kvq_nuq_ranges(g);
+  p.nuq = ranges > 0;
+  if (!p.nuq) ranges = kvq_mma_ranges(g);
   const long long total = (long long)g.B * g.H * n_blocks;
   if (ranges > total) ranges = total;  // every range holds at least one block
   if (ranges > 0 && total < (1LL << 62) / ranges) {
@@ -505,7 +512,10 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
   float* ws_o = ws + 2 * rows + ((4 - (2 * rows) % 4) % 4);  // keep o 16-byte aligned
   if (n_blocks > 0) {
     cudaError_t e;
-    if (plan.ranges > 0) {
+    if (plan.ranges > 0 && plan.nuq) {
+      e = kvq_launch_decode_nuq(g, base, codebook, q, n_blocks, plan.ranges, plan.rows, ws_m, ws_l, ws_o, status,
+                                st);
+    } else if (plan.ranges > 0) {
       e = kvq_launch_decode_mma(g, base, q, n_blocks, plan.ranges, plan.rows, ws_m, ws_l, ws_o, status, hadamard,
                                 st);
     } else {

@@ -181,6 +181,9 @@ DECODE_CASES = [
     ("rtn3_gqa", WL.WORKLOADS[5], dict(bits=3, batch=2, n_kv_heads=2, n_q_heads=8, ctx=3 * 128), [127]),
     ("int4_bf16", WL.WORKLOADS[4], dict(batch=2, n_kv_heads=2, n_q_heads=8, ctx=5 * 128), [0, 64]),
     ("nuq3_rope", WL.WORKLOADS[2], dict(batch=1, n_kv_heads=3, n_q_heads=3, ctx=6 * 128), [0, 1, 127]),
+    ("nuq3_rope_ragged_ranges", WL.WORKLOADS[2], dict(batch=3, n_kv_heads=5, n_q_heads=5, ctx=37 * 128), [0, 77]),
+    ("nuq3_rope_5pct", WL.WORKLOADS[2], dict(outlier_frac=0.05, batch=1, n_kv_heads=2, n_q_heads=2, ctx=9 * 128), [3]),
+    ("nuq3_rope_no_outliers", WL.WORKLOADS[2], dict(outlier_frac=0.0, batch=2, n_kv_heads=2, n_q_heads=2, ctx=4 * 128), [0]),
     ("nuq3_norope_gqa", WL.WORKLOADS[2], dict(pre_rope=False, batch=2, n_kv_heads=2, n_q_heads=4, ctx=3 * 128), [9]),
     ("varn2_gqa", WL.WORKLOADS[3], dict(batch=2, n_kv_heads=2, n_q_heads=8, ctx=4 * 128), [0, 100]),
     ("varn2_g16", WL.WORKLOADS[3], dict(batch=1, n_kv_heads=1, n_q_heads=16, ctx=2 * 128), [1]),
