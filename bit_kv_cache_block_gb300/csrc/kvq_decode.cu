@@ -48,6 +48,7 @@ struct CombineArgs {
   int n_blocks;
   int n_split;          // partial rows per (b, query head)
   long long ranges;     // > 0: partials come from the range-split tensor-core decode
+  int per_range;        // partial rows per range and (b, query head)
   long long total;      // B * H * n_blocks
   const float* ws_m;
   const float* ws_l;
@@ -368,7 +369,7 @@ __global__ void __launch_bounds__(DC_THREADS) combine_kernel(CombineArgs a) {
     const long long u = (long long)b * g.H + h;
     const long long r0 = ((u * a.n_blocks + 1) * a.ranges - 1) / a.total;
     const long long r1 = (((u + 1) * a.n_blocks) * a.ranges - 1) / a.total;
-    n_part = (int)(r1 - r0 + 1);
+    n_part = (int)(r1 - r0 + 1) * a.per_range;
     if (n_part > a.n_split) n_part = a.n_split;
   }
 
@@ -467,6 +468,7 @@ cudaError_t launch_decode_m(const DecodeArgs& a, cudaStream_t st) {
 
 long long kvq_mma_ranges(const kvq::Geo& g);
 long long kvq_nuq_ranges(const kvq::Geo& g);
+int kvq_nuq_parts_per_range();
 cudaError_t kvq_launch_decode_nuq(const kvq::Geo& g, const uint8_t* base, const float* codebook, const uint16_t* q,
                                   int n_blocks, long long ranges, long long slots, float* ws_m, float* ws_l,
                                   float* ws_o, int* status, cudaStream_t st);
@@ -483,11 +485,13 @@ struct DecodePlan {
   long long ranges;  // > 0: tensor-core decode over this many ranges (warps, or CTAs for nuq)
   long long rows;    // partial rows per (b, query head)
   bool nuq;          // the 3-bit nuq pre-RoPE decode
+  long long slots;   // range slots per (b, query head) (rows = slots * per_range)
+  int per_range;     // partial rows one range writes per (b, query head)
 };
 
 DecodePlan plan_decode(const kvq::Geo& g, int n_blocks, int v1_splits) {
-  DecodePlan p{0, v1_splits, false};
-  if (n_blocks <= 0) return DecodePlan{0, 0, false};
+  DecodePlan p{0, v1_splits, false, v1_splits, 1};
+  if (n_blocks <= 0) return DecodePlan{0, 0, false, 0, 1};
   long long ranges = kvq_nuq_ranges(g);
   p.nuq = ranges > 0;
   if (!p.nuq) ranges = kvq_mma_ranges(g);
@@ -495,7 +499,9 @@ DecodePlan plan_decode(const kvq::Geo& g, int n_blocks, int v1_splits) {
   if (ranges > total) ranges = total;  // every range holds at least one block
   if (ranges > 0 && total < (1LL << 62) / ranges) {
     p.ranges = ranges;
-    p.rows = kvq_mma_slots(g, n_blocks, ranges);
+    p.slots = kvq_mma_slots(g, n_blocks, ranges);
+    p.per_range = p.nuq ? kvq_nuq_parts_per_range() : 1;
+    p.rows = p.slots * p.per_range;
   }
   return p;
 }
@@ -513,7 +519,7 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
   if (n_blocks > 0) {
     cudaError_t e;
     if (plan.ranges > 0 && plan.nuq) {
-      e = kvq_launch_decode_nuq(g, base, codebook, q, n_blocks, plan.ranges, plan.rows, ws_m, ws_l, ws_o, status,
+      e = kvq_launch_decode_nuq(g, base, codebook, q, n_blocks, plan.ranges, plan.slots, ws_m, ws_l, ws_o, status,
                                 st);
     } else if (plan.ranges > 0) {
       e = kvq_launch_decode_mma(g, base, q, n_blocks, plan.ranges, plan.rows, ws_m, ws_l, ws_o, status, hadamard,
@@ -533,7 +539,7 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
   }
   CombineArgs c;
   c.g = g; c.base = base; c.q = q; c.tail_k = tail_k; c.tail_v = tail_v; c.n_tail = n_tail;
-  c.n_blocks = n_blocks; c.n_split = (int)plan.rows; c.ranges = plan.ranges;
+  c.n_blocks = n_blocks; c.n_split = (int)plan.rows; c.ranges = plan.ranges; c.per_range = plan.per_range;
   c.total = (long long)g.B * g.H * n_blocks;
   c.ws_m = ws_m; c.ws_l = ws_l; c.ws_o = ws_o; c.out = out; c.hadamard = hadamard;
   dim3 grid(g.Hq, g.B);

@@ -2,39 +2,57 @@
 // (one query head per KV head).
 //
 // Work split. The (b, h, block) sequence of the whole batch is cut into one contiguous range
-// per CTA (persistent: one wave). A CTA of 8 warps streams whole block records (K tile, V tile,
-// fp16 metadata, CSR outliers) through a ring of shared-memory stages with 1-D bulk copies
-// (cp.async.bulk, mbarrier completion, bounded waits). Warp w owns tokens 16w..16w+15 of every
-// block and keeps its own flash-decode state (running max, sum, output); at the end of each
-// (b, h) segment the 8 states merge into one partial (m, l, o[128]) for the combine kernel.
+// per CTA (persistent: one wave). A CTA runs 12 warps that meet on mbarriers (every wait
+// bounded):
+//   4 aux warps       : stream each block record (K tile, V tile, fp16 metadata, CSR outliers)
+//                       plus the block's RoPE start-angle row into a ring stage with 1-D bulk
+//                       copies, build the block's shared score operands, turn the key outliers
+//                       into one additive score term per token and tag every value outlier with
+//                       its token;
+//   8 consumer warps  : warp w owns tokens 16w..16w+15 of every block and keeps its own
+//                       flash-decode state (running max, sum, output), written as its own
+//                       partial (m, l, o[128]) at the end of each (b, h) segment; the combine
+//                       kernel merges the partials.
 //
 // Keys ([KVQ] §3.2 pre-RoPE quantisation, Algorithm 1 dequantisation, worked example step 5):
 // the key at absolute position n = n0 + t (n0 = 128 * block) is k_n = R(n) (s*C[q] + zp + o),
 // so q . k_n = (R(t)^T q_b) . (s*C[q] + zp + o) with q_b = R(n0)^T q. Per channel pair i
 // (angle t*theta_i) this is cos * X_i + sin * Y_i with
 //     X_i = q_b0 k0 + q_b1 k1,    Y_i = q_b1 k0 - q_b0 k1.
-// X and Y of 16 tokens x 4 pairs come out of one mma.sync m16n8k16: A = the codebook values
-// C[q] of 16 tokens x 8 channels (looked up from the packed codes with byte permutes on an fp16
-// table held in registers; the 8 channels repeated in k = 8..15), B = the block's q_b * s as an
-// fp16 high part (k < 8) and low part (k >= 8) in the X and Y columns of each pair, C = the
-// zero-point terms. The cos/sin of a lane's own (token, pair) cells are fixed over blocks and
-// stay in registers; the fp16 outliers of the CSR add their rotated contribution per entry.
+// X and Y of 16 tokens x 4 pairs come out of one mma.sync m16n8k8: A = the codebook values C[q]
+// of 16 tokens x 8 channels (looked up from the packed codes with byte permutes on an fp16 table
+// held in registers), B = the block's q_b * s in fp16 in the X and Y columns of each pair, C =
+// the zero-point terms. The cos/sin of a lane's own (token, pair) cells are fixed over blocks
+// and stay in registers; the fp16 outliers o of the CSR enter as per-token score terms.
 // Values ([KVQ] §3.7 value matvec): O[channel] = sum_t p_t s_t C[q] + sum_t p_t zp_t + outliers,
 // one m16n8k16 per 16 channels x the warp's 16 tokens; B = p*s in high/low fp16 columns.
 // Softmax in base 2 with the running max per warp (rescaling only when the max grows).
 #include "kvq_internal.cuh"
 
+#include <type_traits>
+
 namespace kvq {
 namespace nuqdec {
 
-constexpr int NW = 8;  // warps per CTA (16 tokens of each block per warp)
-constexpr int NT = NW * 32;
+constexpr int NW = 8;               // consumer warps (16 tokens of each block per warp)
+constexpr int NAUX = 128;          // aux threads: copies, block operands, outlier terms
+constexpr int NTHREADS = NW * 32 + NAUX;
+constexpr int ROPE_ROW = 64 * 8;    // bytes of one (cos, sin) row of 64 pairs
+constexpr int MAX_OUTLIERS = 2048;  // per tile, on this path
 constexpr float LOG2E_RSQRT_D = 1.4426950408889634f * 0.08838834764831845f;
 
 #ifndef KVQ_NUQ_NB
-#define KVQ_NUQ_NB 4
+#define KVQ_NUQ_NB 8
 #endif
-constexpr int NB = KVQ_NUQ_NB;  // record stages in the ring
+constexpr int NB = KVQ_NUQ_NB;  // ring stages
+#ifndef KVQ_NUQ_LEAD
+#define KVQ_NUQ_LEAD 4
+#endif
+constexpr int LEAD = KVQ_NUQ_LEAD;  // blocks the aux warps may prepare ahead of the slowest consumer
+static_assert(LEAD >= 2 && LEAD < NB, "the ring must hold the lead plus the copies in flight");
+#ifndef KVQ_NUQ_PAIR
+#define KVQ_NUQ_PAIR 0
+#endif
 
 struct Args {
   Geo g;
@@ -44,30 +62,37 @@ struct Args {
   int nb;                 // cached blocks per (b, h)
   long long total;        // B * H * nb
   int n_ranges;           // CTAs in the grid
-  int n_slots;            // partial slots per (b, query head)
+  int n_slots;            // range slots per (b, query head)
   float* ws_m;
   float* ws_l;
   float* ws_o;
   int* status;
 };
 
-// Per-block operands shared by the 8 warps (double-buffered by block parity).
-struct Prep {
-  uint32_t bk[9][36];  // score B fragments of column g (16 k-groups x (high, low)), padded rows;
-                       // row 8 stays zero (read by the lanes whose B entries are zero)
-  float cz[4][36];     // zero-point terms (X, Y) of pair 4*kgroup + tq, per tq, padded rows
-  float qb[D];         // q rotated back by the block's start angle
+// Per-stage operands the aux warps prepare for the consumer warps.
+struct Ops {
+  uint32_t bk[9][20];  // score B fragments of column g (16 k-groups), padded rows; row 8 stays zero
+  float4 cz[4][17];    // zero-point terms (X, Y, X, Y) of pair 4*kgroup + tq, per tq, padded rows
+  float sk[T];         // key-outlier score term per token
 };
 
 struct Smem {
-  float2 rope_loc[T * 64];  // (cos, sin) of t * theta_i, t = 0..127 (for the key outliers)
-  Prep prep[2];
-  float q[D];               // query of the current (b, h), times log2(e)/sqrt(128)
-  float outv[NW][D];        // value outliers weighted by p, per warp
-  float red_o[NW][D];       // per-warp outputs at a segment end
-  float red_ml[NW][2];
-  uint64_t bar[NB];
+  float2 rope_loc[T * 64];  // (cos, sin) of t * theta_i, t = 0..127
+  Ops op[NB];
+  float qb[2][D];           // aux: q rotated back by the block's start angle (by block parity)
+  float outv[NW][D];        // value outliers weighted by p, per consumer warp
+  uint64_t rec_full[NB];    // record and RoPE row landed (bulk copies)
+  uint64_t ops_full[NB];    // score operands and outlier terms ready (NAUX arrivals)
+  uint64_t done[NB];        // the consumer warps are done with the stage (NW arrivals)
+  // followed by NB x round16(n_outliers) bytes: the token of each value outlier, per stage
 };
+
+__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0, const float (&c)[4]) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%8,%9,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1, const float (&c)[4]) {
@@ -78,7 +103,7 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
 }
 
-// Nibble word u of a lane's 6-word code group: 8 codes in 4-bit slots (bit 3 of each slot clear),
+// Nibble word U of a lane's 6-word code group: 8 codes in 4-bit slots (bit 3 of each slot clear),
 // ready to serve as byte-permute selectors (low 16 bits: slots 0..3, high 16 bits: slots 4..7).
 __device__ __forceinline__ uint32_t nibble_word(const uint32_t (&w)[6], const int U) {  // U: unrolled
   const uint32_t L = w[U >> 1], H = w[4 + (U >> 2)];
@@ -87,13 +112,19 @@ __device__ __forceinline__ uint32_t nibble_word(const uint32_t (&w)[6], const in
   return (lo & 0x33333333u) | (hi & 0x44444444u);
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+  return d;
+}
+
 // Codebook values of the 4 codes selected by sel[15:0] as two fp16 pairs: (slot 0, slot 1) and
 // (slot 2, slot 3). tl/th: low and high bytes of the 8 fp16 entries.
 __device__ __forceinline__ void lookup4(uint32_t sel, uint32_t tl0, uint32_t tl1, uint32_t th0, uint32_t th1,
                                         uint32_t& p01, uint32_t& p23) {
-  const uint32_t lo = __byte_perm(tl0, tl1, sel), hi = __byte_perm(th0, th1, sel);
-  p01 = __byte_perm(lo, hi, 0x5140);
-  p23 = __byte_perm(lo, hi, 0x7362);
+  const uint32_t lo = prmt(tl0, tl1, sel), hi = prmt(th0, th1, sel);
+  p01 = prmt(lo, hi, 0x5140u);
+  p23 = prmt(lo, hi, 0x7362u);
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
@@ -105,255 +136,327 @@ __host__ __device__ inline long long range_of(long long x, long long total, long
   return ((x + 1) * N - 1) / total;
 }
 
+// Query of (b, h) pairs lane and lane+32, scaled by log2(e)/sqrt(128).
+__device__ __forceinline__ void load_q_pairs(const Args& a, long long u, int lane, float (&qv)[2][2]) {
+  const long long b = u / a.g.H, h = u - b * a.g.H;
+  const uint16_t* qp = a.q + ((uint64_t)(b * a.g.Hq + h)) * D;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int pi = lane + 32 * k;
+    qv[k][0] = load_in(qp + 2 * pi, a.g.in_bf16) * LOG2E_RSQRT_D;
+    qv[k][1] = load_in(qp + 2 * pi + 1, a.g.in_bf16) * LOG2E_RSQRT_D;
+  }
+}
+
+// __syncthreads_or over the NAUX aux threads (named barrier 1).
+__device__ __forceinline__ bool syncthreads_or_aux(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ uint32_t stage_bytes(const Geo& g) { return (uint32_t)g.rec_bytes + ROPE_ROW; }
+
+// Aux warps (4 warps, 128 threads, named barrier 1). Lanes 0..2 of the first issue the copies
+// (K half, V half, RoPE start-angle row of each record) up to NBS - LEAD blocks ahead of the block
+// being prepared; a stage is reused once the consumer warps have signalled `done` for its
+// previous block. Per block, threads 0..63 build the score operands of channel pair ax (B
+// fragments, zero-point C tuples), threads 64..127 q_b of pair ax - 64; then thread ax handles
+// token ax: its key-outlier score term
+//     sk[t] = sum over the token's CSR entries (c, v) of v * (R(t)^T q_b)_c,
+// and the token tag of each of its value-outlier entries (the consumers scatter p_t * v).
 template <int NBS>
-__global__ void __launch_bounds__(NT, 1) decode_nuq_kernel(Args a) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
+__device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows, int rows_stride, long long x0,
+                          int n, int ax) {
   const Geo& g = a.g;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gq = lane >> 2, tq = lane & 3;
-  const uint32_t rec = (uint32_t)g.rec_bytes;
-  uint8_t* ring = smem_raw;
-  Smem* sm = reinterpret_cast<Smem*>(smem_raw + (size_t)NBS * rec);
-
-  const long long R = blockIdx.x;
-  if (R >= a.n_ranges) return;
-  const long long x0 = R * a.total / a.n_ranges, x1 = (R + 1) * a.total / a.n_ranges;
-  const int n = (int)(x1 - x0);
-  if (n <= 0) return;
-
-  const float2* rope_blk = reinterpret_cast<const float2*>(a.base + g.rope_off);
-  const float2* rope_loc = rope_blk + (size_t)(g.max_blocks + 1) * 64;
-
+  const uint32_t rec = (uint32_t)g.rec_bytes, sb = stage_bytes(g), khalf = g.codes_off[1];
+  const int n_out = g.n_out;
+  const int lane = ax & 31;
+  const bool copier = ax < 32;  // warp 0 of the group issues the copies (lane 0)
   long long u = x0 / a.nb;
   int blk = (int)(x0 - u * a.nb);
-  // producer state (thread 0): next record to copy
-  int pnext = 0, pbuf = 0, pblk = blk;
-  const uint8_t* psrc = a.base + ((uint64_t)u * g.max_blocks + (uint64_t)blk) * g.rec_bytes;
-  auto issue_next = [&]() {
-    if (pnext >= n) return;
-    mbar_arrive_expect_tx(&sm->bar[pbuf], rec);
-    bulk_g2s(ring + (size_t)pbuf * rec, psrc, rec, &sm->bar[pbuf]);
-    ++pnext;
-    if (++pbuf == NBS) pbuf = 0;
-    if (++pblk == a.nb) {
-      pblk = 0;
-      psrc += (uint64_t)(g.max_blocks - a.nb + 1) * g.rec_bytes;
-    } else {
-      psrc += g.rec_bytes;
+  int issued = 0, cblk = blk;
+  const uint8_t* csrc = a.base + ((uint64_t)u * g.max_blocks + (uint64_t)blk) * g.rec_bytes;
+  const uint8_t* rope_blk = a.base + g.rope_off;
+  auto bar_aux = []() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
+  auto issue = [&]() -> bool {  // warp 0: the next copy, once its stage is free; false on a timeout
+    const int s = issued % NBS;
+    if (issued >= NBS) {
+      const bool got = mbar_wait_bounded(&sm->done[s], (uint32_t)(((issued / NBS) - 1) & 1), a.status);
+      if (__any_sync(0xffffffffu, !got)) return false;
     }
+    // Each issuing thread streams its bulk copies one after another, so the K half, the V half and
+    // the RoPE row of a record go out from three lanes.
+    if (lane == 0) mbar_arrive_expect_tx(&sm->rec_full[s], rec + ROPE_ROW);
+    __syncwarp();
+    if (lane < 3) {
+      fence_proxy_async();
+      uint8_t* dst = ring + (size_t)s * sb;
+      if (lane == 0) bulk_g2s(dst, csrc, khalf, &sm->rec_full[s]);
+      else if (lane == 1) bulk_g2s(dst + khalf, csrc + khalf, rec - khalf, &sm->rec_full[s]);
+      else bulk_g2s(dst + rec, rope_blk + (size_t)cblk * ROPE_ROW, ROPE_ROW, &sm->rec_full[s]);
+    }
+    ++issued;
+    if (++cblk == a.nb) {
+      cblk = 0;
+      csrc += (uint64_t)(g.max_blocks - a.nb + 1) * g.rec_bytes;
+    } else {
+      csrc += g.rec_bytes;
+    }
+    return true;
   };
-  if (tid == 0) {
-    for (int s = 0; s < NBS; ++s) mbar_init(&sm->bar[s], 1);
-    fence_mbar_init();
-    fence_proxy_async();
-    for (int s = 0; s < NBS; ++s) issue_next();
-  }
+  bool ok = true;
+  if (copier)
+    while (ok && issued < n && issued < NBS) ok = issue();
 
-  // the in-block angle table, staged once per CTA
-  {
-    const float4* src = reinterpret_cast<const float4*>(rope_loc);
-    float4* dst = reinterpret_cast<float4*>(sm->rope_loc);
-    for (int e = tid; e < T * 32; e += NT) dst[e] = __ldg(src + e);
+  long long cur_u = -1;
+  const int pi = ax & 63;  // this thread's channel pair
+  float q0 = 0.0f, q1 = 0.0f;
+  for (int p = 0; p < n; ++p) {
+    if (u != cur_u) {
+      cur_u = u;
+      const long long b = u / g.H, h = u - b * g.H;
+      const uint16_t* qp = a.q + ((uint64_t)(b * g.Hq + h)) * D;
+      q0 = load_in(qp + 2 * pi, g.in_bf16) * LOG2E_RSQRT_D;
+      q1 = load_in(qp + 2 * pi + 1, g.in_bf16) * LOG2E_RSQRT_D;
+    }
+    const int s = p % NBS;
+    const bool got = ok && mbar_wait_bounded(&sm->rec_full[s], (uint32_t)((p / NBS) & 1), a.status);
+    if (syncthreads_or_aux(!got)) {
+      ok = false;
+      break;
+    }
+    const uint8_t* st = ring + (size_t)s * sb;
+    Ops& op = sm->op[s];
+    float* qb = sm->qb[p & 1];
+    {
+      const float2 cs = reinterpret_cast<const float2*>(st + rec)[pi];
+      const float qb0 = cs.x * q0 + cs.y * q1, qb1 = -cs.y * q0 + cs.x * q1;
+      if (ax < 64) {
+        const uint16_t* km = reinterpret_cast<const uint16_t*>(st + g.meta_off[0]);
+        const int kg = pi >> 2, tqp = pi & 3;
+        const float s0 = h2f(km[2 * pi]), s1 = h2f(km[2 * pi + 1]);
+        const float z0 = h2f(km[T + 2 * pi]), z1 = h2f(km[T + 2 * pi + 1]);
+        op.bk[2 * tqp][kg] = pack_h2(qb0 * s0, qb1 * s1);       // X column of pair pi
+        op.bk[2 * tqp + 1][kg] = pack_h2(qb1 * s0, -qb0 * s1);  // Y column
+        const float zx = qb0 * z0 + qb1 * z1, zy = qb1 * z0 - qb0 * z1;
+        op.cz[tqp][kg] = make_float4(zx, zy, zx, zy);
+      } else {
+        *reinterpret_cast<float2*>(&qb[2 * pi]) = make_float2(qb0, qb1);
+      }
+    }
+    float skt = 0.0f;
+    if (n_out > 0) {
+      bar_aux();  // q_b visible
+      const int t = ax;
+      const uint8_t* csr = st + g.csr_off[0];
+      const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
+      const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * n_out);
+      const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
+      const int e1 = min((int)rp[t + 1], n_out);
+      for (int e = min((int)rp[t], n_out); e < e1; ++e) {  // keys
+        const int c = col[e] & (D - 1);
+        const float2 cr = sm->rope_loc[t * 64 + (c >> 1)];
+        const float qa = qb[c & ~1], qc = qb[c | 1];
+        const float qq = (c & 1) ? (-cr.y * qa + cr.x * qc) : (cr.x * qa + cr.y * qc);
+        skt = fmaf(h2f(val[e]), qq, skt);
+      }
+      const uint16_t* rpv = reinterpret_cast<const uint16_t*>(st + g.csr_off[1] + 2 * n_out);
+      uint8_t* rw = rows + (size_t)s * rows_stride;
+      const int f1 = min((int)rpv[t + 1], n_out);
+      for (int e = min((int)rpv[t], n_out); e < f1; ++e) rw[e] = (uint8_t)t;  // values: token tags
+    }
+    op.sk[ax] = skt;
+    mbar_arrive(&sm->ops_full[s]);  // NAUX arrivals complete the phase
+    if (++blk == a.nb) {
+      blk = 0;
+      ++u;
+    }
+    if (copier)
+      while (ok && issued < n && issued <= p + NBS - LEAD) ok = issue();
   }
+  // leave no copy in flight: wait (bounded) for the copies not yet seen complete
+  if (copier && !ok) {
+    for (int j = issued - NBS; j < issued; ++j)
+      if (j >= 0) mbar_wait_bounded(&sm->rec_full[j % NBS], (uint32_t)((j / NBS) & 1), nullptr, 200000000LL);
+  }
+}
+
+// Scores of a consumer warp's 16 tokens in one block (after the reduction over the 4 lanes of a
+// token and the key-outlier terms): s0 for token 16w + gq, s1 for token 16w + gq + 8.
+__device__ __forceinline__ void block_scores(const uint8_t* st, const Ops& op, uint32_t codes_off, int warp, int lane,
+                                             int brow, int tq, int t0, int t1, uint32_t tl0, uint32_t tl1,
+                                             uint32_t th0, uint32_t th1, const float (&wc)[2][16],
+                                             const float (&ws)[2][16], float& s0, float& s1) {
+  uint32_t cw[6];
+  const uint2* kp = reinterpret_cast<const uint2*>(st + codes_off + warp * 768 + lane * 24);
+  const uint2 k0 = kp[0], k1 = kp[1], k2 = kp[2];
+  cw[0] = k0.x; cw[1] = k0.y; cw[2] = k1.x; cw[3] = k1.y; cw[4] = k2.x; cw[5] = k2.y;
+  const uint4* bp = reinterpret_cast<const uint4*>(&op.bk[brow][0]);
+  float sc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}}, ss[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+#pragma unroll
+  for (int uu = 0; uu < 8; ++uu) {
+    const uint32_t nw = nibble_word(cw, uu);
+    const uint4 bq = bp[uu >> 1];  // k-groups 4(uu/2) .. 4(uu/2)+3
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+      const int kg = 2 * uu + hf;
+      uint32_t a0, a1;
+      lookup4(hf ? (nw >> 16) : nw, tl0, tl1, th0, th1, a0, a1);
+      const float4 z = op.cz[tq][kg];
+      const float c4[4] = {z.x, z.y, z.z, z.w};
+      const uint32_t bb = (kg & 3) == 0 ? bq.x : (kg & 3) == 1 ? bq.y : (kg & 3) == 2 ? bq.z : bq.w;
+      float d[4];
+      mma1688(d, a0, a1, bb, c4);
+      sc[0][hf] = fmaf(wc[0][kg], d[0], sc[0][hf]);
+      ss[0][hf] = fmaf(ws[0][kg], d[1], ss[0][hf]);
+      sc[1][hf] = fmaf(wc[1][kg], d[2], sc[1][hf]);
+      ss[1][hf] = fmaf(ws[1][kg], d[3], ss[1][hf]);
+    }
+  }
+  s0 = (sc[0][0] + sc[0][1]) + (ss[0][0] + ss[0][1]);
+  s1 = (sc[1][0] + sc[1][1]) + (ss[1][0] + ss[1][1]);
+  s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+  s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+  s0 += __shfl_xor_sync(0xffffffffu, s0, 2) + op.sk[t0];
+  s1 += __shfl_xor_sync(0xffffffffu, s1, 2) + op.sk[t1];
+}
+
+// Value part of one block for a consumer warp: p' = p * s_token as high/low B columns, the
+// zero-point sum, the value outliers (entry e of the warp's token range goes to lane e mod 32,
+// which takes p of its token from the token's owner lane) and 8 m16n8k16 over the V codes.
+__device__ __forceinline__ void block_values(const uint8_t* st, const Geo& g, const uint8_t* rw, int warp, int lane,
+                                             int t0, int t1, int src_a, uint32_t xsel, uint32_t ysel, float p0,
+                                             float p1, uint32_t tl0, uint32_t tl1, uint32_t th0, uint32_t th1,
+                                             float* outv, float& z_w, float (&acc)[8][4]) {
+  const uint16_t* vm = reinterpret_cast<const uint16_t*>(st + g.meta_off[1]);
+  uint32_t vb0, vb1;
+  {
+    const float pp0 = p0 * h2f(vm[t0]), pp1 = p1 * h2f(vm[t1]);
+    z_w = fmaf(p0, h2f(vm[T + t0]), fmaf(p1, h2f(vm[T + t1]), z_w));
+    const __half h0 = __float2half_rn(pp0), h1 = __float2half_rn(pp1);
+    const uint32_t hi = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
+    const uint32_t lo = pack_h2(pp0 - __half2float(h0), pp1 - __half2float(h1));
+    const uint32_t x = (hi & xsel) | (lo & ysel);
+    vb0 = __shfl_sync(0xffffffffu, x, src_a);
+    vb1 = __shfl_sync(0xffffffffu, x, src_a + 16);
+  }
+  const int n_out = g.n_out;
+  if (n_out > 0) {
+    const uint8_t* csr = st + g.csr_off[1];
+    const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
+    const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * n_out);
+    const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
+    const int e0 = min((int)rp[16 * warp], n_out), e1 = min((int)rp[16 * warp + 16], n_out);
+    for (int e = e0 + lane; e - lane < e1; e += 32) {  // uniform trip count
+      const bool valid = e < e1;
+      const int t = valid ? rw[e] : t0;
+      const int src = 4 * (t & 7);
+      const float pa = __shfl_sync(0xffffffffu, p0, src), pb = __shfl_sync(0xffffffffu, p1, src);
+      if (valid) atomicAdd(&outv[col[e] & (D - 1)], ((t & 8) ? pb : pa) * h2f(val[e]));
+    }
+  }
+  uint32_t cw[6];
+  const uint2* vp = reinterpret_cast<const uint2*>(st + g.codes_off[1] + warp * 768 + lane * 24);
+  const uint2 v0 = vp[0], v1 = vp[1], v2 = vp[2];
+  cw[0] = v0.x; cw[1] = v0.y; cw[2] = v1.x; cw[3] = v1.y; cw[4] = v2.x; cw[5] = v2.y;
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    const uint32_t nw = nibble_word(cw, mt);
+    uint32_t a0, a1, a2, a3;
+    lookup4(nw, tl0, tl1, th0, th1, a0, a1);
+    lookup4(nw >> 16, tl0, tl1, th0, th1, a2, a3);
+    mma16816(acc[mt], a0, a1, a2, a3, vb0, vb1, acc[mt]);
+  }
+}
+
+// Consumer warp w: tokens 16w..16w+15 of every block of the CTA's range, two blocks of the same
+// (b, h) at a time where it can (their scores feed one softmax update). Its flash-decode state
+// goes to its own partial row at the end of each (b, h) segment.
+template <int NBS>
+__device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uint8_t* rows, int rows_stride,
+                         long long R, long long x0, int n, int warp, int lane) {
+  const Geo& g = a.g;
+  const uint32_t sb = stage_bytes(g);
+  const int gq = lane >> 2, tq = lane & 3;
   // cos/sin of the lane's (token, pair) cells: tokens 16w + gq + 8r, pairs 4kg + tq
   float wc[2][16], ws[2][16];
 #pragma unroll
   for (int r = 0; r < 2; ++r)
 #pragma unroll
     for (int kg = 0; kg < 16; ++kg) {
-      const float2 cs = __ldg(rope_loc + (16 * warp + gq + 8 * r) * 64 + 4 * kg + tq);
+      const float2 cs = sm->rope_loc[(16 * warp + gq + 8 * r) * 64 + 4 * kg + tq];
       wc[r][kg] = cs.x;
       ws[r][kg] = cs.y;
     }
-  // the block-start angle of the prep's channel pair, loaded one block ahead
-  const int prep_pair = tid >> 2;
-  float2 cs_next = __ldg(rope_blk + (size_t)blk * 64 + prep_pair);
   const int brow = (gq >> 1) == tq ? gq : 8;             // lanes holding nonzero score B entries
-  for (int e = tid; e < 2 * 36; e += NT) sm->prep[e / 36].bk[8][e % 36] = 0u;
   const int src_a = 4 * tq + (gq < 2 ? gq : 2);          // value B: (high, low, zero) source lanes
   const uint32_t xsel = tq == 0 ? 0xffffffffu : 0u;      // this lane sends p' high (tq 0) ...
   const uint32_t ysel = tq == 1 ? 0xffffffffu : 0u;      // ... or low (tq 1) or zero
+  const int t0 = 16 * warp + gq, t1 = t0 + 8;
 
+  long long u = x0 / a.nb;
+  int blk = (int)(x0 - u * a.nb);
   uint32_t tl0 = 0, tl1 = 0, th0 = 0, th1 = 0;
   float acc[8][4];
   float m_w = -INFINITY, l_w = 0.0f, z_w = 0.0f;
   long long cur_u = -1;
-  bool ok = true;
-  int failed_at = n;
+  float* outv = sm->outv[warp];
 
   auto flush = [&](long long uu) {
-    // per-warp totals over its 16 tokens (l, z replicated over tq: reduce over gq only)
-    float lt = l_w, zt = z_w;
+    float lt = l_w, zt = z_w;  // replicated over tq: reduce over gq only
 #pragma unroll
     for (int o = 4; o < 32; o <<= 1) {
       lt += __shfl_xor_sync(0xffffffffu, lt, o);
       zt += __shfl_xor_sync(0xffffffffu, zt, o);
     }
     __syncwarp();
-    if (tq == 0) {
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int c0 = 16 * mt + gq, c1 = c0 + 8;
-        sm->red_o[warp][c0] = acc[mt][0] + acc[mt][1] + zt + sm->outv[warp][c0];
-        sm->red_o[warp][c1] = acc[mt][2] + acc[mt][3] + zt + sm->outv[warp][c1];
-      }
-    }
-    if (lane == 0) {
-      sm->red_ml[warp][0] = m_w;
-      sm->red_ml[warp][1] = lt;
-    }
-    __syncthreads();
     const long long b = uu / g.H, h = uu - b * g.H;
     const long long slot = R - range_of(uu * a.nb, a.total, a.n_ranges);
-    if (tid < D && slot >= 0 && slot < a.n_slots) {
-      float M = -INFINITY;
+    if (slot >= 0 && slot < a.n_slots) {
+      const uint64_t row = (((uint64_t)(b * g.Hq + h)) * a.n_slots + slot) * NW + warp;
+      if (tq == 0) {
 #pragma unroll
-      for (int w = 0; w < NW; ++w) M = fmaxf(M, sm->red_ml[w][0]);
-      float L = 0.0f, O = 0.0f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        const float f = exp2f(sm->red_ml[w][0] - M);
-        L = fmaf(sm->red_ml[w][1], f, L);
-        O = fmaf(sm->red_o[w][tid], f, O);
+        for (int mt = 0; mt < 8; ++mt) {
+          const int c0 = 16 * mt + gq, c1 = c0 + 8;
+          a.ws_o[row * D + c0] = acc[mt][0] + acc[mt][1] + zt + outv[c0];
+          a.ws_o[row * D + c1] = acc[mt][2] + acc[mt][3] + zt + outv[c1];
+        }
       }
-      const uint64_t row = ((uint64_t)(b * g.Hq + h)) * a.n_slots + slot;
-      a.ws_o[row * D + tid] = O;
-      if (tid == 0) {
-        a.ws_m[row] = M;
-        a.ws_l[row] = L;
+      if (lane == 0) {
+        a.ws_m[row] = m_w;
+        a.ws_l[row] = lt;
       }
     }
-    __syncthreads();
+    __syncwarp();
   };
 
-  for (int i = 0; i < n; ++i) {
-    if (u != cur_u) {
-      if (cur_u >= 0) flush(cur_u);
-      cur_u = u;
-      const long long b = u / g.H, h = u - b * g.H;
-      if (tid < D) sm->q[tid] = load_in(a.q + ((uint64_t)(b * g.Hq + h)) * D + tid, g.in_bf16) * LOG2E_RSQRT_D;
-      {
-        uint32_t hb[8];
+  // Blocks i .. i+NBK-1 (same (b, h)); false when a wait gave up.
+  auto step = [&](int i, auto nbk) -> bool {
+    constexpr int NBK = decltype(nbk)::value;
+    int sidx[NBK];
+    bool got = true;
 #pragma unroll
-        for (int j = 0; j < 8; ++j) hb[j] = f2h_rn(__ldg(a.codebook + h * 8 + j));
-        tl0 = (hb[0] & 0xffu) | (hb[1] & 0xffu) << 8 | (hb[2] & 0xffu) << 16 | (hb[3] & 0xffu) << 24;
-        tl1 = (hb[4] & 0xffu) | (hb[5] & 0xffu) << 8 | (hb[6] & 0xffu) << 16 | (hb[7] & 0xffu) << 24;
-        th0 = (hb[0] >> 8) | (hb[1] >> 8) << 8 | (hb[2] >> 8) << 16 | (hb[3] >> 8) << 24;
-        th1 = (hb[4] >> 8) | (hb[5] >> 8) << 8 | (hb[6] >> 8) << 16 | (hb[7] >> 8) << 24;
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) sm->outv[warp][lane + 32 * k] = 0.0f;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
-      m_w = -INFINITY;
-      l_w = 0.0f;
-      z_w = 0.0f;
-      __syncthreads();  // the query is visible to the block preparation
+    for (int k = 0; k < NBK; ++k) {
+      sidx[k] = (i + k) % NBS;
+      const uint32_t par = (uint32_t)(((i + k) / NBS) & 1);
+      got = got && mbar_wait_bounded(&sm->ops_full[sidx[k]], par, a.status) &&
+            mbar_wait_bounded(&sm->rec_full[sidx[k]], par, a.status);
     }
-
-    // ---- wait for the record; prepare the block's score operands (all 256 threads)
-    const int slot_i = i % NBS;
-    const bool got = mbar_wait_bounded(&sm->bar[slot_i], (uint32_t)((i / NBS) & 1), a.status);
-    const uint8_t* st = ring + (size_t)slot_i * rec;
-    Prep& pr = sm->prep[i & 1];
-    if (got) {
-      const uint16_t* km = reinterpret_cast<const uint16_t*>(st + g.meta_off[0]);
-      const int pi = prep_pair, sub = tid & 3, kg = pi >> 2, tqp = pi & 3;
-      const float2 cs = cs_next;
-      const float q0 = sm->q[2 * pi], q1 = sm->q[2 * pi + 1];
-      const float qb0 = cs.x * q0 + cs.y * q1, qb1 = -cs.y * q0 + cs.x * q1;
-      if (sub < 2) {
-        const float s0 = h2f(km[2 * pi]), s1 = h2f(km[2 * pi + 1]);
-        const float v0 = sub == 0 ? qb0 * s0 : qb1 * s0;
-        const float v1 = sub == 0 ? qb1 * s1 : -qb0 * s1;
-        const __half h0 = __float2half_rn(v0), h1 = __float2half_rn(v1);
-        const float r0 = v0 - __half2float(h0), r1 = v1 - __half2float(h1);
-        uint32_t* dst = &pr.bk[2 * tqp + sub][2 * kg];
-        dst[0] = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-        dst[1] = pack_h2(r0, r1);
-      } else if (sub == 2) {
-        const float z0 = h2f(km[T + 2 * pi]), z1 = h2f(km[T + 2 * pi + 1]);
-        pr.cz[tqp][2 * kg] = qb0 * z0 + qb1 * z1;
-        pr.cz[tqp][2 * kg + 1] = qb1 * z0 - qb0 * z1;
-      } else {
-        pr.qb[2 * pi] = qb0;
-        pr.qb[2 * pi + 1] = qb1;
-      }
-    }
-    if (__syncthreads_or(!got)) {  // every thread leaves together
-      ok = false;
-      failed_at = i;
-      break;
-    }
-    if (tid == 0 && i > 0) {  // every thread is done with block i-1: refill its stage
-      fence_proxy_async();
-      issue_next();
-    }
-    if (i + 1 < n) cs_next = __ldg(rope_blk + (size_t)(blk + 1 == a.nb ? 0 : blk + 1) * 64 + prep_pair);
-
-    // ---- scores of the warp's 16 tokens
-    float s0 = 0.0f, s1 = 0.0f;
-    {
-      uint32_t cw[6];
-      const uint2* kp = reinterpret_cast<const uint2*>(st + g.codes_off[0] + warp * 768 + lane * 24);
-      const uint2 k0 = kp[0], k1 = kp[1], k2 = kp[2];
-      cw[0] = k0.x; cw[1] = k0.y; cw[2] = k1.x; cw[3] = k1.y; cw[4] = k2.x; cw[5] = k2.y;
-      uint32_t bf[32];
-      {
-        const uint4* bp = reinterpret_cast<const uint4*>(&pr.bk[brow][0]);
+    if (__any_sync(0xffffffffu, !got)) return false;  // the aux warps drain the copies in flight
+    float sv[NBK][2];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          const uint4 v = bp[j];
-          bf[4 * j] = v.x; bf[4 * j + 1] = v.y; bf[4 * j + 2] = v.z; bf[4 * j + 3] = v.w;
-        }
-      }
-      const float4* cp = reinterpret_cast<const float4*>(&pr.cz[tq][0]);
+    for (int k = 0; k < NBK; ++k)
+      block_scores(ring + (size_t)sidx[k] * sb, sm->op[sidx[k]], g.codes_off[0], warp, lane, brow, tq, t0, t1, tl0,
+                   tl1, th0, th1, wc, ws, sv[k][0], sv[k][1]);
+    // online softmax over the NBK blocks' tokens of this warp (base 2)
+    float mloc = fmaxf(sv[0][0], sv[0][1]);
 #pragma unroll
-      for (int uu = 0; uu < 8; ++uu) {
-        const uint32_t nw = nibble_word(cw, uu);
-        const float4 z = cp[uu];  // (ZX, ZY) of k-groups 2uu and 2uu+1
-#pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int kg = 2 * uu + hf;
-          uint32_t a0, a1;
-          lookup4(hf ? (nw >> 16) : nw, tl0, tl1, th0, th1, a0, a1);
-          const float c4[4] = {hf ? z.z : z.x, hf ? z.w : z.y, hf ? z.z : z.x, hf ? z.w : z.y};
-          float d[4];
-          mma16816(d, a0, a1, a0, a1, bf[2 * kg], bf[2 * kg + 1], c4);
-          s0 = fmaf(wc[0][kg], d[0], fmaf(ws[0][kg], d[1], s0));
-          s1 = fmaf(wc[1][kg], d[2], fmaf(ws[1][kg], d[3], s1));
-        }
-      }
-    }
-    // key outliers of the warp's tokens: entries split over the 4 lanes of each token
-    const int t0 = 16 * warp + gq, t1 = t0 + 8;
-    if (g.n_out > 0) {
-      const uint8_t* csr = st + g.csr_off[0];
-      const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
-      const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * g.n_out);
-      const uint8_t* col = csr + 2 * g.n_out + 2 * (T + 1);
-#pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int t = r ? t1 : t0;
-        const int j1 = min((int)rp[t + 1], g.n_out);
-        float add = 0.0f;
-        for (int j = min((int)rp[t], g.n_out) + tq; j < j1; j += 4) {
-          const int c = col[j] & (D - 1);
-          const float2 cs = sm->rope_loc[t * 64 + (c >> 1)];
-          const float qa = pr.qb[c & ~1], qc = pr.qb[c | 1];
-          const float qq = (c & 1) ? (-cs.y * qa + cs.x * qc) : (cs.x * qa + cs.y * qc);
-          add = fmaf(h2f(val[j]), qq, add);
-        }
-        if (r) s1 += add; else s0 += add;
-      }
-    }
-    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-
-    // ---- online softmax over the warp's tokens (base 2)
-    float mloc = fmaxf(s0, s1);
+    for (int k = 1; k < NBK; ++k) mloc = fmaxf(mloc, fmaxf(sv[k][0], sv[k][1]));
     mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
     mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
     mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
@@ -367,75 +470,96 @@ __global__ void __launch_bounds__(NT, 1) decode_nuq_kernel(Args a) {
       z_w *= al;
       __syncwarp();
 #pragma unroll
-      for (int k = 0; k < 4; ++k) sm->outv[warp][lane + 32 * k] *= al;
+      for (int k = 0; k < 4; ++k) outv[lane + 32 * k] *= al;
       __syncwarp();
       m_w = mloc;
     }
-    const float p0 = exp2f(s0 - m_w), p1 = exp2f(s1 - m_w);
-    l_w += p0 + p1;
-
-    // ---- value B fragments: p' = p * s_token, high and low fp16 columns
-    const uint16_t* vm = reinterpret_cast<const uint16_t*>(st + g.meta_off[1]);
-    uint32_t vb0, vb1;
-    {
-      const float pp0 = p0 * h2f(vm[t0]), pp1 = p1 * h2f(vm[t1]);
-      z_w = fmaf(p0, h2f(vm[T + t0]), fmaf(p1, h2f(vm[T + t1]), z_w));
-      const __half h0 = __float2half_rn(pp0), h1 = __float2half_rn(pp1);
-      const uint32_t hi = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
-      const uint32_t lo = pack_h2(pp0 - __half2float(h0), pp1 - __half2float(h1));
-      const uint32_t x = (hi & xsel) | (lo & ysel);
-      vb0 = __shfl_sync(0xffffffffu, x, src_a);
-      vb1 = __shfl_sync(0xffffffffu, x, src_a + 16);
-    }
-    // value outliers of the warp's tokens, weighted by p
-    if (g.n_out > 0) {
-      const uint8_t* csr = st + g.csr_off[1];
-      const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
-      const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * g.n_out);
-      const uint8_t* col = csr + 2 * g.n_out + 2 * (T + 1);
 #pragma unroll
-      for (int r = 0; r < 2; ++r) {
-        const int t = r ? t1 : t0;
-        const float p = r ? p1 : p0;
-        const int j1 = min((int)rp[t + 1], g.n_out);
-        for (int j = min((int)rp[t], g.n_out) + tq; j < j1; j += 4)
-          atomicAdd(&sm->outv[warp][col[j] & (D - 1)], p * h2f(val[j]));
-      }
+    for (int k = 0; k < NBK; ++k) {
+      const float p0 = exp2f(sv[k][0] - m_w), p1 = exp2f(sv[k][1] - m_w);
+      l_w += p0 + p1;
+      block_values(ring + (size_t)sidx[k] * sb, g, rows + (size_t)sidx[k] * rows_stride, warp, lane, t0, t1, src_a,
+                   xsel, ysel, p0, p1, tl0, tl1, th0, th1, outv, z_w, acc);
     }
-
-    // ---- outputs: 8 m-tiles of 16 channels x the warp's 16 tokens
-    {
-      uint32_t cw[6];
-      const uint2* vp = reinterpret_cast<const uint2*>(st + g.codes_off[1] + warp * 768 + lane * 24);
-      const uint2 v0 = vp[0], v1 = vp[1], v2 = vp[2];
-      cw[0] = v0.x; cw[1] = v0.y; cw[2] = v1.x; cw[3] = v1.y; cw[4] = v2.x; cw[5] = v2.y;
+    __syncwarp();
+    if (lane == 0) {
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const uint32_t nw = nibble_word(cw, mt);
-        uint32_t a0, a1, a2, a3;
-        lookup4(nw, tl0, tl1, th0, th1, a0, a1);
-        lookup4(nw >> 16, tl0, tl1, th0, th1, a2, a3);
-        mma16816(acc[mt], a0, a1, a2, a3, vb0, vb1, acc[mt]);
-      }
+      for (int k = 0; k < NBK; ++k) mbar_arrive(&sm->done[sidx[k]]);  // this warp is done with the stages
     }
-    if (++blk == a.nb) {
+    return true;
+  };
+
+  int i = 0;
+  while (i < n) {
+    if (u != cur_u) {
+      if (cur_u >= 0) flush(cur_u);
+      cur_u = u;
+      const long long h = u % g.H;
+      uint32_t hb[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) hb[j] = f2h_rn(__ldg(a.codebook + h * 8 + j));
+      tl0 = (hb[0] & 0xffu) | (hb[1] & 0xffu) << 8 | (hb[2] & 0xffu) << 16 | (hb[3] & 0xffu) << 24;
+      tl1 = (hb[4] & 0xffu) | (hb[5] & 0xffu) << 8 | (hb[6] & 0xffu) << 16 | (hb[7] & 0xffu) << 24;
+      th0 = (hb[0] >> 8) | (hb[1] >> 8) << 8 | (hb[2] >> 8) << 16 | (hb[3] >> 8) << 24;
+      th1 = (hb[4] >> 8) | (hb[5] >> 8) << 8 | (hb[6] >> 8) << 16 | (hb[7] >> 8) << 24;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) outv[lane + 32 * k] = 0.0f;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+      m_w = -INFINITY;
+      l_w = 0.0f;
+      z_w = 0.0f;
+      __syncwarp();
+    }
+    const bool two = KVQ_NUQ_PAIR && i + 1 < n && blk + 1 < a.nb;  // the next block is in the same (b, h)
+    const bool ok = two ? step(i, std::integral_constant<int, 2>()) : step(i, std::integral_constant<int, 1>());
+    if (!ok) return;
+    const int adv = two ? 2 : 1;
+    i += adv;
+    blk += adv;
+    if (blk == a.nb) {
       blk = 0;
       ++u;
     }
   }
-
-  if (!ok) {  // drain the copies still in flight (bounded) before the CTA exits
-    if (tid == 0) {
-      for (int j = failed_at; j < pnext; ++j)
-        mbar_wait_bounded(&sm->bar[j % NBS], (uint32_t)((j / NBS) & 1), nullptr, 200000000LL);
-    }
-    __syncthreads();
-    return;
-  }
   if (cur_u >= 0) flush(cur_u);
 }
 
-size_t smem_bytes(const Geo& g) { return (size_t)NB * g.rec_bytes + sizeof(Smem); }
+template <int NBS>
+__global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint8_t* ring = smem_raw;
+  Smem* sm = reinterpret_cast<Smem*>(smem_raw + (size_t)NBS * stage_bytes(a.g));
+  uint8_t* rows = reinterpret_cast<uint8_t*>(sm + 1);
+  const int rows_stride = (int)round16((uint64_t)a.g.n_out);
+  const long long R = blockIdx.x;
+  if (R >= a.n_ranges) return;
+  const long long x0 = R * a.total / a.n_ranges, x1 = (R + 1) * a.total / a.n_ranges;
+  const int n = (int)(x1 - x0);
+  if (n <= 0) return;
+  {  // the in-block angle table, staged once per CTA
+    const float4* src = reinterpret_cast<const float4*>(a.base + a.g.rope_off) + (size_t)(a.g.max_blocks + 1) * 32;
+    float4* dst = reinterpret_cast<float4*>(sm->rope_loc);
+    for (int e = tid; e < T * 32; e += NTHREADS) dst[e] = __ldg(src + e);
+  }
+  for (int e = tid; e < NBS * 20; e += NTHREADS) sm->op[e / 20].bk[8][e % 20] = 0u;
+  if (tid == 0) {
+    for (int s = 0; s < NBS; ++s) {
+      mbar_init(&sm->rec_full[s], 1);
+      mbar_init(&sm->ops_full[s], NAUX);
+      mbar_init(&sm->done[s], NW);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (warp >= NW) aux_warps<NBS>(a, sm, ring, rows, rows_stride, x0, n, tid - NW * 32);
+  else consumer<NBS>(a, sm, ring, rows, rows_stride, R, x0, n, warp, lane);
+}
+
+size_t smem_bytes(const Geo& g) {
+  return (size_t)NB * ((size_t)g.rec_bytes + ROPE_ROW) + sizeof(Smem) + (size_t)NB * round16((uint64_t)g.n_out);
+}
 
 }  // namespace nuqdec
 }  // namespace kvq
@@ -453,7 +577,7 @@ thread_local NuqOcc t_nuq_occ[4];
 
 bool kvq_nuq_supported(const kvq::Geo& g) {
   return g.method == KVQ_NUQ && g.bits == 3 && g.G == 1 && g.pre_rope == 1 &&
-         kvq::nuqdec::smem_bytes(g) <= 227 * 1024;
+         g.n_out <= kvq::nuqdec::MAX_OUTLIERS && kvq::nuqdec::smem_bytes(g) <= 227 * 1024;
 }
 
 // CTAs (ranges) the nuq decode uses on the current device, or 0 if the path does not apply.
@@ -472,7 +596,8 @@ long long kvq_nuq_ranges(const kvq::Geo& g) {
     if (!hit) {
       cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       int occ = 0;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, NT, smem) != cudaSuccess || occ < 1) occ = 1;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, NTHREADS, smem) != cudaSuccess || occ < 1)
+        occ = 1;
       for (auto& c : t_nuq_occ)
         if (c.dev < 0 || &c == &t_nuq_occ[3]) {
           c.dev = dev; c.smem = smem; c.ctas = occ;
@@ -488,6 +613,10 @@ long long kvq_nuq_ranges(const kvq::Geo& g) {
   return (long long)sms * ctas;
 }
 
+// Partial rows each range writes per (b, query head): one per consumer warp.
+int kvq_nuq_parts_per_range() { return kvq::nuqdec::NW; }
+
+// slots: range slots per (b, query head); the workspace holds slots * NW partial rows each.
 cudaError_t kvq_launch_decode_nuq(const kvq::Geo& g, const uint8_t* base, const float* codebook, const uint16_t* q,
                                   int n_blocks, long long ranges, long long slots, float* ws_m, float* ws_l,
                                   float* ws_o, int* status, cudaStream_t st) {
@@ -500,6 +629,6 @@ cudaError_t kvq_launch_decode_nuq(const kvq::Geo& g, const uint8_t* base, const 
   a.g = g; a.base = base; a.codebook = codebook; a.q = q; a.nb = n_blocks;
   a.total = (long long)g.B * g.H * n_blocks; a.n_ranges = (int)ranges; a.n_slots = (int)slots;
   a.ws_m = ws_m; a.ws_l = ws_l; a.ws_o = ws_o; a.status = status;
-  fn<<<(int)ranges, NT, smem, st>>>(a);
+  fn<<<(int)ranges, NTHREADS, smem, st>>>(a);
   return cudaGetLastError();
 }
