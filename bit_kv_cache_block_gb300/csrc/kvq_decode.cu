@@ -355,13 +355,38 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
   }
 }
 
-__global__ void __launch_bounds__(DC_THREADS) combine_kernel(CombineArgs a) {
+constexpr int CB_THREADS = 512, CB_GROUPS = CB_THREADS / D;  // 4 thread groups of 128 channels
+
+// Block-wide reductions over CB_THREADS threads (red: CB_THREADS/32 floats of scratch).
+__device__ __forceinline__ float cb_max(float v, float* red) {
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = red[0];
+  for (int w = 1; w < CB_THREADS / 32; ++w) r = fmaxf(r, red[w]);
+  return r;
+}
+__device__ __forceinline__ float cb_sum(float v, float* red) {
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  __syncthreads();
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+  __syncthreads();
+  float r = 0.0f;
+  for (int w = 0; w < CB_THREADS / 32; ++w) r += red[w];
+  return r;
+}
+
+// grid (H_q, B), CB_THREADS threads: thread (grp, c) = (tid / 128, tid % 128).
+__global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
+  __shared__ float red[CB_THREADS / 32];
+  __shared__ float part[CB_GROUPS][D];
   __shared__ float ob[D];
   __shared__ float qv[D];
   __shared__ float sc[T];
-  __shared__ float red[DC_THREADS / 32];
+  __shared__ uint16_t tks[T - 1][D];  // tail keys (input dtype bits)
   const Geo& g = a.g;
-  const int c = threadIdx.x, lane = c & 31, warp = c >> 5;
+  const int tid = threadIdx.x, c = tid & (D - 1), grp = tid >> 7;
   const int hq = blockIdx.x, b = blockIdx.y, h = hq / g.G;
   const uint64_t row0 = ((uint64_t)b * g.Hq + hq) * a.n_split;
   int n_part = a.n_split;
@@ -373,75 +398,119 @@ __global__ void __launch_bounds__(DC_THREADS) combine_kernel(CombineArgs a) {
     if (n_part > a.n_split) n_part = a.n_split;
   }
 
-  float M = -INFINITY;
-  for (int s = 0; s < n_part; ++s) M = fmaxf(M, a.ws_m[row0 + s]);
-  float L = 0.0f, O = 0.0f;
-  for (int s = 0; s < n_part; ++s) {
-    float f = exp2f(a.ws_m[row0 + s] - M);
-    L += a.ws_l[row0 + s] * f;
-    O += a.ws_o[(row0 + s) * D + c] * f;
+  // ---- merge the partials: max over all, then group grp sums partials grp, grp+4, ...
+  float mm = -INFINITY;
+  for (int s = tid; s < n_part; s += CB_THREADS) mm = fmaxf(mm, a.ws_m[row0 + s]);
+  const float M = cb_max(mm, red);
+  float Lg = 0.0f, Og = 0.0f;
+  {
+    float Lp[2] = {0.0f, 0.0f}, Op[2] = {0.0f, 0.0f};
+    int s = grp;
+    for (; s + CB_GROUPS < n_part; s += 2 * CB_GROUPS) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint64_t r = row0 + s + k * CB_GROUPS;
+        const float f = exp2f(a.ws_m[r] - M);
+        Lp[k] = fmaf(a.ws_l[r], f, Lp[k]);
+        Op[k] = fmaf(a.ws_o[r * D + c], f, Op[k]);
+      }
+    }
+    if (s < n_part) {
+      const uint64_t r = row0 + s;
+      const float f = exp2f(a.ws_m[r] - M);
+      Lp[0] = fmaf(a.ws_l[r], f, Lp[0]);
+      Op[0] = fmaf(a.ws_o[r * D + c], f, Op[0]);
+    }
+    Lg = Lp[0] + Lp[1];
+    Og = Op[0] + Op[1];
   }
+  part[grp][c] = Og;
+  // L: the same value in every thread of a group; take channel 0 of each group
+  float L = cb_sum(c == 0 ? Lg : 0.0f, red);  // (also orders the part[] stores)
+  float O = (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
   if (g.method == KVQ_VARN && a.hadamard && n_part > 0) {
-    ob[c] = O;
+    __syncthreads();
+    if (grp == 0) ob[c] = O;
     __syncthreads();
     smem_fwht(ob, 1);
     O = ob[c];
   }
+
+  // ---- the fp residual tail (< 128 tokens)
+  float Mn = M;
   if (a.n_tail > 0) {
+    const int nt = a.n_tail;
+    const uint16_t* tk = a.tail_k + ((uint64_t)b * g.H + h) * nt * D;
+    const uint16_t* tv = a.tail_v + ((uint64_t)b * g.H + h) * nt * D;
+    for (int e = tid; e < nt * D; e += CB_THREADS) tks[e >> 7][e & (D - 1)] = tk[e];
     const float2* rope_blk = reinterpret_cast<const float2*>(a.base + g.rope_off);
-    const float2* rope_off = rope_blk + (size_t)(g.max_blocks + 1) * 64;
-    float qc = load_in(a.q + ((uint64_t)b * g.Hq + hq) * D + c, g.in_bf16);
-    qv[c] = qc;
+    const float2* rope_loc = rope_blk + (size_t)(g.max_blocks + 1) * 64;
+    if (grp == 0) {
+      const float qc = load_in(a.q + ((uint64_t)b * g.Hq + hq) * D + c, g.in_bf16);
+      qv[c] = qc;
+    }
     __syncthreads();
-    if (g.pre_rope) {  // q0 = R(n0)^T q with n0 = n_blocks*128
+    float qr = 0.0f;
+    if (grp == 0 && g.pre_rope) {  // q0 = R(n0)^T q with n0 = n_blocks*128
       const int p = c >> 1;
-      float2 cs = rope_blk[(size_t)a.n_blocks * 64 + p];
-      float x0 = qv[2 * p], x1 = qv[2 * p + 1];
-      qc = (c & 1) ? (-cs.y * x0 + cs.x * x1) : (cs.x * x0 + cs.y * x1);
+      const float2 cs = rope_blk[(size_t)a.n_blocks * 64 + p];
+      const float x0 = qv[2 * p], x1 = qv[2 * p + 1];
+      qr = (c & 1) ? (-cs.y * x0 + cs.x * x1) : (cs.x * x0 + cs.y * x1);
     }
     __syncthreads();
-    qv[c] = qc;
+    if (grp == 0 && g.pre_rope) qv[c] = qr;
     __syncthreads();
-    const uint16_t* tk = a.tail_k + ((uint64_t)b * g.H + h) * a.n_tail * D;
-    const uint16_t* tv = a.tail_v + ((uint64_t)b * g.H + h) * a.n_tail * D;
-    float mine = -INFINITY;
-    if (c < a.n_tail) {
+    // scores: token t = tid / 4, channel pairs 16*(tid%4) .. +15
+    {
+      const int t = tid >> 2, q4 = tid & 3;
       float acc = 0.0f;
-      for (int p = 0; p < 64; ++p) {
-        float k0 = load_in(tk + (uint64_t)c * D + 2 * p, g.in_bf16);
-        float k1 = load_in(tk + (uint64_t)c * D + 2 * p + 1, g.in_bf16);
-        if (g.pre_rope) {
-          float2 cs = rope_off[c * 64 + p];
-          float r0 = cs.x * k0 - cs.y * k1, r1 = cs.y * k0 + cs.x * k1;
-          k0 = r0;
-          k1 = r1;
+      if (t < nt) {
+#pragma unroll 4
+        for (int j = 0; j < 16; ++j) {
+          const int p = 16 * q4 + j;
+          float k0 = in_bits_to_f32(tks[t][2 * p], g.in_bf16), k1 = in_bits_to_f32(tks[t][2 * p + 1], g.in_bf16);
+          if (g.pre_rope) {
+            const float2 cs = rope_loc[t * 64 + p];
+            const float r0 = cs.x * k0 - cs.y * k1, r1 = cs.y * k0 + cs.x * k1;
+            k0 = r0;
+            k1 = r1;
+          }
+          acc = fmaf(qv[2 * p], k0, fmaf(qv[2 * p + 1], k1, acc));
         }
-        acc += qv[2 * p] * k0 + qv[2 * p + 1] * k1;
       }
-      mine = acc * LOG2E_RSQRT_D;
-      sc[c] = mine;
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      if (t < nt && q4 == 0) sc[t] = acc * LOG2E_RSQRT_D;
     }
-    float mx = mine;
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    if (lane == 0) red[warp] = mx;
     __syncthreads();
-    const float Mn = fmaxf(M, fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3])));
+    const float mt = cb_max(tid < nt ? sc[tid] : -INFINITY, red);
+    Mn = fmaxf(M, mt);
     const float f = exp2f(M - Mn);
     L *= f;
     O *= f;
-    __syncthreads();
     float pl = 0.0f;
-    if (c < a.n_tail) {
-      pl = exp2f(sc[c] - Mn);
-      sc[c] = pl;
+    if (tid < nt) {
+      pl = exp2f(sc[tid] - Mn);
+      sc[tid] = pl;
     }
-    for (int off = 16; off > 0; off >>= 1) pl += __shfl_xor_sync(0xffffffffu, pl, off);
-    if (lane == 0) red[warp] = pl;
+    L += cb_sum(pl, red);  // (also orders the sc[] stores)
+    // values: group grp sums tokens grp, grp+4, ...
+    float ov[2] = {0.0f, 0.0f};
+    int j = grp;
+    for (; j + CB_GROUPS < nt; j += 2 * CB_GROUPS) {
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int jj = j + k * CB_GROUPS;
+        ov[k] = fmaf(sc[jj], load_in(tv + (uint64_t)jj * D + c, g.in_bf16), ov[k]);
+      }
+    }
+    if (j < nt) ov[0] = fmaf(sc[j], load_in(tv + (uint64_t)j * D + c, g.in_bf16), ov[0]);
     __syncthreads();
-    L += (red[0] + red[1]) + (red[2] + red[3]);
-    for (int j = 0; j < a.n_tail; ++j) O += sc[j] * load_in(tv + (uint64_t)j * D + c, g.in_bf16);
+    part[grp][c] = ov[0] + ov[1];
+    __syncthreads();
+    O += (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
   }
-  a.out[((uint64_t)b * g.Hq + hq) * D + c] = O / L;
+  if (grp == 0) a.out[((uint64_t)b * g.Hq + hq) * D + c] = O / L;
 }
 
 template <int METHOD, int GMAX>
@@ -543,7 +612,7 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
   c.total = (long long)g.B * g.H * n_blocks;
   c.ws_m = ws_m; c.ws_l = ws_l; c.ws_o = ws_o; c.out = out; c.hadamard = hadamard;
   dim3 grid(g.Hq, g.B);
-  combine_kernel<<<grid, DC_THREADS, 0, st>>>(c);
+  combine_kernel<<<grid, CB_THREADS, 0, st>>>(c);
   return cudaGetLastError();
 }
 

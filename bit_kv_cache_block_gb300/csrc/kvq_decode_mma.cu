@@ -684,7 +684,8 @@ long long kvq_mma_ranges(const kvq::Geo& g) {
     for (auto& c : t_occ)
       if (c.dev == dev && c.fn == (void*)p.fn && c.smem == smem) hit = &c;
     if (!hit) {
-      cudaFuncSetAttribute(p.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      // raise (never lower) the kernel's shared-memory limit through the shared bookkeeping
+      if (kvq::ensure_smem_attr((const void*)p.fn, smem) != cudaSuccess) cudaGetLastError();
       int occ = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p.fn, p.nw * 32, smem) != cudaSuccess || occ < 1)
         occ = 1;

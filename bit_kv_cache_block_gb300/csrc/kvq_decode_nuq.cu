@@ -594,7 +594,8 @@ long long kvq_nuq_ranges(const kvq::Geo& g) {
     for (auto& c : t_nuq_occ)
       if (c.dev == dev && c.smem == smem) hit = &c;
     if (!hit) {
-      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      // raise (never lower) the kernel's shared-memory limit through the shared bookkeeping
+      if (kvq::ensure_smem_attr((const void*)fn, smem) != cudaSuccess) cudaGetLastError();
       int occ = 0;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, NTHREADS, smem) != cudaSuccess || occ < 1)
         occ = 1;

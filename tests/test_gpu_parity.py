@@ -199,6 +199,16 @@ def test_decode_parity(name, base, kw, tails):
         assert err <= TOL, f"{name} tail={n_tail}: max abs err {err:.3e}"
 
 
+def test_decode_shared_memory_sizes_in_any_order():
+    """Decodes whose kernels need different dynamic shared memory (outlier fractions 1%, 5%, 0%,
+    then 1% again, in one process) all launch: a smaller configuration must not leave the
+    kernel's shared-memory limit below what a later, larger one needs."""
+    for frac in (0.01, 0.05, 0.0, 0.01, 0.05):
+        w = WL.WORKLOADS[2].scaled(outlier_frac=frac, batch=1, n_kv_heads=2, n_q_heads=2, ctx=3 * 128)
+        out, ref = _run_decode(w, w.n_blocks, 0)
+        assert np.max(np.abs(out - ref)) <= TOL, f"outlier_frac={frac}"
+
+
 def test_decode_varn_own_planes():
     w = WL.WORKLOADS[3].scaled(batch=1, n_kv_heads=2, n_q_heads=8, ctx=3 * 128)
     out, ref = _run_decode(w, w.n_blocks, 17, oracle_planes=False)
