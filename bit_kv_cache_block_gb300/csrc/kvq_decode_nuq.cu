@@ -71,8 +71,8 @@ struct Args {
 
 // Per-stage operands the aux warps prepare for the consumer warps.
 struct Ops {
-  uint32_t bk[9][20];  // score B fragments of column g (16 k-groups), padded rows; row 8 stays zero
-  float4 cz[4][17];    // zero-point terms (X, Y, X, Y) of pair 4*kgroup + tq, per tq, padded rows
+  uint32_t bk[9][20];  // score B rows 0..7 (q_b * s) of column g, 16 k-groups, padded; row 8 stays zero
+  uint32_t bz[9][20];  // score B rows 8, 9 of column g: zero-point term (high, low); row 8 stays zero
   float sk[T];         // key-outlier score term per token
 };
 
@@ -244,7 +244,9 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
         op.bk[2 * tqp][kg] = pack_h2(qb0 * s0, qb1 * s1);       // X column of pair pi
         op.bk[2 * tqp + 1][kg] = pack_h2(qb1 * s0, -qb0 * s1);  // Y column
         const float zx = qb0 * z0 + qb1 * z1, zy = qb1 * z0 - qb0 * z1;
-        op.cz[tqp][kg] = make_float4(zx, zy, zx, zy);
+        const __half zxh = __float2half_rn(zx), zyh = __float2half_rn(zy);
+        op.bz[2 * tqp][kg] = pack_h2(zx, zx - __half2float(zxh));      // X column: (high, low)
+        op.bz[2 * tqp + 1][kg] = pack_h2(zy, zy - __half2float(zyh));  // Y column
       } else {
         *reinterpret_cast<float2*>(&qb[2 * pi]) = make_float2(qb0, qb1);
       }
@@ -289,37 +291,36 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
 // Scores of a consumer warp's 16 tokens in one block (after the reduction over the 4 lanes of a
 // token and the key-outlier terms): s0 for token 16w + gq, s1 for token 16w + gq + 8.
 __device__ __forceinline__ void block_scores(const uint8_t* st, const Ops& op, uint32_t codes_off, int warp, int lane,
-                                             int brow, int tq, int t0, int t1, uint32_t tl0, uint32_t tl1,
-                                             uint32_t th0, uint32_t th1, const float (&wc)[2][16],
-                                             const float (&ws)[2][16], float& s0, float& s1) {
+                                             int brow, int zrow, uint32_t ones, int t0, int t1, uint32_t tl0,
+                                             uint32_t tl1, uint32_t th0, uint32_t th1, const float2 (&w)[2][16],
+                                             float& s0, float& s1) {
   uint32_t cw[6];
   const uint2* kp = reinterpret_cast<const uint2*>(st + codes_off + warp * 768 + lane * 24);
   const uint2 k0 = kp[0], k1 = kp[1], k2 = kp[2];
   cw[0] = k0.x; cw[1] = k0.y; cw[2] = k1.x; cw[3] = k1.y; cw[4] = k2.x; cw[5] = k2.y;
   const uint4* bp = reinterpret_cast<const uint4*>(&op.bk[brow][0]);
-  float sc[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}}, ss[2][2] = {{0.0f, 0.0f}, {0.0f, 0.0f}};
+  const uint4* zp = reinterpret_cast<const uint4*>(&op.bz[zrow][0]);
+  const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  float2 acc[2][2] = {{{0.0f, 0.0f}, {0.0f, 0.0f}}, {{0.0f, 0.0f}, {0.0f, 0.0f}}};
 #pragma unroll
   for (int uu = 0; uu < 8; ++uu) {
     const uint32_t nw = nibble_word(cw, uu);
-    const uint4 bq = bp[uu >> 1];  // k-groups 4(uu/2) .. 4(uu/2)+3
+    const uint4 bq = bp[uu >> 1], zq = zp[uu >> 1];  // k-groups 4(uu/2) .. 4(uu/2)+3
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
       const int kg = 2 * uu + hf;
       uint32_t a0, a1;
       lookup4(hf ? (nw >> 16) : nw, tl0, tl1, th0, th1, a0, a1);
-      const float4 z = op.cz[tq][kg];
-      const float c4[4] = {z.x, z.y, z.z, z.w};
       const uint32_t bb = (kg & 3) == 0 ? bq.x : (kg & 3) == 1 ? bq.y : (kg & 3) == 2 ? bq.z : bq.w;
+      const uint32_t bz = (kg & 3) == 0 ? zq.x : (kg & 3) == 1 ? zq.y : (kg & 3) == 2 ? zq.z : zq.w;
       float d[4];
-      mma1688(d, a0, a1, bb, c4);
-      sc[0][hf] = fmaf(wc[0][kg], d[0], sc[0][hf]);
-      ss[0][hf] = fmaf(ws[0][kg], d[1], ss[0][hf]);
-      sc[1][hf] = fmaf(wc[1][kg], d[2], sc[1][hf]);
-      ss[1][hf] = fmaf(ws[1][kg], d[3], ss[1][hf]);
+      mma16816(d, a0, a1, ones, ones, bb, bz, zero4);  // X, Y of pair 4kg+tq incl. the zero-point term
+      acc[0][hf] = __ffma2_rn(w[0][kg], make_float2(d[0], d[1]), acc[0][hf]);
+      acc[1][hf] = __ffma2_rn(w[1][kg], make_float2(d[2], d[3]), acc[1][hf]);
     }
   }
-  s0 = (sc[0][0] + sc[0][1]) + (ss[0][0] + ss[0][1]);
-  s1 = (sc[1][0] + sc[1][1]) + (ss[1][0] + ss[1][1]);
+  s0 = (acc[0][0].x + acc[0][1].x) + (acc[0][0].y + acc[0][1].y);
+  s1 = (acc[1][0].x + acc[1][1].x) + (acc[1][0].y + acc[1][1].y);
   s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
   s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
   s0 += __shfl_xor_sync(0xffffffffu, s0, 2) + op.sk[t0];
@@ -383,17 +384,15 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
   const Geo& g = a.g;
   const uint32_t sb = stage_bytes(g);
   const int gq = lane >> 2, tq = lane & 3;
-  // cos/sin of the lane's (token, pair) cells: tokens 16w + gq + 8r, pairs 4kg + tq
-  float wc[2][16], ws[2][16];
+  // (cos, sin) of the lane's (token, pair) cells: tokens 16w + gq + 8r, pairs 4kg + tq
+  float2 wcs[2][16];
 #pragma unroll
   for (int r = 0; r < 2; ++r)
 #pragma unroll
-    for (int kg = 0; kg < 16; ++kg) {
-      const float2 cs = sm->rope_loc[(16 * warp + gq + 8 * r) * 64 + 4 * kg + tq];
-      wc[r][kg] = cs.x;
-      ws[r][kg] = cs.y;
-    }
-  const int brow = (gq >> 1) == tq ? gq : 8;             // lanes holding nonzero score B entries
+    for (int kg = 0; kg < 16; ++kg) wcs[r][kg] = sm->rope_loc[(16 * warp + gq + 8 * r) * 64 + 4 * kg + tq];
+  const int brow = (gq >> 1) == tq ? gq : 8;             // lanes holding nonzero score B rows 0..7
+  const int zrow = tq == 0 ? gq : 8;                     // lanes holding the zero-point rows 8, 9
+  const uint32_t ones = tq == 0 ? 0x3c003c00u : 0u;      // A columns 8, 9 = 1.0 (fp16), others 0
   const int src_a = 4 * tq + (gq < 2 ? gq : 2);          // value B: (high, low, zero) source lanes
   const uint32_t xsel = tq == 0 ? 0xffffffffu : 0u;      // this lane sends p' high (tq 0) ...
   const uint32_t ysel = tq == 1 ? 0xffffffffu : 0u;      // ... or low (tq 1) or zero
@@ -451,8 +450,8 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
     float sv[NBK][2];
 #pragma unroll
     for (int k = 0; k < NBK; ++k)
-      block_scores(ring + (size_t)sidx[k] * sb, sm->op[sidx[k]], g.codes_off[0], warp, lane, brow, tq, t0, t1, tl0,
-                   tl1, th0, th1, wc, ws, sv[k][0], sv[k][1]);
+      block_scores(ring + (size_t)sidx[k] * sb, sm->op[sidx[k]], g.codes_off[0], warp, lane, brow, zrow, ones, t0, t1,
+                   tl0, tl1, th0, th1, wcs, sv[k][0], sv[k][1]);
     // online softmax over the NBK blocks' tokens of this warp (base 2)
     float mloc = fmaxf(sv[0][0], sv[0][1]);
 #pragma unroll
@@ -543,7 +542,10 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
     float4* dst = reinterpret_cast<float4*>(sm->rope_loc);
     for (int e = tid; e < T * 32; e += NTHREADS) dst[e] = __ldg(src + e);
   }
-  for (int e = tid; e < NBS * 20; e += NTHREADS) sm->op[e / 20].bk[8][e % 20] = 0u;
+  for (int e = tid; e < NBS * 20; e += NTHREADS) {
+    sm->op[e / 20].bk[8][e % 20] = 0u;
+    sm->op[e / 20].bz[8][e % 20] = 0u;
+  }
   if (tid == 0) {
     for (int s = 0; s < NBS; ++s) {
       mbar_init(&sm->rec_full[s], 1);
