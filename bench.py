@@ -33,6 +33,11 @@ import workloads as WL  # noqa: E402
 
 L2_BYTES = 126.5 * 2 ** 20
 DECODES_PER_STEP = 128
+# The cache's code layout: the tensor-core tile format (3-bit codes as 48-byte bit planes per 128
+# codes, 2/4-bit value tiles one row per channel), which the tensor-core decode kernels read. The
+# row layout of the KVQuant page's bit listing is the library's default and is covered by the
+# parity tests; its decode runs on the CUDA-core kernel.
+BENCH_LAYOUT = "mma"
 
 
 def _peaks():
@@ -162,7 +167,7 @@ def run_kvq(args):
         w = w.scaled(ctx=args.ctx)
     nb = w.n_blocks
     cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, nb + 1, w.dtype, w.pre_rope,
-                        w.rope_theta, w.outlier_frac, w.varn_iters, True)
+                        w.rope_theta, w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT)
     lay = K.kvq_layout(cfg)
     cb = None
     if w.method == "nuq":
@@ -275,7 +280,7 @@ def run_kvq(args):
         "config": {"workload": w.name, "method": w.method, "bits": w.bits, "batch": w.batch,
                    "n_kv_heads": w.n_kv_heads, "n_q_heads": w.n_q_heads, "context": w.ctx,
                    "decodes_per_step": DECODES_PER_STEP, "tail_tokens": "0..127",
-                   "packed_bytes_per_decode": cache_bytes, "cache_copies": n_copies,
+                   "layout": BENCH_LAYOUT, "packed_bytes_per_decode": cache_bytes, "cache_copies": n_copies,
                    "l2": f"{n_copies} cache copies rotated ({n_copies * int(lay.records_bytes) / 2**20:.0f} MiB > 3x L2)",
                    "parallelism": f"replicas x{world}"},
         "pct_of_8TBs": round(100 * value / 8000, 2),
@@ -359,7 +364,7 @@ def run_e2e(args, K, torch, dev, caches, cfg, w, nb, q, tail_k, tail_v, cache_by
 def _oracle_sample(w, heads, seed=0):
     """Oracle append (timed) and decode (timed) for a few (b, h) of the workload."""
     import oracle as O
-    oc = O.OracleCache.for_workload(w)
+    oc = O.OracleCache.for_workload(w, layout=O.LAYOUT_MMA if BENCH_LAYOUT == "mma" else O.LAYOUT_ROWS)
     t_app = 0.0
     for blk in range(w.n_blocks):
         K = np.empty((w.batch, w.n_kv_heads, 128, 128), np.float32)
@@ -391,7 +396,7 @@ def cpu_baseline(w, n_heads):
     t_app, t_dec = json.loads(r.stdout.strip().splitlines()[-1])
     import bit_kv_cache_block_gb300 as K
     cfg = K.make_config(w.method, w.bits, 1, 1, w.group, w.n_blocks, w.dtype, w.pre_rope, w.rope_theta,
-                        w.outlier_frac, w.varn_iters, True)
+                        w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT)
     per_head = K.kvq_decode_bytes(cfg, w.n_blocks)
     nbytes = per_head * len(heads)
     return {"value": round(nbytes / t_dec / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -450,7 +455,8 @@ def _decode_kernel_name(w):
 
 def _decode_bytes_per_head(w):
     """Algorithmic packed bytes of one (b, h) over the context (same count as kvq_decode_bytes)."""
-    W = 12 if w.bits == 3 else -(-128 // (32 // w.bits))  # 3-bit tiles: 48 B per 128 codes
+    # 3-bit tiles: 48 B per 128 codes as bit planes, 52 B as 10-code rows
+    W = 12 if (w.bits == 3 and BENCH_LAYOUT == "mma") else -(-128 // (32 // w.bits))
     meta = {"rtn": 2, "nuq": 2, "varn": 3, "int4": 1}[w.method] * 256
     csr = 0
     if w.method == "nuq":

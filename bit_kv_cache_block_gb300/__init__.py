@@ -12,7 +12,8 @@ from __future__ import annotations
 import ctypes as C
 
 from . import _lib
-from ._lib import (KVQ_BF16, KVQ_F16, KVQ_INT4, KVQ_NUQ, KVQ_OK, KVQ_RTN, KVQ_VARN, KVQError, METHODS,
+from ._lib import (KVQ_BF16, KVQ_F16, KVQ_INT4, KVQ_LAYOUT_MMA, KVQ_LAYOUT_ROWS, KVQ_NUQ, KVQ_OK, KVQ_RTN, KVQ_VARN,
+                   KVQError, LAYOUTS, METHODS,
                    kvq_cache, kvq_config, kvq_layout_t)
 
 __all__ = ["make_config", "kvq_layout", "kvq_dense_kv_bytes", "kvq_cache_init", "kvq_append_block",
@@ -27,7 +28,8 @@ def lib_path() -> str:
 
 def make_config(method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: int, max_blocks: int,
                 in_dtype: str = "f16", pre_rope: bool = False, rope_theta: float = 10000.0,
-                outlier_frac: float = 0.01, varn_iters: int = 8, hadamard: bool = True) -> kvq_config:
+                outlier_frac: float = 0.01, varn_iters: int = 8, hadamard: bool = True,
+                layout: str = "rows") -> kvq_config:
     c = kvq_config()
     c.method = METHODS[method] if isinstance(method, str) else int(method)
     c.bits, c.batch, c.n_kv_heads, c.n_q_heads = bits, batch, n_kv_heads, n_q_heads
@@ -38,6 +40,7 @@ def make_config(method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: 
     c.outlier_frac = float(outlier_frac)
     c.varn_iters = int(varn_iters)
     c.hadamard = int(bool(hadamard))
+    c.layout = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
     return c
 
 

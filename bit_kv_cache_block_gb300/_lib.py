@@ -15,6 +15,8 @@ KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY, KVQ_ERR_ALIG
     KVQ_ERR_TIMEOUT = range(7)
 KVQ_RTN, KVQ_NUQ, KVQ_VARN, KVQ_INT4 = range(4)
 KVQ_F16, KVQ_BF16 = 0, 1
+KVQ_LAYOUT_ROWS, KVQ_LAYOUT_MMA = 0, 1
+LAYOUTS = {"rows": KVQ_LAYOUT_ROWS, "mma": KVQ_LAYOUT_MMA}
 KVQ_FORMAT_VERSION = 2
 KVQ_STATIC_WORKSPACE_BYTES = 8 << 20
 METHODS = {"rtn": KVQ_RTN, "nuq": KVQ_NUQ, "varn": KVQ_VARN, "int4": KVQ_INT4}
@@ -30,7 +32,7 @@ class kvq_config(C.Structure):
                 ("n_q_heads", C.c_int32), ("head_dim", C.c_int32), ("block", C.c_int32),
                 ("max_blocks", C.c_int32), ("in_dtype", C.c_int32), ("pre_rope", C.c_int32),
                 ("rope_theta", C.c_double), ("outlier_frac", C.c_float), ("varn_iters", C.c_int32),
-                ("hadamard", C.c_int32)]
+                ("hadamard", C.c_int32), ("layout", C.c_int32)]
 
 
 class kvq_layout_t(C.Structure):

@@ -30,6 +30,7 @@ kvq_status check_config(const kvq_config* c) {
   if (c->n_q_heads / c->n_kv_heads > KVQ_MAX_GROUP) return KVQ_ERR_UNSUPPORTED;
   if (c->in_dtype != KVQ_F16 && c->in_dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARG;
   if (c->bits < 2 || c->bits > 4) return KVQ_ERR_UNSUPPORTED;
+  if (c->layout != KVQ_LAYOUT_ROWS && c->layout != KVQ_LAYOUT_MMA) return KVQ_ERR_INVALID_ARG;
   if (c->method == KVQ_INT4 && c->bits != 4) return KVQ_ERR_UNSUPPORTED;
   if (c->pre_rope != 0 && c->pre_rope != 1) return KVQ_ERR_INVALID_ARG;
   if (c->pre_rope && c->method != KVQ_NUQ) return KVQ_ERR_UNSUPPORTED;
@@ -84,7 +85,7 @@ kvq_status kvq_layout(const kvq_config* c, kvq_layout_t* out) {
   if (!out) return KVQ_ERR_INVALID_ARG;
   kvq_layout_t l;
   std::memset(&l, 0, sizeof(l));
-  l.words_per_row = kvq::words_per_row(c->bits);
+  l.words_per_row = kvq::words_per_row(c->bits, c->layout);
   l.n_outliers = c->method == KVQ_NUQ ? kvq::n_outliers_for(c->outlier_frac) : 0;
   const uint64_t codes = (uint64_t)kvq::T * l.words_per_row * 4;
   const uint64_t meta = (uint64_t)kvq::meta_vectors(c->method) * kvq::T * 2;

@@ -115,13 +115,12 @@ __device__ void rtn_tile(AppendSmem* sm, int axis, int bits, uint16_t* m16) {
   __syncthreads();
 }
 
-// Pack sm->codes (token-major, [t][c]) into words. 2 and 4 bits: code i of a row at bits
-// [b*(i%n)+b-1 : b*(i%n)] of word i/n; key tiles one row per token (its 128 channel codes),
-// value tiles (transpose = true) one row per channel (its codes for the 128 tokens).
-// 3 bits: the plane layout of tile3_slot (one thread per output word).
-__device__ void pack_tile(const AppendSmem* sm, int bits, bool transpose, uint32_t* dst) {
-  if (bits == 3) {
-    const int kind = transpose ? 1 : 0;
+// Pack sm->codes (token-major, [t][c]) into words. Rows: code i of a row at bits
+// [b*(i%n)+b-1 : b*(i%n)] of word i/n, n = floor(32/b); one row per token, or (transpose) one row
+// per channel (its codes for the 128 tokens). planes: the 3-bit plane layout of tile3_slot (one
+// thread per output word; kind 0 keys, 1 values).
+__device__ void pack_tile(const AppendSmem* sm, int bits, bool transpose, bool planes, int kind, uint32_t* dst) {
+  if (planes) {
     for (int wi = threadIdx.x; wi < TILE3_WORDS; wi += AP_THREADS) {
       const int s = wi / 192, rem = wi - s * 192, grp = rem / 6, o = rem - grp * 6;
       uint32_t word = 0;
@@ -421,7 +420,7 @@ __global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
     }
     __syncthreads();
   }
-  pack_tile(sm, g.bits, kind == 1, codes_dst);
+  pack_tile(sm, g.bits, kind == 1 && g.vrows_ch, g.planes3 != 0, kind, codes_dst);
 }
 
 size_t append_smem_bytes() { return sizeof(AppendSmem); }

@@ -177,10 +177,10 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
     for (int c = 0; c < D; c += 2) {
       {
         uint32_t c0, c1;
-        if (bits == 3) {
+        if (g.planes3) {
           c0 = tile3_code(kc, 0, t, c);
           c1 = tile3_code(kc, 0, t, c + 1);
-        } else {  // n = 32/bits is even: a channel pair never straddles two words
+        } else {  // n = floor(32/bits) (16, 10, 8) is even: a channel pair never straddles two words
           const int w = c / nw, j = c - w * nw;
           const uint32_t word = kc[t * W + w];
           c0 = (word >> (bits * j)) & cmask;
@@ -299,9 +299,9 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
 #pragma unroll
       for (int k = 0; k < GMAX; ++k) bs[k] = 0.0f;
       for (int tt = 0; tt < T; ++tt) {
-        const int wt = tt / nw;
-        const uint32_t code =
-            bits == 3 ? tile3_code(vc, 1, tt, c) : (vc[c * W + wt] >> (bits * (tt - wt * nw))) & cmask;
+        const uint32_t code = g.planes3 ? tile3_code(vc, 1, tt, c)
+                              : g.vrows_ch ? (vc[c * W + tt / nw] >> (bits * (tt % nw))) & cmask
+                                           : (vc[tt * W + c / nw] >> (bits * (c % nw))) & cmask;
         float val;
         if (METHOD == KVQ_RTN || METHOD == KVQ_VARN) {
           val = (float)code + h2f(vm[T + tt]);

@@ -637,6 +637,7 @@ Plan plan_g(int G) {
 }
 
 bool supported(const Geo& g) {
+  if (g.layout != KVQ_LAYOUT_MMA) return false;  // value tiles must hold one row per channel
   if (g.G > GQ) return false;
   if (g.bits != 2 && g.bits != 4) return false;
   return g.method == KVQ_RTN || g.method == KVQ_VARN || g.method == KVQ_INT4;

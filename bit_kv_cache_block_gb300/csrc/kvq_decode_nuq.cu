@@ -578,7 +578,7 @@ thread_local NuqOcc t_nuq_occ[4];
 }  // namespace
 
 bool kvq_nuq_supported(const kvq::Geo& g) {
-  return g.method == KVQ_NUQ && g.bits == 3 && g.G == 1 && g.pre_rope == 1 &&
+  return g.method == KVQ_NUQ && g.bits == 3 && g.planes3 && g.G == 1 && g.pre_rope == 1 &&
          g.n_out <= kvq::nuqdec::MAX_OUTLIERS && kvq::nuqdec::smem_bytes(g) <= 227 * 1024;
 }
 

@@ -33,10 +33,10 @@ __global__ void __launch_bounds__(DQ_THREADS) dequant_kernel(DequantArgs a) {
   const uint32_t cmask = (1u << bits) - 1u;
   float* row = xs + t * 129;
   for (int c = 0; c < D; ++c) {
-    // 2/4 bits: key rows are tokens, value rows are channels; 3 bits: plane layout
-    const uint32_t q = bits == 3 ? tile3_code(codes, kind, t, c)
-                       : kind == 0 ? (codes[t * W + c / nw] >> (bits * (c % nw))) & cmask
-                                   : (codes[c * W + t / nw] >> (bits * (t % nw))) & cmask;
+    // rows of tokens (value tiles: rows of channels when vrows_ch), or the 3-bit planes
+    const uint32_t q = g.planes3 ? tile3_code(codes, kind, t, c)
+                       : (kind == 0 || !g.vrows_ch) ? (codes[t * W + c / nw] >> (bits * (c % nw))) & cmask
+                                                    : (codes[c * W + t / nw] >> (bits * (t % nw))) & cmask;
     float v;
     if (g.method == KVQ_RTN || g.method == KVQ_VARN) {
       const int gi = kind == 0 ? c : t;

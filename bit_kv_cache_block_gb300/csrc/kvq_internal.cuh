@@ -17,8 +17,9 @@ constexpr int D = 128;      // head dim
 constexpr int TILE = T * D; // elements per tile
 
 __host__ __device__ constexpr int codes_per_word(int bits) { return 32 / bits; }
-__host__ __device__ constexpr int words_per_row(int bits) {
-  return bits == 3 ? 12 : (D + codes_per_word(bits) - 1) / codes_per_word(bits);
+// Words per 128-code row; 3-bit tiles in the plane layout (KVQ_LAYOUT_MMA) count as 12.
+__host__ __device__ constexpr int words_per_row(int bits, int layout) {
+  return (bits == 3 && layout == KVQ_LAYOUT_MMA) ? 12 : (D + codes_per_word(bits) - 1) / codes_per_word(bits);
 }
 
 // 3-bit tiles ([KVQ] §9.3: 48 bytes per 128 codes) keep each code's two low bits and its high
@@ -97,6 +98,9 @@ inline uint64_t csr_bytes_for(int n_out) {
 // Parameters every kernel needs, passed by value.
 struct Geo {
   int method, bits, B, H, Hq, G, max_blocks, in_bf16, pre_rope, n_out, W;
+  int layout;   // kvq_code_layout
+  int planes3;  // 3-bit tiles in bit planes (KVQ_LAYOUT_MMA)
+  int vrows_ch; // value tiles hold one row per channel (KVQ_LAYOUT_MMA, 2 and 4 bits)
   uint64_t rec_bytes;
   uint32_t codes_off[2], meta_off[2], csr_off[2];
   uint64_t rope_off;
@@ -107,6 +111,9 @@ inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
   g.method = c.method; g.bits = c.bits; g.B = c.batch; g.H = c.n_kv_heads; g.Hq = c.n_q_heads;
   g.G = c.n_q_heads / c.n_kv_heads; g.max_blocks = c.max_blocks; g.in_bf16 = c.in_dtype == KVQ_BF16;
   g.pre_rope = c.pre_rope; g.n_out = l.n_outliers; g.W = l.words_per_row; g.rec_bytes = l.record_bytes;
+  g.layout = c.layout;
+  g.planes3 = c.layout == KVQ_LAYOUT_MMA && c.bits == 3;
+  g.vrows_ch = c.layout == KVQ_LAYOUT_MMA && c.bits != 3;
   for (int k = 0; k < 2; ++k) {
     g.codes_off[k] = (uint32_t)l.codes_off[k];
     g.meta_off[k] = (uint32_t)l.meta_off[k];

@@ -71,6 +71,15 @@ typedef enum {
 
 typedef enum { KVQ_F16 = 0, KVQ_BF16 = 1 } kvq_dtype;
 
+/* Layout of the code words of a tile (see kvq_layout_t).
+ *   KVQ_LAYOUT_ROWS: one row per token for keys and values, each row's 128 codes in
+ *                    floor(32/b)-code words ([KVQ] §9.3 bit layout; 3-bit rows are 13 words).
+ *   KVQ_LAYOUT_MMA : the tensor-core decode's format: 2- and 4-bit value tiles hold one row per
+ *                    channel; 3-bit tiles are bit planes in matrix-fragment order, 48 bytes per
+ *                    128 codes ([KVQ] §9.3 byte count). The tensor-core decodes need this layout;
+ *                    with KVQ_LAYOUT_ROWS every decode runs on the CUDA cores. */
+typedef enum { KVQ_LAYOUT_ROWS = 0, KVQ_LAYOUT_MMA = 1 } kvq_code_layout;
+
 /* Cache configuration. All fields are read by kvq_layout / kvq_cache_init. */
 typedef struct {
   int32_t method;        /* kvq_method */
@@ -89,16 +98,18 @@ typedef struct {
   float outlier_frac;    /* NUQ: fraction of each tile kept as fp16 outliers (0.01); 0 disables */
   int32_t varn_iters;    /* VARN: variance-normalisation iterations (8); 0..64 */
   int32_t hadamard;      /* VARN: 1 applies the FWHT-128 (the decode transforms q and o too) */
+  int32_t layout;        /* kvq_code_layout of the code words (0: KVQ_LAYOUT_ROWS) */
 } kvq_config;
 
 /* Byte layout of a cache, from kvq_layout. One record per (b, h, block), at
  *   base + ((b * n_kv_heads + h) * max_blocks + block) * record_bytes,
  * holding the K tile then the V tile; every region starts 16-byte aligned:
- *   codes : 2- and 4-bit tiles: 128 rows x words_per_row uint32; code i of a row at bits
- *           [b*(i%n)+b-1 : b*(i%n)] of word i/n, n = 32/b ([KVQ] §9.3 layout, generalised).
- *           K tile: one row per token (its 128 channel codes). V tile: one row per channel
+ *   codes : KVQ_LAYOUT_ROWS: 128 rows x words_per_row uint32, one row per token (K and V);
+ *           code i of a row at bits [b*(i%n)+b-1 : b*(i%n)] of word i/n, n = floor(32/b),
+ *           unused high bits zero ([KVQ] §9.3 layout, generalised; 3-bit: 13 words per row).
+ *           KVQ_LAYOUT_MMA, 2 and 4 bits: the same rows, but a V tile has one row per channel
  *           (its codes for the 128 tokens).
- *           3-bit tiles: 1536 uint32 (48 bytes per 128 codes, the count of [KVQ] §9.3),
+ *           KVQ_LAYOUT_MMA, 3 bits: 1536 uint32 (48 bytes per 128 codes, the count of [KVQ] §9.3),
  *           bit planes in matrix-fragment order. Segment s = t/16 (t = token in the block)
  *           holds 32 groups of 6 words (group base word s*192 + 6*grp); in a group, slot k
  *           (0..7) of nibble word u (0..7) keeps a code's two low bits in word u/2 at bit
@@ -107,7 +118,7 @@ typedef struct {
  *             k = 4((c/8)%2) + 2((t%16)/8) + c%2.
  *           V tile, code (t, c): grp = 4(c%8) + t%4, u = c/16,
  *             k = 4(((t%16)/4)%2) + 2((c/8)%2) + (t%16)/8.
- *           words_per_row is 12 for 3-bit caches (the tile holds 128 x 12 words).
+ *           words_per_row is 12 for 3-bit KVQ_LAYOUT_MMA caches (the tile holds 128 x 12 words).
  *   meta  : fp16 vectors of 128. RTN and VARN: s, z (keys: per channel; values: per token),
  *           VARN adds s1 (keys: per token; values: per channel). NUQ: s (half-range),
  *           zp (centre). INT4: s (per token).

@@ -122,14 +122,21 @@ def unpack_rows(words: np.ndarray, bits: int) -> np.ndarray:
     return out
 
 
-# 3-bit tiles. [KVQ] §9.3 counts 128 x 3 bits = 48 bytes per key vector, which ten codes per
-# 32-bit word (its bit example, 13 words = 52 bytes) cannot reach; a 3-bit tile here takes the
-# 48-byte count: 128 x 128 codes in 1536 words, with every code's two low bits and its high bit
-# in separate bit planes. The plane order follows the decode's matrix fragments: the tile is
-# cut into 8 segments of 16 tokens, each segment into 32 groups of 64 codes (6 words each),
-# and within a group the codes sit in 8 four-bit slots of 8 "nibble words" u (the low bits of
-# nibble word u in word u//2 at bit 4k + 2(u%2), its high bit in word 4 + u//4 at bit
-# 4k + (2, 3, 0, 1)[u%4], k = 0..7 the slot).
+# Two packed layouts of a tile.
+#
+# LAYOUT_ROWS (the default): one row per token, for keys and values alike, each row its 128 codes
+# in floor(32/b)-code words as `pack_rows` above ([KVQ] §9.3 bit layout; a 3-bit row is 13 words
+# = 52 bytes).
+#
+# LAYOUT_MMA (the tensor-core decode's format): 2- and 4-bit value tiles hold one row per channel
+# (its codes for the 128 tokens); 3-bit tiles take [KVQ] §9.3's other figure, 128 x 3 bits = 48
+# bytes per vector, which ten codes per word cannot reach: 128 x 128 codes in 1536 words, every
+# code's two low bits and its high bit in separate bit planes. The plane order follows the decode's
+# matrix fragments: the tile is cut into 8 segments of 16 tokens, each segment into 32 groups of
+# 64 codes (6 words each), and within a group the codes sit in 8 four-bit slots of 8 "nibble
+# words" u (the low bits of nibble word u in word u//2 at bit 4k + 2(u%2), its high bit in word
+# 4 + u//4 at bit 4k + (2, 3, 0, 1)[u%4], k = 0..7 the slot).
+LAYOUT_ROWS, LAYOUT_MMA = 0, 1
 TILE3_WORDS = 1536
 
 
@@ -176,16 +183,19 @@ def unpack_tile3(words: np.ndarray, kind: int) -> np.ndarray:
     return (lo | (hi << np.uint64(2))).astype(np.uint8).reshape(T, D)
 
 
-def pack_tile(codes: np.ndarray, bits: int, kind: int) -> np.ndarray:
-    """Code words of one tile (codes [token][channel]): 3-bit tiles use the plane layout above;
-    2- and 4-bit key tiles hold one row per token, value tiles one row per channel."""
+def pack_tile(codes: np.ndarray, bits: int, kind: int, layout: int = LAYOUT_ROWS) -> np.ndarray:
+    """Code words of one tile (codes [token][channel]) in `layout` (see above)."""
+    if layout == LAYOUT_ROWS:
+        return pack_rows(codes, bits)
     if bits == 3:
         return pack_tile3(codes, kind)
     return pack_rows(codes if kind == KIND_K else np.asarray(codes).T, bits)
 
 
-def unpack_tile(words: np.ndarray, bits: int, kind: int) -> np.ndarray:
+def unpack_tile(words: np.ndarray, bits: int, kind: int, layout: int = LAYOUT_ROWS) -> np.ndarray:
     """Inverse of pack_tile: codes [token][channel]."""
+    if layout == LAYOUT_ROWS:
+        return unpack_rows(words, bits)
     if bits == 3:
         return unpack_tile3(words, kind)
     codes = unpack_rows(words, bits)
@@ -514,8 +524,8 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:
 class OracleCache:
     """A packed cache kept as per-tile records plus the decode that reads it.
 
-    One record per (batch b, KV head h, block, kind): the packed code words (pack_tile), the
-    fp16 metadata and, for nuq, the CSR outliers. decode() unpacks and dequantises every
+    One record per (batch b, KV head h, block, kind): the packed code words (pack_tile in the
+    cache's layout), the fp16 metadata and, for nuq, the CSR outliers. decode() unpacks and dequantises every
     record in fp64 (RoPE at absolute positions for pre-RoPE keys; the Hadamard domain
     for KVarN, with the query transformed the same way and the output transformed back),
     appends the fp residual tail and evaluates softmax attention. Query head j reads KV
@@ -524,9 +534,10 @@ class OracleCache:
 
     def __init__(self, method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: int,
                  pre_rope: bool = False, rope_theta: float = 10000.0, outlier_frac: float = 0.01,
-                 varn_iters: int = 8, use_hadamard: bool = True, codebook=None):
+                 varn_iters: int = 8, use_hadamard: bool = True, codebook=None, layout: int = LAYOUT_ROWS):
         assert method in ("rtn", "nuq", "varn", "int4")
-        self.method, self.bits = method, bits
+        assert layout in (LAYOUT_ROWS, LAYOUT_MMA)
+        self.method, self.bits, self.layout = method, bits, layout
         self.batch, self.n_kv_heads, self.n_q_heads = batch, n_kv_heads, n_q_heads
         self.pre_rope, self.rope_theta = pre_rope, rope_theta
         self.outlier_frac, self.varn_iters, self.use_hadamard = outlier_frac, varn_iters, use_hadamard
@@ -556,7 +567,7 @@ class OracleCache:
             rec = nuq_quantize(x, self.codebook[h], 0 if kind == KIND_K else 1, self.n_out)
         else:
             rec = varn_quantize(x, b, kind, self.varn_iters, self.use_hadamard)
-        rec["words"] = pack_tile(rec["codes"], b, kind)
+        rec["words"] = pack_tile(rec["codes"], b, kind, self.layout)
         return rec
 
     def append(self, K: np.ndarray, V: np.ndarray, only_heads=None):
@@ -578,7 +589,7 @@ class OracleCache:
         """domain 'stored': the quantised representation (pre-RoPE keys un-rotated, KVarN
         in the Hadamard domain); 'input': back in the input domain (inverse Hadamard for
         KVarN); 'attn': what attention reads (RoPE applied to pre-RoPE keys)."""
-        codes = unpack_tile(rec["words"], self.bits, kind)
+        codes = unpack_tile(rec["words"], self.bits, kind, self.layout)
         m = self.method
         if m == "rtn":
             x = rtn_dequant(codes, rec["s16"], rec["z16"], 0 if kind == KIND_K else 1)

@@ -15,12 +15,16 @@ def torch_mod():
     return torch
 
 
-def cfg_for(w: WL.Workload, max_blocks=None, batch=None):
+def cfg_for(w: WL.Workload, max_blocks=None, batch=None, layout="rows"):
     import bit_kv_cache_block_gb300 as K
     return K.make_config(w.method, w.bits, batch or w.batch, w.n_kv_heads, w.n_q_heads,
                          max_blocks or w.n_blocks, in_dtype=w.dtype, pre_rope=w.pre_rope,
                          rope_theta=w.rope_theta, outlier_frac=w.outlier_frac, varn_iters=w.varn_iters,
-                         hadamard=True)
+                         hadamard=True, layout=layout)
+
+
+def oracle_layout(layout: str) -> int:
+    return O.LAYOUT_MMA if layout == "mma" else O.LAYOUT_ROWS
 
 
 def codebook_for(w: WL.Workload):
@@ -37,24 +41,25 @@ def to_device(x: np.ndarray, dtype: str, device="cuda"):
     return t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
 
 
-def new_cache(w: WL.Workload, max_blocks=None, batch=None):
+def new_cache(w: WL.Workload, max_blocks=None, batch=None, layout="rows"):
     import bit_kv_cache_block_gb300 as K
     torch = torch_mod()
     cb = codebook_for(w)
-    return K.KVCache(cfg_for(w, max_blocks, batch), None if cb is None else torch.from_numpy(cb))
+    return K.KVCache(cfg_for(w, max_blocks, batch, layout), None if cb is None else torch.from_numpy(cb))
 
 
 def records_np(cache) -> np.ndarray:
     return cache.record_view().cpu().numpy()
 
 
-def tile_fields(rec: np.ndarray, lay, kind: int, method: str, bits: int) -> dict:
-    """Decode one record's K (kind 0) or V (kind 1) regions into arrays."""
+def tile_fields(rec: np.ndarray, lay, kind: int, method: str, bits: int, layout: str = "rows") -> dict:
+    """Decode one record's K (kind 0) or V (kind 1) regions into arrays (code words shaped as the
+    oracle's pack_tile returns them: flat planes for 3-bit "mma" tiles, else [128 rows][W])."""
     W = lay.words_per_row
     co, cb = int(lay.codes_off[kind]), int(lay.codes_bytes[kind])
     mo, mb = int(lay.meta_off[kind]), int(lay.meta_bytes[kind])
     words = rec[co:co + cb].view(np.uint32).copy()
-    out = dict(words=words if bits == 3 else words.reshape(T, W))
+    out = dict(words=words if (bits == 3 and layout == "mma") else words.reshape(T, W))
     meta = rec[mo:mo + mb].view(np.uint16).reshape(-1, T)
     out["s16"] = meta[0].view(np.float16).copy()
     if method in ("rtn", "varn"):

@@ -78,19 +78,26 @@ def _cfg(K, wid, **kw):
                          w.rope_theta, w.outlier_frac, w.varn_iters, True)
 
 
-# algorithmic packed bytes per decode step at the full workloads (codes + fp16 metadata + CSR)
-EXPECTED_DECODE_BYTES = {1: 278528, 2: 121339904, 3: 79691776, 4: 1107296256, 5: 2415919104}
-EXPECTED_RECORD_BYTES = {1: 2 * (8192 + 512), 2: 2 * (6144 + 512 + 752), 3: 2 * (4096 + 768),
+# algorithmic packed bytes per decode step at the full workloads (codes + fp16 metadata + CSR); the
+# layouts differ only for 3-bit tiles (13-word rows vs 48-byte planes)
+EXPECTED_DECODE_BYTES = {1: 278528, 2: 129728512, 3: 79691776, 4: 1107296256, 5: 2415919104}
+EXPECTED_RECORD_BYTES = {1: 2 * (8192 + 512), 2: 2 * (6656 + 512 + 752), 3: 2 * (4096 + 768),
                          4: 2 * (8192 + 256), 5: 2 * (4096 + 512)}
+EXPECTED_MMA = {2: (121339904, 2 * (6144 + 512 + 752))}
 
 
+@pytest.mark.parametrize("layout", ["rows", "mma"])
 @pytest.mark.parametrize("wid", [1, 2, 3, 4, 5])
-def test_layout_and_decode_bytes(K, wid):
+def test_layout_and_decode_bytes(K, wid, layout):
     cfg = _cfg(K, wid)
+    cfg.layout = K.LAYOUTS[layout]
     lay = K.kvq_layout(cfg)
     w = WL.WORKLOADS[wid]
-    assert lay.record_bytes == EXPECTED_RECORD_BYTES[wid]
-    assert lay.words_per_row == (12 if w.bits == 3 else -(-128 // (32 // w.bits)))
+    dec_bytes, rec_bytes = EXPECTED_DECODE_BYTES[wid], EXPECTED_RECORD_BYTES[wid]
+    if layout == "mma" and wid in EXPECTED_MMA:
+        dec_bytes, rec_bytes = EXPECTED_MMA[wid]
+    assert lay.record_bytes == rec_bytes
+    assert lay.words_per_row == (12 if w.bits == 3 and layout == "mma" else -(-128 // (32 // w.bits)))
     assert lay.format_version == 2
     for k in range(2):
         assert lay.codes_off[k] % 16 == 0 and lay.meta_off[k] % 16 == 0 and lay.csr_off[k] % 16 == 0
@@ -100,7 +107,7 @@ def test_layout_and_decode_bytes(K, wid):
         assert lay.rope_off % 128 == 0 and lay.rope_bytes == (w.n_blocks + 1 + 128) * 64 * 8
     if w.method == "nuq":
         assert lay.n_outliers == O.n_outliers(w.outlier_frac) == 164
-    assert K.kvq_decode_bytes(cfg, w.n_blocks) == EXPECTED_DECODE_BYTES[wid]
+    assert K.kvq_decode_bytes(cfg, w.n_blocks) == dec_bytes
     S = K.kvq_decode_splits(cfg, w.n_blocks)
     assert 1 <= S <= w.n_blocks
     # at least one partial (m, l, o[128]) per (batch, query head)
@@ -110,7 +117,8 @@ def test_layout_and_decode_bytes(K, wid):
 def test_config_checks(K):
     L = K._lib
     bad = [dict(head_dim=64), dict(block=64), dict(bits=5), dict(bits=1), dict(n_q_heads=33),
-           dict(n_q_heads=8 * 17), dict(max_blocks=0), dict(batch=0), dict(in_dtype=7), dict(method=9)]
+           dict(n_q_heads=8 * 17), dict(max_blocks=0), dict(batch=0), dict(in_dtype=7), dict(method=9),
+           dict(layout=2), dict(layout=-1)]
     for b in bad:
         cfg = _cfg(K, 4)
         for k, v in b.items():

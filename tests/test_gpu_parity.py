@@ -33,14 +33,19 @@ def _append_all(cache, w, K, V, chunks):
             cache.append(U.to_device(K[:, :, a * 128:b * 128], w.dtype), U.to_device(V[:, :, a * 128:b * 128], w.dtype))
 
 
-def _compare_exact(cache, oc, w, nb):
+def _oracle_cache(w, layout):
+    return O.OracleCache.for_workload(w, codebook=U.codebook_for(w)[0] if w.method == "nuq" else None,
+                                      layout=U.oracle_layout(layout))
+
+
+def _compare_exact(cache, oc, w, nb, layout):
     recs = U.records_np(cache)
     lay = cache.layout
     for b in range(w.batch):
         for h in range(w.n_kv_heads):
             for blk in range(nb):
                 for kind in (0, 1):
-                    got = U.tile_fields(recs[b, h, blk], lay, kind, w.method, w.bits)
+                    got = U.tile_fields(recs[b, h, blk], lay, kind, w.method, w.bits, layout)
                     exp = oc.recs[(b, h, blk, kind)]
                     where = f"b={b} h={h} blk={blk} kind={kind}"
                     assert np.array_equal(got["words"], exp["words"]), where + " code words"
@@ -70,20 +75,21 @@ CASES_EXACT = [
 ]
 
 
+@pytest.mark.parametrize("layout", ["rows", "mma"])
 @pytest.mark.parametrize("name,base,kw", CASES_EXACT, ids=[c[0] for c in CASES_EXACT])
-def test_append_records_bit_exact(name, base, kw):
+def test_append_records_bit_exact(name, base, kw, layout):
     w = base.scaled(**kw)
     nb = w.n_blocks
-    cache = U.new_cache(w)
+    cache = U.new_cache(w, layout=layout)
     K, V = WL.blocks(w, 0, nb)
     _append_all(cache, w, K, V, chunks=min(3, nb))
-    oc = O.OracleCache.for_workload(w, codebook=U.codebook_for(w)[0] if w.method == "nuq" else None)
+    oc = _oracle_cache(w, layout)
     oc.append(K, V)
-    _compare_exact(cache, oc, w, nb)
+    _compare_exact(cache, oc, w, nb, layout)
     assert cache.device_status() == 0
 
 
-def _varn_check_tile(got, exp, K_in, kind, dbg_rc):
+def _varn_check_tile(got, exp, K_in, kind, dbg_rc, layout):
     """KVarN exemptions (see module docstring). Returns counts of exempted differences."""
     r_o, c_o = exp["r"], exp["c"]
     assert np.all(np.abs(dbg_rc[0] - r_o) <= 1e-5 * np.abs(r_o)), "VarN token scales r"
@@ -117,7 +123,7 @@ def _varn_check_tile(got, exp, K_in, kind, dbg_rc):
     else:
         tt = Z32 / s[:, None] - z[:, None]
     e = np.clip(np.rint(tt), 0, 2 ** bits - 1)
-    codes = O.unpack_tile(got["words"], bits, kind).astype(np.int64)
+    codes = O.unpack_tile(got["words"], bits, kind, U.oracle_layout(layout)).astype(np.int64)
     diff = np.abs(codes - e)
     frac = np.abs(tt.astype(np.float64) - np.floor(tt.astype(np.float64)) - 0.5)
     near = frac <= 1e-5 * np.maximum(1.0, np.abs(tt))
@@ -126,15 +132,16 @@ def _varn_check_tile(got, exp, K_in, kind, dbg_rc):
     return n_ex
 
 
-def test_append_varn_exemptions():
+@pytest.mark.parametrize("layout", ["rows", "mma"])
+def test_append_varn_exemptions(layout):
     import torch
     w = WL.WORKLOADS[3].scaled(batch=2, n_kv_heads=2, n_q_heads=8, ctx=3 * 128)
     nb = w.n_blocks
-    cache = U.new_cache(w)
+    cache = U.new_cache(w, layout=layout)
     K, V = WL.blocks(w, 0, nb)
     dbg = torch.zeros((w.batch, w.n_kv_heads, nb, 2, 2, 128), dtype=torch.float32, device="cuda")
     cache.append(U.to_device(K, w.dtype), U.to_device(V, w.dtype), dbg_varn_scales=dbg)
-    oc = O.OracleCache.for_workload(w)
+    oc = _oracle_cache(w, layout)
     oc.append(K, V)
     dbg = dbg.cpu().numpy()
     recs = U.records_np(cache)
@@ -143,17 +150,17 @@ def test_append_varn_exemptions():
         for h in range(w.n_kv_heads):
             for blk in range(nb):
                 for kind in (0, 1):
-                    got = U.tile_fields(recs[b, h, blk], cache.layout, kind, "varn", 2)
-                    n_ex += _varn_check_tile(got, oc.recs[(b, h, blk, kind)], None, kind, dbg[b, h, blk, kind])
+                    got = U.tile_fields(recs[b, h, blk], cache.layout, kind, "varn", 2, layout)
+                    n_ex += _varn_check_tile(got, oc.recs[(b, h, blk, kind)], None, kind, dbg[b, h, blk, kind], layout)
     # exemptions must stay rare
     assert n_ex <= 0.001 * (w.batch * w.n_kv_heads * nb * 2 * 16384)
 
 
-def _run_decode(w, nb, n_tail, chunks=2, oracle_planes=False, step=0):
+def _run_decode(w, nb, n_tail, chunks=2, oracle_planes=False, step=0, layout="rows"):
     import torch
-    cache = U.new_cache(w, max_blocks=max(nb, 1))
+    cache = U.new_cache(w, max_blocks=max(nb, 1), layout=layout)
     K, V = WL.blocks(w, 0, nb) if nb else (None, None)
-    oc = O.OracleCache.for_workload(w, codebook=U.codebook_for(w)[0] if w.method == "nuq" else None)
+    oc = _oracle_cache(w, layout)
     if nb:
         _append_all(cache, w, K, V, chunks)
         oc.append(K, V)
@@ -190,11 +197,12 @@ DECODE_CASES = [
 ]
 
 
+@pytest.mark.parametrize("layout", ["rows", "mma"])
 @pytest.mark.parametrize("name,base,kw,tails", DECODE_CASES, ids=[c[0] for c in DECODE_CASES])
-def test_decode_parity(name, base, kw, tails):
+def test_decode_parity(name, base, kw, tails, layout):
     w = base.scaled(**kw)
     for n_tail in tails:
-        out, ref = _run_decode(w, w.n_blocks, n_tail, oracle_planes=(w.method == "varn"))
+        out, ref = _run_decode(w, w.n_blocks, n_tail, oracle_planes=(w.method == "varn"), layout=layout)
         err = np.max(np.abs(out - ref))
         assert err <= TOL, f"{name} tail={n_tail}: max abs err {err:.3e}"
 
@@ -205,13 +213,14 @@ def test_decode_shared_memory_sizes_in_any_order():
     kernel's shared-memory limit below what a later, larger one needs."""
     for frac in (0.01, 0.05, 0.0, 0.01, 0.05):
         w = WL.WORKLOADS[2].scaled(outlier_frac=frac, batch=1, n_kv_heads=2, n_q_heads=2, ctx=3 * 128)
-        out, ref = _run_decode(w, w.n_blocks, 0)
+        out, ref = _run_decode(w, w.n_blocks, 0, layout="mma")
         assert np.max(np.abs(out - ref)) <= TOL, f"outlier_frac={frac}"
 
 
-def test_decode_varn_own_planes():
+@pytest.mark.parametrize("layout", ["rows", "mma"])
+def test_decode_varn_own_planes(layout):
     w = WL.WORKLOADS[3].scaled(batch=1, n_kv_heads=2, n_q_heads=8, ctx=3 * 128)
-    out, ref = _run_decode(w, w.n_blocks, 17, oracle_planes=False)
+    out, ref = _run_decode(w, w.n_blocks, 17, oracle_planes=False, layout=layout)
     assert np.max(np.abs(out - ref)) <= TOL
 
 
@@ -223,15 +232,16 @@ def test_decode_tail_only(method):
     assert np.max(np.abs(out - ref)) <= TOL
 
 
+@pytest.mark.parametrize("layout", ["rows", "mma"])
 @pytest.mark.parametrize("name,base,kw", CASES_EXACT[1:8:2] + [("varn", WL.WORKLOADS[3], dict(batch=1, n_kv_heads=2, n_q_heads=2, ctx=2 * 128))],
                          ids=[c[0] for c in CASES_EXACT[1:8:2]] + ["varn"])
-def test_dequant_parity(name, base, kw):
+def test_dequant_parity(name, base, kw, layout):
     w = base.scaled(**kw)
     nb = w.n_blocks
-    cache = U.new_cache(w)
+    cache = U.new_cache(w, layout=layout)
     K, V = WL.blocks(w, 0, nb)
     cache.append(U.to_device(K, w.dtype), U.to_device(V, w.dtype))
-    oc = O.OracleCache.for_workload(w, codebook=U.codebook_for(w)[0] if w.method == "nuq" else None)
+    oc = _oracle_cache(w, layout)
     oc.append(K, V)
     for domain in (0, 1):
         dk, dv = cache.dequant(0, nb, domain)
@@ -241,7 +251,7 @@ def test_dequant_parity(name, base, kw):
                 for kind, got in ((0, dk), (1, dv)):
                     if w.method == "varn":   # compare the kernel's planes, dequantised by the oracle
                         recs = U.records_np(cache)
-                        ref = np.concatenate([oc.dequant_tile(U.tile_fields(recs[b, h, blk], cache.layout, kind, "varn", 2),
+                        ref = np.concatenate([oc.dequant_tile(U.tile_fields(recs[b, h, blk], cache.layout, kind, "varn", 2, layout),
                                                               kind, h, blk, "input" if domain else "stored")
                                               for blk in range(nb)])
                         tol = 1e-5 * (1 + np.abs(ref))

@@ -577,3 +577,29 @@ def test_varn_cache_decode_matches_dequantised_attention():
         Kd = np.concatenate([cache.dequant(0, h, 0, "input"), tk[0, h]])
         Vd = np.concatenate([cache.dequant(0, h, 1, "input"), tv[0, h]])
         assert np.allclose(got[0, j], O.attention(q[0, j][None], Kd, Vd)[0], rtol=1e-10, atol=1e-10)
+
+
+@pytest.mark.parametrize("bits", [2, 3, 4])
+def test_pack_tile_layouts(golden_dir, bits):
+    """Row layout: keys and values alike are token rows of the bit listing (13 words per 3-bit row).
+    Tensor-core layout: 3-bit tiles are the 48-byte-per-vector planes, 2/4-bit value tiles are
+    channel rows (the transpose), 2/4-bit key tiles are unchanged token rows."""
+    rng = np.random.default_rng(bits)
+    codes = rng.integers(0, 2 ** bits, size=(128, 128)).astype(np.uint8)
+    for kind in (O.KIND_K, O.KIND_V):
+        rows = O.pack_tile(codes, bits, kind, O.LAYOUT_ROWS)
+        assert rows.shape == (128, -(-128 // (32 // bits)))
+        assert np.array_equal(rows, O.pack_rows(codes, bits))
+        assert np.array_equal(O.unpack_tile(rows, bits, kind, O.LAYOUT_ROWS), codes)
+        mma = O.pack_tile(codes, bits, kind, O.LAYOUT_MMA)
+        assert np.array_equal(O.unpack_tile(mma, bits, kind, O.LAYOUT_MMA), codes)
+        if bits == 3:
+            assert rows.size * 4 == 128 * 52 and mma.size * 4 == 128 * 48
+            assert np.array_equal(mma, O.pack_tile3(codes, kind))
+        elif kind == O.KIND_V:
+            # channel row c holds the codes of tokens 0..127 of channel c
+            n = 32 // bits
+            c, t = 37, 2 * n + 3
+            assert (int(mma[c, t // n]) >> (bits * (t % n))) & (2 ** bits - 1) == codes[t, c]
+        else:
+            assert np.array_equal(mma, rows)

@@ -32,13 +32,14 @@ def _p(t):
     return None if t is None else C.c_void_p(t.data_ptr())
 
 
-def test_static_scratch_matches_workspace_decode_twice(K):
+@pytest.mark.parametrize("layout", ["rows", "mma"])
+def test_static_scratch_matches_workspace_decode_twice(K, layout):
     import torch
     L = K._lib
     lib = L.lib()
     # nuq3 with pre-RoPE keys and CSR outliers, several sequence splits per head
     w = WL.WORKLOADS[2].scaled(batch=1, n_kv_heads=4, n_q_heads=4, ctx=12 * 128)
-    cache = U.new_cache(w)
+    cache = U.new_cache(w, layout=layout)
     Kx, Vx = WL.blocks(w, 0, w.n_blocks)
     cache.append(U.to_device(Kx, w.dtype), U.to_device(Vx, w.dtype))
     assert K.kvq_decode_workspace_bytes(cache.cfg, cache.n_blocks) <= L.KVQ_STATIC_WORKSPACE_BYTES
