@@ -2,17 +2,19 @@
 // (one query head per KV head).
 //
 // Work split. The (b, h, block) sequence of the whole batch is cut into one contiguous range
-// per CTA (persistent: one wave). A CTA runs 12 warps that meet on mbarriers (every wait
-// bounded):
-//   4 aux warps       : stream each block record (K tile, V tile, fp16 metadata, CSR outliers)
-//                       plus the block's RoPE start-angle row into a ring stage with 1-D bulk
-//                       copies, build the block's shared score operands, turn the key outliers
-//                       into one additive score term per token and tag every value outlier with
-//                       its token;
+// per CTA (persistent: one wave). A CTA runs 4 warpgroups whose roles meet only on mbarriers
+// (every wait bounded):
+//   producer warp     : copies each block record (K tile, V tile, fp16 metadata, CSR outliers)
+//                       and the block's RoPE start-angle row into an NB-stage ring with 1-D bulk
+//                       copies, as soon as the consumers have released the stage;
+//   4 aux warps       : two groups taking alternate blocks; they build each block's shared score
+//                       operands, turn the key outliers into one additive score term per token
+//                       and tag every outlier with its token;
 //   8 consumer warps  : warp w owns tokens 16w..16w+15 of every block and keeps its own
 //                       flash-decode state (running max, sum, output), written as its own
 //                       partial (m, l, o[128]) at the end of each (b, h) segment; the combine
 //                       kernel merges the partials.
+// The consumer warpgroups run with 168 registers per thread, the others with 88 (setmaxnreg).
 //
 // Keys ([KVQ] §3.2 pre-RoPE quantisation, Algorithm 1 dequantisation, worked example step 5):
 // the key at absolute position n = n0 + t (n0 = 128 * block) is k_n = R(n) (s*C[q] + zp + o),
@@ -35,8 +37,14 @@ namespace kvq {
 namespace nuqdec {
 
 constexpr int NW = 8;               // consumer warps (16 tokens of each block per warp)
-constexpr int NAUX = 128;          // aux threads: copies, block operands, outlier terms
-constexpr int NTHREADS = NW * 32 + NAUX;
+constexpr int NAUX = 128;           // aux threads: two groups that take alternate blocks
+constexpr int AUX_GROUP = 64;       // threads of one aux group: one per channel pair, two tokens each
+constexpr int PRODUCER_WARP = NW + NAUX / 32;  // issues the bulk copies; the warpgroup's other 3 warps idle
+constexpr int NTHREADS = 512;       // 4 warpgroups: consumers (2), aux, producer
+// Register split (setmaxnreg): launched at 65536 / 512 = 128 per thread; the consumer warpgroups
+// take 168 and the others give back down to 88 (2 x 128 x 168 + 2 x 128 x 88 = 65536).
+constexpr int REGS_CONSUMER = 168, REGS_OTHER = 88;
+static_assert(2 * 128 * REGS_CONSUMER + 2 * 128 * REGS_OTHER <= 65536, "register split over the launch total");
 constexpr int ROPE_ROW = 64 * 8;    // bytes of one (cos, sin) row of 64 pairs
 constexpr int MAX_OUTLIERS = 2048;  // per tile, on this path
 constexpr float LOG2E_RSQRT_D = 1.4426950408889634f * 0.08838834764831845f;
@@ -45,14 +53,6 @@ constexpr float LOG2E_RSQRT_D = 1.4426950408889634f * 0.08838834764831845f;
 #define KVQ_NUQ_NB 8
 #endif
 constexpr int NB = KVQ_NUQ_NB;  // ring stages
-#ifndef KVQ_NUQ_LEAD
-#define KVQ_NUQ_LEAD 4
-#endif
-constexpr int LEAD = KVQ_NUQ_LEAD;  // blocks the aux warps may prepare ahead of the slowest consumer
-static_assert(LEAD >= 2 && LEAD < NB, "the ring must hold the lead plus the copies in flight");
-#ifndef KVQ_NUQ_PAIR
-#define KVQ_NUQ_PAIR 0
-#endif
 
 struct Args {
   Geo g;
@@ -79,24 +79,18 @@ struct Ops {
 struct Smem {
   float2 rope_loc[T * 64];  // (cos, sin) of t * theta_i, t = 0..127
   Ops op[NB];
-  float qb[2][D];           // aux: q rotated back by the block's start angle (by block parity)
+  float qb[2][D];           // per aux group: q rotated back by the block's start angle
   float outv[NW][D];        // value outliers weighted by p, per consumer warp
   uint64_t rec_full[NB];    // record and RoPE row landed (bulk copies)
-  uint64_t ops_full[NB];    // score operands and outlier terms ready (NAUX arrivals)
-  uint64_t done[NB];        // the consumer warps are done with the stage (NW arrivals)
-  // followed by NB x round16(n_outliers) bytes: the token of each value outlier, per stage
+  uint64_t ops_full[NB];    // score operands and outlier terms ready (AUX_GROUP arrivals)
+  uint64_t empty[NB];       // the consumer warps are done with the stage (NW arrivals)
+  // followed by NB x 2 x round16(n_outliers) bytes, per stage: the token of each key outlier,
+  // then the token of each value outlier
 };
-
-__device__ __forceinline__ void mma1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0, const float (&c)[4]) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%7,%8,%9,%10};"
-      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a0), "r"(a1), "r"(b0), "f"(c[0]), "f"(c[1]), "f"(c[2]), "f"(c[3]));
-}
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1, const float (&c)[4]) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%10,%11,%12,%13};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
@@ -136,155 +130,167 @@ __host__ __device__ inline long long range_of(long long x, long long total, long
   return ((x + 1) * N - 1) / total;
 }
 
-// Query of (b, h) pairs lane and lane+32, scaled by log2(e)/sqrt(128).
-__device__ __forceinline__ void load_q_pairs(const Args& a, long long u, int lane, float (&qv)[2][2]) {
+// Query pair pi of (b, h) = u, scaled by log2(e)/sqrt(128).
+__device__ __forceinline__ float2 load_q_pair(const Args& a, long long u, int pi) {
   const long long b = u / a.g.H, h = u - b * a.g.H;
   const uint16_t* qp = a.q + ((uint64_t)(b * a.g.Hq + h)) * D;
-#pragma unroll
-  for (int k = 0; k < 2; ++k) {
-    const int pi = lane + 32 * k;
-    qv[k][0] = load_in(qp + 2 * pi, a.g.in_bf16) * LOG2E_RSQRT_D;
-    qv[k][1] = load_in(qp + 2 * pi + 1, a.g.in_bf16) * LOG2E_RSQRT_D;
-  }
+  return make_float2(load_in(qp + 2 * pi, a.g.in_bf16) * LOG2E_RSQRT_D,
+                     load_in(qp + 2 * pi + 1, a.g.in_bf16) * LOG2E_RSQRT_D);
 }
 
-// __syncthreads_or over the NAUX aux threads (named barrier 1).
-__device__ __forceinline__ bool syncthreads_or_aux(bool pred) {
+// __syncthreads_or over the 64 threads of aux group grp (named barrier 1 + grp).
+__device__ __forceinline__ bool bar_or_group(int grp, bool pred) {
   uint32_t r;
   asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, 1, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.or.pred q, %2, 64, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)pred)
+      : "r"((uint32_t)pred), "r"(1 + grp)
       : "memory");
   return r != 0;
 }
 
+__device__ __forceinline__ void bar_group(int grp) { asm volatile("bar.sync %0, 64;" ::"r"(1 + grp) : "memory"); }
+
 __device__ __forceinline__ uint32_t stage_bytes(const Geo& g) { return (uint32_t)g.rec_bytes + ROPE_ROW; }
 
-// Aux warps (4 warps, 128 threads, named barrier 1). Lanes 0..2 of the first issue the copies
-// (K half, V half, RoPE start-angle row of each record) up to NBS - LEAD blocks ahead of the block
-// being prepared; a stage is reused once the consumer warps have signalled `done` for its
-// previous block. Per block, threads 0..63 build the score operands of channel pair ax (B
-// fragments, zero-point C tuples), threads 64..127 q_b of pair ax - 64; then thread ax handles
-// token ax: its key-outlier score term
-//     sk[t] = sum over the token's CSR entries (c, v) of v * (R(t)^T q_b)_c,
-// and the token tag of each of its value-outlier entries (the consumers scatter p_t * v).
+__device__ __forceinline__ const uint8_t* record_at(const Args& a, long long u, int blk) {
+  return a.base + ((uint64_t)u * a.g.max_blocks + (uint64_t)blk) * a.g.rec_bytes;
+}
+
+template <uint32_t R>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(R));
+}
+template <uint32_t R>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R));
+}
+
+// Producer warp: copies block p of the range into stage p % NBS once the consumer warps have
+// released the stage's previous block (NW arrivals on empty). A block's three copies (K half;
+// V half with the CSR; the block's RoPE start-angle row) go out as one instruction from three
+// lanes, and the lane triple rotates over blocks: a thread services its own bulk copies one
+// after another, a few hundred cycles each whatever their size, so copies from distinct lanes
+// overlap. Before leaving it waits (bounded) for the last copies it issued.
 template <int NBS>
-__device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows, int rows_stride, long long x0,
-                          int n, int ax) {
+__device__ void producer(const Args& a, Smem* sm, uint8_t* ring, long long x0, int n, int lane) {
   const Geo& g = a.g;
-  const uint32_t rec = (uint32_t)g.rec_bytes, sb = stage_bytes(g), khalf = g.codes_off[1];
-  const int n_out = g.n_out;
-  const int lane = ax & 31;
-  const bool copier = ax < 32;  // warp 0 of the group issues the copies (lane 0)
+  const uint32_t rec = (uint32_t)g.rec_bytes, khalf = g.codes_off[1], sb = stage_bytes(g);
   long long u = x0 / a.nb;
   int blk = (int)(x0 - u * a.nb);
-  int issued = 0, cblk = blk;
-  const uint8_t* csrc = a.base + ((uint64_t)u * g.max_blocks + (uint64_t)blk) * g.rec_bytes;
-  const uint8_t* rope_blk = a.base + g.rope_off;
-  auto bar_aux = []() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
-  auto issue = [&]() -> bool {  // warp 0: the next copy, once its stage is free; false on a timeout
-    const int s = issued % NBS;
-    if (issued >= NBS) {
-      const bool got = mbar_wait_bounded(&sm->done[s], (uint32_t)(((issued / NBS) - 1) & 1), a.status);
-      if (__any_sync(0xffffffffu, !got)) return false;
-    }
-    // Each issuing thread streams its bulk copies one after another, so the K half, the V half and
-    // the RoPE row of a record go out from three lanes.
-    if (lane == 0) mbar_arrive_expect_tx(&sm->rec_full[s], rec + ROPE_ROW);
-    __syncwarp();
-    if (lane < 3) {
-      fence_proxy_async();
-      uint8_t* dst = ring + (size_t)s * sb;
-      if (lane == 0) bulk_g2s(dst, csrc, khalf, &sm->rec_full[s]);
-      else if (lane == 1) bulk_g2s(dst + khalf, csrc + khalf, rec - khalf, &sm->rec_full[s]);
-      else bulk_g2s(dst + rec, rope_blk + (size_t)cblk * ROPE_ROW, ROPE_ROW, &sm->rec_full[s]);
-    }
-    ++issued;
-    if (++cblk == a.nb) {
-      cblk = 0;
-      csrc += (uint64_t)(g.max_blocks - a.nb + 1) * g.rec_bytes;
-    } else {
-      csrc += g.rec_bytes;
-    }
-    return true;
-  };
-  bool ok = true;
-  if (copier)
-    while (ok && issued < n && issued < NBS) ok = issue();
-
-  long long cur_u = -1;
-  const int pi = ax & 63;  // this thread's channel pair
-  float q0 = 0.0f, q1 = 0.0f;
+  int issued = 0;
   for (int p = 0; p < n; ++p) {
-    if (u != cur_u) {
-      cur_u = u;
-      const long long b = u / g.H, h = u - b * g.H;
-      const uint16_t* qp = a.q + ((uint64_t)(b * g.Hq + h)) * D;
-      q0 = load_in(qp + 2 * pi, g.in_bf16) * LOG2E_RSQRT_D;
-      q1 = load_in(qp + 2 * pi + 1, g.in_bf16) * LOG2E_RSQRT_D;
-    }
     const int s = p % NBS;
-    const bool got = ok && mbar_wait_bounded(&sm->rec_full[s], (uint32_t)((p / NBS) & 1), a.status);
-    if (syncthreads_or_aux(!got)) {
-      ok = false;
-      break;
+    if (p >= NBS) {
+      const bool got = mbar_wait_bounded(&sm->empty[s], (uint32_t)(((p / NBS) - 1) & 1), a.status);
+      if (__any_sync(0xffffffffu, !got)) break;
     }
-    const uint8_t* st = ring + (size_t)s * sb;
-    Ops& op = sm->op[s];
-    float* qb = sm->qb[p & 1];
-    {
-      const float2 cs = reinterpret_cast<const float2*>(st + rec)[pi];
-      const float qb0 = cs.x * q0 + cs.y * q1, qb1 = -cs.y * q0 + cs.x * q1;
-      if (ax < 64) {
-        const uint16_t* km = reinterpret_cast<const uint16_t*>(st + g.meta_off[0]);
-        const int kg = pi >> 2, tqp = pi & 3;
-        const float s0 = h2f(km[2 * pi]), s1 = h2f(km[2 * pi + 1]);
-        const float z0 = h2f(km[T + 2 * pi]), z1 = h2f(km[T + 2 * pi + 1]);
-        op.bk[2 * tqp][kg] = pack_h2(qb0 * s0, qb1 * s1);       // X column of pair pi
-        op.bk[2 * tqp + 1][kg] = pack_h2(qb1 * s0, -qb0 * s1);  // Y column
-        const float zx = qb0 * z0 + qb1 * z1, zy = qb1 * z0 - qb0 * z1;
-        const __half zxh = __float2half_rn(zx), zyh = __float2half_rn(zy);
-        op.bz[2 * tqp][kg] = pack_h2(zx, zx - __half2float(zxh));      // X column: (high, low)
-        op.bz[2 * tqp + 1][kg] = pack_h2(zy, zy - __half2float(zyh));  // Y column
-      } else {
-        *reinterpret_cast<float2*>(&qb[2 * pi]) = make_float2(qb0, qb1);
-      }
+    const int set = 3 * (p & 7), part = lane - set;  // lanes set .. set+2 copy this block
+    if (lane == set) mbar_arrive_expect_tx(&sm->rec_full[s], rec + ROPE_ROW);
+    __syncwarp();
+    if (part >= 0 && part < 3) {
+      fence_proxy_async();
+      const uint32_t off = part == 0 ? 0u : part == 1 ? khalf : rec;
+      const uint32_t bytes = part == 0 ? khalf : part == 1 ? rec - khalf : (uint32_t)ROPE_ROW;
+      const uint8_t* from = part == 2 ? a.base + g.rope_off + (size_t)blk * ROPE_ROW : record_at(a, u, blk) + off;
+      bulk_g2s(ring + (size_t)s * sb + off, from, bytes, &sm->rec_full[s]);
     }
-    float skt = 0.0f;
-    if (n_out > 0) {
-      bar_aux();  // q_b visible
-      const int t = ax;
-      const uint8_t* csr = st + g.csr_off[0];
-      const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
-      const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * n_out);
-      const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
-      const int e1 = min((int)rp[t + 1], n_out);
-      for (int e = min((int)rp[t], n_out); e < e1; ++e) {  // keys
-        const int c = col[e] & (D - 1);
-        const float2 cr = sm->rope_loc[t * 64 + (c >> 1)];
-        const float qa = qb[c & ~1], qc = qb[c | 1];
-        const float qq = (c & 1) ? (-cr.y * qa + cr.x * qc) : (cr.x * qa + cr.y * qc);
-        skt = fmaf(h2f(val[e]), qq, skt);
-      }
-      const uint16_t* rpv = reinterpret_cast<const uint16_t*>(st + g.csr_off[1] + 2 * n_out);
-      uint8_t* rw = rows + (size_t)s * rows_stride;
-      const int f1 = min((int)rpv[t + 1], n_out);
-      for (int e = min((int)rpv[t], n_out); e < f1; ++e) rw[e] = (uint8_t)t;  // values: token tags
-    }
-    op.sk[ax] = skt;
-    mbar_arrive(&sm->ops_full[s]);  // NAUX arrivals complete the phase
+    issued = p + 1;
     if (++blk == a.nb) {
       blk = 0;
       ++u;
     }
-    if (copier)
-      while (ok && issued < n && issued <= p + NBS - LEAD) ok = issue();
   }
-  // leave no copy in flight: wait (bounded) for the copies not yet seen complete
-  if (copier && !ok) {
-    for (int j = issued - NBS; j < issued; ++j)
-      if (j >= 0) mbar_wait_bounded(&sm->rec_full[j % NBS], (uint32_t)((j / NBS) & 1), nullptr, 200000000LL);
+  for (int p = max(0, issued - NBS); p < issued; ++p)
+    mbar_wait_bounded(&sm->rec_full[p % NBS], (uint32_t)((p / NBS) & 1), nullptr, 200000000LL);
+}
+
+// Aux warps: two groups of 64 threads, group grp preparing blocks grp, grp + 2, grp + 4, ... of
+// the range (named barrier 1 + grp), so each group has two block periods per block. Per block,
+// thread j of a group first handles channel pair j (score B operand, zero-point terms, q_b) and
+// tokens j and j + 64 (the token tag of each of their key- and value-outlier entries); then,
+// over the key-outlier entries e = j, j + 64, ..., it adds each entry's score term
+//     v * (R(t)^T q_b)_c    (entry e = (t, c, v) of the CSR)
+// to sk[t] with a shared-memory atomic. The consumers scatter p_t * v for the value outliers.
+template <int NBS>
+__device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows, int rows_stride, long long x0,
+                          int n, int ax) {
+  const Geo& g = a.g;
+  const uint32_t rec = (uint32_t)g.rec_bytes, sb = stage_bytes(g);
+  const int n_out = g.n_out;
+  const int grp = ax >> 6, j = ax & 63;
+  const int tag_bytes = (int)round16((uint64_t)n_out);
+  long long u = x0 / a.nb;
+  int blk = (int)(x0 - u * a.nb);
+  if (grp == 1 && ++blk == a.nb) {
+    blk = 0;
+    ++u;
+  }
+  long long cur_u = -1;
+  float2 qv = make_float2(0.0f, 0.0f);
+  float* qb = sm->qb[grp];
+  const int tA = j, tB = j + 64;
+  for (int p = grp; p < n; p += 2) {
+    if (u != cur_u) {
+      cur_u = u;
+      qv = load_q_pair(a, u, j);
+    }
+    const int s = p % NBS;
+    const bool got = mbar_wait_bounded(&sm->rec_full[s], (uint32_t)((p / NBS) & 1), a.status);
+    if (bar_or_group(grp, !got)) break;  // the consumers time out on their own waits
+    const uint8_t* st = ring + (size_t)s * sb;
+    Ops& op = sm->op[s];
+    {
+      const float2 cs = reinterpret_cast<const float2*>(st + rec)[j];
+      const float qb0 = cs.x * qv.x + cs.y * qv.y, qb1 = -cs.y * qv.x + cs.x * qv.y;
+      const uint16_t* km = reinterpret_cast<const uint16_t*>(st + g.meta_off[0]);
+      const int kg = j >> 2, tqp = j & 3;
+      const float s0 = h2f(km[2 * j]), s1 = h2f(km[2 * j + 1]);
+      const float z0 = h2f(km[T + 2 * j]), z1 = h2f(km[T + 2 * j + 1]);
+      op.bk[2 * tqp][kg] = pack_h2(qb0 * s0, qb1 * s1);       // X column of pair j
+      op.bk[2 * tqp + 1][kg] = pack_h2(qb1 * s0, -qb0 * s1);  // Y column
+      const float zx = qb0 * z0 + qb1 * z1, zy = qb1 * z0 - qb0 * z1;
+      const __half zxh = __float2half_rn(zx), zyh = __float2half_rn(zy);
+      op.bz[2 * tqp][kg] = pack_h2(zx, zx - __half2float(zxh));      // X column: (high, low)
+      op.bz[2 * tqp + 1][kg] = pack_h2(zy, zy - __half2float(zyh));  // Y column
+      *reinterpret_cast<float2*>(&qb[2 * j]) = make_float2(qb0, qb1);
+    }
+    op.sk[tA] = 0.0f;
+    op.sk[tB] = 0.0f;
+    if (n_out > 0) {
+      uint8_t* ktag = rows + (size_t)s * rows_stride;
+      uint8_t* vtag = ktag + tag_bytes;
+      const uint8_t* csr = st + g.csr_off[0];
+      const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * n_out);
+      const uint16_t* rpv = reinterpret_cast<const uint16_t*>(st + g.csr_off[1] + 2 * n_out);
+      {
+        const int ka0 = min((int)rp[tA], n_out), ka1 = min((int)rp[tA + 1], n_out);
+        const int kb0 = min((int)rp[tB], n_out), kb1 = min((int)rp[tB + 1], n_out);
+        const int va0 = min((int)rpv[tA], n_out), va1 = min((int)rpv[tA + 1], n_out);
+        const int vb0 = min((int)rpv[tB], n_out), vb1 = min((int)rpv[tB + 1], n_out);
+        for (int e = ka0; e < ka1; ++e) ktag[e] = (uint8_t)tA;
+        for (int e = kb0; e < kb1; ++e) ktag[e] = (uint8_t)tB;
+        for (int e = va0; e < va1; ++e) vtag[e] = (uint8_t)tA;
+        for (int e = vb0; e < vb1; ++e) vtag[e] = (uint8_t)tB;
+      }
+      bar_group(grp);  // q_b, the key tags and the zeroed sk visible
+      const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
+      const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
+      const int n_k = min((int)rp[T], n_out);
+      for (int e = j; e < n_k; e += AUX_GROUP) {
+        const int t = ktag[e] & (T - 1), c = col[e] & (D - 1);
+        const float2 cr = sm->rope_loc[t * 64 + (c >> 1)];
+        const float qa = qb[c & ~1], qc = qb[c | 1];
+        const float qq = (c & 1) ? (-cr.y * qa + cr.x * qc) : (cr.x * qa + cr.y * qc);
+        atomicAdd(&op.sk[t], h2f(val[e]) * qq);
+      }
+    }
+    mbar_arrive(&sm->ops_full[s]);  // AUX_GROUP arrivals complete the phase
+    blk += 2;
+    while (blk >= a.nb) {
+      blk -= a.nb;
+      ++u;
+    }
   }
 }
 
@@ -327,13 +333,12 @@ __device__ __forceinline__ void block_scores(const uint8_t* st, const Ops& op, u
   s1 += __shfl_xor_sync(0xffffffffu, s1, 2) + op.sk[t1];
 }
 
-// Value part of one block for a consumer warp: p' = p * s_token as high/low B columns, the
-// zero-point sum, the value outliers (entry e of the warp's token range goes to lane e mod 32,
-// which takes p of its token from the token's owner lane) and 8 m16n8k16 over the V codes.
-__device__ __forceinline__ void block_values(const uint8_t* st, const Geo& g, const uint8_t* rw, int warp, int lane,
-                                             int t0, int t1, int src_a, uint32_t xsel, uint32_t ysel, float p0,
-                                             float p1, uint32_t tl0, uint32_t tl1, uint32_t th0, uint32_t th1,
-                                             float* outv, float& z_w, float (&acc)[8][4]) {
+// Value product of one block for a consumer warp: p' = p * s_token as high/low B columns, the
+// zero-point sum and 8 m16n8k16 over the V codes.
+__device__ __forceinline__ void block_values(const uint8_t* st, const Geo& g, int warp, int lane, int t0, int t1,
+                                             int src_a, uint32_t xsel, uint32_t ysel, float p0, float p1,
+                                             uint32_t tl0, uint32_t tl1, uint32_t th0, uint32_t th1, float& z_w,
+                                             float (&acc)[8][4]) {
   const uint16_t* vm = reinterpret_cast<const uint16_t*>(st + g.meta_off[1]);
   uint32_t vb0, vb1;
   {
@@ -345,21 +350,6 @@ __device__ __forceinline__ void block_values(const uint8_t* st, const Geo& g, co
     const uint32_t x = (hi & xsel) | (lo & ysel);
     vb0 = __shfl_sync(0xffffffffu, x, src_a);
     vb1 = __shfl_sync(0xffffffffu, x, src_a + 16);
-  }
-  const int n_out = g.n_out;
-  if (n_out > 0) {
-    const uint8_t* csr = st + g.csr_off[1];
-    const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
-    const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * n_out);
-    const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
-    const int e0 = min((int)rp[16 * warp], n_out), e1 = min((int)rp[16 * warp + 16], n_out);
-    for (int e = e0 + lane; e - lane < e1; e += 32) {  // uniform trip count
-      const bool valid = e < e1;
-      const int t = valid ? rw[e] : t0;
-      const int src = 4 * (t & 7);
-      const float pa = __shfl_sync(0xffffffffu, p0, src), pb = __shfl_sync(0xffffffffu, p1, src);
-      if (valid) atomicAdd(&outv[col[e] & (D - 1)], ((t & 8) ? pb : pa) * h2f(val[e]));
-    }
   }
   uint32_t cw[6];
   const uint2* vp = reinterpret_cast<const uint2*>(st + g.codes_off[1] + warp * 768 + lane * 24);
@@ -375,12 +365,33 @@ __device__ __forceinline__ void block_values(const uint8_t* st, const Geo& g, co
   }
 }
 
-// Consumer warp w: tokens 16w..16w+15 of every block of the CTA's range, two blocks of the same
-// (b, h) at a time where it can (their scores feed one softmax update). Its flash-decode state
-// goes to its own partial row at the end of each (b, h) segment.
+// Value outliers of a consumer warp's tokens in one block: entry e of the warp's token range goes
+// to lane e mod 32, which takes p of its token from the token's owner lane (rw: the entries'
+// token tags).
+__device__ __forceinline__ void value_outliers(const uint8_t* st, const Geo& g, const uint8_t* rw, int warp, int lane,
+                                               int t0, float p0, float p1, float* outv) {
+  const int n_out = g.n_out;
+  const uint8_t* csr = st + g.csr_off[1];
+  const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
+  const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * n_out);
+  const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
+  const int e0 = min((int)rp[16 * warp], n_out), e1 = min((int)rp[16 * warp + 16], n_out);
+  for (int e = e0 + lane; e - lane < e1; e += 32) {  // uniform trip count
+    const bool valid = e < e1;
+    const int t = valid ? rw[e] : t0;
+    const int src = 4 * (t & 7);
+    const float pa = __shfl_sync(0xffffffffu, p0, src), pb = __shfl_sync(0xffffffffu, p1, src);
+    if (valid) atomicAdd(&outv[col[e] & (D - 1)], ((t & 8) ? pb : pa) * h2f(val[e]));
+  }
+}
+
+// Consumer warp w: tokens 16w..16w+15 of every block of the CTA's range. Within a (b, h) segment
+// the value product of block j and the scores of block j + 1 form one straight-line stretch, so
+// their dependency chains overlap. Its flash-decode state goes to its own partial row at the end
+// of each segment.
 template <int NBS>
-__device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uint8_t* rows, int rows_stride,
-                         long long R, long long x0, int n, int warp, int lane) {
+__device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uint8_t* rows, int rows_stride, long long R,
+                         long long x0, int n, int warp, int lane) {
   const Geo& g = a.g;
   const uint32_t sb = stage_bytes(g);
   const int gq = lane >> 2, tq = lane & 3;
@@ -397,131 +408,117 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
   const uint32_t xsel = tq == 0 ? 0xffffffffu : 0u;      // this lane sends p' high (tq 0) ...
   const uint32_t ysel = tq == 1 ? 0xffffffffu : 0u;      // ... or low (tq 1) or zero
   const int t0 = 16 * warp + gq, t1 = t0 + 8;
+  float* outv = sm->outv[warp];
+
+  auto wait_stage = [&](int i) -> bool {  // false when a wait gave up
+    const int s = i % NBS;
+    const uint32_t par = (uint32_t)((i / NBS) & 1);
+    const bool got = mbar_wait_bounded(&sm->ops_full[s], par, a.status) &&
+                     mbar_wait_bounded(&sm->rec_full[s], par, a.status);
+    return !__any_sync(0xffffffffu, !got);
+  };
+  auto release = [&](int s) {  // this warp is done with stage s
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm->empty[s]);
+  };
 
   long long u = x0 / a.nb;
   int blk = (int)(x0 - u * a.nb);
-  uint32_t tl0 = 0, tl1 = 0, th0 = 0, th1 = 0;
   float acc[8][4];
-  float m_w = -INFINITY, l_w = 0.0f, z_w = 0.0f;
-  long long cur_u = -1;
-  float* outv = sm->outv[warp];
-
-  auto flush = [&](long long uu) {
-    float lt = l_w, zt = z_w;  // replicated over tq: reduce over gq only
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      lt += __shfl_xor_sync(0xffffffffu, lt, o);
-      zt += __shfl_xor_sync(0xffffffffu, zt, o);
-    }
-    __syncwarp();
-    const long long b = uu / g.H, h = uu - b * g.H;
-    const long long slot = R - range_of(uu * a.nb, a.total, a.n_ranges);
-    if (slot >= 0 && slot < a.n_slots) {
-      const uint64_t row = (((uint64_t)(b * g.Hq + h)) * a.n_slots + slot) * NW + warp;
-      if (tq == 0) {
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-          const int c0 = 16 * mt + gq, c1 = c0 + 8;
-          a.ws_o[row * D + c0] = acc[mt][0] + acc[mt][1] + zt + outv[c0];
-          a.ws_o[row * D + c1] = acc[mt][2] + acc[mt][3] + zt + outv[c1];
-        }
-      }
-      if (lane == 0) {
-        a.ws_m[row] = m_w;
-        a.ws_l[row] = lt;
-      }
-    }
-    __syncwarp();
-  };
-
-  // Blocks i .. i+NBK-1 (same (b, h)); false when a wait gave up.
-  auto step = [&](int i, auto nbk) -> bool {
-    constexpr int NBK = decltype(nbk)::value;
-    int sidx[NBK];
-    bool got = true;
-#pragma unroll
-    for (int k = 0; k < NBK; ++k) {
-      sidx[k] = (i + k) % NBS;
-      const uint32_t par = (uint32_t)(((i + k) / NBS) & 1);
-      got = got && mbar_wait_bounded(&sm->ops_full[sidx[k]], par, a.status) &&
-            mbar_wait_bounded(&sm->rec_full[sidx[k]], par, a.status);
-    }
-    if (__any_sync(0xffffffffu, !got)) return false;  // the aux warps drain the copies in flight
-    float sv[NBK][2];
-#pragma unroll
-    for (int k = 0; k < NBK; ++k)
-      block_scores(ring + (size_t)sidx[k] * sb, sm->op[sidx[k]], g.codes_off[0], warp, lane, brow, zrow, ones, t0, t1,
-                   tl0, tl1, th0, th1, wcs, sv[k][0], sv[k][1]);
-    // online softmax over the NBK blocks' tokens of this warp (base 2)
-    float mloc = fmaxf(sv[0][0], sv[0][1]);
-#pragma unroll
-    for (int k = 1; k < NBK; ++k) mloc = fmaxf(mloc, fmaxf(sv[k][0], sv[k][1]));
-    mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
-    mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
-    mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
-    if (mloc > m_w) {  // warp-uniform; rare after the first blocks
-      const float al = exp2f(m_w - mloc);
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        acc[mt][0] *= al; acc[mt][1] *= al; acc[mt][2] *= al; acc[mt][3] *= al;
-      }
-      l_w *= al;
-      z_w *= al;
-      __syncwarp();
-#pragma unroll
-      for (int k = 0; k < 4; ++k) outv[lane + 32 * k] *= al;
-      __syncwarp();
-      m_w = mloc;
-    }
-#pragma unroll
-    for (int k = 0; k < NBK; ++k) {
-      const float p0 = exp2f(sv[k][0] - m_w), p1 = exp2f(sv[k][1] - m_w);
-      l_w += p0 + p1;
-      block_values(ring + (size_t)sidx[k] * sb, g, rows + (size_t)sidx[k] * rows_stride, warp, lane, t0, t1, src_a,
-                   xsel, ysel, p0, p1, tl0, tl1, th0, th1, outv, z_w, acc);
-    }
-    __syncwarp();
-    if (lane == 0) {
-#pragma unroll
-      for (int k = 0; k < NBK; ++k) mbar_arrive(&sm->done[sidx[k]]);  // this warp is done with the stages
-    }
-    return true;
-  };
-
   int i = 0;
   while (i < n) {
-    if (u != cur_u) {
-      if (cur_u >= 0) flush(cur_u);
-      cur_u = u;
+    const int iend = (int)min((long long)n, (long long)i + (a.nb - blk));  // this (b, h) segment
+    uint32_t tl0, tl1, th0, th1;
+    {
       const long long h = u % g.H;
       uint32_t hb[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) hb[j] = f2h_rn(__ldg(a.codebook + h * 8 + j));
+      for (int k = 0; k < 8; ++k) hb[k] = f2h_rn(__ldg(a.codebook + h * 8 + k));
       tl0 = (hb[0] & 0xffu) | (hb[1] & 0xffu) << 8 | (hb[2] & 0xffu) << 16 | (hb[3] & 0xffu) << 24;
       tl1 = (hb[4] & 0xffu) | (hb[5] & 0xffu) << 8 | (hb[6] & 0xffu) << 16 | (hb[7] & 0xffu) << 24;
       th0 = (hb[0] >> 8) | (hb[1] >> 8) << 8 | (hb[2] >> 8) << 16 | (hb[3] >> 8) << 24;
       th1 = (hb[4] >> 8) | (hb[5] >> 8) << 8 | (hb[6] >> 8) << 16 | (hb[7] >> 8) << 24;
+    }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) outv[lane + 32 * k] = 0.0f;
+    for (int k = 0; k < 4; ++k) outv[lane + 32 * k] = 0.0f;
 #pragma unroll
-      for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
-      m_w = -INFINITY;
-      l_w = 0.0f;
-      z_w = 0.0f;
+    for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
+    float m_w = -INFINITY, l_w = 0.0f, z_w = 0.0f;
+    __syncwarp();
+    if (!wait_stage(i)) return;
+    float sv0, sv1;
+    block_scores(ring + (size_t)(i % NBS) * sb, sm->op[i % NBS], g.codes_off[0], warp, lane, brow, zrow, ones, t0, t1,
+                 tl0, tl1, th0, th1, wcs, sv0, sv1);
+    for (int j = i; j < iend; ++j) {
+      const int s = j % NBS;
+      const uint8_t* st = ring + (size_t)s * sb;
+      // online softmax with block j's scores (base 2)
+      float mloc = fmaxf(sv0, sv1);
+      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
+      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
+      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
+      if (mloc > m_w) {  // warp-uniform; rare after the first blocks
+        const float al = exp2f(m_w - mloc);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          acc[mt][0] *= al; acc[mt][1] *= al; acc[mt][2] *= al; acc[mt][3] *= al;
+        }
+        l_w *= al;
+        z_w *= al;
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) outv[lane + 32 * k] *= al;
+        __syncwarp();
+        m_w = mloc;
+      }
+      const float p0 = exp2f(sv0 - m_w), p1 = exp2f(sv1 - m_w);
+      l_w += p0 + p1;
+      if (j + 1 < iend) {
+        if (!wait_stage(j + 1)) return;
+        const int s1 = (j + 1) % NBS;
+        block_values(st, g, warp, lane, t0, t1, src_a, xsel, ysel, p0, p1, tl0, tl1, th0, th1, z_w, acc);
+        block_scores(ring + (size_t)s1 * sb, sm->op[s1], g.codes_off[0], warp, lane, brow, zrow, ones, t0, t1, tl0,
+                     tl1, th0, th1, wcs, sv0, sv1);
+      } else {
+        block_values(st, g, warp, lane, t0, t1, src_a, xsel, ysel, p0, p1, tl0, tl1, th0, th1, z_w, acc);
+      }
+      if (g.n_out > 0)
+        value_outliers(st, g, rows + (size_t)s * rows_stride + round16((uint64_t)g.n_out), warp, lane, t0, p0, p1,
+                       outv);
+      release(s);
+    }
+    // the segment's partial row
+    {
+      float lt = l_w, zt = z_w;  // replicated over tq: reduce over gq only
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        lt += __shfl_xor_sync(0xffffffffu, lt, o);
+        zt += __shfl_xor_sync(0xffffffffu, zt, o);
+      }
+      __syncwarp();
+      const long long b = u / g.H, h = u - b * g.H;
+      const long long slot = R - range_of(u * a.nb, a.total, a.n_ranges);
+      if (slot >= 0 && slot < a.n_slots) {
+        const uint64_t row = (((uint64_t)(b * g.Hq + h)) * a.n_slots + slot) * NW + warp;
+        if (tq == 0) {
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) {
+            const int c0 = 16 * mt + gq, c1 = c0 + 8;
+            a.ws_o[row * D + c0] = acc[mt][0] + acc[mt][1] + zt + outv[c0];
+            a.ws_o[row * D + c1] = acc[mt][2] + acc[mt][3] + zt + outv[c1];
+          }
+        }
+        if (lane == 0) {
+          a.ws_m[row] = m_w;
+          a.ws_l[row] = lt;
+        }
+      }
       __syncwarp();
     }
-    const bool two = KVQ_NUQ_PAIR && i + 1 < n && blk + 1 < a.nb;  // the next block is in the same (b, h)
-    const bool ok = two ? step(i, std::integral_constant<int, 2>()) : step(i, std::integral_constant<int, 1>());
-    if (!ok) return;
-    const int adv = two ? 2 : 1;
-    i += adv;
-    blk += adv;
-    if (blk == a.nb) {
-      blk = 0;
-      ++u;
-    }
+    i = iend;
+    blk = 0;
+    ++u;
   }
-  if (cur_u >= 0) flush(cur_u);
 }
 
 template <int NBS>
@@ -531,7 +528,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
   uint8_t* ring = smem_raw;
   Smem* sm = reinterpret_cast<Smem*>(smem_raw + (size_t)NBS * stage_bytes(a.g));
   uint8_t* rows = reinterpret_cast<uint8_t*>(sm + 1);
-  const int rows_stride = (int)round16((uint64_t)a.g.n_out);
+  const int rows_stride = 2 * (int)round16((uint64_t)a.g.n_out);
   const long long R = blockIdx.x;
   if (R >= a.n_ranges) return;
   const long long x0 = R * a.total / a.n_ranges, x1 = (R + 1) * a.total / a.n_ranges;
@@ -549,18 +546,24 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
   if (tid == 0) {
     for (int s = 0; s < NBS; ++s) {
       mbar_init(&sm->rec_full[s], 1);
-      mbar_init(&sm->ops_full[s], NAUX);
-      mbar_init(&sm->done[s], NW);
+      mbar_init(&sm->ops_full[s], AUX_GROUP);
+      mbar_init(&sm->empty[s], NW);
     }
     fence_mbar_init();
   }
   __syncthreads();
-  if (warp >= NW) aux_warps<NBS>(a, sm, ring, rows, rows_stride, x0, n, tid - NW * 32);
-  else consumer<NBS>(a, sm, ring, rows, rows_stride, R, x0, n, warp, lane);
+  if (warp < NW) {
+    regs_inc<REGS_CONSUMER>();
+    consumer<NBS>(a, sm, ring, rows, rows_stride, R, x0, n, warp, lane);
+  } else {
+    regs_dec<REGS_OTHER>();
+    if (warp < PRODUCER_WARP) aux_warps<NBS>(a, sm, ring, rows, rows_stride, x0, n, tid - NW * 32);
+    else if (warp == PRODUCER_WARP) producer<NBS>(a, sm, ring, x0, n, lane);
+  }
 }
 
 size_t smem_bytes(const Geo& g) {
-  return (size_t)NB * ((size_t)g.rec_bytes + ROPE_ROW) + sizeof(Smem) + (size_t)NB * round16((uint64_t)g.n_out);
+  return (size_t)NB * ((size_t)g.rec_bytes + ROPE_ROW) + sizeof(Smem) + (size_t)NB * 2 * round16((uint64_t)g.n_out);
 }
 
 }  // namespace nuqdec
