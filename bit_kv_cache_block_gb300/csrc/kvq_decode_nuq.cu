@@ -365,24 +365,28 @@ __device__ __forceinline__ void block_values(const uint8_t* st, const Geo& g, in
   }
 }
 
-// Value outliers of a consumer warp's tokens in one block: entry e of the warp's token range goes
-// to lane e mod 32, which takes p of its token from the token's owner lane (rw: the entries'
-// token tags).
-__device__ __forceinline__ void value_outliers(const uint8_t* st, const Geo& g, const uint8_t* rw, int warp, int lane,
-                                               int t0, float p0, float p1, float* outv) {
+// Value outliers of a consumer warp's tokens in one block (rw: the entries' token tags). Entry e
+// of the warp's token range goes to lane (e - e0) mod 32, which takes p of its token from the
+// token's owner lane and adds p * v to the warp's outv. The first 32 entries are straight-line,
+// predicated code (it overlaps the tensor-core work it is placed with); later ones loop.
+__device__ __forceinline__ void value_outlier_span(const uint8_t* st, const Geo& g, int warp, int& e0, int& e1) {
+  const int n_out = g.n_out;
+  const uint16_t* rp = reinterpret_cast<const uint16_t*>(st + g.csr_off[1] + 2 * n_out);
+  e0 = min((int)rp[16 * warp], n_out);
+  e1 = min((int)rp[16 * warp + 16], n_out);
+}
+
+__device__ __forceinline__ void value_outlier_entry(const uint8_t* st, const Geo& g, const uint8_t* rw, int e, int e1,
+                                                    int t0, float p0, float p1, float* outv) {
   const int n_out = g.n_out;
   const uint8_t* csr = st + g.csr_off[1];
   const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
-  const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * n_out);
   const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
-  const int e0 = min((int)rp[16 * warp], n_out), e1 = min((int)rp[16 * warp + 16], n_out);
-  for (int e = e0 + lane; e - lane < e1; e += 32) {  // uniform trip count
-    const bool valid = e < e1;
-    const int t = valid ? rw[e] : t0;
-    const int src = 4 * (t & 7);
-    const float pa = __shfl_sync(0xffffffffu, p0, src), pb = __shfl_sync(0xffffffffu, p1, src);
-    if (valid) atomicAdd(&outv[col[e] & (D - 1)], ((t & 8) ? pb : pa) * h2f(val[e]));
-  }
+  const bool valid = e < e1;
+  const int t = valid ? rw[e] : t0;
+  const int src = 4 * (t & 7);
+  const float pa = __shfl_sync(0xffffffffu, p0, src), pb = __shfl_sync(0xffffffffu, p1, src);
+  if (valid) atomicAdd(&outv[col[e] & (D - 1)], ((t & 8) ? pb : pa) * h2f(val[e]));
 }
 
 // Consumer warp w: tokens 16w..16w+15 of every block of the CTA's range. Within a (b, h) segment
@@ -410,6 +414,11 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
   const int t0 = 16 * warp + gq, t1 = t0 + 8;
   float* outv = sm->outv[warp];
 
+  auto ready_now = [&](int i) -> bool {  // the stage of range block i is ready (no waiting)
+    const int s = i % NBS;
+    const uint32_t par = (uint32_t)((i / NBS) & 1);
+    return mbar_test_wait(&sm->ops_full[s], par) & mbar_test_wait(&sm->rec_full[s], par);
+  };
   auto wait_stage = [&](int i) -> bool {  // false when a wait gave up
     const int s = i % NBS;
     const uint32_t par = (uint32_t)((i / NBS) & 1);
@@ -452,6 +461,8 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
     for (int j = i; j < iend; ++j) {
       const int s = j % NBS;
       const uint8_t* st = ring + (size_t)s * sb;
+      const bool more = j + 1 < iend;  // warp-uniform
+      const bool ready = more ? ready_now(j + 1) : true;  // its latency overlaps the softmax
       // online softmax with block j's scores (base 2)
       float mloc = fmaxf(sv0, sv1);
       mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
@@ -473,18 +484,22 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
       }
       const float p0 = exp2f(sv0 - m_w), p1 = exp2f(sv1 - m_w);
       l_w += p0 + p1;
-      if (j + 1 < iend) {
-        if (!wait_stage(j + 1)) return;
+      const uint8_t* rw = rows + (size_t)s * rows_stride + round16((uint64_t)g.n_out);
+      int e0 = 0, e1 = 0;
+      if (g.n_out > 0) value_outlier_span(st, g, warp, e0, e1);
+      if (more) {
+        if (!__all_sync(0xffffffffu, ready) && !wait_stage(j + 1)) return;
         const int s1 = (j + 1) % NBS;
+        value_outlier_entry(st, g, rw, e0 + lane, e1, t0, p0, p1, outv);
         block_values(st, g, warp, lane, t0, t1, src_a, xsel, ysel, p0, p1, tl0, tl1, th0, th1, z_w, acc);
         block_scores(ring + (size_t)s1 * sb, sm->op[s1], g.codes_off[0], warp, lane, brow, zrow, ones, t0, t1, tl0,
                      tl1, th0, th1, wcs, sv0, sv1);
       } else {
+        value_outlier_entry(st, g, rw, e0 + lane, e1, t0, p0, p1, outv);
         block_values(st, g, warp, lane, t0, t1, src_a, xsel, ysel, p0, p1, tl0, tl1, th0, th1, z_w, acc);
       }
-      if (g.n_out > 0)
-        value_outliers(st, g, rows + (size_t)s * rows_stride + round16((uint64_t)g.n_out), warp, lane, t0, p0, p1,
-                       outv);
+      for (int e = e0 + 32 + lane; e - lane < e1; e += 32)  // more than 32 entries: uniform trip count
+        value_outlier_entry(st, g, rw, e, e1, t0, p0, p1, outv);
       release(s);
     }
     // the segment's partial row
