@@ -132,32 +132,33 @@ def unpack_rows(words: np.ndarray, bits: int) -> np.ndarray:
 # (its codes for the 128 tokens); 3-bit tiles take [KVQ] §9.3's other figure, 128 x 3 bits = 48
 # bytes per vector, which ten codes per word cannot reach: 128 x 128 codes in 1536 words, every
 # code's two low bits and its high bit in separate bit planes. The plane order follows the decode's
-# matrix fragments: the tile is cut into 16 segments of 8 tokens, each segment into 32 groups of
-# 32 codes (3 words each), and within a group the codes sit in 8 four-bit slots of 4 "nibble
+# matrix fragments: the tile is cut into 8 segments of 16 tokens, each segment into 32 groups of
+# 64 codes (6 words each), and within a group the codes sit in 8 four-bit slots of 8 "nibble
 # words" u (the low bits of nibble word u in word u//2 at bit 4k + 2(u%2), its high bit in word
-# 2 at bit 4k + (2, 3, 0, 1)[u], k = 0..7 the slot).
+# 4 + u//4 at bit 4k + (2, 3, 0, 1)[u%4], k = 0..7 the slot).
 LAYOUT_ROWS, LAYOUT_MMA = 0, 1
 TILE3_WORDS = 1536
 
 
 def tile3_slot(kind: int, t, c):
     """Where code (token t, channel c) of a 3-bit tile lives: (low-bits word, its shift,
-    high-bit word, its shift). Keys: group 4*(t%8) + (c%8)//2 of segment t//8, nibble word
-    c//32, slot 4*((c//16)%2) + 2*((c//8)%2) + c%2. Values: group 4*(c%8) + (t%8)//2 of
-    segment t//8, nibble word c//32, slot 4*((c//16)%2) + 2*((c//8)%2) + t%2."""
+    high-bit word, its shift). Keys: group 4*(t%8) + (c//2)%4 of segment t//16, nibble word
+    c//16, slot 4*((c//8)%2) + 2*((t%16)//8) + c%2. Values: group 4*(c%8) + t%4 of segment
+    t//16, nibble word c//16, slot 4*((t%16)//4 % 2) + 2*((c//8)%2) + (t%16)//8."""
     t = np.asarray(t, np.int64)
     c = np.asarray(c, np.int64)
-    seg = t >> 3
+    s, tl = t >> 4, t & 15
     if kind == KIND_K:
-        grp = 4 * (t & 7) + ((c & 7) >> 1)
-        k = 4 * ((c >> 4) & 1) + 2 * ((c >> 3) & 1) + (c & 1)
+        g, r = tl & 7, tl >> 3
+        tq, kg, j = (c >> 1) & 3, c >> 3, c & 1
+        u, k = kg >> 1, 4 * (kg & 1) + 2 * r + j
     else:
-        grp = 4 * (c & 7) + ((t & 7) >> 1)
-        k = 4 * ((c >> 4) & 1) + 2 * ((c >> 3) & 1) + (t & 1)
-    u = c >> 5
-    base = seg * 96 + grp * 3
-    hi_pos = np.array([2, 3, 0, 1])[u]
-    return base + (u >> 1), 4 * k + 2 * (u & 1), base + 2, 4 * k + hi_pos
+        tq, v = tl & 3, tl >> 2
+        g, r, mt = c & 7, (c >> 3) & 1, c >> 4
+        u, k = mt, 4 * (v & 1) + 2 * r + (v >> 1)
+    base = s * 192 + (4 * g + tq) * 6
+    hi_pos = np.array([2, 3, 0, 1])[u & 3]
+    return base + (u >> 1), 4 * k + 2 * (u & 1), base + 4 + (u >> 2), 4 * k + hi_pos
 
 
 def pack_tile3(codes: np.ndarray, kind: int) -> np.ndarray:

@@ -86,9 +86,9 @@ def test_tile3_swapped_high_bit_planes_are_caught(monkeypatch):
 
     def slot(kind, t, c):
         lw, ls, hw, hs = orig(kind, t, c)
-        u = np.asarray(c, np.int64) >> 5  # the nibble word, for keys and values alike
+        u = np.asarray(c, np.int64) >> 4  # the nibble word, for keys and values alike
         # high bits of nibble words 2 and 3 exchanged: still a valid permutation
-        return lw, ls, hw, np.where(u >= 2, hs ^ 1, hs)
+        return lw, ls, hw, np.where((u & 3) >= 2, hs ^ 1, hs)
     monkeypatch.setattr(K, "tile3_slot", slot)
     monkeypatch.setattr(O, "tile3_slot", slot)
     assert _fails(P.test_tile3_slots_follow_the_documented_rule)
@@ -98,8 +98,8 @@ def test_tile3_value_token_order_is_caught(monkeypatch):
     orig = K.tile3_slot
 
     def slot(kind, t, c):
-        if kind == K.KIND_V:  # tokens t and t^1 exchanged (the two tokens of a lane's fragment)
-            t = np.asarray(t, np.int64) ^ 1
+        if kind == K.KIND_V:  # tokens t and t^8 of each segment exchanged
+            t = np.asarray(t, np.int64) ^ 8
         return orig(kind, t, c)
     monkeypatch.setattr(K, "tile3_slot", slot)
     monkeypatch.setattr(O, "tile3_slot", slot)

@@ -94,56 +94,42 @@ def test_tile3_size_bijection_and_roundtrip(golden_dir):
 
 def test_tile3_slots_follow_the_documented_rule():
     """Hand-evaluated positions from the rule in the layout's description."""
-    # key (t=9, c=13): segment 1, t%8=1, (c%8)//2=2: group 6 (word base 96+18=114);
-    #   nibble word 13//32=0, slot 4*((13//16)%2=0) + 2*((13//8)%2=1) + 13%2=1 = 3
-    #   low bits: word 114, shift 4*3+0=12; high bit: word 116, shift 12+(2,3,0,1)[0]=14
-    assert tuple(int(x) for x in O.tile3_slot(O.KIND_K, 9, 13)) == (114, 12, 116, 14)
-    # key (t=50, c=100): segment 6, t%8=2, (c%8)//2=2: group 10 (base 576+30=606);
-    #   nibble word 100//32=3, slot 4*((100//16)%2=0) + 2*((100//8)%2=0) + 0 = 0
-    #   low bits: word 606+1, shift 0+2*1=2; high bit: word 608, shift 0+(2,3,0,1)[3]=1
-    assert tuple(int(x) for x in O.tile3_slot(O.KIND_K, 50, 100)) == (607, 2, 608, 1)
-    # value (t=23, c=45): segment 2, c%8=5, (t%8)//2=3: group 23 (base 192+69=261);
-    #   nibble word 45//32=1, slot 4*((45//16)%2=0) + 2*((45//8)%2=1) + 23%2=1 = 3
-    #   low bits: word 261, shift 12+2*1=14; high bit: word 263, shift 12+(2,3,0,1)[1]=15
-    assert tuple(int(x) for x in O.tile3_slot(O.KIND_V, 23, 45)) == (261, 14, 263, 15)
+    # key (t=9, c=13): segment 0, t%8=1, (t%16)//8=1, (c//2)%4=2, c//8=1, c%2=1
+    #   group 4*1+2=6 (word base 36), nibble word 13//16=0, slot 4*1+2*1+1=7
+    assert tuple(int(x) for x in O.tile3_slot(O.KIND_K, 9, 13)) == (36, 28, 40, 30)
+    # key (t=50, c=100): segment 3, t%16=2 -> g=2, r=0,
+    #   (c//2)%4=2, c//8=12, c%2=0: group 10 (base 3*192+60=636), nibble word 6, slot 0
+    #   low bits: word 636+3, shift 0; high bit: word 636+4+1, shift (2,3,0,1)[2] = 0
+    assert tuple(int(x) for x in O.tile3_slot(O.KIND_K, 50, 100)) == (639, 0, 641, 0)
+    # value (t=23, c=45): segment 1, t%16=7 -> t%4=3, (t%16)//4=1; c%8=5, (c//8)%2=1, c//16=2
+    #   group 4*5+3=23 (base 192+138=330), nibble word 2, slot 4*1+2*1+0=6
+    #   low bits: word 330+1, shift 24; high bit: word 330+4, shift 24+(2,3,0,1)[2]=24
+    assert tuple(int(x) for x in O.tile3_slot(O.KIND_V, 23, 45)) == (331, 24, 334, 24)
 
 
 @pytest.mark.parametrize("kind", [0, 1])
 def test_tile3_groups_hold_one_lanes_fragment_codes(kind):
-    """Group l = 4g + tq of segment s holds: keys, token 8s+g at the 32 channels c with
-    (c%8)//2 = tq; values, tokens 8s+2tq and 8s+2tq+1 at the 16 channels 16m+g and 16m+g+8.
-    Within the group, the four codes a matrix fragment takes together fill four consecutive
-    slots of one nibble word: keys, channels 16j+2tq, +1, +8, +9 (j = 0..7); values, channel
-    16j+g at tokens 8s+2tq, +1, then channel 16j+g+8 at the same two tokens."""
+    """Group l = 4g + tq of segment s holds: keys, tokens 16s+g and 16s+g+8 at the 32
+    channels c with (c//2)%4 = tq; values, tokens 16s+tq+4v (v = 0..3) at the 16 channels
+    16m+g and 16m+g+8."""
     t, c = np.meshgrid(np.arange(128), np.arange(128), indexing="ij")
-    lw, ls, hw, hs = O.tile3_slot(kind, t, c)
-    grp = lw // 3
-    assert np.array_equal(grp, hw // 3)
-    assert np.all(hw % 3 == 2) and np.all(lw % 3 < 2)
-    for s in (0, 11):
+    lw, _, hw, _ = O.tile3_slot(kind, t, c)
+    grp = lw // 6
+    assert np.array_equal(grp, hw // 6)
+    for s in (0, 5):
         for g in range(8):
             for tq in range(4):
                 sel = grp == s * 32 + 4 * g + tq
-                exp = np.zeros((128, 128), bool)
                 if kind == O.KIND_K:
-                    exp[8 * s + g, [ch for ch in range(128) if (ch % 8) // 2 == tq]] = True
+                    exp = np.zeros((128, 128), bool)
+                    for r in (0, 1):
+                        exp[16 * s + g + 8 * r, [ch for ch in range(128) if (ch // 2) % 4 == tq]] = True
                 else:
-                    for m in range(8):
-                        exp[8 * s + 2 * tq:8 * s + 2 * tq + 2, [16 * m + g, 16 * m + g + 8]] = True
+                    exp = np.zeros((128, 128), bool)
+                    for v in range(4):
+                        for m in range(8):
+                            exp[16 * s + tq + 4 * v, [16 * m + g, 16 * m + g + 8]] = True
                 assert np.array_equal(sel, exp)
-                # fragment order: (nibble word, slot) of each code of fragment j
-                for j in range(8):
-                    if kind == O.KIND_K:
-                        cells = [(8 * s + g, 16 * j + 2 * tq + e) for e in (0, 1, 8, 9)]
-                    else:
-                        cells = [(8 * s + 2 * tq + e, 16 * j + g + h) for h in (0, 8) for e in (0, 1)]
-                    tt = np.array([x[0] for x in cells])
-                    cc = np.array([x[1] for x in cells])
-                    lw1, ls1, _, _ = O.tile3_slot(kind, tt, cc)
-                    u = (lw1 % 3) * 2 + (ls1 % 4) // 2
-                    k = ls1 // 4
-                    assert np.all(u == j // 2), (kind, s, g, tq, j)
-                    assert np.array_equal(k, 4 * (j % 2) + np.arange(4)), (kind, s, g, tq, j)
 
 
 # ------------------------------------------------------------------ uniform RTN
