@@ -277,12 +277,30 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
       const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
       const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
       const int n_k = min((int)rp[T], n_out);
-      for (int e = j; e < n_k; e += AUX_GROUP) {
-        const int t = ktag[e] & (T - 1), c = col[e] & (D - 1);
+      auto key_term = [&](int e, int& t) {  // entry e < n_k: its token and score term
+        const int c = col[e] & (D - 1);
+        t = ktag[e] & (T - 1);
         const float2 cr = sm->rope_loc[t * 64 + (c >> 1)];
         const float qa = qb[c & ~1], qc = qb[c | 1];
         const float qq = (c & 1) ? (-cr.y * qa + cr.x * qc) : (cr.x * qa + cr.y * qc);
-        atomicAdd(&op.sk[t], h2f(val[e]) * qq);
+        return h2f(val[e]) * qq;
+      };
+      // up to 4 entries per thread side by side (1% of a tile is 164 entries): every load
+      // first, then the atomics; then any further entries one by one
+      float tv[4];
+      int tt[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        tt[k] = 0;
+        tv[k] = j + AUX_GROUP * k < n_k ? key_term(j + AUX_GROUP * k, tt[k]) : 0.0f;
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (j + AUX_GROUP * k < n_k) atomicAdd(&op.sk[tt[k]], tv[k]);
+      for (int e = j + 4 * AUX_GROUP; e < n_k; e += AUX_GROUP) {
+        int t;
+        const float v = key_term(e, t);
+        atomicAdd(&op.sk[t], v);
       }
     }
     mbar_arrive(&sm->ops_full[s]);  // AUX_GROUP arrivals complete the phase

@@ -227,12 +227,27 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Waits for phase `parity` of an mbarrier for at most ~`max_cycles` SM clocks. Returns false
 // (and records KVQ_ERR_TIMEOUT) when the wait gives up.
+// try_wait that may suspend the thread until the phase completes or about 1 ms passes, so a
+// waiting warp issues a few instructions per wait instead of spinning on the issue slots of
+// the warps it waits for.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
+      : "memory");
+  return ok != 0;
+}
+
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status,
                                                   long long max_cycles = 2000000000LL) {
   if (mbar_try_wait(bar, parity)) return true;
   long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity)) return true;
     if (clock64() - t0 > max_cycles) {
       report(status, KVQ_ERR_TIMEOUT);
       return false;
