@@ -39,6 +39,38 @@ DECODES_PER_STEP = 128
 # parity tests; its decode runs on the CUDA-core kernel.
 BENCH_LAYOUT = "mma"
 
+# DRAM traffic of the decode kernel per block record (dram__bytes_read.sum + dram__bytes_write.sum
+# of ncu captures of three launches, divided by the records one launch reads), by workload. A
+# launch reads every record once, so the traffic of a full launch is this figure times its
+# records. Each entry holds the sources it was measured on (sha256 of the kernel file and the
+# shared header); once they change the traffic reads null until a new capture replaces it.
+# Captures and commands: profiles/dram_traffic_decode_kernels.md.
+PROFILED_TRAFFIC = {
+    2: {"bytes_per_record": 14866.6, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
+        "sha256_16": "985d7f5939ed70db", "capture": "same workload at L = 16384 (4096 records)"},
+    3: {"bytes_per_record": 9790.3, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "447d708844969358", "capture": "full workload (8192 records)"},
+    4: {"bytes_per_record": 17086.6, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "447d708844969358", "capture": "same workload at L = 4096 (8192 records)"},
+    5: {"bytes_per_record": 9291.6, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "447d708844969358", "capture": "same workload at L = 65536 (16384 records)"},
+}
+
+
+def _profiled_traffic(cfg_id, records):
+    """DRAM bytes of one full decode launch from the captured per-record traffic, or (None, why)."""
+    import hashlib
+    e = PROFILED_TRAFFIC.get(cfg_id)
+    if e is None:
+        return None, "no capture for this workload"
+    m = hashlib.sha256()
+    for f in e["sources"]:
+        with open(os.path.join(ROOT, "bit_kv_cache_block_gb300", "csrc", f), "rb") as fh:
+            m.update(fh.read())
+    if m.hexdigest()[:16] != e["sha256_16"]:
+        return None, "kernel sources changed since the capture"
+    return round(e["bytes_per_record"] * records), f"ncu capture of the {e['capture']}, scaled by records"
+
 
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -270,6 +302,7 @@ def run_kvq(args):
     dec_avg_us = (1e3 * step_ms - app_us) / DECODES_PER_STEP
     peak, peak_kind = _peaks()
     achieved = cache_bytes / (dec0_us * 1e-6) / 1e9   # decode call with an empty tail
+    traffic, traffic_note = _profiled_traffic(w.cfg_id, w.batch * w.n_kv_heads * nb)
     res = {
         "metric": "quantized decode-attn packed-KV GB/s (% of 8 TB/s HBM), us/step; append tokens/s",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -291,7 +324,7 @@ def run_kvq(args):
         "timed_region_ms": round(total_ms, 3),
         "timing": "CUDA graph replays, CUDA events on the launching stream",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "traffic_source": traffic_note,
                      "kernel": _decode_kernel_name(w) + " + combine_kernel (kvq_decode_attn, empty tail)",
                      "peak_source": f"{peak_kind} hbm_gbs"},
         "gpu_launches": args.steps * (2 * DECODES_PER_STEP + 1),
