@@ -356,6 +356,9 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
 }
 
 constexpr int CB_THREADS = 512, CB_GROUPS = CB_THREADS / D;  // 4 thread groups of 128 channels
+// Words per staged tail-key row: 64 channel pairs padded to 68, so that the 32 lanes reading
+// pair 4j + q of tokens t (lane = 4t + q) hit 32 distinct banks (68t + q = 4t + q mod 32).
+constexpr int TK_STRIDE = 68;
 
 // Block-wide reductions over CB_THREADS threads (red: CB_THREADS/32 floats of scratch).
 __device__ __forceinline__ float cb_max(float v, float* red) {
@@ -384,7 +387,7 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
   __shared__ float ob[D];
   __shared__ float qv[D];
   __shared__ float sc[T];
-  __shared__ uint16_t tks[T - 1][D];  // tail keys (input dtype bits)
+  __shared__ uint32_t tkw[(T - 1) * TK_STRIDE];  // tail keys, one word per channel pair (input dtype bits)
   const Geo& g = a.g;
   const int tid = threadIdx.x, c = tid & (D - 1), grp = tid >> 7;
   const int hq = blockIdx.x, b = blockIdx.y, h = hq / g.G;
@@ -404,23 +407,35 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
   const float M = cb_max(mm, red);
   float Lg = 0.0f, Og = 0.0f;
   {
-    float Lp[2] = {0.0f, 0.0f}, Op[2] = {0.0f, 0.0f};
+    // four partials of the group per iteration, their loads side by side (they sit in L2)
+    float Lp[4] = {0.0f, 0.0f, 0.0f, 0.0f}, Op[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     int s = grp;
-    for (; s + CB_GROUPS < n_part; s += 2 * CB_GROUPS) {
+    for (; s + 3 * CB_GROUPS < n_part; s += 4 * CB_GROUPS) {
+      float mv[4], lv[4], ovv[4];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
+      for (int k = 0; k < 4; ++k) {
         const uint64_t r = row0 + s + k * CB_GROUPS;
-        const float f = exp2f(a.ws_m[r] - M);
-        Lp[k] = fmaf(a.ws_l[r], f, Lp[k]);
-        Op[k] = fmaf(a.ws_o[r * D + c], f, Op[k]);
+        mv[k] = a.ws_m[r];
+        lv[k] = a.ws_l[r];
+        ovv[k] = a.ws_o[r * D + c];
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float f = exp2f(mv[k] - M);
+        Lp[k] = fmaf(lv[k], f, Lp[k]);
+        Op[k] = fmaf(ovv[k], f, Op[k]);
       }
     }
-    if (s < n_part) {
+    for (; s < n_part; s += CB_GROUPS) {
       const uint64_t r = row0 + s;
       const float f = exp2f(a.ws_m[r] - M);
       Lp[0] = fmaf(a.ws_l[r], f, Lp[0]);
       Op[0] = fmaf(a.ws_o[r * D + c], f, Op[0]);
     }
+    Lp[0] += Lp[2];
+    Lp[1] += Lp[3];
+    Op[0] += Op[2];
+    Op[1] += Op[3];
     Lg = Lp[0] + Lp[1];
     Og = Op[0] + Op[1];
   }
@@ -442,7 +457,10 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
     const int nt = a.n_tail;
     const uint16_t* tk = a.tail_k + ((uint64_t)b * g.H + h) * nt * D;
     const uint16_t* tv = a.tail_v + ((uint64_t)b * g.H + h) * nt * D;
-    for (int e = tid; e < nt * D; e += CB_THREADS) tks[e >> 7][e & (D - 1)] = tk[e];
+    {
+      const uint32_t* tk2 = reinterpret_cast<const uint32_t*>(tk);  // channel pairs
+      for (int e = tid; e < nt * (D / 2); e += CB_THREADS) tkw[(e >> 6) * TK_STRIDE + (e & 63)] = tk2[e];
+    }
     const float2* rope_blk = reinterpret_cast<const float2*>(a.base + g.rope_off);
     const float2* rope_loc = rope_blk + (size_t)(g.max_blocks + 1) * 64;
     if (grp == 0) {
@@ -460,15 +478,16 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
     __syncthreads();
     if (grp == 0 && g.pre_rope) qv[c] = qr;
     __syncthreads();
-    // scores: token t = tid / 4, channel pairs 16*(tid%4) .. +15
+    // scores: token t = tid / 4, channel pairs 4j + tid%4 (j = 0..15)
     {
       const int t = tid >> 2, q4 = tid & 3;
       float acc = 0.0f;
       if (t < nt) {
 #pragma unroll 4
         for (int j = 0; j < 16; ++j) {
-          const int p = 16 * q4 + j;
-          float k0 = in_bits_to_f32(tks[t][2 * p], g.in_bf16), k1 = in_bits_to_f32(tks[t][2 * p + 1], g.in_bf16);
+          const int p = 4 * j + q4;
+          const uint32_t kw = tkw[t * TK_STRIDE + p];
+          float k0 = in_bits_to_f32((uint16_t)(kw & 0xffffu), g.in_bf16), k1 = in_bits_to_f32((uint16_t)(kw >> 16), g.in_bf16);
           if (g.pre_rope) {
             const float2 cs = rope_loc[t * 64 + p];
             const float r0 = cs.x * k0 - cs.y * k1, r1 = cs.y * k0 + cs.x * k1;
@@ -494,19 +513,20 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
       sc[tid] = pl;
     }
     L += cb_sum(pl, red);  // (also orders the sc[] stores)
-    // values: group grp sums tokens grp, grp+4, ...
-    float ov[2] = {0.0f, 0.0f};
+    // values: group grp sums tokens grp, grp+4, ..., four of them per iteration with their
+    // loads side by side
+    float ov[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     int j = grp;
-    for (; j + CB_GROUPS < nt; j += 2 * CB_GROUPS) {
+    for (; j + 3 * CB_GROUPS < nt; j += 4 * CB_GROUPS) {
+      float vv[4];
 #pragma unroll
-      for (int k = 0; k < 2; ++k) {
-        const int jj = j + k * CB_GROUPS;
-        ov[k] = fmaf(sc[jj], load_in(tv + (uint64_t)jj * D + c, g.in_bf16), ov[k]);
-      }
+      for (int k = 0; k < 4; ++k) vv[k] = load_in(tv + (uint64_t)(j + k * CB_GROUPS) * D + c, g.in_bf16);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ov[k] = fmaf(sc[j + k * CB_GROUPS], vv[k], ov[k]);
     }
-    if (j < nt) ov[0] = fmaf(sc[j], load_in(tv + (uint64_t)j * D + c, g.in_bf16), ov[0]);
+    for (; j < nt; j += CB_GROUPS) ov[0] = fmaf(sc[j], load_in(tv + (uint64_t)j * D + c, g.in_bf16), ov[0]);
     __syncthreads();
-    part[grp][c] = ov[0] + ov[1];
+    part[grp][c] = (ov[0] + ov[1]) + (ov[2] + ov[3]);
     __syncthreads();
     O += (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
   }

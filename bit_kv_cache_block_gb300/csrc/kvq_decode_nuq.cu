@@ -48,6 +48,9 @@ static_assert(2 * 128 * REGS_CONSUMER + 2 * 128 * REGS_OTHER <= 65536, "register
 constexpr int ROPE_ROW = 64 * 8;    // bytes of one (cos, sin) row of 64 pairs
 constexpr int MAX_OUTLIERS = 2048;  // per tile, on this path
 constexpr float LOG2E_RSQRT_D = 1.4426950408889634f * 0.08838834764831845f;
+// The running reference of a warp's softmax moves only when a score exceeds it by more than this
+// (base-2 units): probabilities then stay below 2^8, so p * s of a token stays far inside fp16.
+constexpr float RESCALE_SLACK = 8.0f;
 
 #ifndef KVQ_NUQ_NB
 #define KVQ_NUQ_NB 8
@@ -481,12 +484,16 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
       const uint8_t* st = ring + (size_t)s * sb;
       const bool more = j + 1 < iend;  // warp-uniform
       const bool ready = more ? ready_now(j + 1) : true;  // its latency overlaps the softmax
-      // online softmax with block j's scores (base 2)
-      float mloc = fmaxf(sv0, sv1);
-      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
-      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
-      mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
-      if (mloc > m_w) {  // warp-uniform; rare after the first blocks
+      // online softmax with block j's scores (base 2). m_w is the reference the warp's sums are
+      // kept relative to; it moves up only when a score passes it by more than RESCALE_SLACK, so
+      // p = 2^(s - m_w) stays below 2^RESCALE_SLACK and the usual block needs one vote instead of
+      // a max reduction.
+      if (__any_sync(0xffffffffu, fmaxf(sv0, sv1) > m_w + RESCALE_SLACK)) {  // rare after the first blocks
+        float mloc = fmaxf(sv0, sv1);
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
+        mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
+        mloc = fmaxf(mloc, m_w);
         const float al = exp2f(m_w - mloc);
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
