@@ -507,7 +507,7 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
-    ap.add_argument("--cpu-sample-heads", type=int, default=2)
+    ap.add_argument("--cpu-sample-heads", type=int, default=10)
     ap.add_argument("--ctx", type=int, default=0, help="override the context length (tokens, multiple of 128)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
