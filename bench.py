@@ -198,8 +198,13 @@ def run_kvq(args):
     if args.ctx:
         w = w.scaled(ctx=args.ctx)
     nb = w.n_blocks
+    n_pages = w.batch * (nb + 1) if args.paged else 0
     cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, nb + 1, w.dtype, w.pre_rope,
-                        w.rope_theta, w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT)
+                        w.rope_theta, w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT, n_pages)
+    table = None
+    if args.paged:  # every block on a page of a shuffled pool
+        perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(5 + rank)).to(torch.int32)
+        table = perm.view(w.batch, nb + 1)
     lay = K.kvq_layout(cfg)
     cb = None
     if w.method == "nuq":
@@ -210,12 +215,12 @@ def run_kvq(args):
         cb = torch.tensor([vals] * w.n_kv_heads, dtype=torch.float32)
     cache_bytes = K.kvq_decode_bytes(cfg, nb)
     n_copies = max(1, math.ceil(3 * L2_BYTES / max(1, int(lay.records_bytes))))
-    caches = [K.KVCache(cfg, cb, device=dev)]
+    caches = [K.KVCache(cfg, cb, device=dev, block_table=table)]
     Kd, Vd, tk, tv, q, gen = _inputs(w, torch, dev, rank)
     caches[0].append(Kd, Vd)
     del Kd, Vd
     for _ in range(n_copies - 1):
-        c = K.KVCache(cfg, cb, device=dev)
+        c = K.KVCache(cfg, cb, device=dev, block_table=table)
         c.base.copy_(caches[0].base)
         K.kvq_truncate(c.cache, 0)
         c.cache.n_blocks = nb
@@ -313,7 +318,8 @@ def run_kvq(args):
         "config": {"workload": w.name, "method": w.method, "bits": w.bits, "batch": w.batch,
                    "n_kv_heads": w.n_kv_heads, "n_q_heads": w.n_q_heads, "context": w.ctx,
                    "decodes_per_step": DECODES_PER_STEP, "tail_tokens": "0..127",
-                   "layout": BENCH_LAYOUT, "packed_bytes_per_decode": cache_bytes, "cache_copies": n_copies,
+                   "layout": BENCH_LAYOUT, "paged": bool(args.paged),
+                   "packed_bytes_per_decode": cache_bytes, "cache_copies": n_copies,
                    "l2": f"{n_copies} cache copies rotated ({n_copies * int(lay.records_bytes) / 2**20:.0f} MiB > 3x L2)",
                    "parallelism": f"replicas x{world}"},
         "pct_of_8TBs": round(100 * value / 8000, 2),
@@ -507,6 +513,8 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--paged", action="store_true",
+                    help="records on the pages of a shuffled pool, found through a block table")
     ap.add_argument("--cpu-sample-heads", type=int, default=10)
     ap.add_argument("--ctx", type=int, default=0, help="override the context length (tokens, multiple of 128)")
     args = ap.parse_args()

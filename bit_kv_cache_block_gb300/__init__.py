@@ -29,7 +29,7 @@ def lib_path() -> str:
 def make_config(method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: int, max_blocks: int,
                 in_dtype: str = "f16", pre_rope: bool = False, rope_theta: float = 10000.0,
                 outlier_frac: float = 0.01, varn_iters: int = 8, hadamard: bool = True,
-                layout: str = "rows") -> kvq_config:
+                layout: str = "rows", n_pages: int = 0) -> kvq_config:
     c = kvq_config()
     c.method = METHODS[method] if isinstance(method, str) else int(method)
     c.bits, c.batch, c.n_kv_heads, c.n_q_heads = bits, batch, n_kv_heads, n_q_heads
@@ -41,6 +41,7 @@ def make_config(method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: 
     c.varn_iters = int(varn_iters)
     c.hadamard = int(bool(hadamard))
     c.layout = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
+    c.n_pages = int(n_pages)
     return c
 
 
@@ -145,7 +146,9 @@ class KVCache:
     """Convenience owner of the device buffers of one cache (allocated by PyTorch) plus the
     decode workspace; every call goes through the C ABI above."""
 
-    def __init__(self, cfg: kvq_config, codebook=None, device="cuda", stream=None):
+    def __init__(self, cfg: kvq_config, codebook=None, device="cuda", stream=None, block_table=None):
+        """block_table: paged caches (cfg.n_pages > 0) only, int32 [B][max_blocks] of page ids;
+        default: sequence b's block blk on page b * max_blocks + blk (needs n_pages >= B * max_blocks)."""
         import torch
         self.cfg = cfg
         self.layout = kvq_layout(cfg)
@@ -154,6 +157,11 @@ class KVCache:
         self.status = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.codebook = None if codebook is None else codebook.to(self.device, torch.float32).contiguous()
         self.cache = kvq_cache_init(cfg, self.base, self.codebook, self.status, stream)
+        self.block_table = None
+        if cfg.n_pages > 0:
+            if block_table is None:
+                block_table = torch.arange(cfg.batch * cfg.max_blocks, dtype=torch.int32).view(cfg.batch, cfg.max_blocks)
+            self.set_block_table(block_table)
         self.workspace = torch.empty(max(16, kvq_decode_workspace_bytes(cfg, cfg.max_blocks)),
                                      dtype=torch.uint8, device=self.device)
 
@@ -187,11 +195,24 @@ class KVCache:
         kvq_dequant(self.cache, first_block, n_blocks, domain, ok, ov, stream)
         return ok, ov
 
+    def set_block_table(self, table):
+        """Binds a page table (int32 [B][max_blocks]); it is read by every later call."""
+        import torch
+        t = table.to(self.device, torch.int32).contiguous()
+        if tuple(t.shape) != (self.cfg.batch, self.cfg.max_blocks):
+            raise ValueError("block table must be [batch][max_blocks]")
+        self.block_table = t
+        self.cache.block_table = t.data_ptr()
+
     def device_status(self) -> int:
         return int(self.status.item())
 
     def record_view(self):
-        """The records as a uint8 tensor [B][H_kv][max_blocks][record_bytes] (for checking)."""
+        """The records as a uint8 tensor (for checking): [B][H_kv][max_blocks][record_bytes], or
+        for paged caches the pool [n_pages][H_kv][record_bytes]."""
         c = self.cfg
-        n = c.batch * c.n_kv_heads * c.max_blocks * int(self.layout.record_bytes)
-        return self.base[:n].view(c.batch, c.n_kv_heads, c.max_blocks, int(self.layout.record_bytes))
+        rb = int(self.layout.record_bytes)
+        if c.n_pages > 0:
+            return self.base[:c.n_pages * c.n_kv_heads * rb].view(c.n_pages, c.n_kv_heads, rb)
+        n = c.batch * c.n_kv_heads * c.max_blocks * rb
+        return self.base[:n].view(c.batch, c.n_kv_heads, c.max_blocks, rb)

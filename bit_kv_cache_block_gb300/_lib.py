@@ -12,7 +12,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libkvq.so")
 
 KVQ_OK, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED, KVQ_ERR_CAPACITY, KVQ_ERR_ALIGNMENT, KVQ_ERR_CUDA, \
-    KVQ_ERR_TIMEOUT = range(7)
+    KVQ_ERR_TIMEOUT, KVQ_ERR_PAGE = range(8)
 KVQ_RTN, KVQ_NUQ, KVQ_VARN, KVQ_INT4 = range(4)
 KVQ_F16, KVQ_BF16 = 0, 1
 KVQ_LAYOUT_ROWS, KVQ_LAYOUT_MMA = 0, 1
@@ -32,7 +32,7 @@ class kvq_config(C.Structure):
                 ("n_q_heads", C.c_int32), ("head_dim", C.c_int32), ("block", C.c_int32),
                 ("max_blocks", C.c_int32), ("in_dtype", C.c_int32), ("pre_rope", C.c_int32),
                 ("rope_theta", C.c_double), ("outlier_frac", C.c_float), ("varn_iters", C.c_int32),
-                ("hadamard", C.c_int32), ("layout", C.c_int32)]
+                ("hadamard", C.c_int32), ("layout", C.c_int32), ("n_pages", C.c_int32)]
 
 
 class kvq_layout_t(C.Structure):
@@ -45,7 +45,8 @@ class kvq_layout_t(C.Structure):
 
 class kvq_cache(C.Structure):
     _fields_ = [("cfg", kvq_config), ("lay", kvq_layout_t), ("base", C.c_void_p), ("codebook", C.c_void_p),
-                ("dev_status", C.c_void_p), ("n_blocks", C.c_int32), ("device", C.c_int32)]
+                ("dev_status", C.c_void_p), ("n_blocks", C.c_int32), ("device", C.c_int32),
+                ("block_table", C.c_void_p)]
 
 
 _lib = None

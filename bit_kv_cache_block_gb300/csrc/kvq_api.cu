@@ -11,7 +11,7 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
                               int n_split, float* ws, float* out, int* status, int hadamard, cudaStream_t st);
 size_t kvq_decode_ws_floats(const kvq::Geo& g, int n_blocks, int v1_splits);
 cudaError_t kvq_launch_dequant(const kvq::Geo& g, const uint8_t* base, const float* codebook, int first, int n,
-                               int domain, int hadamard, float* out_k, float* out_v, cudaStream_t st);
+                               int domain, int hadamard, float* out_k, float* out_v, int* status, cudaStream_t st);
 cudaError_t kvq_launch_rope_init(float2* tab, int max_blocks, double theta, cudaStream_t st);
 cudaError_t kvq_static_workspace(float** ptr, size_t* n_floats);
 
@@ -31,6 +31,7 @@ kvq_status check_config(const kvq_config* c) {
   if (c->in_dtype != KVQ_F16 && c->in_dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARG;
   if (c->bits < 2 || c->bits > 4) return KVQ_ERR_UNSUPPORTED;
   if (c->layout != KVQ_LAYOUT_ROWS && c->layout != KVQ_LAYOUT_MMA) return KVQ_ERR_INVALID_ARG;
+  if (c->n_pages < 0 || c->n_pages > (1 << 28)) return KVQ_ERR_INVALID_ARG;
   if (c->method == KVQ_INT4 && c->bits != 4) return KVQ_ERR_UNSUPPORTED;
   if (c->pre_rope != 0 && c->pre_rope != 1) return KVQ_ERR_INVALID_ARG;
   if (c->pre_rope && c->method != KVQ_NUQ) return KVQ_ERR_UNSUPPORTED;
@@ -56,6 +57,17 @@ kvq_status on_device(int dev, F fn) {
 
 int hadamard_of(const kvq_config& c) { return c.method == KVQ_VARN ? c.hadamard : 0; }
 
+// Kernel parameters of a cache; paged caches need their block table (non-null, 4-byte aligned).
+kvq_status geo_of(const kvq_cache* cache, kvq::Geo& g) {
+  g = kvq::make_geo(cache->cfg, cache->lay);
+  if (cache->cfg.n_pages > 0) {
+    if (!cache->block_table) return KVQ_ERR_INVALID_ARG;
+    if (!aligned(cache->block_table, 4)) return KVQ_ERR_ALIGNMENT;
+    g.table = cache->block_table;
+  }
+  return KVQ_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -69,6 +81,7 @@ const char* kvq_status_str(kvq_status s) {
     case KVQ_ERR_ALIGNMENT: return "misaligned pointer";
     case KVQ_ERR_CUDA: return "CUDA error";
     case KVQ_ERR_TIMEOUT: return "device wait timed out";
+    case KVQ_ERR_PAGE: return "block table entry out of range";
   }
   return "unknown status";
 }
@@ -97,7 +110,8 @@ kvq_status kvq_layout(const kvq_config* c, kvq_layout_t* out) {
     l.csr_off[k] = off; l.csr_bytes[k] = csr; off += csr;
   }
   l.record_bytes = off;
-  l.records_bytes = (uint64_t)c->batch * c->n_kv_heads * (uint64_t)c->max_blocks * l.record_bytes;
+  l.records_bytes = c->n_pages > 0 ? (uint64_t)c->n_pages * c->n_kv_heads * l.record_bytes
+                                   : (uint64_t)c->batch * c->n_kv_heads * (uint64_t)c->max_blocks * l.record_bytes;
   l.rope_off = (l.records_bytes + 127) & ~uint64_t(127);
   l.rope_bytes = c->pre_rope ? (uint64_t)((c->max_blocks + 1) + kvq::T) * 64 * 8 : 0;
   l.total_bytes = c->pre_rope ? l.rope_off + l.rope_bytes : l.records_bytes;
@@ -151,7 +165,8 @@ kvq_status kvq_append_block(kvq_cache* cache, const void* k, const void* v, int3
   if (dbg_varn_scales && !aligned(dbg_varn_scales, 16)) return KVQ_ERR_ALIGNMENT;
   if (n_blocks > 65535) return KVQ_ERR_INVALID_ARG;
   if ((int64_t)cache->n_blocks + n_blocks > cache->cfg.max_blocks) return KVQ_ERR_CAPACITY;
-  const kvq::Geo g = kvq::make_geo(cache->cfg, cache->lay);
+  kvq::Geo g;
+  if (kvq_status gs = geo_of(cache, g); gs != KVQ_OK) return gs;
   float* dbg = cache->cfg.method == KVQ_VARN ? dbg_varn_scales : nullptr;
   kvq_status s = on_device(cache->device, [&]() {
     return kvq_launch_append(g, static_cast<const uint16_t*>(k), static_cast<const uint16_t*>(v), n_blocks,
@@ -214,7 +229,8 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const void* ta
   if (nb + n_tail == 0) return KVQ_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16)) return KVQ_ERR_ALIGNMENT;
   if (n_tail > 0 && (!aligned(tail_k, 16) || !aligned(tail_v, 16))) return KVQ_ERR_ALIGNMENT;
-  const kvq::Geo g = kvq::make_geo(cache->cfg, cache->lay);
+  kvq::Geo g;
+  if (kvq_status gs = geo_of(cache, g); gs != KVQ_OK) return gs;
   const int S = kvq_decode_splits(&cache->cfg, nb);
   const size_t need = kvq_decode_ws_floats(g, nb, S) * sizeof(float);
   if (nb > 0) {
@@ -240,7 +256,8 @@ kvq_status kvq_decode_attn_static(const kvq_cache* cache, const void* q, const v
   if (nb + n_tail == 0) return KVQ_ERR_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(out, 16)) return KVQ_ERR_ALIGNMENT;
   if (n_tail > 0 && (!aligned(tail_k, 16) || !aligned(tail_v, 16))) return KVQ_ERR_ALIGNMENT;
-  const kvq::Geo g = kvq::make_geo(cache->cfg, cache->lay);
+  kvq::Geo g;
+  if (kvq_status gs = geo_of(cache, g); gs != KVQ_OK) return gs;
   const int S = kvq_decode_splits(&cache->cfg, nb);
   const size_t need = kvq_decode_ws_floats(g, nb, S) * sizeof(float);
   if (need > KVQ_STATIC_WORKSPACE_BYTES) return KVQ_ERR_CAPACITY;
@@ -272,10 +289,11 @@ kvq_status kvq_dequant(const kvq_cache* cache, int32_t first_block, int32_t n_bl
   if (domain != 0 && domain != 1) return KVQ_ERR_INVALID_ARG;
   if (!out_k && !out_v) return KVQ_ERR_INVALID_ARG;
   if ((out_k && !aligned(out_k, 16)) || (out_v && !aligned(out_v, 16))) return KVQ_ERR_ALIGNMENT;
-  const kvq::Geo g = kvq::make_geo(cache->cfg, cache->lay);
+  kvq::Geo g;
+  if (kvq_status gs = geo_of(cache, g); gs != KVQ_OK) return gs;
   return on_device(cache->device, [&]() {
     return kvq_launch_dequant(g, static_cast<const uint8_t*>(cache->base), cache->codebook, first_block, n_blocks,
-                              domain, hadamard_of(cache->cfg), out_k, out_v, stream);
+                              domain, hadamard_of(cache->cfg), out_k, out_v, cache->dev_status, stream);
   });
 }
 

@@ -234,7 +234,7 @@ __global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
   }
   __syncthreads();
 
-  uint8_t* rec = a.base + record_index(g, b, h, blk) * g.rec_bytes;
+  uint8_t* rec = a.base + record_offset(g, b, h, blk, a.status);
   uint32_t* codes_dst = reinterpret_cast<uint32_t*>(rec + g.codes_off[kind]);
   uint16_t* m16 = reinterpret_cast<uint16_t*>(rec + g.meta_off[kind]);
   const int axis = kind == 0 ? 0 : 1;  // keys per channel, values per token

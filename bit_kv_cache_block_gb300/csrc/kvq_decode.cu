@@ -99,7 +99,6 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
   const int blk_begin = (int)((long long)nb * split / a.n_split);
   const int blk_end = (int)((long long)nb * (split + 1) / a.n_split);
   const int n_my = blk_end - blk_begin;
-  const uint8_t* rec0 = a.base + record_index(g, b, h, 0) * g.rec_bytes;
 
   if (tid == 0) {
     for (int s = 0; s < NSTAGE; ++s) mbar_init(&sm->bar[s], 1);
@@ -107,7 +106,7 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
     fence_proxy_async();
     for (int s = 0; s < NSTAGE && s < n_my; ++s) {
       mbar_arrive_expect_tx(&sm->bar[s], (uint32_t)rec);
-      bulk_g2s(stages + s * rec, rec0 + (uint64_t)(blk_begin + s) * g.rec_bytes, (uint32_t)rec, &sm->bar[s]);
+      bulk_g2s(stages + s * rec, a.base + record_offset(g, b, h, blk_begin + s, a.status), (uint32_t)rec, &sm->bar[s]);
     }
   }
   // queries of this KV head's group
@@ -276,19 +275,33 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
         l_run[k] = l_run[k] * alpha[k] +
                    ((sm->red[1][k][0] + sm->red[1][k][1]) + (sm->red[1][k][2] + sm->red[1][k][3]));
 
-    if (METHOD == KVQ_NUQ && g.n_out > 0) {  // value outliers of row t, weighted by p
+    if (METHOD == KVQ_NUQ && g.n_out > 0) {  // value outliers, weighted by p
       const uint8_t* csr = st + g.csr_off[1];
       const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
       const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * g.n_out);
       const uint8_t* col = csr + 2 * g.n_out + 2 * (T + 1);
-      const int j1 = min((int)rp[t + 1], g.n_out);
-      for (int j = min((int)rp[t], g.n_out); j < j1; ++j) {
-        const int c = col[j] & (D - 1);
+      uint8_t* vtag = reinterpret_cast<uint8_t*>(sm + 1);  // the token of each entry
+      {
+        const int j1 = min((int)rp[t + 1], g.n_out);
+        for (int j = min((int)rp[t], g.n_out); j < j1; ++j) vtag[j] = (uint8_t)t;
+      }
+      __syncthreads();
+      // thread c adds the entries of channel c in entry order (the sum does not depend on timing)
+      const int c = tid, n_v = min((int)rp[T], g.n_out);
+      float acc[GMAX];
+#pragma unroll
+      for (int k = 0; k < GMAX; ++k) acc[k] = 0.0f;
+      for (int j = 0; j < n_v; ++j) {
+        if ((col[j] & (D - 1)) != c) continue;
+        const int tj = vtag[j];
         const float v = h2f(val[j]);
 #pragma unroll
         for (int k = 0; k < GMAX; ++k)
-          if (k < G) atomicAdd(&sm->osp[k][c], sm->pv[k][t] * v);
+          if (k < G) acc[k] = fmaf(sm->pv[k][tj], v, acc[k]);
       }
+#pragma unroll
+      for (int k = 0; k < GMAX; ++k)
+        if (k < G) sm->osp[k][c] += acc[k];
       __syncthreads();
     }
 
@@ -329,7 +342,7 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
     if (tid == 0 && i + NSTAGE < n_my) {
       fence_proxy_async();
       mbar_arrive_expect_tx(&sm->bar[s], (uint32_t)rec);
-      bulk_g2s(stages + s * rec, rec0 + (uint64_t)(blk + NSTAGE) * g.rec_bytes, (uint32_t)rec, &sm->bar[s]);
+      bulk_g2s(stages + s * rec, a.base + record_offset(g, b, h, blk + NSTAGE, a.status), (uint32_t)rec, &sm->bar[s]);
     }
   }
 
@@ -535,7 +548,7 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
 
 template <int METHOD, int GMAX>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
-  size_t smem = (size_t)NSTAGE * a.g.rec_bytes + sizeof(DecSmem<GMAX>);
+  size_t smem = (size_t)NSTAGE * a.g.rec_bytes + sizeof(DecSmem<GMAX>) + round16((uint64_t)a.g.n_out);
   cudaError_t e = ensure_smem_attr((const void*)decode_kernel<METHOD, GMAX>, (size_t)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_split, a.g.H, a.g.B);

@@ -314,8 +314,9 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
   long long u = x0 / a.nb;
   int blk = (int)(x0 - u * a.nb);
   const int n_units = WHOLE ? n : 2 * n;  // copies: whole records, or K and V halves
-  int pnext = 0, pbuf = 0, pblk = blk;  // next copy to issue, its buffer, its block
-  const uint8_t* psrc = a.base + ((uint64_t)u * g.max_blocks + (uint64_t)blk) * g.rec_bytes;
+  int pnext = 0, pbuf = 0, pblk = blk;              // next copy to issue, its buffer, its block
+  int pb = (int)(u / g.H), ph = (int)(u - (long long)pb * g.H);  // and its (b, h)
+  const uint8_t* psrc = a.base + record_offset(g, pb, ph, pblk, a.status);
   auto issue_next = [&]() {  // lane 0 only
     if (pnext >= n_units) return;
     const bool is_v = !WHOLE && (pnext & 1);
@@ -325,11 +326,22 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
     ++pnext;
     if (++pbuf == NB) pbuf = 0;
     if (WHOLE || is_v) {  // next block: the next record, or the first record of the next (b, h)
-      if (++pblk == a.nb) {
-        pblk = 0;
-        psrc += (uint64_t)(g.max_blocks - a.nb + 1) * g.rec_bytes;
-      } else {
-        psrc += g.rec_bytes;
+      if (g.n_pages <= 0) {  // contiguous: the next record, or the first one of the next (b, h)
+        if (++pblk == a.nb) {
+          pblk = 0;
+          psrc += (uint64_t)(g.max_blocks - a.nb + 1) * g.rec_bytes;
+        } else {
+          psrc += g.rec_bytes;
+        }
+      } else {                // paged: through the block table
+        if (++pblk == a.nb) {
+          pblk = 0;
+          if (++ph == g.H) {
+            ph = 0;
+            ++pb;
+          }
+        }
+        if (pnext < n_units) psrc = a.base + record_offset(g, pb, ph, pblk, a.status);
       }
     }
   };

@@ -51,6 +51,12 @@ constexpr float LOG2E_RSQRT_D = 1.4426950408889634f * 0.08838834764831845f;
 // The running reference of a warp's softmax moves only when a score exceeds it by more than this
 // (base-2 units): probabilities then stay below 2^8, so p * s of a token stays far inside fp16.
 constexpr float RESCALE_SLACK = 8.0f;
+// Value outliers are summed as 64-bit fixed point with OUTV_FRAC fraction bits: integer addition
+// is exact, so the sums do not depend on the order of the shared-memory atomics. |p * v| < 2^24
+// (p <= 2^RESCALE_SLACK, |v| <= 65504), so 2^19 entries per warp and (b, h) segment stay inside
+// the range even at that bound; the rounding is 2^-21 per entry.
+constexpr int OUTV_FRAC = 20;
+constexpr float OUTV_ONE = (float)(1 << OUTV_FRAC), OUTV_UNIT = 1.0f / OUTV_ONE;
 
 #ifndef KVQ_NUQ_NB
 #define KVQ_NUQ_NB 8
@@ -83,12 +89,13 @@ struct Smem {
   float2 rope_loc[T * 64];  // (cos, sin) of t * theta_i, t = 0..127
   Ops op[NB];
   float qb[2][D];           // per aux group: q rotated back by the block's start angle
-  float outv[NW][D];        // value outliers weighted by p, per consumer warp
+  long long outv[NW][D];    // value outliers weighted by p, per consumer warp, in units of 2^-OUTV_FRAC
   uint64_t rec_full[NB];    // record and RoPE row landed (bulk copies)
   uint64_t ops_full[NB];    // score operands and outlier terms ready (AUX_GROUP arrivals)
   uint64_t empty[NB];       // the consumer warps are done with the stage (NW arrivals)
   // followed by NB x 2 x round16(n_outliers) bytes, per stage: the token of each key outlier,
-  // then the token of each value outlier
+  // then the token of each value outlier; then 2 x round16(n_outliers) floats, per aux group:
+  // the score term of each key outlier
 };
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -156,10 +163,6 @@ __device__ __forceinline__ void bar_group(int grp) { asm volatile("bar.sync %0, 
 
 __device__ __forceinline__ uint32_t stage_bytes(const Geo& g) { return (uint32_t)g.rec_bytes + ROPE_ROW; }
 
-__device__ __forceinline__ const uint8_t* record_at(const Args& a, long long u, int blk) {
-  return a.base + ((uint64_t)u * a.g.max_blocks + (uint64_t)blk) * a.g.rec_bytes;
-}
-
 template <uint32_t R>
 __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(R));
@@ -181,6 +184,7 @@ __device__ void producer(const Args& a, Smem* sm, uint8_t* ring, long long x0, i
   const uint32_t rec = (uint32_t)g.rec_bytes, khalf = g.codes_off[1], sb = stage_bytes(g);
   long long u = x0 / a.nb;
   int blk = (int)(x0 - u * a.nb);
+  int pb = (int)(u / g.H), ph = (int)(u - (long long)pb * g.H);  // (b, h) of block p
   int issued = 0;
   for (int p = 0; p < n; ++p) {
     const int s = p % NBS;
@@ -195,13 +199,17 @@ __device__ void producer(const Args& a, Smem* sm, uint8_t* ring, long long x0, i
       fence_proxy_async();
       const uint32_t off = part == 0 ? 0u : part == 1 ? khalf : rec;
       const uint32_t bytes = part == 0 ? khalf : part == 1 ? rec - khalf : (uint32_t)ROPE_ROW;
-      const uint8_t* from = part == 2 ? a.base + g.rope_off + (size_t)blk * ROPE_ROW : record_at(a, u, blk) + off;
+      const uint8_t* from =
+          part == 2 ? a.base + g.rope_off + (size_t)blk * ROPE_ROW : a.base + record_offset(g, pb, ph, blk, a.status) + off;
       bulk_g2s(ring + (size_t)s * sb + off, from, bytes, &sm->rec_full[s]);
     }
     issued = p + 1;
     if (++blk == a.nb) {
       blk = 0;
-      ++u;
+      if (++ph == g.H) {
+        ph = 0;
+        ++pb;
+      }
     }
   }
   for (int p = max(0, issued - NBS); p < issued; ++p)
@@ -211,10 +219,11 @@ __device__ void producer(const Args& a, Smem* sm, uint8_t* ring, long long x0, i
 // Aux warps: two groups of 64 threads, group grp preparing blocks grp, grp + 2, grp + 4, ... of
 // the range (named barrier 1 + grp), so each group has two block periods per block. Per block,
 // thread j of a group first handles channel pair j (score B operand, zero-point terms, q_b) and
-// tokens j and j + 64 (the token tag of each of their key- and value-outlier entries); then,
-// over the key-outlier entries e = j, j + 64, ..., it adds each entry's score term
+// tokens j and j + 64 (the token tag of each of their key- and value-outlier entries); then it
+// computes the score terms of the key-outlier entries e = j, j + 64, ...
 //     v * (R(t)^T q_b)_c    (entry e = (t, c, v) of the CSR)
-// to sk[t] with a shared-memory atomic. The consumers scatter p_t * v for the value outliers.
+// and, after a group barrier, the sum sk[t] of each of its two tokens' terms in entry order.
+// The consumers scatter p_t * v for the value outliers.
 template <int NBS>
 __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows, int rows_stride, long long x0,
                           int n, int ax) {
@@ -232,6 +241,7 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
   long long cur_u = -1;
   float2 qv = make_float2(0.0f, 0.0f);
   float* qb = sm->qb[grp];
+  float* kterm = reinterpret_cast<float*>(rows + (size_t)NBS * rows_stride) + grp * tag_bytes;  // per group
   const int tA = j, tB = j + 64;
   for (int p = grp; p < n; p += 2) {
     if (u != cur_u) {
@@ -258,17 +268,16 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
       op.bz[2 * tqp + 1][kg] = pack_h2(zy, zy - __half2float(zyh));  // Y column
       *reinterpret_cast<float2*>(&qb[2 * j]) = make_float2(qb0, qb1);
     }
-    op.sk[tA] = 0.0f;
-    op.sk[tB] = 0.0f;
+    float skA = 0.0f, skB = 0.0f;
     if (n_out > 0) {
       uint8_t* ktag = rows + (size_t)s * rows_stride;
       uint8_t* vtag = ktag + tag_bytes;
       const uint8_t* csr = st + g.csr_off[0];
       const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * n_out);
       const uint16_t* rpv = reinterpret_cast<const uint16_t*>(st + g.csr_off[1] + 2 * n_out);
+      const int ka0 = min((int)rp[tA], n_out), ka1 = min((int)rp[tA + 1], n_out);
+      const int kb0 = min((int)rp[tB], n_out), kb1 = min((int)rp[tB + 1], n_out);
       {
-        const int ka0 = min((int)rp[tA], n_out), ka1 = min((int)rp[tA + 1], n_out);
-        const int kb0 = min((int)rp[tB], n_out), kb1 = min((int)rp[tB + 1], n_out);
         const int va0 = min((int)rpv[tA], n_out), va1 = min((int)rpv[tA + 1], n_out);
         const int vb0 = min((int)rpv[tB], n_out), vb1 = min((int)rpv[tB + 1], n_out);
         for (int e = ka0; e < ka1; ++e) ktag[e] = (uint8_t)tA;
@@ -276,36 +285,29 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
         for (int e = va0; e < va1; ++e) vtag[e] = (uint8_t)tA;
         for (int e = vb0; e < vb1; ++e) vtag[e] = (uint8_t)tB;
       }
-      bar_group(grp);  // q_b, the key tags and the zeroed sk visible
+      bar_group(grp);  // q_b and the key tags visible
       const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
       const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
       const int n_k = min((int)rp[T], n_out);
-      auto key_term = [&](int e, int& t) {  // entry e < n_k: its token and score term
-        const int c = col[e] & (D - 1);
-        t = ktag[e] & (T - 1);
+      auto key_term = [&](int e) {  // score term of key-outlier entry e < n_k
+        const int c = col[e] & (D - 1), t = ktag[e] & (T - 1);
         const float2 cr = sm->rope_loc[t * 64 + (c >> 1)];
         const float qa = qb[c & ~1], qc = qb[c | 1];
         const float qq = (c & 1) ? (-cr.y * qa + cr.x * qc) : (cr.x * qa + cr.y * qc);
         return h2f(val[e]) * qq;
       };
-      // up to 4 entries per thread side by side (1% of a tile is 164 entries): every load
-      // first, then the atomics; then any further entries one by one
-      float tv[4];
-      int tt[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        tt[k] = 0;
-        tv[k] = j + AUX_GROUP * k < n_k ? key_term(j + AUX_GROUP * k, tt[k]) : 0.0f;
-      }
+      // every entry's term (up to 4 per thread side by side; 1% of a tile is 164 entries), then
+      // each token's terms summed in entry order: the result does not depend on thread timing
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        if (j + AUX_GROUP * k < n_k) atomicAdd(&op.sk[tt[k]], tv[k]);
-      for (int e = j + 4 * AUX_GROUP; e < n_k; e += AUX_GROUP) {
-        int t;
-        const float v = key_term(e, t);
-        atomicAdd(&op.sk[t], v);
-      }
+        if (j + AUX_GROUP * k < n_k) kterm[j + AUX_GROUP * k] = key_term(j + AUX_GROUP * k);
+      for (int e = j + 4 * AUX_GROUP; e < n_k; e += AUX_GROUP) kterm[e] = key_term(e);
+      bar_group(grp);
+      for (int e = ka0; e < ka1; ++e) skA += kterm[e];
+      for (int e = kb0; e < kb1; ++e) skB += kterm[e];
     }
+    op.sk[tA] = skA;
+    op.sk[tB] = skB;
     mbar_arrive(&sm->ops_full[s]);  // AUX_GROUP arrivals complete the phase
     blk += 2;
     while (blk >= a.nb) {
@@ -388,8 +390,8 @@ __device__ __forceinline__ void block_values(const uint8_t* st, const Geo& g, in
 
 // Value outliers of a consumer warp's tokens in one block (rw: the entries' token tags). Entry e
 // of the warp's token range goes to lane (e - e0) mod 32, which takes p of its token from the
-// token's owner lane and adds p * v to the warp's outv. The first 32 entries are straight-line,
-// predicated code (it overlaps the tensor-core work it is placed with); later ones loop.
+// token's owner lane and adds p * v to the warp's outv. The first 32 entries run as one batch
+// placed with the tensor-core work of the block; later ones loop.
 __device__ __forceinline__ void value_outlier_span(const uint8_t* st, const Geo& g, int warp, int& e0, int& e1) {
   const int n_out = g.n_out;
   const uint16_t* rp = reinterpret_cast<const uint16_t*>(st + g.csr_off[1] + 2 * n_out);
@@ -397,8 +399,10 @@ __device__ __forceinline__ void value_outlier_span(const uint8_t* st, const Geo&
   e1 = min((int)rp[16 * warp + 16], n_out);
 }
 
+// Value-outlier entry e of the lane (e >= e1: none): p_t * v added to the warp's outv[c] in
+// fixed point (a shared-memory integer atomic; no branch, so it sits among the tensor-core work).
 __device__ __forceinline__ void value_outlier_entry(const uint8_t* st, const Geo& g, const uint8_t* rw, int e, int e1,
-                                                    int t0, float p0, float p1, float* outv) {
+                                                    int t0, float p0, float p1, long long* outv) {
   const int n_out = g.n_out;
   const uint8_t* csr = st + g.csr_off[1];
   const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
@@ -407,7 +411,11 @@ __device__ __forceinline__ void value_outlier_entry(const uint8_t* st, const Geo
   const int t = valid ? rw[e] : t0;
   const int src = 4 * (t & 7);
   const float pa = __shfl_sync(0xffffffffu, p0, src), pb = __shfl_sync(0xffffffffu, p1, src);
-  if (valid) atomicAdd(&outv[col[e] & (D - 1)], ((t & 8) ? pb : pa) * h2f(val[e]));
+  if (valid) {
+    const float x = ((t & 8) ? pb : pa) * h2f(val[e]);
+    atomicAdd(reinterpret_cast<unsigned long long*>(&outv[col[e] & (D - 1)]),
+              (unsigned long long)llrintf(x * OUTV_ONE));
+  }
 }
 
 // Consumer warp w: tokens 16w..16w+15 of every block of the CTA's range. Within a (b, h) segment
@@ -433,7 +441,7 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
   const uint32_t xsel = tq == 0 ? 0xffffffffu : 0u;      // this lane sends p' high (tq 0) ...
   const uint32_t ysel = tq == 1 ? 0xffffffffu : 0u;      // ... or low (tq 1) or zero
   const int t0 = 16 * warp + gq, t1 = t0 + 8;
-  float* outv = sm->outv[warp];
+  long long* outv = sm->outv[warp];
 
   auto ready_now = [&](int i) -> bool {  // the stage of range block i is ready (no waiting)
     const int s = i % NBS;
@@ -470,7 +478,7 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
       th1 = (hb[4] >> 8) | (hb[5] >> 8) << 8 | (hb[6] >> 8) << 16 | (hb[7] >> 8) << 24;
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) outv[lane + 32 * k] = 0.0f;
+    for (int k = 0; k < 4; ++k) outv[lane + 32 * k] = 0;
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
     float m_w = -INFINITY, l_w = 0.0f, z_w = 0.0f;
@@ -503,7 +511,7 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
         z_w *= al;
         __syncwarp();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) outv[lane + 32 * k] *= al;
+        for (int k = 0; k < 4; ++k) outv[lane + 32 * k] = llrintf((float)outv[lane + 32 * k] * al);
         __syncwarp();
         m_w = mloc;
       }
@@ -544,8 +552,8 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
             const int c0 = 16 * mt + gq, c1 = c0 + 8;
-            a.ws_o[row * D + c0] = acc[mt][0] + acc[mt][1] + zt + outv[c0];
-            a.ws_o[row * D + c1] = acc[mt][2] + acc[mt][3] + zt + outv[c1];
+            a.ws_o[row * D + c0] = acc[mt][0] + acc[mt][1] + zt + (float)outv[c0] * OUTV_UNIT;
+            a.ws_o[row * D + c1] = acc[mt][2] + acc[mt][3] + zt + (float)outv[c1] * OUTV_UNIT;
           }
         }
         if (lane == 0) {
@@ -603,7 +611,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
 }
 
 size_t smem_bytes(const Geo& g) {
-  return (size_t)NB * ((size_t)g.rec_bytes + ROPE_ROW) + sizeof(Smem) + (size_t)NB * 2 * round16((uint64_t)g.n_out);
+  return (size_t)NB * ((size_t)g.rec_bytes + ROPE_ROW) + sizeof(Smem) + (size_t)NB * 2 * round16((uint64_t)g.n_out) +
+         2 * sizeof(float) * round16((uint64_t)g.n_out);
 }
 
 }  // namespace nuqdec

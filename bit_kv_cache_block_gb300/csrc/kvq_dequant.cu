@@ -14,6 +14,7 @@ struct DequantArgs {
   int hadamard;
   float* out_k;
   float* out_v;
+  int* status;
 };
 
 // grid (n, H, B*2), thread = token row of the tile; rows staged in shared memory (stride 129)
@@ -26,7 +27,7 @@ __global__ void __launch_bounds__(DQ_THREADS) dequant_kernel(DequantArgs a) {
   float* out = kind ? a.out_v : a.out_k;
   if (!out) return;
   const int blk = a.first + bi;
-  const uint8_t* rec = a.base + record_index(g, b, h, blk) * g.rec_bytes;
+  const uint8_t* rec = a.base + record_offset(g, b, h, blk, a.status);
   const uint32_t* codes = reinterpret_cast<const uint32_t*>(rec + g.codes_off[kind]);
   const uint16_t* m = reinterpret_cast<const uint16_t*>(rec + g.meta_off[kind]);
   const int bits = g.bits, W = g.W, nw = 32 / bits;
@@ -91,10 +92,10 @@ __global__ void rope_table_kernel(float2* tab, int max_blocks, double theta) {
 }  // namespace kvq
 
 cudaError_t kvq_launch_dequant(const kvq::Geo& g, const uint8_t* base, const float* codebook, int first, int n,
-                               int domain, int hadamard, float* out_k, float* out_v, cudaStream_t st) {
+                               int domain, int hadamard, float* out_k, float* out_v, int* status, cudaStream_t st) {
   kvq::DequantArgs a;
   a.g = g; a.base = base; a.codebook = codebook; a.first = first; a.n = n; a.domain = domain;
-  a.hadamard = hadamard; a.out_k = out_k; a.out_v = out_v;
+  a.hadamard = hadamard; a.out_k = out_k; a.out_v = out_v; a.status = status;
   const int smem = kvq::T * 129 * (int)sizeof(float);
   cudaError_t e = kvq::ensure_smem_attr((const void*)kvq::dequant_kernel, (size_t)smem);
   if (e != cudaSuccess) return e;

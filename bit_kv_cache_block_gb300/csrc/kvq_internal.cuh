@@ -104,6 +104,8 @@ struct Geo {
   uint64_t rec_bytes;
   uint32_t codes_off[2], meta_off[2], csr_off[2];
   uint64_t rope_off;
+  int n_pages;          // > 0: paged cache (records addressed through `table`)
+  const int32_t* table; // paged caches: device block table [B][max_blocks] (else NULL)
 };
 
 inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
@@ -120,11 +122,9 @@ inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
     g.csr_off[k] = (uint32_t)l.csr_off[k];
   }
   g.rope_off = l.rope_off;
+  g.n_pages = c.n_pages;
+  g.table = nullptr;
   return g;
-}
-
-__host__ __device__ inline uint64_t record_index(const Geo& g, int b, int h, int blk) {
-  return ((uint64_t)b * g.H + h) * g.max_blocks + blk;
 }
 
 // Raises a kernel's dynamic shared-memory limit on the current device once (the setting is
@@ -240,6 +240,20 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
       : "r"(smem_u32(bar)), "r"(parity), "r"(1000000u)
       : "memory");
   return ok != 0;
+}
+
+// Byte offset from the cache base of the record of (b, h, block): contiguous records, or for
+// paged caches page table[b][block] of the pool, whose pages hold the records of all H heads.
+// A table entry outside [0, n_pages) is reported as KVQ_ERR_PAGE and page 0 used instead, so a
+// bad table never addresses memory outside the pool.
+__device__ __forceinline__ uint64_t record_offset(const Geo& g, int b, int h, int blk, int* status) {
+  if (g.n_pages <= 0) return (((uint64_t)b * g.H + h) * g.max_blocks + blk) * g.rec_bytes;
+  int page = __ldg(g.table + (size_t)b * g.max_blocks + blk);
+  if (page < 0 || page >= g.n_pages) {
+    report(status, KVQ_ERR_PAGE);
+    page = 0;
+  }
+  return ((uint64_t)page * g.H + h) * g.rec_bytes;
 }
 
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status,

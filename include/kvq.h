@@ -48,7 +48,9 @@ typedef enum {
   KVQ_ERR_CAPACITY = 3,      /* an append past cfg.max_blocks, or a buffer smaller than needed */
   KVQ_ERR_ALIGNMENT = 4,     /* a pointer that breaks the alignment rules above */
   KVQ_ERR_CUDA = 5,          /* a CUDA runtime error (launch failure, no device) */
-  KVQ_ERR_TIMEOUT = 6        /* device side: a bounded wait gave up (written to dev_status) */
+  KVQ_ERR_TIMEOUT = 6,       /* device side: a bounded wait gave up (written to dev_status) */
+  KVQ_ERR_PAGE = 7           /* device side: a block-table entry outside [0, n_pages) was read
+                                (written to dev_status; that block used page 0 instead) */
 } kvq_status;
 
 /* Quantization method of a cache (fixed for its lifetime). */
@@ -99,10 +101,17 @@ typedef struct {
   int32_t varn_iters;    /* VARN: variance-normalisation iterations (8); 0..64 */
   int32_t hadamard;      /* VARN: 1 applies the FWHT-128 (the decode transforms q and o too) */
   int32_t layout;        /* kvq_code_layout of the code words (0: KVQ_LAYOUT_ROWS) */
+  int32_t n_pages;       /* 0: the records of (b, h) are contiguous, [B][H_kv][max_blocks].
+                            > 0: paged cache. The record pool holds n_pages pages; a page holds
+                            the records of all H_kv heads of one 128-token block, and a block
+                            table (kvq_cache.block_table) maps block blk of sequence b to its
+                            page (the paged KV cache the KVQuant and TurboQuant pages' serving
+                            sections use, vLLM-style). */
 } kvq_config;
 
 /* Byte layout of a cache, from kvq_layout. One record per (b, h, block), at
- *   base + ((b * n_kv_heads + h) * max_blocks + block) * record_bytes,
+ *   base + ((b * n_kv_heads + h) * max_blocks + block) * record_bytes            (n_pages = 0)
+ *   base + (block_table[b * max_blocks + block] * n_kv_heads + h) * record_bytes  (n_pages > 0),
  * holding the K tile then the V tile; every region starts 16-byte aligned:
  *   codes : KVQ_LAYOUT_ROWS: 128 rows x words_per_row uint32, one row per token (K and V);
  *           code i of a row at bits [b*(i%n)+b-1 : b*(i%n)] of word i/n, n = floor(32/b),
@@ -150,6 +159,16 @@ typedef struct {
   int32_t* dev_status;     /* device int32, caller-owned; 0 = no device-side error */
   int32_t n_blocks;        /* blocks appended so far, per (b, h) */
   int32_t device;          /* CUDA device ordinal the cache was initialised on */
+  const int32_t* block_table; /* paged caches (cfg.n_pages > 0): device int32 [B][max_blocks],
+                            caller-owned and caller-filled: entry (b, blk) is the page of block
+                            blk of sequence b. kvq_cache_init sets it to NULL; set it before the
+                            first append. Decode and dequant read the entries of blocks
+                            [0, n_blocks), append those of the new blocks and writes their pages
+                            (sequences may share a page for reading, e.g. a common prefix, but an
+                            append must not write a page that another block uses). An entry
+                            outside [0, n_pages) is reported as KVQ_ERR_PAGE in dev_status and
+                            that block uses page 0 instead. NULL for contiguous caches.
+                            4-byte aligned. */
 } kvq_cache;
 
 /* Human-readable name of a status code (static string). */

@@ -52,6 +52,8 @@ int main(void) {
          offsetof(kvq_config, hadamard), offsetof(kvq_layout_t, total_bytes));
   printf("%zu %zu %zu %zu\n", offsetof(kvq_cache, lay), offsetof(kvq_cache, base), offsetof(kvq_cache, n_blocks),
          offsetof(kvq_cache, device));
+  printf("%zu %zu %zu\n", offsetof(kvq_config, layout), offsetof(kvq_config, n_pages),
+         offsetof(kvq_cache, block_table));
   return 0;
 }
 ''')
@@ -63,7 +65,8 @@ int main(void) {
     py = [C.sizeof(L.kvq_config), C.sizeof(L.kvq_layout_t), C.sizeof(L.kvq_cache),
           L.kvq_config.rope_theta.offset, L.kvq_config.outlier_frac.offset, L.kvq_config.hadamard.offset,
           L.kvq_layout_t.total_bytes.offset, L.kvq_cache.lay.offset, L.kvq_cache.base.offset,
-          L.kvq_cache.n_blocks.offset, L.kvq_cache.device.offset]
+          L.kvq_cache.n_blocks.offset, L.kvq_cache.device.offset, L.kvq_config.layout.offset,
+          L.kvq_config.n_pages.offset, L.kvq_cache.block_table.offset]
     assert vals == py
 
 
@@ -185,3 +188,42 @@ def test_host_argument_checks_launch_nothing(K):
     assert lib.kvq_truncate(C.byref(cache), 2) == L.KVQ_OK and cache.n_blocks == 2
     assert lib.kvq_reset(C.byref(cache)) == L.KVQ_OK and cache.n_blocks == 0
     assert K.kvq_status_str(L.KVQ_ERR_TIMEOUT) == "device wait timed out"
+    assert K.kvq_status_str(L.KVQ_ERR_PAGE) == "block table entry out of range"
+
+
+def test_paged_layout_and_checks(K):
+    """A paged cache's record pool is n_pages pages of H_kv records; append, decode and dequant
+    need its block table (non-null, 4-byte aligned) and refuse on the host without one."""
+    L = K._lib
+    lib = L.lib()
+    w = WL.WORKLOADS[2].scaled(batch=3, n_kv_heads=4, n_q_heads=4, ctx=5 * 128)
+    cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, w.n_blocks, w.dtype, w.pre_rope,
+                        w.rope_theta, w.outlier_frac, layout="mma", n_pages=17)
+    lay = K.kvq_layout(cfg)
+    flat_cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, w.n_blocks, w.dtype,
+                             w.pre_rope, w.rope_theta, w.outlier_frac, layout="mma")
+    flat = K.kvq_layout(flat_cfg)
+    assert lay.record_bytes == flat.record_bytes
+    assert lay.records_bytes == 17 * 4 * lay.record_bytes
+    assert flat.records_bytes == 3 * 4 * 5 * flat.record_bytes
+    assert lay.rope_off % 128 == 0 and lay.rope_off >= lay.records_bytes
+    assert K.kvq_decode_bytes(cfg, 5) == K.kvq_decode_bytes(flat_cfg, 5)
+    bad = K.make_config("rtn", 2, 1, 1, 1, 4, n_pages=-1)
+    out = L.kvq_layout_t()
+    assert lib.kvq_layout(C.byref(bad), C.byref(out)) == L.KVQ_ERR_INVALID_ARG
+    cache = L.kvq_cache()
+    cache.cfg = cfg
+    cache.lay = lay
+    cache.base = 0x100000
+    cache.codebook = 0x200000
+    cache.n_blocks = 0
+    k, v = C.c_void_p(0x1000), C.c_void_p(0x2000)
+    assert lib.kvq_append_block(C.byref(cache), k, v, 1, None, None) == L.KVQ_ERR_INVALID_ARG  # no table
+    cache.block_table = 0x3002
+    assert lib.kvq_append_block(C.byref(cache), k, v, 1, None, None) == L.KVQ_ERR_ALIGNMENT
+    cache.block_table = None
+    cache.n_blocks = 2
+    q, o, ws = C.c_void_p(0x1000), C.c_void_p(0x3000), C.c_void_p(0x5000)
+    assert lib.kvq_decode_attn(C.byref(cache), q, None, None, 0, o, ws, 1 << 24, None) == L.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_decode_attn_static(C.byref(cache), q, None, None, 0, o, None) == L.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_dequant(C.byref(cache), 0, 1, 0, o, None, None) == L.KVQ_ERR_INVALID_ARG

@@ -275,3 +275,27 @@ def test_capacity_and_truncate():
     cache.append(U.to_device(Kx[:, :, 128:], "f16"), U.to_device(Vx[:, :, 128:], "f16"))
     torch.cuda.synchronize()
     assert cache.n_blocks == 2 and cache.device_status() == 0
+
+
+DETERMINISM_CASES = [c for c in DECODE_CASES if c[0] in ("rtn2_mha", "rtn3_gqa", "int4_bf16", "nuq3_rope",
+                                                         "nuq3_rope_5pct", "nuq3_norope_gqa", "varn2_gqa")]
+
+
+@pytest.mark.parametrize("layout", ["rows", "mma"])
+@pytest.mark.parametrize("name,base,kw,tails", DETERMINISM_CASES, ids=[c[0] for c in DETERMINISM_CASES])
+def test_decode_is_deterministic(name, base, kw, tails, layout):
+    """Two decodes of the same cache and inputs give bitwise-equal outputs (no result depends on
+    thread timing: outlier sums run in a fixed order)."""
+    import torch
+    w = base.scaled(**kw)
+    cache = U.new_cache(w, layout=layout)
+    K, V = WL.blocks(w, 0, w.n_blocks)
+    cache.append(U.to_device(K, w.dtype), U.to_device(V, w.dtype))
+    n_tail = tails[-1]
+    tk, tv = WL.tail(w, n_tail)
+    args = (U.to_device(WL.query(w), w.dtype), U.to_device(tk, w.dtype) if n_tail else None,
+            U.to_device(tv, w.dtype) if n_tail else None)
+    outs = [cache.decode(*args).cpu().numpy() for _ in range(3)]
+    torch.cuda.synchronize()
+    assert cache.device_status() == 0
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2]), name
