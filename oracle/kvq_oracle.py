@@ -397,6 +397,45 @@ def nuq_quantize(x: np.ndarray, codebook: np.ndarray, axis: int, n_out: int):
     return dict(codes=codes, s16=s16, zp16=zp16, mask=mask, row_ptr=row_ptr, col=col, val=val)
 
 
+def calibrate_keys(K: np.ndarray, outlier_frac: float):
+    """Offline per-channel key statistics of one head ([KVQ] Algorithm 1 offline steps 3-4 and
+    §3.5): K [N][128] calibration keys (values representable in the input dtype), token 0 (the
+    attention sink) excluded. Per channel c over the M = N - 1 remaining tokens:
+      tau_c = the ceil((1 - f) M)-th smallest |K[t, c]|   (f = 0: no threshold, tau = inf),
+      zp_c, s_c = centre and half-range of the entries with |K[t, c]| <= tau_c (fp32, stored fp16).
+    Entries above tau_c are the channel's outliers. Returns (tau fp32[128], s16, zp16)."""
+    x = _f32(K)[1:]
+    M = x.shape[0]
+    a = np.sort(np.abs(x), axis=0)
+    f = float(np.float32(outlier_frac))
+    if f > 0.0:
+        r = max(1, int(math.ceil((1.0 - f) * M)))
+        tau = a[r - 1].astype(np.float32)
+    else:
+        tau = np.full(D, np.inf, np.float32)
+    mask = np.abs(x) > tau[None, :]
+    s16, zp16 = nuq_meta(x, mask, 0)
+    return tau, s16, zp16
+
+
+def nuq_quantize_calibrated(x: np.ndarray, codebook: np.ndarray, tau, s16, zp16, n_out: int):
+    """Key tile quantised with calibrated statistics ([KVQ] Algorithm 1 inference steps 1-4):
+    1. entries with |x[t, c]| > tau_c are outliers, at most n_out of them per tile (the largest,
+       in the order of `outlier_mask`); they go to CSR in fp16 and are zeroed in the dense part;
+    2. the dense part is normalised with the calibrated zp_c, s_c;
+    3. each dense entry takes the nearest codebook index.
+    Returns dict(codes, s16, zp16, mask, row_ptr, col, val)."""
+    x = _f32(x)
+    over = np.abs(x) > np.asarray(tau, np.float32)[None, :]
+    mask = outlier_mask(x, n_out) & over
+    dense = np.where(mask, np.float32(0.0), x)
+    s16 = np.asarray(s16, np.float16)
+    zp16 = np.asarray(zp16, np.float16)
+    codes = nuq_encode(nuq_normalise(dense, s16[None, :], zp16[None, :]), codebook)
+    row_ptr, col, val = csr_of(x, mask)
+    return dict(codes=codes, s16=s16.copy(), zp16=zp16.copy(), mask=mask, row_ptr=row_ptr, col=col, val=val)
+
+
 def nuq_dequant(codes, s16, zp16, codebook, axis: int, row_ptr=None, col=None, val=None):
     """x_dq = C[q]*s + zp, then the fp16 outliers are added back
     ([KVQ] Algorithm 1 dequantisation: K_hat[mask] += outlier_vals)."""
@@ -530,11 +569,18 @@ class OracleCache:
     for KVarN, with the query transformed the same way and the output transformed back),
     appends the fp residual tail and evaluates softmax attention. Query head j reads KV
     head j // (H_q / H_kv).
+
+    nuq only: key_calib = (tau [H][128], s16 [H][128], zp16 [H][128]) from calibrate_keys makes
+    key tiles use the calibrated statistics (nuq_quantize_calibrated); sink = True keeps the first
+    token of every sequence in the input precision ([KVQ] §3.5): its K and V rows of block 0 are
+    zero in the quantised tiles, and decode attends the kept rows at position 0 instead of the
+    quantised token 0.
     """
 
     def __init__(self, method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: int,
                  pre_rope: bool = False, rope_theta: float = 10000.0, outlier_frac: float = 0.01,
-                 varn_iters: int = 8, use_hadamard: bool = True, codebook=None, layout: int = LAYOUT_ROWS):
+                 varn_iters: int = 8, use_hadamard: bool = True, codebook=None, layout: int = LAYOUT_ROWS,
+                 key_calib=None, sink: bool = False):
         assert method in ("rtn", "nuq", "varn", "int4")
         assert layout in (LAYOUT_ROWS, LAYOUT_MMA)
         self.method, self.bits, self.layout = method, bits, layout
@@ -545,6 +591,9 @@ class OracleCache:
             cb = nuq_codebook(bits) if codebook is None else np.asarray(codebook, np.float32)
             self.codebook = np.broadcast_to(cb, (n_kv_heads, 2 ** bits)) if cb.ndim == 1 else cb
             self.n_out = n_outliers(outlier_frac)
+        assert (key_calib is None and not sink) or method == "nuq"
+        self.key_calib, self.sink = key_calib, bool(sink)
+        self.sink_kv = {}  # (b, h) -> (k row, v row) of the first token
         self.recs = {}
         self.n_blocks = 0
 
@@ -563,6 +612,9 @@ class OracleCache:
         elif m == "int4":
             q, s16 = int4_quantize(x)
             rec = dict(codes=int4_nibbles(q), s16=s16)
+        elif m == "nuq" and kind == KIND_K and self.key_calib is not None:
+            tau, s16, zp16 = (np.asarray(a)[h] for a in self.key_calib)
+            rec = nuq_quantize_calibrated(x, self.codebook[h], tau, s16, zp16, self.n_out)
         elif m == "nuq":
             rec = nuq_quantize(x, self.codebook[h], 0 if kind == KIND_K else 1, self.n_out)
         else:
@@ -579,8 +631,13 @@ class OracleCache:
                 for h in range(self.n_kv_heads):
                     if only_heads is not None and (b, h) not in only_heads:
                         continue
+                    first = self.sink and self.n_blocks + blk == 0
+                    if first:
+                        self.sink_kv[(b, h)] = (np.array(K[b, h, 0], np.float64), np.array(V[b, h, 0], np.float64))
                     for kind, X in ((KIND_K, K), (KIND_V, V)):
-                        x = X[b, h, blk * T:(blk + 1) * T]
+                        x = np.array(X[b, h, blk * T:(blk + 1) * T], np.float32)
+                        if first:
+                            x[0] = 0.0
                         self.recs[(b, h, self.n_blocks + blk, kind)] = self.quantize_tile(x, kind, h)
         self.n_blocks += n
 
@@ -630,6 +687,11 @@ class OracleCache:
                 is_varn = self.method == "varn" and self.use_hadamard
                 qc = fwht(qg) if is_varn else qg
                 s = qc @ Kc.T / math.sqrt(D)
+                if self.sink and Kc.shape[0]:  # the kept first token replaces quantised token 0
+                    ks, vs = self.sink_kv[(b, h)]
+                    s[:, 0] = qg @ ks / math.sqrt(D)  # position 0: RoPE is the identity
+                    Vc = Vc.copy()
+                    Vc[0] = vs
                 if n_tail:
                     kt = np.asarray(tail_k[b, h], np.float64)
                     if self.pre_rope:

@@ -165,3 +165,38 @@ def test_gqa_mapping_interleaved_is_caught(monkeypatch):
         return orig(self, q, tail_k, tail_v, only_heads)
     monkeypatch.setattr(K.OracleCache, "decode", dec)
     assert _fails(P.test_cache_decode_equals_plain_attention_on_lossless_inputs, "rtn", 4, False)
+
+
+def test_calibration_including_the_first_token_is_caught(monkeypatch):
+    orig = K.calibrate_keys
+    monkeypatch.setattr(K, "calibrate_keys", lambda Kc, f: orig(np.concatenate([Kc[:1], Kc]), f))
+    monkeypatch.setattr(O, "calibrate_keys", K.calibrate_keys)
+    assert _fails(P.test_calibrate_keys_brute_force)
+
+
+def test_calibrated_threshold_off_by_one_is_caught(monkeypatch):
+    def calib(Kc, f):  # the next order statistic up: one outlier fewer per channel
+        x = np.asarray(Kc, np.float32)[1:]
+        a = np.sort(np.abs(x), axis=0)
+        r = min(x.shape[0], int(np.ceil((1.0 - float(np.float32(f))) * x.shape[0])) + 1)
+        tau = a[r - 1].astype(np.float32) if f > 0 else np.full(128, np.inf, np.float32)
+        s16, zp16 = K.nuq_meta(x, np.abs(x) > tau[None, :], 0)
+        return tau, s16, zp16
+    monkeypatch.setattr(K, "calibrate_keys", calib)
+    monkeypatch.setattr(O, "calibrate_keys", calib)
+    assert _fails(P.test_calibrate_keys_brute_force)
+
+
+def test_sink_row_left_in_the_tiles_is_caught(monkeypatch):
+    orig = K.OracleCache.append
+    def append(self, Kx, Vx, only_heads=None):  # keeps the first token but never zeroes it
+        sink, self.sink = self.sink, False
+        first = self.n_blocks == 0
+        orig(self, Kx, Vx, only_heads)
+        self.sink = sink
+        if sink and first:
+            for b in range(self.batch):
+                for h in range(self.n_kv_heads):
+                    self.sink_kv[(b, h)] = (np.array(Kx[b, h, 0], np.float64), np.array(Vx[b, h, 0], np.float64))
+    monkeypatch.setattr(K.OracleCache, "append", append)
+    assert _fails(P.test_sink_decode_equals_plain_attention_on_lossless_inputs, False)

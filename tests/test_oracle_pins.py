@@ -603,3 +603,90 @@ def test_pack_tile_layouts(golden_dir, bits):
             assert (int(mma[c, t // n]) >> (bits * (t % n))) & (2 ** bits - 1) == codes[t, c]
         else:
             assert np.array_equal(mma, rows)
+
+
+# ------------------------------------------------------------------ calibrated keys, attention sink
+
+def test_calibrate_keys_brute_force():
+    """tau_c is the ceil((1-f)M)-th smallest |K[t, c]| over tokens 1..N-1 (token 0, the sink,
+    excluded); zp_c, s_c are the centre and half-range of the entries at or below tau_c."""
+    rng = np.random.default_rng(21)
+    N, f = 301, 0.02
+    K = rng.standard_normal((N, 128)).astype(np.float16).astype(np.float32)
+    tau, s16, zp16 = O.calibrate_keys(K, f)
+    M = N - 1
+    r = math.ceil((1 - float(np.float32(f))) * M)   # the fraction as the fp32 value a config holds
+    for c in (0, 37, 127):
+        col = [abs(float(K[t, c])) for t in range(1, N)]
+        assert tau[c] == sorted(col)[r - 1]
+        keep = [float(K[t, c]) for t in range(1, N) if abs(float(K[t, c])) <= tau[c]]
+        assert len(keep) >= r
+        assert float(zp16[c]) == float(np.float16((np.float32(max(keep)) + np.float32(min(keep))) / 2))
+        assert float(s16[c]) == float(np.float16((np.float32(max(keep)) - np.float32(min(keep))) / 2))
+    K2 = K.copy()
+    K2[0] = 1000.0                                   # the first token does not enter
+    for a, b in zip(O.calibrate_keys(K2, f), (tau, s16, zp16)):
+        assert np.array_equal(a, b)
+    t0, s0, z0 = O.calibrate_keys(K, 0.0)            # no outliers: the full range of tokens 1..
+    assert np.all(np.isinf(t0))
+    assert np.array_equal(s0, ((K[1:].max(0) - K[1:].min(0)) / 2).astype(np.float16))
+
+
+def test_calibrated_quantizer_threshold_cap_and_grid():
+    rng = np.random.default_rng(22)
+    cb = np.array([-1, -0.75, -0.5, -0.25, 0.25, 0.5, 0.75, 1.0], np.float32)
+    q = rng.integers(0, 8, size=(128, 128))
+    x = (cb[q] * 0.5 + 0.25).astype(np.float32)     # on the grid of s = 0.5, zp = 0.25
+    tau = np.full(128, 2.0, np.float32)
+    s16, zp16 = np.full(128, 0.5, np.float16), np.full(128, 0.25, np.float16)
+    planted = [(3, 4, 9.5), (3, 90, -7.25), (77, 4, 5.0)]
+    for t, c, v in planted:
+        x[t, c] = v
+    r = O.nuq_quantize_calibrated(x, cb, tau, s16, zp16, n_out=10)
+    dense, sparse = O.threshold_split(x, tau)       # the pages' threshold form
+    assert np.array_equal(r["mask"], sparse != 0)
+    assert int(r["row_ptr"][-1]) == len(planted)
+    xh = O.nuq_dequant(r["codes"], r["s16"], r["zp16"], cb, 0, r["row_ptr"], r["col"], r["val"])
+    for t, c, v in planted:                          # dense zero (code of -0.25 on this grid) + v
+        assert xh[t, c] == pytest.approx(v + 0.0)
+        xh[t, c] = x[t, c]
+    assert np.array_equal(xh, x.astype(np.float64))
+    capped = O.nuq_quantize_calibrated(x, cb, tau, s16, zp16, n_out=2)
+    assert capped["mask"].sum() == 2 and capped["mask"][3, 4] and capped["mask"][3, 90]
+
+
+@pytest.mark.parametrize("calibrated", [False, True])
+def test_sink_decode_equals_plain_attention_on_lossless_inputs(calibrated):
+    """With the first token kept in the input precision, decode over lossless nuq inputs equals
+    plain fp64 attention over the raw K/V, the first token included at position 0 (with and
+    without calibrated key statistics: calibrating on such inputs recovers their grid)."""
+    rng = np.random.default_rng(23)
+    B, H, nb = 1, 2, 2
+    cb = np.array([-1, -0.75, -0.5, -0.25, 0.25, 0.5, 0.75, 1.0], np.float32)
+    ch = (2.0 ** (np.arange(128) % 3 - 2))[None, :]
+    K = np.empty((B, H, nb * 128, 128), np.float32)
+    V = np.empty_like(K)
+    for h in range(H):
+        qk = rng.integers(0, 8, (nb * 128, 128))
+        qk[1::128], qk[2::128] = 0, 7                # every block's extremes off the sink row
+        K[0, h] = cb[qk] * ch + 0.25 * ch
+        qv = rng.integers(0, 8, (nb * 128, 128))
+        qv[:, 0], qv[:, 1] = 0, 7
+        V[0, h] = cb[qv] * 0.5 - 0.125
+        K[0, h, 0] = rng.standard_normal(128) * 3    # the sink token: off every grid
+        V[0, h, 0] = rng.standard_normal(128) * 3
+    calib = None
+    if calibrated:
+        parts = [O.calibrate_keys(K[0, h], 0.0) for h in range(H)]
+        calib = tuple(np.stack([p[i] for p in parts]) for i in range(3))
+    cache = O.OracleCache("nuq", 3, B, H, H, pre_rope=True, outlier_frac=0.0, codebook=cb, key_calib=calib,
+                          sink=True)
+    cache.append(K, V)
+    qv_ = rng.standard_normal((B, H, 128))
+    tk, tv = rng.standard_normal((B, H, 3, 128)), rng.standard_normal((B, H, 3, 128))
+    got = cache.decode(qv_, tk, tv)
+    for h in range(H):
+        Kf = O.rope(np.concatenate([K[0, h], tk[0, h]]).astype(np.float64), np.arange(nb * 128 + 3))
+        Vf = np.concatenate([V[0, h], tv[0, h]]).astype(np.float64)
+        ref = O.attention(qv_[0, h][None], Kf, Vf)[0]
+        assert np.allclose(got[0, h], ref, rtol=1e-12, atol=1e-12)
