@@ -29,7 +29,7 @@ def lib_path() -> str:
 def make_config(method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: int, max_blocks: int,
                 in_dtype: str = "f16", pre_rope: bool = False, rope_theta: float = 10000.0,
                 outlier_frac: float = 0.01, varn_iters: int = 8, hadamard: bool = True,
-                layout: str = "rows", n_pages: int = 0) -> kvq_config:
+                layout: str = "rows", n_pages: int = 0, key_calib: bool = False, sink: bool = False) -> kvq_config:
     c = kvq_config()
     c.method = METHODS[method] if isinstance(method, str) else int(method)
     c.bits, c.batch, c.n_kv_heads, c.n_q_heads = bits, batch, n_kv_heads, n_q_heads
@@ -42,6 +42,8 @@ def make_config(method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: 
     c.hadamard = int(bool(hadamard))
     c.layout = LAYOUTS[layout] if isinstance(layout, str) else int(layout)
     c.n_pages = int(n_pages)
+    c.key_calib = int(bool(key_calib))
+    c.sink = int(bool(sink))
     return c
 
 
@@ -142,6 +144,14 @@ def kvq_dequant(cache: kvq_cache, first_block: int, n_blocks: int, domain: int, 
                                       _ptr(out_v), _stream(stream)), "kvq_dequant")
 
 
+def kvq_calibrate_keys(cache: kvq_cache, k_calib, stream=None) -> None:
+    """k_calib: device [H_kv][n_tokens][128] in the cache's input dtype (calibration keys)."""
+    if k_calib.dim() != 3 or k_calib.shape[2] != 128:
+        raise ValueError("calibration keys must be [H_kv][n_tokens][128]")
+    _lib.check(_lib.lib().kvq_calibrate_keys(C.byref(cache), _ptr(k_calib), int(k_calib.shape[1]),
+                                             _stream(stream)), "kvq_calibrate_keys")
+
+
 class KVCache:
     """Convenience owner of the device buffers of one cache (allocated by PyTorch) plus the
     decode workspace; every call goes through the C ABI above."""
@@ -194,6 +204,10 @@ class KVCache:
         ov = torch.empty(shape, dtype=torch.float32, device=self.device)
         kvq_dequant(self.cache, first_block, n_blocks, domain, ok, ov, stream)
         return ok, ov
+
+    def calibrate_keys(self, k_calib, stream=None):
+        """Offline key statistics from calibration keys [H_kv][n_tokens][128] (key_calib caches)."""
+        kvq_calibrate_keys(self.cache, k_calib, stream)
 
     def set_block_table(self, table):
         """Binds a page table (int32 [B][max_blocks]); it is read by every later call."""

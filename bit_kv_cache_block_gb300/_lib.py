@@ -24,7 +24,7 @@ METHODS = {"rtn": KVQ_RTN, "nuq": KVQ_NUQ, "varn": KVQ_VARN, "int4": KVQ_INT4}
 # every entry point declared in include/kvq.h
 EXPORTS = ["kvq_status_str", "kvq_dense_kv_bytes", "kvq_layout", "kvq_cache_init", "kvq_append_block",
            "kvq_truncate", "kvq_reset", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
-           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_dequant"]
+           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_dequant", "kvq_calibrate_keys"]
 
 
 class kvq_config(C.Structure):
@@ -32,7 +32,8 @@ class kvq_config(C.Structure):
                 ("n_q_heads", C.c_int32), ("head_dim", C.c_int32), ("block", C.c_int32),
                 ("max_blocks", C.c_int32), ("in_dtype", C.c_int32), ("pre_rope", C.c_int32),
                 ("rope_theta", C.c_double), ("outlier_frac", C.c_float), ("varn_iters", C.c_int32),
-                ("hadamard", C.c_int32), ("layout", C.c_int32), ("n_pages", C.c_int32)]
+                ("hadamard", C.c_int32), ("layout", C.c_int32), ("n_pages", C.c_int32),
+                ("key_calib", C.c_int32), ("sink", C.c_int32)]
 
 
 class kvq_layout_t(C.Structure):
@@ -40,13 +41,15 @@ class kvq_layout_t(C.Structure):
                 ("meta_off", C.c_uint64 * 2), ("meta_bytes", C.c_uint64 * 2), ("csr_off", C.c_uint64 * 2),
                 ("csr_bytes", C.c_uint64 * 2), ("records_bytes", C.c_uint64), ("rope_off", C.c_uint64),
                 ("rope_bytes", C.c_uint64), ("total_bytes", C.c_uint64), ("words_per_row", C.c_int32),
-                ("n_outliers", C.c_int32), ("format_version", C.c_uint32), ("reserved", C.c_int32)]
+                ("n_outliers", C.c_int32), ("format_version", C.c_uint32), ("reserved", C.c_int32),
+                ("calib_off", C.c_uint64), ("calib_bytes", C.c_uint64), ("sink_off", C.c_uint64),
+                ("sink_bytes", C.c_uint64)]
 
 
 class kvq_cache(C.Structure):
     _fields_ = [("cfg", kvq_config), ("lay", kvq_layout_t), ("base", C.c_void_p), ("codebook", C.c_void_p),
                 ("dev_status", C.c_void_p), ("n_blocks", C.c_int32), ("device", C.c_int32),
-                ("block_table", C.c_void_p)]
+                ("block_table", C.c_void_p), ("calibrated", C.c_int32)]
 
 
 _lib = None
@@ -89,6 +92,8 @@ def lib() -> C.CDLL:
     L.kvq_decode_attn_static.argtypes = [P(kvq_cache), vp, vp, vp, i32, vp, vp]
     L.kvq_dequant.restype = C.c_int
     L.kvq_dequant.argtypes = [P(kvq_cache), i32, i32, i32, vp, vp, vp]
+    L.kvq_calibrate_keys.restype = C.c_int
+    L.kvq_calibrate_keys.argtypes = [P(kvq_cache), vp, i32, vp]
     _lib = L
     return L
 

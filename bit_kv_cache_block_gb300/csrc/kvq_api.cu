@@ -1,4 +1,5 @@
 // Host side of the C ABI: argument checks, layout arithmetic and kernel launches.
+#include <cmath>
 #include <cstring>
 
 #include "kvq_internal.cuh"
@@ -13,6 +14,8 @@ size_t kvq_decode_ws_floats(const kvq::Geo& g, int n_blocks, int v1_splits);
 cudaError_t kvq_launch_dequant(const kvq::Geo& g, const uint8_t* base, const float* codebook, int first, int n,
                                int domain, int hadamard, float* out_k, float* out_v, int* status, cudaStream_t st);
 cudaError_t kvq_launch_rope_init(float2* tab, int max_blocks, double theta, cudaStream_t st);
+cudaError_t kvq_launch_calibrate(const kvq::Geo& g, uint8_t* base, const uint16_t* k, int n_tokens, int rank,
+                                 cudaStream_t st);
 cudaError_t kvq_static_workspace(float** ptr, size_t* n_floats);
 
 namespace {
@@ -32,6 +35,8 @@ kvq_status check_config(const kvq_config* c) {
   if (c->bits < 2 || c->bits > 4) return KVQ_ERR_UNSUPPORTED;
   if (c->layout != KVQ_LAYOUT_ROWS && c->layout != KVQ_LAYOUT_MMA) return KVQ_ERR_INVALID_ARG;
   if (c->n_pages < 0 || c->n_pages > (1 << 28)) return KVQ_ERR_INVALID_ARG;
+  if ((c->key_calib != 0 && c->key_calib != 1) || (c->sink != 0 && c->sink != 1)) return KVQ_ERR_INVALID_ARG;
+  if ((c->key_calib || c->sink) && c->method != KVQ_NUQ) return KVQ_ERR_UNSUPPORTED;
   if (c->method == KVQ_INT4 && c->bits != 4) return KVQ_ERR_UNSUPPORTED;
   if (c->pre_rope != 0 && c->pre_rope != 1) return KVQ_ERR_INVALID_ARG;
   if (c->pre_rope && c->method != KVQ_NUQ) return KVQ_ERR_UNSUPPORTED;
@@ -114,7 +119,18 @@ kvq_status kvq_layout(const kvq_config* c, kvq_layout_t* out) {
                                    : (uint64_t)c->batch * c->n_kv_heads * (uint64_t)c->max_blocks * l.record_bytes;
   l.rope_off = (l.records_bytes + 127) & ~uint64_t(127);
   l.rope_bytes = c->pre_rope ? (uint64_t)((c->max_blocks + 1) + kvq::T) * 64 * 8 : 0;
-  l.total_bytes = c->pre_rope ? l.rope_off + l.rope_bytes : l.records_bytes;
+  uint64_t end = c->pre_rope ? l.rope_off + l.rope_bytes : l.records_bytes;
+  if (c->key_calib) {
+    l.calib_off = (end + 127) & ~uint64_t(127);
+    l.calib_bytes = (uint64_t)c->n_kv_heads * kvq::D * (4 + 2 + 2);
+    end = l.calib_off + l.calib_bytes;
+  }
+  if (c->sink) {
+    l.sink_off = (end + 127) & ~uint64_t(127);
+    l.sink_bytes = (uint64_t)c->batch * c->n_kv_heads * 2 * kvq::D * 2;
+    end = l.sink_off + l.sink_bytes;
+  }
+  l.total_bytes = end;
   l.format_version = KVQ_FORMAT_VERSION;
   *out = l;
   return KVQ_OK;
@@ -165,6 +181,7 @@ kvq_status kvq_append_block(kvq_cache* cache, const void* k, const void* v, int3
   if (dbg_varn_scales && !aligned(dbg_varn_scales, 16)) return KVQ_ERR_ALIGNMENT;
   if (n_blocks > 65535) return KVQ_ERR_INVALID_ARG;
   if ((int64_t)cache->n_blocks + n_blocks > cache->cfg.max_blocks) return KVQ_ERR_CAPACITY;
+  if (cache->cfg.key_calib && !cache->calibrated) return KVQ_ERR_INVALID_ARG;
   kvq::Geo g;
   if (kvq_status gs = geo_of(cache, g); gs != KVQ_OK) return gs;
   float* dbg = cache->cfg.method == KVQ_VARN ? dbg_varn_scales : nullptr;
@@ -174,6 +191,27 @@ kvq_status kvq_append_block(kvq_cache* cache, const void* k, const void* v, int3
                              cache->dev_status, cache->cfg.varn_iters, hadamard_of(cache->cfg), stream);
   });
   if (s == KVQ_OK) cache->n_blocks += n_blocks;
+  return s;
+}
+
+kvq_status kvq_calibrate_keys(kvq_cache* cache, const void* k_calib, int32_t n_tokens, cudaStream_t stream) {
+  if (!cache || !cache->base || !k_calib) return KVQ_ERR_INVALID_ARG;
+  if (check_config(&cache->cfg) != KVQ_OK || !cache->cfg.key_calib) return KVQ_ERR_INVALID_ARG;
+  if (n_tokens < 2 || n_tokens > (1 << 24)) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(k_calib, 16)) return KVQ_ERR_ALIGNMENT;
+  // rank of tau among the |k| of tokens 1 .. n_tokens-1, ascending (1-based); 0: no threshold
+  const double f = (double)cache->cfg.outlier_frac, m = (double)(n_tokens - 1);
+  int rank = 0;
+  if (f > 0.0) {
+    rank = (int)std::ceil((1.0 - f) * m);
+    if (rank < 1) rank = 1;
+  }
+  const kvq::Geo g = kvq::make_geo(cache->cfg, cache->lay);
+  kvq_status s = on_device(cache->device, [&]() {
+    return kvq_launch_calibrate(g, static_cast<uint8_t*>(cache->base), static_cast<const uint16_t*>(k_calib),
+                                n_tokens, rank, stream);
+  });
+  if (s == KVQ_OK) cache->calibrated = 1;
   return s;
 }
 

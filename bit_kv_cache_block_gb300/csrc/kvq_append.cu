@@ -221,9 +221,14 @@ __global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
   // ---- stage the tile (one read of HBM), fp32
   const uint16_t* src = (kind ? a.v : a.k) +
                         (((uint64_t)b * g.H + h) * (uint64_t)a.n_new * T + (uint64_t)blk_src * T) * D;
+  const bool sink_row = g.sink && blk == 0;  // token 0 of the sequence: kept, zero in the tile
   for (int i = tid; i < TILE / 8; i += AP_THREADS) {
     uint4 u = reinterpret_cast<const uint4*>(src)[i];
     int e = i * 8, t = e >> 7, c = e & 127;
+    if (sink_row && t == 0) {
+      reinterpret_cast<uint4*>(a.base + g.sink_off + (((uint64_t)b * g.H + h) * 2 + kind) * D * 2)[i] = u;
+      u = make_uint4(0u, 0u, 0u, 0u);
+    }
     const uint16_t* hv = reinterpret_cast<const uint16_t*>(&u);
 #pragma unroll
     for (int j = 0; j < 8; ++j) sm->x[t * XS + c + j] = in_bits_to_f32(hv[j], g.in_bf16);
@@ -293,6 +298,11 @@ __global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
     for (int i = tid; i < TILE / 32; i += AP_THREADS) sm->mask[i] = 0u;
     uint8_t* csr = rec + g.csr_off[kind];
     const int n_out = g.n_out;
+    // calibrated keys: per-channel threshold and statistics from the calibration table
+    const bool calib = g.key_calib && kind == 0;
+    const float* tau_tab = reinterpret_cast<const float*>(a.base + g.calib_off) + h * D;
+    const uint16_t* s_tab = reinterpret_cast<const uint16_t*>(a.base + g.calib_off + (uint64_t)g.H * D * 4) + h * D;
+    const uint16_t* zp_tab = s_tab + (uint64_t)g.H * D;
     __syncthreads();
     if (n_out > 0) {
       // pass 1: histogram of the high 8 bits of the 15-bit fp16 magnitude
@@ -347,13 +357,22 @@ __global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
         }
         if (s) selbits |= 1ull << j;
       }
+      if (calib) {  // of the tile's largest entries, only those over the channel's threshold
+        for (int j = 0; j < 64; ++j)
+          if (!(fabsf(sm->x[t0 * XS + c0 + j]) > tau_tab[c0 + j])) selbits &= ~(1ull << j);
+      }
       const int n_sel = __popcll(selbits);
-      int pos = block_excl_scan(n_sel, sm->scan, nullptr);
+      int n_total = 0;
+      int pos = block_excl_scan(n_sel, sm->scan, &n_total);
       uint16_t* val = reinterpret_cast<uint16_t*>(csr);
       uint16_t* row_ptr = reinterpret_cast<uint16_t*>(csr + 2 * n_out);
       uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
       if ((tid & 1) == 0) row_ptr[t0] = (uint16_t)pos;
-      if (tid == 0) row_ptr[T] = (uint16_t)n_out;
+      if (tid == 0) row_ptr[T] = (uint16_t)n_total;
+      for (int i = n_total + tid; i < n_out; i += AP_THREADS) {  // unused capacity (calibrated keys)
+        val[i] = 0;
+        col[i] = 0;
+      }
       sm->mask[e0 >> 5] = (uint32_t)selbits;
       sm->mask[(e0 >> 5) + 1] = (uint32_t)(selbits >> 32);
       for (int j = 0; j < 64; ++j) {
@@ -388,7 +407,10 @@ __global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
       mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, 1));
       if (half == 0) {
         uint16_t s16 = 0, zp16 = 0;
-        if (mx != -INFINITY) {
+        if (calib) {
+          s16 = s_tab[gi];
+          zp16 = zp_tab[gi];
+        } else if (mx != -INFINITY) {
           zp16 = f2h_rn(__fdiv_rn(__fadd_rn(mx, mn), 2.0f));
           s16 = f2h_rn(__fdiv_rn(__fsub_rn(mx, mn), 2.0f));
         }

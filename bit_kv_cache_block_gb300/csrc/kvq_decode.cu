@@ -242,6 +242,7 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
 #pragma unroll
     for (int k = 0; k < GMAX; ++k) {
       s2[k] = acc[k] * tscale;
+      if (METHOD == KVQ_NUQ && g.sink && blk == 0 && t == 0) s2[k] = -INFINITY;  // the kept first token
       float mx = s2[k];
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -464,8 +465,23 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
     O = ob[c];
   }
 
+  // ---- the kept first token of the sequence (attention sink, [KVQ] §3.5) at position 0, where
+  // RoPE is the identity: quantised token 0 was left out of the partials
+  float Mc = M;
+  if (g.sink && a.n_blocks > 0) {
+    const uint16_t* ks = reinterpret_cast<const uint16_t*>(a.base + g.sink_off) + ((uint64_t)b * g.H + h) * 2 * D;
+    const float qk = grp == 0 ? load_in(a.q + ((uint64_t)b * g.Hq + hq) * D + c, g.in_bf16) *
+                                    in_bits_to_f32(ks[c], g.in_bf16)
+                              : 0.0f;
+    const float ss = cb_sum(qk, red) * LOG2E_RSQRT_D;
+    const float m2 = fmaxf(Mc, ss), f = exp2f(Mc - m2), ps = exp2f(ss - m2);
+    L = L * f + ps;
+    O = O * f + ps * in_bits_to_f32(ks[D + c], g.in_bf16);
+    Mc = m2;
+  }
+
   // ---- the fp residual tail (< 128 tokens)
-  float Mn = M;
+  float Mn = Mc;
   if (a.n_tail > 0) {
     const int nt = a.n_tail;
     const uint16_t* tk = a.tail_k + ((uint64_t)b * g.H + h) * nt * D;
@@ -516,8 +532,8 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
     }
     __syncthreads();
     const float mt = cb_max(tid < nt ? sc[tid] : -INFINITY, red);
-    Mn = fmaxf(M, mt);
-    const float f = exp2f(M - Mn);
+    Mn = fmaxf(Mc, mt);
+    const float f = exp2f(Mc - Mn);
     L *= f;
     O *= f;
     float pl = 0.0f;

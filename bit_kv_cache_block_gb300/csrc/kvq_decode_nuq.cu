@@ -492,6 +492,7 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
       const uint8_t* st = ring + (size_t)s * sb;
       const bool more = j + 1 < iend;  // warp-uniform
       const bool ready = more ? ready_now(j + 1) : true;  // its latency overlaps the softmax
+      if (g.sink && blk + (j - i) == 0 && warp == 0 && gq == 0) sv0 = -INFINITY;  // the kept first token
       // online softmax with block j's scores (base 2). m_w is the reference the warp's sums are
       // kept relative to; it moves up only when a score passes it by more than RESCALE_SLACK, so
       // p = 2^(s - m_w) stays below 2^RESCALE_SLACK and the usual block needs one vote instead of

@@ -106,6 +106,9 @@ struct Geo {
   uint64_t rope_off;
   int n_pages;          // > 0: paged cache (records addressed through `table`)
   const int32_t* table; // paged caches: device block table [B][max_blocks] (else NULL)
+  int key_calib;        // NUQ keys use the calibration table at calib_off
+  int sink;             // NUQ: the first token of each sequence is kept at sink_off
+  uint64_t calib_off, sink_off;
 };
 
 inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
@@ -124,6 +127,10 @@ inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
   g.rope_off = l.rope_off;
   g.n_pages = c.n_pages;
   g.table = nullptr;
+  g.key_calib = c.key_calib;
+  g.sink = c.sink;
+  g.calib_off = l.calib_off;
+  g.sink_off = l.sink_off;
   return g;
 }
 

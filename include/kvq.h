@@ -107,6 +107,15 @@ typedef struct {
                             table (kvq_cache.block_table) maps block blk of sequence b to its
                             page (the paged KV cache the KVQuant and TurboQuant pages' serving
                             sections use, vLLM-style). */
+  int32_t key_calib;     /* NUQ only. 0: key statistics per block (centre/half-range of each
+                            channel, the tile's top outlier_frac entries as outliers). 1: offline
+                            statistics per (KV head, channel) from kvq_calibrate_keys ([KVQ]
+                            §3.6, Algorithm 1): entries with |k| > tau_c are outliers (at most
+                            n_outliers per tile, the largest first), the rest normalised with the
+                            calibrated centre and half-range. Values stay per token, online. */
+  int32_t sink;          /* NUQ only. 1: the first token of every sequence is kept in the input
+                            precision ([KVQ] §3.5 attention sink): block 0's tiles hold zeros in
+                            its place and decode attends the kept K and V rows at position 0. */
 } kvq_config;
 
 /* Byte layout of a cache, from kvq_layout. One record per (b, h, block), at
@@ -148,6 +157,10 @@ typedef struct {
   int32_t n_outliers;                      /* NUQ: outliers per tile; 0 otherwise */
   uint32_t format_version;                 /* KVQ_FORMAT_VERSION */
   int32_t reserved;
+  uint64_t calib_off, calib_bytes;         /* key_calib: float tau[H_kv][128], then fp16
+                                              s[H_kv][128], then fp16 zp[H_kv][128]; else 0 */
+  uint64_t sink_off, sink_bytes;           /* sink: per (b, h), the first token's K row then V
+                                              row, 128 values each in cfg.in_dtype; else 0 */
 } kvq_layout_t;
 
 /* A cache handle: plain data owned by the caller. kvq_cache_init fills it. */
@@ -169,6 +182,7 @@ typedef struct {
                             outside [0, n_pages) is reported as KVQ_ERR_PAGE in dev_status and
                             that block uses page 0 instead. NULL for contiguous caches.
                             4-byte aligned. */
+  int32_t calibrated;      /* key_calib caches: set by kvq_calibrate_keys; append refuses until then */
 } kvq_cache;
 
 /* Human-readable name of a status code (static string). */
@@ -188,6 +202,17 @@ kvq_status kvq_layout(const kvq_config* cfg, kvq_layout_t* out);
  * every append and decode (keep it alive and unchanged). No allocation. */
 kvq_status kvq_cache_init(kvq_cache* cache, const kvq_config* cfg, void* dev_base, size_t bytes,
                           const float* dev_codebook, int32_t* dev_status, cudaStream_t stream);
+
+/* Offline key calibration of a key_calib cache ([KVQ] §3.6 and Algorithm 1 offline steps 3-4,
+ * the first token excluded as §3.5 asks). For every KV head h and channel c, over tokens
+ * 1 .. n_tokens-1 of k_calib[h]:
+ *   tau     = the ceil((1 - f) * (n_tokens - 1))-th smallest |k| (f = cfg.outlier_frac as fp32,
+ *             computed in fp64; f = 0: tau = +inf, no outliers),
+ *   zp, s   = centre and half-range of the entries with |k| <= tau (fp32, stored fp16).
+ * k_calib : device [H_kv][n_tokens][128] in cfg.in_dtype (pre-RoPE keys for pre-RoPE caches),
+ *           n_tokens >= 2, 16-byte aligned. Writes the cache's calibration table on `stream`
+ * and sets cache->calibrated. KVQ_ERR_INVALID_ARG if the cache has no key_calib. */
+kvq_status kvq_calibrate_keys(kvq_cache* cache, const void* k_calib, int32_t n_tokens, cudaStream_t stream);
 
 /* Quantizes n_blocks new blocks of 128 tokens for every (b, h) and stores them at block
  * positions cache->n_blocks .. cache->n_blocks + n_blocks - 1; on success cache->n_blocks

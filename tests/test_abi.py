@@ -54,6 +54,8 @@ int main(void) {
          offsetof(kvq_cache, device));
   printf("%zu %zu %zu\n", offsetof(kvq_config, layout), offsetof(kvq_config, n_pages),
          offsetof(kvq_cache, block_table));
+  printf("%zu %zu %zu %zu %zu\n", offsetof(kvq_config, key_calib), offsetof(kvq_config, sink),
+         offsetof(kvq_layout_t, calib_off), offsetof(kvq_layout_t, sink_bytes), offsetof(kvq_cache, calibrated));
   return 0;
 }
 ''')
@@ -66,7 +68,9 @@ int main(void) {
           L.kvq_config.rope_theta.offset, L.kvq_config.outlier_frac.offset, L.kvq_config.hadamard.offset,
           L.kvq_layout_t.total_bytes.offset, L.kvq_cache.lay.offset, L.kvq_cache.base.offset,
           L.kvq_cache.n_blocks.offset, L.kvq_cache.device.offset, L.kvq_config.layout.offset,
-          L.kvq_config.n_pages.offset, L.kvq_cache.block_table.offset]
+          L.kvq_config.n_pages.offset, L.kvq_cache.block_table.offset, L.kvq_config.key_calib.offset,
+          L.kvq_config.sink.offset, L.kvq_layout_t.calib_off.offset, L.kvq_layout_t.sink_bytes.offset,
+          L.kvq_cache.calibrated.offset]
     assert vals == py
 
 
@@ -227,3 +231,38 @@ def test_paged_layout_and_checks(K):
     assert lib.kvq_decode_attn(C.byref(cache), q, None, None, 0, o, ws, 1 << 24, None) == L.KVQ_ERR_INVALID_ARG
     assert lib.kvq_decode_attn_static(C.byref(cache), q, None, None, 0, o, None) == L.KVQ_ERR_INVALID_ARG
     assert lib.kvq_dequant(C.byref(cache), 0, 1, 0, o, None, None) == L.KVQ_ERR_INVALID_ARG
+
+
+def test_calibrated_keys_and_sink_layout_and_checks(K):
+    """key_calib and sink are NUQ-only; they add a calibration table (tau fp32, s and zp fp16 per
+    (KV head, channel)) and a sink region (the first token's K and V rows per (b, h)) after the
+    records; append refuses a key_calib cache until kvq_calibrate_keys has run."""
+    L = K._lib
+    lib = L.lib()
+    w = WL.WORKLOADS[2].scaled(batch=3, n_kv_heads=4, n_q_heads=4, ctx=5 * 128)
+    mk = lambda **kw: K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, w.n_blocks, w.dtype,
+                                    w.pre_rope, w.rope_theta, w.outlier_frac, layout="mma", **kw)
+    plain, both = K.kvq_layout(mk()), K.kvq_layout(mk(key_calib=True, sink=True))
+    assert plain.calib_bytes == 0 and plain.sink_bytes == 0 and plain.total_bytes < both.total_bytes
+    assert both.records_bytes == plain.records_bytes
+    assert both.calib_bytes == 4 * 128 * 8 and both.sink_bytes == 3 * 4 * 2 * 128 * 2
+    assert both.calib_off % 128 == 0 and both.calib_off >= plain.rope_off + plain.rope_bytes
+    assert both.sink_off % 128 == 0 and both.sink_off >= both.calib_off + both.calib_bytes
+    assert both.total_bytes == both.sink_off + both.sink_bytes
+    out = L.kvq_layout_t()
+    for kw in (dict(key_calib=True), dict(sink=True)):
+        assert lib.kvq_layout(C.byref(K.make_config("rtn", 2, 1, 1, 1, 4, **kw)), C.byref(out)) == L.KVQ_ERR_UNSUPPORTED
+    bad = mk()
+    bad.sink = 2
+    assert lib.kvq_layout(C.byref(bad), C.byref(out)) == L.KVQ_ERR_INVALID_ARG
+    cache = L.kvq_cache()
+    cache.cfg = mk(key_calib=True)
+    cache.lay = K.kvq_layout(cache.cfg)
+    cache.base = 0x100000
+    cache.codebook = 0x200000
+    k, v = C.c_void_p(0x1000), C.c_void_p(0x2000)
+    assert lib.kvq_append_block(C.byref(cache), k, v, 1, None, None) == L.KVQ_ERR_INVALID_ARG  # not calibrated
+    assert lib.kvq_calibrate_keys(C.byref(cache), k, 1, None) == L.KVQ_ERR_INVALID_ARG        # < 2 tokens
+    assert lib.kvq_calibrate_keys(C.byref(cache), C.c_void_p(0x1008), 64, None) == L.KVQ_ERR_ALIGNMENT
+    cache.cfg = mk()
+    assert lib.kvq_calibrate_keys(C.byref(cache), k, 64, None) == L.KVQ_ERR_INVALID_ARG        # no key_calib
