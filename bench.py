@@ -199,8 +199,11 @@ def run_kvq(args):
         w = w.scaled(ctx=args.ctx)
     nb = w.n_blocks
     n_pages = w.batch * (nb + 1) if args.paged else 0
+    if (args.key_calib or args.sink) and w.method != "nuq":
+        raise SystemExit("--key-calib and --sink apply to nuq workloads")
     cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, nb + 1, w.dtype, w.pre_rope,
-                        w.rope_theta, w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT, n_pages)
+                        w.rope_theta, w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT, n_pages, args.key_calib,
+                        args.sink)
     table = None
     if args.paged:  # every block on a page of a shuffled pool
         perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(5 + rank)).to(torch.int32)
@@ -217,6 +220,10 @@ def run_kvq(args):
     n_copies = max(1, math.ceil(3 * L2_BYTES / max(1, int(lay.records_bytes))))
     caches = [K.KVCache(cfg, cb, device=dev, block_table=table)]
     Kd, Vd, tk, tv, q, gen = _inputs(w, torch, dev, rank)
+    if args.key_calib:  # offline statistics from 3 blocks of the workload's keys drawn with another seed
+        kc = np.stack([np.concatenate([WL.tile(w, 0, h, blk, WL.KIND_K, seed=99) for blk in range(3)])
+                       for h in range(w.n_kv_heads)])
+        caches[0].calibrate_keys(torch.from_numpy(WL.to_storage(kc, w.dtype).view(np.int16)).to(dev).view(Kd.dtype))
     caches[0].append(Kd, Vd)
     del Kd, Vd
     for _ in range(n_copies - 1):
@@ -318,7 +325,8 @@ def run_kvq(args):
         "config": {"workload": w.name, "method": w.method, "bits": w.bits, "batch": w.batch,
                    "n_kv_heads": w.n_kv_heads, "n_q_heads": w.n_q_heads, "context": w.ctx,
                    "decodes_per_step": DECODES_PER_STEP, "tail_tokens": "0..127",
-                   "layout": BENCH_LAYOUT, "paged": bool(args.paged),
+                   "layout": BENCH_LAYOUT, "paged": bool(args.paged), "key_calib": bool(args.key_calib),
+                   "sink": bool(args.sink),
                    "packed_bytes_per_decode": cache_bytes, "cache_copies": n_copies,
                    "l2": f"{n_copies} cache copies rotated ({n_copies * int(lay.records_bytes) / 2**20:.0f} MiB > 3x L2)",
                    "parallelism": f"replicas x{world}"},
@@ -513,6 +521,9 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--key-calib", dest="key_calib", action="store_true",
+                    help="nuq: offline-calibrated key statistics (calibration keys drawn with another seed)")
+    ap.add_argument("--sink", action="store_true", help="nuq: keep the first token in the input precision")
     ap.add_argument("--paged", action="store_true",
                     help="records on the pages of a shuffled pool, found through a block table")
     ap.add_argument("--cpu-sample-heads", type=int, default=10)
