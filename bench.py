@@ -46,14 +46,14 @@ BENCH_LAYOUT = "mma"
 # shared header); once they change the traffic reads null until a new capture replaces it.
 # Captures and commands: profiles/dram_traffic_decode_kernels.md.
 PROFILED_TRAFFIC = {
-    2: {"bytes_per_record": 14872.4, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
-        "sha256_16": "6b6b842fdceb915a", "capture": "same workload at L = 16384 (4096 records)"},
-    3: {"bytes_per_record": 9790.3, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "447d708844969358", "capture": "full workload (8192 records)"},
-    4: {"bytes_per_record": 17086.6, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "447d708844969358", "capture": "same workload at L = 4096 (8192 records)"},
-    5: {"bytes_per_record": 9291.6, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "447d708844969358", "capture": "same workload at L = 65536 (16384 records)"},
+    2: {"bytes_per_record": 14867.7, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
+        "sha256_16": "6355dcc3031f38c7", "capture": "same workload at L = 16384 (4096 records)"},
+    3: {"bytes_per_record": 9783.2, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "009d5ee3f8020a06", "capture": "full workload (8192 records)"},
+    4: {"bytes_per_record": 17076.7, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "009d5ee3f8020a06", "capture": "same workload at L = 4096 (8192 records)"},
+    5: {"bytes_per_record": 9285.9, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "009d5ee3f8020a06", "capture": "same workload at L = 65536 (16384 records)"},
 }
 
 
