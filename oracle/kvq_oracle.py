@@ -547,6 +547,43 @@ def norm_direction_errors(K: np.ndarray, Kdq: np.ndarray):
     return (nk - nd) ** 2, 2.0 * nk * nd * (1.0 - cos)
 
 
+def token_error_stats(X: np.ndarray, Xdq: np.ndarray) -> np.ndarray:
+    """Per row (one token's 128 channels) of an input X and its reconstruction Xdq, fp64:
+    (|x|, |x_dq| - |x|, E_T = |x - x_dq|^2, E_D) with E_D the direction part of [KVN]'s split
+    |x - x_dq|^2 = (|x| - |x_dq|)^2 + 2|x||x_dq|(1 - cos theta) (key innovation, Figure 1a); the
+    norm part is E_M = (|x_dq| - |x|)^2, the square of the second column, and the second column
+    itself is the token-norm deviation of Figure 1b. Rows with a zero norm on either side have
+    no direction, so E_D = 0 there."""
+    X = np.asarray(X, np.float64)
+    Xdq = np.asarray(Xdq, np.float64)
+    nx = np.sqrt((X * X).sum(axis=-1))
+    nq = np.sqrt((Xdq * Xdq).sum(axis=-1))
+    et = ((X - Xdq) ** 2).sum(axis=-1)
+    both = (nx > 0) & (nq > 0)
+    cos = np.where(both, (X * Xdq).sum(axis=-1) / np.where(both, nx * nq, 1.0), 1.0)
+    ed = np.where(both, 2.0 * nx * nq * (1.0 - cos), 0.0)
+    return np.stack([nx, nq - nx, et, ed], axis=-1)
+
+
+def topk_error_share(stats: np.ndarray, fracs) -> np.ndarray:
+    """For each fraction f: the k = ceil(f * n) rows with the largest E_T (stats column 2; equal
+    errors: the lower row first) and, over them, (k, sum E_T, sum E_M, sum E_D) with E_M the
+    square of column 1 ([KVN] Figure 1a plots sum E_M / sum E_T against the top-k% of errors).
+    The sums run in fp64 over the rows' values as given."""
+    stats = np.asarray(stats).reshape(-1, 4)
+    n = stats.shape[0]
+    et = stats[:, 2].astype(np.float64)
+    em = stats[:, 1].astype(np.float64) ** 2
+    ed = stats[:, 3].astype(np.float64)
+    order = np.lexsort((np.arange(n), -et))  # E_T descending, then row ascending
+    out = np.zeros((len(fracs), 4))
+    for i, f in enumerate(fracs):
+        k = min(n, int(math.ceil(float(f) * n)))
+        sel = order[:k]
+        out[i] = (k, et[sel].sum(), em[sel].sum(), ed[sel].sum())
+    return out
+
+
 # =========================================================================== attention
 
 def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray) -> np.ndarray:

@@ -200,3 +200,42 @@ def test_sink_row_left_in_the_tiles_is_caught(monkeypatch):
                     self.sink_kv[(b, h)] = (np.array(Kx[b, h, 0], np.float64), np.array(Vx[b, h, 0], np.float64))
     monkeypatch.setattr(K.OracleCache, "append", append)
     assert _fails(P.test_sink_decode_equals_plain_attention_on_lossless_inputs, False)
+
+
+def test_direction_error_without_factor_two_is_caught(monkeypatch):
+    orig = K.token_error_stats
+
+    def half_ed(X, Xdq):
+        s = orig(X, Xdq)
+        s[..., 3] *= 0.5
+        return s
+    monkeypatch.setattr(K, "token_error_stats", half_ed)
+    monkeypatch.setattr(O, "token_error_stats", half_ed)
+    assert _fails(P.test_token_error_stats_closed_forms)
+
+
+def test_norm_deviation_sign_flip_is_caught(monkeypatch):
+    orig = K.token_error_stats
+
+    def flipped(X, Xdq):
+        s = orig(X, Xdq)
+        s[..., 1] *= -1.0
+        return s
+    monkeypatch.setattr(K, "token_error_stats", flipped)
+    monkeypatch.setattr(O, "token_error_stats", flipped)
+    assert _fails(P.test_token_error_stats_closed_forms)
+
+
+def test_topk_ties_to_the_higher_row_are_caught(monkeypatch):
+    def later_first(stats, fracs):
+        stats = np.asarray(stats).reshape(-1, 4)
+        n = stats.shape[0]
+        order = np.lexsort((-np.arange(n), -stats[:, 2].astype(np.float64)))
+        out = np.zeros((len(fracs), 4))
+        for i, f in enumerate(fracs):
+            sel = order[:min(n, int(np.ceil(float(f) * n)))]
+            out[i] = (len(sel), stats[sel, 2].sum(), (stats[sel, 1] ** 2).sum(), stats[sel, 3].sum())
+        return out
+    monkeypatch.setattr(K, "topk_error_share", later_first)
+    monkeypatch.setattr(O, "topk_error_share", later_first)
+    assert _fails(P.test_topk_error_share_brute_force)

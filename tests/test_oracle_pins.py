@@ -470,6 +470,66 @@ def test_norm_direction_decomposition_closed_forms():
     assert e[0][0] == pytest.approx(0.0) and e[1][0] == pytest.approx(2.0)   # rotation: direction only
 
 
+def test_token_error_stats_closed_forms():
+    x = np.array([[3.0, 4.0, 0.0], [1.0, 0.0, 0.0], [0.0, 2.0, 0.0], [0.0, 0.0, 0.0], [1.0, 1.0, 1.0]])
+    xq = np.array([[6.0, 8.0, 0.0],    # scaled copy: |dx| = |x|, all of it norm error
+                   [0.0, 1.0, 0.0],    # same norm, orthogonal: all of it direction error, 2|x|^2
+                   [0.0, 0.0, 0.0],    # reconstructed as zero: E_T = E_M = |x|^2, no direction
+                   [0.0, 0.0, 1.0],    # input zero
+                   [1.0, 1.0, 1.0]])   # exact
+    s = O.token_error_stats(x, xq)
+    assert np.allclose(s[0], [5.0, 5.0, 25.0, 0.0], atol=1e-12)
+    assert np.allclose(s[1], [1.0, 0.0, 2.0, 2.0], atol=1e-12)
+    assert np.allclose(s[2], [2.0, -2.0, 4.0, 0.0], atol=1e-12)
+    assert np.allclose(s[3], [0.0, 1.0, 1.0, 0.0], atol=1e-12)
+    assert np.allclose(s[4], [math.sqrt(3.0), 0.0, 0.0, 0.0], atol=1e-12)
+    # antiparallel copy of equal norm: E_D = 4|x|^2, E_M = 0
+    assert np.allclose(O.token_error_stats(x[:1], -x[:1])[0], [5.0, 0.0, 100.0, 100.0], atol=1e-9)
+
+
+def test_token_error_stats_identity_on_reconstructions():
+    """E_T = E_M + E_D on real reconstructions (RTN2 keys and values, int4), with the norm part
+    the square of the norm deviation; and E_T equals the squared error summed directly."""
+    w = WL.WORKLOADS[3]
+    for kind in (0, 1):
+        x = WL.tile(w, 0, 1, 3, kind)
+        c, s16, z16 = O.rtn_quantize(x, 2, 0 if kind == 0 else 1)
+        xq = O.rtn_dequant(c, s16, z16, 0 if kind == 0 else 1)
+        st = O.token_error_stats(x, xq)
+        em, ed = O.norm_direction_errors(x, xq)
+        assert np.allclose(st[:, 1] ** 2, em, rtol=1e-9, atol=1e-12)
+        assert np.allclose(st[:, 3], ed, rtol=1e-9, atol=1e-12)
+        assert np.allclose(st[:, 1] ** 2 + st[:, 3], st[:, 2], rtol=1e-9, atol=1e-12)
+        assert np.allclose(st[:, 2], [sum((float(a) - float(b)) ** 2 for a, b in zip(r, rq)) for r, rq in zip(x, xq)],
+                           rtol=1e-12)
+    q, s16 = O.int4_quantize(WL.tile(w, 0, 0, 0, 0))
+    xq = O.int4_dequant(q, s16)
+    st = O.token_error_stats(WL.tile(w, 0, 0, 0, 0), xq)
+    assert np.allclose(st[:, 1] ** 2 + st[:, 3], st[:, 2], rtol=1e-9, atol=1e-12)
+
+
+def test_topk_error_share_brute_force():
+    rng = np.random.default_rng(5)
+    n = 37
+    st = np.zeros((n, 4))
+    st[:, 0] = rng.random(n) + 1.0
+    st[:, 1] = rng.standard_normal(n) * 0.1
+    st[:, 2] = np.round(rng.random(n) * 8) / 8.0 + st[:, 1] ** 2  # several equal errors
+    st[:, 3] = st[:, 2] - st[:, 1] ** 2
+    st[[3, 17, 30], 2] = 7.0  # three-way tie at the top
+    fracs = [1 / 37, 2 / 37, 0.1, 0.5, 1.0]
+    got = O.topk_error_share(st, fracs)
+    for f, row in zip(fracs, got):
+        k = math.ceil(f * n)
+        ranked = sorted(range(n), key=lambda i: (-st[i, 2], i))[:k]  # Python's own sort
+        assert row[0] == k
+        assert row[1] == pytest.approx(math.fsum(st[i, 2] for i in ranked), rel=1e-14)
+        assert row[2] == pytest.approx(math.fsum(st[i, 1] ** 2 for i in ranked), rel=1e-14)
+        assert row[3] == pytest.approx(math.fsum(st[i, 3] for i in ranked), rel=1e-14)
+    assert got[0, 1] == 7.0 and got[0, 2] == st[3, 1] ** 2   # the tie goes to the lowest row
+    assert got[1, 2] == pytest.approx(st[3, 1] ** 2 + st[17, 1] ** 2, rel=1e-14)
+
+
 # ------------------------------------------------------------------ attention
 
 def _brute_attention(q, K, V):
