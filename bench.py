@@ -491,6 +491,123 @@ def run_reference(args):
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
+def run_diag(args):
+    """Error diagnostics ([KVN] Figures 1a/1b) over the whole cache of a workload: kvq_error_stats
+    (per-token |x|, norm deviation, E_T, E_D for K and V) timed as one launch, then
+    kvq_error_topk; the JSON line carries the E_M / E_T shares of the largest errors, and for
+    RTN / KVarN workloads the same shares with the other of the two methods on the same inputs."""
+    import torch
+    import bit_kv_cache_block_gb300 as K
+    import __graft_entry__
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    __graft_entry__.build()
+    K._lib.lib()
+    w = WL.WORKLOADS[args.config]
+    if args.ctx:
+        w = w.scaled(ctx=args.ctx)
+    nb = w.n_blocks
+    Kd, Vd, _, _, _, gen = _inputs(w, torch, dev, 0)
+    fracs = [0.001, 0.01, 0.05, 0.1, 1.0]
+
+    def build(method):
+        cfg = K.make_config(method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, nb, w.dtype, w.pre_rope,
+                            w.rope_theta, w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT)
+        cb = None
+        if method == "nuq":
+            from statistics import NormalDist
+            inv = NormalDist().inv_cdf
+            n = 2 ** w.bits
+            cb = torch.tensor([[inv((j + 0.5) / n) / inv((n - 0.5) / n) for j in range(n)]] * w.n_kv_heads,
+                              dtype=torch.float32)
+        c = K.KVCache(cfg, cb, device=dev)
+        c.append(Kd, Vd)
+        return cfg, c
+
+    def shares(c):
+        sk, sv = c.error_stats(Kd, Vd)
+        res = {}
+        for name, S in (("K", sk), ("V", sv)):
+            t = K.error_topk(S, fracs).cpu().numpy()
+            res[name] = {"top_frac": fracs, "k": [int(x) for x in t[:, 0]],
+                         "E_M_over_E_T": [round(float(x), 4) for x in t[:, 2] / t[:, 1]],
+                         "mean_E_T": [float("%.5g" % x) for x in t[:, 1] / t[:, 0]]}
+            nd = S[..., 1] / S[..., 0]
+            res[name]["token_norm_dev_p99_abs"] = float("%.4g" % torch.quantile(nd.abs().flatten()[:2 ** 24].float(), 0.99).item())
+        return res
+
+    cfg, cache = build(w.method)
+    shape = (w.batch, w.n_kv_heads, nb * 128, 4)
+    sk = torch.empty(shape, dtype=torch.float32, device=dev)
+    sv = torch.empty_like(sk)
+    n_rows = sk.numel() // 4
+    out = torch.empty(len(fracs), 4, dtype=torch.float64, device=dev)
+    tws = torch.empty(K.kvq_error_topk_workspace_bytes(), dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream()
+
+    def one():
+        K.kvq_error_stats(cache.cache, 0, nb, Kd, Vd, sk, sv, st)
+
+    def topk():
+        K.kvq_error_topk(sk, fracs, out, tws, st)
+
+    for _ in range(args.warmup):
+        one()
+        topk()
+    torch.cuda.synchronize()
+
+    def timed(fn, reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            fn()
+        e1.record(st)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(0).uuid)
+    except Exception:
+        gpu_id = "0"
+    with Clocks(gpu_id) as clk:
+        torch.cuda.synchronize()
+        ms = timed(one, args.steps)
+        topk_ms = timed(topk, max(3, args.steps // 4))
+        torch.cuda.synchronize()
+    if cache.device_status() != 0:
+        raise RuntimeError("device status %d" % cache.device_status())
+    in_bytes = 2 * Kd.numel() * Kd.element_size()
+    rec_bytes = K.kvq_decode_bytes(cfg, nb)
+    out_bytes = 2 * sk.numel() * 4
+    alg = in_bytes + rec_bytes + out_bytes
+    gbs = alg / (ms * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    diag = {w.method: shares(cache)}
+    if w.method in ("rtn", "varn"):
+        other = "varn" if w.method == "rtn" else "rtn"
+        _, c2 = build(other)
+        diag[other] = shares(c2)
+    return {
+        "metric": "error-stats GB/s (kvq_error_stats over the whole cache, K and V)", "value": round(gbs, 1),
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32 dequantise and sums", "data": f"synthetic ({gen}, seeded)",
+        "config": {"workload": w.name, "method": w.method, "bits": w.bits, "batch": w.batch,
+                   "n_kv_heads": w.n_kv_heads, "context": w.ctx, "layout": BENCH_LAYOUT, "rows": n_rows,
+                   "l2": f"inputs {in_bytes / 2**20:.0f} MiB per launch (> L2)"},
+        "us_error_stats": round(1e3 * ms, 2), "us_error_topk": round(1e3 * topk_ms, 2),
+        "topk_rows_per_s": round(n_rows / (topk_ms * 1e-3), 1),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None, "traffic_source": "not captured",
+                     "kernel": "error_stats_kernel", "peak_source": f"{peak_kind} hbm_gbs",
+                     "algorithmic_bytes": alg},
+        "gpu_launches": args.steps + 19 * max(3, args.steps // 4),
+        "diagnostics": diag,
+        "clocks": clk.summary(),
+    }
+
+
 def _decode_kernel_name(w):
     """The decode kernel the library picks for this workload (mirrors its dispatch rules)."""
     if w.method == "nuq" and w.bits == 3 and w.group == 1 and w.pre_rope:
@@ -528,9 +645,14 @@ def main():
                     help="records on the pages of a shuffled pool, found through a block table")
     ap.add_argument("--cpu-sample-heads", type=int, default=10)
     ap.add_argument("--ctx", type=int, default=0, help="override the context length (tokens, multiple of 128)")
+    ap.add_argument("--diag", action="store_true",
+                    help="time the error diagnostics (kvq_error_stats, kvq_error_topk) instead of decode")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    res = run_reference(args) if args.impl == "reference" else run_kvq(args)
+    if args.diag:
+        res = run_diag(args) if args.impl == "kvq" else {"impl": "reference", "unavailable": "--diag has no CPU arm"}
+    else:
+        res = run_reference(args) if args.impl == "reference" else run_kvq(args)
     if res is not None:
         print(json.dumps(res), flush=True)
 

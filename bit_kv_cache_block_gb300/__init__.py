@@ -18,7 +18,8 @@ from ._lib import (KVQ_BF16, KVQ_F16, KVQ_INT4, KVQ_LAYOUT_MMA, KVQ_LAYOUT_ROWS,
 
 __all__ = ["make_config", "kvq_layout", "kvq_dense_kv_bytes", "kvq_cache_init", "kvq_append_block",
            "kvq_truncate", "kvq_reset", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
-           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_dequant", "kvq_status_str", "KVCache", "KVQError", "kvq_config",
+           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_dequant", "kvq_error_stats", "kvq_error_topk",
+           "kvq_error_topk_workspace_bytes", "error_topk", "kvq_status_str", "KVCache", "KVQError", "kvq_config",
            "kvq_layout_t", "kvq_cache", "lib_path"]
 
 
@@ -152,6 +153,38 @@ def kvq_calibrate_keys(cache: kvq_cache, k_calib, stream=None) -> None:
                                              _stream(stream)), "kvq_calibrate_keys")
 
 
+def kvq_error_stats(cache: kvq_cache, first_block: int, n_blocks: int, k, v, stats_k, stats_v, stream=None) -> None:
+    """Per-token (|x|, |x_dq| - |x|, E_T, E_D) of cached blocks against their inputs; either
+    (k, stats_k) or (v, stats_v) may be None."""
+    _lib.check(_lib.lib().kvq_error_stats(C.byref(cache), _ptr(k), _ptr(v), int(first_block), int(n_blocks),
+                                          _ptr(stats_k), _ptr(stats_v), _stream(stream)), "kvq_error_stats")
+
+
+def kvq_error_topk_workspace_bytes() -> int:
+    return int(_lib.lib().kvq_error_topk_workspace_bytes())
+
+
+def kvq_error_topk(stats, fracs, out, workspace, stream=None) -> None:
+    """stats: device fp32 [..., 4] rows from kvq_error_stats; fracs: host sequence of fractions;
+    out: device fp64 [len(fracs)][4] = (k, sum E_T, sum E_M, sum E_D) over the k largest E_T."""
+    if stats.shape[-1] != 4:
+        raise ValueError("stats rows must have 4 columns")
+    fr = (C.c_double * len(fracs))(*[float(f) for f in fracs])
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _lib.check(_lib.lib().kvq_error_topk(_ptr(stats), int(stats.numel() // 4), fr, len(fracs), _ptr(out),
+                                         _ptr(workspace), ws_bytes, _stream(stream)), "kvq_error_topk")
+
+
+def error_topk(stats, fracs, stream=None):
+    """kvq_error_topk with its own output and workspace: returns fp64 [len(fracs)][4] on the
+    stats' device."""
+    import torch
+    out = torch.empty(len(fracs), 4, dtype=torch.float64, device=stats.device)
+    ws = torch.empty(kvq_error_topk_workspace_bytes(), dtype=torch.uint8, device=stats.device)
+    kvq_error_topk(stats, fracs, out, ws, stream)
+    return out
+
+
 class KVCache:
     """Convenience owner of the device buffers of one cache (allocated by PyTorch) plus the
     decode workspace; every call goes through the C ABI above."""
@@ -204,6 +237,23 @@ class KVCache:
         ov = torch.empty(shape, dtype=torch.float32, device=self.device)
         kvq_dequant(self.cache, first_block, n_blocks, domain, ok, ov, stream)
         return ok, ov
+
+    def error_stats(self, k, v, first_block: int = 0, stream=None):
+        """Per-token error statistics of blocks first_block .. first_block + n - 1 against the
+        inputs k, v [B][H_kv][n*128][128] they were appended from (either may be None): fp32
+        [B][H_kv][n*128][4] per kind = (|x|, |x_dq| - |x|, E_T, E_D)."""
+        import torch
+        src = k if k is not None else v
+        n_blocks = int(src.shape[2]) // 128
+        for x in (k, v):
+            if x is not None and (tuple(x.shape) != (self.cfg.batch, self.cfg.n_kv_heads, n_blocks * 128, 128)
+                                  or x.element_size() != 2):
+                raise ValueError("inputs must be [B][H_kv][n*128][128] in the cache's 16-bit input dtype")
+        shape = (self.cfg.batch, self.cfg.n_kv_heads, n_blocks * 128, 4)
+        sk = None if k is None else torch.empty(shape, dtype=torch.float32, device=self.device)
+        sv = None if v is None else torch.empty(shape, dtype=torch.float32, device=self.device)
+        kvq_error_stats(self.cache, first_block, n_blocks, k, v, sk, sv, stream)
+        return sk, sv
 
     def calibrate_keys(self, k_calib, stream=None):
         """Offline key statistics from calibration keys [H_kv][n_tokens][128] (key_calib caches)."""

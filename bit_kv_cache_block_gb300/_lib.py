@@ -24,7 +24,8 @@ METHODS = {"rtn": KVQ_RTN, "nuq": KVQ_NUQ, "varn": KVQ_VARN, "int4": KVQ_INT4}
 # every entry point declared in include/kvq.h
 EXPORTS = ["kvq_status_str", "kvq_dense_kv_bytes", "kvq_layout", "kvq_cache_init", "kvq_append_block",
            "kvq_truncate", "kvq_reset", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
-           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_dequant", "kvq_calibrate_keys"]
+           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_dequant", "kvq_calibrate_keys", "kvq_error_stats",
+           "kvq_error_topk_workspace_bytes", "kvq_error_topk"]
 
 
 class kvq_config(C.Structure):
@@ -94,6 +95,12 @@ def lib() -> C.CDLL:
     L.kvq_dequant.argtypes = [P(kvq_cache), i32, i32, i32, vp, vp, vp]
     L.kvq_calibrate_keys.restype = C.c_int
     L.kvq_calibrate_keys.argtypes = [P(kvq_cache), vp, i32, vp]
+    L.kvq_error_stats.restype = C.c_int
+    L.kvq_error_stats.argtypes = [P(kvq_cache), vp, vp, i32, i32, vp, vp, vp]
+    L.kvq_error_topk_workspace_bytes.restype = sz
+    L.kvq_error_topk_workspace_bytes.argtypes = []
+    L.kvq_error_topk.restype = C.c_int
+    L.kvq_error_topk.argtypes = [vp, C.c_int64, P(C.c_double), i32, vp, vp, sz, vp]
     _lib = L
     return L
 

@@ -17,6 +17,12 @@ cudaError_t kvq_launch_rope_init(float2* tab, int max_blocks, double theta, cuda
 cudaError_t kvq_launch_calibrate(const kvq::Geo& g, uint8_t* base, const uint16_t* k, int n_tokens, int rank,
                                  cudaStream_t st);
 cudaError_t kvq_static_workspace(float** ptr, size_t* n_floats);
+cudaError_t kvq_launch_error_stats(const kvq::Geo& g, const uint8_t* base, const float* codebook, int first, int n,
+                                   int hadamard, const uint16_t* in_k, const uint16_t* in_v, float* st_k, float* st_v,
+                                   int* status, cudaStream_t st);
+size_t kvq_topk_ws_bytes();
+cudaError_t kvq_launch_topk(const float* stats, unsigned long long n, const unsigned long long* k, int nf, double* out,
+                            void* ws, cudaStream_t st);
 
 namespace {
 
@@ -333,6 +339,47 @@ kvq_status kvq_dequant(const kvq_cache* cache, int32_t first_block, int32_t n_bl
     return kvq_launch_dequant(g, static_cast<const uint8_t*>(cache->base), cache->codebook, first_block, n_blocks,
                               domain, hadamard_of(cache->cfg), out_k, out_v, cache->dev_status, stream);
   });
+}
+
+kvq_status kvq_error_stats(const kvq_cache* cache, const void* k, const void* v, int32_t first_block,
+                           int32_t n_blocks, float* stats_k, float* stats_v, cudaStream_t stream) {
+  if (!cache || !cache->base) return KVQ_ERR_INVALID_ARG;
+  if (check_config(&cache->cfg) != KVQ_OK) return KVQ_ERR_INVALID_ARG;
+  if (first_block < 0 || n_blocks < 1 || (int64_t)first_block + n_blocks > cache->n_blocks)
+    return KVQ_ERR_INVALID_ARG;
+  if (n_blocks > 65535) return KVQ_ERR_INVALID_ARG;
+  if (!k != !stats_k || !v != !stats_v || (!k && !v)) return KVQ_ERR_INVALID_ARG;
+  for (const void* p : {k, v, (const void*)stats_k, (const void*)stats_v})
+    if (p && !aligned(p, 16)) return KVQ_ERR_ALIGNMENT;
+  kvq::Geo g;
+  if (kvq_status gs = geo_of(cache, g); gs != KVQ_OK) return gs;
+  return on_device(cache->device, [&]() {
+    return kvq_launch_error_stats(g, static_cast<const uint8_t*>(cache->base), cache->codebook, first_block, n_blocks,
+                                  hadamard_of(cache->cfg), static_cast<const uint16_t*>(k),
+                                  static_cast<const uint16_t*>(v), stats_k, stats_v, cache->dev_status, stream);
+  });
+}
+
+size_t kvq_error_topk_workspace_bytes(void) { return kvq_topk_ws_bytes(); }
+
+kvq_status kvq_error_topk(const float* stats, int64_t n_rows, const double* fracs, int32_t n_fracs, double* out,
+                          void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (!stats || !fracs || !out || !workspace) return KVQ_ERR_INVALID_ARG;
+  if (n_rows < 1 || n_rows > (int64_t)0xffffffffLL) return KVQ_ERR_INVALID_ARG;
+  if (n_fracs < 1 || n_fracs > KVQ_TOPK_MAX_FRACS) return KVQ_ERR_INVALID_ARG;
+  if (workspace_bytes < kvq_topk_ws_bytes()) return KVQ_ERR_CAPACITY;
+  if (!aligned(stats, 16) || !aligned(out, 8) || !aligned(workspace, 16)) return KVQ_ERR_ALIGNMENT;
+  unsigned long long kk[KVQ_TOPK_MAX_FRACS];
+  for (int f = 0; f < n_fracs; ++f) {
+    const double fr = fracs[f];
+    if (!(fr > 0.0 && fr <= 1.0)) return KVQ_ERR_INVALID_ARG;
+    double kd = std::ceil(fr * (double)n_rows);
+    if (kd > (double)n_rows) kd = (double)n_rows;
+    kk[f] = (unsigned long long)kd;
+  }
+  return kvq_launch_topk(stats, (unsigned long long)n_rows, kk, n_fracs, out, workspace, stream) == cudaSuccess
+             ? KVQ_OK
+             : KVQ_ERR_CUDA;
 }
 
 }  // extern "C"

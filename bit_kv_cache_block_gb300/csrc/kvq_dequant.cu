@@ -17,22 +17,16 @@ struct DequantArgs {
   int* status;
 };
 
-// grid (n, H, B*2), thread = token row of the tile; rows staged in shared memory (stride 129)
-// so that the inverse Hadamard transform and the stores run on whole rows.
-__global__ void __launch_bounds__(DQ_THREADS) dequant_kernel(DequantArgs a) {
-  extern __shared__ float xs[];
-  const Geo& g = a.g;
-  const int t = threadIdx.x;
-  const int bi = blockIdx.x, h = blockIdx.y, b = blockIdx.z >> 1, kind = blockIdx.z & 1;
-  float* out = kind ? a.out_v : a.out_k;
-  if (!out) return;
-  const int blk = a.first + bi;
-  const uint8_t* rec = a.base + record_offset(g, b, h, blk, a.status);
+// Row t of one tile record dequantised to fp32 into row[0..127]: token t for key tiles and
+// value tiles alike (the value planes of the tensor-core format hold channels per row and are
+// indexed accordingly), CSR outliers added for nuq, and for KVarN with the Hadamard transform
+// the inverse transform applied when to_input is set.
+__device__ void dequant_row(const Geo& g, const uint8_t* rec, const float* codebook, int h, int kind, int t,
+                            bool to_input, float* row) {
   const uint32_t* codes = reinterpret_cast<const uint32_t*>(rec + g.codes_off[kind]);
   const uint16_t* m = reinterpret_cast<const uint16_t*>(rec + g.meta_off[kind]);
   const int bits = g.bits, W = g.W, nw = 32 / bits;
   const uint32_t cmask = (1u << bits) - 1u;
-  float* row = xs + t * 129;
   for (int c = 0; c < D; ++c) {
     // rows of tokens (value tiles: rows of channels when vrows_ch), or the 3-bit planes
     const uint32_t q = g.planes3 ? tile3_code(codes, kind, t, c)
@@ -47,7 +41,7 @@ __global__ void __launch_bounds__(DQ_THREADS) dequant_kernel(DequantArgs a) {
       v = (float)((int)(q << 28) >> 28) * h2f(m[t]);
     } else {
       const int gi = kind == 0 ? c : t;
-      v = a.codebook[h * (1 << bits) + q] * h2f(m[gi]) + h2f(m[T + gi]);
+      v = codebook[h * (1 << bits) + q] * h2f(m[gi]) + h2f(m[T + gi]);
     }
     row[c] = v;
   }
@@ -59,7 +53,7 @@ __global__ void __launch_bounds__(DQ_THREADS) dequant_kernel(DequantArgs a) {
     const int j1 = min((int)rp[t + 1], g.n_out);
     for (int j = min((int)rp[t], g.n_out); j < j1; ++j) row[col[j] & (D - 1)] += h2f(val[j]);
   }
-  if (g.method == KVQ_VARN && a.hadamard && a.domain == 1) {
+  if (g.method == KVQ_VARN && to_input) {
     for (int hh = 1; hh < D; hh <<= 1)
       for (int j = 0; j < D / 2; ++j) {
         int i0 = (j / hh) * (2 * hh) + (j % hh);
@@ -69,9 +63,100 @@ __global__ void __launch_bounds__(DQ_THREADS) dequant_kernel(DequantArgs a) {
       }
     for (int c = 0; c < D; ++c) row[c] *= 0.08838834764831845f;
   }
+}
+
+// grid (n, H, B*2), thread = token row of the tile; rows staged in shared memory (stride 129)
+// so that the inverse Hadamard transform and the stores run on whole rows.
+__global__ void __launch_bounds__(DQ_THREADS) dequant_kernel(DequantArgs a) {
+  extern __shared__ float xs[];
+  const Geo& g = a.g;
+  const int t = threadIdx.x;
+  const int bi = blockIdx.x, h = blockIdx.y, b = blockIdx.z >> 1, kind = blockIdx.z & 1;
+  float* out = kind ? a.out_v : a.out_k;
+  if (!out) return;
+  const int blk = a.first + bi;
+  const uint8_t* rec = a.base + record_offset(g, b, h, blk, a.status);
+  dequant_row(g, rec, a.codebook, h, kind, t, a.hadamard && a.domain == 1, xs + t * 129);
   __syncthreads();
   float* dst = out + (((uint64_t)b * g.H + h) * (uint64_t)a.n * T + (uint64_t)bi * T) * D;
   for (int e = t; e < TILE; e += DQ_THREADS) dst[e] = xs[(e >> 7) * 129 + (e & 127)];
+}
+
+struct ErrArgs {
+  Geo g;
+  const uint8_t* base;
+  const float* codebook;
+  int first, n;
+  int hadamard;
+  const uint16_t* in_k;
+  const uint16_t* in_v;
+  float* st_k;
+  float* st_v;
+  int* status;
+};
+
+// Per-token error statistics ([KVN] key innovation: |x - x_dq|^2 = E_M + E_D). grid (n, H, B*2):
+// the tile is dequantised row by row into shared memory as above (input domain), then each warp
+// takes rows w, w + 4, ...: lane l reads channels l + 32j of the input row (coalesced) and of the
+// staged row (conflict-free), and the sums close with xor shuffles.
+__global__ void __launch_bounds__(DQ_THREADS) error_stats_kernel(ErrArgs a) {
+  extern __shared__ float xs[];
+  const Geo& g = a.g;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  const int bi = blockIdx.x, h = blockIdx.y, b = blockIdx.z >> 1, kind = blockIdx.z & 1;
+  const uint16_t* in = kind ? a.in_v : a.in_k;
+  float* st = kind ? a.st_v : a.st_k;
+  if (!in || !st) return;
+  const int blk = a.first + bi;
+  const uint8_t* rec = a.base + record_offset(g, b, h, blk, a.status);
+  float* row = xs + t * 129;
+  if (g.sink && blk == 0 && t == 0) {  // the kept first token: what decode attends
+    const uint16_t* kept = reinterpret_cast<const uint16_t*>(a.base + g.sink_off) + (((uint64_t)b * g.H + h) * 2 + kind) * D;
+    for (int c = 0; c < D; ++c) row[c] = in_bits_to_f32(kept[c], g.in_bf16);
+  } else {
+    dequant_row(g, rec, a.codebook, h, kind, t, a.hadamard != 0, row);
+  }
+  __syncthreads();
+  const uint64_t tok0 = ((uint64_t)b * g.H + h) * (uint64_t)a.n * T + (uint64_t)bi * T;
+  for (int r = warp; r < T; r += DQ_THREADS / 32) {
+    const uint16_t* xr = in + (tok0 + r) * D;
+    const float* qr = xs + r * 129;
+    float x[4], q[4];
+    float sxx = 0.0f, sqq = 0.0f, sdd = 0.0f, spm = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      x[j] = in_bits_to_f32(xr[lane + 32 * j], g.in_bf16);
+      q[j] = qr[lane + 32 * j];
+      const float dd = x[j] - q[j];
+      sxx = fmaf(x[j], x[j], sxx);
+      sqq = fmaf(q[j], q[j], sqq);
+      sdd = fmaf(dd, dd, sdd);
+      spm = fmaf(q[j] - x[j], q[j] + x[j], spm);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      sxx += __shfl_xor_sync(0xffffffffu, sxx, o);
+      sqq += __shfl_xor_sync(0xffffffffu, sqq, o);
+      sdd += __shfl_xor_sync(0xffffffffu, sdd, o);
+      spm += __shfl_xor_sync(0xffffffffu, spm, o);
+    }
+    const float nx = sqrtf(sxx), nq = sqrtf(sqq);
+    const float dn = nx + nq > 0.0f ? spm / (nx + nq) : 0.0f;
+    float ed = 0.0f;
+    if (nx > 0.0f && nq > 0.0f) {  // warp-uniform
+      const float ix = 1.0f / nx, iq = 1.0f / nq;
+      float su = 0.0f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float u = __fsub_rn(__fmul_rn(x[j], ix), __fmul_rn(q[j], iq));  // 0 when x_dq = x
+        su = fmaf(u, u, su);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
+      ed = nx * nq * su;
+    }
+    if (lane == 0) reinterpret_cast<float4*>(st)[tok0 + r] = make_float4(nx, dn, sdd, ed);
+  }
 }
 
 // RoPE tables: (cos, sin) of blk*128*theta_i for blk = 0..max_blocks, then of t*theta_i for
@@ -101,6 +186,20 @@ cudaError_t kvq_launch_dequant(const kvq::Geo& g, const uint8_t* base, const flo
   if (e != cudaSuccess) return e;
   dim3 grid(n, g.H, g.B * 2);
   kvq::dequant_kernel<<<grid, kvq::DQ_THREADS, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t kvq_launch_error_stats(const kvq::Geo& g, const uint8_t* base, const float* codebook, int first, int n,
+                                   int hadamard, const uint16_t* in_k, const uint16_t* in_v, float* st_k, float* st_v,
+                                   int* status, cudaStream_t st) {
+  kvq::ErrArgs a;
+  a.g = g; a.base = base; a.codebook = codebook; a.first = first; a.n = n; a.hadamard = hadamard;
+  a.in_k = in_k; a.in_v = in_v; a.st_k = st_k; a.st_v = st_v; a.status = status;
+  const int smem = kvq::T * 129 * (int)sizeof(float);
+  cudaError_t e = kvq::ensure_smem_attr((const void*)kvq::error_stats_kernel, (size_t)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid(n, g.H, g.B * 2);
+  kvq::error_stats_kernel<<<grid, kvq::DQ_THREADS, smem, st>>>(a);
   return cudaGetLastError();
 }
 

@@ -294,6 +294,46 @@ kvq_status kvq_decode_attn_static(const kvq_cache* cache, const void* q, const v
 kvq_status kvq_dequant(const kvq_cache* cache, int32_t first_block, int32_t n_blocks,
                        int32_t domain, float* out_k, float* out_v, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- error diagnostics
+ * [KVN] splits the squared reconstruction error of a token into a norm part and a direction
+ * part, |x - x_dq|^2 = E_M + E_D with E_M = (|x| - |x_dq|)^2 and E_D = 2|x||x_dq|(1 - cos theta)
+ * (key innovation; Figure 1a plots sum E_M / sum E_T over the largest errors, Figure 1b the
+ * token-norm deviation). These two calls compute both on the GPU for cached blocks. */
+
+/* Per-token error statistics of blocks [first_block, first_block + n_blocks) of every (b, h)
+ * against the inputs they were appended from. For each token row (its 128 channels, in the
+ * input domain: KVarN rows are transformed back from the Hadamard domain; pre-RoPE keys stay
+ * un-rotated) four fp32 values:
+ *   [0] |x|,  [1] |x_dq| - |x| (the token-norm deviation; E_M is its square),
+ *   [2] E_T = |x - x_dq|^2,  [3] E_D (0 when |x| or |x_dq| is 0).
+ * [1] and [3] are evaluated without cancellation: [1] = sum (x_dq - x)(x_dq + x) / (|x_dq| + |x|),
+ * [3] = |x||x_dq| |x/|x| - x_dq/|x_dq||^2. For caches with the attention sink, token 0 of block 0
+ * is the kept row (decode attends it instead of the tile's row).
+ *   k, v           : device [B][H_kv][n_blocks*128][128] in cfg.in_dtype: the rows given to
+ *                    kvq_append_block for those blocks (pre-RoPE keys for pre-RoPE caches)
+ *   stats_k/stats_v: device fp32 [B][H_kv][n_blocks*128][4]; either pair (k, stats_k) or
+ *                    (v, stats_v) may be NULL to skip that kind.
+ * Fails (KVQ_ERR_INVALID_ARG) outside the cached range. Inputs 16-byte aligned. */
+kvq_status kvq_error_stats(const kvq_cache* cache, const void* k, const void* v, int32_t first_block,
+                           int32_t n_blocks, float* stats_k, float* stats_v, cudaStream_t stream);
+
+/* Most fractions kvq_error_topk takes in one call. */
+#define KVQ_TOPK_MAX_FRACS 8
+
+/* Workspace kvq_error_topk needs, in bytes. Pure. */
+size_t kvq_error_topk_workspace_bytes(void);
+
+/* Shares of the largest errors ([KVN] Figure 1a). For each fraction f (host array, 0 < f <= 1):
+ * the k = ceil(f * n_rows) rows (k computed in fp64) of `stats` with the largest E_T (column 2;
+ * equal values: the lower row first) and, summed in fp64 over them,
+ *   out[i] = { k, sum E_T, sum E_M (column 1 squared), sum E_D }  (device fp64 [n_fracs][4]).
+ * stats: device fp32 [n_rows][4] as kvq_error_stats writes them (finite, E_T >= 0).
+ * The selection is a radix select on (E_T, row) keys; every step runs on `stream` with no host
+ * synchronisation and the sums come out in a fixed order (bitwise reproducible).
+ * 1 <= n_fracs <= KVQ_TOPK_MAX_FRACS, n_rows >= 1 and < 2^32. */
+kvq_status kvq_error_topk(const float* stats, int64_t n_rows, const double* fracs, int32_t n_fracs,
+                          double* out, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

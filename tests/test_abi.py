@@ -188,6 +188,28 @@ def test_host_argument_checks_launch_nothing(K):
         == L.KVQ_ERR_ALIGNMENT
     assert lib.kvq_dequant(C.byref(cache), 3, 2, 0, out, None, None) == L.KVQ_ERR_INVALID_ARG
     assert lib.kvq_dequant(C.byref(cache), 0, 1, 2, out, None, None) == L.KVQ_ERR_INVALID_ARG
+    # error statistics: range, pairing and alignment
+    x, sx = C.c_void_p(0x1000), C.c_void_p(0x7000)
+    assert lib.kvq_error_stats(C.byref(cache), x, None, 3, 2, sx, None, None) == L.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_error_stats(C.byref(cache), x, None, 0, 1, None, None, None) == L.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_error_stats(C.byref(cache), None, None, 0, 1, None, None, None) == L.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_error_stats(C.byref(cache), x, None, 0, 1, C.c_void_p(0x7004), None, None) \
+        == L.KVQ_ERR_ALIGNMENT
+    # top-k shares: sizes, fractions, workspace
+    wsb = lib.kvq_error_topk_workspace_bytes()
+    assert wsb > 0
+    fr = (C.c_double * 9)(*([0.5] * 9))
+    bad = (C.c_double * 2)(0.0, 0.5)
+    big = (C.c_double * 1)(1.5)
+    topk = lib.kvq_error_topk
+    assert topk(sx, 100, fr, 9, out, ws, wsb, None) == L.KVQ_ERR_INVALID_ARG          # > 8 fractions
+    assert topk(sx, 100, fr, 0, out, ws, wsb, None) == L.KVQ_ERR_INVALID_ARG
+    assert topk(sx, 0, fr, 1, out, ws, wsb, None) == L.KVQ_ERR_INVALID_ARG
+    assert topk(sx, 1 << 32, fr, 1, out, ws, wsb, None) == L.KVQ_ERR_INVALID_ARG
+    assert topk(sx, 100, bad, 2, out, ws, wsb, None) == L.KVQ_ERR_INVALID_ARG         # f = 0
+    assert topk(sx, 100, big, 1, out, ws, wsb, None) == L.KVQ_ERR_INVALID_ARG         # f > 1
+    assert topk(sx, 100, fr, 1, out, ws, wsb - 1, None) == L.KVQ_ERR_CAPACITY
+    assert topk(C.c_void_p(0x7008), 100, fr, 1, out, ws, wsb, None) == L.KVQ_ERR_ALIGNMENT
     assert lib.kvq_truncate(C.byref(cache), 5) == L.KVQ_ERR_INVALID_ARG
     assert lib.kvq_truncate(C.byref(cache), 2) == L.KVQ_OK and cache.n_blocks == 2
     assert lib.kvq_reset(C.byref(cache)) == L.KVQ_OK and cache.n_blocks == 0
