@@ -37,7 +37,8 @@ in the design notes):
   largest-|x| entries of a 128x128 tile (a per-tile fixed count stands in for
   the offline per-channel 99% threshold, which needs calibration data).
 * int4 absmax blocks are one token's 128 channels, symmetric, two's complement
-  nibbles ([TQ] §2.1 and §4.2 code).
+  nibbles ([TQ] §2.1 and §4.2 code); the variants take 8 bits ([TQ] §5.1's
+  sensitive layers) and/or blocks of 64 channels ([TQ] §2.1), two per token.
 * KVarN: x <- H x / sqrt(128) per token (Sylvester order); VarN alternates
   column then row population-std normalisation for 8 iterations with the
   scales accumulated in the log domain; for keys the channel scales merge into
@@ -254,40 +255,72 @@ def rtn_dequant(codes, s16, z16, axis: int) -> np.ndarray:
     return (q + z[:, None]) * s[:, None]
 
 
-# =========================================================================== int4 absmax
+# =========================================================================== int4 / int8 absmax
 
-def int4_quantize(x: np.ndarray):
-    """Symmetric int4 absmax blocks of 128 elements = one token's 128 channels.
+def absmax_quantize(x: np.ndarray, bits: int = 4, group: int = 128):
+    """Symmetric absmax integer blocks of `group` contiguous channels of one token: 128 (one
+    scale per token's head vector, the reading of [TQ] §4.1 "a scale every 128 elements") or 64
+    (two per token, [TQ] §2.1's smaller block), b = 4 bits or 8 (the "sensitive layer" precision
+    of [TQ] §5.1).
 
-    scale = absmax/7 (fp32 division), stored fp16 (saturating at the fp16 maximum);
-    q = clamp(rne(x/scale), -8, 7) with fp32 division; a zero scale gives q = 0
-    ([TQ] §2.1 block quantization and §4.2 quantize_kv_block).
-    Returns (q int8 [128][128], s16 [128]).
+    scale = absmax/(2^(b-1) - 1) (fp32 division), stored fp16 (saturating at the fp16 maximum);
+    q = clamp(rne(x/scale), -2^(b-1), 2^(b-1) - 1) with fp32 division; a zero scale gives q = 0
+    ([TQ] §2.1 block quantization and §4.2 quantize_kv_block, there with b = 4).
+    Returns (q int16 [128][128], s16 [128/group][128]: s16[g][t] scales channels g*group ..
+    g*group + group - 1 of token t).
     """
+    assert bits in (4, 8) and group in (64, 128)
     x = _f32(x)
-    a = np.abs(x).max(axis=1)
-    s16 = _half(np.minimum(a / np.float32(7.0), np.float32(65504.0)))
+    qmax = 2 ** (bits - 1) - 1
+    ng = D // group
+    xg = x.reshape(T, ng, group)
+    a = np.abs(xg).max(axis=2)                                       # [t][g]
+    s16 = _half(np.minimum(a / np.float32(qmax), np.float32(65504.0)))
     sf = _f32_of_half(s16)
     with np.errstate(invalid="ignore", divide="ignore"):
-        t = x / sf[:, None]
-        q = np.clip(np.rint(t), -8, 7)
-    q[sf == 0, :] = 0
-    return q.astype(np.int8), s16
+        t = xg / sf[:, :, None]
+        q = np.clip(np.rint(t), -qmax - 1, qmax)
+    q[sf == 0] = 0
+    return q.reshape(T, D).astype(np.int16), np.ascontiguousarray(s16.T)
+
+
+def int4_quantize(x: np.ndarray):
+    """absmax_quantize with b = 4 and one scale per token: (q int8 [128][128], s16 [128])."""
+    q, s16 = absmax_quantize(x, 4, 128)
+    return q.astype(np.int8), s16[0]
+
+
+def absmax_codes(q: np.ndarray, bits: int = 4) -> np.ndarray:
+    """Two's complement b-bit code q & (2^b - 1) ([TQ] §4.2, `q.to(int8) & 0xF` for b = 4)."""
+    return (np.asarray(q, np.int16) & ((1 << bits) - 1)).astype(np.uint8)
+
+
+def absmax_from_codes(codes: np.ndarray, bits: int = 4) -> np.ndarray:
+    n = np.asarray(codes, np.int16)
+    return np.where(n >= 2 ** (bits - 1), n - 2 ** bits, n).astype(np.int16)
 
 
 def int4_nibbles(q: np.ndarray) -> np.ndarray:
-    """Two's complement nibble q & 0xF ([TQ] §4.2, `q.to(int8) & 0xF`)."""
-    return (np.asarray(q, np.int16) & 0xF).astype(np.uint8)
+    return absmax_codes(q, 4)
 
 
 def int4_from_nibbles(nib: np.ndarray) -> np.ndarray:
-    n = np.asarray(nib, np.int16)
-    return np.where(n >= 8, n - 16, n).astype(np.int8)
+    return absmax_from_codes(nib, 4).astype(np.int8)
+
+
+def absmax_dequant(q, s16) -> np.ndarray:
+    """x_dq = q * scale of the element's group (zero point 0), fp64. s16: [128] (one group per
+    token) or [n_groups][128]."""
+    s = np.asarray(s16, np.float64)
+    if s.ndim == 1:
+        s = s[None, :]
+    group = D // s.shape[0]
+    return np.asarray(q, np.float64) * np.repeat(s.T, group, axis=1)
 
 
 def int4_dequant(q, s16) -> np.ndarray:
     """x_dq = q * scale (zero point 0), fp64."""
-    return np.asarray(q, np.float64) * np.asarray(s16, np.float64)[:, None]
+    return absmax_dequant(q, s16)
 
 
 # =========================================================================== nuq (KVQuant)
@@ -617,8 +650,10 @@ class OracleCache:
     def __init__(self, method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: int,
                  pre_rope: bool = False, rope_theta: float = 10000.0, outlier_frac: float = 0.01,
                  varn_iters: int = 8, use_hadamard: bool = True, codebook=None, layout: int = LAYOUT_ROWS,
-                 key_calib=None, sink: bool = False):
+                 key_calib=None, sink: bool = False, scale_group: int = 128):
         assert method in ("rtn", "nuq", "varn", "int4")
+        assert scale_group == 128 or method == "int4"
+        self.scale_group = scale_group
         assert layout in (LAYOUT_ROWS, LAYOUT_MMA)
         self.method, self.bits, self.layout = method, bits, layout
         self.batch, self.n_kv_heads, self.n_q_heads = batch, n_kv_heads, n_q_heads
@@ -638,7 +673,7 @@ class OracleCache:
     def for_workload(cls, w, **kw):
         return cls(w.method, w.bits, kw.pop("batch", w.batch), w.n_kv_heads, w.n_q_heads,
                    pre_rope=w.pre_rope, rope_theta=w.rope_theta, outlier_frac=w.outlier_frac,
-                   varn_iters=w.varn_iters, **kw)
+                   varn_iters=w.varn_iters, scale_group=getattr(w, "scale_group", 128), **kw)
 
     # ------------------------------------------------------------------ encode
     def quantize_tile(self, x: np.ndarray, kind: int, h: int = 0) -> dict:
@@ -647,8 +682,8 @@ class OracleCache:
             codes, s16, z16 = rtn_quantize(x, b, 0 if kind == KIND_K else 1)
             rec = dict(codes=codes, s16=s16, z16=z16)
         elif m == "int4":
-            q, s16 = int4_quantize(x)
-            rec = dict(codes=int4_nibbles(q), s16=s16)
+            q, s16 = absmax_quantize(x, b, self.scale_group)
+            rec = dict(codes=absmax_codes(q, b), s16=s16[0] if s16.shape[0] == 1 else s16)
         elif m == "nuq" and kind == KIND_K and self.key_calib is not None:
             tau, s16, zp16 = (np.asarray(a)[h] for a in self.key_calib)
             rec = nuq_quantize_calibrated(x, self.codebook[h], tau, s16, zp16, self.n_out)
@@ -688,7 +723,7 @@ class OracleCache:
         if m == "rtn":
             x = rtn_dequant(codes, rec["s16"], rec["z16"], 0 if kind == KIND_K else 1)
         elif m == "int4":
-            x = int4_dequant(int4_from_nibbles(codes), rec["s16"])
+            x = absmax_dequant(absmax_from_codes(codes, self.bits), rec["s16"])
         elif m == "nuq":
             x = nuq_dequant(codes, rec["s16"], rec["zp16"], self.codebook[h],
                             0 if kind == KIND_K else 1, rec["row_ptr"], rec["col"], rec["val"])

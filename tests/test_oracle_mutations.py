@@ -239,3 +239,33 @@ def test_topk_ties_to_the_higher_row_are_caught(monkeypatch):
     monkeypatch.setattr(K, "topk_error_share", later_first)
     monkeypatch.setattr(O, "topk_error_share", later_first)
     assert _fails(P.test_topk_error_share_brute_force)
+
+
+def test_int8_divisor_128_is_caught(monkeypatch):
+    orig = K.absmax_quantize
+
+    def wrong(x, bits=4, group=128):
+        if bits != 8:
+            return orig(x, bits, group)
+        x = np.asarray(x, np.float32)
+        ng = 128 // group
+        xg = x.reshape(128, ng, group)
+        s16 = np.minimum(np.abs(xg).max(axis=2) / np.float32(128.0), np.float32(65504.0)).astype(np.float16)
+        sf = s16.astype(np.float32)
+        with np.errstate(invalid="ignore", divide="ignore"):
+            q = np.clip(np.rint(xg / sf[:, :, None]), -128, 127)
+        q[sf == 0] = 0
+        return q.reshape(128, 128).astype(np.int16), np.ascontiguousarray(s16.T)
+    monkeypatch.setattr(K, "absmax_quantize", wrong)
+    monkeypatch.setattr(O, "absmax_quantize", wrong)
+    assert _fails(P.test_absmax_variants_codes_range_and_bound, 8, 128)
+
+
+def test_group64_scales_of_the_wrong_half_are_caught(monkeypatch):
+    orig = K.absmax_dequant
+
+    def swapped(q, s16):
+        s = np.asarray(s16)
+        return orig(q, s[::-1] if s.ndim == 2 and s.shape[0] == 2 else s)
+    monkeypatch.setattr(K, "absmax_dequant", swapped)
+    assert _fails(P.test_cache_decode_equals_plain_attention_on_lossless_inputs, "int4g64", 1, False)

@@ -249,6 +249,60 @@ def test_int4_zero_block_and_lossless_grid():
     assert O.int4_nibbles(np.array([-1, -7, 7, 0]))[:4].tolist() == [15, 9, 7, 0]
 
 
+@pytest.mark.parametrize("bits,group", [(8, 128), (8, 64), (4, 64)])
+def test_absmax_variants_codes_range_and_bound(bits, group):
+    """8-bit and 64-channel blocks ([TQ] §5.1, §2.1): codes within +-(2^(b-1)-1), each block's
+    largest element at the end of the range, |x - q*s| <= s/2 per block, s = absmax/(2^(b-1)-1)
+    rounded once to fp16, codes round-trip through their two's complement form."""
+    w = WL.WORKLOADS[4]
+    qmax = 2 ** (bits - 1) - 1
+    for blk in range(2):
+        x = WL.tile(w, 1, 2, blk, WL.KIND_K)
+        q, s16 = O.absmax_quantize(x, bits, group)
+        assert s16.shape == (128 // group, 128)
+        assert q.min() >= -qmax and q.max() <= qmax
+        xg = x.astype(np.float64).reshape(128, 128 // group, group)
+        a = np.abs(xg).max(axis=2)                       # [t][g]
+        s = s16.T.astype(np.float64)                     # [t][g]
+        assert np.all(np.abs(s - a / qmax) <= np.abs(a / qmax) * 2.0 ** -11)
+        qg = q.reshape(128, 128 // group, group)
+        for t in range(0, 128, 7):
+            for g in range(128 // group):
+                j = int(np.argmax(np.abs(xg[t, g])))
+                assert abs(int(qg[t, g, j])) == qmax
+        err = np.abs(xg - qg * s[:, :, None])
+        assert np.all(err <= s[:, :, None] * 0.5 * (1 + 2.0 ** -10))
+        assert np.allclose(O.absmax_dequant(q, s16), (qg * s[:, :, None]).reshape(128, 128), rtol=0, atol=0)
+        codes = O.absmax_codes(q, bits)
+        assert codes.max() < 2 ** bits and np.array_equal(O.absmax_from_codes(codes, bits), q)
+    assert O.absmax_codes(np.array([-1, -127, 127, -128]), 8).tolist() == [255, 129, 127, 128]
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_absmax_group64_is_group128_on_each_half(bits):
+    """A 64-channel block is a 128-channel block whose other half is zero."""
+    x = WL.tile(WL.WORKLOADS[4], 0, 1, 1, WL.KIND_V)
+    q, s16 = O.absmax_quantize(x, bits, 64)
+    for g in range(2):
+        pad = np.zeros_like(x)
+        pad[:, :64] = x[:, 64 * g:64 * (g + 1)]
+        q1, s1 = O.absmax_quantize(pad, bits, 128)
+        assert np.array_equal(q[:, 64 * g:64 * (g + 1)], q1[:, :64]) and not q1[:, 64:].any()
+        assert np.array_equal(s16[g], s1[0])
+
+
+def test_absmax_int8_lossless_grid_and_zero_block():
+    rng = np.random.default_rng(3)
+    q0 = rng.integers(-127, 128, size=(128, 128))
+    q0[:, 5], q0[:, 77] = 127, -127
+    x = (q0 * 0.0078125).astype(np.float32)      # scale = 127/128/127 = 2^-7 exactly
+    for group in (128, 64):
+        q, s16 = O.absmax_quantize(x, 8, group)
+        assert np.array_equal(q, q0) and np.all(s16 == 0.0078125)
+    q, s16 = O.absmax_quantize(np.zeros((128, 128), np.float32), 8, 64)
+    assert not q.any() and not s16.any()
+
+
 # ------------------------------------------------------------------ nuq (KVQuant)
 
 def test_worked_example_normalise_and_argmin(golden_dir):
@@ -579,9 +633,10 @@ def _lossless_cache_inputs(method, B, H, n_blocks, rng, cb=None):
                     qv = rng.integers(0, 4, (128, 128)); qv[:, 0], qv[:, 1] = 0, 3
                     K[b, h, sl] = (qk - 1.5) * ch
                     V[b, h, sl] = (qv - 2.0) * tok
-                elif method == "int4":         # per token for both
-                    qk = rng.integers(-7, 8, (128, 128)); qk[:, 3] = -7
-                    qv = rng.integers(-7, 8, (128, 128)); qv[:, 9] = 7
+                elif method.startswith("int"):  # per token (per half-token for g64) for both
+                    m = 127 if method.startswith("int8") else 7
+                    qk = rng.integers(-m, m + 1, (128, 128)); qk[:, 3] = qk[:, 70] = -m
+                    qv = rng.integers(-m, m + 1, (128, 128)); qv[:, 9] = qv[:, 100] = m
                     K[b, h, sl] = qk * 0.125 * tok
                     V[b, h, sl] = qv * 0.0625 * tok[::-1]
                 else:                          # nuq with a dyadic codebook, no outliers
@@ -593,7 +648,8 @@ def _lossless_cache_inputs(method, B, H, n_blocks, rng, cb=None):
 
 
 @pytest.mark.parametrize("method,G,pre_rope", [("rtn", 1, False), ("rtn", 4, False),
-                                               ("int4", 4, False), ("nuq", 1, True), ("nuq", 2, False)])
+                                               ("int4", 4, False), ("nuq", 1, True), ("nuq", 2, False),
+                                               ("int8", 2, False), ("int4g64", 1, False), ("int8g64", 4, False)])
 def test_cache_decode_equals_plain_attention_on_lossless_inputs(method, G, pre_rope):
     """On inputs the quantizer reproduces exactly, decode over the packed cache must equal
     plain fp64 attention over the raw K/V (RoPE at absolute positions for pre-RoPE keys),
@@ -601,9 +657,10 @@ def test_cache_decode_equals_plain_attention_on_lossless_inputs(method, G, pre_r
     rng = np.random.default_rng(12)
     B, H, nb = 2, 2, 3
     cb = np.array([-1, -0.75, -0.5, -0.25, 0.25, 0.5, 0.75, 1.0], np.float32)
-    bits = {"rtn": 2, "int4": 4, "nuq": 3}[method]
-    cache = O.OracleCache(method, bits, B, H, H * G, pre_rope=pre_rope, outlier_frac=0.0,
-                          codebook=cb if method == "nuq" else None)
+    bits = {"rtn": 2, "int4": 4, "nuq": 3, "int8": 8, "int4g64": 4, "int8g64": 8}[method]
+    group = 64 if method.endswith("g64") else 128
+    cache = O.OracleCache("int4" if method.startswith("int") else method, bits, B, H, H * G, pre_rope=pre_rope,
+                          outlier_frac=0.0, codebook=cb if method == "nuq" else None, scale_group=group)
     K, V = _lossless_cache_inputs(method, B, H, nb, rng, cb)
     cache.append(K[:, :, :256], V[:, :, :256])
     cache.append(K[:, :, 256:], V[:, :, 256:])

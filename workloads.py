@@ -48,6 +48,7 @@ class Workload:
     rope_theta: float = 10000.0
     outlier_frac: float = 0.01
     varn_iters: int = 8
+    scale_group: int = 128   # int4 / int8 absmax: channels per scale (128 or 64)
 
     @property
     def n_blocks(self) -> int:
