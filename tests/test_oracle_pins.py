@@ -639,6 +639,9 @@ def _lossless_cache_inputs(method, B, H, n_blocks, rng, cb=None):
                     qv = rng.integers(-m, m + 1, (128, 128)); qv[:, 9] = qv[:, 100] = m
                     K[b, h, sl] = qk * 0.125 * tok
                     V[b, h, sl] = qv * 0.0625 * tok[::-1]
+                    if method.endswith("g64"):  # the two halves of a token on different grids
+                        K[b, h, sl, 64:] *= 2.0
+                        V[b, h, sl, 64:] *= 0.5
                 else:                          # nuq with a dyadic codebook, no outliers
                     qk = rng.integers(0, 8, (128, 128)); qk[0], qk[1] = 0, 7
                     qv = rng.integers(0, 8, (128, 128)); qv[:, 0], qv[:, 1] = 0, 7
