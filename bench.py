@@ -179,6 +179,20 @@ def _inputs(w, torch, dev, rank):
     return Kd, Vd, tk, tv, q, "torch-device"
 
 
+def _workload(args):
+    """The chosen workload, with the context and the absmax format overrides applied."""
+    w = WL.WORKLOADS[args.config]
+    if args.ctx:
+        w = w.scaled(ctx=args.ctx)
+    if args.bits or args.scale_group:
+        if w.method != "int4":
+            raise SystemExit("--bits and --scale-group apply to the absmax (int4) workload")
+        w = w.scaled(bits=args.bits or w.bits, scale_group=args.scale_group or w.scale_group)
+        w = w.scaled(name=w.name.replace("int4", f"int{w.bits}") +
+                     (", 64-channel scales" if w.scale_group == 64 else ""))
+    return w
+
+
 def run_kvq(args):
     import torch
     import bit_kv_cache_block_gb300 as K
@@ -194,16 +208,14 @@ def run_kvq(args):
     if world > 1:
         torch.distributed.barrier()
     K._lib.lib()
-    w = WL.WORKLOADS[args.config]
-    if args.ctx:
-        w = w.scaled(ctx=args.ctx)
+    w = _workload(args)
     nb = w.n_blocks
     n_pages = w.batch * (nb + 1) if args.paged else 0
     if (args.key_calib or args.sink) and w.method != "nuq":
         raise SystemExit("--key-calib and --sink apply to nuq workloads")
     cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, nb + 1, w.dtype, w.pre_rope,
                         w.rope_theta, w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT, n_pages, args.key_calib,
-                        args.sink)
+                        args.sink, w.scale_group)
     table = None
     if args.paged:  # every block on a page of a shuffled pool
         perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(5 + rank)).to(torch.int32)
@@ -314,18 +326,22 @@ def run_kvq(args):
     dec_avg_us = (1e3 * step_ms - app_us) / DECODES_PER_STEP
     peak, peak_kind = _peaks()
     achieved = cache_bytes / (dec0_us * 1e-6) / 1e9   # decode call with an empty tail
-    traffic, traffic_note = _profiled_traffic(w.cfg_id, w.batch * w.n_kv_heads * nb)
+    base_w = WL.WORKLOADS[w.cfg_id]
+    same_format = (w.bits, w.scale_group) == (base_w.bits, base_w.scale_group)
+    traffic, traffic_note = (_profiled_traffic(w.cfg_id, w.batch * w.n_kv_heads * nb) if same_format
+                             else (None, "no capture for this format"))
     res = {
         "metric": "quantized decode-attn packed-KV GB/s (% of 8 TB/s HBM), us/step; append tokens/s",
         "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": {"rtn": "u%d codes, fp32 accumulate" % w.bits, "nuq": "u3 codes + fp16 csr, fp32 accumulate",
-                  "varn": "u2 codes, fp32 accumulate", "int4": "s4 codes, fp32 accumulate"}[w.method],
+                  "varn": "u2 codes, fp32 accumulate", "int4": "s%d codes, fp32 accumulate" % w.bits}[w.method],
         "data": f"synthetic ({gen}, seeded)",
         "config": {"workload": w.name, "method": w.method, "bits": w.bits, "batch": w.batch,
                    "n_kv_heads": w.n_kv_heads, "n_q_heads": w.n_q_heads, "context": w.ctx,
                    "decodes_per_step": DECODES_PER_STEP, "tail_tokens": "0..127",
-                   "layout": BENCH_LAYOUT, "paged": bool(args.paged), "key_calib": bool(args.key_calib),
+                   "layout": BENCH_LAYOUT, "scale_group": w.scale_group,
+                   "paged": bool(args.paged), "key_calib": bool(args.key_calib),
                    "sink": bool(args.sink),
                    "packed_bytes_per_decode": cache_bytes, "cache_copies": n_copies,
                    "l2": f"{n_copies} cache copies rotated ({n_copies * int(lay.records_bytes) / 2**20:.0f} MiB > 3x L2)",
@@ -503,16 +519,15 @@ def run_diag(args):
     dev = torch.device("cuda", 0)
     __graft_entry__.build()
     K._lib.lib()
-    w = WL.WORKLOADS[args.config]
-    if args.ctx:
-        w = w.scaled(ctx=args.ctx)
+    w = _workload(args)
     nb = w.n_blocks
     Kd, Vd, _, _, _, gen = _inputs(w, torch, dev, 0)
     fracs = [0.001, 0.01, 0.05, 0.1, 1.0]
 
     def build(method):
         cfg = K.make_config(method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, nb, w.dtype, w.pre_rope,
-                            w.rope_theta, w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT)
+                            w.rope_theta, w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT,
+                            scale_group=w.scale_group if method == "int4" else 128)
         cb = None
         if method == "nuq":
             from statistics import NormalDist
@@ -612,7 +627,7 @@ def _decode_kernel_name(w):
     """The decode kernel the library picks for this workload (mirrors its dispatch rules)."""
     if w.method == "nuq" and w.bits == 3 and w.group == 1 and w.pre_rope:
         return "decode_nuq_kernel"
-    if w.method in ("rtn", "varn", "int4") and w.bits in (2, 4) and w.group <= 4:
+    if w.method in ("rtn", "varn", "int4") and w.bits in (2, 4) and w.group <= 4 and w.scale_group == 128:
         return "decode_mma_kernel"
     return "decode_kernel"
 
@@ -621,7 +636,7 @@ def _decode_bytes_per_head(w):
     """Algorithmic packed bytes of one (b, h) over the context (same count as kvq_decode_bytes)."""
     # 3-bit tiles: 48 B per 128 codes as bit planes, 52 B as 10-code rows
     W = 12 if (w.bits == 3 and BENCH_LAYOUT == "mma") else -(-128 // (32 // w.bits))
-    meta = {"rtn": 2, "nuq": 2, "varn": 3, "int4": 1}[w.method] * 256
+    meta = {"rtn": 2, "nuq": 2, "varn": 3, "int4": 2 if w.scale_group == 64 else 1}[w.method] * 256
     csr = 0
     if w.method == "nuq":
         n = math.ceil(float(np.float32(w.outlier_frac)) * 16384)
@@ -645,6 +660,10 @@ def main():
                     help="records on the pages of a shuffled pool, found through a block table")
     ap.add_argument("--cpu-sample-heads", type=int, default=10)
     ap.add_argument("--ctx", type=int, default=0, help="override the context length (tokens, multiple of 128)")
+    ap.add_argument("--bits", type=int, default=0, choices=[0, 4, 8],
+                    help="absmax workload: code width (8: the sensitive-layer precision)")
+    ap.add_argument("--scale-group", dest="scale_group", type=int, default=0, choices=[0, 64, 128],
+                    help="absmax workload: channels per scale")
     ap.add_argument("--diag", action="store_true",
                     help="time the error diagnostics (kvq_error_stats, kvq_error_topk) instead of decode")
     args = ap.parse_args()

@@ -38,12 +38,14 @@ kvq_status check_config(const kvq_config* c) {
   if (c->n_q_heads % c->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
   if (c->n_q_heads / c->n_kv_heads > KVQ_MAX_GROUP) return KVQ_ERR_UNSUPPORTED;
   if (c->in_dtype != KVQ_F16 && c->in_dtype != KVQ_BF16) return KVQ_ERR_INVALID_ARG;
-  if (c->bits < 2 || c->bits > 4) return KVQ_ERR_UNSUPPORTED;
+  if ((c->bits < 2 || c->bits > 4) && !(c->method == KVQ_INT4 && c->bits == 8)) return KVQ_ERR_UNSUPPORTED;
   if (c->layout != KVQ_LAYOUT_ROWS && c->layout != KVQ_LAYOUT_MMA) return KVQ_ERR_INVALID_ARG;
   if (c->n_pages < 0 || c->n_pages > (1 << 28)) return KVQ_ERR_INVALID_ARG;
   if ((c->key_calib != 0 && c->key_calib != 1) || (c->sink != 0 && c->sink != 1)) return KVQ_ERR_INVALID_ARG;
   if ((c->key_calib || c->sink) && c->method != KVQ_NUQ) return KVQ_ERR_UNSUPPORTED;
-  if (c->method == KVQ_INT4 && c->bits != 4) return KVQ_ERR_UNSUPPORTED;
+  if (c->method == KVQ_INT4 && c->bits != 4 && c->bits != 8) return KVQ_ERR_UNSUPPORTED;
+  if (c->scale_group != 0 && c->scale_group != 128 && c->scale_group != 64) return KVQ_ERR_INVALID_ARG;
+  if (c->scale_group == 64 && c->method != KVQ_INT4) return KVQ_ERR_UNSUPPORTED;
   if (c->pre_rope != 0 && c->pre_rope != 1) return KVQ_ERR_INVALID_ARG;
   if (c->pre_rope && c->method != KVQ_NUQ) return KVQ_ERR_UNSUPPORTED;
   if (c->pre_rope && !(c->rope_theta > 1.0)) return KVQ_ERR_INVALID_ARG;
@@ -112,7 +114,7 @@ kvq_status kvq_layout(const kvq_config* c, kvq_layout_t* out) {
   l.words_per_row = kvq::words_per_row(c->bits, c->layout);
   l.n_outliers = c->method == KVQ_NUQ ? kvq::n_outliers_for(c->outlier_frac) : 0;
   const uint64_t codes = (uint64_t)kvq::T * l.words_per_row * 4;
-  const uint64_t meta = (uint64_t)kvq::meta_vectors(c->method) * kvq::T * 2;
+  const uint64_t meta = (uint64_t)kvq::meta_vectors(c->method, c->scale_group) * kvq::T * 2;
   const uint64_t csr = kvq::csr_bytes_for(l.n_outliers);
   uint64_t off = 0;
   for (int k = 0; k < 2; ++k) {

@@ -6,7 +6,7 @@
 //          ([KVN] preliminaries, KIVI representation (K_q + z) * s; [KVQ] §1.2, §3.1)
 //   VARN : FWHT-128 on each token row, Sinkhorn-style variance normalisation (columns, then
 //          rows, repeated), merge of the scales, RTN, second scale s1 ([KVN] method steps 1-4)
-//   INT4 : per-token absmax/7 -> fp16 scale -> q = clamp(rne(x/s), -8, 7) -> nibbles
+//   INT4 : per-token (or per-64-channel) absmax/(2^(b-1)-1) -> fp16 scale -> q = clamp(rne(x/s)) -> b-bit two's complement (b = 4, 8)
 //          ([TQ] §2.1, §4.2 quantize_kv_block)
 //   NUQ  : exact top-n |x| selection (radix select on the fp16 magnitude, ties to the lower
 //          flat index) -> CSR; centre/half-range of the non-outliers -> nearest codebook entry
@@ -270,26 +270,29 @@ __global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
     }
     rtn_tile(sm, axis, g.bits, m16);
   } else if (g.method == KVQ_INT4) {
+    // scale = absmax / qmax per token (or per half-token), q = clamp(rne(x / scale), -qmax-1, qmax)
+    const float qmax = g.bits == 8 ? 127.0f : 7.0f;
+    const uint32_t cmask = (1u << g.bits) - 1u;
     const int gi = tid >> 1, half = tid & 1;
     float am = 0.0f;
     for (int j = 0; j < 64; ++j) am = fmaxf(am, fabsf(sm->x[gi * XS + half * 64 + j]));
-    am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
-    if (half == 0) {
-      float s32 = fminf(__fdiv_rn(am, 7.0f), 65504.0f);
+    if (!g.g64) am = fmaxf(am, __shfl_xor_sync(0xffffffffu, am, 1));
+    if (g.g64 || half == 0) {
+      float s32 = fminf(__fdiv_rn(am, qmax), 65504.0f);
       uint16_t s16 = f2h_rn(s32);
-      sm->gs[gi] = h2f(s16);
-      m16[gi] = s16;
+      (half ? sm->gz : sm->gs)[gi] = h2f(s16);  // g64: channels 64..127 in gz
+      m16[half * T + gi] = s16;
     }
     __syncthreads();
     for (int e = tid; e < TILE; e += AP_THREADS) {
       int t = e >> 7, c = e & 127;
-      float sf = sm->gs[t];
+      float sf = (g.g64 && c >= 64) ? sm->gz[t] : sm->gs[t];
       int q = 0;
       if (sf != 0.0f) {
         float qf = rintf(__fdiv_rn(sm->x[t * XS + c], sf));
-        q = (int)fminf(fmaxf(qf, -8.0f), 7.0f);
+        q = (int)fminf(fmaxf(qf, -qmax - 1.0f), qmax);
       }
-      sm->codes[e] = (uint8_t)(q & 0xF);
+      sm->codes[e] = (uint8_t)((uint32_t)q & cmask);
     }
     __syncthreads();
   } else {  // KVQ_NUQ

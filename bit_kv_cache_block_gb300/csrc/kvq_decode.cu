@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
         if (g.planes3) {
           c0 = tile3_code(kc, 0, t, c);
           c1 = tile3_code(kc, 0, t, c + 1);
-        } else {  // n = floor(32/bits) (16, 10, 8) is even: a channel pair never straddles two words
+        } else {  // n = floor(32/bits) (16, 10, 8, 4) is even: a channel pair never straddles two words
           const int w = c / nw, j = c - w * nw;
           const uint32_t word = kc[t * W + w];
           c0 = (word >> (bits * j)) & cmask;
@@ -189,9 +189,14 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
         if (METHOD == KVQ_RTN || METHOD == KVQ_VARN) {
           k0 = ((float)c0 + h2f(km[T + c])) * h2f(km[c]);
           k1 = ((float)c1 + h2f(km[T + c + 1])) * h2f(km[c + 1]);
-        } else if (METHOD == KVQ_INT4) {
-          k0 = (float)((int)(c0 << 28) >> 28);
-          k1 = (float)((int)(c1 << 28) >> 28);
+        } else if (METHOD == KVQ_INT4) {  // b-bit two's complement; per-half scales applied here
+          k0 = (float)((int)(c0 << (32 - bits)) >> (32 - bits));
+          k1 = (float)((int)(c1 << (32 - bits)) >> (32 - bits));
+          if (g.g64) {
+            const float sc = h2f(km[(c >> 6) * T + t]);
+            k0 *= sc;
+            k1 *= sc;
+          }
         } else {
           k0 = sm->cb[c0] * h2f(km[c]) + h2f(km[T + c]);
           k1 = sm->cb[c1] * h2f(km[c + 1]) + h2f(km[T + c + 1]);
@@ -234,7 +239,7 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
       }
     }
     float tscale = LOG2E_RSQRT_D;
-    if (METHOD == KVQ_INT4) tscale *= h2f(km[t]);
+    if (METHOD == KVQ_INT4 && !g.g64) tscale *= h2f(km[t]);
     if (METHOD == KVQ_VARN) tscale *= h2f(km[2 * T + t]);
 
     // ---------------- online softmax (base 2)
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
         for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
         if (lane == 0) sm->red[1][k][warp] = ps;
         float vs = 1.0f;
-        if (METHOD != KVQ_NUQ) vs = h2f(vm[t]);  // per-token value scale folded into p
+        if (METHOD != KVQ_NUQ && !(METHOD == KVQ_INT4 && g.g64)) vs = h2f(vm[t]);  // per-token value scale folded into p
         sm->pv[k][t] = p * vs;
       } else {
         alpha[k] = 1.0f;
@@ -320,7 +325,8 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
         if (METHOD == KVQ_RTN || METHOD == KVQ_VARN) {
           val = (float)code + h2f(vm[T + tt]);
         } else if (METHOD == KVQ_INT4) {
-          val = (float)((int)(code << 28) >> 28);
+          val = (float)((int)(code << (32 - bits)) >> (32 - bits));
+          if (g.g64) val *= h2f(vm[(c >> 6) * T + tt]);
         } else {
           val = sm->cb[code] * h2f(vm[tt]) + h2f(vm[T + tt]);
         }

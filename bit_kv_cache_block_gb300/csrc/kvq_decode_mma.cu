@@ -652,6 +652,7 @@ bool supported(const Geo& g) {
   if (g.layout != KVQ_LAYOUT_MMA) return false;  // value tiles must hold one row per channel
   if (g.G > GQ) return false;
   if (g.bits != 2 && g.bits != 4) return false;
+  if (g.g64) return false;  // one scale per token is folded into the score and probability columns
   return g.method == KVQ_RTN || g.method == KVQ_VARN || g.method == KVQ_INT4;
 }
 

@@ -37,8 +37,8 @@ __device__ void dequant_row(const Geo& g, const uint8_t* rec, const float* codeb
       const int gi = kind == 0 ? c : t;
       v = ((float)q + h2f(m[T + gi])) * h2f(m[gi]);
       if (g.method == KVQ_VARN) v *= h2f(m[2 * T + (kind == 0 ? t : c)]);
-    } else if (g.method == KVQ_INT4) {
-      v = (float)((int)(q << 28) >> 28) * h2f(m[t]);
+    } else if (g.method == KVQ_INT4) {  // b-bit two's complement times the scale of (t, c's group)
+      v = (float)((int)(q << (32 - bits)) >> (32 - bits)) * h2f(m[(g.g64 && c >= 64 ? T : 0) + t]);
     } else {
       const int gi = kind == 0 ? c : t;
       v = codebook[h * (1 << bits) + q] * h2f(m[gi]) + h2f(m[T + gi]);

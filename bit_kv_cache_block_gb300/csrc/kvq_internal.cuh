@@ -71,12 +71,12 @@ __device__ __forceinline__ uint32_t tile3_code(const uint32_t* w, int kind, int 
 __host__ __device__ constexpr uint64_t round16(uint64_t x) { return (x + 15) & ~uint64_t(15); }
 
 // Number of fp16 vectors of 128 in a tile's metadata region.
-__host__ __device__ inline int meta_vectors(int method) {
+__host__ __device__ inline int meta_vectors(int method, int scale_group) {
   switch (method) {
     case KVQ_RTN: return 2;    // s, z
     case KVQ_NUQ: return 2;    // s, zp
     case KVQ_VARN: return 3;   // s, z, s1
-    default: return 1;         // INT4: s
+    default: return scale_group == 64 ? 2 : 1;  // INT4: s per token (or per half-token)
   }
 }
 
@@ -109,6 +109,7 @@ struct Geo {
   int key_calib;        // NUQ keys use the calibration table at calib_off
   int sink;             // NUQ: the first token of each sequence is kept at sink_off
   uint64_t calib_off, sink_off;
+  int g64;              // INT4: one scale per 64 channels (meta vectors: channels 0..63, 64..127)
 };
 
 inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
@@ -131,6 +132,7 @@ inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
   g.sink = c.sink;
   g.calib_off = l.calib_off;
   g.sink_off = l.sink_off;
+  g.g64 = c.method == KVQ_INT4 && c.scale_group == 64;
   return g;
 }
 

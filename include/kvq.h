@@ -44,7 +44,7 @@ extern "C" {
 typedef enum {
   KVQ_OK = 0,
   KVQ_ERR_INVALID_ARG = 1,   /* a NULL pointer, a size out of range, an inconsistent config */
-  KVQ_ERR_UNSUPPORTED = 2,   /* a valid but unimplemented combination (e.g. INT4 with bits != 4) */
+  KVQ_ERR_UNSUPPORTED = 2,   /* a valid but unimplemented combination (e.g. INT4 with bits 2) */
   KVQ_ERR_CAPACITY = 3,      /* an append past cfg.max_blocks, or a buffer smaller than needed */
   KVQ_ERR_ALIGNMENT = 4,     /* a pointer that breaks the alignment rules above */
   KVQ_ERR_CUDA = 5,          /* a CUDA runtime error (launch failure, no device) */
@@ -66,9 +66,11 @@ typedef enum {
                     (keys per channel, values per token) and a second fp16 scale s1 (keys: per
                     token, values: per channel); x_dq = (q + z) * s * s1 ([KVN] method steps 1-5).
                     bits 2..4. */
-  KVQ_INT4 = 3   /* TurboQuant-style symmetric int4 absmax: one fp16 scale per token's 128
-                    channels, q = clamp(rne(x/s), -8, 7) stored as two's complement nibbles
-                    ([TQ] §2.1, §4.2). bits must be 4. */
+  KVQ_INT4 = 3   /* TurboQuant-style symmetric absmax integers: one fp16 scale s = absmax/(2^(b-1)-1)
+                    per block of scale_group contiguous channels of a token (128: the whole head
+                    vector; 64: two blocks per token), q = clamp(rne(x/s), -2^(b-1), 2^(b-1)-1)
+                    stored as b-bit two's complement ([TQ] §2.1, §4.2). bits 4 (int4 nibbles)
+                    or 8 (the 8-bit precision [TQ] §5.1 keeps for sensitive layers). */
 } kvq_method;
 
 typedef enum { KVQ_F16 = 0, KVQ_BF16 = 1 } kvq_dtype;
@@ -85,7 +87,7 @@ typedef enum { KVQ_LAYOUT_ROWS = 0, KVQ_LAYOUT_MMA = 1 } kvq_code_layout;
 /* Cache configuration. All fields are read by kvq_layout / kvq_cache_init. */
 typedef struct {
   int32_t method;        /* kvq_method */
-  int32_t bits;          /* code width: 2, 3 or 4 (INT4: 4) */
+  int32_t bits;          /* code width: 2, 3 or 4 (INT4: 4 or 8) */
   int32_t batch;         /* B >= 1 */
   int32_t n_kv_heads;    /* H_kv >= 1 */
   int32_t n_q_heads;     /* H_q, a multiple of H_kv, H_q / H_kv <= KVQ_MAX_GROUP */
@@ -116,6 +118,9 @@ typedef struct {
   int32_t sink;          /* NUQ only. 1: the first token of every sequence is kept in the input
                             precision ([KVQ] §3.5 attention sink): block 0's tiles hold zeros in
                             its place and decode attends the kept K and V rows at position 0. */
+  int32_t scale_group;   /* INT4 only: channels per absmax scale, 128 (also 0) or 64 ([TQ] §2.1:
+                            a smaller block doubles the scale overhead). Other methods: 0 or 128.
+                            Tiles with bits 8 or groups of 64 decode on the CUDA cores. */
 } kvq_config;
 
 /* Byte layout of a cache, from kvq_layout. One record per (b, h, block), at
@@ -139,7 +144,8 @@ typedef struct {
  *           words_per_row is 12 for 3-bit KVQ_LAYOUT_MMA caches (the tile holds 128 x 12 words).
  *   meta  : fp16 vectors of 128. RTN and VARN: s, z (keys: per channel; values: per token),
  *           VARN adds s1 (keys: per token; values: per channel). NUQ: s (half-range),
- *           zp (centre). INT4: s (per token).
+ *           zp (centre). INT4: s (per token); with scale_group 64 two vectors, the scales
+ *           of channels 0..63 of every token, then those of channels 64..127.
  *   csr   : NUQ only: val fp16[n_outliers], row_ptr uint16[129] (row = token),
  *           col uint8[n_outliers] (channel), zero padded.
  * After the records, for pre-RoPE caches: a table of (cos, sin) fp32 pairs of

@@ -20,7 +20,7 @@ def cfg_for(w: WL.Workload, max_blocks=None, batch=None, layout="rows"):
     return K.make_config(w.method, w.bits, batch or w.batch, w.n_kv_heads, w.n_q_heads,
                          max_blocks or w.n_blocks, in_dtype=w.dtype, pre_rope=w.pre_rope,
                          rope_theta=w.rope_theta, outlier_frac=w.outlier_frac, varn_iters=w.varn_iters,
-                         hadamard=True, layout=layout)
+                         hadamard=True, layout=layout, scale_group=w.scale_group)
 
 
 def oracle_layout(layout: str) -> int:
@@ -62,6 +62,8 @@ def tile_fields(rec: np.ndarray, lay, kind: int, method: str, bits: int, layout:
     out = dict(words=words if (bits == 3 and layout == "mma") else words.reshape(T, W))
     meta = rec[mo:mo + mb].view(np.uint16).reshape(-1, T)
     out["s16"] = meta[0].view(np.float16).copy()
+    if method == "int4" and meta.shape[0] == 2:  # one scale per 64 channels: [2][128]
+        out["s16"] = meta.view(np.float16).copy()
     if method in ("rtn", "varn"):
         out["z16"] = meta[1].view(np.float16).copy()
     if method == "varn":

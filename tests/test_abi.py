@@ -56,6 +56,7 @@ int main(void) {
          offsetof(kvq_cache, block_table));
   printf("%zu %zu %zu %zu %zu\n", offsetof(kvq_config, key_calib), offsetof(kvq_config, sink),
          offsetof(kvq_layout_t, calib_off), offsetof(kvq_layout_t, sink_bytes), offsetof(kvq_cache, calibrated));
+  printf("%zu\n", offsetof(kvq_config, scale_group));
   return 0;
 }
 ''')
@@ -70,7 +71,7 @@ int main(void) {
           L.kvq_cache.n_blocks.offset, L.kvq_cache.device.offset, L.kvq_config.layout.offset,
           L.kvq_config.n_pages.offset, L.kvq_cache.block_table.offset, L.kvq_config.key_calib.offset,
           L.kvq_config.sink.offset, L.kvq_layout_t.calib_off.offset, L.kvq_layout_t.sink_bytes.offset,
-          L.kvq_cache.calibrated.offset]
+          L.kvq_cache.calibrated.offset, L.kvq_config.scale_group.offset]
     assert vals == py
 
 
@@ -133,7 +134,7 @@ def test_config_checks(K):
         with pytest.raises(K.KVQError):
             K.kvq_layout(cfg)
     cfg = _cfg(K, 4)
-    cfg.bits = 3                      # int4 is 4-bit only
+    cfg.bits = 3                      # absmax is 4- or 8-bit only
     with pytest.raises(K.KVQError) as e:
         K.kvq_layout(cfg)
     assert e.value.status == L.KVQ_ERR_UNSUPPORTED
@@ -253,6 +254,33 @@ def test_paged_layout_and_checks(K):
     assert lib.kvq_decode_attn(C.byref(cache), q, None, None, 0, o, ws, 1 << 24, None) == L.KVQ_ERR_INVALID_ARG
     assert lib.kvq_decode_attn_static(C.byref(cache), q, None, None, 0, o, None) == L.KVQ_ERR_INVALID_ARG
     assert lib.kvq_dequant(C.byref(cache), 0, 1, 0, o, None, None) == L.KVQ_ERR_INVALID_ARG
+
+
+def test_absmax_variants_layout_and_checks(K):
+    """8-bit absmax tiles hold 4 codes per word (32 words per row) and one fp16 scale per token;
+    64-channel blocks double the scales. Both are INT4-only; other bit widths are refused."""
+    L = K._lib
+    mk = lambda **kw: K.make_config("int4", kw.pop("bits", 4), 2, 3, 6, 5, **kw)
+    for layout in ("rows", "mma"):
+        for bits in (4, 8):
+            for sg in (128, 64):
+                lay = K.kvq_layout(mk(bits=bits, scale_group=sg, layout=layout))
+                W = 128 // (32 // bits)
+                assert lay.words_per_row == W and lay.codes_bytes[0] == 128 * W * 4
+                assert lay.meta_bytes[0] == lay.meta_bytes[1] == (128 // sg) * 256
+                assert lay.record_bytes == 2 * (128 * W * 4 + (128 // sg) * 256)
+                assert K.kvq_decode_bytes(mk(bits=bits, scale_group=sg, layout=layout), 3) == 2 * 3 * 3 * lay.record_bytes
+    assert K.kvq_layout(mk(scale_group=0)).meta_bytes[0] == 256
+    for bad in (dict(bits=2), dict(bits=3), dict(bits=6), dict(bits=16)):
+        with pytest.raises(K.KVQError):
+            K.kvq_layout(mk(**bad))
+    with pytest.raises(K.KVQError):
+        K.kvq_layout(mk(scale_group=32))
+    for m in ("rtn", "nuq", "varn"):
+        with pytest.raises(K.KVQError):
+            K.kvq_layout(K.make_config(m, 8, 1, 1, 1, 2))
+        with pytest.raises(K.KVQError):
+            K.kvq_layout(K.make_config(m, 2, 1, 1, 1, 2, scale_group=64))
 
 
 def test_calibrated_keys_and_sink_layout_and_checks(K):

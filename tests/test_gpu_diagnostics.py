@@ -40,6 +40,7 @@ CASES = [
     ("nuq3_rows", 2, dict(batch=2, n_kv_heads=2, n_q_heads=2, ctx=2 * 128), "rows", {}),
     ("nuq3_calib_sink", 2, dict(batch=2, n_kv_heads=2, n_q_heads=2, ctx=3 * 128), "mma",
      dict(key_calib=True, sink=True)),
+    ("int8_g64_rows", 4, dict(bits=8, scale_group=64, batch=1, n_kv_heads=2, n_q_heads=2, ctx=2 * 128), "rows", {}),
 ]
 
 
@@ -49,7 +50,8 @@ def _build(w, layout, key_calib=False, sink=False):
     cb = U.codebook_for(w)
     cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, w.n_blocks, in_dtype=w.dtype,
                         pre_rope=w.pre_rope, rope_theta=w.rope_theta, outlier_frac=w.outlier_frac,
-                        varn_iters=w.varn_iters, hadamard=True, layout=layout, key_calib=key_calib, sink=sink)
+                        varn_iters=w.varn_iters, hadamard=True, layout=layout, key_calib=key_calib, sink=sink,
+                        scale_group=w.scale_group)
     cache = K.KVCache(cfg, None if cb is None else torch.from_numpy(cb))
     if key_calib:
         kc = np.stack([np.concatenate([WL.tile(w, 0, h, blk, WL.KIND_K, seed=99) for blk in range(3)])

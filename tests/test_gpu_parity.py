@@ -72,6 +72,10 @@ CASES_EXACT = [
     ("nuq3_gqa_norope", WL.WORKLOADS[2], dict(pre_rope=False, batch=2, n_kv_heads=2, n_q_heads=4, ctx=2 * 128)),
     ("nuq2_5pct", WL.WORKLOADS[2], dict(bits=2, outlier_frac=0.05, batch=1, n_kv_heads=1, n_q_heads=1, ctx=2 * 128)),
     ("nuq4_nooutl", WL.WORKLOADS[2], dict(bits=4, outlier_frac=0.0, batch=1, n_kv_heads=2, n_q_heads=2, ctx=2 * 128)),
+    ("int8_bf16", WL.WORKLOADS[4], dict(bits=8, batch=2, n_kv_heads=2, n_q_heads=8, ctx=3 * 128)),
+    ("int8_f16_g64", WL.WORKLOADS[4], dict(bits=8, scale_group=64, dtype="f16", batch=1, n_kv_heads=2, n_q_heads=2,
+                                           ctx=2 * 128)),
+    ("int4_g64", WL.WORKLOADS[4], dict(scale_group=64, batch=2, n_kv_heads=1, n_q_heads=4, ctx=2 * 128)),
 ]
 
 
@@ -194,6 +198,10 @@ DECODE_CASES = [
     ("nuq3_norope_gqa", WL.WORKLOADS[2], dict(pre_rope=False, batch=2, n_kv_heads=2, n_q_heads=4, ctx=3 * 128), [9]),
     ("varn2_gqa", WL.WORKLOADS[3], dict(batch=2, n_kv_heads=2, n_q_heads=8, ctx=4 * 128), [0, 100]),
     ("varn2_g16", WL.WORKLOADS[3], dict(batch=1, n_kv_heads=1, n_q_heads=16, ctx=2 * 128), [1]),
+    ("int8_bf16", WL.WORKLOADS[4], dict(bits=8, batch=2, n_kv_heads=2, n_q_heads=8, ctx=5 * 128), [0, 64]),
+    ("int8_g64_f16", WL.WORKLOADS[4], dict(bits=8, scale_group=64, dtype="f16", batch=1, n_kv_heads=3, n_q_heads=3,
+                                           ctx=4 * 128), [127]),
+    ("int4_g64_bf16", WL.WORKLOADS[4], dict(scale_group=64, batch=2, n_kv_heads=2, n_q_heads=4, ctx=3 * 128), [5]),
 ]
 
 
@@ -233,8 +241,9 @@ def test_decode_tail_only(method):
 
 
 @pytest.mark.parametrize("layout", ["rows", "mma"])
-@pytest.mark.parametrize("name,base,kw", CASES_EXACT[1:8:2] + [("varn", WL.WORKLOADS[3], dict(batch=1, n_kv_heads=2, n_q_heads=2, ctx=2 * 128))],
-                         ids=[c[0] for c in CASES_EXACT[1:8:2]] + ["varn"])
+@pytest.mark.parametrize("name,base,kw", CASES_EXACT[1:8:2] + CASES_EXACT[11:12] +
+                         [("varn", WL.WORKLOADS[3], dict(batch=1, n_kv_heads=2, n_q_heads=2, ctx=2 * 128))],
+                         ids=[c[0] for c in CASES_EXACT[1:8:2] + CASES_EXACT[11:12]] + ["varn"])
 def test_dequant_parity(name, base, kw, layout):
     w = base.scaled(**kw)
     nb = w.n_blocks
@@ -278,7 +287,8 @@ def test_capacity_and_truncate():
 
 
 DETERMINISM_CASES = [c for c in DECODE_CASES if c[0] in ("rtn2_mha", "rtn3_gqa", "int4_bf16", "nuq3_rope",
-                                                         "nuq3_rope_5pct", "nuq3_norope_gqa", "varn2_gqa")]
+                                                         "nuq3_rope_5pct", "nuq3_norope_gqa", "varn2_gqa",
+                                                         "int8_g64_f16")]
 
 
 @pytest.mark.parametrize("layout", ["rows", "mma"])
