@@ -627,7 +627,8 @@ def _decode_kernel_name(w):
     """The decode kernel the library picks for this workload (mirrors its dispatch rules)."""
     if w.method == "nuq" and w.bits == 3 and w.group == 1 and w.pre_rope:
         return "decode_nuq_kernel"
-    if w.method in ("rtn", "varn", "int4") and w.bits in (2, 4) and w.group <= 4 and w.scale_group == 128:
+    if (w.method in ("rtn", "varn", "int4") and (w.bits in (2, 4) or (w.method, w.bits) == ("int4", 8))
+            and w.group <= 4 and w.scale_group == 128):
         return "decode_mma_kernel"
     return "decode_kernel"
 

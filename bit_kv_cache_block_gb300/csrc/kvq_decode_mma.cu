@@ -1,5 +1,5 @@
 // Decode attention over the packed cache on the tensor cores (linear codes: RTN, KVarN, int4;
-// 2- and 4-bit codes; up to 4 query heads per KV head).
+// 2- and 4-bit codes, and 8-bit absmax codes; up to 4 query heads per KV head).
 //
 // Work split. The (b, h, block) sequence of the whole batch is cut into one contiguous range
 // per resident warp (persistent: one wave, equal ranges). A warp streams its blocks through
@@ -16,7 +16,9 @@
 // code at bits [2p, 2p+1] of a 16-bit half becomes the exact value code * 4^p * 2^-24 (p <= 4;
 // the upper positions are shifted down first), a 4-bit code code * 16^p * 2^-24; int4 codes
 // are biased by 8 with one xor. One LOP3 yields two operands, about half an instruction per
-// element. The power of two of each position is divided out of the matching B entry.
+// element. The power of two of each position is divided out of the matching B entry. 8-bit
+// codes take one byte per half (code * 2^-24, biased by 128 with one xor), two operands per
+// word.
 // B columns are (query head, hi/lo): the per-channel key scales (RTN/KVarN, [KVN]
 // preliminaries (K_q + z) * s) are folded into q, and the per-token value scales into the
 // probabilities, each split into a high and a low fp16 half so the products keep about 22
@@ -65,6 +67,11 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 // as fp16 subnormals.
 template <int BITS, bool BIAS8>
 __device__ __forceinline__ uint32_t operand(uint32_t w, int qr) {
+  if (BITS == 8) {  // bytes 0, 2 (qr 0) or 1, 3 (qr 1); two's complement -> offset binary
+    uint32_t v = (qr ? (w >> 8) : w) & 0x00ff00ffu;
+    if (BIAS8) v ^= 0x00800080u;
+    return v;
+  }
   if (BITS == 2) {
     return qr <= 4 ? (w & (0x00030003u << (2 * qr))) : ((w >> 10) & (0x00030003u << (2 * (qr - 5))));
   } else {
@@ -146,7 +153,29 @@ __host__ __device__ inline long long range_of(long long x, long long total, long
 template <int BITS, bool BIAS8>
 __device__ __forceinline__ void tile_mma(float (&acc)[8][4], const uint32_t* codes, int gq, int tq,
                                          const uint32_t (&b)[16]) {
-  if (BITS == 2) {
+  if (BITS == 8) {  // rows of 32 words; lane tq feeds k-step ks from word 8*tq + ks of its rows
+#pragma unroll
+    for (int hm = 0; hm < 4; ++hm) {  // 2 m-tiles at a time
+      uint4 w0[2][2], w1[2][2];
+#pragma unroll
+      for (int m = 0; m < 2; ++m) {
+        const int mt = 2 * hm + m;
+        const uint4* r0 = reinterpret_cast<const uint4*>(codes + (16 * mt + gq) * 32 + 8 * tq);
+        const uint4* r1 = reinterpret_cast<const uint4*>(codes + (16 * mt + gq + 8) * 32 + 8 * tq);
+        w0[m][0] = r0[0]; w0[m][1] = r0[1];
+        w1[m][0] = r1[0]; w1[m][1] = r1[1];
+      }
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          const uint32_t x0 = (&w0[m][ks >> 2].x)[ks & 3], x1 = (&w1[m][ks >> 2].x)[ks & 3];
+          mma16816(acc[2 * hm + m], operand<8, BIAS8>(x0, 0), operand<8, BIAS8>(x1, 0), operand<8, BIAS8>(x0, 1),
+                   operand<8, BIAS8>(x1, 1), b[2 * ks], b[2 * ks + 1]);
+        }
+      }
+    }
+  } else if (BITS == 2) {
     uint2 w0[8], w1[8];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
@@ -198,10 +227,13 @@ __device__ __forceinline__ void put_col(uint32_t* frag, int col, int off, __half
 // operand() and the fragment layout).
 template <int BITS>
 __device__ __forceinline__ int col_off(int mt, int gq, int hlf) {
+  if (BITS == 8)  // code x = 16mt + gq + 8hlf: word x/4 (lane x/32, k-step (x/4)%8), byte x%4
+    return 16 * mt + 8 * hlf + 4 * (gq >> 2) + 2 * (gq & 1) + ((gq >> 1) & 1);
   return BITS == 2 ? 16 * mt + 2 * gq + hlf : 16 * mt + 8 * hlf + 2 * (gq & 3) + (gq >> 2);
 }
 template <int BITS>
 __device__ __forceinline__ float lane_inv_f(int gq) {
+  if (BITS == 8) return 1.0f;  // every byte operand is code * 2^-24
   if (BITS == 2) {
     const int e = gq <= 4 ? 2 * gq : 2 * (gq - 5);
     return __int_as_float((127 - e) << 23);
@@ -245,7 +277,7 @@ __device__ __forceinline__ void stage_cols(uint32_t* frag, int h, int gq, int rh
       *reinterpret_cast<__half2*>(col_hi + o) = __halves2half2(h0, h1);
       *reinterpret_cast<__half2*>(col_lo + o) = __halves2half2(l0, l1);
     } else {
-      const int o0 = col_off<4>(mt, gq, 0), o1 = col_off<4>(mt, gq, 1);
+      const int o0 = col_off<BITS>(mt, gq, 0), o1 = col_off<BITS>(mt, gq, 1);
       col_hi[o0] = h0; col_lo[o0] = l0;
       col_hi[o1] = h1; col_lo[o1] = l1;
     }
@@ -282,7 +314,8 @@ __device__ __forceinline__ void load_frag(const uint32_t* frag, int lane, int G,
 // or the V tile of a block, with its metadata): the ring streams K(0), V(0), K(1), V(1), ...
 template <int METHOD, int BITS, int GT, int NW, int NB, bool WHOLE>
 __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
-  constexpr bool BIAS8 = METHOD == KVQ_INT4;
+  constexpr bool BIAS8 = METHOD == KVQ_INT4;          // signed codes enter biased by 8 (or 128)
+  constexpr float BIASF = BITS == 8 ? 128.0f : 8.0f;
   constexpr int RP = 4 / GT;
   constexpr int NMT = 8 / RP;  // m-tiles (16 rows) a lane finishes
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -501,7 +534,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
       for (int hf = 0; hf < 2; ++hf) {
         const int tok = 16 * mt + gq + 8 * hf;
         float v = (c4[2 * hf] + c4[2 * hf + 1]) * ksc;
-        if (METHOD == KVQ_INT4) v = (v - 8.0f * sumq) * h2f(km[tok]);
+        if (METHOD == KVQ_INT4) v = (v - BIASF * sumq) * h2f(km[tok]);
         else v += zk;
         if (METHOD == KVQ_VARN) v *= h2f(km[2 * T + tok]);
         v *= LOG2E_RSQRT_D;
@@ -539,7 +572,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
         lsum += p;
         const float pp = p * h2f(vm[tok]);  // per-token value scale folded into p
         sv[2 * j + hf] = pp;
-        if (METHOD == KVQ_INT4) zsum_blk -= 8.0f * pp;
+        if (METHOD == KVQ_INT4) zsum_blk -= BIASF * pp;
         else zsum_blk = fmaf(pp, h2f(vm[T + tok]), zsum_blk);
         pmax = fmaxf(pmax, pp);
       }
@@ -634,10 +667,18 @@ struct Plan {
 #define KVQ_MMA4_WHOLE 0
 #endif
 
+#ifndef KVQ_MMA8_NW
+#define KVQ_MMA8_NW 4
+#endif
+#ifndef KVQ_MMA8_NB
+#define KVQ_MMA8_NB 2
+#endif
+
 template <int METHOD, int BITS, int GT>
 Plan plan_for() {
-  constexpr int NW = BITS == 2 ? KVQ_MMA2_NW : KVQ_MMA4_NW, NB = BITS == 2 ? KVQ_MMA2_NB : KVQ_MMA4_NB;
-  constexpr bool WH = BITS == 2 ? KVQ_MMA2_WHOLE : KVQ_MMA4_WHOLE;
+  constexpr int NW = BITS == 2 ? KVQ_MMA2_NW : BITS == 4 ? KVQ_MMA4_NW : KVQ_MMA8_NW;
+  constexpr int NB = BITS == 2 ? KVQ_MMA2_NB : BITS == 4 ? KVQ_MMA4_NB : KVQ_MMA8_NB;
+  constexpr bool WH = BITS == 2 ? KVQ_MMA2_WHOLE : BITS == 4 ? KVQ_MMA4_WHOLE : false;
   return Plan{decode_mma_kernel<METHOD, BITS, GT, NW, NB, WH>, NW, NB, WH};
 }
 
@@ -651,7 +692,7 @@ Plan plan_g(int G) {
 bool supported(const Geo& g) {
   if (g.layout != KVQ_LAYOUT_MMA) return false;  // value tiles must hold one row per channel
   if (g.G > GQ) return false;
-  if (g.bits != 2 && g.bits != 4) return false;
+  if (g.bits != 2 && g.bits != 4 && !(g.bits == 8 && g.method == KVQ_INT4)) return false;
   if (g.g64) return false;  // one scale per token is folded into the score and probability columns
   return g.method == KVQ_RTN || g.method == KVQ_VARN || g.method == KVQ_INT4;
 }
@@ -659,7 +700,7 @@ bool supported(const Geo& g) {
 Plan get_plan(const Geo& g) {
   if (g.method == KVQ_RTN) return g.bits == 2 ? plan_g<KVQ_RTN, 2>(g.G) : plan_g<KVQ_RTN, 4>(g.G);
   if (g.method == KVQ_VARN) return g.bits == 2 ? plan_g<KVQ_VARN, 2>(g.G) : plan_g<KVQ_VARN, 4>(g.G);
-  return plan_g<KVQ_INT4, 4>(g.G);
+  return g.bits == 8 ? plan_g<KVQ_INT4, 8>(g.G) : plan_g<KVQ_INT4, 4>(g.G);
 }
 
 size_t smem_bytes(const Geo& g, const Plan& p) {

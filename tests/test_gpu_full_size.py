@@ -24,7 +24,9 @@ N_TAIL = 77
 CHUNK = 512  # blocks per host->device copy of a sampled head
 
 SAMPLES = {1: [(0, 0)], 2: [(0, 0), (0, 13), (0, 31)], 3: [(0, 0), (3, 5), (7, 7)], 4: [(0, 0), (17, 3), (31, 7)],
-           5: [(0, 0), (0, 17)]}
+           5: [(0, 0), (0, 17)], "4-int8": [(0, 0), (31, 7)]}
+# the absmax workload with 8-bit codes (the sensitive-layer precision), same shapes
+VARIANTS = {"4-int8": (4, dict(bits=8))}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -46,16 +48,16 @@ def _head_tiles(w, b, h, first, n):
     return K, V
 
 
-@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5, "4-int8"])
 def test_full_size_sampled_heads(cfg):
     import torch
-    w = WL.WORKLOADS[cfg]
+    w = WL.WORKLOADS[VARIANTS[cfg][0]].scaled(**VARIANTS[cfg][1]) if cfg in VARIANTS else WL.WORKLOADS[cfg]
     nb, G = w.n_blocks, w.group
     dt = torch.float16 if w.dtype == "f16" else torch.bfloat16
     cache = U.new_cache(w, layout="mma")
     shape = (w.batch, w.n_kv_heads, nb * 128, 128)
     gen = torch.Generator(device="cuda")
-    gen.manual_seed(7919 * cfg)
+    gen.manual_seed(7919 * (cfg if isinstance(cfg, int) else 11))
     Kd = torch.randn(shape, generator=gen, device="cuda", dtype=dt)
     Vd = torch.randn(shape, generator=gen, device="cuda", dtype=dt)
     heads = {}

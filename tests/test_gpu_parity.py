@@ -288,7 +288,7 @@ def test_capacity_and_truncate():
 
 DETERMINISM_CASES = [c for c in DECODE_CASES if c[0] in ("rtn2_mha", "rtn3_gqa", "int4_bf16", "nuq3_rope",
                                                          "nuq3_rope_5pct", "nuq3_norope_gqa", "varn2_gqa",
-                                                         "int8_g64_f16")]
+                                                         "int8_g64_f16", "int8_bf16")]
 
 
 @pytest.mark.parametrize("layout", ["rows", "mma"])
