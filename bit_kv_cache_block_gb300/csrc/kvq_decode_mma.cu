@@ -150,12 +150,14 @@ __host__ __device__ inline long long range_of(long long x, long long total, long
 
 // acc[mt] += (rows 16mt+gq and 16mt+gq+8 of a 128-row code tile) . B, for the 8 m-tiles of the
 // tile; the k-step loop is outermost so that consecutive MMAs use independent accumulators.
-template <int BITS, bool BIAS8>
+// Only m-tiles MT0 .. MT1-1 are computed (the halves of a tile whose rows carry two scale sets).
+template <int BITS, bool BIAS8, int MT0 = 0, int MT1 = 8>
 __device__ __forceinline__ void tile_mma(float (&acc)[8][4], const uint32_t* codes, int gq, int tq,
                                          const uint32_t (&b)[16]) {
   if (BITS == 8) {  // rows of 32 words; lane tq feeds k-step ks from word 8*tq + ks of its rows
 #pragma unroll
     for (int hm = 0; hm < 4; ++hm) {  // 2 m-tiles at a time
+      if (2 * hm < MT0 || 2 * hm >= MT1) continue;
       uint4 w0[2][2], w1[2][2];
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
@@ -179,6 +181,7 @@ __device__ __forceinline__ void tile_mma(float (&acc)[8][4], const uint32_t* cod
     uint2 w0[8], w1[8];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) {
+      if (mt < MT0 || mt >= MT1) continue;
       w0[mt] = *reinterpret_cast<const uint2*>(codes + (16 * mt + gq) * 8 + 2 * tq);
       w1[mt] = *reinterpret_cast<const uint2*>(codes + (16 * mt + gq + 8) * 8 + 2 * tq);
     }
@@ -187,6 +190,7 @@ __device__ __forceinline__ void tile_mma(float (&acc)[8][4], const uint32_t* cod
       const int qr = 2 * (ks & 3);
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
+        if (mt < MT0 || mt >= MT1) continue;
         const uint32_t x0 = ks < 4 ? w0[mt].x : w0[mt].y, x1 = ks < 4 ? w1[mt].x : w1[mt].y;
         mma16816(acc[mt], operand<2, BIAS8>(x0, qr), operand<2, BIAS8>(x1, qr), operand<2, BIAS8>(x0, qr + 1),
                  operand<2, BIAS8>(x1, qr + 1), b[2 * ks], b[2 * ks + 1]);
@@ -195,6 +199,7 @@ __device__ __forceinline__ void tile_mma(float (&acc)[8][4], const uint32_t* cod
   } else {
 #pragma unroll
     for (int hm = 0; hm < 2; ++hm) {  // 4 m-tiles at a time
+      if (4 * hm + 3 < MT0 || 4 * hm >= MT1) continue;
       uint4 w0[4], w1[4];
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
@@ -312,7 +317,10 @@ __device__ __forceinline__ void load_frag(const uint32_t* frag, int lane, int G,
 // real scores and finishes 16/RP of the block's tokens.
 // NW warps per CTA; NB shared-memory buffers per warp, each holding one half-record (the K tile
 // or the V tile of a block, with its metadata): the ring streams K(0), V(0), K(1), V(1), ...
-template <int METHOD, int BITS, int GT, int NW, int NB, bool WHOLE>
+// G64 (absmax only): every token has two scales, one per 64 channels. Scores run the key tile
+// twice, against q restricted to each half, and the value product runs m-tiles 0-3 (channels
+// 0..63) and 4-7 against probabilities scaled by the matching half's scales.
+template <int METHOD, int BITS, int GT, int NW, int NB, bool WHOLE, bool G64>
 __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
   constexpr bool BIAS8 = METHOD == KVQ_INT4;          // signed codes enter biased by 8 (or 128)
   constexpr float BIASF = BITS == 8 ? 128.0f : 8.0f;
@@ -392,11 +400,11 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
     for (int s = 0; s < NB; ++s) issue_next();
   }
 
-  float m_run = -INFINITY, l_run = 0.0f, zv = 0.0f;
+  float m_run = -INFINITY, l_run = 0.0f, zv = 0.0f, zv1 = 0.0f;
   float O[8][4];
   int g1_cur = 0;
-  uint32_t bk[16], bv[16];
-  float zk = 0.0f, sumq = 0.0f;
+  uint32_t bk[16], bv[16], bk1[16], bv1[16];  // bk1, bv1: second scale half (G64)
+  float zk = 0.0f, sumq = 0.0f, sumq1 = 0.0f;
   int g0_fixed = 0;
   long long cur_u = -1;
   bool ok = true;
@@ -408,9 +416,9 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
     if (rho == 0 && head_ok && slot >= 0 && slot < a.n_slots) {
       const uint64_t row = ((uint64_t)(b * g.Hq + h * G + hl)) * a.n_slots + slot;
       const float sc = (METHOD == KVQ_VARN) ? 1.0f : exp2i(24 - g1_cur);
-      const float add = (METHOD == KVQ_VARN) ? 0.0f : zv;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
+        const float add = (METHOD == KVQ_VARN) ? 0.0f : (G64 && mt >= 4) ? zv1 : zv;
         a.ws_o[row * D + 16 * mt + gq] = (O[mt][0] + O[mt][1]) * sc + add;
         a.ws_o[row * D + 16 * mt + gq + 8] = (O[mt][2] + O[mt][3]) * sc + add;
       }
@@ -451,30 +459,44 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
       m_run = -INFINITY;
       l_run = 0.0f;
       zv = 0.0f;
+      zv1 = 0.0f;
       g1_cur = 0;
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.0f;
-      if (METHOD == KVQ_INT4) {  // int4 keys carry no per-channel scale: B is fixed per (b, h)
-        float mx = 0.0f, sq = 0.0f;
-        float v[2 * NMT];
+      if (METHOD == KVQ_INT4) {  // absmax keys carry no per-channel scale: B is fixed per (b, h)
+        float mx = 0.0f, sq = 0.0f, sq1 = 0.0f;
+        float v[2 * NMT], v1[2 * NMT];
 #pragma unroll
         for (int j = 0; j < NMT; ++j)
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             const float qv = head_ok ? sw->q[hl][16 * (rho + RP * j) + gq + 8 * hf] : 0.0f;
-            v[2 * j + hf] = qv;
-            sq += qv;
+            const bool lo = !G64 || rho + RP * j < 4;  // channel < 64
+            v[2 * j + hf] = lo ? qv : 0.0f;
+            v1[2 * j + hf] = lo ? 0.0f : qv;
+            if (lo) sq += qv;
+            else sq1 += qv;
             mx = fmaxf(mx, fabsf(qv));
           }
         mx = warp_max_all(mx);
         sumq = head_sum<GT>(sq);
+        if (G64) sumq1 = head_sum<GT>(sq1);
         g0_fixed = range_exp(mx);
         const float sc = exp2i(g0_fixed) * inv_f;
 #pragma unroll
-        for (int k = 0; k < 2 * NMT; ++k) v[k] *= sc;
+        for (int k = 0; k < 2 * NMT; ++k) {
+          v[k] *= sc;
+          v1[k] *= sc;
+        }
         if (head_ok) stage_cols<BITS, NMT>(sw->frag, hl, gq, rho, RP, v);
         __syncwarp();
         load_frag(sw->frag, lane, G, bk);
+        if (G64) {
+          __syncwarp();
+          if (head_ok) stage_cols<BITS, NMT>(sw->frag, hl, gq, rho, RP, v1);
+          __syncwarp();
+          load_frag(sw->frag, lane, G, bk1);
+        }
       }
     }
 
@@ -520,6 +542,12 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) sc8[mt][0] = sc8[mt][1] = sc8[mt][2] = sc8[mt][3] = 0.0f;
     tile_mma<BITS, BIAS8>(sc8, kc, gq, tq, bk);
+    float sc8b[8][4];  // G64: the scores of channels 64..127
+    if (G64) {
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) sc8b[mt][0] = sc8b[mt][1] = sc8b[mt][2] = sc8b[mt][3] = 0.0f;
+      tile_mma<BITS, BIAS8>(sc8b, kc, gq, tq, bk1);
+    }
 
     // ---- finish the scores of the lane's tokens, online softmax (base 2)
     const float ksc = exp2i(24 - g0);
@@ -528,14 +556,19 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
 #pragma unroll
     for (int j = 0; j < NMT; ++j) {
       const int mt = rho + RP * j;
-      float c4[4];
+      float c4[4], d4[4];
       pick_tile<RP>(sc8, j, rho, c4);
+      if (G64) pick_tile<RP>(sc8b, j, rho, d4);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         const int tok = 16 * mt + gq + 8 * hf;
         float v = (c4[2 * hf] + c4[2 * hf + 1]) * ksc;
-        if (METHOD == KVQ_INT4) v = (v - BIASF * sumq) * h2f(km[tok]);
-        else v += zk;
+        if (METHOD == KVQ_INT4) {
+          v = (v - BIASF * sumq) * h2f(km[tok]);
+          if (G64) v += ((d4[2 * hf] + d4[2 * hf + 1]) * ksc - BIASF * sumq1) * h2f(km[T + tok]);
+        } else {
+          v += zk;
+        }
         if (METHOD == KVQ_VARN) v *= h2f(km[2 * T + tok]);
         v *= LOG2E_RSQRT_D;
         sv[2 * j + hf] = v;
@@ -561,7 +594,8 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
     mloc = head_max<GT>(mloc);
     const float m_new = fmaxf(m_run, mloc);
     const float alpha = exp2f(m_run - m_new);
-    float lsum = 0.0f, zsum_blk = 0.0f, pmax = 0.0f;
+    float lsum = 0.0f, zsum_blk = 0.0f, zsum1 = 0.0f, pmax = 0.0f;
+    float sv1[2 * NMT];  // G64: probabilities times the scales of channels 64..127
 #pragma unroll
     for (int j = 0; j < NMT; ++j) {
       const int mt = rho + RP * j;
@@ -575,10 +609,17 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
         if (METHOD == KVQ_INT4) zsum_blk -= BIASF * pp;
         else zsum_blk = fmaf(pp, h2f(vm[T + tok]), zsum_blk);
         pmax = fmaxf(pmax, pp);
+        if (G64) {
+          const float pp1 = p * h2f(vm[T + tok]);
+          sv1[2 * j + hf] = pp1;
+          zsum1 -= BIASF * pp1;
+          pmax = fmaxf(pmax, pp1);
+        }
       }
     }
     lsum = head_sum<GT>(lsum);
     zsum_blk = head_sum<GT>(zsum_blk);
+    if (G64) zsum1 = head_sum<GT>(zsum1);
     l_run = l_run * alpha + lsum;
     m_run = m_new;
     const int g1 = range_exp(warp_max_all(head_ok ? pmax : 0.0f));
@@ -592,6 +633,14 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
       if (head_ok) stage_cols<BITS, NMT>(sw->frag, hl, gq, rho, RP, sv);
       __syncwarp();
       load_frag(sw->frag, lane, G, bv);
+      if (G64) {
+#pragma unroll
+        for (int k = 0; k < 2 * NMT; ++k) sv1[k] *= sc;
+        __syncwarp();
+        if (head_ok) stage_cols<BITS, NMT>(sw->frag, hl, gq, rho, RP, sv1);
+        __syncwarp();
+        load_frag(sw->frag, lane, G, bv1);
+      }
     }
 
     // ---- outputs: O = V . Bp  (8 m-tiles of 16 channels x 8 k-steps of 16 tokens)
@@ -603,7 +652,13 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
       }
       zv = zv * alpha + zsum_blk;
       g1_cur = g1;
-      tile_mma<BITS, BIAS8>(O, vc, gq, tq, bv);
+      if (G64) {
+        zv1 = zv1 * alpha + zsum1;
+        tile_mma<BITS, BIAS8, 0, 4>(O, vc, gq, tq, bv);
+        tile_mma<BITS, BIAS8, 4, 8>(O, vc, gq, tq, bv1);
+      } else {
+        tile_mma<BITS, BIAS8>(O, vc, gq, tq, bv);
+      }
     } else {  // second scale s1 per channel: o_c += s1_c * (P.V_c + sum p' z)
       float acc[8][4];
 #pragma unroll
@@ -674,32 +729,32 @@ struct Plan {
 #define KVQ_MMA8_NB 2
 #endif
 
-template <int METHOD, int BITS, int GT>
+template <int METHOD, int BITS, int GT, bool G64>
 Plan plan_for() {
   constexpr int NW = BITS == 2 ? KVQ_MMA2_NW : BITS == 4 ? KVQ_MMA4_NW : KVQ_MMA8_NW;
   constexpr int NB = BITS == 2 ? KVQ_MMA2_NB : BITS == 4 ? KVQ_MMA4_NB : KVQ_MMA8_NB;
   constexpr bool WH = BITS == 2 ? KVQ_MMA2_WHOLE : BITS == 4 ? KVQ_MMA4_WHOLE : false;
-  return Plan{decode_mma_kernel<METHOD, BITS, GT, NW, NB, WH>, NW, NB, WH};
+  return Plan{decode_mma_kernel<METHOD, BITS, GT, NW, NB, WH, G64>, NW, NB, WH};
 }
 
-template <int METHOD, int BITS>
+template <int METHOD, int BITS, bool G64 = false>
 Plan plan_g(int G) {
-  if (G == 1) return plan_for<METHOD, BITS, 1>();
-  if (G == 2) return plan_for<METHOD, BITS, 2>();
-  return plan_for<METHOD, BITS, 4>();
+  if (G == 1) return plan_for<METHOD, BITS, 1, G64>();
+  if (G == 2) return plan_for<METHOD, BITS, 2, G64>();
+  return plan_for<METHOD, BITS, 4, G64>();
 }
 
 bool supported(const Geo& g) {
   if (g.layout != KVQ_LAYOUT_MMA) return false;  // value tiles must hold one row per channel
   if (g.G > GQ) return false;
   if (g.bits != 2 && g.bits != 4 && !(g.bits == 8 && g.method == KVQ_INT4)) return false;
-  if (g.g64) return false;  // one scale per token is folded into the score and probability columns
   return g.method == KVQ_RTN || g.method == KVQ_VARN || g.method == KVQ_INT4;
 }
 
 Plan get_plan(const Geo& g) {
   if (g.method == KVQ_RTN) return g.bits == 2 ? plan_g<KVQ_RTN, 2>(g.G) : plan_g<KVQ_RTN, 4>(g.G);
   if (g.method == KVQ_VARN) return g.bits == 2 ? plan_g<KVQ_VARN, 2>(g.G) : plan_g<KVQ_VARN, 4>(g.G);
+  if (g.g64) return g.bits == 8 ? plan_g<KVQ_INT4, 8, true>(g.G) : plan_g<KVQ_INT4, 4, true>(g.G);
   return g.bits == 8 ? plan_g<KVQ_INT4, 8>(g.G) : plan_g<KVQ_INT4, 4>(g.G);
 }
 
