@@ -86,6 +86,7 @@ struct DecSmem {
 
 template <int METHOD, int GMAX>
 __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
+  launch_dependents();  // the combine kernel may be scheduled once every CTA of this grid runs
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const Geo& g = a.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -411,84 +412,23 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
   const Geo& g = a.g;
   const int tid = threadIdx.x, c = tid & (D - 1), grp = tid >> 7;
   const int hq = blockIdx.x, b = blockIdx.y, h = hq / g.G;
-  const uint64_t row0 = ((uint64_t)b * g.Hq + hq) * a.n_split;
-  int n_part = a.n_split;
-  if (a.ranges > 0 && a.n_blocks > 0) {  // the ranges that hold blocks of this (b, h)
-    const long long u = (long long)b * g.H + h;
-    const long long r0 = ((u * a.n_blocks + 1) * a.ranges - 1) / a.total;
-    const long long r1 = (((u + 1) * a.n_blocks) * a.ranges - 1) / a.total;
-    n_part = (int)(r1 - r0 + 1) * a.per_range;
-    if (n_part > a.n_split) n_part = a.n_split;
-  }
 
-  // ---- merge the partials: max over all, then group grp sums partials grp, grp+4, ...
-  float mm = -INFINITY;
-  for (int s = tid; s < n_part; s += CB_THREADS) mm = fmaxf(mm, a.ws_m[row0 + s]);
-  const float M = cb_max(mm, red);
-  float Lg = 0.0f, Og = 0.0f;
-  {
-    // four partials of the group per iteration, their loads side by side (they sit in L2)
-    float Lp[4] = {0.0f, 0.0f, 0.0f, 0.0f}, Op[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    int s = grp;
-    for (; s + 3 * CB_GROUPS < n_part; s += 4 * CB_GROUPS) {
-      float mv[4], lv[4], ovv[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint64_t r = row0 + s + k * CB_GROUPS;
-        mv[k] = a.ws_m[r];
-        lv[k] = a.ws_l[r];
-        ovv[k] = a.ws_o[r * D + c];
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float f = exp2f(mv[k] - M);
-        Lp[k] = fmaf(lv[k], f, Lp[k]);
-        Op[k] = fmaf(ovv[k], f, Op[k]);
-      }
-    }
-    for (; s < n_part; s += CB_GROUPS) {
-      const uint64_t r = row0 + s;
-      const float f = exp2f(a.ws_m[r] - M);
-      Lp[0] = fmaf(a.ws_l[r], f, Lp[0]);
-      Op[0] = fmaf(a.ws_o[r * D + c], f, Op[0]);
-    }
-    Lp[0] += Lp[2];
-    Lp[1] += Lp[3];
-    Op[0] += Op[2];
-    Op[1] += Op[3];
-    Lg = Lp[0] + Lp[1];
-    Og = Op[0] + Op[1];
-  }
-  part[grp][c] = Og;
-  // L: the same value in every thread of a group; take channel 0 of each group
-  float L = cb_sum(c == 0 ? Lg : 0.0f, red);  // (also orders the part[] stores)
-  float O = (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
-  if (g.method == KVQ_VARN && a.hadamard && n_part > 0) {
-    __syncthreads();
-    if (grp == 0) ob[c] = O;
-    __syncthreads();
-    smem_fwht(ob, 1);
-    O = ob[c];
-  }
-
-  // ---- the kept first token of the sequence (attention sink, [KVQ] §3.5) at position 0, where
-  // RoPE is the identity: quantised token 0 was left out of the partials
-  float Mc = M;
+  // ---- first what reads only the call's inputs: the kept first token and the fp tail, as one
+  // softmax state (Mt, Lt, Ot). Launched as a programmatic dependent of the decode kernel, this
+  // part overlaps the decode's last blocks; the partials are read after the grid dependency.
+  float Mt = -INFINITY, Lt = 0.0f, Ot = 0.0f;
+  // the kept first token of the sequence (attention sink, [KVQ] §3.5) at position 0, where RoPE
+  // is the identity: quantised token 0 was left out of the partials
   if (g.sink && a.n_blocks > 0) {
     const uint16_t* ks = reinterpret_cast<const uint16_t*>(a.base + g.sink_off) + ((uint64_t)b * g.H + h) * 2 * D;
     const float qk = grp == 0 ? load_in(a.q + ((uint64_t)b * g.Hq + hq) * D + c, g.in_bf16) *
                                     in_bits_to_f32(ks[c], g.in_bf16)
                               : 0.0f;
-    const float ss = cb_sum(qk, red) * LOG2E_RSQRT_D;
-    const float m2 = fmaxf(Mc, ss), f = exp2f(Mc - m2), ps = exp2f(ss - m2);
-    L = L * f + ps;
-    O = O * f + ps * in_bits_to_f32(ks[D + c], g.in_bf16);
-    Mc = m2;
+    Mt = cb_sum(qk, red) * LOG2E_RSQRT_D;
+    Lt = 1.0f;
+    Ot = in_bits_to_f32(ks[D + c], g.in_bf16);
   }
-
-  // ---- the fp residual tail (< 128 tokens)
-  float Mn = Mc;
-  if (a.n_tail > 0) {
+  if (a.n_tail > 0) {  // the fp residual tail (< 128 tokens)
     const int nt = a.n_tail;
     const uint16_t* tk = a.tail_k + ((uint64_t)b * g.H + h) * nt * D;
     const uint16_t* tv = a.tail_v + ((uint64_t)b * g.H + h) * nt * D;
@@ -538,16 +478,16 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
     }
     __syncthreads();
     const float mt = cb_max(tid < nt ? sc[tid] : -INFINITY, red);
-    Mn = fmaxf(Mc, mt);
-    const float f = exp2f(Mc - Mn);
-    L *= f;
-    O *= f;
+    const float Mn = fmaxf(Mt, mt);
+    const float f = exp2f(Mt - Mn);  // 0 when there is no sink term
+    Lt *= f;
+    Ot *= f;
     float pl = 0.0f;
     if (tid < nt) {
       pl = exp2f(sc[tid] - Mn);
       sc[tid] = pl;
     }
-    L += cb_sum(pl, red);  // (also orders the sc[] stores)
+    Lt += cb_sum(pl, red);  // (also orders the sc[] stores)
     // values: group grp sums tokens grp, grp+4, ..., four of them per iteration with their
     // loads side by side
     float ov[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -563,8 +503,80 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
     __syncthreads();
     part[grp][c] = (ov[0] + ov[1]) + (ov[2] + ov[3]);
     __syncthreads();
-    O += (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
+    Ot += (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
+    Mt = Mn;
   }
+
+  grid_dependency_wait();  // the decode kernel's partials are complete and visible
+  if (a.n_blocks <= 0) {
+    if (grp == 0) a.out[((uint64_t)b * g.Hq + hq) * D + c] = Ot / Lt;
+    return;
+  }
+  const uint64_t row0 = ((uint64_t)b * g.Hq + hq) * a.n_split;
+  int n_part = a.n_split;
+  if (a.ranges > 0) {  // the ranges that hold blocks of this (b, h)
+    const long long u = (long long)b * g.H + h;
+    const long long r0 = ((u * a.n_blocks + 1) * a.ranges - 1) / a.total;
+    const long long r1 = (((u + 1) * a.n_blocks) * a.ranges - 1) / a.total;
+    n_part = (int)(r1 - r0 + 1) * a.per_range;
+    if (n_part > a.n_split) n_part = a.n_split;
+  }
+
+  // ---- merge the partials: max over all, then group grp sums partials grp, grp+4, ...
+  __syncthreads();  // part[] is reused below
+  float mm = -INFINITY;
+  for (int s = tid; s < n_part; s += CB_THREADS) mm = fmaxf(mm, a.ws_m[row0 + s]);
+  const float M = cb_max(mm, red);
+  float Lg = 0.0f, Og = 0.0f;
+  {
+    // four partials of the group per iteration, their loads side by side (they sit in L2)
+    float Lp[4] = {0.0f, 0.0f, 0.0f, 0.0f}, Op[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    int s = grp;
+    for (; s + 3 * CB_GROUPS < n_part; s += 4 * CB_GROUPS) {
+      float mv[4], lv[4], ovv[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint64_t r = row0 + s + k * CB_GROUPS;
+        mv[k] = a.ws_m[r];
+        lv[k] = a.ws_l[r];
+        ovv[k] = a.ws_o[r * D + c];
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float f = exp2f(mv[k] - M);
+        Lp[k] = fmaf(lv[k], f, Lp[k]);
+        Op[k] = fmaf(ovv[k], f, Op[k]);
+      }
+    }
+    for (; s < n_part; s += CB_GROUPS) {
+      const uint64_t r = row0 + s;
+      const float f = exp2f(a.ws_m[r] - M);
+      Lp[0] = fmaf(a.ws_l[r], f, Lp[0]);
+      Op[0] = fmaf(a.ws_o[r * D + c], f, Op[0]);
+    }
+    Lp[0] += Lp[2];
+    Lp[1] += Lp[3];
+    Op[0] += Op[2];
+    Op[1] += Op[3];
+    Lg = Lp[0] + Lp[1];
+    Og = Op[0] + Op[1];
+  }
+  part[grp][c] = Og;
+  // L: the same value in every thread of a group; take channel 0 of each group
+  float L = cb_sum(c == 0 ? Lg : 0.0f, red);  // (also orders the part[] stores)
+  float O = (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
+  if (g.method == KVQ_VARN && a.hadamard && n_part > 0) {
+    __syncthreads();
+    if (grp == 0) ob[c] = O;
+    __syncthreads();
+    smem_fwht(ob, 1);
+    O = ob[c];
+  }
+  // ---- the cached part and the sink/tail state together
+  const float Mf = fmaxf(M, Mt);
+  const float fc = exp2f(M - Mf), ft = exp2f(Mt - Mf);
+  L = L * fc + Lt * ft;
+  O = O * fc + Ot * ft;
   if (grp == 0) a.out[((uint64_t)b * g.Hq + hq) * D + c] = O / L;
 }
 
@@ -666,9 +678,19 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
   c.n_blocks = n_blocks; c.n_split = (int)plan.rows; c.ranges = plan.ranges; c.per_range = plan.per_range;
   c.total = (long long)g.B * g.H * n_blocks;
   c.ws_m = ws_m; c.ws_l = ws_l; c.ws_o = ws_o; c.out = out; c.hadamard = hadamard;
-  dim3 grid(g.Hq, g.B);
-  combine_kernel<<<grid, CB_THREADS, 0, st>>>(c);
-  return cudaGetLastError();
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(g.Hq, g.B);
+  lc.blockDim = dim3(CB_THREADS);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // after a decode kernel (which releases its dependents once all its CTAs run), the combine may
+  // start early and attend the tail meanwhile; with no cached blocks it is an ordinary launch
+  lc.attrs = attr;
+  lc.numAttrs = n_blocks > 0 ? 1 : 0;
+  return cudaLaunchKernelEx(&lc, combine_kernel, c);
 }
 
 // Workspace floats the decode of n_blocks blocks needs on the current device (v1_splits: the

@@ -322,6 +322,7 @@ __device__ __forceinline__ void load_frag(const uint32_t* frag, int lane, int G,
 // 0..63) and 4-7 against probabilities scaled by the matching half's scales.
 template <int METHOD, int BITS, int GT, int NW, int NB, bool WHOLE, bool G64>
 __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
+  launch_dependents();  // the combine kernel may be scheduled once every CTA of this grid runs
   constexpr bool BIAS8 = METHOD == KVQ_INT4;          // signed codes enter biased by 8 (or 128)
   constexpr float BIASF = BITS == 8 ? 128.0f : 8.0f;
   constexpr int RP = 4 / GT;

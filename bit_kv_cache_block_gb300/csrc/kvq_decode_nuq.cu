@@ -572,6 +572,7 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
 
 template <int NBS>
 __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
+  launch_dependents();  // the combine kernel may be scheduled once every CTA of this grid runs
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint8_t* ring = smem_raw;

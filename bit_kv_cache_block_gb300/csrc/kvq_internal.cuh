@@ -136,6 +136,13 @@ inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
   return g;
 }
 
+// Programmatic dependent launch: a kernel lets the next launch in its stream (when that launch
+// allows programmatic serialization) be scheduled once every CTA of this grid has executed
+// launch_dependents or exited; the dependent's grid_dependency_wait returns when this grid has
+// completed and its memory is visible. Both are no-ops for ordinary launches.
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Raises a kernel's dynamic shared-memory limit on the current device once (the setting is
 // cached per device and kernel), so repeated launches make no extra runtime calls.
 inline cudaError_t ensure_smem_attr(const void* fn, size_t smem) {
