@@ -713,6 +713,9 @@ struct Plan {
 #ifndef KVQ_MMA2_WHOLE
 #define KVQ_MMA2_WHOLE 1
 #endif
+#ifndef KVQ_MMA2_WHOLE_G1
+#define KVQ_MMA2_WHOLE_G1 0
+#endif
 #ifndef KVQ_MMA4_NW
 #define KVQ_MMA4_NW 5
 #endif
@@ -734,7 +737,9 @@ template <int METHOD, int BITS, int GT, bool G64>
 Plan plan_for() {
   constexpr int NW = BITS == 2 ? KVQ_MMA2_NW : BITS == 4 ? KVQ_MMA4_NW : KVQ_MMA8_NW;
   constexpr int NB = BITS == 2 ? KVQ_MMA2_NB : BITS == 4 ? KVQ_MMA4_NB : KVQ_MMA8_NB;
-  constexpr bool WH = BITS == 2 ? KVQ_MMA2_WHOLE : BITS == 4 ? KVQ_MMA4_WHOLE : false;
+  // one query head (GT 1, four replicas of its columns): a long stream of light records runs
+  // best from K/V half buffers; several heads per record: whole records
+  constexpr bool WH = BITS == 2 ? (GT == 1 ? KVQ_MMA2_WHOLE_G1 : KVQ_MMA2_WHOLE) : BITS == 4 ? KVQ_MMA4_WHOLE : false;
   return Plan{decode_mma_kernel<METHOD, BITS, GT, NW, NB, WH, G64>, NW, NB, WH};
 }
 
