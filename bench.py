@@ -46,8 +46,8 @@ BENCH_LAYOUT = "mma"
 # shared header); once they change the traffic reads null until a new capture replaces it.
 # Captures and commands: profiles/dram_traffic_decode_kernels.md.
 PROFILED_TRAFFIC = {
-    2: {"bytes_per_record": 14867.7, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
-        "sha256_16": "6355dcc3031f38c7", "capture": "same workload at L = 16384 (4096 records)"},
+    2: {"bytes_per_record": 14867.6, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
+        "sha256_16": "9fc7b31bdc440fab", "capture": "same workload at L = 16384 (4096 records)"},
     3: {"bytes_per_record": 9783.2, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
         "sha256_16": "009d5ee3f8020a06", "capture": "full workload (8192 records)"},
     4: {"bytes_per_record": 17076.7, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
