@@ -659,7 +659,7 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
       e = kvq_launch_decode_nuq(g, base, codebook, q, n_blocks, plan.ranges, plan.slots, ws_m, ws_l, ws_o, status,
                                 st);
     } else if (plan.ranges > 0) {
-      e = kvq_launch_decode_mma(g, base, q, n_blocks, plan.ranges, plan.rows, ws_m, ws_l, ws_o, status, hadamard,
+      e = kvq_launch_decode_mma(g, base, q, n_blocks, plan.ranges, plan.slots, ws_m, ws_l, ws_o, status, hadamard,
                                 st);
     } else {
       DecodeArgs a;
