@@ -710,23 +710,25 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
 namespace cta {
 
 constexpr int NC = 8;                       // consumer warps
-constexpr int AUX_WARP = NC, PROD_WARP = NC + 1;
-constexpr int NTHREADS = (NC + 2) * 32;
+constexpr int NAUX = 4;                     // aux warps (blocks k, k + NAUX, ... of the range)
+constexpr int PROD_WARP = NC + NAUX;
+constexpr int NTHREADS = (NC + NAUX + 1) * 32;
 #ifndef KVQ_CTA_NB
 #define KVQ_CTA_NB 8
 #endif
 constexpr int NB = KVQ_CTA_NB;              // ring stages
+static_assert(NB % NAUX == 0, "a stage is always prepared by the same aux warp");
 
 struct StageOps {
   uint32_t frag[8 * 64];  // score B: 8 columns (head h: 2h high, 2h + 1 low) x 128 halves
   float zk[GQ];           // per head: zero-point score term (RTN, KVarN) or bias * sum q (absmax)
   int g0;                 // power of two the B values carry
-  int pad[3];
+  int pad;
+  long long seg;          // (b, h) segment the operand was built for (-1: none)
 };
 
 struct CtaSmem {
   StageOps op[NB];
-  float q[GQ][D];         // aux: the queries of the current (b, h) (Hadamard domain for KVarN)
   uint64_t rec_full[NB];  // record landed (bulk copy)
   uint64_t ops_full[NB];  // score operand staged (aux)
   uint64_t empty[NB];     // NC consumer warps done with the stage
@@ -771,98 +773,111 @@ __device__ void cta_producer(const Args& a, CtaSmem* sm, uint8_t* ring, long lon
       mbar_wait_bounded(&sm->rec_full[p % NB], (uint32_t)((p / NB) & 1), nullptr, 200000000LL);
 }
 
-// Aux warp: the score B operand of every block (columns 2h, 2h + 1: high and low fp16 halves of
-// q_h * s_c * 2^g0 / f(c), f(c) the power of two code position c carries in its A operand).
+// Aux warps: the score B operand of every block (columns 2h, 2h + 1: high and low fp16 halves of
+// q_h * s_c * 2^g0 / f(c), f(c) the power of two code position c carries in its A operand). Aux
+// warp k takes blocks k, k + NAUX, ... of the range; lane l holds channels l + 32j of every head's
+// query in registers (KVarN: transformed to the Hadamard domain with shuffles). Absmax keys carry
+// no per-channel scale, so a stage keeps its operand while the (b, h) segment does not change.
 template <int METHOD, int BITS>
-__device__ void cta_aux(const Args& a, CtaSmem* sm, const uint8_t* ring, long long x0, int n, int lane) {
+__device__ void cta_aux(const Args& a, CtaSmem* sm, const uint8_t* ring, long long x0, int n, int k, int lane) {
   const Geo& g = a.g;
   const int G = g.G;
   const uint32_t rec = (uint32_t)g.rec_bytes;
   constexpr float BIASF = 8.0f;
   long long u = x0 / a.nb;
-  int blk = (int)(x0 - u * a.nb);
+  int blk = (int)(x0 - u * a.nb) + k;
+  while (blk >= a.nb) {
+    blk -= a.nb;
+    ++u;
+  }
   long long cur_u = -1;
-  for (int p = 0; p < n; ++p) {
+  float qv[GQ][4];
+  for (int p = k; p < n; p += NAUX) {
     const int s = p % NB;
     if (u != cur_u) {  // the queries of this (b, h)
       cur_u = u;
       const long long b = u / g.H, h = u - b * g.H;
-      __syncwarp();
-      for (int e = lane; e < GQ * D; e += 32) {
-        const int hh = e >> 7, c = e & 127;
-        sm->q[hh][c] = hh < G ? load_in(a.q + ((uint64_t)(b * g.Hq + h * G + hh)) * D + c, g.in_bf16) : 0.0f;
-      }
-      __syncwarp();
-      if (METHOD == KVQ_VARN && a.hadamard) {
-        for (int hh = 0; hh < G; ++hh) {
-          float* v = sm->q[hh];
-          for (int st = 1; st < D; st <<= 1) {
-            for (int j = lane; j < D / 2; j += 32) {
-              const int i0 = (j / st) * (2 * st) + (j % st);
-              const float p0 = v[i0], p1 = v[i0 + st];
-              v[i0] = p0 + p1;
-              v[i0 + st] = p0 - p1;
+#pragma unroll
+      for (int hh = 0; hh < GQ; ++hh)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          qv[hh][j] = hh < G ? load_in(a.q + ((uint64_t)(b * g.Hq + h * G + hh)) * D + lane + 32 * j, g.in_bf16) : 0.0f;
+      if (METHOD == KVQ_VARN && a.hadamard) {  // distances 1..16 across lanes, 32 and 64 in the lane
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+#pragma unroll
+          for (int hl = 1; hl < 32; hl <<= 1) {
+            const bool upper = lane & hl;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float o = __shfl_xor_sync(0xffffffffu, qv[hh][j], hl);
+              qv[hh][j] = upper ? o - qv[hh][j] : qv[hh][j] + o;
             }
-            __syncwarp();
           }
-          for (int c = lane; c < D; c += 32) v[c] *= 0.08838834764831845f;
-          __syncwarp();
+          const float y0 = qv[hh][0] + qv[hh][1], y1 = qv[hh][0] - qv[hh][1];
+          const float y2 = qv[hh][2] + qv[hh][3], y3 = qv[hh][2] - qv[hh][3];
+          qv[hh][0] = (y0 + y2) * 0.08838834764831845f;
+          qv[hh][2] = (y0 - y2) * 0.08838834764831845f;
+          qv[hh][1] = (y1 + y3) * 0.08838834764831845f;
+          qv[hh][3] = (y1 - y3) * 0.08838834764831845f;
         }
       }
     }
     const bool got = mbar_wait_bounded(&sm->rec_full[s], (uint32_t)((p / NB) & 1), a.status);
     if (__any_sync(0xffffffffu, !got)) break;
-    const uint16_t* km = reinterpret_cast<const uint16_t*>(ring + (size_t)s * rec + g.meta_off[0]);
-    // lane l: channels l + 32j of every head
-    float v[GQ][4];
-    float mx = 0.0f, zk[GQ];
+    StageOps& op = sm->op[s];
+    if (!(METHOD == KVQ_INT4 && op.seg == u)) {
+      const uint16_t* km = reinterpret_cast<const uint16_t*>(ring + (size_t)s * rec + g.meta_off[0]);
+      float v[GQ][4];
+      float mx = 0.0f, zk[GQ];
 #pragma unroll
-    for (int hh = 0; hh < GQ; ++hh) {
-      zk[hh] = 0.0f;
+      for (int hh = 0; hh < GQ; ++hh) zk[hh] = 0.0f;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int c = lane + 32 * j;
-        const float qv = sm->q[hh][c];
-        float x;
-        if (METHOD == KVQ_INT4) {
-          x = qv;
-          zk[hh] += qv;
-        } else {
-          const float sc = h2f(km[c]);
-          x = qv * sc;
-          zk[hh] = fmaf(x, h2f(km[T + c]), zk[hh]);
+        const float sc = METHOD == KVQ_INT4 ? 1.0f : h2f(km[c]);
+        const float zc = METHOD == KVQ_INT4 ? 1.0f : h2f(km[T + c]);
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+          const float x = qv[hh][j] * sc;
+          zk[hh] = fmaf(x, zc, zk[hh]);
+          v[hh][j] = x;
+          mx = fmaxf(mx, fabsf(x));
         }
-        v[hh][j] = x;
-        mx = fmaxf(mx, fabsf(x));
+      }
+      mx = warp_max_all(mx);
+#pragma unroll
+      for (int hh = 0; hh < GQ; ++hh) zk[hh] = warp_sum_all(zk[hh]);
+      const int g0 = range_exp(mx);
+      const float s0 = exp2i(g0);
+      __half* fh = reinterpret_cast<__half*>(op.frag);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = lane + 32 * j;
+        const int o = pos_off<BITS>(c);
+        const float f = s0 * lane_inv_f<BITS>(c & 7);
+#pragma unroll
+        for (int hh = 0; hh < GQ; ++hh) {
+          __half hi, lo;
+          split_hl(v[hh][j] * f, hi, lo);
+          fh[(2 * hh) * 128 + o] = hi;
+          fh[(2 * hh + 1) * 128 + o] = lo;
+        }
+      }
+      float zsel = zk[0];
+#pragma unroll
+      for (int hh = 1; hh < GQ; ++hh) zsel = lane == hh ? zk[hh] : zsel;
+      if (lane < GQ) op.zk[lane] = METHOD == KVQ_INT4 ? BIASF * zsel : zsel;
+      if (lane == 0) {
+        op.g0 = g0;
+        op.seg = u;
       }
     }
-    mx = warp_max_all(mx);
-#pragma unroll
-    for (int hh = 0; hh < GQ; ++hh) zk[hh] = warp_sum_all(zk[hh]);
-    const int g0 = range_exp(mx);
-    const float s0 = exp2i(g0);
-    StageOps& op = sm->op[s];
-    __half* fh = reinterpret_cast<__half*>(op.frag);
-#pragma unroll
-    for (int hh = 0; hh < GQ; ++hh)
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = lane + 32 * j;
-        __half hi, lo;
-        split_hl(v[hh][j] * s0 * lane_inv_f<BITS>(c & 7), hi, lo);
-        const int o = pos_off<BITS>(c);
-        fh[(2 * hh) * 128 + o] = hi;
-        fh[(2 * hh + 1) * 128 + o] = lo;
-      }
-    float zsel = zk[0];
-#pragma unroll
-    for (int hh = 1; hh < GQ; ++hh) zsel = lane == hh ? zk[hh] : zsel;
-    if (lane < GQ) op.zk[lane] = METHOD == KVQ_INT4 ? BIASF * zsel : zsel;
-    if (lane == 0) op.g0 = g0;
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm->ops_full[s]);
-    if (++blk == a.nb) {
-      blk = 0;
+    blk += NAUX;
+    while (blk >= a.nb) {
+      blk -= a.nb;
       ++u;
     }
   }
@@ -1132,12 +1147,13 @@ __global__ void __launch_bounds__(cta::NTHREADS, 1) decode_cta_kernel(Args a) {
       mbar_init(&sm->rec_full[s], 1);
       mbar_init(&sm->ops_full[s], 1);
       mbar_init(&sm->empty[s], NC);
+      sm->op[s].seg = -1;
     }
     fence_mbar_init();
   }
   __syncthreads();
   if (warp < NC) cta_consumer<METHOD, BITS>(a, sm, ring, R, x0, n, warp, lane);
-  else if (warp == AUX_WARP) cta_aux<METHOD, BITS>(a, sm, ring, x0, n, lane);
+  else if (warp < PROD_WARP) cta_aux<METHOD, BITS>(a, sm, ring, x0, n, warp - NC, lane);
   else cta_producer<METHOD, BITS>(a, sm, ring, x0, n, lane);
 }
 
