@@ -973,6 +973,10 @@ __device__ __forceinline__ void value_mma(float (&O)[8][4], const uint32_t* vc, 
   }
 }
 
+// Consumer warp w. Per block, the value product of block j and the scores of block j + 1 form one
+// straight-line stretch, so their dependency chains overlap (the scores do not depend on the
+// softmax state). Its flash-decode state goes to its own partial row at the end of each (b, h)
+// segment.
 template <int METHOD, int BITS>
 __device__ void cta_consumer(const Args& a, CtaSmem* sm, const uint8_t* ring, long long R, long long x0, int n, int w,
                              int lane) {
@@ -991,7 +995,6 @@ __device__ void cta_consumer(const Args& a, CtaSmem* sm, const uint8_t* ring, lo
   float m_run = -INFINITY, l_run = 0.0f, zv = 0.0f;
   float O[8][4];
   int g1_cur = 0;
-  bool ok = true;
 
   auto flush = [&](long long uu) {
     const long long b = uu / g.H, h = uu - b * g.H;
@@ -1011,34 +1014,20 @@ __device__ void cta_consumer(const Args& a, CtaSmem* sm, const uint8_t* ring, lo
       }
     }
   };
-
-  for (int p = 0; p < n; ++p) {
-    if (u != cur_u) {
-      if (cur_u >= 0) flush(cur_u);
-      cur_u = u;
-      m_run = -INFINITY;
-      l_run = 0.0f;
-      zv = 0.0f;
-      g1_cur = 0;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.0f;
-    }
+  auto wait_stage = [&](int p) -> bool {  // false when a wait gave up (all lanes agree)
     const int s = p % NB;
     const uint32_t par = (uint32_t)((p / NB) & 1);
     const bool got = mbar_wait_bounded(&sm->rec_full[s], par, a.status) &&
                      mbar_wait_bounded(&sm->ops_full[s], par, a.status);
-    if (__any_sync(0xffffffffu, !got)) {
-      ok = false;
-      break;
-    }
+    return !__any_sync(0xffffffffu, !got);
+  };
+  // scores of the warp's 16 tokens, every head, in base-2 units: token ta (xa) and tb (xb)
+  auto scores = [&](int p, float& xa, float& xb) {
+    const int s = p % NB;
     const uint8_t* st = ring + (size_t)s * rec;
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + g.codes_off[0]);
     const uint16_t* km = reinterpret_cast<const uint16_t*>(st + g.meta_off[0]);
-    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + g.codes_off[1]);
-    const uint16_t* vm = reinterpret_cast<const uint16_t*>(st + g.meta_off[1]);
     const StageOps& op = sm->op[s];
-
-    // ---- scores of the warp's 16 tokens, every head
     uint32_t bk[16];
     load_frag(op.frag, lane, G, bk);
     float acc[4];
@@ -1057,9 +1046,57 @@ __device__ void cta_consumer(const Args& a, CtaSmem* sm, const uint8_t* ring, lo
       sa *= h2f(km[2 * T + ta]);
       sb *= h2f(km[2 * T + tb]);
     }
-    sa *= LOG2E_RSQRT_D;
-    sb *= LOG2E_RSQRT_D;
+    xa = sa * LOG2E_RSQRT_D;
+    xb = sb * LOG2E_RSQRT_D;
+  };
+  // values of block p: O[channel][head] += V[channel][warp's tokens] . p'
+  auto values = [&](int p, float alpha, int g1, float zs, uint32_t b0, uint32_t b1) {
+    const int s = p % NB;
+    const uint8_t* st = ring + (size_t)s * rec;
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + g.codes_off[1]);
+    const uint16_t* vm = reinterpret_cast<const uint16_t*>(st + g.meta_off[1]);
+    if (METHOD != KVQ_VARN) {
+      const float rs = alpha * exp2i(g1 - g1_cur);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        O[mt][0] *= rs; O[mt][1] *= rs; O[mt][2] *= rs; O[mt][3] *= rs;
+      }
+      zv = zv * alpha + zs;
+      g1_cur = g1;
+      value_mma<BITS, BIAS8>(O, vc, w, gq, tq, b0, b1);
+    } else {  // second scale s1 per channel: o_c += s1_c * (P.V_c + sum p' z)
+      float av[8][4];
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) av[mt][0] = av[mt][1] = av[mt][2] = av[mt][3] = 0.0f;
+      value_mma<BITS, BIAS8>(av, vc, w, gq, tq, b0, b1);
+      const float usc = exp2i(24 - g1);
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) {
+        const int r0 = 16 * mt + gq, r1 = r0 + 8;
+        const float s1a = h2f(vm[2 * T + r0]), s1b = h2f(vm[2 * T + r1]);
+        O[mt][0] = O[mt][0] * alpha + (av[mt][0] * usc + zs) * s1a;
+        O[mt][1] = O[mt][1] * alpha + av[mt][1] * usc * s1a;
+        O[mt][2] = O[mt][2] * alpha + (av[mt][2] * usc + zs) * s1b;
+        O[mt][3] = O[mt][3] * alpha + av[mt][3] * usc * s1b;
+      }
+    }
+  };
 
+  if (n <= 0 || !wait_stage(0)) return;
+  float sa, sb;
+  scores(0, sa, sb);
+  for (int p = 0; p < n; ++p) {
+    if (u != cur_u) {
+      if (cur_u >= 0) flush(cur_u);
+      cur_u = u;
+      m_run = -INFINITY;
+      l_run = 0.0f;
+      zv = 0.0f;
+      g1_cur = 0;
+#pragma unroll
+      for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.0f;
+    }
+    const uint16_t* vm = reinterpret_cast<const uint16_t*>(ring + (size_t)(p % NB) * rec + g.meta_off[1]);
     // ---- online softmax per head over the warp's tokens (base 2)
     float mloc = fmaxf(sa, sb);
     mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
@@ -1090,41 +1127,24 @@ __device__ void cta_consumer(const Args& a, CtaSmem* sm, const uint8_t* ring, lo
       const uint32_t LO = (uint32_t)__half_as_ushort(la) | ((uint32_t)__half_as_ushort(lb) << 16);
       value_b<BITS>(HI, LO, gq, tq, b0, b1);
     }
-
-    // ---- values: O[channel][head] += V[channel][warp's tokens] . p'
-    if (METHOD != KVQ_VARN) {
-      const float rs = alpha * exp2i(g1 - g1_cur);
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        O[mt][0] *= rs; O[mt][1] *= rs; O[mt][2] *= rs; O[mt][3] *= rs;
-      }
-      zv = zv * alpha + zs;
-      g1_cur = g1;
-      value_mma<BITS, BIAS8>(O, vc, w, gq, tq, b0, b1);
-    } else {  // second scale s1 per channel: o_c += s1_c * (P.V_c + sum p' z)
-      float av[8][4];
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) av[mt][0] = av[mt][1] = av[mt][2] = av[mt][3] = 0.0f;
-      value_mma<BITS, BIAS8>(av, vc, w, gq, tq, b0, b1);
-      const float usc = exp2i(24 - g1);
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int r0 = 16 * mt + gq, r1 = r0 + 8;
-        const float s1a = h2f(vm[2 * T + r0]), s1b = h2f(vm[2 * T + r1]);
-        O[mt][0] = O[mt][0] * alpha + (av[mt][0] * usc + zs) * s1a;
-        O[mt][1] = O[mt][1] * alpha + av[mt][1] * usc * s1a;
-        O[mt][2] = O[mt][2] * alpha + (av[mt][2] * usc + zs) * s1b;
-        O[mt][3] = O[mt][3] * alpha + av[mt][3] * usc * s1b;
-      }
+    if (p + 1 < n) {
+      if (!wait_stage(p + 1)) break;
+      float na, nb2;
+      values(p, alpha, g1, zs, b0, b1);
+      scores(p + 1, na, nb2);
+      sa = na;
+      sb = nb2;
+    } else {
+      values(p, alpha, g1, zs, b0, b1);
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&sm->empty[s]);
+    if (lane == 0) mbar_arrive(&sm->empty[p % NB]);
     if (++blk == a.nb) {
       blk = 0;
       ++u;
     }
+    if (p + 1 == n) flush(cur_u);
   }
-  if (ok && cur_u >= 0) flush(cur_u);
 }
 
 }  // namespace cta
