@@ -605,7 +605,6 @@ cudaError_t launch_decode_m(const DecodeArgs& a, cudaStream_t st) {
 long long kvq_mma_ranges(const kvq::Geo& g);
 long long kvq_nuq_ranges(const kvq::Geo& g);
 int kvq_nuq_parts_per_range();
-int kvq_mma_parts_per_range(const kvq::Geo& g);
 cudaError_t kvq_launch_decode_nuq(const kvq::Geo& g, const uint8_t* base, const float* codebook, const uint16_t* q,
                                   int n_blocks, long long ranges, long long slots, float* ws_m, float* ws_l,
                                   float* ws_o, int* status, cudaStream_t st);
@@ -637,7 +636,7 @@ DecodePlan plan_decode(const kvq::Geo& g, int n_blocks, int v1_splits) {
   if (ranges > 0 && total < (1LL << 62) / ranges) {
     p.ranges = ranges;
     p.slots = kvq_mma_slots(g, n_blocks, ranges);
-    p.per_range = p.nuq ? kvq_nuq_parts_per_range() : kvq_mma_parts_per_range(g);
+    p.per_range = p.nuq ? kvq_nuq_parts_per_range() : 1;
     p.rows = p.slots * p.per_range;
   }
   return p;

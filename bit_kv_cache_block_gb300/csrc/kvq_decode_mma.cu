@@ -696,505 +696,6 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
   if (cur_u >= 0) flush(cur_u);
 }
 
-// ------------------------------------------------------------------ CTA-wide decode (GQA)
-//
-// For caches whose KV heads serve 3 or 4 query heads (2- and 4-bit codes), the records of a CTA's
-// range stream through one CTA-wide ring, and each record's work is split over 8 consumer warps:
-// consumer warp w owns tokens 16w..16w+15 of every block (scores: one m-tile of the key tile;
-// values: the k-step of its own tokens over all 128 channels), with its own flash-decode state and
-// its own partial row per (b, query head) segment. An aux warp builds each block's score B operand
-// (q times the per-channel key scales, all heads, high/low halves) once for the 8 consumers, and a
-// producer warp copies whole records (one bulk copy from a rotating lane). The value B operand
-// (probabilities times the per-token value scales) goes from the lanes that own a token's score to
-// the lanes that need it in the fragment with shuffles, so no CTA barrier is needed per block.
-namespace cta {
-
-constexpr int NC = 8;                       // consumer warps
-constexpr int NAUX = 4;                     // aux warps (blocks k, k + NAUX, ... of the range)
-constexpr int PROD_WARP = NC + NAUX;
-constexpr int NTHREADS = (NC + NAUX + 1) * 32;
-#ifndef KVQ_CTA_NB
-#define KVQ_CTA_NB 8
-#endif
-constexpr int NB = KVQ_CTA_NB;              // ring stages
-static_assert(NB % NAUX == 0, "a stage is always prepared by the same aux warp");
-
-struct StageOps {
-  uint32_t frag[8 * 64];  // score B: 8 columns (head h: 2h high, 2h + 1 low) x 128 halves
-  float zk[GQ];           // per head: zero-point score term (RTN, KVarN) or bias * sum q (absmax)
-  int g0;                 // power of two the B values carry
-  int pad;
-  long long seg;          // (b, h) segment the operand was built for (-1: none)
-};
-
-struct CtaSmem {
-  StageOps op[NB];
-  uint64_t rec_full[NB];  // record landed (bulk copy)
-  uint64_t ops_full[NB];  // score operand staged (aux)
-  uint64_t empty[NB];     // NC consumer warps done with the stage
-};
-
-// Half offset of code position c (0..127) inside a staged B column (see col_off).
-template <int BITS>
-__device__ __forceinline__ int pos_off(int c) {
-  return col_off<BITS>(c >> 4, c & 7, (c >> 3) & 1);
-}
-
-template <int METHOD, int BITS>
-__device__ void cta_producer(const Args& a, CtaSmem* sm, uint8_t* ring, long long x0, int n, int lane) {
-  const Geo& g = a.g;
-  const uint32_t rec = (uint32_t)g.rec_bytes;
-  long long u = x0 / a.nb;
-  int blk = (int)(x0 - u * a.nb);
-  int pb = (int)(u / g.H), ph = (int)(u - (long long)pb * g.H);
-  int issued = 0;
-  for (int p = 0; p < n; ++p) {
-    const int s = p % NB;
-    if (p >= NB) {
-      const bool got = mbar_wait_bounded(&sm->empty[s], (uint32_t)(((p / NB) - 1) & 1), a.status);
-      if (__any_sync(0xffffffffu, !got)) break;
-    }
-    if (lane == (p & 31)) {  // a thread services its own copies one after another: rotate lanes
-      mbar_arrive_expect_tx(&sm->rec_full[s], rec);
-      fence_proxy_async();
-      bulk_g2s(ring + (size_t)s * rec, a.base + record_offset(g, pb, ph, blk, a.status), rec, &sm->rec_full[s]);
-    }
-    issued = p + 1;
-    if (++blk == a.nb) {
-      blk = 0;
-      if (++ph == g.H) {
-        ph = 0;
-        ++pb;
-      }
-    }
-  }
-  if (lane == 0)
-    for (int p = max(0, issued - NB); p < issued; ++p)
-      mbar_wait_bounded(&sm->rec_full[p % NB], (uint32_t)((p / NB) & 1), nullptr, 200000000LL);
-}
-
-// Aux warps: the score B operand of every block (columns 2h, 2h + 1: high and low fp16 halves of
-// q_h * s_c * 2^g0 / f(c), f(c) the power of two code position c carries in its A operand). Aux
-// warp k takes blocks k, k + NAUX, ... of the range; lane l holds channels l + 32j of every head's
-// query in registers (KVarN: transformed to the Hadamard domain with shuffles). Absmax keys carry
-// no per-channel scale, so a stage keeps its operand while the (b, h) segment does not change.
-template <int METHOD, int BITS>
-__device__ void cta_aux(const Args& a, CtaSmem* sm, const uint8_t* ring, long long x0, int n, int k, int lane) {
-  const Geo& g = a.g;
-  const int G = g.G;
-  const uint32_t rec = (uint32_t)g.rec_bytes;
-  constexpr float BIASF = 8.0f;
-  long long u = x0 / a.nb;
-  int blk = (int)(x0 - u * a.nb) + k;
-  while (blk >= a.nb) {
-    blk -= a.nb;
-    ++u;
-  }
-  long long cur_u = -1;
-  float qv[GQ][4];
-  for (int p = k; p < n; p += NAUX) {
-    const int s = p % NB;
-    if (u != cur_u) {  // the queries of this (b, h)
-      cur_u = u;
-      const long long b = u / g.H, h = u - b * g.H;
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          qv[hh][j] = hh < G ? load_in(a.q + ((uint64_t)(b * g.Hq + h * G + hh)) * D + lane + 32 * j, g.in_bf16) : 0.0f;
-      if (METHOD == KVQ_VARN && a.hadamard) {  // distances 1..16 across lanes, 32 and 64 in the lane
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-#pragma unroll
-          for (int hl = 1; hl < 32; hl <<= 1) {
-            const bool upper = lane & hl;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float o = __shfl_xor_sync(0xffffffffu, qv[hh][j], hl);
-              qv[hh][j] = upper ? o - qv[hh][j] : qv[hh][j] + o;
-            }
-          }
-          const float y0 = qv[hh][0] + qv[hh][1], y1 = qv[hh][0] - qv[hh][1];
-          const float y2 = qv[hh][2] + qv[hh][3], y3 = qv[hh][2] - qv[hh][3];
-          qv[hh][0] = (y0 + y2) * 0.08838834764831845f;
-          qv[hh][2] = (y0 - y2) * 0.08838834764831845f;
-          qv[hh][1] = (y1 + y3) * 0.08838834764831845f;
-          qv[hh][3] = (y1 - y3) * 0.08838834764831845f;
-        }
-      }
-    }
-    const bool got = mbar_wait_bounded(&sm->rec_full[s], (uint32_t)((p / NB) & 1), a.status);
-    if (__any_sync(0xffffffffu, !got)) break;
-    StageOps& op = sm->op[s];
-    if (!(METHOD == KVQ_INT4 && op.seg == u)) {
-      const uint16_t* km = reinterpret_cast<const uint16_t*>(ring + (size_t)s * rec + g.meta_off[0]);
-      float v[GQ][4];
-      float mx = 0.0f, zk[GQ];
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) zk[hh] = 0.0f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = lane + 32 * j;
-        const float sc = METHOD == KVQ_INT4 ? 1.0f : h2f(km[c]);
-        const float zc = METHOD == KVQ_INT4 ? 1.0f : h2f(km[T + c]);
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-          const float x = qv[hh][j] * sc;
-          zk[hh] = fmaf(x, zc, zk[hh]);
-          v[hh][j] = x;
-          mx = fmaxf(mx, fabsf(x));
-        }
-      }
-      mx = warp_max_all(mx);
-#pragma unroll
-      for (int hh = 0; hh < GQ; ++hh) zk[hh] = warp_sum_all(zk[hh]);
-      const int g0 = range_exp(mx);
-      const float s0 = exp2i(g0);
-      __half* fh = reinterpret_cast<__half*>(op.frag);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = lane + 32 * j;
-        const int o = pos_off<BITS>(c);
-        const float f = s0 * lane_inv_f<BITS>(c & 7);
-#pragma unroll
-        for (int hh = 0; hh < GQ; ++hh) {
-          __half hi, lo;
-          split_hl(v[hh][j] * f, hi, lo);
-          fh[(2 * hh) * 128 + o] = hi;
-          fh[(2 * hh + 1) * 128 + o] = lo;
-        }
-      }
-      float zsel = zk[0];
-#pragma unroll
-      for (int hh = 1; hh < GQ; ++hh) zsel = lane == hh ? zk[hh] : zsel;
-      if (lane < GQ) op.zk[lane] = METHOD == KVQ_INT4 ? BIASF * zsel : zsel;
-      if (lane == 0) {
-        op.g0 = g0;
-        op.seg = u;
-      }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm->ops_full[s]);
-    blk += NAUX;
-    while (blk >= a.nb) {
-      blk -= a.nb;
-      ++u;
-    }
-  }
-}
-
-// Score of the consumer warp's m-tile (tokens 16w + gq, 16w + gq + 8) against the staged B.
-template <int BITS, bool BIAS8>
-__device__ __forceinline__ void mtile_scores(float (&acc)[4], const uint32_t* kc, int w, int gq, int tq,
-                                             const uint32_t (&b)[16]) {
-  acc[0] = acc[1] = acc[2] = acc[3] = 0.0f;
-  if (BITS == 2) {
-    const uint2 w0 = *reinterpret_cast<const uint2*>(kc + (16 * w + gq) * 8 + 2 * tq);
-    const uint2 w1 = *reinterpret_cast<const uint2*>(kc + (16 * w + gq + 8) * 8 + 2 * tq);
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int qr = 2 * (ks & 3);
-      const uint32_t x0 = ks < 4 ? w0.x : w0.y, x1 = ks < 4 ? w1.x : w1.y;
-      mma16816(acc, operand<2, BIAS8>(x0, qr), operand<2, BIAS8>(x1, qr), operand<2, BIAS8>(x0, qr + 1),
-               operand<2, BIAS8>(x1, qr + 1), b[2 * ks], b[2 * ks + 1]);
-    }
-  } else {
-    const uint4 w0 = *reinterpret_cast<const uint4*>(kc + (16 * w + gq) * 16 + 4 * tq);
-    const uint4 w1 = *reinterpret_cast<const uint4*>(kc + (16 * w + gq + 8) * 16 + 4 * tq);
-    const uint32_t* p0 = &w0.x;
-    const uint32_t* p1 = &w1.x;
-#pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      const int qr = 2 * (ks & 1);
-      const uint32_t x0 = p0[ks >> 1], x1 = p1[ks >> 1];
-      mma16816(acc, operand<4, BIAS8>(x0, qr), operand<4, BIAS8>(x1, qr), operand<4, BIAS8>(x0, qr + 1),
-               operand<4, BIAS8>(x1, qr + 1), b[2 * ks], b[2 * ks + 1]);
-    }
-  }
-}
-
-// Value B registers of lane (gq, tq) for the warp's 16 tokens: column gq (head gq/2, high or low
-// half), k rows 2tq, 2tq + 1 (b0) and 2tq + 8, 2tq + 9 (b1). The lane that scored positions p and
-// p + 8 (p = its gq, for head = its tq) holds them packed as HI = (high_p, high_p+8) and LO.
-// 2-bit operands pair positions (q, q + 8): b0 = positions (2tq, 2tq + 8), b1 = (2tq + 1, 2tq + 9).
-// 4-bit operands pair positions (8wi + r, 8wi + r + 4) of word wi = tq / 2, r = 2(tq % 2) (+1 for
-// b1): halves from two lanes.
-template <int BITS>
-__device__ __forceinline__ void value_b(uint32_t HI, uint32_t LO, int gq, int tq, uint32_t& b0, uint32_t& b1) {
-  const int hd = gq >> 1;
-  const bool lo = gq & 1;
-  if (BITS == 2) {
-    const int s0 = 4 * (2 * tq) + hd, s1 = 4 * (2 * tq + 1) + hd;
-    const uint32_t h0 = __shfl_sync(0xffffffffu, HI, s0), l0 = __shfl_sync(0xffffffffu, LO, s0);
-    const uint32_t h1 = __shfl_sync(0xffffffffu, HI, s1), l1 = __shfl_sync(0xffffffffu, LO, s1);
-    b0 = lo ? l0 : h0;
-    b1 = lo ? l1 : h1;
-  } else {
-    const int wi = tq >> 1, r = 2 * (tq & 1);
-    // position P -> source lane 4 * (P & 7) + hd, half P >> 3 of its packed pair (every lane
-    // takes part in every shuffle; the column's half is selected afterwards)
-    const int pa = 8 * wi + r, pb = pa + 4, pc = pa + 1, pd = pa + 5;
-    const int la = 4 * (pa & 7) + hd, lb = 4 * (pb & 7) + hd, lc = 4 * (pc & 7) + hd, ld = 4 * (pd & 7) + hd;
-    const uint32_t ha = __shfl_sync(0xffffffffu, HI, la), la_ = __shfl_sync(0xffffffffu, LO, la);
-    const uint32_t hb = __shfl_sync(0xffffffffu, HI, lb), lb_ = __shfl_sync(0xffffffffu, LO, lb);
-    const uint32_t hc = __shfl_sync(0xffffffffu, HI, lc), lc_ = __shfl_sync(0xffffffffu, LO, lc);
-    const uint32_t hd2 = __shfl_sync(0xffffffffu, HI, ld), ld_ = __shfl_sync(0xffffffffu, LO, ld);
-    const uint32_t xa = lo ? la_ : ha, xb = lo ? lb_ : hb, xc = lo ? lc_ : hc, xd = lo ? ld_ : hd2;
-    // wi 0: the low halves (positions < 8); wi 1: the high halves
-    const uint32_t sel = wi ? 0x7632u : 0x5410u;
-    b0 = __byte_perm(xa, xb, sel);
-    b1 = __byte_perm(xc, xd, sel);
-  }
-}
-
-// The value product of the warp's 16 tokens (one k-step) over the 8 channel m-tiles.
-template <int BITS, bool BIAS8>
-__device__ __forceinline__ void value_mma(float (&O)[8][4], const uint32_t* vc, int w, int gq, int tq, uint32_t b0,
-                                          uint32_t b1) {
-#pragma unroll
-  for (int mt = 0; mt < 8; ++mt) {
-    const int r0 = 16 * mt + gq, r1 = r0 + 8;
-    uint32_t a0, a1, a2, a3;
-    if (BITS == 2) {  // word w of a channel row: tokens 16w .. 16w + 15
-      const uint32_t x0 = vc[r0 * 8 + w], x1 = vc[r1 * 8 + w];
-      a0 = operand<2, BIAS8>(x0, 2 * tq);
-      a1 = operand<2, BIAS8>(x1, 2 * tq);
-      a2 = operand<2, BIAS8>(x0, 2 * tq + 1);
-      a3 = operand<2, BIAS8>(x1, 2 * tq + 1);
-    } else {          // words 2w, 2w + 1 of a channel row; lane tq reads word 2w + tq / 2
-      const int wi = tq >> 1, r = 2 * (tq & 1);
-      const uint32_t x0 = vc[r0 * 16 + 2 * w + wi], x1 = vc[r1 * 16 + 2 * w + wi];
-      a0 = operand<4, BIAS8>(x0, r);
-      a1 = operand<4, BIAS8>(x1, r);
-      a2 = operand<4, BIAS8>(x0, r + 1);
-      a3 = operand<4, BIAS8>(x1, r + 1);
-    }
-    mma16816(O[mt], a0, a1, a2, a3, b0, b1);
-  }
-}
-
-// Consumer warp w. Per block, the value product of block j and the scores of block j + 1 form one
-// straight-line stretch, so their dependency chains overlap (the scores do not depend on the
-// softmax state). Its flash-decode state goes to its own partial row at the end of each (b, h)
-// segment.
-template <int METHOD, int BITS>
-__device__ void cta_consumer(const Args& a, CtaSmem* sm, const uint8_t* ring, long long R, long long x0, int n, int w,
-                             int lane) {
-  const Geo& g = a.g;
-  const int G = g.G;
-  constexpr bool BIAS8 = METHOD == KVQ_INT4;
-  const int gq = lane >> 2, tq = lane & 3;
-  const int hl = tq;  // the lane's head: column pair tq
-  const bool head_ok = hl < G;
-  const uint32_t rec = (uint32_t)g.rec_bytes;
-  const int ta = 16 * w + gq, tb = ta + 8;
-  const float inv_f = lane_inv_f<BITS>(gq);  // positions gq, gq + 8 of the warp's k-step
-  long long u = x0 / a.nb;
-  int blk = (int)(x0 - u * a.nb);
-  long long cur_u = -1;
-  float m_run = -INFINITY, l_run = 0.0f, zv = 0.0f;
-  float O[8][4];
-  int g1_cur = 0;
-
-  auto flush = [&](long long uu) {
-    const long long b = uu / g.H, h = uu - b * g.H;
-    const long long slot = R - range_of(uu * a.nb, a.total, a.n_ranges);
-    if (head_ok && slot >= 0 && slot < a.n_slots) {
-      const uint64_t row = (((uint64_t)(b * g.Hq + h * G + hl)) * a.n_slots + slot) * NC + w;
-      const float sc = (METHOD == KVQ_VARN) ? 1.0f : exp2i(24 - g1_cur);
-      const float add = (METHOD == KVQ_VARN) ? 0.0f : zv;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        a.ws_o[row * D + 16 * mt + gq] = (O[mt][0] + O[mt][1]) * sc + add;
-        a.ws_o[row * D + 16 * mt + gq + 8] = (O[mt][2] + O[mt][3]) * sc + add;
-      }
-      if (gq == 0) {
-        a.ws_m[row] = m_run;
-        a.ws_l[row] = l_run;
-      }
-    }
-  };
-  auto wait_stage = [&](int p) -> bool {  // false when a wait gave up (all lanes agree)
-    const int s = p % NB;
-    const uint32_t par = (uint32_t)((p / NB) & 1);
-    const bool got = mbar_wait_bounded(&sm->rec_full[s], par, a.status) &&
-                     mbar_wait_bounded(&sm->ops_full[s], par, a.status);
-    return !__any_sync(0xffffffffu, !got);
-  };
-  // scores of the warp's 16 tokens, every head, in base-2 units: token ta (xa) and tb (xb)
-  auto scores = [&](int p, float& xa, float& xb) {
-    const int s = p % NB;
-    const uint8_t* st = ring + (size_t)s * rec;
-    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st + g.codes_off[0]);
-    const uint16_t* km = reinterpret_cast<const uint16_t*>(st + g.meta_off[0]);
-    const StageOps& op = sm->op[s];
-    uint32_t bk[16];
-    load_frag(op.frag, lane, G, bk);
-    float acc[4];
-    mtile_scores<BITS, BIAS8>(acc, kc, w, gq, tq, bk);
-    const float ksc = exp2i(24 - op.g0);
-    const float zkh = head_ok ? op.zk[hl] : 0.0f;
-    float sa = (acc[0] + acc[1]) * ksc, sb = (acc[2] + acc[3]) * ksc;
-    if (METHOD == KVQ_INT4) {
-      sa = (sa - zkh) * h2f(km[ta]);
-      sb = (sb - zkh) * h2f(km[tb]);
-    } else {
-      sa += zkh;
-      sb += zkh;
-    }
-    if (METHOD == KVQ_VARN) {
-      sa *= h2f(km[2 * T + ta]);
-      sb *= h2f(km[2 * T + tb]);
-    }
-    xa = sa * LOG2E_RSQRT_D;
-    xb = sb * LOG2E_RSQRT_D;
-  };
-  // values of block p: O[channel][head] += V[channel][warp's tokens] . p'
-  auto values = [&](int p, float alpha, int g1, float zs, uint32_t b0, uint32_t b1) {
-    const int s = p % NB;
-    const uint8_t* st = ring + (size_t)s * rec;
-    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + g.codes_off[1]);
-    const uint16_t* vm = reinterpret_cast<const uint16_t*>(st + g.meta_off[1]);
-    if (METHOD != KVQ_VARN) {
-      const float rs = alpha * exp2i(g1 - g1_cur);
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        O[mt][0] *= rs; O[mt][1] *= rs; O[mt][2] *= rs; O[mt][3] *= rs;
-      }
-      zv = zv * alpha + zs;
-      g1_cur = g1;
-      value_mma<BITS, BIAS8>(O, vc, w, gq, tq, b0, b1);
-    } else {  // second scale s1 per channel: o_c += s1_c * (P.V_c + sum p' z)
-      float av[8][4];
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) av[mt][0] = av[mt][1] = av[mt][2] = av[mt][3] = 0.0f;
-      value_mma<BITS, BIAS8>(av, vc, w, gq, tq, b0, b1);
-      const float usc = exp2i(24 - g1);
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) {
-        const int r0 = 16 * mt + gq, r1 = r0 + 8;
-        const float s1a = h2f(vm[2 * T + r0]), s1b = h2f(vm[2 * T + r1]);
-        O[mt][0] = O[mt][0] * alpha + (av[mt][0] * usc + zs) * s1a;
-        O[mt][1] = O[mt][1] * alpha + av[mt][1] * usc * s1a;
-        O[mt][2] = O[mt][2] * alpha + (av[mt][2] * usc + zs) * s1b;
-        O[mt][3] = O[mt][3] * alpha + av[mt][3] * usc * s1b;
-      }
-    }
-  };
-
-  if (n <= 0 || !wait_stage(0)) return;
-  float sa, sb;
-  scores(0, sa, sb);
-  for (int p = 0; p < n; ++p) {
-    if (u != cur_u) {
-      if (cur_u >= 0) flush(cur_u);
-      cur_u = u;
-      m_run = -INFINITY;
-      l_run = 0.0f;
-      zv = 0.0f;
-      g1_cur = 0;
-#pragma unroll
-      for (int mt = 0; mt < 8; ++mt) O[mt][0] = O[mt][1] = O[mt][2] = O[mt][3] = 0.0f;
-    }
-    const uint16_t* vm = reinterpret_cast<const uint16_t*>(ring + (size_t)(p % NB) * rec + g.meta_off[1]);
-    // ---- online softmax per head over the warp's tokens (base 2)
-    float mloc = fmaxf(sa, sb);
-    mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 4));
-    mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
-    mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
-    const float m_new = fmaxf(m_run, mloc);
-    const float alpha = head_ok ? exp2f(m_run - m_new) : 1.0f;
-    const float pa = head_ok ? exp2f(sa - m_new) : 0.0f, pb = head_ok ? exp2f(sb - m_new) : 0.0f;
-    float lsum = pa + pb;
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 4);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 8);
-    lsum += __shfl_xor_sync(0xffffffffu, lsum, 16);
-    l_run = l_run * alpha + lsum;
-    m_run = m_new;
-    const float ppa = pa * h2f(vm[ta]), ppb = pb * h2f(vm[tb]);  // per-token value scale folded into p
-    float zs = METHOD == KVQ_INT4 ? -8.0f * (ppa + ppb) : fmaf(ppa, h2f(vm[T + ta]), ppb * h2f(vm[T + tb]));
-    zs += __shfl_xor_sync(0xffffffffu, zs, 4);
-    zs += __shfl_xor_sync(0xffffffffu, zs, 8);
-    zs += __shfl_xor_sync(0xffffffffu, zs, 16);
-    const int g1 = range_exp(warp_max_all(fmaxf(ppa, ppb)));  // one column scale for all heads
-    uint32_t b0, b1;
-    {
-      const float sc = exp2i(g1) * inv_f;
-      __half ha, la, hb, lb;
-      split_hl(ppa * sc, ha, la);
-      split_hl(ppb * sc, hb, lb);
-      const uint32_t HI = (uint32_t)__half_as_ushort(ha) | ((uint32_t)__half_as_ushort(hb) << 16);
-      const uint32_t LO = (uint32_t)__half_as_ushort(la) | ((uint32_t)__half_as_ushort(lb) << 16);
-      value_b<BITS>(HI, LO, gq, tq, b0, b1);
-    }
-    if (p + 1 < n) {
-      if (!wait_stage(p + 1)) break;
-      float na, nb2;
-      values(p, alpha, g1, zs, b0, b1);
-      scores(p + 1, na, nb2);
-      sa = na;
-      sb = nb2;
-    } else {
-      values(p, alpha, g1, zs, b0, b1);
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm->empty[p % NB]);
-    if (++blk == a.nb) {
-      blk = 0;
-      ++u;
-    }
-    if (p + 1 == n) flush(cur_u);
-  }
-}
-
-}  // namespace cta
-
-template <int METHOD, int BITS>
-__global__ void __launch_bounds__(cta::NTHREADS, 1) decode_cta_kernel(Args a) {
-  launch_dependents();  // the combine kernel may be scheduled once every CTA of this grid runs
-  using namespace cta;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  uint8_t* ring = smem_raw;
-  CtaSmem* sm = reinterpret_cast<CtaSmem*>(smem_raw + (size_t)NB * a.g.rec_bytes);
-  const long long R = blockIdx.x;
-  if (R >= a.n_ranges) return;
-  const long long x0 = R * a.total / a.n_ranges, x1 = (R + 1) * a.total / a.n_ranges;
-  const int n = (int)(x1 - x0);
-  if (n <= 0) return;
-  if (tid == 0) {
-    for (int s = 0; s < NB; ++s) {
-      mbar_init(&sm->rec_full[s], 1);
-      mbar_init(&sm->ops_full[s], 1);
-      mbar_init(&sm->empty[s], NC);
-      sm->op[s].seg = -1;
-    }
-    fence_mbar_init();
-  }
-  __syncthreads();
-  if (warp < NC) cta_consumer<METHOD, BITS>(a, sm, ring, R, x0, n, warp, lane);
-  else if (warp < PROD_WARP) cta_aux<METHOD, BITS>(a, sm, ring, x0, n, warp - NC, lane);
-  else cta_producer<METHOD, BITS>(a, sm, ring, x0, n, lane);
-}
-
-size_t cta_smem_bytes(const Geo& g) { return (size_t)cta::NB * g.rec_bytes + sizeof(cta::CtaSmem); }
-
-bool cta_supported(const Geo& g) {
-  if (g.layout != KVQ_LAYOUT_MMA || g.g64) return false;
-  if (g.G < 3 || g.G > GQ) return false;
-  if (g.bits != 2 && g.bits != 4) return false;
-  if (g.method != KVQ_RTN && g.method != KVQ_VARN && g.method != KVQ_INT4) return false;
-  if (g.method == KVQ_INT4 && g.bits != 4) return false;
-  return cta_smem_bytes(g) <= 227 * 1024;
-}
-
-using CtaFn = void (*)(Args);
-CtaFn cta_fn(const Geo& g) {
-  if (g.method == KVQ_RTN) return g.bits == 2 ? decode_cta_kernel<KVQ_RTN, 2> : decode_cta_kernel<KVQ_RTN, 4>;
-  if (g.method == KVQ_VARN) return g.bits == 2 ? decode_cta_kernel<KVQ_VARN, 2> : decode_cta_kernel<KVQ_VARN, 4>;
-  return decode_cta_kernel<KVQ_INT4, 4>;
-}
-
 struct Plan {
   void (*fn)(Args);
   int nw, ns;  // warps per CTA, buffers per warp
@@ -1289,9 +790,8 @@ thread_local OccCache t_occ[8];
 long long kvq_mma_ranges(const kvq::Geo& g) {
   using namespace kvq::mmadec;
   if (!supported(g)) return 0;
-  const bool cta = cta_supported(g);
-  const Plan p = cta ? Plan{cta_fn(g), cta::NTHREADS / 32, cta::NB, true} : get_plan(g);
-  const size_t smem = cta ? cta_smem_bytes(g) : smem_bytes(g, p);
+  const Plan p = get_plan(g);
+  const size_t smem = smem_bytes(g, p);
   if (smem > 227 * 1024) return 0;
   int dev = 0, sms = 152, ctas = 1;
   if (cudaGetDevice(&dev) == cudaSuccess &&
@@ -1317,11 +817,8 @@ long long kvq_mma_ranges(const kvq::Geo& g) {
     cudaGetLastError();
     sms = 152;
   }
-  return cta ? (long long)sms * ctas : (long long)sms * ctas * p.nw;  // CTA-wide: one range per CTA
+  return (long long)sms * ctas * p.nw;
 }
-
-// Partial rows each range writes per (b, query head): one per consumer warp on the CTA-wide path.
-int kvq_mma_parts_per_range(const kvq::Geo& g) { return kvq::mmadec::cta_supported(g) ? kvq::mmadec::cta::NC : 1; }
 
 // Partial slots per (b, query head) for n_blocks blocks split into `ranges` ranges.
 long long kvq_mma_slots(const kvq::Geo& g, int n_blocks, long long ranges) {
@@ -1335,16 +832,15 @@ cudaError_t kvq_launch_decode_mma(const kvq::Geo& g, const uint8_t* base, const 
                                   long long ranges, long long slots, float* ws_m, float* ws_l, float* ws_o,
                                   int* status, int hadamard, cudaStream_t st) {
   using namespace kvq::mmadec;
-  const bool cta = cta_supported(g);
-  const Plan p = cta ? Plan{cta_fn(g), cta::NTHREADS / 32, cta::NB, true} : get_plan(g);
-  const size_t smem = cta ? cta_smem_bytes(g) : smem_bytes(g, p);
+  const Plan p = get_plan(g);
+  const size_t smem = smem_bytes(g, p);
   cudaError_t e = kvq::ensure_smem_attr((const void*)p.fn, (size_t)smem);
   if (e != cudaSuccess) return e;
   Args a;
   a.g = g; a.base = base; a.q = q; a.nb = n_blocks; a.total = (long long)g.B * g.H * n_blocks;
   a.n_ranges = (int)ranges; a.n_slots = (int)slots; a.ws_m = ws_m; a.ws_l = ws_l; a.ws_o = ws_o;
   a.status = status; a.hadamard = hadamard;
-  const int grid = cta ? (int)ranges : (int)((ranges + p.nw - 1) / p.nw);
+  const int grid = (int)((ranges + p.nw - 1) / p.nw);
   p.fn<<<grid, p.nw * 32, smem, st>>>(a);
   return cudaGetLastError();
 }
