@@ -48,9 +48,15 @@ struct Args {
   int hadamard;
 };
 
+// Staged B columns are FRAG_COL words apart (64 used; 2 * 68 = 8 mod 32): the writes of the 4
+// column pairs by the lanes of one row group fall on distinct banks and the 16-byte fragment loads
+// meet half as many conflicts. Query rows are padded for the reads of lanes that serve
+// different heads.
+constexpr int FRAG_COL = 68, QROW = D + 8;
+
 struct WarpSmem {
-  float q[GQ][D];         // queries of the current (b, h) (Hadamard domain for KVarN)
-  uint32_t frag[32 * 16]; // B fragments staged per lane (score product, then value product)
+  float q[GQ][QROW];          // queries of the current (b, h) (Hadamard domain for KVarN)
+  uint32_t frag[8 * FRAG_COL];  // B columns staged for the score product, then the value product
   uint64_t bar[4];
 };
 
@@ -80,30 +86,6 @@ __device__ __forceinline__ uint32_t operand(uint32_t w, int qr) {
     if (BIAS8) v ^= (qr & 1) ? 0x00800080u : 0x00080008u;
     return v;
   }
-}
-
-// Where code index i (0..127) of a row sits in the B fragments: lane group tq (0..3), B
-// register (0..15: 2 per k-step) and half, and 1/(power of two of its operand position).
-template <int BITS>
-__device__ __forceinline__ void position(int i, int& tq, int& reg, int& half, float& inv_f) {
-  if (BITS == 2) {
-    const int wd = i >> 4, p = i & 15, qr = p & 7;
-    tq = wd >> 1;
-    half = p >> 3;
-    reg = 2 * ((wd & 1) * 4 + (qr >> 1)) + (qr & 1);
-    const int e = qr <= 4 ? 2 * qr : 2 * (qr - 5);
-    inv_f = __int_as_float((127 - e) << 23);
-  } else {
-    const int wd = i >> 3, p = i & 7, qr = p & 3;
-    tq = wd >> 2;
-    half = p >> 2;
-    reg = 2 * ((wd & 3) * 2 + (qr >> 1)) + (qr & 1);
-    inv_f = (qr & 1) ? 0.0625f : 1.0f;
-  }
-}
-
-__device__ __forceinline__ void put_half(uint32_t* frag, int lane_dst, int reg, int half, __half v) {
-  reinterpret_cast<__half*>(frag + lane_dst * 16 + reg)[half] = v;
 }
 
 // hi/lo fp16 split of x: hi = fp16(x), lo = fp16(x - hi).
@@ -223,10 +205,6 @@ __device__ __forceinline__ void tile_mma(float (&acc)[8][4], const uint32_t* cod
   }
 }
 
-__device__ __forceinline__ void put_col(uint32_t* frag, int col, int off, __half v) {
-  reinterpret_cast<__half*>(frag)[col * 128 + off] = v;
-}
-
 // Half offset inside one staged B column of the code at row position x = 16*mt + gq + 8*hlf
 // (the positions a lane owns), and the power of two that lane's operands carry (both follow from
 // operand() and the fragment layout).
@@ -269,8 +247,8 @@ __device__ __forceinline__ float head_sum(float v) {
 // Stages the hi/lo halves of v (one value per position the lane owns) into columns 2h, 2h+1.
 template <int BITS, int NMT>
 __device__ __forceinline__ void stage_cols(uint32_t* frag, int h, int gq, int rho, int RP, const float (&v)[2 * NMT]) {
-  __half* col_hi = reinterpret_cast<__half*>(frag) + (2 * h) * 128;
-  __half* col_lo = col_hi + 128;
+  __half* col_hi = reinterpret_cast<__half*>(frag) + (2 * h) * (2 * FRAG_COL);
+  __half* col_lo = col_hi + 2 * FRAG_COL;
 #pragma unroll
   for (int j = 0; j < NMT; ++j) {
     const int mt = rho + RP * j;
@@ -304,7 +282,7 @@ __device__ __forceinline__ void pick_tile(const float (&acc)[8][4], int j, int r
 // Loads the lane's 16 B registers: lane (g', t') reads staged column g' mod 2G.
 __device__ __forceinline__ void load_frag(const uint32_t* frag, int lane, int G, uint32_t (&b)[16]) {
   const int col = (lane >> 2) % (2 * G);
-  const uint4* src = reinterpret_cast<const uint4*>(frag + (col * 4 + (lane & 3)) * 16);
+  const uint4* src = reinterpret_cast<const uint4*>(frag + col * FRAG_COL + (lane & 3) * 16);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const uint4 v = src[k];
