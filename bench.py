@@ -372,16 +372,18 @@ def run_kvq(args):
 
 
 def run_e2e(args, K, torch, dev, caches, cfg, w, nb, q, tail_k, tail_v, cache_bytes):
-    """Same step through the C ABI from pinned host buffers: every decode uploads its query
-    and the new tail token, and downloads its output; the block append reads the tail that
-    was uploaded token by token."""
+    """Same step through the C ABI from pinned host buffers: every decode uploads its query and
+    the new tail token (one contiguous copy each for K and V into a token-major tail buffer, read
+    in place by kvq_decode_attn_ex), and downloads its output; the block append reads the tail
+    the step uploaded."""
     stream = torch.cuda.current_stream()
+    BH = w.batch * w.n_kv_heads
     hq = q.cpu().pin_memory()
-    htk = tail_k.cpu().pin_memory()
-    htv = tail_v.cpu().pin_memory()
+    htk = tail_k.permute(2, 0, 1, 3).contiguous().cpu().pin_memory()   # token-major [127][B][H][128]
+    htv = tail_v.permute(2, 0, 1, 3).contiguous().cpu().pin_memory()
     hout = torch.empty((DECODES_PER_STEP, w.batch, w.n_q_heads, 128), dtype=torch.float32).pin_memory()
     dq = torch.empty_like(q)
-    dtk = torch.empty((w.batch, w.n_kv_heads, 128, 128), dtype=tail_k.dtype, device=dev)
+    dtk = torch.empty((128, w.batch, w.n_kv_heads, 128), dtype=tail_k.dtype, device=dev)
     dtv = torch.empty_like(dtk)
     out = torch.empty(w.batch, w.n_q_heads, 128, dtype=torch.float32, device=dev)
     ws = caches[0].workspace
@@ -395,19 +397,18 @@ def run_e2e(args, K, torch, dev, caches, cfg, w, nb, q, tail_k, tail_v, cache_by
             dq.copy_(hq, non_blocking=True)
             h2d += hq.numel() * hq.element_size()
             if d > 0:
-                dtk[:, :, d - 1].copy_(htk[:, :, d - 1], non_blocking=True)
-                dtv[:, :, d - 1].copy_(htv[:, :, d - 1], non_blocking=True)
-                h2d += 2 * htk[:, :, 0].numel() * htk.element_size()
+                dtk[d - 1].copy_(htk[d - 1], non_blocking=True)
+                dtv[d - 1].copy_(htv[d - 1], non_blocking=True)
+                h2d += 2 * htk[0].numel() * htk.element_size()
             c = caches[(i * DECODES_PER_STEP + d) % n_copies]
-            tk_ = dtk[:, :, :d].contiguous() if d else None
-            tv_ = dtv[:, :, :d].contiguous() if d else None
-            K.kvq_decode_attn(c.cache, dq, tk_, tv_, d, out, ws, stream)
+            K.kvq_decode_attn_ex(c.cache, dq, dtk if d else None, dtv if d else None, d, 128, BH * 128, out, ws,
+                                 stream)
             hout[d].copy_(out, non_blocking=True)
             d2h += out.numel() * 4
-        dtk[:, :, 127].copy_(htk[:, :, 0], non_blocking=True)
-        dtv[:, :, 127].copy_(htv[:, :, 0], non_blocking=True)
+        dtk[127].copy_(htk[0], non_blocking=True)
+        dtv[127].copy_(htv[0], non_blocking=True)
         c = caches[i % n_copies]
-        c.append(dtk, dtv, stream=stream)
+        c.append(dtk.permute(1, 2, 0, 3).contiguous(), dtv.permute(1, 2, 0, 3).contiguous(), stream=stream)
         K.kvq_truncate(c.cache, nb)
         torch.cuda.synchronize()
 

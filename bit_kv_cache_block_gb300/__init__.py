@@ -18,7 +18,7 @@ from ._lib import (KVQ_BF16, KVQ_F16, KVQ_INT4, KVQ_LAYOUT_MMA, KVQ_LAYOUT_ROWS,
 
 __all__ = ["make_config", "kvq_layout", "kvq_dense_kv_bytes", "kvq_cache_init", "kvq_append_block",
            "kvq_truncate", "kvq_reset", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
-           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_dequant", "kvq_error_stats", "kvq_error_topk",
+           "kvq_decode_attn", "kvq_decode_attn_ex", "kvq_decode_attn_static", "kvq_dequant", "kvq_error_stats", "kvq_error_topk",
            "kvq_error_topk_workspace_bytes", "error_topk", "kvq_status_str", "KVCache", "KVQError", "kvq_config",
            "kvq_layout_t", "kvq_cache", "lib_path"]
 
@@ -133,6 +133,15 @@ def kvq_decode_attn(cache: kvq_cache, q, tail_k, tail_v, n_tail: int, out, works
                "kvq_decode_attn")
 
 
+def kvq_decode_attn_ex(cache: kvq_cache, q, tail_k, tail_v, n_tail: int, bh_stride: int, token_stride: int, out,
+                       workspace, stream=None) -> None:
+    """kvq_decode_attn over tail buffers laid out by (b, h) and token strides, in elements."""
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _lib.check(_lib.lib().kvq_decode_attn_ex(C.byref(cache), _ptr(q), _ptr(tail_k), _ptr(tail_v), int(n_tail),
+                                             int(bh_stride), int(token_stride), _ptr(out), _ptr(workspace),
+                                             ws_bytes, _stream(stream)), "kvq_decode_attn_ex")
+
+
 def kvq_decode_attn_static(cache: kvq_cache, q, tail_k, tail_v, n_tail: int, out, stream=None) -> None:
     """kvq_decode_attn with the library's own fixed scratch instead of a caller workspace, for
     callers that cannot allocate device memory. Calls that may overlap on the GPU share that
@@ -220,16 +229,19 @@ class KVCache:
     def truncate(self, n_blocks: int):
         kvq_truncate(self.cache, n_blocks)
 
-    def decode(self, q, tail_k=None, tail_v=None, out=None, stream=None):
+    def decode(self, q, tail_k=None, tail_v=None, out=None, stream=None, n_tail=None):
+        """n_tail: tokens of the tail buffers to attend when they are allocated with a larger
+        capacity ([B][H_kv][capacity][128]); default: all of them."""
         import torch
         if out is None:
             out = torch.empty(q.shape[0], q.shape[1], 128, dtype=torch.float32, device=self.device)
-        n_tail = 0 if tail_k is None else int(tail_k.shape[2])
+        stride = 0 if tail_k is None else int(tail_k.shape[2])
+        n_tail = stride if n_tail is None else int(n_tail)
         need = kvq_decode_workspace_bytes(self.cfg, self.n_blocks)
         if self.workspace.numel() < need:
             self.workspace = torch.empty(need, dtype=torch.uint8, device=self.device)
-        kvq_decode_attn(self.cache, q, tail_k if n_tail else None, tail_v if n_tail else None, n_tail, out,
-                        self.workspace, stream)
+        kvq_decode_attn_ex(self.cache, q, tail_k if n_tail else None, tail_v if n_tail else None, n_tail,
+                           max(stride, n_tail) * 128, 128, out, self.workspace, stream)
         return out
 
     def dequant(self, first_block: int, n_blocks: int, domain: int = 0, stream=None):

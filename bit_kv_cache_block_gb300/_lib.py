@@ -24,7 +24,7 @@ METHODS = {"rtn": KVQ_RTN, "nuq": KVQ_NUQ, "varn": KVQ_VARN, "int4": KVQ_INT4}
 # every entry point declared in include/kvq.h
 EXPORTS = ["kvq_status_str", "kvq_dense_kv_bytes", "kvq_layout", "kvq_cache_init", "kvq_append_block",
            "kvq_truncate", "kvq_reset", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
-           "kvq_decode_attn", "kvq_decode_attn_static", "kvq_dequant", "kvq_calibrate_keys", "kvq_error_stats",
+           "kvq_decode_attn", "kvq_decode_attn_ex", "kvq_decode_attn_static", "kvq_dequant", "kvq_calibrate_keys", "kvq_error_stats",
            "kvq_error_topk_workspace_bytes", "kvq_error_topk"]
 
 
@@ -89,6 +89,8 @@ def lib() -> C.CDLL:
     L.kvq_decode_bytes.argtypes = [P(kvq_config), i32]
     L.kvq_decode_attn.restype = C.c_int
     L.kvq_decode_attn.argtypes = [P(kvq_cache), vp, vp, vp, i32, vp, vp, sz, vp]
+    L.kvq_decode_attn_ex.restype = C.c_int
+    L.kvq_decode_attn_ex.argtypes = [P(kvq_cache), vp, vp, vp, i32, C.c_int64, C.c_int64, vp, vp, sz, vp]
     L.kvq_decode_attn_static.restype = C.c_int
     L.kvq_decode_attn_static.argtypes = [P(kvq_cache), vp, vp, vp, i32, vp, vp]
     L.kvq_dequant.restype = C.c_int

@@ -8,7 +8,8 @@ cudaError_t kvq_launch_append(const kvq::Geo& g, const uint16_t* k, const uint16
                               uint8_t* base, const float* codebook, float* dbg, int* status, int varn_iters,
                               int hadamard, cudaStream_t st);
 cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const float* codebook, const uint16_t* q,
-                              const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, int n_blocks,
+                              const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, long long tail_bh,
+                              long long tail_tok, int n_blocks,
                               int n_split, float* ws, float* out, int* status, int hadamard, cudaStream_t st);
 size_t kvq_decode_ws_floats(const kvq::Geo& g, int n_blocks, int v1_splits);
 cudaError_t kvq_launch_dequant(const kvq::Geo& g, const uint8_t* base, const float* codebook, int first, int n,
@@ -267,9 +268,21 @@ uint64_t kvq_decode_bytes(const kvq_config* cfg, int32_t n_blocks) {
 kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const void* tail_k, const void* tail_v,
                            int32_t n_tail, float* out, void* workspace, size_t workspace_bytes,
                            cudaStream_t stream) {
+  return kvq_decode_attn_ex(cache, q, tail_k, tail_v, n_tail, (int64_t)n_tail * KVQ_HEAD_DIM, KVQ_HEAD_DIM, out,
+                            workspace, workspace_bytes, stream);
+}
+
+kvq_status kvq_decode_attn_ex(const kvq_cache* cache, const void* q, const void* tail_k, const void* tail_v,
+                              int32_t n_tail, int64_t tail_bh_stride, int64_t tail_token_stride, float* out,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (!cache || !cache->base || !q || !out) return KVQ_ERR_INVALID_ARG;
   if (check_config(&cache->cfg) != KVQ_OK) return KVQ_ERR_INVALID_ARG;
   if (n_tail < 0 || n_tail >= KVQ_BLOCK) return KVQ_ERR_INVALID_ARG;
+  if (n_tail > 0) {  // strides in elements, multiples of 8 (16-byte rows), within 2^40
+    if (tail_bh_stride < 0 || tail_token_stride < KVQ_HEAD_DIM) return KVQ_ERR_INVALID_ARG;
+    if (tail_bh_stride > ((int64_t)1 << 40) || tail_token_stride > ((int64_t)1 << 40)) return KVQ_ERR_INVALID_ARG;
+    if ((tail_bh_stride & 7) || (tail_token_stride & 7)) return KVQ_ERR_ALIGNMENT;
+  }
   if (n_tail > 0 && (!tail_k || !tail_v)) return KVQ_ERR_INVALID_ARG;
   const int nb = cache->n_blocks;
   if (nb + n_tail == 0) return KVQ_ERR_INVALID_ARG;
@@ -287,7 +300,8 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const void* ta
   return on_device(cache->device, [&]() {
     return kvq_launch_decode(g, static_cast<const uint8_t*>(cache->base), cache->codebook,
                              static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(tail_k),
-                             static_cast<const uint16_t*>(tail_v), n_tail, nb, S, static_cast<float*>(workspace),
+                             static_cast<const uint16_t*>(tail_v), n_tail, tail_bh_stride, tail_token_stride, nb, S,
+                             static_cast<float*>(workspace),
                              out, cache->dev_status, hadamard_of(cache->cfg), stream);
   });
 }
@@ -319,7 +333,8 @@ kvq_status kvq_decode_attn_static(const kvq_cache* cache, const void* q, const v
     }
     return kvq_launch_decode(g, static_cast<const uint8_t*>(cache->base), cache->codebook,
                              static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(tail_k),
-                             static_cast<const uint16_t*>(tail_v), n_tail, nb, S, ws, out, cache->dev_status,
+                             static_cast<const uint16_t*>(tail_v), n_tail, (long long)n_tail * kvq::D, kvq::D, nb, S,
+                             ws, out, cache->dev_status,
                              hadamard_of(cache->cfg), stream);
   });
   return s != KVQ_OK ? s : cap;

@@ -45,6 +45,8 @@ struct CombineArgs {
   const uint16_t* tail_k;
   const uint16_t* tail_v;
   int n_tail;
+  long long tail_bh;    // elements between the tail rows of consecutive (b, h)
+  long long tail_tok;   // elements between consecutive tokens of a tail row
   int n_blocks;
   int n_split;          // partial rows per (b, query head)
   long long ranges;     // > 0: partials come from the range-split tensor-core decode
@@ -430,12 +432,10 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
   }
   if (a.n_tail > 0) {  // the fp residual tail (< 128 tokens)
     const int nt = a.n_tail;
-    const uint16_t* tk = a.tail_k + ((uint64_t)b * g.H + h) * nt * D;
-    const uint16_t* tv = a.tail_v + ((uint64_t)b * g.H + h) * nt * D;
-    {
-      const uint32_t* tk2 = reinterpret_cast<const uint32_t*>(tk);  // channel pairs
-      for (int e = tid; e < nt * (D / 2); e += CB_THREADS) tkw[(e >> 6) * TK_STRIDE + (e & 63)] = tk2[e];
-    }
+    const uint16_t* tk = a.tail_k + ((uint64_t)b * g.H + h) * a.tail_bh;
+    const uint16_t* tv = a.tail_v + ((uint64_t)b * g.H + h) * a.tail_bh;
+    for (int e = tid; e < nt * (D / 2); e += CB_THREADS)  // channel pairs
+      tkw[(e >> 6) * TK_STRIDE + (e & 63)] = *reinterpret_cast<const uint32_t*>(tk + (e >> 6) * a.tail_tok + 2 * (e & 63));
     const float2* rope_blk = reinterpret_cast<const float2*>(a.base + g.rope_off);
     const float2* rope_loc = rope_blk + (size_t)(g.max_blocks + 1) * 64;
     if (grp == 0) {
@@ -495,11 +495,11 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
     for (; j + 3 * CB_GROUPS < nt; j += 4 * CB_GROUPS) {
       float vv[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) vv[k] = load_in(tv + (uint64_t)(j + k * CB_GROUPS) * D + c, g.in_bf16);
+      for (int k = 0; k < 4; ++k) vv[k] = load_in(tv + (uint64_t)(j + k * CB_GROUPS) * a.tail_tok + c, g.in_bf16);
 #pragma unroll
       for (int k = 0; k < 4; ++k) ov[k] = fmaf(sc[j + k * CB_GROUPS], vv[k], ov[k]);
     }
-    for (; j < nt; j += CB_GROUPS) ov[0] = fmaf(sc[j], load_in(tv + (uint64_t)j * D + c, g.in_bf16), ov[0]);
+    for (; j < nt; j += CB_GROUPS) ov[0] = fmaf(sc[j], load_in(tv + (uint64_t)j * a.tail_tok + c, g.in_bf16), ov[0]);
     __syncthreads();
     part[grp][c] = (ov[0] + ov[1]) + (ov[2] + ov[3]);
     __syncthreads();
@@ -644,7 +644,8 @@ DecodePlan plan_decode(const kvq::Geo& g, int n_blocks, int v1_splits) {
 }  // namespace
 
 cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const float* codebook, const uint16_t* q,
-                              const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, int n_blocks,
+                              const uint16_t* tail_k, const uint16_t* tail_v, int n_tail, long long tail_bh,
+                              long long tail_tok, int n_blocks,
                               int n_split, float* ws, float* out, int* status, int hadamard, cudaStream_t st) {
   using namespace kvq;
   const DecodePlan plan = plan_decode(g, n_blocks, n_split);
@@ -675,6 +676,8 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
   }
   CombineArgs c;
   c.g = g; c.base = base; c.q = q; c.tail_k = tail_k; c.tail_v = tail_v; c.n_tail = n_tail;
+  c.tail_bh = tail_bh;
+  c.tail_tok = tail_tok;
   c.n_blocks = n_blocks; c.n_split = (int)plan.rows; c.ranges = plan.ranges; c.per_range = plan.per_range;
   c.total = (long long)g.B * g.H * n_blocks;
   c.ws_m = ws_m; c.ws_l = ws_l; c.ws_o = ws_o; c.out = out; c.hadamard = hadamard;

@@ -269,6 +269,19 @@ kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const void* ta
                            const void* tail_v, int32_t n_tail, float* out, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
 
+/* kvq_decode_attn over tail buffers laid out by two strides (in elements): channel c of tail
+ * token t of (b, h) is at ((b * H_kv + h) * tail_bh_stride + t * tail_token_stride + c). A caller
+ * that keeps its tail in a buffer of fixed capacity, [B][H_kv][capacity][128] (bh stride
+ * capacity * 128, token stride 128) or token-major [capacity][B][H_kv][128] (bh stride 128, token
+ * stride B * H_kv * 128, so that each new token is one contiguous copy), decodes without
+ * repacking it. Both strides are multiples of 8 (KVQ_ERR_ALIGNMENT otherwise), the token stride
+ * is at least 128, both at most 2^40; rows must not overlap. kvq_decode_attn is this call with
+ * the packed strides (n_tail * 128, 128). */
+kvq_status kvq_decode_attn_ex(const kvq_cache* cache, const void* q, const void* tail_k,
+                              const void* tail_v, int32_t n_tail, int64_t tail_bh_stride,
+                              int64_t tail_token_stride, float* out, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
+
 /* Size of the decode scratch that the library itself holds for kvq_decode_attn_static:
  * one copy per GPU that loads the library, kept until the process exits. */
 #define KVQ_STATIC_WORKSPACE_BYTES (8u << 20)

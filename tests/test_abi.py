@@ -184,6 +184,13 @@ def test_host_argument_checks_launch_nothing(K):
     cache.n_blocks = 4
     assert lib.kvq_decode_attn(C.byref(cache), q, None, None, 128, out, ws, 1 << 20, None) == L.KVQ_ERR_INVALID_ARG
     assert lib.kvq_decode_attn(C.byref(cache), q, None, None, 3, out, ws, 1 << 20, None) == L.KVQ_ERR_INVALID_ARG
+    tk = C.c_void_p(0x9000)
+    ex = lib.kvq_decode_attn_ex
+    assert ex(C.byref(cache), q, tk, tk, 5, 640, 64, out, ws, 1 << 20, None) == L.KVQ_ERR_INVALID_ARG  # token < 128
+    assert ex(C.byref(cache), q, tk, tk, 5, -128, 128, out, ws, 1 << 20, None) == L.KVQ_ERR_INVALID_ARG
+    assert ex(C.byref(cache), q, tk, tk, 5, (1 << 40) + 8, 128, out, ws, 1 << 20, None) == L.KVQ_ERR_INVALID_ARG
+    assert ex(C.byref(cache), q, tk, tk, 5, 644, 128, out, ws, 1 << 20, None) == L.KVQ_ERR_ALIGNMENT
+    assert ex(C.byref(cache), q, tk, tk, 5, 640, 132, out, ws, 1 << 20, None) == L.KVQ_ERR_ALIGNMENT
     assert lib.kvq_decode_attn(C.byref(cache), q, None, None, 0, out, ws, 16, None) == L.KVQ_ERR_CAPACITY
     assert lib.kvq_decode_attn(C.byref(cache), C.c_void_p(0x1004), None, None, 0, out, ws, 1 << 20, None) \
         == L.KVQ_ERR_ALIGNMENT

@@ -309,3 +309,31 @@ def test_decode_is_deterministic(name, base, kw, tails, layout):
     torch.cuda.synchronize()
     assert cache.device_status() == 0
     assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2]), name
+
+
+@pytest.mark.parametrize("name,cfg_id,kw", [("nuq3_rope", 2, dict(batch=2, n_kv_heads=2, n_q_heads=2, ctx=3 * 128)),
+                                            ("varn2_gqa", 3, dict(batch=2, n_kv_heads=2, n_q_heads=8, ctx=2 * 128))])
+def test_decode_tail_capacity_buffers(name, cfg_id, kw):
+    """kvq_decode_attn_ex over tail buffers of capacity 127 tokens (per-(b, h) rows, and token-major),
+    n_tail of them in use, equals the decode over the same tokens packed contiguously, bit for bit."""
+    import torch
+    w = WL.WORKLOADS[cfg_id].scaled(**kw)
+    cache = U.new_cache(w, layout="mma")
+    K, V = WL.blocks(w, 0, w.n_blocks)
+    cache.append(U.to_device(K, w.dtype), U.to_device(V, w.dtype))
+    q = U.to_device(WL.query(w), w.dtype)
+    tk, tv = WL.tail(w, 127)
+    dk, dv = U.to_device(tk, w.dtype), U.to_device(tv, w.dtype)
+    import bit_kv_cache_block_gb300 as K
+    tok_k = dk.permute(2, 0, 1, 3).contiguous()  # token-major [127][B][H][128]
+    tok_v = dv.permute(2, 0, 1, 3).contiguous()
+    for n_tail in (1, 37, 127):
+        a = cache.decode(q, dk, dv, n_tail=n_tail).cpu().numpy()
+        b = cache.decode(q, dk[:, :, :n_tail].contiguous(), dv[:, :, :n_tail].contiguous()).cpu().numpy()
+        assert np.array_equal(a, b), f"{name} n_tail={n_tail}"
+        c = torch.empty(q.shape[0], q.shape[1], 128, dtype=torch.float32, device="cuda")
+        K.kvq_decode_attn_ex(cache.cache, q, tok_k, tok_v, n_tail, 128, w.batch * w.n_kv_heads * 128, c,
+                             cache.workspace)
+        assert np.array_equal(a, c.cpu().numpy()), f"{name} token-major n_tail={n_tail}"
+    torch.cuda.synchronize()
+    assert cache.device_status() == 0
