@@ -48,12 +48,12 @@ BENCH_LAYOUT = "mma"
 PROFILED_TRAFFIC = {
     2: {"bytes_per_record": 14867.6, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
         "sha256_16": "9fc7b31bdc440fab", "capture": "same workload at L = 16384 (4096 records)"},
-    3: {"bytes_per_record": 9783.2, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "009d5ee3f8020a06", "capture": "full workload (8192 records)"},
-    4: {"bytes_per_record": 17076.7, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "009d5ee3f8020a06", "capture": "same workload at L = 4096 (8192 records)"},
-    5: {"bytes_per_record": 9285.9, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "009d5ee3f8020a06", "capture": "same workload at L = 65536 (16384 records)"},
+    3: {"bytes_per_record": 9789.4, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "285b5a378333c7f9", "capture": "full workload (8192 records)"},
+    4: {"bytes_per_record": 17094.0, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "285b5a378333c7f9", "capture": "same workload at L = 4096 (8192 records)"},
+    5: {"bytes_per_record": 9276.4, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "285b5a378333c7f9", "capture": "same workload at L = 65536 (16384 records)"},
 }
 
 
