@@ -372,20 +372,27 @@ def run_kvq(args):
 
 
 def run_e2e(args, K, torch, dev, caches, cfg, w, nb, q, tail_k, tail_v, cache_bytes):
-    """Same step through the C ABI from pinned host buffers: every decode uploads its query and
-    the new tail token (one contiguous copy each for K and V into a token-major tail buffer, read
-    in place by kvq_decode_attn_ex), and downloads its output; the block append reads the tail
-    the step uploaded."""
+    """Same step through the C ABI from pinned host buffers. Row d of one staging buffer holds
+    decode d's query and the tail token it adds (K and V), so each decode uploads one contiguous
+    row; kvq_decode_attn_ex reads the tail in place through a token stride of one row (token t
+    sits in row t + 1). The 128 outputs of the step come back in one copy, and the block append
+    reads the step's tail."""
     stream = torch.cuda.current_stream()
     BH = w.batch * w.n_kv_heads
-    hq = q.cpu().pin_memory()
-    htk = tail_k.permute(2, 0, 1, 3).contiguous().cpu().pin_memory()   # token-major [127][B][H][128]
-    htv = tail_v.permute(2, 0, 1, 3).contiguous().cpu().pin_memory()
-    hout = torch.empty((DECODES_PER_STEP, w.batch, w.n_q_heads, 128), dtype=torch.float32).pin_memory()
-    dq = torch.empty_like(q)
-    dtk = torch.empty((128, w.batch, w.n_kv_heads, 128), dtype=tail_k.dtype, device=dev)
-    dtv = torch.empty_like(dtk)
-    out = torch.empty(w.batch, w.n_q_heads, 128, dtype=torch.float32, device=dev)
+    nq, nkv = q.numel(), BH * 128
+    row = nq + 2 * nkv                                   # elements per staging row
+    hbuf = torch.empty((DECODES_PER_STEP + 1, row), dtype=q.dtype).pin_memory()
+    tk_tok = tail_k.permute(2, 0, 1, 3).reshape(127, nkv).cpu()   # token-major
+    tv_tok = tail_v.permute(2, 0, 1, 3).reshape(127, nkv).cpu()
+    for d in range(DECODES_PER_STEP + 1):
+        hbuf[d, :nq] = q.reshape(-1).cpu()
+        if d > 0:
+            t = (d - 1) % 127
+            hbuf[d, nq:nq + nkv] = tk_tok[t]
+            hbuf[d, nq + nkv:] = tv_tok[t]
+    dbuf = torch.empty((DECODES_PER_STEP + 1, row), dtype=q.dtype, device=dev)
+    outs = torch.empty((DECODES_PER_STEP, w.batch, w.n_q_heads, 128), dtype=torch.float32, device=dev)
+    hout = torch.empty_like(outs, device="cpu").pin_memory()
     ws = caches[0].workspace
     n_copies = len(caches)
     h2d = d2h = 0
@@ -394,21 +401,21 @@ def run_e2e(args, K, torch, dev, caches, cfg, w, nb, q, tail_k, tail_v, cache_by
         nonlocal h2d, d2h
         h2d = d2h = 0
         for d in range(DECODES_PER_STEP):
-            dq.copy_(hq, non_blocking=True)
-            h2d += hq.numel() * hq.element_size()
-            if d > 0:
-                dtk[d - 1].copy_(htk[d - 1], non_blocking=True)
-                dtv[d - 1].copy_(htv[d - 1], non_blocking=True)
-                h2d += 2 * htk[0].numel() * htk.element_size()
+            dbuf[d].copy_(hbuf[d], non_blocking=True)
+            h2d += hbuf[d].numel() * hbuf.element_size()
             c = caches[(i * DECODES_PER_STEP + d) % n_copies]
-            K.kvq_decode_attn_ex(c.cache, dq, dtk if d else None, dtv if d else None, d, 128, BH * 128, out, ws,
-                                 stream)
-            hout[d].copy_(out, non_blocking=True)
-            d2h += out.numel() * 4
-        dtk[127].copy_(htk[0], non_blocking=True)
-        dtv[127].copy_(htv[0], non_blocking=True)
+            qd = dbuf[d, :nq].view(q.shape)
+            tk_ = dbuf[1, nq:] if d else None                  # K token t in row t + 1
+            tv_ = dbuf[1, nq + nkv:] if d else None
+            K.kvq_decode_attn_ex(c.cache, qd, tk_, tv_, d, 128, row, outs[d], ws, stream)
+        dbuf[DECODES_PER_STEP].copy_(hbuf[DECODES_PER_STEP], non_blocking=True)  # the token completing the block
+        h2d += hbuf[DECODES_PER_STEP].numel() * hbuf.element_size()
+        hout.copy_(outs, non_blocking=True)
+        d2h += outs.numel() * 4
+        kt = dbuf[1:, nq:nq + nkv].view(128, w.batch, w.n_kv_heads, 128).permute(1, 2, 0, 3).contiguous()
+        vt = dbuf[1:, nq + nkv:].view(128, w.batch, w.n_kv_heads, 128).permute(1, 2, 0, 3).contiguous()
         c = caches[i % n_copies]
-        c.append(dtk.permute(1, 2, 0, 3).contiguous(), dtv.permute(1, 2, 0, 3).contiguous(), stream=stream)
+        c.append(kt, vt, stream=stream)
         K.kvq_truncate(c.cache, nb)
         torch.cuda.synchronize()
 
