@@ -83,14 +83,15 @@ __global__ void __launch_bounds__(DQ_THREADS) dequant_kernel(DequantArgs a) {
 }
 
 // Per-token error statistics ([KVN] key innovation: |x - x_dq|^2 = E_M + E_D). grid (n, H, B*2),
-// ES_THREADS threads, one instantiation per (method, bits). The tile's part of the record (codes,
-// metadata, CSR) is copied into shared memory; value tiles stored as channel rows get a row
-// stride of W + 1 words (odd), so the 32 channels a warp reads at once sit in 32 banks. Then warp
-// w takes token rows w, w + 8, ...: lane l holds channels l + 32j (j = 0..3), dequantises them
-// (per-channel scales kept in registers), applies the row's CSR entries and, for KVarN, the
-// inverse Hadamard transform (distances 1 .. 16 across lanes, 32 and 64 inside the lane), and
-// the sums close with xor shuffles.
+// ES_THREADS threads, one instantiation per (method, bits). The tile's part of the record
+// (codes, metadata, CSR) is copied into shared memory and its codes are unpacked once into a
+// token-major byte tile (value channel rows are transposed on the way). Then 8 lanes take one
+// token row: lane j holds channels 16j .. 16j+15, reads their codes with one 16-byte load and
+// the input with two, dequantises (per-channel scales in registers), adds the row's CSR entries,
+// applies the inverse Hadamard transform for KVarN (distances 1..8 inside the lane, 16..64
+// across the 8 lanes), and the sums close over the 8 lanes; a warp finishes 4 rows at a time.
 constexpr int ES_THREADS = 256;
+constexpr int ES_BROW = D + 16;  // bytes per token row of the unpacked code tile
 
 struct ErrArgs {
   Geo g;
@@ -105,22 +106,10 @@ struct ErrArgs {
   int* status;
 };
 
-template <int BITS>
-struct EsGeom {
-  static constexpr int NWC = 32 / BITS;             // codes per word
-  static constexpr int W = (D + NWC - 1) / NWC;     // words per row
-  static constexpr uint32_t MASK = (1u << BITS) - 1u;
-};
-
-// Shared-memory bytes of the staged code region (channel rows padded to W + 1 words).
-template <int BITS>
-__host__ __device__ inline uint32_t es_codes_bytes(bool padded, uint32_t plain_bytes) {
-  return padded ? (uint32_t)round16((uint64_t)T * (EsGeom<BITS>::W + 1) * 4) : plain_bytes;
-}
-
 template <int METHOD, int BITS>
 __global__ void __launch_bounds__(ES_THREADS) error_stats_kernel(ErrArgs a) {
-  using E = EsGeom<BITS>;
+  constexpr int NWC = 32 / BITS, W = (D + NWC - 1) / NWC;
+  constexpr uint32_t MASK = (1u << BITS) - 1u;
   extern __shared__ __align__(16) uint8_t es_smem[];
   const Geo& g = a.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -130,126 +119,144 @@ __global__ void __launch_bounds__(ES_THREADS) error_stats_kernel(ErrArgs a) {
   if (!in || !st) return;
   const int blk = a.first + bi;
   const uint8_t* rec = a.base + record_offset(g, b, h, blk, a.status);
-  const bool planes = BITS == 3 && g.planes3;
-  const bool chrows = kind == 1 && g.vrows_ch && !planes;  // value codes as channel rows
-  const uint32_t off = g.codes_off[kind], moff = g.meta_off[kind];
-  const uint32_t end = kind ? (uint32_t)g.rec_bytes : g.codes_off[1];
-  const uint32_t cbytes = es_codes_bytes<BITS>(chrows, moff - off);
+  const uint32_t off = g.codes_off[kind], end = kind ? (uint32_t)g.rec_bytes : g.codes_off[1];
+  uint8_t* ctile = es_smem;                                   // [128 tokens][ES_BROW] codes
+  uint8_t* part = es_smem + T * ES_BROW;                      // the record's part of this kind
   {
-    if (chrows) {  // row r (channel) at word r * (W + 1)
-      const uint32_t* src = reinterpret_cast<const uint32_t*>(rec + off);
-      uint32_t* dst = reinterpret_cast<uint32_t*>(es_smem);
-      for (int i = tid; i < T * E::W; i += ES_THREADS) dst[(i / E::W) * (E::W + 1) + i % E::W] = src[i];
-    } else {
-      const uint4* src = reinterpret_cast<const uint4*>(rec + off);
-      uint4* dst = reinterpret_cast<uint4*>(es_smem);
-      for (uint32_t i = tid; i < (moff - off) / 16; i += ES_THREADS) dst[i] = src[i];
-    }
-    const uint4* src = reinterpret_cast<const uint4*>(rec + moff);  // metadata and CSR
-    uint4* dst = reinterpret_cast<uint4*>(es_smem + cbytes);
-    for (uint32_t i = tid; i < (end - moff) / 16; i += ES_THREADS) dst[i] = src[i];
+    const uint4* src = reinterpret_cast<const uint4*>(rec + off);
+    uint4* dst = reinterpret_cast<uint4*>(part);
+    for (uint32_t i = tid; i < (end - off) / 16; i += ES_THREADS) dst[i] = src[i];
   }
-  const uint32_t* codes = reinterpret_cast<const uint32_t*>(es_smem);
-  const uint16_t* m = reinterpret_cast<const uint16_t*>(es_smem + cbytes);
   __shared__ float cb[16];  // nuq codebook of this head
   if (METHOD == KVQ_NUQ && tid < (1 << BITS)) cb[tid] = a.codebook[h * (1 << BITS) + tid];
   __syncthreads();
-  // per-channel metadata of the lane's channels l + 32j (keys: s, z or zp; values: s1)
-  float cs[4], cz[4];
+  const uint32_t* codes = reinterpret_cast<const uint32_t*>(part);
+  const uint16_t* m = reinterpret_cast<const uint16_t*>(part + (g.meta_off[kind] - off));
+  if (BITS == 3 && g.planes3) {  // bit planes: element by element
+    for (int e = tid; e < TILE; e += ES_THREADS) {
+      const int t = e >> 7, c = e & 127;
+      ctile[t * ES_BROW + c] = (uint8_t)tile3_code(codes, kind, t, c);
+    }
+  } else {
+    const bool chrows = kind == 1 && g.vrows_ch;  // value codes stored as channel rows
+    for (int i = tid; i < T * W; i += ES_THREADS) {
+      const int r = i / W, w = i - r * W;
+      const uint32_t word = codes[i];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int c = lane + 32 * j;
-    cs[j] = 1.0f;
-    cz[j] = 0.0f;
+      for (int j = 0; j < NWC; ++j) {
+        const int pos = w * NWC + j;
+        if (pos < D) {
+          const uint8_t q = (uint8_t)((word >> (BITS * j)) & MASK);
+          if (chrows) ctile[pos * ES_BROW + r] = q;  // row r = channel, pos = token
+          else ctile[r * ES_BROW + pos] = q;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int sub = lane >> 3, j8 = lane & 7, c0 = 16 * j8;  // row within the warp's 4, channel group
+  // per-channel metadata of the lane's 16 channels (keys: s, z or zp; values: s1)
+  float cs[16], cz[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    cs[i] = 1.0f;
+    cz[i] = 0.0f;
     if (kind == 0 && METHOD != KVQ_INT4) {
-      cs[j] = h2f(m[c]);
-      cz[j] = h2f(m[T + c]);
+      cs[i] = h2f(m[c0 + i]);
+      cz[i] = h2f(m[T + c0 + i]);
     } else if (kind == 1 && METHOD == KVQ_VARN) {
-      cs[j] = h2f(m[2 * T + c]);  // s1 per channel
+      cs[i] = h2f(m[2 * T + c0 + i]);  // s1 per channel
     }
   }
   const bool to_input = METHOD == KVQ_VARN && a.hadamard;
   const uint64_t tok0 = ((uint64_t)b * g.H + h) * (uint64_t)a.n * T + (uint64_t)bi * T;
-  for (int t = warp; t < T; t += ES_THREADS / 32) {
-    const uint16_t* xr = in + (tok0 + t) * D + lane;
-    float x[4], q[4];
+  for (int t = 4 * warp + sub; t < T; t += 4 * (ES_THREADS / 32)) {
+    float x[16], q[16];
+    {
+      const uint4* xp = reinterpret_cast<const uint4*>(in + (tok0 + t) * D + c0);
+      const uint4 x0 = xp[0], x1 = xp[1];
+      const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) x[j] = in_bits_to_f32(xr[32 * j], g.in_bf16);
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = in_bits_to_f32((uint16_t)(xw[i] & 0xffffu), g.in_bf16);
+        x[2 * i + 1] = in_bits_to_f32((uint16_t)(xw[i] >> 16), g.in_bf16);
+      }
+    }
     if (g.sink && blk == 0 && t == 0) {  // the kept first token: what decode attends
       const uint16_t* kept =
-          reinterpret_cast<const uint16_t*>(a.base + g.sink_off) + (((uint64_t)b * g.H + h) * 2 + kind) * D + lane;
+          reinterpret_cast<const uint16_t*>(a.base + g.sink_off) + (((uint64_t)b * g.H + h) * 2 + kind) * D + c0;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) q[j] = in_bits_to_f32(kept[32 * j], g.in_bf16);
+      for (int i = 0; i < 16; ++i) q[i] = in_bits_to_f32(kept[i], g.in_bf16);
     } else {
+      const uint4 cw = *reinterpret_cast<const uint4*>(ctile + t * ES_BROW + c0);
+      const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
       // per-token metadata of this row (values: s, z or zp; keys: KVarN s1; absmax: s per block)
-      const float ts0 = (kind == 1 || METHOD == KVQ_INT4) ? h2f(m[t]) : 1.0f;
-      const float ts1 = (METHOD == KVQ_INT4 && g.g64) ? h2f(m[T + t]) : ts0;  // channels 64..127
+      const float ts = (kind == 1 || METHOD == KVQ_INT4) ? h2f(m[(METHOD == KVQ_INT4 && g.g64 && c0 >= 64 ? T : 0) + t])
+                                                         : 1.0f;
       const float tz = (kind == 1 && METHOD != KVQ_INT4) ? h2f(m[T + t]) : 0.0f;
       const float tk1 = (kind == 0 && METHOD == KVQ_VARN) ? h2f(m[2 * T + t]) : 1.0f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int c = lane + 32 * j;
-        uint32_t code;
-        if (planes) code = tile3_code(codes, kind, t, c);
-        else if (chrows) code = (codes[c * (E::W + 1) + t / E::NWC] >> (BITS * (t % E::NWC))) & E::MASK;
-        else code = (codes[t * E::W + c / E::NWC] >> (BITS * (c % E::NWC))) & E::MASK;
-        const float ts = j < 2 ? ts0 : ts1;
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t code = (cws[i >> 2] >> (8 * (i & 3))) & 0xffu;
         float v;
         if (METHOD == KVQ_RTN || METHOD == KVQ_VARN) {
-          v = kind == 0 ? ((float)code + cz[j]) * cs[j] : ((float)code + tz) * ts;
-          if (METHOD == KVQ_VARN) v *= kind == 0 ? tk1 : cs[j];
+          v = kind == 0 ? ((float)code + cz[i]) * cs[i] : ((float)code + tz) * ts;
+          if (METHOD == KVQ_VARN) v *= kind == 0 ? tk1 : cs[i];
         } else if (METHOD == KVQ_INT4) {
           constexpr int SH = 32 - BITS;
           v = (float)((int)(code << SH) >> SH) * ts;
         } else {
-          v = kind == 0 ? cb[code] * cs[j] + cz[j] : cb[code] * ts + tz;
+          v = kind == 0 ? cb[code] * cs[i] + cz[i] : cb[code] * ts + tz;
         }
-        q[j] = v;
+        q[i] = v;
       }
       if (METHOD == KVQ_NUQ && g.n_out > 0) {  // this row's outliers (few): the owning lane adds
-        const uint8_t* csr = es_smem + cbytes + (g.csr_off[kind] - moff);
+        const uint8_t* csr = part + (g.csr_off[kind] - off);
         const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
         const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * g.n_out);
         const uint8_t* col = csr + 2 * g.n_out + 2 * (T + 1);
         const int e1 = min((int)rp[t + 1], g.n_out);
         for (int e = min((int)rp[t], g.n_out); e < e1; ++e) {
           const int c = col[e] & (D - 1);
-          if ((c & 31) == lane) {
-            const float vv = h2f(val[e]);
+          const float vv = (c >> 4) == j8 ? h2f(val[e]) : 0.0f;
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if ((c >> 5) == j) q[j] += vv;
-          }
+          for (int i = 0; i < 16; ++i) q[i] += (c & 15) == i ? vv : 0.0f;  // no indexed register
         }
       }
       if (to_input) {  // inverse Hadamard (H / sqrt(128) is its own inverse), Sylvester order
 #pragma unroll
-        for (int hl = 1; hl < 32; hl <<= 1) {  // channel distance hl: across lanes
-          const bool upper = lane & hl;
+        for (int d = 1; d < 16; d <<= 1)  // distances 1..8: inside the lane
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const float o = __shfl_xor_sync(0xffffffffu, q[j], hl);
-            q[j] = upper ? o - q[j] : q[j] + o;
+          for (int i = 0; i < 16; ++i)
+            if (!(i & d)) {
+              const float u0 = q[i], u1 = q[i + d];
+              q[i] = u0 + u1;
+              q[i + d] = u0 - u1;
+            }
+#pragma unroll
+        for (int dl = 1; dl < 8; dl <<= 1) {  // distances 16, 32, 64: across the row's 8 lanes
+          const bool upper = j8 & dl;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, q[i], dl);
+            q[i] = upper ? o - q[i] : q[i] + o;
           }
         }
-        const float y0 = q[0] + q[1], y1 = q[0] - q[1], y2 = q[2] + q[3], y3 = q[2] - q[3];  // distance 32
-        q[0] = (y0 + y2) * 0.08838834764831845f;  // distance 64
-        q[2] = (y0 - y2) * 0.08838834764831845f;
-        q[1] = (y1 + y3) * 0.08838834764831845f;
-        q[3] = (y1 - y3) * 0.08838834764831845f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q[i] *= 0.08838834764831845f;
       }
     }
     float sxx = 0.0f, sqq = 0.0f, sdd = 0.0f, spm = 0.0f;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float dd = x[j] - q[j];
-      sxx = fmaf(x[j], x[j], sxx);
-      sqq = fmaf(q[j], q[j], sqq);
+    for (int i = 0; i < 16; ++i) {
+      const float dd = x[i] - q[i];
+      sxx = fmaf(x[i], x[i], sxx);
+      sqq = fmaf(q[i], q[i], sqq);
       sdd = fmaf(dd, dd, sdd);
-      spm = fmaf(q[j] - x[j], q[j] + x[j], spm);
+      spm = fmaf(q[i] - x[i], q[i] + x[i], spm);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
+    for (int o = 1; o < 8; o <<= 1) {
       sxx += __shfl_xor_sync(0xffffffffu, sxx, o);
       sqq += __shfl_xor_sync(0xffffffffu, sqq, o);
       sdd += __shfl_xor_sync(0xffffffffu, sdd, o);
@@ -257,20 +264,18 @@ __global__ void __launch_bounds__(ES_THREADS) error_stats_kernel(ErrArgs a) {
     }
     const float nx = sqrtf(sxx), nq = sqrtf(sqq);
     const float dn = nx + nq > 0.0f ? spm / (nx + nq) : 0.0f;
-    float ed = 0.0f;
-    if (nx > 0.0f && nq > 0.0f) {  // warp-uniform
-      const float ix = 1.0f / nx, iq = 1.0f / nq;
-      float su = 0.0f;
+    float su = 0.0f;
+    const bool both = nx > 0.0f && nq > 0.0f;  // uniform over the row's 8 lanes
+    const float ix = both ? 1.0f / nx : 0.0f, iq = both ? 1.0f / nq : 0.0f;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float u = __fsub_rn(__fmul_rn(x[j], ix), __fmul_rn(q[j], iq));  // 0 when x_dq = x
-        su = fmaf(u, u, su);
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
-      ed = nx * nq * su;
+    for (int i = 0; i < 16; ++i) {
+      const float u = __fsub_rn(__fmul_rn(x[i], ix), __fmul_rn(q[i], iq));  // 0 when x_dq = x
+      su = fmaf(u, u, su);
     }
-    if (lane == 0) reinterpret_cast<float4*>(st)[tok0 + t] = make_float4(nx, dn, sdd, ed);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
+    const float ed = both ? nx * nq * su : 0.0f;
+    if (j8 == 0) reinterpret_cast<float4*>(st)[tok0 + t] = make_float4(nx, dn, sdd, ed);
   }
 }
 
@@ -310,9 +315,9 @@ cudaError_t kvq_launch_error_stats(const kvq::Geo& g, const uint8_t* base, const
   kvq::ErrArgs a;
   a.g = g; a.base = base; a.codebook = codebook; a.first = first; a.n = n; a.hadamard = hadamard;
   a.in_k = in_k; a.in_v = in_v; a.st_k = st_k; a.st_v = st_v; a.status = status;
-  // largest staged region: a kind's record part, plus the padding of value channel rows
+  // the unpacked code tile, then the larger of the two kinds' record parts
   const uint32_t kb = g.codes_off[1] - g.codes_off[0], vb = (uint32_t)g.rec_bytes - g.codes_off[1];
-  const int smem = (int)(kb > vb ? kb : vb) + (int)kvq::round16((uint64_t)kvq::T * 4) + 16;
+  const int smem = kvq::T * kvq::ES_BROW + (int)(kb > vb ? kb : vb);
   using Fn = void (*)(kvq::ErrArgs);
   Fn fn = nullptr;
   const int m = g.method, b = g.bits;
