@@ -83,9 +83,10 @@ __global__ void __launch_bounds__(DQ_THREADS) dequant_kernel(DequantArgs a) {
 }
 
 // Per-token error statistics ([KVN] key innovation: |x - x_dq|^2 = E_M + E_D). grid (n, H, B*2),
-// ES_THREADS threads, one instantiation per (method, bits). The tile's part of the record
-// (codes, metadata, CSR) is copied into shared memory and its codes are unpacked once into a
-// token-major byte tile (value channel rows are transposed on the way). Then 8 lanes take one
+// ES_THREADS threads, one instantiation per (method, bits). Two bulk copies bring the tile's
+// 32 KB of input rows and its part of the record (codes, metadata, CSR) into shared memory; the
+// codes are unpacked once into a token-major byte tile (value channel rows are transposed on the
+// way). Then 8 lanes take one
 // token row: lane j holds channels 16j .. 16j+15, reads their codes with one 16-byte load and
 // the input with two, dequantises (per-channel scales in registers), adds the row's CSR entries,
 // applies the inverse Hadamard transform for KVarN (distances 1..8 inside the lane, 16..64
@@ -107,7 +108,7 @@ struct ErrArgs {
 };
 
 template <int METHOD, int BITS>
-__global__ void __launch_bounds__(ES_THREADS) error_stats_kernel(ErrArgs a) {
+__global__ void __launch_bounds__(ES_THREADS, 2) error_stats_kernel(ErrArgs a) {
   constexpr int NWC = 32 / BITS, W = (D + NWC - 1) / NWC;
   constexpr uint32_t MASK = (1u << BITS) - 1u;
   extern __shared__ __align__(16) uint8_t es_smem[];
@@ -120,16 +121,25 @@ __global__ void __launch_bounds__(ES_THREADS) error_stats_kernel(ErrArgs a) {
   const int blk = a.first + bi;
   const uint8_t* rec = a.base + record_offset(g, b, h, blk, a.status);
   const uint32_t off = g.codes_off[kind], end = kind ? (uint32_t)g.rec_bytes : g.codes_off[1];
-  uint8_t* ctile = es_smem;                                   // [128 tokens][ES_BROW] codes
-  uint8_t* part = es_smem + T * ES_BROW;                      // the record's part of this kind
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(rec + off);
-    uint4* dst = reinterpret_cast<uint4*>(part);
-    for (uint32_t i = tid; i < (end - off) / 16; i += ES_THREADS) dst[i] = src[i];
-  }
+  const uint64_t tok0 = ((uint64_t)b * g.H + h) * (uint64_t)a.n * T + (uint64_t)bi * T;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(es_smem);        // [128 tokens][128] input rows
+  uint8_t* ctile = es_smem + TILE * 2;                        // [128 tokens][ES_BROW] codes
+  uint8_t* part = ctile + T * ES_BROW;                        // the record's part of this kind
+  __shared__ uint64_t landed;
   __shared__ float cb[16];  // nuq codebook of this head
+  if (tid == 0) {
+    mbar_init(&landed, 1);
+    fence_mbar_init();
+  }
   if (METHOD == KVQ_NUQ && tid < (1 << BITS)) cb[tid] = a.codebook[h * (1 << BITS) + tid];
   __syncthreads();
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&landed, (uint32_t)(TILE * 2) + (end - off));
+    bulk_g2s(xs, in + tok0 * D, (uint32_t)(TILE * 2), &landed);
+    bulk_g2s(part, rec + off, end - off, &landed);
+  }
+  const bool got = mbar_wait_bounded(&landed, 0u, a.status);
+  if (__syncthreads_or(!got)) return;  // every thread leaves together
   const uint32_t* codes = reinterpret_cast<const uint32_t*>(part);
   const uint16_t* m = reinterpret_cast<const uint16_t*>(part + (g.meta_off[kind] - off));
   if (BITS == 3 && g.planes3) {  // bit planes: element by element
@@ -169,11 +179,10 @@ __global__ void __launch_bounds__(ES_THREADS) error_stats_kernel(ErrArgs a) {
     }
   }
   const bool to_input = METHOD == KVQ_VARN && a.hadamard;
-  const uint64_t tok0 = ((uint64_t)b * g.H + h) * (uint64_t)a.n * T + (uint64_t)bi * T;
   for (int t = 4 * warp + sub; t < T; t += 4 * (ES_THREADS / 32)) {
     float x[16], q[16];
     {
-      const uint4* xp = reinterpret_cast<const uint4*>(in + (tok0 + t) * D + c0);
+      const uint4* xp = reinterpret_cast<const uint4*>(xs + t * D + c0);
       const uint4 x0 = xp[0], x1 = xp[1];
       const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
@@ -317,7 +326,7 @@ cudaError_t kvq_launch_error_stats(const kvq::Geo& g, const uint8_t* base, const
   a.in_k = in_k; a.in_v = in_v; a.st_k = st_k; a.st_v = st_v; a.status = status;
   // the unpacked code tile, then the larger of the two kinds' record parts
   const uint32_t kb = g.codes_off[1] - g.codes_off[0], vb = (uint32_t)g.rec_bytes - g.codes_off[1];
-  const int smem = kvq::T * kvq::ES_BROW + (int)(kb > vb ? kb : vb);
+  const int smem = kvq::TILE * 2 + kvq::T * kvq::ES_BROW + (int)(kb > vb ? kb : vb);
   using Fn = void (*)(kvq::ErrArgs);
   Fn fn = nullptr;
   const int m = g.method, b = g.bits;
