@@ -82,17 +82,16 @@ __global__ void __launch_bounds__(DQ_THREADS) dequant_kernel(DequantArgs a) {
   for (int e = t; e < TILE; e += DQ_THREADS) dst[e] = xs[(e >> 7) * 129 + (e & 127)];
 }
 
-// Per-token error statistics ([KVN] key innovation: |x - x_dq|^2 = E_M + E_D). One persistent
-// CTA per SM, ES_THREADS threads, one instantiation per (method, bits); the CTA walks its share of
-// the tiles (b, h, block, K|V) with a two-stage ring: two bulk copies bring a tile's 32 KB of
-// input rows and its part of the record (codes, metadata, CSR) into one stage while the other
-// stage is processed. The codes are unpacked into a token-major byte tile (value channel rows
-// transposed on the way). Then 8 lanes take one token row: lane j holds channels 16j .. 16j+15,
-// reads their codes with one 16-byte load and the input with two, dequantises (per-channel
-// scales in registers), adds the row's CSR entries, applies the inverse Hadamard transform for
-// KVarN (distances 1..8 inside the lane, 16..64 across the 8 lanes), and the sums close over the
-// 8 lanes; a warp finishes 4 rows at a time.
-constexpr int ES_THREADS = 512;
+// Per-token error statistics ([KVN] key innovation: |x - x_dq|^2 = E_M + E_D). grid (n, H, B*2),
+// ES_THREADS threads, one instantiation per (method, bits). Two bulk copies bring the tile's
+// 32 KB of input rows and its part of the record (codes, metadata, CSR) into shared memory; the
+// codes are unpacked once into a token-major byte tile (value channel rows are transposed on the
+// way). Then 8 lanes take one
+// token row: lane j holds channels 16j .. 16j+15, reads their codes with one 16-byte load and
+// the input with two, dequantises (per-channel scales in registers), adds the row's CSR entries,
+// applies the inverse Hadamard transform for KVarN (distances 1..8 inside the lane, 16..64
+// across the 8 lanes), and the sums close over the 8 lanes; a warp finishes 4 rows at a time.
+constexpr int ES_THREADS = 256;
 constexpr int ES_BROW = D + 16;  // bytes per token row of the unpacked code tile
 
 struct ErrArgs {
@@ -106,222 +105,186 @@ struct ErrArgs {
   float* st_k;
   float* st_v;
   int* status;
-  uint32_t part_bytes;  // the larger of the K and V parts of a record (a stage's record buffer)
 };
 
 template <int METHOD, int BITS>
-__global__ void __launch_bounds__(ES_THREADS, 1) error_stats_kernel(ErrArgs a) {
+__global__ void __launch_bounds__(ES_THREADS, 2) error_stats_kernel(ErrArgs a) {
   constexpr int NWC = 32 / BITS, W = (D + NWC - 1) / NWC;
   constexpr uint32_t MASK = (1u << BITS) - 1u;
   extern __shared__ __align__(16) uint8_t es_smem[];
   const Geo& g = a.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int nk = (a.in_k ? 1 : 0) + (a.in_v ? 1 : 0);
-  const long long n_tiles = (long long)nk * g.B * g.H * a.n;
-  const uint32_t stage_bytes = (uint32_t)(TILE * 2) + a.part_bytes;
-  uint8_t* ctile = es_smem + 2 * (size_t)stage_bytes;  // [128 tokens][ES_BROW] codes
-  __shared__ uint64_t landed[2];
-  __shared__ float cb[16];  // nuq codebook of the current head
+  const int bi = blockIdx.x, h = blockIdx.y, b = blockIdx.z >> 1, kind = blockIdx.z & 1;
+  const uint16_t* in = kind ? a.in_v : a.in_k;
+  float* st = kind ? a.st_v : a.st_k;
+  if (!in || !st) return;
+  const int blk = a.first + bi;
+  const uint8_t* rec = a.base + record_offset(g, b, h, blk, a.status);
+  const uint32_t off = g.codes_off[kind], end = kind ? (uint32_t)g.rec_bytes : g.codes_off[1];
+  const uint64_t tok0 = ((uint64_t)b * g.H + h) * (uint64_t)a.n * T + (uint64_t)bi * T;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(es_smem);        // [128 tokens][128] input rows
+  uint8_t* ctile = es_smem + TILE * 2;                        // [128 tokens][ES_BROW] codes
+  uint8_t* part = ctile + T * ES_BROW;                        // the record's part of this kind
+  __shared__ uint64_t landed;
+  __shared__ float cb[16];  // nuq codebook of this head
   if (tid == 0) {
-    mbar_init(&landed[0], 1);
-    mbar_init(&landed[1], 1);
+    mbar_init(&landed, 1);
     fence_mbar_init();
   }
+  if (METHOD == KVQ_NUQ && tid < (1 << BITS)) cb[tid] = a.codebook[h * (1 << BITS) + tid];
   __syncthreads();
-  // tile i -> kind, (b, h), block
-  auto decode_tile = [&](long long i, int& kind, int& b, int& h, int& bi) {
-    kind = nk == 2 ? (int)(i & 1) : (a.in_k ? 0 : 1);
-    const long long r = nk == 2 ? (i >> 1) : i;
-    bi = (int)(r % a.n);
-    const long long u = r / a.n;
-    b = (int)(u / g.H);
-    h = (int)(u - (long long)b * g.H);
-  };
-  auto issue = [&](long long i, int s) {  // thread 0: the copies of tile i into stage s
-    int kind, b, h, bi;
-    decode_tile(i, kind, b, h, bi);
-    const uint16_t* in = kind ? a.in_v : a.in_k;
-    const uint32_t off = g.codes_off[kind], end = kind ? (uint32_t)g.rec_bytes : g.codes_off[1];
-    const uint8_t* rec = a.base + record_offset(g, b, h, a.first + bi, a.status);
-    const uint64_t tok0 = ((uint64_t)b * g.H + h) * (uint64_t)a.n * T + (uint64_t)bi * T;
-    uint8_t* st = es_smem + (size_t)s * stage_bytes;
-    fence_proxy_async();
-    mbar_arrive_expect_tx(&landed[s], (uint32_t)(TILE * 2) + (end - off));
-    bulk_g2s(st, in + tok0 * D, (uint32_t)(TILE * 2), &landed[s]);
-    bulk_g2s(st + TILE * 2, rec + off, end - off, &landed[s]);
-  };
-  long long k = 0;        // tiles this CTA has processed
-  long long broke = -1;   // tile whose copies did not land in time (-1: none)
-  if (tid == 0 && (long long)blockIdx.x < n_tiles) issue(blockIdx.x, 0);
-  for (long long i = blockIdx.x; i < n_tiles; i += gridDim.x, ++k) {
-    const int s = (int)(k & 1);
-    if (tid == 0 && i + gridDim.x < n_tiles) issue(i + gridDim.x, s ^ 1);  // its stage was freed below
-    int kind, b, h, bi;
-    decode_tile(i, kind, b, h, bi);
-    const int blk = a.first + bi;
-    const uint32_t off = g.codes_off[kind];
-    const uint16_t* xs = reinterpret_cast<const uint16_t*>(es_smem + (size_t)s * stage_bytes);
-    const uint8_t* part = es_smem + (size_t)s * stage_bytes + TILE * 2;
-    float* st = kind ? a.st_v : a.st_k;
-    const uint64_t tok0 = ((uint64_t)b * g.H + h) * (uint64_t)a.n * T + (uint64_t)bi * T;
-    if (METHOD == KVQ_NUQ && tid < (1 << BITS)) cb[tid] = a.codebook[h * (1 << BITS) + tid];
-    const bool got = mbar_wait_bounded(&landed[s], (uint32_t)((k >> 1) & 1), a.status);
-    if (__syncthreads_or(!got)) {  // every thread leaves together; the copies are drained below
-      broke = i;
-      break;
-    }
-    const uint32_t* codes = reinterpret_cast<const uint32_t*>(part);
-    const uint16_t* m = reinterpret_cast<const uint16_t*>(part + (g.meta_off[kind] - off));
-    if (BITS == 3 && g.planes3) {  // bit planes: element by element
-      for (int e = tid; e < TILE; e += ES_THREADS) {
-        const int t = e >> 7, c = e & 127;
-        ctile[t * ES_BROW + c] = (uint8_t)tile3_code(codes, kind, t, c);
-      }
-    } else {
-      const bool chrows = kind == 1 && g.vrows_ch;  // value codes stored as channel rows
-      for (int j = tid; j < T * W; j += ES_THREADS) {
-        const int r = j / W, w = j - r * W;
-        const uint32_t word = codes[j];
-#pragma unroll
-        for (int jj = 0; jj < NWC; ++jj) {
-          const int pos = w * NWC + jj;
-          if (pos < D) {
-            const uint8_t q = (uint8_t)((word >> (BITS * jj)) & MASK);
-            if (chrows) ctile[pos * ES_BROW + r] = q;  // row r = channel, pos = token
-            else ctile[r * ES_BROW + pos] = q;
-          }
-        }
-      }
-    }
-    __syncthreads();
-    const int sub = lane >> 3, j8 = lane & 7, c0 = 16 * j8;  // row within the warp's 4, channel group
-    // per-channel metadata of the lane's 16 channels (keys: s, z or zp; values: s1)
-    float cs[16], cz[16];
-  #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      cs[i] = 1.0f;
-      cz[i] = 0.0f;
-      if (kind == 0 && METHOD != KVQ_INT4) {
-        cs[i] = h2f(m[c0 + i]);
-        cz[i] = h2f(m[T + c0 + i]);
-      } else if (kind == 1 && METHOD == KVQ_VARN) {
-        cs[i] = h2f(m[2 * T + c0 + i]);  // s1 per channel
-      }
-    }
-    const bool to_input = METHOD == KVQ_VARN && a.hadamard;
-    for (int t = 4 * warp + sub; t < T; t += 4 * (ES_THREADS / 32)) {
-      float x[16], q[16];
-      {
-        const uint4* xp = reinterpret_cast<const uint4*>(xs + t * D + c0);
-        const uint4 x0 = xp[0], x1 = xp[1];
-        const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-  #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          x[2 * i] = in_bits_to_f32((uint16_t)(xw[i] & 0xffffu), g.in_bf16);
-          x[2 * i + 1] = in_bits_to_f32((uint16_t)(xw[i] >> 16), g.in_bf16);
-        }
-      }
-      if (g.sink && blk == 0 && t == 0) {  // the kept first token: what decode attends
-        const uint16_t* kept =
-            reinterpret_cast<const uint16_t*>(a.base + g.sink_off) + (((uint64_t)b * g.H + h) * 2 + kind) * D + c0;
-  #pragma unroll
-        for (int i = 0; i < 16; ++i) q[i] = in_bits_to_f32(kept[i], g.in_bf16);
-      } else {
-        const uint4 cw = *reinterpret_cast<const uint4*>(ctile + t * ES_BROW + c0);
-        const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
-        // per-token metadata of this row (values: s, z or zp; keys: KVarN s1; absmax: s per block)
-        const float ts = (kind == 1 || METHOD == KVQ_INT4) ? h2f(m[(METHOD == KVQ_INT4 && g.g64 && c0 >= 64 ? T : 0) + t])
-                                                           : 1.0f;
-        const float tz = (kind == 1 && METHOD != KVQ_INT4) ? h2f(m[T + t]) : 0.0f;
-        const float tk1 = (kind == 0 && METHOD == KVQ_VARN) ? h2f(m[2 * T + t]) : 1.0f;
-  #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t code = (cws[i >> 2] >> (8 * (i & 3))) & 0xffu;
-          float v;
-          if (METHOD == KVQ_RTN || METHOD == KVQ_VARN) {
-            v = kind == 0 ? ((float)code + cz[i]) * cs[i] : ((float)code + tz) * ts;
-            if (METHOD == KVQ_VARN) v *= kind == 0 ? tk1 : cs[i];
-          } else if (METHOD == KVQ_INT4) {
-            constexpr int SH = 32 - BITS;
-            v = (float)((int)(code << SH) >> SH) * ts;
-          } else {
-            v = kind == 0 ? cb[code] * cs[i] + cz[i] : cb[code] * ts + tz;
-          }
-          q[i] = v;
-        }
-        if (METHOD == KVQ_NUQ && g.n_out > 0) {  // this row's outliers (few): the owning lane adds
-          const uint8_t* csr = part + (g.csr_off[kind] - off);
-          const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
-          const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * g.n_out);
-          const uint8_t* col = csr + 2 * g.n_out + 2 * (T + 1);
-          const int e1 = min((int)rp[t + 1], g.n_out);
-          for (int e = min((int)rp[t], g.n_out); e < e1; ++e) {
-            const int c = col[e] & (D - 1);
-            const float vv = (c >> 4) == j8 ? h2f(val[e]) : 0.0f;
-  #pragma unroll
-            for (int i = 0; i < 16; ++i) q[i] += (c & 15) == i ? vv : 0.0f;  // no indexed register
-          }
-        }
-        if (to_input) {  // inverse Hadamard (H / sqrt(128) is its own inverse), Sylvester order
-  #pragma unroll
-          for (int d = 1; d < 16; d <<= 1)  // distances 1..8: inside the lane
-  #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (!(i & d)) {
-                const float u0 = q[i], u1 = q[i + d];
-                q[i] = u0 + u1;
-                q[i + d] = u0 - u1;
-              }
-  #pragma unroll
-          for (int dl = 1; dl < 8; dl <<= 1) {  // distances 16, 32, 64: across the row's 8 lanes
-            const bool upper = j8 & dl;
-  #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float o = __shfl_xor_sync(0xffffffffu, q[i], dl);
-              q[i] = upper ? o - q[i] : q[i] + o;
-            }
-          }
-  #pragma unroll
-          for (int i = 0; i < 16; ++i) q[i] *= 0.08838834764831845f;
-        }
-      }
-      float sxx = 0.0f, sqq = 0.0f, sdd = 0.0f, spm = 0.0f;
-  #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float dd = x[i] - q[i];
-        sxx = fmaf(x[i], x[i], sxx);
-        sqq = fmaf(q[i], q[i], sqq);
-        sdd = fmaf(dd, dd, sdd);
-        spm = fmaf(q[i] - x[i], q[i] + x[i], spm);
-      }
-  #pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {
-        sxx += __shfl_xor_sync(0xffffffffu, sxx, o);
-        sqq += __shfl_xor_sync(0xffffffffu, sqq, o);
-        sdd += __shfl_xor_sync(0xffffffffu, sdd, o);
-        spm += __shfl_xor_sync(0xffffffffu, spm, o);
-      }
-      const float nx = sqrtf(sxx), nq = sqrtf(sqq);
-      const float dn = nx + nq > 0.0f ? spm / (nx + nq) : 0.0f;
-      float su = 0.0f;
-      const bool both = nx > 0.0f && nq > 0.0f;  // uniform over the row's 8 lanes
-      const float ix = both ? 1.0f / nx : 0.0f, iq = both ? 1.0f / nq : 0.0f;
-  #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float u = __fsub_rn(__fmul_rn(x[i], ix), __fmul_rn(q[i], iq));  // 0 when x_dq = x
-        su = fmaf(u, u, su);
-      }
-  #pragma unroll
-      for (int o = 1; o < 8; o <<= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
-      const float ed = both ? nx * nq * su : 0.0f;
-      if (j8 == 0) reinterpret_cast<float4*>(st)[tok0 + t] = make_float4(nx, dn, sdd, ed);
-    }
-    __syncthreads();  // the stage and the code tile are free for the next tile
+  if (tid == 0) {
+    mbar_arrive_expect_tx(&landed, (uint32_t)(TILE * 2) + (end - off));
+    bulk_g2s(xs, in + tok0 * D, (uint32_t)(TILE * 2), &landed);
+    bulk_g2s(part, rec + off, end - off, &landed);
   }
-  if (tid == 0 && broke >= 0) {  // a wait gave up: let this tile's and the next one's copies land (bounded)
-    mbar_wait_bounded(&landed[k & 1], (uint32_t)((k >> 1) & 1), nullptr, 200000000LL);
-    if (broke + gridDim.x < n_tiles)
-      mbar_wait_bounded(&landed[(k + 1) & 1], (uint32_t)(((k + 1) >> 1) & 1), nullptr, 200000000LL);
+  const bool got = mbar_wait_bounded(&landed, 0u, a.status);
+  if (__syncthreads_or(!got)) return;  // every thread leaves together
+  const uint32_t* codes = reinterpret_cast<const uint32_t*>(part);
+  const uint16_t* m = reinterpret_cast<const uint16_t*>(part + (g.meta_off[kind] - off));
+  if (BITS == 3 && g.planes3) {  // bit planes: element by element
+    for (int e = tid; e < TILE; e += ES_THREADS) {
+      const int t = e >> 7, c = e & 127;
+      ctile[t * ES_BROW + c] = (uint8_t)tile3_code(codes, kind, t, c);
+    }
+  } else {
+    const bool chrows = kind == 1 && g.vrows_ch;  // value codes stored as channel rows
+    for (int i = tid; i < T * W; i += ES_THREADS) {
+      const int r = i / W, w = i - r * W;
+      const uint32_t word = codes[i];
+#pragma unroll
+      for (int j = 0; j < NWC; ++j) {
+        const int pos = w * NWC + j;
+        if (pos < D) {
+          const uint8_t q = (uint8_t)((word >> (BITS * j)) & MASK);
+          if (chrows) ctile[pos * ES_BROW + r] = q;  // row r = channel, pos = token
+          else ctile[r * ES_BROW + pos] = q;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const int sub = lane >> 3, j8 = lane & 7, c0 = 16 * j8;  // row within the warp's 4, channel group
+  // per-channel metadata of the lane's 16 channels (keys: s, z or zp; values: s1)
+  float cs[16], cz[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    cs[i] = 1.0f;
+    cz[i] = 0.0f;
+    if (kind == 0 && METHOD != KVQ_INT4) {
+      cs[i] = h2f(m[c0 + i]);
+      cz[i] = h2f(m[T + c0 + i]);
+    } else if (kind == 1 && METHOD == KVQ_VARN) {
+      cs[i] = h2f(m[2 * T + c0 + i]);  // s1 per channel
+    }
+  }
+  const bool to_input = METHOD == KVQ_VARN && a.hadamard;
+  for (int t = 4 * warp + sub; t < T; t += 4 * (ES_THREADS / 32)) {
+    float x[16], q[16];
+    {
+      const uint4* xp = reinterpret_cast<const uint4*>(xs + t * D + c0);
+      const uint4 x0 = xp[0], x1 = xp[1];
+      const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        x[2 * i] = in_bits_to_f32((uint16_t)(xw[i] & 0xffffu), g.in_bf16);
+        x[2 * i + 1] = in_bits_to_f32((uint16_t)(xw[i] >> 16), g.in_bf16);
+      }
+    }
+    if (g.sink && blk == 0 && t == 0) {  // the kept first token: what decode attends
+      const uint16_t* kept =
+          reinterpret_cast<const uint16_t*>(a.base + g.sink_off) + (((uint64_t)b * g.H + h) * 2 + kind) * D + c0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) q[i] = in_bits_to_f32(kept[i], g.in_bf16);
+    } else {
+      const uint4 cw = *reinterpret_cast<const uint4*>(ctile + t * ES_BROW + c0);
+      const uint32_t cws[4] = {cw.x, cw.y, cw.z, cw.w};
+      // per-token metadata of this row (values: s, z or zp; keys: KVarN s1; absmax: s per block)
+      const float ts = (kind == 1 || METHOD == KVQ_INT4) ? h2f(m[(METHOD == KVQ_INT4 && g.g64 && c0 >= 64 ? T : 0) + t])
+                                                         : 1.0f;
+      const float tz = (kind == 1 && METHOD != KVQ_INT4) ? h2f(m[T + t]) : 0.0f;
+      const float tk1 = (kind == 0 && METHOD == KVQ_VARN) ? h2f(m[2 * T + t]) : 1.0f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t code = (cws[i >> 2] >> (8 * (i & 3))) & 0xffu;
+        float v;
+        if (METHOD == KVQ_RTN || METHOD == KVQ_VARN) {
+          v = kind == 0 ? ((float)code + cz[i]) * cs[i] : ((float)code + tz) * ts;
+          if (METHOD == KVQ_VARN) v *= kind == 0 ? tk1 : cs[i];
+        } else if (METHOD == KVQ_INT4) {
+          constexpr int SH = 32 - BITS;
+          v = (float)((int)(code << SH) >> SH) * ts;
+        } else {
+          v = kind == 0 ? cb[code] * cs[i] + cz[i] : cb[code] * ts + tz;
+        }
+        q[i] = v;
+      }
+      if (METHOD == KVQ_NUQ && g.n_out > 0) {  // this row's outliers (few): the owning lane adds
+        const uint8_t* csr = part + (g.csr_off[kind] - off);
+        const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
+        const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * g.n_out);
+        const uint8_t* col = csr + 2 * g.n_out + 2 * (T + 1);
+        const int e1 = min((int)rp[t + 1], g.n_out);
+        for (int e = min((int)rp[t], g.n_out); e < e1; ++e) {
+          const int c = col[e] & (D - 1);
+          const float vv = (c >> 4) == j8 ? h2f(val[e]) : 0.0f;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) q[i] += (c & 15) == i ? vv : 0.0f;  // no indexed register
+        }
+      }
+      if (to_input) {  // inverse Hadamard (H / sqrt(128) is its own inverse), Sylvester order
+#pragma unroll
+        for (int d = 1; d < 16; d <<= 1)  // distances 1..8: inside the lane
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (!(i & d)) {
+              const float u0 = q[i], u1 = q[i + d];
+              q[i] = u0 + u1;
+              q[i + d] = u0 - u1;
+            }
+#pragma unroll
+        for (int dl = 1; dl < 8; dl <<= 1) {  // distances 16, 32, 64: across the row's 8 lanes
+          const bool upper = j8 & dl;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float o = __shfl_xor_sync(0xffffffffu, q[i], dl);
+            q[i] = upper ? o - q[i] : q[i] + o;
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) q[i] *= 0.08838834764831845f;
+      }
+    }
+    float sxx = 0.0f, sqq = 0.0f, sdd = 0.0f, spm = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float dd = x[i] - q[i];
+      sxx = fmaf(x[i], x[i], sxx);
+      sqq = fmaf(q[i], q[i], sqq);
+      sdd = fmaf(dd, dd, sdd);
+      spm = fmaf(q[i] - x[i], q[i] + x[i], spm);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      sxx += __shfl_xor_sync(0xffffffffu, sxx, o);
+      sqq += __shfl_xor_sync(0xffffffffu, sqq, o);
+      sdd += __shfl_xor_sync(0xffffffffu, sdd, o);
+      spm += __shfl_xor_sync(0xffffffffu, spm, o);
+    }
+    const float nx = sqrtf(sxx), nq = sqrtf(sqq);
+    const float dn = nx + nq > 0.0f ? spm / (nx + nq) : 0.0f;
+    float su = 0.0f;
+    const bool both = nx > 0.0f && nq > 0.0f;  // uniform over the row's 8 lanes
+    const float ix = both ? 1.0f / nx : 0.0f, iq = both ? 1.0f / nq : 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float u = __fsub_rn(__fmul_rn(x[i], ix), __fmul_rn(q[i], iq));  // 0 when x_dq = x
+      su = fmaf(u, u, su);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) su += __shfl_xor_sync(0xffffffffu, su, o);
+    const float ed = both ? nx * nq * su : 0.0f;
+    if (j8 == 0) reinterpret_cast<float4*>(st)[tok0 + t] = make_float4(nx, dn, sdd, ed);
   }
 }
 
@@ -361,10 +324,9 @@ cudaError_t kvq_launch_error_stats(const kvq::Geo& g, const uint8_t* base, const
   kvq::ErrArgs a;
   a.g = g; a.base = base; a.codebook = codebook; a.first = first; a.n = n; a.hadamard = hadamard;
   a.in_k = in_k; a.in_v = in_v; a.st_k = st_k; a.st_v = st_v; a.status = status;
+  // the unpacked code tile, then the larger of the two kinds' record parts
   const uint32_t kb = g.codes_off[1] - g.codes_off[0], vb = (uint32_t)g.rec_bytes - g.codes_off[1];
-  a.part_bytes = kb > vb ? kb : vb;
-  // two stages (input tile + record part), then the unpacked code tile
-  const int smem = 2 * (kvq::TILE * 2 + (int)a.part_bytes) + kvq::T * kvq::ES_BROW;
+  const int smem = kvq::TILE * 2 + kvq::T * kvq::ES_BROW + (int)(kb > vb ? kb : vb);
   using Fn = void (*)(kvq::ErrArgs);
   Fn fn = nullptr;
   const int m = g.method, b = g.bits;
@@ -377,11 +339,7 @@ cudaError_t kvq_launch_error_stats(const kvq::Geo& g, const uint8_t* base, const
   if (!fn) return cudaErrorInvalidValue;
   cudaError_t e = kvq::ensure_smem_attr((const void*)fn, (size_t)smem);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 152;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return cudaGetLastError();
-  const long long tiles = (long long)((in_k ? 1 : 0) + (in_v ? 1 : 0)) * g.B * g.H * n;
-  const int grid = (int)(tiles < sms ? tiles : sms);
+  dim3 grid(n, g.H, g.B * 2);
   fn<<<grid, kvq::ES_THREADS, smem, st>>>(a);
   return cudaGetLastError();
 }
