@@ -88,6 +88,23 @@ def _dist():
     return rank, world, local
 
 
+def _max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest of every rank's x (the job's step time is its slowest rank's)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device or "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _job_gbs(bytes_per_step_per_rank: int, step_ms: float, world: int) -> float:
+    """Whole-job throughput: every rank streams its own replica (weak scaling), so the job moves
+    world times one rank's bytes in the slowest rank's step time."""
+    return world * bytes_per_step_per_rank / (step_ms * 1e-3) / 1e9
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -317,12 +334,9 @@ def run_kvq(args):
     status = max(int(c.status.item()) for c in caches)
     if status != 0:
         raise RuntimeError(f"device status {status} ({K.kvq_status_str(status)})")
-    if world > 1:
-        tt = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(tt.item())
+    step_ms = _max_over_ranks(step_ms, world, dev)
     dec_bytes_step = cache_bytes * DECODES_PER_STEP
-    value = world * dec_bytes_step / (step_ms * 1e-3) / 1e9
+    value = _job_gbs(dec_bytes_step, step_ms, world)
     dec_avg_us = (1e3 * step_ms - app_us) / DECODES_PER_STEP
     peak, peak_kind = _peaks()
     achieved = cache_bytes / (dec0_us * 1e-6) / 1e9   # decode call with an empty tail
