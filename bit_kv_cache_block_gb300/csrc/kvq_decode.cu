@@ -522,49 +522,54 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
     if (n_part > a.n_split) n_part = a.n_split;
   }
 
-  // ---- merge the partials: max over all, then group grp sums partials grp, grp+4, ...
+  // ---- merge the partials in one pass: group grp takes partials grp, grp+4, ..., eight of them
+  // per chunk with their loads side by side (they sit in L2), against its own running maximum;
+  // then the four groups meet in shared memory (fixed order: the result does not depend on timing)
+  __shared__ float gm[CB_GROUPS], gl[CB_GROUPS];
   __syncthreads();  // part[] is reused below
-  float mm = -INFINITY;
-  for (int s = tid; s < n_part; s += CB_THREADS) mm = fmaxf(mm, a.ws_m[row0 + s]);
-  const float M = cb_max(mm, red);
-  float Lg = 0.0f, Og = 0.0f;
-  {
-    // four partials of the group per iteration, their loads side by side (they sit in L2)
-    float Lp[4] = {0.0f, 0.0f, 0.0f, 0.0f}, Op[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    int s = grp;
-    for (; s + 3 * CB_GROUPS < n_part; s += 4 * CB_GROUPS) {
-      float mv[4], lv[4], ovv[4];
+  float mg = -INFINITY, Lg = 0.0f, Og = 0.0f;
+  for (int s0 = grp; s0 < n_part; s0 += 8 * CB_GROUPS) {
+    float mv[8], lv[8], ovv[8];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const uint64_t r = row0 + s + k * CB_GROUPS;
-        mv[k] = a.ws_m[r];
-        lv[k] = a.ws_l[r];
-        ovv[k] = a.ws_o[r * D + c];
-      }
+    for (int k = 0; k < 8; ++k) {
+      const int s = s0 + k * CB_GROUPS;
+      const uint64_t r = row0 + (s < n_part ? s : s0);
+      mv[k] = s < n_part ? a.ws_m[r] : -INFINITY;
+      lv[k] = a.ws_l[r];
+      ovv[k] = a.ws_o[r * D + c];
+    }
+    float mc = mg;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float f = exp2f(mv[k] - M);
-        Lp[k] = fmaf(lv[k], f, Lp[k]);
-        Op[k] = fmaf(ovv[k], f, Op[k]);
-      }
+    for (int k = 0; k < 8; ++k) mc = fmaxf(mc, mv[k]);
+    if (mc > mg) {  // group-uniform
+      const float f = exp2f(mg - mc);
+      Lg *= f;
+      Og *= f;
+      mg = mc;
     }
-    for (; s < n_part; s += CB_GROUPS) {
-      const uint64_t r = row0 + s;
-      const float f = exp2f(a.ws_m[r] - M);
-      Lp[0] = fmaf(a.ws_l[r], f, Lp[0]);
-      Op[0] = fmaf(a.ws_o[r * D + c], f, Op[0]);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float f = mv[k] == -INFINITY ? 0.0f : exp2f(mv[k] - mg);
+      Lg = fmaf(lv[k], f, Lg);
+      Og = fmaf(ovv[k], f, Og);
     }
-    Lp[0] += Lp[2];
-    Lp[1] += Lp[3];
-    Op[0] += Op[2];
-    Op[1] += Op[3];
-    Lg = Lp[0] + Lp[1];
-    Og = Op[0] + Op[1];
   }
   part[grp][c] = Og;
-  // L: the same value in every thread of a group; take channel 0 of each group
-  float L = cb_sum(c == 0 ? Lg : 0.0f, red);  // (also orders the part[] stores)
-  float O = (part[0][c] + part[1][c]) + (part[2][c] + part[3][c]);
+  if (c == 0) {
+    gm[grp] = mg;
+    gl[grp] = Lg;
+  }
+  __syncthreads();
+  float M = gm[0];
+#pragma unroll
+  for (int k = 1; k < CB_GROUPS; ++k) M = fmaxf(M, gm[k]);
+  float L = 0.0f, O = 0.0f;
+#pragma unroll
+  for (int k = 0; k < CB_GROUPS; ++k) {
+    const float f = gm[k] == -INFINITY ? 0.0f : exp2f(gm[k] - M);
+    L = fmaf(gl[k], f, L);
+    O = fmaf(part[k][c], f, O);
+  }
   if (g.method == KVQ_VARN && a.hadamard && n_part > 0) {
     __syncthreads();
     if (grp == 0) ob[c] = O;
