@@ -115,31 +115,62 @@ __device__ void rtn_tile(AppendSmem* sm, int axis, int bits, uint16_t* m16) {
   __syncthreads();
 }
 
+// Warp-wide selection over PER * 32 histogram bins (lane l holds bins PER*l .. PER*l + PER-1):
+// the highest bin b such that base + (count in bins above b) < target <= base + (count in bins b
+// and above); bin 0 when no bin qualifies. The lane holding b returns true with cum = base +
+// count above b. Same result as scanning the bins one by one from the top.
+template <int PER>
+__device__ __forceinline__ bool select_bin(const int* hist, int base, int target, int lane, int& cum, int& bin) {
+  int hv[PER], sl = 0;
+#pragma unroll
+  for (int k = 0; k < PER; ++k) {
+    hv[k] = hist[PER * lane + k];
+    sl += hv[k];
+  }
+  int incl = sl;  // bins of this lane and of the lanes above it
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_down_sync(0xffffffffu, incl, o);
+    if (lane + o < 32) incl += y;
+  }
+  const int above = base + incl - sl;
+  const bool here = (above < target && base + incl >= target) || (lane == 0 && base + incl < target);
+  if (!here) return false;
+  cum = above;
+  int b = PER - 1;
+#pragma unroll
+  for (int k = PER - 1; k > 0; --k) {
+    if (b == k) {
+      if (cum + hv[k] >= target) break;
+      cum += hv[k];
+      b = k - 1;
+    }
+  }
+  bin = PER * lane + b;
+  return true;
+}
+
 // Pack sm->codes (token-major, [t][c]) into words. Rows: code i of a row at bits
 // [b*(i%n)+b-1 : b*(i%n)] of word i/n, n = floor(32/b); one row per token, or (transpose) one row
 // per channel (its codes for the 128 tokens). planes: the 3-bit plane layout of tile3_slot (one
 // thread per output word; kind 0 keys, 1 values).
 __device__ void pack_tile(const AppendSmem* sm, int bits, bool transpose, bool planes, int kind, uint32_t* dst) {
-  if (planes) {
-    for (int wi = threadIdx.x; wi < TILE3_WORDS; wi += AP_THREADS) {
-      const int s = wi / 192, rem = wi - s * 192, grp = rem / 6, o = rem - grp * 6;
-      uint32_t word = 0;
-      for (int k = 0; k < 8; ++k) {
-        if (o < 4) {  // low-bit plane: nibble words 2o and 2o+1
-          for (int hf = 0; hf < 2; ++hf) {
-            int t, c;
-            tile3_code_at(kind, s, grp, 2 * o + hf, k, t, c);
-            word |= ((uint32_t)sm->codes[t * D + c] & 3u) << (4 * k + 2 * hf);
-          }
-        } else {      // high-bit plane: nibble words 4(o-4) .. 4(o-4)+3
-          for (int q = 0; q < 4; ++q) {
-            int t, c;
-            tile3_code_at(kind, s, grp, 4 * (o - 4) + q, k, t, c);
-            word |= (((uint32_t)sm->codes[t * D + c] >> 2) & 1u) << (4 * k + (q ^ 2));
-          }
+  if (planes) {  // thread = one 6-word group (segment s, group grp): each of its 64 codes read once
+    for (int gi = threadIdx.x; gi < TILE3_WORDS / 6; gi += AP_THREADS) {
+      const int s = gi >> 5, grp = gi & 31;
+      uint32_t w[6] = {0u, 0u, 0u, 0u, 0u, 0u};
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          int t, c;
+          tile3_code_at(kind, s, grp, u, k, t, c);
+          const uint32_t q = sm->codes[t * D + c];
+          w[u >> 1] |= (q & 3u) << (4 * k + 2 * (u & 1));              // low bits
+          w[4 + (u >> 2)] |= ((q >> 2) & 1u) << (4 * k + ((u & 3) ^ 2));  // high bit
         }
-      }
-      dst[wi] = word;
+#pragma unroll
+      for (int o = 0; o < 6; ++o) dst[gi * 6 + o] = w[o];
     }
     return;
   }
@@ -313,46 +344,49 @@ __global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
       __syncthreads();
       const int e0 = tid * 64;  // this thread's chunk of flat indices (half a row)
       const int t0 = e0 >> 7, c0 = e0 & 127;
-      for (int j = 0; j < 64; ++j) {
-        int mag = f2h_rn(sm->x[t0 * XS + c0 + j]) & 0x7fff;
-        atomicAdd(&sm->hist[mag >> 7], 1);
-      }
+      uint32_t mpk[32];         // the chunk's fp16 magnitudes, two per register
+#pragma unroll
+      for (int j = 0; j < 64; j += 2)
+        mpk[j >> 1] = (uint32_t)(f2h_rn(sm->x[t0 * XS + c0 + j]) & 0x7fff) |
+                      ((uint32_t)(f2h_rn(sm->x[t0 * XS + c0 + j + 1]) & 0x7fff) << 16);
+      auto mag_of = [&](int j) -> int { return (int)((mpk[j >> 1] >> (16 * (j & 1))) & 0x7fffu); };
+#pragma unroll
+      for (int j = 0; j < 64; ++j) atomicAdd(&sm->hist[mag_of(j) >> 7], 1);
       __syncthreads();
-      if (tid == 0) {
-        int cum = 0, bin = 255;
-        for (; bin > 0; --bin) {
-          if (cum + sm->hist[bin] >= n_out) break;
-          cum += sm->hist[bin];
+      if (tid < 32) {  // the bin holding the n_out-th largest: suffix sums over 8 bins per lane
+        int cum, bin;
+        if (select_bin<8>(sm->hist, 0, n_out, tid, cum, bin)) {
+          sm->sel[0] = bin;
+          sm->sel[1] = cum;  // count strictly above this bin
         }
-        sm->sel[0] = bin;
-        sm->sel[1] = cum;  // count strictly above this bin
       }
       __syncthreads();
       const int bin1 = sm->sel[0];
       sm->hist[tid] = 0;
       __syncthreads();
+#pragma unroll
       for (int j = 0; j < 64; ++j) {
-        int mag = f2h_rn(sm->x[t0 * XS + c0 + j]) & 0x7fff;
+        const int mag = mag_of(j);
         if ((mag >> 7) == bin1) atomicAdd(&sm->hist[mag & 0x7f], 1);
       }
       __syncthreads();
-      if (tid == 0) {
-        int cum = sm->sel[1], lo = 127;
-        for (; lo > 0; --lo) {
-          if (cum + sm->hist[lo] >= n_out) break;
-          cum += sm->hist[lo];
+      if (tid < 32) {  // the same inside that bin: 128 bins of the low 7 bits, 4 per lane
+        int cum, lo;
+        if (select_bin<4>(sm->hist, sm->sel[1], n_out, tid, cum, lo)) {
+          sm->sel[2] = (bin1 << 7) | lo;  // threshold magnitude
+          sm->sel[3] = n_out - cum;       // how many entries equal to the threshold are taken
         }
-        sm->sel[2] = (bin1 << 7) | lo;  // threshold magnitude
-        sm->sel[3] = n_out - cum;       // how many entries equal to the threshold are taken
       }
       __syncthreads();
       const int thr = sm->sel[2], need_eq = sm->sel[3];
       int n_eq = 0;
-      for (int j = 0; j < 64; ++j) n_eq += (f2h_rn(sm->x[t0 * XS + c0 + j]) & 0x7fff) == thr;
+#pragma unroll
+      for (int j = 0; j < 64; ++j) n_eq += mag_of(j) == thr;
       int eq_rank = block_excl_scan(n_eq, sm->scan, nullptr);
       uint64_t selbits = 0;
+#pragma unroll
       for (int j = 0; j < 64; ++j) {
-        int mag = f2h_rn(sm->x[t0 * XS + c0 + j]) & 0x7fff;
+        const int mag = mag_of(j);
         bool s = mag > thr;
         if (mag == thr) {
           s = eq_rank < need_eq;
