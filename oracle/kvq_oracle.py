@@ -335,6 +335,42 @@ def nuq_codebook(bits: int = 3) -> np.ndarray:
     return np.array([inv((j + 0.5) / n) / top for j in range(n)], np.float64).astype(np.float32)
 
 
+FIT_SCALE = 2.0 ** 32   # fixed-point resolution of the weighted sums of fit_codebook
+
+
+def fit_codebook(a: np.ndarray, w: np.ndarray, bits: int, max_iter: int = 50):
+    """Sensitivity-weighted nuq codebook ([KVQ] §3.3, Algorithm 2): Lloyd iterations on the
+    normalised samples a (clamped to [-1, 1]) with weights w (Fisher information, clamped to
+    [0, 1]). Start from k = 2^b centres spaced evenly over [-1, 1] (reading: c_j = -1 + 2j/(k-1)).
+    Each iteration assigns every sample to its nearest centre (|a - c_j| in fp32, the lowest j
+    on ties), stops if no assignment changed, else moves each centre to the weighted mean of its
+    members (a centre without members stays). The weighted sums are exact: w*a and w (products
+    exact in fp64) are scaled by 2^32, rounded half-even to 64-bit integers and added as
+    integers; each centre is the fp64 quotient of the two sums rounded to fp32.
+    Returns (codebook fp32 [k], iterations run)."""
+    a = np.clip(np.asarray(a, np.float32), np.float32(-1.0), np.float32(1.0))
+    w = np.clip(np.asarray(w, np.float32), np.float32(0.0), np.float32(1.0))
+    k = 2 ** bits
+    c = np.array([-1.0 + 2.0 * j / (k - 1) for j in range(k)], np.float64).astype(np.float32)
+    P = np.rint(w.astype(np.float64) * a.astype(np.float64) * FIT_SCALE).astype(np.int64)
+    W = np.rint(w.astype(np.float64) * FIT_SCALE).astype(np.int64)
+    prev = None
+    it = 0
+    for it in range(1, max_iter + 1):
+        d = np.abs(a[:, None] - c[None, :])             # fp32 subtraction, then |.|
+        assign = np.argmin(d, axis=1)                    # first index on ties
+        if prev is not None and np.array_equal(assign, prev):
+            break
+        for j in range(k):
+            m = assign == j
+            if m.any():
+                sw = int(W[m].sum())
+                if sw > 0:
+                    c[j] = np.float32(np.float64(int(P[m].sum())) / np.float64(sw))
+        prev = assign
+    return c, it
+
+
 def n_outliers(frac: float) -> int:
     """Outliers per 128x128 tile: ceil(frac * 16384), frac taken as an fp32 value."""
     return int(math.ceil(float(np.float32(frac)) * TILE))

@@ -269,3 +269,23 @@ def test_group64_scales_of_the_wrong_half_are_caught(monkeypatch):
         return orig(q, s[::-1] if s.ndim == 2 and s.shape[0] == 2 else s)
     monkeypatch.setattr(K, "absmax_dequant", swapped)
     assert _fails(P.test_cache_decode_equals_plain_attention_on_lossless_inputs, "int4g64", 1, False)
+
+
+def test_unweighted_codebook_update_is_caught(monkeypatch):
+    orig = K.fit_codebook
+    monkeypatch.setattr(K, "fit_codebook", lambda a, w, bits, max_iter=50: orig(a, np.ones_like(np.asarray(w)), bits,
+                                                                               max_iter))
+    monkeypatch.setattr(O, "fit_codebook", K.fit_codebook)
+    assert _fails(P.test_fit_codebook_weighted_means_of_separated_groups)
+
+
+def test_codebook_ties_to_the_higher_centre_are_caught(monkeypatch):
+    orig = K.fit_codebook
+
+    def flipped(a, w, bits, max_iter=50):
+        c, it = orig(-np.asarray(a, np.float32), w, bits, max_iter)  # mirrored data: ties go the other way
+        return -c[::-1], it
+    monkeypatch.setattr(K, "fit_codebook", flipped)
+    monkeypatch.setattr(O, "fit_codebook", flipped)
+    assert _fails(P.test_fit_codebook_converged_state_and_ties)
+

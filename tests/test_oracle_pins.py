@@ -584,6 +584,63 @@ def test_topk_error_share_brute_force():
     assert got[1, 2] == pytest.approx(st[3, 1] ** 2 + st[17, 1] ** 2, rel=1e-14)
 
 
+# ------------------------------------------------------------------ codebook fitting (KVQuant Algorithm 2)
+
+def test_fit_codebook_uniform_density_gives_the_uniform_quantizer():
+    """Lloyd's fixed point for a uniform density on [-1, 1] with equal weights is the uniform
+    quantizer: centres at the midpoints (2j + 1)/k - 1 of k equal cells."""
+    rng = np.random.default_rng(0)
+    a = rng.uniform(-1, 1, 200_000).astype(np.float32)
+    for bits in (2, 3):
+        k = 2 ** bits
+        c, it = O.fit_codebook(a, np.ones_like(a), bits, 200)
+        assert it < 200
+        assert np.allclose(c, (2 * np.arange(k) + 1) / k - 1, atol=0.01)
+
+
+def test_fit_codebook_weighted_means_of_separated_groups():
+    """Four well-separated groups: after convergence each centre is its group's weighted mean
+    (Python's exact fsum of w*a over fsum of w), not the plain mean."""
+    rng = np.random.default_rng(1)
+    groups = [(-0.9, 0.03), (-0.3, 0.05), (0.25, 0.04), (0.85, 0.02)]
+    a = np.concatenate([np.float32(m) + np.float32(sd) * rng.standard_normal(500).astype(np.float32) for m, sd in groups])
+    w = rng.uniform(0.0, 1.0, a.size).astype(np.float32) ** 3
+    c, _ = O.fit_codebook(a, w, 2, 100)
+    for j, (m, _) in enumerate(groups):
+        sel = slice(500 * j, 500 * (j + 1))
+        exp = math.fsum(float(x) * float(y) for x, y in zip(a[sel], w[sel])) / math.fsum(float(y) for y in w[sel])
+        assert abs(float(c[j]) - exp) <= 1e-6, (j, c[j], exp)
+        plain = float(np.mean(a[sel].astype(np.float64)))
+        assert abs(exp - plain) > 1e-4  # the weights matter in this fixture
+
+
+def test_fit_codebook_converged_state_and_ties():
+    rng = np.random.default_rng(2)
+    a = np.tanh(rng.standard_normal(20_000)).astype(np.float32)
+    w = rng.uniform(0, 1, a.size).astype(np.float32)
+    c, it = O.fit_codebook(a, w, 3, 500)
+    assert it < 500
+    # every sample's nearest centre (brute force, first on ties) is the one it was averaged into
+    d = np.abs(a[:, None] - c[None, :])
+    assign = np.array([min(range(8), key=lambda j: (d[i, j], j)) for i in range(0, a.size, 97)])
+    assert np.array_equal(assign, np.argmin(d[::97], axis=1))
+    full = np.argmin(d, axis=1)
+    for j in range(8):
+        m = full == j
+        exp = float(np.sum(w[m].astype(np.float64) * a[m]) / np.sum(w[m].astype(np.float64)))
+        assert abs(float(c[j]) - exp) <= 1e-6
+    # a sample equidistant from two centres joins the lower one: bits 1, centres start at -1, 1
+    c, _ = O.fit_codebook(np.array([0.0, 0.5], np.float32), np.ones(2, np.float32), 1, 10)
+    assert c.tolist() == [0.0, 0.5]
+    # one-bit symmetric data: the centres are -+ the weighted mean magnitude
+    x = np.array([-0.75, -0.25, 0.25, 0.75], np.float32)
+    c, _ = O.fit_codebook(x, np.array([0.25, 0.75, 0.75, 0.25], np.float32), 1, 10)
+    assert c.tolist() == [-0.375, 0.375]
+    # weights are clamped to [0, 1] (and samples to [-1, 1]): 3 weighs as 1
+    c, _ = O.fit_codebook(x, np.array([1, 3, 3, 1], np.float32), 1, 10)
+    assert c.tolist() == [-0.5, 0.5]
+
+
 # ------------------------------------------------------------------ attention
 
 def _brute_attention(q, K, V):
