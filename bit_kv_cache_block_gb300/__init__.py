@@ -19,7 +19,7 @@ from ._lib import (KVQ_BF16, KVQ_F16, KVQ_INT4, KVQ_LAYOUT_MMA, KVQ_LAYOUT_ROWS,
 __all__ = ["make_config", "kvq_layout", "kvq_dense_kv_bytes", "kvq_cache_init", "kvq_append_block",
            "kvq_truncate", "kvq_reset", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
            "kvq_decode_attn", "kvq_decode_attn_ex", "kvq_decode_attn_static", "kvq_dequant", "kvq_error_stats", "kvq_error_topk",
-           "kvq_error_topk_workspace_bytes", "error_topk", "kvq_status_str", "KVCache", "KVQError", "kvq_config",
+           "kvq_error_topk_workspace_bytes", "error_topk", "fit_codebook", "kvq_status_str", "KVCache", "KVQError", "kvq_config",
            "kvq_layout_t", "kvq_cache", "lib_path"]
 
 
@@ -193,6 +193,21 @@ def error_topk(stats, fracs, stream=None):
     out = torch.empty(len(fracs), 4, dtype=torch.float64, device=stats.device)
     ws = torch.empty(kvq_error_topk_workspace_bytes(), dtype=torch.uint8, device=stats.device)
     kvq_error_topk(stats, fracs, out, ws, stream)
+    return out
+
+
+def fit_codebook(a, w, bits: int, max_iter: int = 50, stream=None):
+    """Sensitivity-weighted nuq codebook per KV head ([KVQ] Algorithm 2): a, w device fp32
+    [n_heads][n] (normalised samples, Fisher weights); returns fp32 [n_heads][2^bits]."""
+    import torch
+    if a.dim() != 2 or tuple(w.shape) != tuple(a.shape) or a.dtype != torch.float32 or w.dtype != torch.float32:
+        raise ValueError("a and w must be fp32 [n_heads][n] of one shape")
+    H, n = int(a.shape[0]), int(a.shape[1])
+    out = torch.empty(H, 2 ** int(bits), dtype=torch.float32, device=a.device)
+    wsb = int(_lib.lib().kvq_fit_codebook_workspace_bytes(H, n))
+    ws = torch.empty(max(16, wsb), dtype=torch.uint8, device=a.device)
+    _lib.check(_lib.lib().kvq_fit_codebook(_ptr(a), _ptr(w), H, n, int(bits), int(max_iter), _ptr(out), _ptr(ws),
+                                           ws.numel(), _stream(stream)), "kvq_fit_codebook")
     return out
 
 

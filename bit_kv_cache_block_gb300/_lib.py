@@ -25,7 +25,8 @@ METHODS = {"rtn": KVQ_RTN, "nuq": KVQ_NUQ, "varn": KVQ_VARN, "int4": KVQ_INT4}
 EXPORTS = ["kvq_status_str", "kvq_dense_kv_bytes", "kvq_layout", "kvq_cache_init", "kvq_append_block",
            "kvq_truncate", "kvq_reset", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
            "kvq_decode_attn", "kvq_decode_attn_ex", "kvq_decode_attn_static", "kvq_dequant", "kvq_calibrate_keys", "kvq_error_stats",
-           "kvq_error_topk_workspace_bytes", "kvq_error_topk"]
+           "kvq_error_topk_workspace_bytes", "kvq_error_topk", "kvq_fit_codebook_workspace_bytes",
+           "kvq_fit_codebook"]
 
 
 class kvq_config(C.Structure):
@@ -101,6 +102,10 @@ def lib() -> C.CDLL:
     L.kvq_error_stats.argtypes = [P(kvq_cache), vp, vp, i32, i32, vp, vp, vp]
     L.kvq_error_topk_workspace_bytes.restype = sz
     L.kvq_error_topk_workspace_bytes.argtypes = []
+    L.kvq_fit_codebook_workspace_bytes.restype = sz
+    L.kvq_fit_codebook_workspace_bytes.argtypes = [i32, C.c_int64]
+    L.kvq_fit_codebook.restype = C.c_int
+    L.kvq_fit_codebook.argtypes = [vp, vp, i32, C.c_int64, i32, i32, vp, vp, sz, vp]
     L.kvq_error_topk.restype = C.c_int
     L.kvq_error_topk.argtypes = [vp, C.c_int64, P(C.c_double), i32, vp, vp, sz, vp]
     _lib = L

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libkvq.so")
 SOURCES = ["kvq_api.cu", "kvq_append.cu", "kvq_calib.cu", "kvq_decode.cu", "kvq_decode_mma.cu", "kvq_decode_nuq.cu",
-           "kvq_dequant.cu", "kvq_topk.cu"]
+           "kvq_dequant.cu", "kvq_topk.cu", "kvq_fit.cu"]
 HEADERS = [os.path.join(CSRC, "kvq_internal.cuh"), os.path.join(ROOT, "include", "kvq.h")]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

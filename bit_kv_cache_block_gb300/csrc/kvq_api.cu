@@ -22,6 +22,9 @@ cudaError_t kvq_launch_error_stats(const kvq::Geo& g, const uint8_t* base, const
                                    int hadamard, const uint16_t* in_k, const uint16_t* in_v, float* st_k, float* st_v,
                                    int* status, cudaStream_t st);
 size_t kvq_topk_ws_bytes();
+size_t kvq_fit_ws_bytes(int n_heads, long long n);
+cudaError_t kvq_launch_fit(const float* a, const float* w, int n_heads, long long n, int bits, int max_iter, float* c,
+                           void* ws, cudaStream_t st);
 cudaError_t kvq_launch_topk(const float* stats, unsigned long long n, const unsigned long long* k, int nf, double* out,
                             void* ws, cudaStream_t st);
 
@@ -378,6 +381,23 @@ kvq_status kvq_error_stats(const kvq_cache* cache, const void* k, const void* v,
 }
 
 size_t kvq_error_topk_workspace_bytes(void) { return kvq_topk_ws_bytes(); }
+
+size_t kvq_fit_codebook_workspace_bytes(int32_t n_heads, int64_t n) {
+  if (n_heads < 1 || n < 1 || n > ((int64_t)1 << 30)) return 0;
+  return kvq_fit_ws_bytes(n_heads, n);
+}
+
+kvq_status kvq_fit_codebook(const float* a, const float* w, int32_t n_heads, int64_t n, int32_t bits,
+                            int32_t max_iter, float* codebook, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream) {
+  if (!a || !w || !codebook || !workspace) return KVQ_ERR_INVALID_ARG;
+  if (n_heads < 1 || n_heads > 65535 || n < 1 || n > ((int64_t)1 << 30)) return KVQ_ERR_INVALID_ARG;
+  if (bits < 1 || bits > 4 || max_iter < 1 || max_iter > 10000) return KVQ_ERR_INVALID_ARG;
+  if (workspace_bytes < kvq_fit_ws_bytes(n_heads, n)) return KVQ_ERR_CAPACITY;
+  if (!aligned(a, 4) || !aligned(w, 4) || !aligned(codebook, 4) || !aligned(workspace, 16)) return KVQ_ERR_ALIGNMENT;
+  return kvq_launch_fit(a, w, n_heads, n, bits, max_iter, codebook, workspace, stream) == cudaSuccess ? KVQ_OK
+                                                                                                   : KVQ_ERR_CUDA;
+}
 
 kvq_status kvq_error_topk(const float* stats, int64_t n_rows, const double* fracs, int32_t n_fracs, double* out,
                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {

@@ -336,6 +336,26 @@ kvq_status kvq_dequant(const kvq_cache* cache, int32_t first_block, int32_t n_bl
 kvq_status kvq_error_stats(const kvq_cache* cache, const void* k, const void* v, int32_t first_block,
                            int32_t n_blocks, float* stats_k, float* stats_v, cudaStream_t stream);
 
+/* ---------------------------------------------------------------- codebook fitting
+ * Sensitivity-weighted nuq codebook ([KVQ] §3.3, Algorithm 2), per KV head h: Lloyd iterations
+ * on normalised calibration samples a[h][0..n) with Fisher weights w[h][0..n). Samples are
+ * clamped to [-1, 1] and weights to [0, 1]. The k = 2^bits centres start evenly spaced over
+ * [-1, 1] (c_j = -1 + 2j/(k-1), fp64 rounded to fp32). An iteration assigns every sample to its
+ * nearest centre (|a - c_j| in fp32, the lowest j on ties); when no assignment changed the head
+ * stops, else each centre whose members weigh more than zero moves to their weighted mean. The
+ * sums are exact: w*a and w are scaled by 2^32, rounded half-even to 64-bit integers and added
+ * as integers; a centre is the fp64 quotient of its two sums rounded to fp32. So the codebook
+ * does not depend on thread order, and the CPU model reproduces it bit for bit.
+ *   a, w     : device fp32 [n_heads][n], 4-byte aligned; 1 <= n <= 2^30
+ *   bits     : 1..4;  max_iter: 1..10000 iterations at most
+ *   codebook : device fp32 [n_heads][2^bits] (written; usable as kvq_cache_init's codebook)
+ *   workspace: device scratch of kvq_fit_codebook_workspace_bytes(n_heads, n) bytes
+ * Every step runs on `stream` with no host synchronisation. */
+size_t kvq_fit_codebook_workspace_bytes(int32_t n_heads, int64_t n);
+kvq_status kvq_fit_codebook(const float* a, const float* w, int32_t n_heads, int64_t n, int32_t bits,
+                            int32_t max_iter, float* codebook, void* workspace, size_t workspace_bytes,
+                            cudaStream_t stream);
+
 /* Most fractions kvq_error_topk takes in one call. */
 #define KVQ_TOPK_MAX_FRACS 8
 

@@ -218,6 +218,19 @@ def test_host_argument_checks_launch_nothing(K):
     assert topk(sx, 100, big, 1, out, ws, wsb, None) == L.KVQ_ERR_INVALID_ARG         # f > 1
     assert topk(sx, 100, fr, 1, out, ws, wsb - 1, None) == L.KVQ_ERR_CAPACITY
     assert topk(C.c_void_p(0x7008), 100, fr, 1, out, ws, wsb, None) == L.KVQ_ERR_ALIGNMENT
+    # codebook fitting: sizes, bits, iterations, workspace, alignment
+    fit = lib.kvq_fit_codebook
+    fws = lib.kvq_fit_codebook_workspace_bytes(2, 1000)
+    assert fws >= 2 * 1000 and lib.kvq_fit_codebook_workspace_bytes(0, 1000) == 0
+    av, wv, cbv, wsv = C.c_void_p(0x10000), C.c_void_p(0x20000), C.c_void_p(0x30000), C.c_void_p(0x40000)
+    assert fit(av, wv, 2, 1000, 5, 10, cbv, wsv, fws, None) == L.KVQ_ERR_INVALID_ARG      # bits 5
+    assert fit(av, wv, 2, 1000, 0, 10, cbv, wsv, fws, None) == L.KVQ_ERR_INVALID_ARG
+    assert fit(av, wv, 2, 1000, 3, 0, cbv, wsv, fws, None) == L.KVQ_ERR_INVALID_ARG       # no iteration
+    assert fit(av, wv, 2, 0, 3, 10, cbv, wsv, fws, None) == L.KVQ_ERR_INVALID_ARG
+    assert fit(av, wv, 2, (1 << 30) + 1, 3, 10, cbv, wsv, fws, None) == L.KVQ_ERR_INVALID_ARG
+    assert fit(av, wv, 2, 1000, 3, 10, cbv, wsv, fws - 1, None) == L.KVQ_ERR_CAPACITY
+    assert fit(C.c_void_p(0x10002), wv, 2, 1000, 3, 10, cbv, wsv, fws, None) == L.KVQ_ERR_ALIGNMENT
+    assert fit(None, wv, 2, 1000, 3, 10, cbv, wsv, fws, None) == L.KVQ_ERR_INVALID_ARG
     assert lib.kvq_truncate(C.byref(cache), 5) == L.KVQ_ERR_INVALID_ARG
     assert lib.kvq_truncate(C.byref(cache), 2) == L.KVQ_OK and cache.n_blocks == 2
     assert lib.kvq_reset(C.byref(cache)) == L.KVQ_OK and cache.n_blocks == 0
