@@ -666,6 +666,106 @@ def run_diag(args):
     }
 
 
+FIT_HEADS, FIT_SAMPLES = 32, 16 * 2048 * 128   # one layer of LLaMA-7B: 16 sequences of 2K tokens
+
+
+def _fit_inputs_np(n, seed):
+    """Calibration samples of one head: normalised pre-RoPE key entries (tanh of a Gaussian, in
+    [-1, 1]) and Fisher weights (squared Gaussian gradients over their maximum, in [0, 1])."""
+    rng = np.random.default_rng(seed)
+    a = np.tanh(0.8 * rng.standard_normal(n)).astype(np.float32)
+    g = rng.standard_normal(n) ** 2
+    return a, (g / g.max()).astype(np.float32)
+
+
+def _fit_cpu(n, passes):
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    code = ("import sys, time, json; sys.path.insert(0, %r); import bench, oracle as O; "
+            "a, w = bench._fit_inputs_np(%d, 1); t = time.perf_counter(); c, it = O.fit_codebook(a, w, 3, %d); "
+            "print(json.dumps([time.perf_counter() - t, it]))" % (ROOT, n, passes))
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True)
+    if r.returncode != 0:
+        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
+    t, it = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": round(8 * n * it / t / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"one head, {n} samples, 3 bits, {it} passes in {t:.2f} s", "cpu": _cpu_model()}
+
+
+def run_fit(args):
+    """Sensitivity-weighted codebook fitting ([KVQ] Algorithm 2) for one layer: 32 KV heads of
+    16 x 2048 x 128 samples each, 3 bits. The roofline is one Lloyd pass (kvq_fit_codebook with
+    max_iter = 1: every sample read once, 8 bytes); the JSON line also carries the time of a whole
+    fit (max_iter = 50)."""
+    import torch
+    import bit_kv_cache_block_gb300 as K
+    import __graft_entry__
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    __graft_entry__.build()
+    lib = K._lib.lib()
+    H, n = FIT_HEADS, FIT_SAMPLES
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1)
+    a = torch.tanh(0.8 * torch.randn(H, n, device=dev, generator=gen))
+    g = torch.randn(H, n, device=dev, generator=gen) ** 2
+    w = g / g.amax(dim=1, keepdim=True)
+    del g
+    cb = torch.empty(H, 8, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(16, int(lib.kvq_fit_codebook_workspace_bytes(H, n))), dtype=torch.uint8, device=dev)
+    st = torch.cuda.current_stream()
+
+    def fit(max_iter):
+        K._lib.check(lib.kvq_fit_codebook(K._ptr(a), K._ptr(w), H, n, 3, max_iter, K._ptr(cb), K._ptr(ws),
+                                          ws.numel(), K._stream(st)), "kvq_fit_codebook")
+
+    def timed(fn, reps):
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        for _ in range(reps):
+            fn()
+        e1.record(st)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    for _ in range(args.warmup):
+        fit(1)
+    fit(50)
+    torch.cuda.synchronize()
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(0).uuid)
+    except Exception:
+        gpu_id = "0"
+    reps_full = max(3, args.steps // 20)
+    with Clocks(gpu_id) as clk:
+        torch.cuda.synchronize()
+        ms = timed(lambda: fit(1), args.steps)
+        full_ms = timed(lambda: fit(50), reps_full)
+        torch.cuda.synchronize()
+    alg = 8 * H * n
+    gbs = alg / (ms * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    res = {
+        "metric": "codebook-fit GB/s (one weighted Lloyd pass, 8 B per sample)", "value": round(gbs, 1),
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32 samples, exact int64 fixed-point sums", "data": "synthetic (torch device generator, seeded)",
+        "config": {"workload": "nuq3 codebook fit, one LLaMA-7B layer: 32 KV heads x 16 x 2048 x 128 samples",
+                   "n_heads": H, "samples_per_head": n, "bits": 3,
+                   "l2": f"inputs {alg / 2**20:.0f} MiB per pass (> L2)"},
+        "us_per_pass": round(1e3 * ms, 2), "ms_whole_fit_max_iter_50": round(full_ms, 3),
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None, "traffic_source": "not captured",
+                     "kernel": "assign_kernel + update_kernel (kvq_fit_codebook, max_iter 1)",
+                     "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": alg},
+        "gpu_launches": 3 * args.steps + 101 * reps_full,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline:
+        res["cpu_baseline"] = _fit_cpu(1 << 23, 20)
+    return res
+
+
 def _decode_kernel_name(w):
     """The decode kernel the library picks for this workload (mirrors its dispatch rules)."""
     if w.method == "nuq" and w.bits == 3 and w.group == 1 and w.pre_rope:
@@ -710,9 +810,13 @@ def main():
                     help="absmax workload: channels per scale")
     ap.add_argument("--diag", action="store_true",
                     help="time the error diagnostics (kvq_error_stats, kvq_error_topk) instead of decode")
+    ap.add_argument("--fit", action="store_true",
+                    help="time the sensitivity-weighted codebook fitting (kvq_fit_codebook) instead of decode")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    if args.diag:
+    if args.fit:
+        res = run_fit(args) if args.impl == "kvq" else {"impl": "reference", "unavailable": "--fit has no CPU arm"}
+    elif args.diag:
         res = run_diag(args) if args.impl == "kvq" else {"impl": "reference", "unavailable": "--diag has no CPU arm"}
     else:
         res = run_reference(args) if args.impl == "reference" else run_kvq(args)

@@ -345,11 +345,14 @@ kvq_status kvq_error_stats(const kvq_cache* cache, const void* k, const void* v,
  * stops, else each centre whose members weigh more than zero moves to their weighted mean. The
  * sums are exact: w*a and w are scaled by 2^32, rounded half-even to 64-bit integers and added
  * as integers; a centre is the fp64 quotient of its two sums rounded to fp32. So the codebook
- * does not depend on thread order, and the CPU model reproduces it bit for bit.
+ * does not depend on thread order, and the CPU model reproduces it bit for bit. (The kernels
+ * stop a head when an update leaves its centres unchanged, one pass after the rule above at most,
+ * with the same centres; so the result is the same for every max_iter.) Inputs must be finite.
  *   a, w     : device fp32 [n_heads][n], 4-byte aligned; 1 <= n <= 2^30
  *   bits     : 1..4;  max_iter: 1..10000 iterations at most
  *   codebook : device fp32 [n_heads][2^bits] (written; usable as kvq_cache_init's codebook)
- *   workspace: device scratch of kvq_fit_codebook_workspace_bytes(n_heads, n) bytes
+ *   workspace: device scratch of kvq_fit_codebook_workspace_bytes(n_heads, n) bytes (16-byte
+ *              aligned; 272 bytes per head, whatever n)
  * Every step runs on `stream` with no host synchronisation. */
 size_t kvq_fit_codebook_workspace_bytes(int32_t n_heads, int64_t n);
 kvq_status kvq_fit_codebook(const float* a, const float* w, int32_t n_heads, int64_t n, int32_t bits,

@@ -1,8 +1,9 @@
 """Sensitivity-weighted nuq codebook fitting ([KVQ] Algorithm 2) on the GPU: the codebook of
 every head equals the oracle's bit for bit (its sums are exact 64-bit fixed point, so thread
 order cannot matter), for 1..4 bits, one to several heads, sample counts that are not multiples
-of the CTA size, zero weights, out-of-range inputs (clamped), and iteration caps that stop before
-convergence. A fitted codebook then drives a nuq cache whose decode matches the oracle."""
+of the CTA size, zero weights, out-of-range inputs (clamped), iteration caps that stop before
+convergence, and samples so close together that the fitted centres are nearly equal (the
+kernels' plain-argmin path). A fitted codebook then drives a nuq cache whose decode matches the oracle."""
 import numpy as np
 import pytest
 
@@ -28,6 +29,8 @@ def _samples(H, n, seed, kind):
         a = np.tanh(0.8 * rng.standard_normal((H, n)))
     elif kind == "wide":      # includes values outside [-1, 1] (clamped)
         a = 1.3 * rng.standard_normal((H, n))
+    elif kind == "tiny":      # all within 1e-7 of 0: the fitted centres end up closer than 2^-21,
+        a = 5e-8 * rng.standard_normal((H, n))  # where the kernels fall back to the plain argmin
     else:                     # uniform
         a = rng.uniform(-1, 1, (H, n))
     w = rng.uniform(0, 1, (H, n)) ** 2
@@ -39,7 +42,8 @@ def _samples(H, n, seed, kind):
 
 @pytest.mark.parametrize("H,n,bits,max_iter,kind", [
     (1, 1, 3, 5, "normal"), (1, 300, 1, 20, "uniform"), (2, 5000, 2, 30, "normal"), (3, 20011, 3, 50, "wide"),
-    (4, 65536, 4, 40, "normal"), (2, 100003, 3, 3, "normal"), (8, 4096, 3, 200, "uniform")])
+    (4, 65536, 4, 40, "normal"), (2, 100003, 3, 3, "normal"), (8, 4096, 3, 200, "uniform"),
+    (1, 5000, 2, 30, "tiny"), (2, 3001, 3, 30, "tiny")])
 def test_fit_codebook_matches_oracle(H, n, bits, max_iter, kind):
     import torch
     import bit_kv_cache_block_gb300 as K
