@@ -691,6 +691,18 @@ def _fit_cpu(n, passes):
             "sample": f"one head, {n} samples, 3 bits, {it} passes in {t:.2f} s", "cpu": _cpu_model()}
 
 
+FIT_TRAFFIC = (1077113088, "kvq_fit.cu")   # dram read + write bytes of one assign_kernel launch (ncu)
+FIT_TRAFFIC_SHA = "73c2a64531debfc9"   # sha256 prefix of kvq_fit.cu as captured
+
+
+def _fit_traffic():
+    """The ncu traffic of the fit pass, or None once kvq_fit.cu has changed since the capture."""
+    import hashlib
+    path = os.path.join(ROOT, "bit_kv_cache_block_gb300", "csrc", FIT_TRAFFIC[1])
+    h = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    return FIT_TRAFFIC[0] if h == FIT_TRAFFIC_SHA else None
+
+
 def run_fit(args):
     """Sensitivity-weighted codebook fitting ([KVQ] Algorithm 2) for one layer: 32 KV heads of
     16 x 2048 x 128 samples each, 3 bits. The roofline is one Lloyd pass (kvq_fit_codebook with
@@ -755,7 +767,8 @@ def run_fit(args):
                    "l2": f"inputs {alg / 2**20:.0f} MiB per pass (> L2)"},
         "us_per_pass": round(1e3 * ms, 2), "ms_whole_fit_max_iter_50": round(full_ms, 3),
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gbs / peak, 4), "traffic": None, "traffic_source": "not captured",
+                     "frac": round(gbs / peak, 4), "traffic": _fit_traffic(),
+                     "traffic_source": "ncu capture of assign_kernel at this workload",
                      "kernel": "assign_kernel + update_kernel (kvq_fit_codebook, max_iter 1)",
                      "peak_source": f"{peak_kind} hbm_gbs", "algorithmic_bytes": alg},
         "gpu_launches": 3 * args.steps + 101 * reps_full,
