@@ -408,6 +408,26 @@ def csr_of(x: np.ndarray, mask: np.ndarray):
     return row_ptr.astype(np.uint16), cc.astype(np.uint8), val
 
 
+def csc_of(x: np.ndarray, mask: np.ndarray):
+    """CSC with columns = channels, the value storage of [KVQ] §3.4 ("by column"):
+    col_ptr uint16[129], row uint8[nnz] (token), val fp16 bits uint16[nnz], entries sorted by
+    (channel, token)."""
+    counts = mask.sum(axis=0)
+    col_ptr = np.zeros(D + 1, np.int64)
+    col_ptr[1:] = np.cumsum(counts)
+    cc, tt = np.nonzero(np.asarray(mask).T)  # column-major order: sorted by (c, t)
+    val = np.asarray(x, np.float32)[tt, cc].astype(np.float16).view(np.uint16)
+    return col_ptr.astype(np.uint16), tt.astype(np.uint8), val
+
+
+def to_csc(rec: dict, x: np.ndarray) -> dict:
+    """The same quantised tile with its outliers stored by column (the outlier set, codes and
+    metadata unchanged): keys col_ptr, row, val replace row_ptr, col, val."""
+    out = {k: v for k, v in rec.items() if k not in ("row_ptr", "col", "val")}
+    out["col_ptr"], out["row"], out["val"] = csc_of(x, rec["mask"])
+    return out
+
+
 def nuq_meta(x: np.ndarray, mask: np.ndarray, axis: int):
     """Centre zp and half-range s of the non-outlier entries of each group
     ([KVQ] Algorithm 1 offline step 4: normalise to [-1,1] excluding outliers):
@@ -505,9 +525,10 @@ def nuq_quantize_calibrated(x: np.ndarray, codebook: np.ndarray, tau, s16, zp16,
     return dict(codes=codes, s16=s16.copy(), zp16=zp16.copy(), mask=mask, row_ptr=row_ptr, col=col, val=val)
 
 
-def nuq_dequant(codes, s16, zp16, codebook, axis: int, row_ptr=None, col=None, val=None):
+def nuq_dequant(codes, s16, zp16, codebook, axis: int, row_ptr=None, col=None, val=None, col_ptr=None, row=None):
     """x_dq = C[q]*s + zp, then the fp16 outliers are added back
-    ([KVQ] Algorithm 1 dequantisation: K_hat[mask] += outlier_vals)."""
+    ([KVQ] Algorithm 1 dequantisation: K_hat[mask] += outlier_vals), from CSR (row_ptr, col,
+    val) or from CSC (col_ptr, row, val)."""
     c = np.asarray(codebook, np.float64)[np.asarray(codes, np.intp)]
     s = np.asarray(s16, np.float64)
     zp = np.asarray(zp16, np.float64)
@@ -517,6 +538,11 @@ def nuq_dequant(codes, s16, zp16, codebook, axis: int, row_ptr=None, col=None, v
         for t in range(T):
             for j in range(int(row_ptr[t]), int(row_ptr[t + 1])):
                 x[t, int(col[j])] += vals[j]
+    if col_ptr is not None:
+        vals = np.asarray(val, np.uint16).view(np.float16).astype(np.float64)
+        for c in range(D):
+            for j in range(int(col_ptr[c]), int(col_ptr[c + 1])):
+                x[int(row[j]), c] += vals[j]
     return x
 
 
@@ -681,12 +707,14 @@ class OracleCache:
     token of every sequence in the input precision ([KVQ] §3.5): its K and V rows of block 0 are
     zero in the quantised tiles, and decode attends the kept rows at position 0 instead of the
     quantised token 0.
+
+    nuq only: v_csc = True stores the value tiles' outliers by column (to_csc).
     """
 
     def __init__(self, method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: int,
                  pre_rope: bool = False, rope_theta: float = 10000.0, outlier_frac: float = 0.01,
                  varn_iters: int = 8, use_hadamard: bool = True, codebook=None, layout: int = LAYOUT_ROWS,
-                 key_calib=None, sink: bool = False, scale_group: int = 128):
+                 key_calib=None, sink: bool = False, scale_group: int = 128, v_csc: bool = False):
         assert method in ("rtn", "nuq", "varn", "int4")
         assert scale_group == 128 or method == "int4"
         self.scale_group = scale_group
@@ -701,6 +729,8 @@ class OracleCache:
             self.n_out = n_outliers(outlier_frac)
         assert (key_calib is None and not sink) or method == "nuq"
         self.key_calib, self.sink = key_calib, bool(sink)
+        assert not v_csc or method == "nuq"
+        self.v_csc = bool(v_csc)
         self.sink_kv = {}  # (b, h) -> (k row, v row) of the first token
         self.recs = {}
         self.n_blocks = 0
@@ -725,6 +755,8 @@ class OracleCache:
             rec = nuq_quantize_calibrated(x, self.codebook[h], tau, s16, zp16, self.n_out)
         elif m == "nuq":
             rec = nuq_quantize(x, self.codebook[h], 0 if kind == KIND_K else 1, self.n_out)
+            if kind == KIND_V and self.v_csc:
+                rec = to_csc(rec, x)
         else:
             rec = varn_quantize(x, b, kind, self.varn_iters, self.use_hadamard)
         rec["words"] = pack_tile(rec["codes"], b, kind, self.layout)
@@ -761,8 +793,8 @@ class OracleCache:
         elif m == "int4":
             x = absmax_dequant(absmax_from_codes(codes, self.bits), rec["s16"])
         elif m == "nuq":
-            x = nuq_dequant(codes, rec["s16"], rec["zp16"], self.codebook[h],
-                            0 if kind == KIND_K else 1, rec["row_ptr"], rec["col"], rec["val"])
+            x = nuq_dequant(codes, rec["s16"], rec["zp16"], self.codebook[h], 0 if kind == KIND_K else 1,
+                            rec.get("row_ptr"), rec.get("col"), rec["val"], rec.get("col_ptr"), rec.get("row"))
         else:
             x = varn_dequant(codes, rec["s16"], rec["z16"], rec["s1"], kind)
             if domain == "input" and self.use_hadamard:

@@ -289,3 +289,14 @@ def test_codebook_ties_to_the_higher_centre_are_caught(monkeypatch):
     monkeypatch.setattr(O, "fit_codebook", flipped)
     assert _fails(P.test_fit_codebook_converged_state_and_ties)
 
+
+
+def test_csc_in_row_order_is_caught(monkeypatch):
+    def row_order(x, mask):  # entries left in (token, channel) order under column pointers
+        col_ptr = np.zeros(O.D + 1, np.int64)
+        col_ptr[1:] = np.cumsum(np.asarray(mask).sum(axis=0))
+        tt, cc = np.nonzero(mask)
+        return col_ptr.astype(np.uint16), tt.astype(np.uint8), np.asarray(x, np.float32)[tt, cc].astype(np.float16).view(np.uint16)
+    monkeypatch.setattr(K, "csc_of", row_order)
+    monkeypatch.setattr(O, "csc_of", row_order)
+    assert _fails(P.test_csc_of_brute_force_and_same_entries_as_csr)

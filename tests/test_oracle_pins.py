@@ -396,6 +396,54 @@ def test_nuq_quantize_csr_and_bound():
         assert np.all(err[r["mask"]] <= lim[r["mask"]])
 
 
+def test_csc_of_brute_force_and_same_entries_as_csr():
+    """Value outliers by column ([KVQ] §3.4): column pointers and the per-entry token, built
+    here by plain loops over channels then tokens, and the (token, channel, value) set equals
+    the CSR's."""
+    rng = np.random.default_rng(11)
+    x = rng.standard_normal((O.T, O.D)).astype(np.float32)
+    for frac in (0.0, 0.01, 0.05, 0.3):
+        mask = rng.uniform(size=x.shape) < frac
+        mask[5, :] = True   # a full row
+        mask[:, 77] = True  # a full column
+        col_ptr, row, val = O.csc_of(x, mask)
+        cp, rr, vv = [0], [], []
+        for c in range(O.D):
+            for t in range(O.T):
+                if mask[t, c]:
+                    rr.append(t)
+                    vv.append(np.float16(x[t, c]).view(np.uint16))
+            cp.append(len(rr))
+        assert col_ptr.tolist() == cp and row.tolist() == rr and val.tolist() == [int(v) for v in vv]
+        row_ptr, col, val_r = O.csr_of(x, mask)
+        csr_set = {(t, int(col[j]), int(val_r[j])) for t in range(O.T) for j in range(int(row_ptr[t]), int(row_ptr[t + 1]))}
+        csc_set = {(int(row[j]), c, int(val[j])) for c in range(O.D) for j in range(int(col_ptr[c]), int(col_ptr[c + 1]))}
+        assert csr_set == csc_set and len(csc_set) == int(mask.sum())
+
+
+def test_csc_tiles_dequantise_and_decode_like_csr():
+    """The storage order of the value outliers changes nothing: dequantised tiles and the cache's
+    decode are identical for CSR and CSC value tiles, for 1% and 5% outliers."""
+    for frac in (0.01, 0.05):
+        w = WL.WORKLOADS[2].scaled(batch=1, n_kv_heads=2, n_q_heads=2, ctx=2 * 128, outlier_frac=frac)
+        K, V = WL.blocks(w, 0, w.n_blocks)
+        caches = []
+        for csc in (False, True):
+            oc = O.OracleCache.for_workload(w, v_csc=csc)
+            oc.append(K, V)
+            caches.append(oc)
+        for key in caches[0].recs:
+            a, b = caches[0].recs[key], caches[1].recs[key]
+            if key[3] == O.KIND_V:
+                assert "col_ptr" in b and "row_ptr" not in b
+                assert int(b["col_ptr"][-1]) == int(a["row_ptr"][-1]) == O.n_outliers(frac)
+            assert np.array_equal(caches[0].dequant_tile(a, key[3], key[1], key[2], "attn"),
+                                  caches[1].dequant_tile(b, key[3], key[1], key[2], "attn"))
+        q = WL.query(w)
+        tk, tv = WL.tail(w, 9)
+        assert np.array_equal(caches[0].decode(q, tk, tv), caches[1].decode(q, tk, tv))
+
+
 def test_nuq_lossless_on_codebook_grid():
     cb = np.array([-1, -0.75, -0.5, -0.25, 0.25, 0.5, 0.75, 1.0], np.float32)
     rng = np.random.default_rng(5)
