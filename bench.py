@@ -46,14 +46,14 @@ BENCH_LAYOUT = "mma"
 # shared header); once they change the traffic reads null until a new capture replaces it.
 # Captures and commands: profiles/dram_traffic_decode_kernels.md.
 PROFILED_TRAFFIC = {
-    2: {"bytes_per_record": 14867.6, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
-        "sha256_16": "9fc7b31bdc440fab", "capture": "same workload at L = 16384 (4096 records)"},
-    3: {"bytes_per_record": 9789.4, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "285b5a378333c7f9", "capture": "full workload (8192 records)"},
-    4: {"bytes_per_record": 17094.0, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "285b5a378333c7f9", "capture": "same workload at L = 4096 (8192 records)"},
-    5: {"bytes_per_record": 9276.4, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "285b5a378333c7f9", "capture": "same workload at L = 65536 (16384 records)"},
+    2: {"bytes_per_record": 14868.3, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
+        "sha256_16": "a31b66c4928f1fc8", "capture": "same workload at L = 16384 (4096 records)"},
+    3: {"bytes_per_record": 9791.8, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "2c3fc1268b83079d", "capture": "full workload (8192 records)"},
+    4: {"bytes_per_record": 17071.1, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "2c3fc1268b83079d", "capture": "same workload at L = 4096 (8192 records)"},
+    5: {"bytes_per_record": 9288.4, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "2c3fc1268b83079d", "capture": "same workload at L = 65536 (16384 records)"},
 }
 
 
@@ -228,11 +228,11 @@ def run_kvq(args):
     w = _workload(args)
     nb = w.n_blocks
     n_pages = w.batch * (nb + 1) if args.paged else 0
-    if (args.key_calib or args.sink) and w.method != "nuq":
-        raise SystemExit("--key-calib and --sink apply to nuq workloads")
+    if (args.key_calib or args.sink or args.v_csc) and w.method != "nuq":
+        raise SystemExit("--key-calib, --sink and --v-csc apply to nuq workloads")
     cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, nb + 1, w.dtype, w.pre_rope,
                         w.rope_theta, w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT, n_pages, args.key_calib,
-                        args.sink, w.scale_group)
+                        args.sink, w.scale_group, args.v_csc)
     table = None
     if args.paged:  # every block on a page of a shuffled pool
         perm = torch.randperm(n_pages, generator=torch.Generator().manual_seed(5 + rank)).to(torch.int32)
@@ -372,7 +372,7 @@ def run_kvq(args):
                    "decodes_per_step": DECODES_PER_STEP, "tail_tokens": "0..127",
                    "layout": BENCH_LAYOUT, "scale_group": w.scale_group,
                    "paged": bool(args.paged), "key_calib": bool(args.key_calib),
-                   "sink": bool(args.sink),
+                   "sink": bool(args.sink), "v_csc": bool(args.v_csc),
                    "packed_bytes_per_decode": cache_bytes, "cache_copies": n_copies,
                    "l2": f"{n_copies} cache copies rotated ({n_copies * int(lay.records_bytes) / 2**20:.0f} MiB > 3x L2)",
                    "parallelism": f"replicas x{world}"},
@@ -813,6 +813,7 @@ def main():
     ap.add_argument("--key-calib", dest="key_calib", action="store_true",
                     help="nuq: offline-calibrated key statistics (calibration keys drawn with another seed)")
     ap.add_argument("--sink", action="store_true", help="nuq: keep the first token in the input precision")
+    ap.add_argument("--v-csc", dest="v_csc", action="store_true", help="nuq: value outliers stored by column (CSC)")
     ap.add_argument("--paged", action="store_true",
                     help="records on the pages of a shuffled pool, found through a block table")
     ap.add_argument("--cpu-sample-heads", type=int, default=10)

@@ -31,7 +31,7 @@ def make_config(method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: 
                 in_dtype: str = "f16", pre_rope: bool = False, rope_theta: float = 10000.0,
                 outlier_frac: float = 0.01, varn_iters: int = 8, hadamard: bool = True,
                 layout: str = "rows", n_pages: int = 0, key_calib: bool = False, sink: bool = False,
-                scale_group: int = 128) -> kvq_config:
+                scale_group: int = 128, v_csc: bool = False) -> kvq_config:
     c = kvq_config()
     c.method = METHODS[method] if isinstance(method, str) else int(method)
     c.bits, c.batch, c.n_kv_heads, c.n_q_heads = bits, batch, n_kv_heads, n_q_heads
@@ -47,6 +47,7 @@ def make_config(method: str, bits: int, batch: int, n_kv_heads: int, n_q_heads: 
     c.key_calib = int(bool(key_calib))
     c.sink = int(bool(sink))
     c.scale_group = int(scale_group)
+    c.v_csc = int(bool(v_csc))
     return c
 
 

@@ -35,7 +35,8 @@ class kvq_config(C.Structure):
                 ("max_blocks", C.c_int32), ("in_dtype", C.c_int32), ("pre_rope", C.c_int32),
                 ("rope_theta", C.c_double), ("outlier_frac", C.c_float), ("varn_iters", C.c_int32),
                 ("hadamard", C.c_int32), ("layout", C.c_int32), ("n_pages", C.c_int32),
-                ("key_calib", C.c_int32), ("sink", C.c_int32), ("scale_group", C.c_int32)]
+                ("key_calib", C.c_int32), ("sink", C.c_int32), ("scale_group", C.c_int32),
+                ("v_csc", C.c_int32)]
 
 
 class kvq_layout_t(C.Structure):

@@ -50,6 +50,8 @@ kvq_status check_config(const kvq_config* c) {
   if (c->method == KVQ_INT4 && c->bits != 4 && c->bits != 8) return KVQ_ERR_UNSUPPORTED;
   if (c->scale_group != 0 && c->scale_group != 128 && c->scale_group != 64) return KVQ_ERR_INVALID_ARG;
   if (c->scale_group == 64 && c->method != KVQ_INT4) return KVQ_ERR_UNSUPPORTED;
+  if (c->v_csc != 0 && c->v_csc != 1) return KVQ_ERR_INVALID_ARG;
+  if (c->v_csc && c->method != KVQ_NUQ) return KVQ_ERR_UNSUPPORTED;
   if (c->pre_rope != 0 && c->pre_rope != 1) return KVQ_ERR_INVALID_ARG;
   if (c->pre_rope && c->method != KVQ_NUQ) return KVQ_ERR_UNSUPPORTED;
   if (c->pre_rope && !(c->rope_theta > 1.0)) return KVQ_ERR_INVALID_ARG;

@@ -402,25 +402,48 @@ __global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
       int n_total = 0;
       int pos = block_excl_scan(n_sel, sm->scan, &n_total);
       uint16_t* val = reinterpret_cast<uint16_t*>(csr);
-      uint16_t* row_ptr = reinterpret_cast<uint16_t*>(csr + 2 * n_out);
-      uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
-      if ((tid & 1) == 0) row_ptr[t0] = (uint16_t)pos;
-      if (tid == 0) row_ptr[T] = (uint16_t)n_total;
+      uint16_t* ptr = reinterpret_cast<uint16_t*>(csr + 2 * n_out);  // row_ptr (CSR) or col_ptr (CSC)
+      uint8_t* idx = csr + 2 * n_out + 2 * (T + 1);                   // channel (CSR) or token (CSC)
       for (int i = n_total + tid; i < n_out; i += AP_THREADS) {  // unused capacity (calibrated keys)
         val[i] = 0;
-        col[i] = 0;
+        idx[i] = 0;
       }
       sm->mask[e0 >> 5] = (uint32_t)selbits;
       sm->mask[(e0 >> 5) + 1] = (uint32_t)(selbits >> 32);
-      for (int j = 0; j < 64; ++j) {
-        if (selbits >> j & 1) {
-          if (pos < n_out) {
-            val[pos] = f2h_rn(sm->x[t0 * XS + c0 + j]);
-            col[pos] = (uint8_t)(c0 + j);
-          } else {
-            report(a.status, KVQ_ERR_INVALID_ARG);
+      if (!(g.v_csc && kind == 1)) {  // CSR: thread (t0, half) writes its row segment in channel order
+        if ((tid & 1) == 0) ptr[t0] = (uint16_t)pos;
+        if (tid == 0) ptr[T] = (uint16_t)n_total;
+        for (int j = 0; j < 64; ++j) {
+          if (selbits >> j & 1) {
+            if (pos < n_out) {
+              val[pos] = f2h_rn(sm->x[t0 * XS + c0 + j]);
+              idx[pos] = (uint8_t)(c0 + j);
+            } else {
+              report(a.status, KVQ_ERR_INVALID_ARG);
+            }
+            ++pos;
           }
-          ++pos;
+        }
+      } else {  // CSC values: thread c writes column c in token order
+        __syncthreads();  // every mask word written
+        int cnt = 0;
+        if (tid < D)
+          for (int t = 0; t < T; ++t) cnt += (int)(sm->mask[(t * D + tid) >> 5] >> (tid & 31) & 1u);
+        int cpos = block_excl_scan(cnt, sm->scan, nullptr);
+        if (tid < D) {
+          ptr[tid] = (uint16_t)cpos;
+          if (tid == 0) ptr[D] = (uint16_t)n_total;
+          for (int t = 0; t < T; ++t) {
+            if (sm->mask[(t * D + tid) >> 5] >> (tid & 31) & 1u) {
+              if (cpos < n_out) {
+                val[cpos] = f2h_rn(sm->x[t * XS + tid]);
+                idx[cpos] = (uint8_t)t;
+              } else {
+                report(a.status, KVQ_ERR_INVALID_ARG);
+              }
+              ++cpos;
+            }
+          }
         }
       }
       // zero the padding of the CSR region so that records are deterministic

@@ -289,24 +289,37 @@ __global__ void __launch_bounds__(DC_THREADS) decode_kernel(DecodeArgs a) {
       const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
       const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * g.n_out);
       const uint8_t* col = csr + 2 * g.n_out + 2 * (T + 1);
-      uint8_t* vtag = reinterpret_cast<uint8_t*>(sm + 1);  // the token of each entry
-      {
-        const int j1 = min((int)rp[t + 1], g.n_out);
-        for (int j = min((int)rp[t], g.n_out); j < j1; ++j) vtag[j] = (uint8_t)t;
-      }
-      __syncthreads();
-      // thread c adds the entries of channel c in entry order (the sum does not depend on timing)
-      const int c = tid, n_v = min((int)rp[T], g.n_out);
+      // thread c adds the entries of channel c in token order (the sum does not depend on timing,
+      // and it is the same for CSR and CSC tiles)
+      const int c = tid;
       float acc[GMAX];
 #pragma unroll
       for (int k = 0; k < GMAX; ++k) acc[k] = 0.0f;
-      for (int j = 0; j < n_v; ++j) {
-        if ((col[j] & (D - 1)) != c) continue;
-        const int tj = vtag[j];
-        const float v = h2f(val[j]);
+      if (g.v_csc) {  // column c is one run of entries; rp is the column pointer, col the token
+        const int j1 = min((int)rp[c + 1], g.n_out);
+        for (int j = min((int)rp[c], g.n_out); j < j1; ++j) {
+          const int tj = col[j] & (T - 1);
+          const float v = h2f(val[j]);
 #pragma unroll
-        for (int k = 0; k < GMAX; ++k)
-          if (k < G) acc[k] = fmaf(sm->pv[k][tj], v, acc[k]);
+          for (int k = 0; k < GMAX; ++k)
+            if (k < G) acc[k] = fmaf(sm->pv[k][tj], v, acc[k]);
+        }
+      } else {
+        uint8_t* vtag = reinterpret_cast<uint8_t*>(sm + 1);  // the token of each entry
+        {
+          const int j1 = min((int)rp[t + 1], g.n_out);
+          for (int j = min((int)rp[t], g.n_out); j < j1; ++j) vtag[j] = (uint8_t)t;
+        }
+        __syncthreads();
+        const int n_v = min((int)rp[T], g.n_out);
+        for (int j = 0; j < n_v; ++j) {
+          if ((col[j] & (D - 1)) != c) continue;
+          const int tj = vtag[j];
+          const float v = h2f(val[j]);
+#pragma unroll
+          for (int k = 0; k < GMAX; ++k)
+            if (k < G) acc[k] = fmaf(sm->pv[k][tj], v, acc[k]);
+        }
       }
 #pragma unroll
       for (int k = 0; k < GMAX; ++k)

@@ -163,6 +163,17 @@ __device__ __forceinline__ void bar_group(int grp) { asm volatile("bar.sync %0, 
 
 __device__ __forceinline__ uint32_t stage_bytes(const Geo& g) { return (uint32_t)g.rec_bytes + ROPE_ROW; }
 
+// Per-stage outlier area (after the ring and Smem): the token tag of each key outlier
+// [round16(n)], the run index of each value outlier [round16(n)] (token for CSR value tiles,
+// channel for CSC ones), and for CSC value tiles the permutation grouping the value entries by
+// consumer warp (uint16 [n], 16-byte padded) followed by the 9 group offsets (uint16, 32 bytes).
+__host__ __device__ inline int csc_off_of(int n_out) {  // from the value tags to the offsets
+  return (int)round16((uint64_t)n_out) + (int)round16(2 * (uint64_t)n_out);
+}
+__host__ __device__ inline int rows_stride_of(int n_out, bool csc) {
+  return 2 * (int)round16((uint64_t)n_out) + (csc ? (int)round16(2 * (uint64_t)n_out) + 32 : 0);
+}
+
 template <uint32_t R>
 __device__ __forceinline__ void regs_inc() {
   asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(R));
@@ -224,7 +235,7 @@ __device__ void producer(const Args& a, Smem* sm, uint8_t* ring, long long x0, i
 //     v * (R(t)^T q_b)_c    (entry e = (t, c, v) of the CSR)
 // and, after a group barrier, the sum sk[t] of each of its two tokens' terms in entry order.
 // The consumers scatter p_t * v for the value outliers.
-template <int NBS>
+template <int NBS, bool CSC>
 __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows, int rows_stride, long long x0,
                           int n, int ax) {
   const Geo& g = a.g;
@@ -242,6 +253,9 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
   float2 qv = make_float2(0.0f, 0.0f);
   float* qb = sm->qb[grp];
   float* kterm = reinterpret_cast<float*>(rows + (size_t)NBS * rows_stride) + grp * tag_bytes;  // per group
+  // CSC value tiles: per group, entries per consumer warp [8] and the scatter cursors [8]
+  int* gcnt = reinterpret_cast<int*>(reinterpret_cast<float*>(rows + (size_t)NBS * rows_stride) + 2 * tag_bytes) +
+              grp * 16;
   const int tA = j, tB = j + 64;
   for (int p = grp; p < n; p += 2) {
     if (u != cur_u) {
@@ -284,8 +298,28 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
         for (int e = kb0; e < kb1; ++e) ktag[e] = (uint8_t)tB;
         for (int e = va0; e < va1; ++e) vtag[e] = (uint8_t)tA;
         for (int e = vb0; e < vb1; ++e) vtag[e] = (uint8_t)tB;
+        if (CSC && j < 16) gcnt[j] = 0;
       }
       bar_group(grp);  // q_b and the key tags visible
+      if (CSC) {  // group the value entries by consumer warp (16 tokens each): count, offsets, scatter
+        const uint8_t* vtok = st + g.csr_off[1] + 2 * n_out + 2 * (T + 1);  // token of each entry
+        uint16_t* perm = reinterpret_cast<uint16_t*>(vtag + tag_bytes);
+        uint16_t* off = reinterpret_cast<uint16_t*>(vtag + csc_off_of(n_out));
+        const int n_v = min((int)rpv[T], n_out);
+        for (int e = j; e < n_v; e += 64) atomicAdd(&gcnt[(vtok[e] >> 4) & 7], 1);
+        bar_group(grp);
+        if (j == 0) {
+          int acc = 0;
+          for (int w = 0; w < 8; ++w) {
+            off[w] = (uint16_t)acc;
+            gcnt[8 + w] = acc;
+            acc += gcnt[w];
+          }
+          off[8] = (uint16_t)acc;
+        }
+        bar_group(grp);
+        for (int e = j; e < n_v; e += 64) perm[atomicAdd(&gcnt[8 + ((vtok[e] >> 4) & 7)], 1)] = (uint16_t)e;
+      }
       const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
       const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
       const int n_k = min((int)rp[T], n_out);
@@ -388,32 +422,50 @@ __device__ __forceinline__ void block_values(const uint8_t* st, const Geo& g, in
   }
 }
 
-// Value outliers of a consumer warp's tokens in one block (rw: the entries' token tags). Entry e
-// of the warp's token range goes to lane (e - e0) mod 32, which takes p of its token from the
-// token's owner lane and adds p * v to the warp's outv. The first 32 entries run as one batch
-// placed with the tensor-core work of the block; later ones loop.
-__device__ __forceinline__ void value_outlier_span(const uint8_t* st, const Geo& g, int warp, int& e0, int& e1) {
+// Value outliers of a consumer warp's tokens in one block. rw: the stage's value-outlier area
+// written by the aux warps: each entry's pointer-run index (the token for CSR tiles, the channel
+// for CSC tiles), then for CSC tiles a permutation of the entries that groups them by consumer
+// warp (16 tokens each) and the 9 group offsets. Entry k of the warp's span goes to lane
+// (k - e0) mod 32, which takes p of its token from the token's owner lane and adds p * v to the
+// warp's outv (integer atomics: the sum does not depend on the order). The first 32 entries run
+// as one batch placed with the tensor-core work of the block; later ones loop.
+template <bool CSC>
+__device__ __forceinline__ void value_outlier_span(const uint8_t* st, const uint8_t* rw, const Geo& g, int warp,
+                                                   int& e0, int& e1) {
   const int n_out = g.n_out;
-  const uint16_t* rp = reinterpret_cast<const uint16_t*>(st + g.csr_off[1] + 2 * n_out);
-  e0 = min((int)rp[16 * warp], n_out);
-  e1 = min((int)rp[16 * warp + 16], n_out);
+  if (CSC) {
+    const uint16_t* off = reinterpret_cast<const uint16_t*>(rw + csc_off_of(n_out));
+    e0 = off[warp];
+    e1 = off[warp + 1];
+  } else {
+    const uint16_t* rp = reinterpret_cast<const uint16_t*>(st + g.csr_off[1] + 2 * n_out);
+    e0 = min((int)rp[16 * warp], n_out);
+    e1 = min((int)rp[16 * warp + 16], n_out);
+  }
 }
 
-// Value-outlier entry e of the lane (e >= e1: none): p_t * v added to the warp's outv[c] in
+// Value-outlier entry k of the lane (k >= e1: none): p_t * v added to the warp's outv[c] in
 // fixed point (a shared-memory integer atomic; no branch, so it sits among the tensor-core work).
-__device__ __forceinline__ void value_outlier_entry(const uint8_t* st, const Geo& g, const uint8_t* rw, int e, int e1,
+template <bool CSC>
+__device__ __forceinline__ void value_outlier_entry(const uint8_t* st, const Geo& g, const uint8_t* rw, int k, int e1,
                                                     int t0, float p0, float p1, long long* outv) {
   const int n_out = g.n_out;
   const uint8_t* csr = st + g.csr_off[1];
   const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
-  const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
-  const bool valid = e < e1;
-  const int t = valid ? rw[e] : t0;
+  const uint8_t* idx = csr + 2 * n_out + 2 * (T + 1);  // CSR: channel; CSC: token
+  const bool valid = k < e1;
+  int e = k, t;
+  if (CSC) {
+    e = valid ? (int)reinterpret_cast<const uint16_t*>(rw + round16((uint64_t)n_out))[k] : 0;
+    t = valid ? idx[e] : t0;
+  } else {
+    t = valid ? rw[e] : t0;
+  }
   const int src = 4 * (t & 7);
   const float pa = __shfl_sync(0xffffffffu, p0, src), pb = __shfl_sync(0xffffffffu, p1, src);
   if (valid) {
     const float x = ((t & 8) ? pb : pa) * h2f(val[e]);
-    atomicAdd(reinterpret_cast<unsigned long long*>(&outv[col[e] & (D - 1)]),
+    atomicAdd(reinterpret_cast<unsigned long long*>(&outv[(CSC ? rw[e] : idx[e]) & (D - 1)]),
               (unsigned long long)llrintf(x * OUTV_ONE));
   }
 }
@@ -422,7 +474,7 @@ __device__ __forceinline__ void value_outlier_entry(const uint8_t* st, const Geo
 // the value product of block j and the scores of block j + 1 form one straight-line stretch, so
 // their dependency chains overlap. Its flash-decode state goes to its own partial row at the end
 // of each segment.
-template <int NBS>
+template <int NBS, bool CSC>
 __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uint8_t* rows, int rows_stride, long long R,
                          long long x0, int n, int warp, int lane) {
   const Geo& g = a.g;
@@ -520,20 +572,20 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
       l_w += p0 + p1;
       const uint8_t* rw = rows + (size_t)s * rows_stride + round16((uint64_t)g.n_out);
       int e0 = 0, e1 = 0;
-      if (g.n_out > 0) value_outlier_span(st, g, warp, e0, e1);
+      if (g.n_out > 0) value_outlier_span<CSC>(st, rw, g, warp, e0, e1);
       if (more) {
         if (!__all_sync(0xffffffffu, ready) && !wait_stage(j + 1)) return;
         const int s1 = (j + 1) % NBS;
-        value_outlier_entry(st, g, rw, e0 + lane, e1, t0, p0, p1, outv);
+        value_outlier_entry<CSC>(st, g, rw, e0 + lane, e1, t0, p0, p1, outv);
         block_values(st, g, warp, lane, t0, t1, src_a, xsel, ysel, p0, p1, tl0, tl1, th0, th1, z_w, acc);
         block_scores(ring + (size_t)s1 * sb, sm->op[s1], g.codes_off[0], warp, lane, brow, zrow, ones, t0, t1, tl0,
                      tl1, th0, th1, wcs, sv0, sv1);
       } else {
-        value_outlier_entry(st, g, rw, e0 + lane, e1, t0, p0, p1, outv);
+        value_outlier_entry<CSC>(st, g, rw, e0 + lane, e1, t0, p0, p1, outv);
         block_values(st, g, warp, lane, t0, t1, src_a, xsel, ysel, p0, p1, tl0, tl1, th0, th1, z_w, acc);
       }
       for (int e = e0 + 32 + lane; e - lane < e1; e += 32)  // more than 32 entries: uniform trip count
-        value_outlier_entry(st, g, rw, e, e1, t0, p0, p1, outv);
+        value_outlier_entry<CSC>(st, g, rw, e, e1, t0, p0, p1, outv);
       release(s);
     }
     // the segment's partial row
@@ -570,7 +622,7 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
   }
 }
 
-template <int NBS>
+template <int NBS, bool CSC>
 __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
   launch_dependents();  // the combine kernel may be scheduled once every CTA of this grid runs
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -578,7 +630,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
   uint8_t* ring = smem_raw;
   Smem* sm = reinterpret_cast<Smem*>(smem_raw + (size_t)NBS * stage_bytes(a.g));
   uint8_t* rows = reinterpret_cast<uint8_t*>(sm + 1);
-  const int rows_stride = 2 * (int)round16((uint64_t)a.g.n_out);
+  const int rows_stride = rows_stride_of(a.g.n_out, CSC);
   const long long R = blockIdx.x;
   if (R >= a.n_ranges) return;
   const long long x0 = R * a.total / a.n_ranges, x1 = (R + 1) * a.total / a.n_ranges;
@@ -604,17 +656,17 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
   __syncthreads();
   if (warp < NW) {
     regs_inc<REGS_CONSUMER>();
-    consumer<NBS>(a, sm, ring, rows, rows_stride, R, x0, n, warp, lane);
+    consumer<NBS, CSC>(a, sm, ring, rows, rows_stride, R, x0, n, warp, lane);
   } else {
     regs_dec<REGS_OTHER>();
-    if (warp < PRODUCER_WARP) aux_warps<NBS>(a, sm, ring, rows, rows_stride, x0, n, tid - NW * 32);
+    if (warp < PRODUCER_WARP) aux_warps<NBS, CSC>(a, sm, ring, rows, rows_stride, x0, n, tid - NW * 32);
     else if (warp == PRODUCER_WARP) producer<NBS>(a, sm, ring, x0, n, lane);
   }
 }
 
 size_t smem_bytes(const Geo& g) {
-  return (size_t)NB * ((size_t)g.rec_bytes + ROPE_ROW) + sizeof(Smem) + (size_t)NB * 2 * round16((uint64_t)g.n_out) +
-         2 * sizeof(float) * round16((uint64_t)g.n_out);
+  return (size_t)NB * ((size_t)g.rec_bytes + ROPE_ROW) + sizeof(Smem) + (size_t)NB * rows_stride_of(g.n_out, g.v_csc) +
+         2 * sizeof(float) * round16((uint64_t)g.n_out) + (g.v_csc ? 2 * 16 * sizeof(int) : 0);
 }
 
 }  // namespace nuqdec
@@ -642,7 +694,7 @@ long long kvq_nuq_ranges(const kvq::Geo& g) {
   using namespace kvq::nuqdec;
   if (!kvq_nuq_supported(g)) return 0;
   const size_t smem = smem_bytes(g);
-  auto fn = decode_nuq_kernel<NB>;
+  auto fn = g.v_csc ? decode_nuq_kernel<NB, true> : decode_nuq_kernel<NB, false>;
   int dev = 0, sms = 152, ctas = 1;
   if (cudaGetDevice(&dev) == cudaSuccess &&
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess) {
@@ -679,7 +731,7 @@ cudaError_t kvq_launch_decode_nuq(const kvq::Geo& g, const uint8_t* base, const 
                                   float* ws_o, int* status, cudaStream_t st) {
   using namespace kvq::nuqdec;
   const size_t smem = smem_bytes(g);
-  auto fn = decode_nuq_kernel<NB>;
+  auto fn = g.v_csc ? decode_nuq_kernel<NB, true> : decode_nuq_kernel<NB, false>;
   cudaError_t e = kvq::ensure_smem_attr((const void*)fn, smem);
   if (e != cudaSuccess) return e;
   Args a;

@@ -50,8 +50,16 @@ __device__ void dequant_row(const Geo& g, const uint8_t* rec, const float* codeb
     const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
     const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * g.n_out);
     const uint8_t* col = csr + 2 * g.n_out + 2 * (T + 1);
-    const int j1 = min((int)rp[t + 1], g.n_out);
-    for (int j = min((int)rp[t], g.n_out); j < j1; ++j) row[col[j] & (D - 1)] += h2f(val[j]);
+    if (g.v_csc && kind == 1) {  // by column: rp is the column pointer, col the token of each entry
+      for (int c = 0; c < D; ++c) {
+        const int j1 = min((int)rp[c + 1], g.n_out);
+        for (int j = min((int)rp[c], g.n_out); j < j1; ++j)
+          if (col[j] == t) row[c] += h2f(val[j]);
+      }
+    } else {
+      const int j1 = min((int)rp[t + 1], g.n_out);
+      for (int j = min((int)rp[t], g.n_out); j < j1; ++j) row[col[j] & (D - 1)] += h2f(val[j]);
+    }
   }
   if (g.method == KVQ_VARN && to_input) {
     for (int hh = 1; hh < D; hh <<= 1)
@@ -224,12 +232,22 @@ __global__ void __launch_bounds__(ES_THREADS, 2) error_stats_kernel(ErrArgs a) {
         const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
         const uint16_t* rp = reinterpret_cast<const uint16_t*>(csr + 2 * g.n_out);
         const uint8_t* col = csr + 2 * g.n_out + 2 * (T + 1);
-        const int e1 = min((int)rp[t + 1], g.n_out);
-        for (int e = min((int)rp[t], g.n_out); e < e1; ++e) {
-          const int c = col[e] & (D - 1);
-          const float vv = (c >> 4) == j8 ? h2f(val[e]) : 0.0f;
+        if (g.v_csc && kind == 1) {  // by column: the lane scans its 16 columns for token t
 #pragma unroll
-          for (int i = 0; i < 16; ++i) q[i] += (c & 15) == i ? vv : 0.0f;  // no indexed register
+          for (int i = 0; i < 16; ++i) {
+            const int c = 16 * j8 + i;
+            const int e1 = min((int)rp[c + 1], g.n_out);
+            for (int e = min((int)rp[c], g.n_out); e < e1; ++e)
+              if (col[e] == t) q[i] += h2f(val[e]);
+          }
+        } else {
+          const int e1 = min((int)rp[t + 1], g.n_out);
+          for (int e = min((int)rp[t], g.n_out); e < e1; ++e) {
+            const int c = col[e] & (D - 1);
+            const float vv = (c >> 4) == j8 ? h2f(val[e]) : 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) q[i] += (c & 15) == i ? vv : 0.0f;  // no indexed register
+          }
         }
       }
       if (to_input) {  // inverse Hadamard (H / sqrt(128) is its own inverse), Sylvester order

@@ -110,6 +110,7 @@ struct Geo {
   int sink;             // NUQ: the first token of each sequence is kept at sink_off
   uint64_t calib_off, sink_off;
   int g64;              // INT4: one scale per 64 channels (meta vectors: channels 0..63, 64..127)
+  int v_csc;            // NUQ: value outliers by column (col_ptr over channels, token per entry)
 };
 
 inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
@@ -133,6 +134,7 @@ inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
   g.calib_off = l.calib_off;
   g.sink_off = l.sink_off;
   g.g64 = c.method == KVQ_INT4 && c.scale_group == 64;
+  g.v_csc = c.method == KVQ_NUQ && c.v_csc;
   return g;
 }
 

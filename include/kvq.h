@@ -121,6 +121,10 @@ typedef struct {
   int32_t scale_group;   /* INT4 only: channels per absmax scale, 128 (also 0) or 64 ([TQ] §2.1:
                             a smaller block doubles the scale overhead). Other methods: 0 or 128.
                             Tiles with bits 8 or groups of 64 decode on the CUDA cores. */
+  int32_t v_csc;         /* NUQ only. 0: value outliers in CSR like the keys (rows = tokens).
+                            1: value outliers in CSC (columns = channels), the value storage of
+                            [KVQ] §3.4 ("by column"). Same region size and outlier set; decode
+                            results are bitwise those of the CSR cache. */
 } kvq_config;
 
 /* Byte layout of a cache, from kvq_layout. One record per (b, h, block), at
@@ -147,7 +151,10 @@ typedef struct {
  *           zp (centre). INT4: s (per token); with scale_group 64 two vectors, the scales
  *           of channels 0..63 of every token, then those of channels 64..127.
  *   csr   : NUQ only: val fp16[n_outliers], row_ptr uint16[129] (row = token),
- *           col uint8[n_outliers] (channel), zero padded.
+ *           col uint8[n_outliers] (channel), zero padded; entries in (token, channel) order.
+ *           A V tile of a v_csc cache holds the same arrays by column instead: val,
+ *           col_ptr uint16[129] (column = channel), row uint8[n_outliers] (token), entries in
+ *           (channel, token) order.
  * After the records, for pre-RoPE caches: a table of (cos, sin) fp32 pairs of
  * block*128*theta_i for block = 0..max_blocks, then of t*theta_i for t = 0..127 (64 pairs each),
  * written by kvq_cache_init. */

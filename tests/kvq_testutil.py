@@ -15,12 +15,12 @@ def torch_mod():
     return torch
 
 
-def cfg_for(w: WL.Workload, max_blocks=None, batch=None, layout="rows"):
+def cfg_for(w: WL.Workload, max_blocks=None, batch=None, layout="rows", v_csc=False):
     import bit_kv_cache_block_gb300 as K
     return K.make_config(w.method, w.bits, batch or w.batch, w.n_kv_heads, w.n_q_heads,
                          max_blocks or w.n_blocks, in_dtype=w.dtype, pre_rope=w.pre_rope,
                          rope_theta=w.rope_theta, outlier_frac=w.outlier_frac, varn_iters=w.varn_iters,
-                         hadamard=True, layout=layout, scale_group=w.scale_group)
+                         hadamard=True, layout=layout, scale_group=w.scale_group, v_csc=v_csc)
 
 
 def oracle_layout(layout: str) -> int:
@@ -41,11 +41,19 @@ def to_device(x: np.ndarray, dtype: str, device="cuda"):
     return t.view(torch.float16 if dtype == "f16" else torch.bfloat16)
 
 
-def new_cache(w: WL.Workload, max_blocks=None, batch=None, layout="rows"):
+def new_cache(w: WL.Workload, max_blocks=None, batch=None, layout="rows", v_csc=False):
     import bit_kv_cache_block_gb300 as K
     torch = torch_mod()
     cb = codebook_for(w)
-    return K.KVCache(cfg_for(w, max_blocks, batch, layout), None if cb is None else torch.from_numpy(cb))
+    return K.KVCache(cfg_for(w, max_blocks, batch, layout, v_csc), None if cb is None else torch.from_numpy(cb))
+
+
+def sparse_parts(otile: dict):
+    """(pointer array, index array, values) of an oracle nuq tile, CSR or CSC: the three arrays in
+    the order the record's outlier region stores them."""
+    if "col_ptr" in otile:
+        return otile["col_ptr"], otile["row"], otile["val"]
+    return otile["row_ptr"], otile["col"], otile["val"]
 
 
 def records_np(cache) -> np.ndarray:
@@ -99,8 +107,9 @@ def serialize_tile(rec: np.ndarray, lay, kind: int, otile: dict, method: str) ->
     if method == "nuq" and n:
         so = int(lay.csr_off[kind])
         rec[so:so + 2 * n] = np.asarray(otile["val"], np.uint16).view(np.uint8)
-        rec[so + 2 * n:so + 2 * n + 2 * (T + 1)] = np.asarray(otile["row_ptr"], np.uint16).view(np.uint8)
-        rec[so + 2 * n + 2 * (T + 1):so + 3 * n + 2 * (T + 1)] = np.asarray(otile["col"], np.uint8)
+        ptr, idx, _ = sparse_parts(otile)
+        rec[so + 2 * n:so + 2 * n + 2 * (T + 1)] = np.asarray(ptr, np.uint16).view(np.uint8)
+        rec[so + 2 * n + 2 * (T + 1):so + 3 * n + 2 * (T + 1)] = np.asarray(idx, np.uint8)
 
 
 def f16_bits(x) -> np.ndarray:

@@ -56,7 +56,7 @@ int main(void) {
          offsetof(kvq_cache, block_table));
   printf("%zu %zu %zu %zu %zu\n", offsetof(kvq_config, key_calib), offsetof(kvq_config, sink),
          offsetof(kvq_layout_t, calib_off), offsetof(kvq_layout_t, sink_bytes), offsetof(kvq_cache, calibrated));
-  printf("%zu\n", offsetof(kvq_config, scale_group));
+  printf("%zu %zu\n", offsetof(kvq_config, scale_group), offsetof(kvq_config, v_csc));
   return 0;
 }
 ''')
@@ -71,7 +71,7 @@ int main(void) {
           L.kvq_cache.n_blocks.offset, L.kvq_cache.device.offset, L.kvq_config.layout.offset,
           L.kvq_config.n_pages.offset, L.kvq_cache.block_table.offset, L.kvq_config.key_calib.offset,
           L.kvq_config.sink.offset, L.kvq_layout_t.calib_off.offset, L.kvq_layout_t.sink_bytes.offset,
-          L.kvq_cache.calibrated.offset, L.kvq_config.scale_group.offset]
+          L.kvq_cache.calibrated.offset, L.kvq_config.scale_group.offset, L.kvq_config.v_csc.offset]
     assert vals == py
 
 
@@ -291,6 +291,13 @@ def test_absmax_variants_layout_and_checks(K):
                 assert lay.record_bytes == 2 * (128 * W * 4 + (128 // sg) * 256)
                 assert K.kvq_decode_bytes(mk(bits=bits, scale_group=sg, layout=layout), 3) == 2 * 3 * 3 * lay.record_bytes
     assert K.kvq_layout(mk(scale_group=0)).meta_bytes[0] == 256
+    # CSC value outliers: nuq only, same layout as CSR
+    nq = lambda **kw: K.make_config("nuq", 3, 1, 2, 2, 4, **kw)
+    a, b = K.kvq_layout(nq()), K.kvq_layout(nq(v_csc=True))
+    assert (a.record_bytes, a.csr_off[1], a.csr_bytes[1]) == (b.record_bytes, b.csr_off[1], b.csr_bytes[1])
+    for m in ("rtn", "varn", "int4"):
+        with pytest.raises(K.KVQError):
+            K.kvq_layout(K.make_config(m, 4 if m == "int4" else 2, 1, 1, 1, 2, v_csc=True))
     for bad in (dict(bits=2), dict(bits=3), dict(bits=6), dict(bits=16)):
         with pytest.raises(K.KVQError):
             K.kvq_layout(mk(**bad))

@@ -33,9 +33,9 @@ def _append_all(cache, w, K, V, chunks):
             cache.append(U.to_device(K[:, :, a * 128:b * 128], w.dtype), U.to_device(V[:, :, a * 128:b * 128], w.dtype))
 
 
-def _oracle_cache(w, layout):
+def _oracle_cache(w, layout, v_csc=False):
     return O.OracleCache.for_workload(w, codebook=U.codebook_for(w)[0] if w.method == "nuq" else None,
-                                      layout=U.oracle_layout(layout))
+                                      layout=U.oracle_layout(layout), v_csc=v_csc)
 
 
 def _compare_exact(cache, oc, w, nb, layout):
@@ -55,10 +55,11 @@ def _compare_exact(cache, oc, w, nb, layout):
                     if "zp16" in exp:
                         assert np.array_equal(U.f16_bits(got["zp16"]), U.f16_bits(exp["zp16"])), where + " zp"
                     if w.method == "nuq" and oc.n_out:
-                        assert np.array_equal(got["val"], exp["val"]), where + " csr val"
-                        assert np.array_equal(got["row_ptr"], exp["row_ptr"]), where + " csr row_ptr"
-                        assert np.array_equal(got["col"], exp["col"]), where + " csr col"
-                        assert not got["csr_pad"].any(), where + " csr padding"
+                        ptr, idx, val = U.sparse_parts(exp)  # CSR, or CSC for v_csc value tiles
+                        assert np.array_equal(got["val"], val), where + " outlier val"
+                        assert np.array_equal(got["row_ptr"], ptr), where + " outlier pointers"
+                        assert np.array_equal(got["col"], idx), where + " outlier index"
+                        assert not got["csr_pad"].any(), where + " outlier padding"
 
 
 CASES_EXACT = [
