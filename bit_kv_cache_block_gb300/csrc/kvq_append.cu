@@ -9,8 +9,8 @@
 //   INT4 : per-token (or per-64-channel) absmax/(2^(b-1)-1) -> fp16 scale -> q = clamp(rne(x/s)) -> b-bit two's complement (b = 4, 8)
 //          ([TQ] §2.1, §4.2 quantize_kv_block)
 //   NUQ  : exact top-n |x| selection (radix select on the fp16 magnitude, ties to the lower
-//          flat index) -> CSR; centre/half-range of the non-outliers -> nearest codebook entry
-//          ([KVQ] §3.3-3.4, §3.8 Algorithm 1 steps 1-4)
+//          flat index) -> CSR (value tiles of v_csc caches: CSC); centre/half-range of the
+//          non-outliers -> nearest codebook entry ([KVQ] §3.3-3.4, §3.8 Algorithm 1 steps 1-4)
 // Every step that decides a code or a stored fp16 value uses single IEEE fp32 operations
 // (explicit _rn intrinsics, no contraction) in a fixed order, so the records are bit-exact
 // with a plain restatement of the definitions.
@@ -446,7 +446,7 @@ __global__ void __launch_bounds__(AP_THREADS) append_kernel(AppendArgs a) {
           }
         }
       }
-      // zero the padding of the CSR region so that records are deterministic
+      // zero the padding of the outlier region so that records are deterministic
       const int used = 3 * n_out + 2 * (T + 1);
       const int total = (int)round16((uint64_t)used);
       for (int i = used + tid; i < total; i += AP_THREADS) csr[i] = 0;

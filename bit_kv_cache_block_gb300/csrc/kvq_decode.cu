@@ -9,8 +9,9 @@
 //     s1), add the CSR outliers, rotate pre-RoPE keys at their absolute position, dot with the
 //     G queries ([KVQ] §3.7 key matvec steps 1-6, Algorithm 1 dequantisation).
 //   online softmax over the block's 128 scores (running max and sum per head, base 2).
-//   V phase (thread = channel): unpack, dequantise, weighted sum with the probabilities
-//     ([KVQ] §3.7 value matvec; [KVN] step 5 with s1; [TQ] §5.2: dequantise inside attention).
+//   V phase (thread = channel): unpack, dequantise, weighted sum with the probabilities, plus
+//     the channel's value outliers (CSR, or CSC for v_csc caches) ([KVQ] §3.7 value matvec;
+//     [KVN] step 5 with s1; [TQ] §5.2: dequantise inside attention).
 // No dequantised value is written to memory. Each CTA writes (m, l, o[128]) per query head.
 //
 // combine_kernel: grid (H_q, B), 128 threads: merges the splits, applies the inverse FWHT for

@@ -19,8 +19,8 @@ struct DequantArgs {
 
 // Row t of one tile record dequantised to fp32 into row[0..127]: token t for key tiles and
 // value tiles alike (the value planes of the tensor-core format hold channels per row and are
-// indexed accordingly), CSR outliers added for nuq, and for KVarN with the Hadamard transform
-// the inverse transform applied when to_input is set.
+// indexed accordingly), outliers added for nuq (CSR, or CSC value tiles), and for KVarN with
+// the Hadamard transform the inverse transform applied when to_input is set.
 __device__ void dequant_row(const Geo& g, const uint8_t* rec, const float* codebook, int h, int kind, int t,
                             bool to_input, float* row) {
   const uint32_t* codes = reinterpret_cast<const uint32_t*>(rec + g.codes_off[kind]);
