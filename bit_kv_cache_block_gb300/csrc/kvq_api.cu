@@ -12,6 +12,7 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
                               long long tail_tok, int n_blocks,
                               int n_split, float* ws, float* out, int* status, int hadamard, cudaStream_t st);
 size_t kvq_decode_ws_floats(const kvq::Geo& g, int n_blocks, int v1_splits);
+size_t kvq_decode_kernel_smem(const kvq::Geo& g);
 cudaError_t kvq_launch_dequant(const kvq::Geo& g, const uint8_t* base, const float* codebook, int first, int n,
                                int domain, int hadamard, float* out_k, float* out_v, int* status, cudaStream_t st);
 cudaError_t kvq_launch_rope_init(float2* tab, int max_blocks, double theta, cudaStream_t st);
@@ -146,6 +147,9 @@ kvq_status kvq_layout(const kvq_config* c, kvq_layout_t* out) {
   }
   l.total_bytes = end;
   l.format_version = KVQ_FORMAT_VERSION;
+  // every cache must be decodable by the CUDA-core decode (large outlier fractions make its
+  // three-record ring outgrow the 227 KB of shared memory one CTA may use)
+  if (kvq_decode_kernel_smem(kvq::make_geo(*c, l)) > (size_t)227 * 1024) return KVQ_ERR_UNSUPPORTED;
   *out = l;
   return KVQ_OK;
 }

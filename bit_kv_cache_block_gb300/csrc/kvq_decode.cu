@@ -58,6 +58,7 @@ struct CombineArgs {
   const float* ws_o;
   float* out;
   int hadamard;
+  const int* status;    // the cache's status word: a decode that timed out left its partials unwritten
 };
 
 // 1/sqrt(128)-scaled FWHT of `n` rows of 128 fp32 values in shared memory (row stride 128).
@@ -522,6 +523,17 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
   }
 
   grid_dependency_wait();  // the decode kernel's partials are complete and visible
+  // A decode kernel whose bounded wait ran out returned without writing its partial rows, so the
+  // workspace holds an earlier call's values: the output is marked NaN rather than merged.
+  // (one thread reads the word, so that the whole CTA takes the same branch)
+  __shared__ int timed_out;
+  if (tid == 0)
+    timed_out = a.n_blocks > 0 && a.status && *reinterpret_cast<const volatile int*>(a.status) == KVQ_ERR_TIMEOUT;
+  __syncthreads();
+  if (timed_out) {
+    if (grp == 0) a.out[((uint64_t)b * g.Hq + hq) * D + c] = __int_as_float(0x7fc00000);
+    return;
+  }
   if (a.n_blocks <= 0) {
     if (grp == 0) a.out[((uint64_t)b * g.Hq + hq) * D + c] = Ot / Lt;
     return;
@@ -599,9 +611,14 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
   if (grp == 0) a.out[((uint64_t)b * g.Hq + hq) * D + c] = O / L;
 }
 
+template <int GMAX>
+size_t decode_smem_bytes(const Geo& g) {
+  return (size_t)NSTAGE * g.rec_bytes + sizeof(DecSmem<GMAX>) + round16((uint64_t)g.n_out);
+}
+
 template <int METHOD, int GMAX>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t st) {
-  size_t smem = (size_t)NSTAGE * a.g.rec_bytes + sizeof(DecSmem<GMAX>) + round16((uint64_t)a.g.n_out);
+  size_t smem = decode_smem_bytes<GMAX>(a.g);
   cudaError_t e = ensure_smem_attr((const void*)decode_kernel<METHOD, GMAX>, (size_t)smem);
   if (e != cudaSuccess) return e;
   dim3 grid(a.n_split, a.g.H, a.g.B);
@@ -620,6 +637,19 @@ cudaError_t launch_decode_m(const DecodeArgs& a, cudaStream_t st) {
 }
 
 }  // namespace kvq
+
+// Dynamic shared memory of the CUDA-core decode for this geometry: it serves every cache, so a
+// configuration whose records do not fit it three times over (with its other buffers) in one
+// SM's shared memory cannot be decoded.
+size_t kvq_decode_kernel_smem(const kvq::Geo& g) {
+  using namespace kvq;
+  const int G = g.G;
+  if (G <= 1) return decode_smem_bytes<1>(g);
+  if (G <= 2) return decode_smem_bytes<2>(g);
+  if (G <= 4) return decode_smem_bytes<4>(g);
+  if (G <= 8) return decode_smem_bytes<8>(g);
+  return decode_smem_bytes<16>(g);
+}
 
 long long kvq_mma_ranges(const kvq::Geo& g);
 long long kvq_nuq_ranges(const kvq::Geo& g);
@@ -699,7 +729,7 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
   c.tail_tok = tail_tok;
   c.n_blocks = n_blocks; c.n_split = (int)plan.rows; c.ranges = plan.ranges; c.per_range = plan.per_range;
   c.total = (long long)g.B * g.H * n_blocks;
-  c.ws_m = ws_m; c.ws_l = ws_l; c.ws_o = ws_o; c.out = out; c.hadamard = hadamard;
+  c.ws_m = ws_m; c.ws_l = ws_l; c.ws_o = ws_o; c.out = out; c.hadamard = hadamard; c.status = status;
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(g.Hq, g.B);
   lc.blockDim = dim3(CB_THREADS);

@@ -271,7 +271,9 @@ uint64_t kvq_decode_bytes(const kvq_config* cfg, int32_t n_blocks);
  *   n_tail   : 0..127
  *   out      : device fp32 [B][H_q][128]
  *   workspace: device scratch of at least kvq_decode_workspace_bytes(cfg, n_blocks) bytes
- * At least one token must be attended (n_blocks > 0 or n_tail > 0). */
+ * At least one token must be attended (n_blocks > 0 or n_tail > 0). Every device-side wait is
+ * bounded (about one second); a decode whose wait gives up records KVQ_ERR_TIMEOUT in
+ * dev_status and writes NaN to out. */
 kvq_status kvq_decode_attn(const kvq_cache* cache, const void* q, const void* tail_k,
                            const void* tail_v, int32_t n_tail, float* out, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
@@ -307,7 +309,11 @@ kvq_status kvq_decode_attn_ex(const kvq_cache* cache, const void* q, const void*
  * reuse it. Nothing in the array needs to start at zero: every call writes each partial
  * before reading it. All calls on a device share the one array and it keeps the last call's
  * contents, so calls that may overlap on the GPU (other streams, other host threads) race
- * and give wrong results: order them on one stream or synchronise between them. */
+ * and give wrong results: order them on one stream or synchronise between them. A decode
+ * whose bounded wait runs out (KVQ_ERR_TIMEOUT in dev_status) leaves its partials unwritten;
+ * its output is then NaN, never a merge of an earlier call's partials. The looked-up address
+ * belongs to the device's context as it was at the first call: do not call this entry again
+ * after cudaDeviceReset (or any teardown of that context) in the same process. */
 kvq_status kvq_decode_attn_static(const kvq_cache* cache, const void* q, const void* tail_k,
                                   const void* tail_v, int32_t n_tail, float* out, cudaStream_t stream);
 

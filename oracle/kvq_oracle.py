@@ -21,8 +21,8 @@ The Hadamard transform and the Sinkhorn-style variance normalisation run in
 fp64 (their codes are checked with a +-1 exemption at rounding boundaries).
 Dequantisation, RoPE and attention run in fp64.
 
-Readings taken where the pages are silent or disagree (each one is also listed
-in the design notes):
+Readings taken where the pages are silent or disagree (each names the page
+passage it settles):
 
 * rounding is round-half-to-even; fp16 conversion is round-to-nearest-even.
 * uniform RTN stores the zero point in units of the scale, x_dq = (q + z) * s

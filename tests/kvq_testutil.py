@@ -134,3 +134,64 @@ def ulp_apart(a16: np.ndarray, b16: np.ndarray) -> np.ndarray:
         u = np.asarray(x, np.float16).view(np.uint16).astype(np.int32)
         return np.where(u & 0x8000, -(u & 0x7fff), u)
     return np.abs(ordn(a16) - ordn(b16))
+
+
+def varn_check_tile(got: dict, exp: dict, kind: int, dbg_rc, layout: str, bits: int = 2) -> dict:
+    """KVarN record of one tile against the oracle's, under the exemptions the fp32 kernel may take
+    against the fp64 oracle (KVarN summary, method steps 2-5; the window is 1e-5 relative
+    throughout):
+
+    - VarN scales r, c (dbg_rc, or None to skip) within 1e-5 relative of the oracle's;
+    - s1 and the RTN scale s equal to the oracle's fp16 values, or one fp16 ulp apart only where
+      the oracle's unrounded value lies within 1e-5 relative of an fp16 rounding midpoint;
+    - in groups whose s equals the oracle's: the zero point z equal to the oracle's, or one ulp
+      apart only next to a midpoint of the oracle's unrounded min/s; the codes equal to the
+      oracle's, or +-1 only where the oracle's x/s - z lies within 1e-5 (relative to the larger of
+      |x/s - z| and 1) of a rounding boundary n + 1/2;
+    - groups whose s took the one-ulp exemption form their own class: their z is derived from that
+      s, so z and the codes are judged the same way but against the oracle's Z under the kernel's
+      s (the values the oracle would store with that scale).
+
+    Returns counts: s1/s/z cells one ulp apart, codes +-1, and the groups and codes of the
+    derived class."""
+    if dbg_rc is not None:
+        r_o, c_o = exp["r"], exp["c"]
+        assert np.all(np.abs(dbg_rc[0] - r_o) <= 1e-5 * np.abs(r_o)), "VarN token scales r"
+        assert np.all(np.abs(dbg_rc[1] - c_o) <= 1e-5 * np.abs(c_o)), "VarN channel scales c"
+    cnt = dict(s1_ulp=0, s_ulp=0, z_ulp=0, codes_pm1=0, derived_groups=0, derived_codes_pm1=0)
+    s1_true = exp["r"] if kind == 0 else exp["c"]
+    d = ulp_apart(got["s1"], exp["s1"])
+    assert np.all((d == 0) | ((d == 1) & near_f16_midpoint(s1_true))), "s1"
+    cnt["s1_ulp"] = int((d == 1).sum())
+    axis = 0 if kind == 0 else 1
+    Z32 = exp["Z"].astype(np.float32)
+    mx = Z32.max(axis=axis).astype(np.float32)
+    mn = Z32.min(axis=axis).astype(np.float32)
+    s32 = (mx - mn) / np.float32(2 ** bits - 1)
+    ds = ulp_apart(got["s16"], exp["s16"])
+    assert np.all((ds == 0) | ((ds == 1) & near_f16_midpoint(s32))), "RTN scale"
+    cnt["s_ulp"] = int((ds == 1).sum())
+    same = ds == 0
+    # zero point: against the oracle's where s agrees; derived from the kernel's s where it does not
+    s_ref = np.where(same, exp["s16"], got["s16"]).astype(np.float16)
+    z_ref = np.where(same, exp["z16"], (mn / s_ref.astype(np.float32)).astype(np.float16)).astype(np.float16)
+    zt = mn.astype(np.float64) / s_ref.astype(np.float64)
+    dz = ulp_apart(got["z16"], z_ref)
+    assert np.all((dz == 0) | ((dz == 1) & near_f16_midpoint(zt))), "RTN zero point"
+    cnt["z_ulp"] = int(((dz == 1) & same).sum())
+    # codes: the oracle's Z under the reference metadata (the oracle's own where s agrees)
+    s = s_ref.astype(np.float32)
+    z = z_ref.astype(np.float32)
+    with np.errstate(invalid="ignore", over="ignore"):
+        tt = Z32 / s[None, :] - z[None, :] if axis == 0 else Z32 / s[:, None] - z[:, None]
+    e = np.clip(np.rint(tt), 0, 2 ** bits - 1)
+    codes = O.unpack_tile(got["words"], bits, kind, oracle_layout(layout)).astype(np.int64)
+    diff = np.abs(codes - e)
+    t64 = tt.astype(np.float64)
+    near = np.abs(t64 - np.floor(t64) - 0.5) <= 1e-5 * np.maximum(1.0, np.abs(t64))
+    assert np.all((diff == 0) | ((diff == 1) & near)), f"codes: {int(((diff > 0) & ~near).sum())} off"
+    derived = np.broadcast_to(~same[None, :] if axis == 0 else ~same[:, None], diff.shape)
+    cnt["codes_pm1"] = int(((diff == 1) & ~derived).sum())
+    cnt["derived_groups"] = int((~same).sum())
+    cnt["derived_codes_pm1"] = int(((diff == 1) & derived).sum())
+    return cnt

@@ -145,6 +145,24 @@ def test_config_checks(K):
     assert e.value.status == L.KVQ_ERR_UNSUPPORTED
 
 
+@pytest.mark.parametrize("layout", ["rows", "mma"])
+@pytest.mark.parametrize("group", [1, 4])
+def test_outlier_fraction_limited_by_decode_shared_memory(K, layout, group):
+    """A nuq cache whose records would not fit the CUDA-core decode's three-record ring in one
+    CTA's 227 KB of shared memory is refused when its layout is computed, before any memory is
+    bound or any append runs; fractions up to half of each tile still lay out."""
+    L = K._lib
+    for frac, ok in ((0.05, True), (0.5, True), (0.9, False), (1.0, False)):
+        cfg = _cfg(K, 2, outlier_frac=frac, n_kv_heads=2, n_q_heads=2 * group, ctx=4 * 128)
+        cfg.layout = K.LAYOUTS[layout]
+        if ok:
+            assert K.kvq_layout(cfg).n_outliers == O.n_outliers(frac)
+        else:
+            with pytest.raises(K.KVQError) as e:
+                K.kvq_layout(cfg)
+            assert e.value.status == L.KVQ_ERR_UNSUPPORTED
+
+
 def test_host_argument_checks_launch_nothing(K):
     """Argument errors are caught on the host before any CUDA call (works without a GPU)."""
     L = K._lib

@@ -7,9 +7,9 @@ these contexts in reasonable time, so it follows sampled (batch, KV head) pairs 
 their inputs come from the seeded generators of the parity tests, while the other heads hold
 seeded device noise of the same shape (they do not enter the sampled outputs). Checked per
 sampled pair: the decode outputs of all its query heads within max-abs 2e-3 of the oracle's
-fp64 result over the whole context, and (except KVarN, whose records carry documented +-1
-exemptions checked at small sizes) the code words, metadata and CSR of its first, middle and
-last blocks bit-exact. Every output of the launch must be finite and the status word clear.
+fp64 result over the whole context, and the code words, metadata and CSR of its first, middle
+and last blocks bit-exact (KVarN: equal under the exemptions of kvq_testutil.varn_check_tile,
+with the kernel's fp32 VarN scales read back from the bulk append). Every output of the launch must be finite and the status word clear.
 """
 import numpy as np
 import pytest
@@ -71,7 +71,10 @@ def test_full_size_sampled_heads(cfg):
             Kd[b, h, c0 * 128:(c0 + n) * 128] = U.to_device(k, w.dtype)
             Vd[b, h, c0 * 128:(c0 + n) * 128] = U.to_device(v, w.dtype)
         heads[(b, h)] = (Kh, Vh)
-    cache.append(Kd, Vd)
+    dbg = None
+    if w.method == "varn":  # the fp32 VarN scales of every tile, for the exemption check
+        dbg = torch.zeros((w.batch, w.n_kv_heads, nb, 2, 2, 128), dtype=torch.float32, device="cuda")
+    cache.append(Kd, Vd, dbg_varn_scales=dbg)
     del Kd, Vd
     q = WL.query(w)
     tk, tv = WL.tail(w, N_TAIL)
@@ -89,14 +92,16 @@ def test_full_size_sampled_heads(cfg):
         ref = oc.decode(q[b:b + 1, h * G:(h + 1) * G], tk[b:b + 1, h:h + 1], tv[b:b + 1, h:h + 1])
         err = np.max(np.abs(out[b, h * G:(h + 1) * G] - ref[0]))
         assert err <= TOL, f"config {cfg} (b={b}, h={h}): max abs err {err:.3e}"
-        if w.method == "varn":
-            continue
         for blk in sorted({0, nb // 2, nb - 1}):
             rec = recs[b, h, blk].cpu().numpy()
             for kind in (0, 1):
                 got = U.tile_fields(rec, cache.layout, kind, w.method, w.bits, "mma")
                 exp = oc.recs[(0, 0, blk, kind)]
                 where = f"config {cfg} (b={b}, h={h}) blk={blk} kind={kind}"
+                if w.method == "varn":
+                    c = U.varn_check_tile(got, exp, kind, dbg[b, h, blk, kind].cpu().numpy(), "mma")
+                    assert sum(c.values()) - c["derived_groups"] <= 0.001 * 16384 + 2, where + f" exemptions {c}"
+                    continue
                 assert np.array_equal(got["words"], exp["words"]), where + " code words"
                 assert np.array_equal(U.f16_bits(got["s16"]), U.f16_bits(exp["s16"])), where + " s"
                 for key in ("z16", "zp16"):

@@ -2,9 +2,10 @@
 span several tiles, ragged tails and several sequence splits.
 
 Bar: append records (code words, fp16 metadata, CSR) bit-exact for RTN, INT4 and NUQ; KVarN
-records equal except the documented exemptions (VarN scales within 1e-5 relative, fp16
-metadata one ulp apart only next to an fp16 rounding midpoint, codes +-1 only next to a
-rounding boundary); decode outputs within max-abs 2e-3 of the oracle's fp64 result.
+records equal to the oracle's except the exemptions of kvq_testutil.varn_check_tile (VarN
+scales within 1e-5 relative, fp16 metadata one ulp apart only next to an fp16 rounding
+midpoint, codes +-1 only next to a rounding boundary, all judged against the oracle's own
+metadata); decode outputs within max-abs 2e-3 of the oracle's fp64 result.
 """
 import numpy as np
 import pytest
@@ -94,49 +95,6 @@ def test_append_records_bit_exact(name, base, kw, layout):
     assert cache.device_status() == 0
 
 
-def _varn_check_tile(got, exp, K_in, kind, dbg_rc, layout):
-    """KVarN exemptions (see module docstring). Returns counts of exempted differences."""
-    r_o, c_o = exp["r"], exp["c"]
-    assert np.all(np.abs(dbg_rc[0] - r_o) <= 1e-5 * np.abs(r_o)), "VarN token scales r"
-    assert np.all(np.abs(dbg_rc[1] - c_o) <= 1e-5 * np.abs(c_o)), "VarN channel scales c"
-    n_ex = 0
-    # s1: equal, or one ulp next to a midpoint of the oracle's unrounded scale
-    s1_true = r_o if kind == 0 else c_o
-    d = U.ulp_apart(got["s1"], exp["s1"])
-    assert np.all((d == 0) | ((d == 1) & U.near_f16_midpoint(s1_true))), "s1"
-    n_ex += int((d == 1).sum())
-    axis = 0 if kind == 0 else 1
-    Z32 = exp["Z"].astype(np.float32)
-    mx = Z32.max(axis=axis).astype(np.float32)
-    mn = Z32.min(axis=axis).astype(np.float32)
-    bits = 2
-    s32 = (mx - mn) / np.float32(2 ** bits - 1)
-    ds = U.ulp_apart(got["s16"], exp["s16"])
-    assert np.all((ds == 0) | ((ds == 1) & U.near_f16_midpoint(s32))), "RTN scale"
-    n_ex += int((ds == 1).sum())
-    # zero point against the kernel's own scale
-    zt = mn.astype(np.float64) / got["s16"].astype(np.float64)
-    z_exp = (mn / got["s16"].astype(np.float32)).astype(np.float16)
-    dz = U.ulp_apart(got["z16"], z_exp)
-    assert np.all((dz == 0) | ((dz == 1) & U.near_f16_midpoint(zt, 1e-4))), "RTN zero"
-    n_ex += int((dz == 1).sum())
-    # codes: the oracle's Z under the kernel's metadata, +-1 only next to a rounding boundary
-    s = got["s16"].astype(np.float32)
-    z = got["z16"].astype(np.float32)
-    if axis == 0:
-        tt = Z32 / s[None, :] - z[None, :]
-    else:
-        tt = Z32 / s[:, None] - z[:, None]
-    e = np.clip(np.rint(tt), 0, 2 ** bits - 1)
-    codes = O.unpack_tile(got["words"], bits, kind, U.oracle_layout(layout)).astype(np.int64)
-    diff = np.abs(codes - e)
-    frac = np.abs(tt.astype(np.float64) - np.floor(tt.astype(np.float64)) - 0.5)
-    near = frac <= 1e-5 * np.maximum(1.0, np.abs(tt))
-    assert np.all((diff == 0) | ((diff == 1) & near)), f"codes: {int(((diff > 0) & ~near).sum())} off"
-    n_ex += int((diff == 1).sum())
-    return n_ex
-
-
 @pytest.mark.parametrize("layout", ["rows", "mma"])
 def test_append_varn_exemptions(layout):
     import torch
@@ -150,15 +108,19 @@ def test_append_varn_exemptions(layout):
     oc.append(K, V)
     dbg = dbg.cpu().numpy()
     recs = U.records_np(cache)
-    n_ex = 0
+    tot = {}
     for b in range(w.batch):
         for h in range(w.n_kv_heads):
             for blk in range(nb):
                 for kind in (0, 1):
                     got = U.tile_fields(recs[b, h, blk], cache.layout, kind, "varn", 2, layout)
-                    n_ex += _varn_check_tile(got, oc.recs[(b, h, blk, kind)], None, kind, dbg[b, h, blk, kind], layout)
-    # exemptions must stay rare
-    assert n_ex <= 0.001 * (w.batch * w.n_kv_heads * nb * 2 * 16384)
+                    c = U.varn_check_tile(got, oc.recs[(b, h, blk, kind)], kind, dbg[b, h, blk, kind], layout)
+                    for k, v in c.items():
+                        tot[k] = tot.get(k, 0) + v
+    # exemptions must stay rare: every exempted cell and code together under 0.1% of the codes
+    n_codes = w.batch * w.n_kv_heads * nb * 2 * 16384
+    assert sum(tot.values()) - tot["derived_groups"] <= 0.001 * n_codes, tot
+    assert tot["derived_groups"] <= 0.001 * (w.batch * w.n_kv_heads * nb * 2 * 128), tot
 
 
 def _run_decode(w, nb, n_tail, chunks=2, oracle_planes=False, step=0, layout="rows"):
