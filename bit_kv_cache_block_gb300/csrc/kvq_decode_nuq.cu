@@ -4,10 +4,10 @@
 // Work split. The (b, h, block) sequence of the whole batch is cut into one contiguous range
 // per CTA (persistent: one wave). A CTA runs 4 warpgroups whose roles meet only on mbarriers
 // (every wait bounded):
-//   producer warp     : copies each block record (K tile, V tile, fp16 metadata, CSR outliers)
-//                       and the block's RoPE start-angle row into an NB-stage ring with 1-D bulk
-//                       copies, as soon as the consumers have released the stage;
-//   4 aux warps       : two groups taking alternate blocks; they build each block's shared score
+//   producer warp     : copies each block record (K tile; V tile with the CSR outliers) into an
+//                       NB-stage ring with two 1-D bulk copies, as soon as the consumers have
+//                       released the stage;
+//   4 aux warps       : two groups taking alternate blocks; per block they build the shared score
 //                       operands, turn the key outliers into one additive score term per token
 //                       and tag every outlier with its token;
 //   8 consumer warps  : warp w owns tokens 16w..16w+15 of every block and keeps its own
@@ -21,13 +21,16 @@
 // so q . k_n = (R(t)^T q_b) . (s*C[q] + zp + o) with q_b = R(n0)^T q. Per channel pair i
 // (angle t*theta_i) this is cos * X_i + sin * Y_i with
 //     X_i = q_b0 k0 + q_b1 k1,    Y_i = q_b1 k0 - q_b0 k1.
-// X and Y of 16 tokens x 4 pairs come out of one mma.sync m16n8k8: A = the codebook values C[q]
+// X and Y of 16 tokens x 4 pairs come out of one mma.sync m16n8k16: A = the codebook values C[q]
 // of 16 tokens x 8 channels (looked up from the packed codes with byte permutes on an fp16 table
-// held in registers), B = the block's q_b * s in fp16 in the X and Y columns of each pair, C =
-// the zero-point terms. The cos/sin of a lane's own (token, pair) cells are fixed over blocks
-// and stay in registers; the fp16 outliers o of the CSR enter as per-token score terms.
+// held in registers) and ones, B = the block's q_b * s in fp16 in the X and Y columns of each
+// pair and the zero-point terms against the ones. The cos/sin of a lane's own (token, pair)
+// cells are fixed over blocks and stay in registers; the fp16 outliers o of the CSR enter as
+// per-token score terms.
 // Values ([KVQ] §3.7 value matvec): O[channel] = sum_t p_t s_t C[q] + sum_t p_t zp_t + outliers,
-// one m16n8k16 per 16 channels x the warp's 16 tokens; B = p*s in high/low fp16 columns.
+// one m16n8k16 per 16 channels x the warp's 16 tokens with B = p*s in high/low fp16 columns; the
+// value outliers add p_t * v per channel in token order (a fixed sequence of fp32 additions, the
+// same for CSR and CSC value tiles).
 // Softmax in base 2 with the running max per warp (rescaling only when the max grows).
 #include "kvq_internal.cuh"
 
@@ -39,24 +42,17 @@ namespace nuqdec {
 constexpr int NW = 8;               // consumer warps (16 tokens of each block per warp)
 constexpr int NAUX = 128;           // aux threads: two groups that take alternate blocks
 constexpr int AUX_GROUP = 64;       // threads of one aux group: one per channel pair, two tokens each
-constexpr int PRODUCER_WARP = NW + NAUX / 32;  // issues the bulk copies; the warpgroup's other 3 warps idle
+constexpr int PRODUCER_WARP = NW + NAUX / 32;  // issues the bulk copies
 constexpr int NTHREADS = 512;       // 4 warpgroups: consumers (2), aux, producer
 // Register split (setmaxnreg): launched at 65536 / 512 = 128 per thread; the consumer warpgroups
 // take 168 and the others give back down to 88 (2 x 128 x 168 + 2 x 128 x 88 = 65536).
 constexpr int REGS_CONSUMER = 168, REGS_OTHER = 88;
 static_assert(2 * 128 * REGS_CONSUMER + 2 * 128 * REGS_OTHER <= 65536, "register split over the launch total");
-constexpr int ROPE_ROW = 64 * 8;    // bytes of one (cos, sin) row of 64 pairs
 constexpr int MAX_OUTLIERS = 2048;  // per tile, on this path
 constexpr float LOG2E_RSQRT_D = 1.4426950408889634f * 0.08838834764831845f;
 // The running reference of a warp's softmax moves only when a score exceeds it by more than this
 // (base-2 units): probabilities then stay below 2^8, so p * s of a token stays far inside fp16.
 constexpr float RESCALE_SLACK = 8.0f;
-// Value outliers are summed as 64-bit fixed point with OUTV_FRAC fraction bits: integer addition
-// is exact, so the sums do not depend on the order of the shared-memory atomics. |p * v| < 2^24
-// (p <= 2^RESCALE_SLACK, |v| <= 65504), so 2^19 entries per warp and (b, h) segment stay inside
-// the range even at that bound; the rounding is 2^-21 per entry.
-constexpr int OUTV_FRAC = 20;
-constexpr float OUTV_ONE = (float)(1 << OUTV_FRAC), OUTV_UNIT = 1.0f / OUTV_ONE;
 
 #ifndef KVQ_NUQ_NB
 #define KVQ_NUQ_NB 8
@@ -80,22 +76,29 @@ struct Args {
 
 // Per-stage operands the aux warps prepare for the consumer warps.
 struct Ops {
-  uint32_t bk[9][20];  // score B rows 0..7 (q_b * s) of column g, 16 k-groups, padded; row 8 stays zero
-  uint32_t bz[9][20];  // score B rows 8, 9 of column g: zero-point term (high, low); row 8 stays zero
+  // Score B fragments: row n (0..7) holds, for each of the 16 k-groups, the pair (b0, b1) of the
+  // lane that owns column n (X of pair n/2 for even n, Y for odd n): b0 = the column's two code
+  // rows (q_b * s), b1 = its zero-point term (high, low). Row 8 stays zero (lanes holding no
+  // part of B); rows are 36 words apart so that the 8 rows' 16-byte loads hit distinct banks.
+  uint32_t b[9][36];
   float sk[T];         // key-outlier score term per token
 };
 
 struct Smem {
-  float2 rope_loc[T * 64];  // (cos, sin) of t * theta_i, t = 0..127
   Ops op[NB];
-  float qb[2][D];           // per aux group: q rotated back by the block's start angle
-  long long outv[NW][D];    // value outliers weighted by p, per consumer warp, in units of 2^-OUTV_FRAC
-  uint64_t rec_full[NB];    // record and RoPE row landed (bulk copies)
-  uint64_t ops_full[NB];    // score operands and outlier terms ready (AUX_GROUP arrivals)
-  uint64_t empty[NB];       // the consumer warps are done with the stage (NW arrivals)
-  // followed by NB x 2 x round16(n_outliers) bytes, per stage: the token of each key outlier,
-  // then the token of each value outlier; then 2 x round16(n_outliers) floats, per aux group:
-  // the score term of each key outlier
+  float2 rope_a[8][64];      // (cos, sin) of 16a * theta_i, a = 0..7 (in-block angles, coarse)
+  float2 rope_b[16][64];     // (cos, sin) of b * theta_i, b = 0..15 (fine): t = 16a + b
+  float qb[2][D];            // per aux group: q rotated back by the block's start angle
+  float outv[NW][D + 32];    // value outliers weighted by p, per consumer warp (+ a slot per lane)
+  int own[NW][D + 32];       // per consumer warp and channel: the lowest lane holding an entry of it (32: none)
+  uint64_t rec_full[NB];     // record landed (bulk copies)
+  uint64_t ops_full[NB];     // score operands, key-outlier terms and outlier tags ready (AUX_GROUP arrivals)
+  uint64_t empty[NB];        // the consumer warps are done with the stage (NW arrivals)
+  // followed by NB x rows_stride bytes, per stage: the token of each key outlier [round16(n)], the
+  // run index of each value outlier [round16(n)] (token for CSR value tiles, channel for CSC ones)
+  // and, for CSC value tiles, the permutation grouping the value entries by consumer warp (uint16
+  // [n], 16-byte padded) and the 9 group offsets (uint16, 32 bytes); then per aux group round16(n)
+  // floats (the score term of each key outlier) and, for CSC value tiles, 16 int counters
 };
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -161,7 +164,14 @@ __device__ __forceinline__ bool bar_or_group(int grp, bool pred) {
 
 __device__ __forceinline__ void bar_group(int grp) { asm volatile("bar.sync %0, 64;" ::"r"(1 + grp) : "memory"); }
 
-__device__ __forceinline__ uint32_t stage_bytes(const Geo& g) { return (uint32_t)g.rec_bytes + ROPE_ROW; }
+__device__ __forceinline__ uint32_t stage_bytes(const Geo& g) { return (uint32_t)g.rec_bytes; }
+
+// 2^x on the special-function unit (x <= 0 here; -inf gives 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Per-stage outlier area (after the ring and Smem): the token tag of each key outlier
 // [round16(n)], the run index of each value outlier [round16(n)] (token for CSR value tiles,
@@ -174,21 +184,23 @@ __host__ __device__ inline int rows_stride_of(int n_out, bool csc) {
   return 2 * (int)round16((uint64_t)n_out) + (csc ? (int)round16(2 * (uint64_t)n_out) + 32 : 0);
 }
 
+// (the memory clobber keeps loads of the role code below the register split)
 template <uint32_t R>
 __device__ __forceinline__ void regs_inc() {
-  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(R));
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(R) : "memory");
 }
 template <uint32_t R>
 __device__ __forceinline__ void regs_dec() {
-  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R));
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R) : "memory");
 }
 
 // Producer warp: copies block p of the range into stage p % NBS once the consumer warps have
-// released the stage's previous block (NW arrivals on empty). A block's three copies (K half;
-// V half with the CSR; the block's RoPE start-angle row) go out as one instruction from three
-// lanes, and the lane triple rotates over blocks: a thread services its own bulk copies one
-// after another, a few hundred cycles each whatever their size, so copies from distinct lanes
-// overlap. Before leaving it waits (bounded) for the last copies it issued.
+// released the stage's previous block (NW arrivals on empty). A block's two copies (K half; V
+// half with the CSR) go out as one instruction from two lanes, and the lane pair rotates over
+// blocks: a thread services its own bulk copies one after another, a few hundred cycles each
+// whatever their size, so copies from distinct lanes overlap. (Every further copy per block
+// costs the same again: the block's RoPE start row, 512 bytes, comes through the aux warps'
+// plain loads instead.) Before leaving it waits (bounded) for the last copies it issued.
 template <int NBS>
 __device__ void producer(const Args& a, Smem* sm, uint8_t* ring, long long x0, int n, int lane) {
   const Geo& g = a.g;
@@ -200,19 +212,18 @@ __device__ void producer(const Args& a, Smem* sm, uint8_t* ring, long long x0, i
   for (int p = 0; p < n; ++p) {
     const int s = p % NBS;
     if (p >= NBS) {
-      const bool got = mbar_wait_bounded(&sm->empty[s], (uint32_t)(((p / NBS) - 1) & 1), a.status);
+      const bool got = mbar_wait_backoff(&sm->empty[s], (uint32_t)(((p / NBS) - 1) & 1), a.status);
       if (__any_sync(0xffffffffu, !got)) break;
     }
-    const int set = 3 * (p & 7), part = lane - set;  // lanes set .. set+2 copy this block
-    if (lane == set) mbar_arrive_expect_tx(&sm->rec_full[s], rec + ROPE_ROW);
+    const int set = 2 * (p & 15), part = lane - set;  // lanes set, set+1 copy this block
+    if (lane == set) mbar_arrive_expect_tx(&sm->rec_full[s], rec);
     __syncwarp();
-    if (part >= 0 && part < 3) {
+    if (part >= 0 && part < 2) {
       fence_proxy_async();
-      const uint32_t off = part == 0 ? 0u : part == 1 ? khalf : rec;
-      const uint32_t bytes = part == 0 ? khalf : part == 1 ? rec - khalf : (uint32_t)ROPE_ROW;
-      const uint8_t* from =
-          part == 2 ? a.base + g.rope_off + (size_t)blk * ROPE_ROW : a.base + record_offset(g, pb, ph, blk, a.status) + off;
-      bulk_g2s(ring + (size_t)s * sb + off, from, bytes, &sm->rec_full[s]);
+      const uint32_t off = part == 0 ? 0u : khalf;
+      const uint32_t bytes = part == 0 ? khalf : rec - khalf;
+      bulk_g2s(ring + (size_t)s * sb + off, a.base + record_offset(g, pb, ph, blk, a.status) + off, bytes,
+               &sm->rec_full[s]);
     }
     issued = p + 1;
     if (++blk == a.nb) {
@@ -234,12 +245,12 @@ __device__ void producer(const Args& a, Smem* sm, uint8_t* ring, long long x0, i
 // computes the score terms of the key-outlier entries e = j, j + 64, ...
 //     v * (R(t)^T q_b)_c    (entry e = (t, c, v) of the CSR)
 // and, after a group barrier, the sum sk[t] of each of its two tokens' terms in entry order.
-// The consumers scatter p_t * v for the value outliers.
+// The consumers add p_t * v for the value outliers.
 template <int NBS, bool CSC>
 __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows, int rows_stride, long long x0,
                           int n, int ax) {
   const Geo& g = a.g;
-  const uint32_t rec = (uint32_t)g.rec_bytes, sb = stage_bytes(g);
+  const uint32_t sb = stage_bytes(g);
   const int n_out = g.n_out;
   const int grp = ax >> 6, j = ax & 63;
   const int tag_bytes = (int)round16((uint64_t)n_out);
@@ -251,6 +262,10 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
   }
   long long cur_u = -1;
   float2 qv = make_float2(0.0f, 0.0f);
+  const float2* rope_blk = reinterpret_cast<const float2*>(a.base + g.rope_off);
+  // (cos, sin) of the block's start angle for pair j, from the RoPE table (L2-resident), loaded one
+  // block of the group ahead so that its latency is hidden
+  float2 cs_next = grp < n ? __ldg(rope_blk + (size_t)blk * 64 + j) : make_float2(1.0f, 0.0f);
   float* qb = sm->qb[grp];
   float* kterm = reinterpret_cast<float*>(rows + (size_t)NBS * rows_stride) + grp * tag_bytes;  // per group
   // CSC value tiles: per group, entries per consumer warp [8] and the scatter cursors [8]
@@ -263,23 +278,28 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
       qv = load_q_pair(a, u, j);
     }
     const int s = p % NBS;
-    const bool got = mbar_wait_bounded(&sm->rec_full[s], (uint32_t)((p / NBS) & 1), a.status);
+    const float2 cs = cs_next;
+    {
+      int nb2 = blk + 2;
+      while (nb2 >= a.nb) nb2 -= a.nb;
+      if (p + 2 < n) cs_next = __ldg(rope_blk + (size_t)nb2 * 64 + j);
+    }
+    const bool got = mbar_wait_backoff(&sm->rec_full[s], (uint32_t)((p / NBS) & 1), a.status);
     if (bar_or_group(grp, !got)) break;  // the consumers time out on their own waits
     const uint8_t* st = ring + (size_t)s * sb;
     Ops& op = sm->op[s];
     {
-      const float2 cs = reinterpret_cast<const float2*>(st + rec)[j];
       const float qb0 = cs.x * qv.x + cs.y * qv.y, qb1 = -cs.y * qv.x + cs.x * qv.y;
       const uint16_t* km = reinterpret_cast<const uint16_t*>(st + g.meta_off[0]);
       const int kg = j >> 2, tqp = j & 3;
       const float s0 = h2f(km[2 * j]), s1 = h2f(km[2 * j + 1]);
       const float z0 = h2f(km[T + 2 * j]), z1 = h2f(km[T + 2 * j + 1]);
-      op.bk[2 * tqp][kg] = pack_h2(qb0 * s0, qb1 * s1);       // X column of pair j
-      op.bk[2 * tqp + 1][kg] = pack_h2(qb1 * s0, -qb0 * s1);  // Y column
+      const uint32_t bx = pack_h2(qb0 * s0, qb1 * s1);   // X column of pair j
+      const uint32_t by = pack_h2(qb1 * s0, -qb0 * s1);  // Y column
       const float zx = qb0 * z0 + qb1 * z1, zy = qb1 * z0 - qb0 * z1;
       const __half zxh = __float2half_rn(zx), zyh = __float2half_rn(zy);
-      op.bz[2 * tqp][kg] = pack_h2(zx, zx - __half2float(zxh));      // X column: (high, low)
-      op.bz[2 * tqp + 1][kg] = pack_h2(zy, zy - __half2float(zyh));  // Y column
+      *reinterpret_cast<uint2*>(&op.b[2 * tqp][2 * kg]) = make_uint2(bx, pack_h2(zx, zx - __half2float(zxh)));
+      *reinterpret_cast<uint2*>(&op.b[2 * tqp + 1][2 * kg]) = make_uint2(by, pack_h2(zy, zy - __half2float(zyh)));
       *reinterpret_cast<float2*>(&qb[2 * j]) = make_float2(qb0, qb1);
     }
     float skA = 0.0f, skB = 0.0f;
@@ -325,9 +345,11 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
       const int n_k = min((int)rp[T], n_out);
       auto key_term = [&](int e) {  // score term of key-outlier entry e < n_k
         const int c = col[e] & (D - 1), t = ktag[e] & (T - 1);
-        const float2 cr = sm->rope_loc[t * 64 + (c >> 1)];
+        // (cos, sin) of t * theta_pi from the coarse and fine tables (t = 16a + b)
+        const float2 ca = sm->rope_a[t >> 4][c >> 1], cb = sm->rope_b[t & 15][c >> 1];
+        const float cr = ca.x * cb.x - ca.y * cb.y, sr = ca.y * cb.x + ca.x * cb.y;
         const float qa = qb[c & ~1], qc = qb[c | 1];
-        const float qq = (c & 1) ? (-cr.y * qa + cr.x * qc) : (cr.x * qa + cr.y * qc);
+        const float qq = (c & 1) ? (-sr * qa + cr * qc) : (cr * qa + sr * qc);
         return h2f(val[e]) * qq;
       };
       // every entry's term (up to 4 per thread side by side; 1% of a tile is 164 entries), then
@@ -351,33 +373,91 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
   }
 }
 
+// ---- shared-memory accesses of the consumer warps, through 32-bit shared-window addresses (the
+// stage, operand and outlier areas are all addressed from a few per-lane base registers)
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ float lds_f32(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint2 lds_v2(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ void sts_f32(uint32_t a, float v) { asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v)); }
+// the same loads at a compile-time offset from a base register ([base + OFF] addressing)
+template <int OFF>
+__device__ __forceinline__ uint32_t lds_u16_at(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1+%2];" : "=r"(v) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ float lds_f32_at(uint32_t a) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1+%2];" : "=f"(v) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint2 lds_v2_at(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint4 lds_v4_at(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4+%5];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a), "n"(OFF));
+  return v;
+}
+template <int U>
+__device__ __forceinline__ uint4 lds_v4_u(uint32_t a) { return lds_v4_at<16 * U>(a); }
+
+constexpr uint32_t OPS_B = 0, OPS_ROW = 36 * 4, OPS_SK = 9 * 36 * 4;  // byte offsets in Ops
+static_assert(sizeof(Ops) == OPS_SK + T * 4, "Ops layout");
+
 // Scores of a consumer warp's 16 tokens in one block (after the reduction over the 4 lanes of a
 // token and the key-outlier terms): s0 for token 16w + gq, s1 for token 16w + gq + 8.
-__device__ __forceinline__ void block_scores(const uint8_t* st, const Ops& op, uint32_t codes_off, int warp, int lane,
-                                             int brow, int zrow, uint32_t ones, int t0, int t1, uint32_t tl0,
-                                             uint32_t tl1, uint32_t th0, uint32_t th1, const float2 (&w)[2][16],
-                                             float& s0, float& s1) {
-  uint32_t cw[6];
-  const uint2* kp = reinterpret_cast<const uint2*>(st + codes_off + warp * 768 + lane * 24);
-  const uint2 k0 = kp[0], k1 = kp[1], k2 = kp[2];
-  cw[0] = k0.x; cw[1] = k0.y; cw[2] = k1.x; cw[3] = k1.y; cw[4] = k2.x; cw[5] = k2.y;
-  const uint4* bp = reinterpret_cast<const uint4*>(&op.bk[brow][0]);
-  const uint4* zp = reinterpret_cast<const uint4*>(&op.bz[zrow][0]);
+// The m16n8k16 per k-group: A = the codebook values of 16 tokens x the group's 8 channels (k 0..7)
+// and ones (k 8..15); B = the code rows and, at k 8 + 2(n/2) and 9 + 2(n/2), the zero-point term
+// (high, low) of column n. ka: the lane's 24 code bytes; ba: its B row; ska: sk[t0].
+__device__ __forceinline__ void block_scores(uint32_t ka, uint32_t ba, uint32_t ska, uint32_t ones,
+                                             uint32_t tl0, uint32_t tl1, uint32_t th0, uint32_t th1,
+                                             const float2 (&w)[2][16], float& s0, float& s1) {
+  const uint2 k0 = lds_v2_at<0>(ka), k1 = lds_v2_at<8>(ka), k2 = lds_v2_at<16>(ka);
+  const uint32_t cw[6] = {k0.x, k0.y, k1.x, k1.y, k2.x, k2.y};
   const float zero4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   float2 acc[2][2] = {{{0.0f, 0.0f}, {0.0f, 0.0f}}, {{0.0f, 0.0f}, {0.0f, 0.0f}}};
 #pragma unroll
   for (int uu = 0; uu < 8; ++uu) {
+    const uint4 bq = uu == 0 ? lds_v4_u<0>(ba) : uu == 1 ? lds_v4_u<1>(ba) : uu == 2 ? lds_v4_u<2>(ba)
+                   : uu == 3 ? lds_v4_u<3>(ba) : uu == 4 ? lds_v4_u<4>(ba) : uu == 5 ? lds_v4_u<5>(ba)
+                   : uu == 6 ? lds_v4_u<6>(ba) : lds_v4_u<7>(ba);  // (b0, b1) of k-groups 2uu and 2uu + 1
     const uint32_t nw = nibble_word(cw, uu);
-    const uint4 bq = bp[uu >> 1], zq = zp[uu >> 1];  // k-groups 4(uu/2) .. 4(uu/2)+3
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
       const int kg = 2 * uu + hf;
       uint32_t a0, a1;
       lookup4(hf ? (nw >> 16) : nw, tl0, tl1, th0, th1, a0, a1);
-      const uint32_t bb = (kg & 3) == 0 ? bq.x : (kg & 3) == 1 ? bq.y : (kg & 3) == 2 ? bq.z : bq.w;
-      const uint32_t bz = (kg & 3) == 0 ? zq.x : (kg & 3) == 1 ? zq.y : (kg & 3) == 2 ? zq.z : zq.w;
       float d[4];
-      mma16816(d, a0, a1, ones, ones, bb, bz, zero4);  // X, Y of pair 4kg+tq incl. the zero-point term
+      mma16816(d, a0, a1, ones, ones, hf ? bq.z : bq.x, hf ? bq.w : bq.y, zero4);  // X, Y of pair 4kg+tq
       acc[0][hf] = __ffma2_rn(w[0][kg], make_float2(d[0], d[1]), acc[0][hf]);
       acc[1][hf] = __ffma2_rn(w[1][kg], make_float2(d[2], d[3]), acc[1][hf]);
     }
@@ -386,21 +466,20 @@ __device__ __forceinline__ void block_scores(const uint8_t* st, const Ops& op, u
   s1 = (acc[1][0].x + acc[1][1].x) + (acc[1][0].y + acc[1][1].y);
   s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
   s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-  s0 += __shfl_xor_sync(0xffffffffu, s0, 2) + op.sk[t0];
-  s1 += __shfl_xor_sync(0xffffffffu, s1, 2) + op.sk[t1];
+  s0 += __shfl_xor_sync(0xffffffffu, s0, 2) + lds_f32_at<0>(ska);
+  s1 += __shfl_xor_sync(0xffffffffu, s1, 2) + lds_f32_at<32>(ska);
 }
 
 // Value product of one block for a consumer warp: p' = p * s_token as high/low B columns, the
-// zero-point sum and 8 m16n8k16 over the V codes.
-__device__ __forceinline__ void block_values(const uint8_t* st, const Geo& g, int warp, int lane, int t0, int t1,
-                                             int src_a, uint32_t xsel, uint32_t ysel, float p0, float p1,
-                                             uint32_t tl0, uint32_t tl1, uint32_t th0, uint32_t th1, float& z_w,
-                                             float (&acc)[8][4]) {
-  const uint16_t* vm = reinterpret_cast<const uint16_t*>(st + g.meta_off[1]);
+// zero-point sum and 8 m16n8k16 over the V codes. va: the lane's 24 code bytes; vma: s_t0 of the
+// value metadata (s_t1 = +16, zp_t0 = +256, zp_t1 = +272).
+__device__ __forceinline__ void block_values(uint32_t va, uint32_t vma, int src_a, uint32_t xsel, uint32_t ysel,
+                                             float p0, float p1, uint32_t tl0, uint32_t tl1, uint32_t th0,
+                                             uint32_t th1, float& z_w, float (&acc)[8][4]) {
   uint32_t vb0, vb1;
   {
-    const float pp0 = p0 * h2f(vm[t0]), pp1 = p1 * h2f(vm[t1]);
-    z_w = fmaf(p0, h2f(vm[T + t0]), fmaf(p1, h2f(vm[T + t1]), z_w));
+    const float pp0 = p0 * h2f((uint16_t)lds_u16_at<0>(vma)), pp1 = p1 * h2f((uint16_t)lds_u16_at<16>(vma));
+    z_w = fmaf(p0, h2f((uint16_t)lds_u16_at<256>(vma)), fmaf(p1, h2f((uint16_t)lds_u16_at<272>(vma)), z_w));
     const __half h0 = __float2half_rn(pp0), h1 = __float2half_rn(pp1);
     const uint32_t hi = (uint32_t)__half_as_ushort(h0) | ((uint32_t)__half_as_ushort(h1) << 16);
     const uint32_t lo = pack_h2(pp0 - __half2float(h0), pp1 - __half2float(h1));
@@ -408,10 +487,8 @@ __device__ __forceinline__ void block_values(const uint8_t* st, const Geo& g, in
     vb0 = __shfl_sync(0xffffffffu, x, src_a);
     vb1 = __shfl_sync(0xffffffffu, x, src_a + 16);
   }
-  uint32_t cw[6];
-  const uint2* vp = reinterpret_cast<const uint2*>(st + g.codes_off[1] + warp * 768 + lane * 24);
-  const uint2 v0 = vp[0], v1 = vp[1], v2 = vp[2];
-  cw[0] = v0.x; cw[1] = v0.y; cw[2] = v1.x; cw[3] = v1.y; cw[4] = v2.x; cw[5] = v2.y;
+  const uint2 v0 = lds_v2_at<0>(va), v1 = lds_v2_at<8>(va), v2 = lds_v2_at<16>(va);
+  const uint32_t cw[6] = {v0.x, v0.y, v1.x, v1.y, v2.x, v2.y};
 #pragma unroll
   for (int mt = 0; mt < 8; ++mt) {
     const uint32_t nw = nibble_word(cw, mt);
@@ -422,51 +499,93 @@ __device__ __forceinline__ void block_values(const uint8_t* st, const Geo& g, in
   }
 }
 
-// Value outliers of a consumer warp's tokens in one block. rw: the stage's value-outlier area
-// written by the aux warps: each entry's pointer-run index (the token for CSR tiles, the channel
-// for CSC tiles), then for CSC tiles a permutation of the entries that groups them by consumer
-// warp (16 tokens each) and the 9 group offsets. Entry k of the warp's span goes to lane
-// (k - e0) mod 32, which takes p of its token from the token's owner lane and adds p * v to the
-// warp's outv (integer atomics: the sum does not depend on the order). The first 32 entries run
-// as one batch placed with the tensor-core work of the block; later ones loop.
+// Value outliers of a consumer warp's tokens in one block: the span [e0, e1) of its entries. rw:
+// the stage's value-outlier area written by the aux warps: each entry's pointer-run index (the
+// token for CSR tiles, the channel for CSC tiles), then for CSC tiles a permutation of the
+// entries that groups them by consumer warp (16 tokens each) and the 9 group offsets.
 template <bool CSC>
-__device__ __forceinline__ void value_outlier_span(const uint8_t* st, const uint8_t* rw, const Geo& g, int warp,
-                                                   int& e0, int& e1) {
+__device__ __forceinline__ void value_outlier_span(uint32_t sa, uint32_t rw, const Geo& g, int warp, int& e0, int& e1) {
   const int n_out = g.n_out;
   if (CSC) {
-    const uint16_t* off = reinterpret_cast<const uint16_t*>(rw + csc_off_of(n_out));
-    e0 = off[warp];
-    e1 = off[warp + 1];
+    const uint32_t off = rw + (uint32_t)csc_off_of(n_out);
+    e0 = (int)lds_u16(off + 2 * warp);
+    e1 = (int)lds_u16(off + 2 * warp + 2);
   } else {
-    const uint16_t* rp = reinterpret_cast<const uint16_t*>(st + g.csr_off[1] + 2 * n_out);
-    e0 = min((int)rp[16 * warp], n_out);
-    e1 = min((int)rp[16 * warp + 16], n_out);
+    const uint32_t rp = sa + g.csr_off[1] + 2 * n_out;
+    e0 = min((int)lds_u16(rp + 32 * warp), n_out);
+    e1 = min((int)lds_u16(rp + 32 * warp + 32), n_out);
   }
 }
 
-// Value-outlier entry k of the lane (k >= e1: none): p_t * v added to the warp's outv[c] in
-// fixed point (a shared-memory integer atomic; no branch, so it sits among the tensor-core work).
+// Entry k of the span for this lane (k >= e1: none): its channel c (D + lane when there is none,
+// a slot of the lane's own past the channels) and x = p_t * v for its token t (p from the token's
+// owner lane).
 template <bool CSC>
-__device__ __forceinline__ void value_outlier_entry(const uint8_t* st, const Geo& g, const uint8_t* rw, int k, int e1,
-                                                    int t0, float p0, float p1, long long* outv) {
+__device__ __forceinline__ void value_outlier_load(uint32_t sa, uint32_t rw, const Geo& g, int k, int e1, float p0,
+                                                   float p1, int lane, int& c, float& x) {
   const int n_out = g.n_out;
-  const uint8_t* csr = st + g.csr_off[1];
-  const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
-  const uint8_t* idx = csr + 2 * n_out + 2 * (T + 1);  // CSR: channel; CSC: token
   const bool valid = k < e1;
-  int e = k, t;
+  const int kk = valid ? k : 0;
+  const uint32_t csr = sa + g.csr_off[1], idx = csr + 2 * n_out + 2 * (T + 1);  // idx: CSR channel, CSC token
+  int e = kk, t, ch;
   if (CSC) {
-    e = valid ? (int)reinterpret_cast<const uint16_t*>(rw + round16((uint64_t)n_out))[k] : 0;
-    t = valid ? idx[e] : t0;
+    e = min((int)lds_u16(rw + (uint32_t)round16((uint64_t)n_out) + 2 * kk), n_out - 1);
+    t = (int)lds_u8(idx + e);
+    ch = (int)lds_u8(rw + e);
   } else {
-    t = valid ? rw[e] : t0;
+    t = (int)lds_u8(rw + kk);
+    ch = (int)lds_u8(idx + kk);
   }
+  const float v = h2f((uint16_t)lds_u16(csr + 2 * e));
   const int src = 4 * (t & 7);
   const float pa = __shfl_sync(0xffffffffu, p0, src), pb = __shfl_sync(0xffffffffu, p1, src);
-  if (valid) {
-    const float x = ((t & 8) ? pb : pa) * h2f(val[e]);
-    atomicAdd(reinterpret_cast<unsigned long long*>(&outv[(CSC ? rw[e] : idx[e]) & (D - 1)]),
-              (unsigned long long)llrintf(x * OUTV_ONE));
+  c = valid ? (ch & (D - 1)) : D + lane;
+  x = ((t & 8) ? pb : pa) * v;
+}
+
+// Adds one batch of the span's entries (one per lane; c = D + lane for a lane without one) to the
+// warp's outv. The lanes post their ids to the warp's owner table at their channel (a shared-memory
+// atomic minimum) and read it back: the lowest lane of each channel adds its entry, with no
+// branch (a lane without an entry updates a slot of its own), and resets the slot. Returns the
+// other lanes (a channel hit twice or more in the batch), which the caller adds one after another
+// in lane order (value_outlier_rest) before the next batch. Within a channel the lanes' entries
+// are in token order (CSR: (token, channel) order; CSC: (channel, token) order), so every
+// channel's sum is the same sequence of fp32 additions, in token order, for both value-outlier
+// layouts and whatever the thread timing.
+__device__ __forceinline__ uint32_t value_outlier_batch(uint32_t outv, uint32_t own, int c, float x, int lane) {
+  const uint32_t slot = own + 4 * c;
+  asm volatile("red.shared.min.s32 [%0], %1;" ::"r"(slot), "r"(lane));
+  __syncwarp();
+  int o;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(o) : "r"(slot));
+  const bool first = o == lane;  // always for a lane without an entry (its own slot)
+  const uint32_t addr = outv + 4 * (first ? c : D + lane);
+  sts_f32(addr, lds_f32(addr) + x);
+  __syncwarp();
+  asm volatile("st.shared.s32 [%0], %1;" ::"r"(slot), "r"(32));
+  return __ballot_sync(0xffffffffu, !first);
+}
+
+// The left-over entries of a batch, one after another in lane order.
+__device__ __forceinline__ void value_outlier_rest(uint32_t outv, uint32_t rest, int c, float x, int lane) {
+  for (uint32_t m = rest; m; m &= m - 1) {
+    __syncwarp();
+    if (lane == __ffs(m) - 1) sts_f32(outv + 4 * c, lds_f32(outv + 4 * c) + x);
+  }
+  __syncwarp();
+}
+
+// Entries past the span's first 32: whole batches of 32, each finished (first lanes, then the rest
+// in lane order) before the next.
+template <bool CSC>
+__device__ __forceinline__ void value_outlier_more(uint32_t sa, uint32_t rw, uint32_t outv, uint32_t own, const Geo& g,
+                                                   int e0, int e1, float p0, float p1, int lane) {
+  for (int kb = e0 + 32; kb < e1; kb += 32) {
+    int c;
+    float x;
+    value_outlier_load<CSC>(sa, rw, g, kb + lane, e1, p0, p1, lane, c, x);
+    const uint32_t rest = value_outlier_batch(outv, own, c, x, lane);
+    if (rest) value_outlier_rest(outv, rest, c, x, lane);
   }
 }
 
@@ -480,26 +599,37 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
   const Geo& g = a.g;
   const uint32_t sb = stage_bytes(g);
   const int gq = lane >> 2, tq = lane & 3;
-  // (cos, sin) of the lane's (token, pair) cells: tokens 16w + gq + 8r, pairs 4kg + tq
+  // (cos, sin) of the lane's (token, pair) cells: tokens 16w + gq + 8r, pairs 4kg + tq, from the
+  // cache's in-block angle table (L2-resident)
+  const float2* rope_loc = reinterpret_cast<const float2*>(a.base + g.rope_off) + (size_t)(g.max_blocks + 1) * 64;
   float2 wcs[2][16];
 #pragma unroll
   for (int r = 0; r < 2; ++r)
 #pragma unroll
-    for (int kg = 0; kg < 16; ++kg) wcs[r][kg] = sm->rope_loc[(16 * warp + gq + 8 * r) * 64 + 4 * kg + tq];
-  const int brow = (gq >> 1) == tq ? gq : 8;             // lanes holding nonzero score B rows 0..7
-  const int zrow = tq == 0 ? gq : 8;                     // lanes holding the zero-point rows 8, 9
-  const uint32_t ones = tq == 0 ? 0x3c003c00u : 0u;      // A columns 8, 9 = 1.0 (fp16), others 0
+    for (int kg = 0; kg < 16; ++kg) wcs[r][kg] = __ldg(rope_loc + (16 * warp + gq + 8 * r) * 64 + 4 * kg + tq);
+  const int brow = (gq >> 1) == tq ? gq : 8;             // lanes holding a part of the score B operand
+  const uint32_t ones = 0x3c003c00u;                     // A columns 8..15 = 1.0 (fp16)
   const int src_a = 4 * tq + (gq < 2 ? gq : 2);          // value B: (high, low, zero) source lanes
   const uint32_t xsel = tq == 0 ? 0xffffffffu : 0u;      // this lane sends p' high (tq 0) ...
   const uint32_t ysel = tq == 1 ? 0xffffffffu : 0u;      // ... or low (tq 1) or zero
-  const int t0 = 16 * warp + gq, t1 = t0 + 8;
-  long long* outv = sm->outv[warp];
+  const int t0 = 16 * warp + gq;
+  // shared-window addresses: stage bases and the lane's fixed offsets in a stage / operand block
+  const uint32_t ring_sa = smem_u32(ring), ops_sa = smem_u32(&sm->op[0]);
+  const uint32_t rows_sa = smem_u32(rows);
+  const uint32_t outv = smem_u32(&sm->outv[warp][0]), own = smem_u32(&sm->own[warp][0]);
+  const uint32_t vtag_ofs = (uint32_t)round16((uint64_t)g.n_out);
+  const uint32_t kofs = g.codes_off[0] + warp * 768 + lane * 24, vofs = g.codes_off[1] + warp * 768 + lane * 24;
+  const uint32_t vmofs = g.meta_off[1] + 2 * t0;
+  const uint32_t bofs = OPS_B + brow * OPS_ROW, skofs = OPS_SK + 4 * t0;
+  auto stage_sa = [&](int i) { return ring_sa + (uint32_t)(i % NBS) * sb; };
+  auto ops_of = [&](int i) { return ops_sa + (uint32_t)(i % NBS) * (uint32_t)sizeof(Ops); };
 
   auto ready_now = [&](int i) -> bool {  // the stage of range block i is ready (no waiting)
     const int s = i % NBS;
     const uint32_t par = (uint32_t)((i / NBS) & 1);
     return mbar_test_wait(&sm->ops_full[s], par) & mbar_test_wait(&sm->rec_full[s], par);
   };
+  const bool vout = g.n_out > 0;
   auto wait_stage = [&](int i) -> bool {  // false when a wait gave up
     const int s = i % NBS;
     const uint32_t par = (uint32_t)((i / NBS) & 1);
@@ -530,20 +660,34 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
       th1 = (hb[4] >> 8) | (hb[5] >> 8) << 8 | (hb[6] >> 8) << 16 | (hb[7] >> 8) << 24;
     }
 #pragma unroll
-    for (int k = 0; k < 4; ++k) outv[lane + 32 * k] = 0;
+    for (int k = 0; k < 4; ++k) sts_f32(outv + 4 * (lane + 32 * k), 0.0f);
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
     float m_w = -INFINITY, l_w = 0.0f, z_w = 0.0f;
     __syncwarp();
     if (!wait_stage(i)) return;
+    bool ahead = i + 1 < iend ? ready_now(i + 1) : true;
+    // software pipeline: the scores of block j + 1 are issued first (they do not depend on the
+    // softmax), then block j's softmax and value product, whose dependency chain the score work
+    // covers; block j + 1's scores are only needed in the next iteration
     float sv0, sv1;
-    block_scores(ring + (size_t)(i % NBS) * sb, sm->op[i % NBS], g.codes_off[0], warp, lane, brow, zrow, ones, t0, t1,
-                 tl0, tl1, th0, th1, wcs, sv0, sv1);
+    block_scores(stage_sa(i) + kofs, ops_of(i) + bofs, ops_of(i) + skofs, ones, tl0, tl1, th0, th1, wcs, sv0, sv1);
     for (int j = i; j < iend; ++j) {
       const int s = j % NBS;
-      const uint8_t* st = ring + (size_t)s * sb;
+      const uint32_t sa = stage_sa(j);
       const bool more = j + 1 < iend;  // warp-uniform
-      const bool ready = more ? ready_now(j + 1) : true;  // its latency overlaps the softmax
+      // stage j + 1 was probed during the previous block (no waiting); only when that probe
+      // failed does the warp wait for it here
+      if (!__all_sync(0xffffffffu, ahead)) {
+        if (more && !wait_stage(j + 1)) return;
+      }
+      float nv0 = 0.0f, nv1 = 0.0f;
+      if (more) {
+        const uint32_t sa1 = stage_sa(j + 1), op1 = ops_of(j + 1);
+        block_scores(sa1 + kofs, op1 + bofs, op1 + skofs, ones, tl0, tl1, th0, th1, wcs, nv0, nv1);
+      }
+      // probe stage j + 2 (its latency overlaps the work below)
+      ahead = j + 2 < iend ? ready_now(j + 2) : true;
       if (g.sink && blk + (j - i) == 0 && warp == 0 && gq == 0) sv0 = -INFINITY;  // the kept first token
       // online softmax with block j's scores (base 2). m_w is the reference the warp's sums are
       // kept relative to; it moves up only when a score passes it by more than RESCALE_SLACK, so
@@ -555,7 +699,7 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
         mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 8));
         mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, 16));
         mloc = fmaxf(mloc, m_w);
-        const float al = exp2f(m_w - mloc);
+        const float al = fast_exp2(m_w - mloc);
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
           acc[mt][0] *= al; acc[mt][1] *= al; acc[mt][2] *= al; acc[mt][3] *= al;
@@ -564,29 +708,40 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
         z_w *= al;
         __syncwarp();
 #pragma unroll
-        for (int k = 0; k < 4; ++k) outv[lane + 32 * k] = llrintf((float)outv[lane + 32 * k] * al);
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t o = outv + 4 * (lane + 32 * k);
+          sts_f32(o, lds_f32(o) * al);
+        }
         __syncwarp();
         m_w = mloc;
       }
-      const float p0 = exp2f(sv0 - m_w), p1 = exp2f(sv1 - m_w);
+      const float p0 = fast_exp2(sv0 - m_w), p1 = fast_exp2(sv1 - m_w);
       l_w += p0 + p1;
-      const uint8_t* rw = rows + (size_t)s * rows_stride + round16((uint64_t)g.n_out);
-      int e0 = 0, e1 = 0;
-      if (g.n_out > 0) value_outlier_span<CSC>(st, rw, g, warp, e0, e1);
-      if (more) {
-        if (!__all_sync(0xffffffffu, ready) && !wait_stage(j + 1)) return;
-        const int s1 = (j + 1) % NBS;
-        value_outlier_entry<CSC>(st, g, rw, e0 + lane, e1, t0, p0, p1, outv);
-        block_values(st, g, warp, lane, t0, t1, src_a, xsel, ysel, p0, p1, tl0, tl1, th0, th1, z_w, acc);
-        block_scores(ring + (size_t)s1 * sb, sm->op[s1], g.codes_off[0], warp, lane, brow, zrow, ones, t0, t1, tl0,
-                     tl1, th0, th1, wcs, sv0, sv1);
-      } else {
-        value_outlier_entry<CSC>(st, g, rw, e0 + lane, e1, t0, p0, p1, outv);
-        block_values(st, g, warp, lane, t0, t1, src_a, xsel, ysel, p0, p1, tl0, tl1, th0, th1, z_w, acc);
+      // value outliers: the first 32 entries of the warp's span as one branch-free batch placed
+      // with the tensor-core work; what is left (channels hit twice or more, entries past the
+      // first 32) after it, on warp-uniform paths
+      const uint32_t rw = rows_sa + (uint32_t)s * (uint32_t)rows_stride + vtag_ofs;
+      uint32_t rest = 0;
+      int c1 = D + lane;
+      float x1 = 0.0f;
+      bool more_batches = false;
+      if (vout) {
+        int e0, e1;
+        value_outlier_span<CSC>(sa, rw, g, warp, e0, e1);
+        value_outlier_load<CSC>(sa, rw, g, e0 + lane, e1, p0, p1, lane, c1, x1);
+        rest = value_outlier_batch(outv, own, c1, x1, lane);
+        more_batches = e1 - e0 > 32;
       }
-      for (int e = e0 + 32 + lane; e - lane < e1; e += 32)  // more than 32 entries: uniform trip count
-        value_outlier_entry<CSC>(st, g, rw, e, e1, t0, p0, p1, outv);
+      block_values(sa + vofs, sa + vmofs, src_a, xsel, ysel, p0, p1, tl0, tl1, th0, th1, z_w, acc);
+      if (rest) value_outlier_rest(outv, rest, c1, x1, lane);
+      if (more_batches) {
+        int e0, e1;
+        value_outlier_span<CSC>(sa, rw, g, warp, e0, e1);
+        value_outlier_more<CSC>(sa, rw, outv, own, g, e0, e1, p0, p1, lane);
+      }
       release(s);
+      sv0 = nv0;
+      sv1 = nv1;
     }
     // the segment's partial row
     {
@@ -605,8 +760,8 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
             const int c0 = 16 * mt + gq, c1 = c0 + 8;
-            a.ws_o[row * D + c0] = acc[mt][0] + acc[mt][1] + zt + (float)outv[c0] * OUTV_UNIT;
-            a.ws_o[row * D + c1] = acc[mt][2] + acc[mt][3] + zt + (float)outv[c1] * OUTV_UNIT;
+            a.ws_o[row * D + c0] = acc[mt][0] + acc[mt][1] + zt + lds_f32(outv + 4 * c0);
+            a.ws_o[row * D + c1] = acc[mt][2] + acc[mt][3] + zt + lds_f32(outv + 4 * c1);
           }
         }
         if (lane == 0) {
@@ -636,15 +791,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
   const long long x0 = R * a.total / a.n_ranges, x1 = (R + 1) * a.total / a.n_ranges;
   const int n = (int)(x1 - x0);
   if (n <= 0) return;
-  {  // the in-block angle table, staged once per CTA
-    const float4* src = reinterpret_cast<const float4*>(a.base + a.g.rope_off) + (size_t)(a.g.max_blocks + 1) * 32;
-    float4* dst = reinterpret_cast<float4*>(sm->rope_loc);
-    for (int e = tid; e < T * 32; e += NTHREADS) dst[e] = __ldg(src + e);
+  {  // the in-block angle tables of the key outliers: t * theta_i = 16a * theta_i + b * theta_i
+    const float2* loc = reinterpret_cast<const float2*>(a.base + a.g.rope_off) + (size_t)(a.g.max_blocks + 1) * 64;
+    for (int e = tid; e < 8 * 64; e += NTHREADS) sm->rope_a[e >> 6][e & 63] = __ldg(loc + (size_t)(16 * (e >> 6)) * 64 + (e & 63));
+    for (int e = tid; e < 16 * 64; e += NTHREADS) sm->rope_b[e >> 6][e & 63] = __ldg(loc + e);
   }
-  for (int e = tid; e < NBS * 20; e += NTHREADS) {
-    sm->op[e / 20].bk[8][e % 20] = 0u;
-    sm->op[e / 20].bz[8][e % 20] = 0u;
-  }
+  for (int e = tid; e < NBS * 36; e += NTHREADS) sm->op[e / 36].b[8][e % 36] = 0u;
+  for (int e = tid; e < NW * (D + 32); e += NTHREADS) (&sm->own[0][0])[e] = 32;
   if (tid == 0) {
     for (int s = 0; s < NBS; ++s) {
       mbar_init(&sm->rec_full[s], 1);
@@ -665,7 +818,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
 }
 
 size_t smem_bytes(const Geo& g) {
-  return (size_t)NB * ((size_t)g.rec_bytes + ROPE_ROW) + sizeof(Smem) + (size_t)NB * rows_stride_of(g.n_out, g.v_csc) +
+  return (size_t)NB * (size_t)g.rec_bytes + sizeof(Smem) + (size_t)NB * rows_stride_of(g.n_out, g.v_csc) +
          2 * sizeof(float) * round16((uint64_t)g.n_out) + (g.v_csc ? 2 * 16 * sizeof(int) : 0);
 }
 

@@ -287,4 +287,23 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   }
 }
 
+// Waits like mbar_wait_bounded, for warps that run ahead of the ones they feed (producers and
+// helpers): polls with the non-blocking probe and sleeps ~SLEEP_NS between probes, so that a
+// waiting warp neither takes issue slots nor keeps the barrier unit busy for the warps doing the
+// work. A probe that fails records KVQ_ERR_TIMEOUT after ~max_cycles SM clocks.
+template <int SLEEP_NS = 64>
+__device__ __forceinline__ bool mbar_wait_backoff(uint64_t* bar, uint32_t parity, int* status,
+                                                  long long max_cycles = 2000000000LL) {
+  if (mbar_test_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    __nanosleep(SLEEP_NS);
+    if (mbar_test_wait(bar, parity)) return true;
+    if (clock64() - t0 > max_cycles) {
+      report(status, KVQ_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 }  // namespace kvq
