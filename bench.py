@@ -398,12 +398,93 @@ def run_kvq(args):
     }
     if args.e2e:
         res["e2e"] = run_e2e(args, K, torch, dev, caches, cfg, w, nb, q, tail_k, tail_v, cache_bytes)
+    if args.per_config and not args.ctx and (args.bits, args.scale_group) == (0, 0):
+        # the other workloads of the benchmark, one empty-tail decode each at full size
+        others = [c for c in (1, 2, 3, 4, 5) if c != w.cfg_id]
+        del caches, ws
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        with Clocks(gpu_id) as pclk:
+            pc = per_config_decodes(K, torch, dev, rank, others, peak)
+        pc["clocks"] = pclk.summary()
+        pc["timing"] = ("CUDA graph replays of empty-tail decodes (kvq_decode_attn + combine), CUDA events on "
+                        "the launching stream; cache copies rotated so that each decode reads data not in L2")
+        res["per_config"] = pc
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w, args.cpu_sample_heads)
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     return res if rank == 0 else None
+
+
+def per_config_decodes(K, torch, dev, rank, cfg_ids, peak):
+    """One decode with an empty tail per workload, timed like the headline roofline entry: CUDA
+    graph replays of R decodes that rotate over enough cache copies to exceed 3x L2, events on the
+    launching stream, clocks sampled meanwhile. Inputs are drawn on the device (performance only);
+    each workload's cache is freed before the next one is built."""
+    out = {}
+    cap = torch.cuda.Stream(device=dev)
+    for cid in cfg_ids:
+        w = WL.WORKLOADS[cid]
+        nb = w.n_blocks
+        cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, nb, w.dtype, w.pre_rope,
+                            w.rope_theta, w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT, 0, False, False,
+                            w.scale_group, False)
+        lay = K.kvq_layout(cfg)
+        cb = None
+        if w.method == "nuq":
+            from statistics import NormalDist
+            inv = NormalDist().inv_cdf
+            n = 2 ** w.bits
+            cb = torch.tensor([[inv((j + 0.5) / n) / inv((n - 0.5) / n) for j in range(n)]] * w.n_kv_heads,
+                              dtype=torch.float32)
+        shape = (w.batch, w.n_kv_heads, nb * 128, 128)
+        caches = [K.KVCache(cfg, cb, device=dev)]
+        Kd = _gen_device(w, torch, dev, shape, 0, rank)
+        Vd = _gen_device(w, torch, dev, shape, 1, rank)
+        caches[0].append(Kd, Vd)
+        del Kd, Vd
+        n_copies = max(1, math.ceil(3 * L2_BYTES / max(1, int(lay.records_bytes))))
+        for _ in range(n_copies - 1):
+            c = K.KVCache(cfg, cb, device=dev)
+            c.base.copy_(caches[0].base)
+            c.cache.n_blocks = nb
+            caches.append(c)
+        q = _gen_device(w, torch, dev, (w.batch, w.n_q_heads, 128), 1, rank + 11)
+        o = torch.empty(w.batch, w.n_q_heads, 128, dtype=torch.float32, device=dev)
+        ws = caches[0].workspace
+        reps = 8 if w.n_blocks * w.batch * w.n_kv_heads > 100000 else 32
+        cap.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(cap):
+            for i in range(3):
+                K.kvq_decode_attn(caches[i % n_copies].cache, q, None, None, 0, o, ws, cap)
+            cap.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=cap):
+                for i in range(reps):
+                    K.kvq_decode_attn(caches[i % n_copies].cache, q, None, None, 0, o, ws, cap)
+            gr.replay()
+            cap.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cap)
+            for _ in range(3):
+                gr.replay()
+            e1.record(cap)
+            e1.synchronize()
+        us = 1e3 * e0.elapsed_time(e1) / (3 * reps)
+        status = max(int(c.status.item()) for c in caches)
+        if status != 0:
+            raise RuntimeError(f"config {cid}: device status {status} ({K.kvq_status_str(status)})")
+        dec_bytes = K.kvq_decode_bytes(cfg, nb)
+        gbs = dec_bytes / (us * 1e-6) / 1e9
+        out[str(cid)] = {"workload": w.name, "decode_us_empty_tail": round(us, 3), "gbs": round(gbs, 1),
+                         "frac": round(gbs / peak, 4), "packed_bytes_per_decode": dec_bytes,
+                         "kernel": _decode_kernel_name(w) + " + combine_kernel", "cache_copies": n_copies}
+        del caches, gr, q, o, ws
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, K, torch, dev, caches, cfg, w, nb, q, tail_k, tail_v, cache_bytes):
@@ -810,6 +891,8 @@ def main():
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-per-config", dest="per_config", action="store_false",
+                    help="skip the empty-tail decode of every other workload at full size")
     ap.add_argument("--key-calib", dest="key_calib", action="store_true",
                     help="nuq: offline-calibrated key statistics (calibration keys drawn with another seed)")
     ap.add_argument("--sink", action="store_true", help="nuq: keep the first token in the input precision")

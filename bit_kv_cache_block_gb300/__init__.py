@@ -112,6 +112,12 @@ def kvq_reset(cache: kvq_cache) -> None:
     _lib.check(_lib.lib().kvq_reset(C.byref(cache)), "kvq_reset")
 
 
+def kvq_debug_stall_decode(enable: bool) -> None:
+    """Test switch: later nuq tensor-core decodes run with no copies and ~1 ms wait bounds, so they
+    record KVQ_ERR_TIMEOUT and write NaN (see include/kvq.h)."""
+    _lib.check(_lib.lib().kvq_debug_stall_decode(1 if enable else 0), "kvq_debug_stall_decode")
+
+
 def kvq_decode_splits(cfg: kvq_config, n_blocks: int) -> int:
     return int(_lib.lib().kvq_decode_splits(C.byref(cfg), int(n_blocks)))
 

@@ -23,7 +23,7 @@ METHODS = {"rtn": KVQ_RTN, "nuq": KVQ_NUQ, "varn": KVQ_VARN, "int4": KVQ_INT4}
 
 # every entry point declared in include/kvq.h
 EXPORTS = ["kvq_status_str", "kvq_dense_kv_bytes", "kvq_layout", "kvq_cache_init", "kvq_append_block",
-           "kvq_truncate", "kvq_reset", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
+           "kvq_truncate", "kvq_reset", "kvq_debug_stall_decode", "kvq_decode_splits", "kvq_decode_workspace_bytes", "kvq_decode_bytes",
            "kvq_decode_attn", "kvq_decode_attn_ex", "kvq_decode_attn_static", "kvq_dequant", "kvq_calibrate_keys", "kvq_error_stats",
            "kvq_error_topk_workspace_bytes", "kvq_error_topk", "kvq_fit_codebook_workspace_bytes",
            "kvq_fit_codebook"]
@@ -83,6 +83,8 @@ def lib() -> C.CDLL:
     L.kvq_truncate.argtypes = [P(kvq_cache), i32]
     L.kvq_reset.restype = C.c_int
     L.kvq_reset.argtypes = [P(kvq_cache)]
+    L.kvq_debug_stall_decode.restype = C.c_int
+    L.kvq_debug_stall_decode.argtypes = [i32]
     L.kvq_decode_splits.restype = i32
     L.kvq_decode_splits.argtypes = [P(kvq_config), i32]
     L.kvq_decode_workspace_bytes.restype = C.c_int

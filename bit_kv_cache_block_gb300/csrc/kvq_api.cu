@@ -1,4 +1,5 @@
 // Host side of the C ABI: argument checks, layout arithmetic and kernel launches.
+#include <atomic>
 #include <cmath>
 #include <cstring>
 
@@ -76,6 +77,17 @@ kvq_status on_device(int dev, F fn) {
 }
 
 int hadamard_of(const kvq_config& c) { return c.method == KVQ_VARN ? c.hadamard : 0; }
+
+// Test switch of kvq_debug_stall_decode (process-wide; read when a decode is launched).
+std::atomic<int> g_dbg_stall{0};
+
+// A decode's kernel parameters under the test switch: no copies, waits bounded at ~1 ms.
+void apply_debug(kvq::Geo& g) {
+  if (g_dbg_stall.load(std::memory_order_relaxed)) {
+    g.dbg_stall = 1;
+    g.wait_cycles = 2000000LL;
+  }
+}
 
 // Kernel parameters of a cache; paged caches need their block table (non-null, 4-byte aligned).
 kvq_status geo_of(const kvq_cache* cache, kvq::Geo& g) {
@@ -240,6 +252,12 @@ kvq_status kvq_truncate(kvq_cache* cache, int32_t n_blocks) {
   return KVQ_OK;
 }
 
+kvq_status kvq_debug_stall_decode(int32_t enable) {
+  if (enable != 0 && enable != 1) return KVQ_ERR_INVALID_ARG;
+  g_dbg_stall.store(enable, std::memory_order_relaxed);
+  return KVQ_OK;
+}
+
 kvq_status kvq_reset(kvq_cache* cache) { return kvq_truncate(cache, 0); }
 
 int32_t kvq_decode_splits(const kvq_config* cfg, int32_t n_blocks) {
@@ -307,6 +325,7 @@ kvq_status kvq_decode_attn_ex(const kvq_cache* cache, const void* q, const void*
     if (!aligned(workspace, 16)) return KVQ_ERR_ALIGNMENT;
   }
   return on_device(cache->device, [&]() {
+    apply_debug(g);
     return kvq_launch_decode(g, static_cast<const uint8_t*>(cache->base), cache->codebook,
                              static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(tail_k),
                              static_cast<const uint16_t*>(tail_v), n_tail, tail_bh_stride, tail_token_stride, nb, S,
@@ -340,6 +359,7 @@ kvq_status kvq_decode_attn_static(const kvq_cache* cache, const void* q, const v
       cap = KVQ_ERR_CAPACITY;
       return cudaSuccess;
     }
+    apply_debug(g);
     return kvq_launch_decode(g, static_cast<const uint8_t*>(cache->base), cache->codebook,
                              static_cast<const uint16_t*>(q), static_cast<const uint16_t*>(tail_k),
                              static_cast<const uint16_t*>(tail_v), n_tail, (long long)n_tail * kvq::D, kvq::D, nb, S,

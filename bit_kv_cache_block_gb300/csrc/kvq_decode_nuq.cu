@@ -208,11 +208,12 @@ __device__ void producer(const Args& a, Smem* sm, uint8_t* ring, long long x0, i
   long long u = x0 / a.nb;
   int blk = (int)(x0 - u * a.nb);
   int pb = (int)(u / g.H), ph = (int)(u - (long long)pb * g.H);  // (b, h) of block p
+  if (g.dbg_stall) return;  // test switch: no copies, so every stage wait of the others runs out
   int issued = 0;
   for (int p = 0; p < n; ++p) {
     const int s = p % NBS;
     if (p >= NBS) {
-      const bool got = mbar_wait_backoff(&sm->empty[s], (uint32_t)(((p / NBS) - 1) & 1), a.status);
+      const bool got = mbar_wait_backoff(&sm->empty[s], (uint32_t)(((p / NBS) - 1) & 1), a.status, g.wait_cycles);
       if (__any_sync(0xffffffffu, !got)) break;
     }
     const int set = 2 * (p & 15), part = lane - set;  // lanes set, set+1 copy this block
@@ -284,7 +285,7 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
       while (nb2 >= a.nb) nb2 -= a.nb;
       if (p + 2 < n) cs_next = __ldg(rope_blk + (size_t)nb2 * 64 + j);
     }
-    const bool got = mbar_wait_backoff(&sm->rec_full[s], (uint32_t)((p / NBS) & 1), a.status);
+    const bool got = mbar_wait_backoff(&sm->rec_full[s], (uint32_t)((p / NBS) & 1), a.status, g.wait_cycles);
     if (bar_or_group(grp, !got)) break;  // the consumers time out on their own waits
     const uint8_t* st = ring + (size_t)s * sb;
     Ops& op = sm->op[s];
@@ -633,8 +634,8 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
   auto wait_stage = [&](int i) -> bool {  // false when a wait gave up
     const int s = i % NBS;
     const uint32_t par = (uint32_t)((i / NBS) & 1);
-    const bool got = mbar_wait_bounded(&sm->ops_full[s], par, a.status) &&
-                     mbar_wait_bounded(&sm->rec_full[s], par, a.status);
+    const bool got = mbar_wait_bounded(&sm->ops_full[s], par, a.status, g.wait_cycles) &&
+                     mbar_wait_bounded(&sm->rec_full[s], par, a.status, g.wait_cycles);
     return !__any_sync(0xffffffffu, !got);
   };
   auto release = [&](int s) {  // this warp is done with stage s

@@ -111,6 +111,10 @@ struct Geo {
   uint64_t calib_off, sink_off;
   int g64;              // INT4: one scale per 64 channels (meta vectors: channels 0..63, 64..127)
   int v_csc;            // NUQ: value outliers by column (col_ptr over channels, token per entry)
+  // Bound of every stage wait, in SM clocks (about 1 s by default), and a test switch under which
+  // the decode's producer issues no copies, so that its waits run out (kvq_debug_stall_decode).
+  long long wait_cycles;
+  int dbg_stall;
 };
 
 inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
@@ -135,6 +139,8 @@ inline Geo make_geo(const kvq_config& c, const kvq_layout_t& l) {
   g.sink_off = l.sink_off;
   g.g64 = c.method == KVQ_INT4 && c.scale_group == 64;
   g.v_csc = c.method == KVQ_NUQ && c.v_csc;
+  g.wait_cycles = 2000000000LL;
+  g.dbg_stall = 0;
   return g;
 }
 

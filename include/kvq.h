@@ -247,6 +247,15 @@ kvq_status kvq_truncate(kvq_cache* cache, int32_t n_blocks);
 /* kvq_truncate(cache, 0). */
 kvq_status kvq_reset(kvq_cache* cache);
 
+/* Test switch for the failure path of the bounded device waits (not part of the method; no
+ * counterpart on the pages). With enable = 1, every later decode of this process that runs on the
+ * 3-bit nuq tensor-core kernel launches it with its copy-issuing warp idle and its stage waits
+ * bounded at ~2 million SM clocks (about 1 ms): the waits run out, the kernel records
+ * KVQ_ERR_TIMEOUT in dev_status, every thread returns, and out is written as NaN. Nothing faults
+ * and the context stays usable. enable = 0 restores normal decodes; the caller clears dev_status.
+ * Other decode kernels ignore the switch. Returns KVQ_ERR_INVALID_ARG for other values. */
+kvq_status kvq_debug_stall_decode(int32_t enable);
+
 /* Number of sequence splits the decode uses for n_blocks cached blocks (a pure function of
  * the config and n_blocks). */
 int32_t kvq_decode_splits(const kvq_config* cfg, int32_t n_blocks);
