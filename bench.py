@@ -46,8 +46,8 @@ BENCH_LAYOUT = "mma"
 # shared header); once they change the traffic reads null until a new capture replaces it.
 # Captures and commands: profiles/dram_traffic_decode_kernels.md.
 PROFILED_TRAFFIC = {
-    2: {"bytes_per_record": 14868.3, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
-        "sha256_16": "a31b66c4928f1fc8", "capture": "same workload at L = 16384 (4096 records)"},
+    2: {"bytes_per_record": 14870.6, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
+        "sha256_16": "339632d5d3b9c159", "capture": "same workload at L = 16384 (4096 records)"},
     3: {"bytes_per_record": 9791.8, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
         "sha256_16": "2c3fc1268b83079d", "capture": "full workload (8192 records)"},
     4: {"bytes_per_record": 17071.1, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
@@ -569,28 +569,129 @@ def _oracle_sample(w, heads, seed=0):
     return t_app, t_dec
 
 
+def _oracle_pool_worker(cid, pair, n_blocks, barrier, cmd_q, out_q):
+    """One worker of the multi-core oracle runs: builds its (b, h) pair's cache over n_blocks
+    (append timed), then per command decodes it once, all workers starting together at the
+    barrier; reports the monotonic times of each phase."""
+    import oracle as O
+    ws = WL.WORKLOADS[cid].scaled(ctx=128 * n_blocks)
+    oc = O.OracleCache.for_workload(ws, layout=O.LAYOUT_MMA if BENCH_LAYOUT == "mma" else O.LAYOUT_ROWS)
+    a0 = time.perf_counter()
+    for blk in range(n_blocks):
+        K = np.zeros((ws.batch, ws.n_kv_heads, 128, 128), np.float32)
+        V = np.zeros_like(K)
+        K[pair] = WL.tile(ws, pair[0], pair[1], blk, 0)
+        V[pair] = WL.tile(ws, pair[0], pair[1], blk, 1)
+        oc.append(K, V, only_heads={pair})
+    out_q.put((a0, time.perf_counter()))
+    while True:
+        step = cmd_q.get()
+        if step is None:
+            break
+        q = WL.query(ws, step)
+        barrier.wait()
+        d0 = time.perf_counter()
+        oc.decode(q, only_heads={pair})
+        out_q.put((d0, time.perf_counter()))
+
+
+class OraclePool:
+    """The oracle on n_procs spawned processes, one (b, h) pair of workload cid each, over the first
+    n_blocks blocks of its context. Run with BLAS pinned to one thread per process, so n_procs is
+    the number of host cores in use. append_s = wall time of all workers' appends; step(i) = wall
+    time of one decode of every pair, all started together."""
+
+    def __init__(self, cid, n_blocks, n_procs):
+        import multiprocessing as mp
+        w = WL.WORKLOADS[cid]
+        self.pairs = [(b, h) for b in range(w.batch) for h in range(w.n_kv_heads)][:max(1, n_procs)]
+        ctx = mp.get_context("spawn")
+        barrier = ctx.Barrier(len(self.pairs))
+        self.cmd_q, self.out_q = ctx.Queue(), ctx.Queue()
+        self.procs = [ctx.Process(target=_oracle_pool_worker,
+                                  args=(cid, pr, n_blocks, barrier, self.cmd_q, self.out_q))
+                      for pr in self.pairs]
+        for p in self.procs:
+            p.start()
+        res = [self.out_q.get() for _ in self.procs]
+        self.append_s = max(r[1] for r in res) - min(r[0] for r in res)
+
+    def step(self, i):
+        for _ in self.procs:
+            self.cmd_q.put(i)
+        res = [self.out_q.get() for _ in self.procs]
+        return max(r[1] for r in res) - min(r[0] for r in res)
+
+    def close(self):
+        for _ in self.procs:
+            self.cmd_q.put(None)
+        for p in self.procs:
+            p.join()
+
+
+def _host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
+def _pair_bytes(w, nb):
+    """Packed-cache bytes one decode reads for one (b, h) pair over nb blocks."""
+    import bit_kv_cache_block_gb300 as K
+    cfg = K.make_config(w.method, w.bits, 1, 1, w.group, nb, w.dtype, w.pre_rope, w.rope_theta,
+                        w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT)
+    return K.kvq_decode_bytes(cfg, nb)
+
+
+def oracle_baseline_run():
+    """All the oracle timings of the CPU baseline (run in a subprocess with BLAS on one thread):
+    the headline workload on every host core and on one, and a single-core sample of each other
+    workload (append per block and decode per step extrapolated from a sample of blocks)."""
+    n_cores = _host_cores()
+    res = {"cores": n_cores, "cpu": _cpu_model(), "per_config": {}}
+    w = WL.WORKLOADS[2]
+    nb = w.n_blocks
+    for key, n in (("all_cores", min(n_cores, w.batch * w.n_kv_heads)), ("one_core", 1)):
+        pool = OraclePool(2, nb, n)
+        dec = min(pool.step(i) for i in range(2))
+        pool.close()
+        npairs = len(pool.pairs)
+        res[key] = {"pairs": npairs, "blocks": nb, "decode_s": round(dec, 3), "append_s": round(pool.append_s, 3),
+                    "decode_gbs": round(npairs * _pair_bytes(w, nb) / dec / 1e9, 5),
+                    "append_tokens_per_s": round(npairs * nb * 128 / pool.append_s, 1)}
+    for cid in (1, 2, 3, 4, 5):
+        wc = WL.WORKLOADS[cid]
+        ns = min(wc.n_blocks, {1: 16, 2: 256, 3: 32, 4: 32, 5: 256}[cid])
+        ws = wc.scaled(ctx=128 * ns)
+        pool = OraclePool(cid, ns, 1)
+        t_dec = min(pool.step(i) for i in range(2))
+        pool.close()
+        t_app = pool.append_s
+        units = wc.batch * wc.n_kv_heads
+        res["per_config"][str(cid)] = {
+            "workload": wc.name, "sample": f"1 (batch, KV head) pair, {ns} of {wc.n_blocks} blocks, one core",
+            "append_ms_per_block_all_heads": round(1e3 * t_app / ns * units, 3),
+            "decode_ms_per_step": round(1e3 * t_dec / ns * units * wc.n_blocks, 3),
+            "decode_gbs_one_core": round(_pair_bytes(ws, ns) / t_dec / 1e9, 5)}
+    return res
+
+
 def cpu_baseline(w, n_heads):
-    """The oracle (as it stands, single process) on a bounded sample: n_heads (b, h) pairs of
-    the workload, every block of their context."""
-    heads = [(0, h) for h in range(min(n_heads, w.n_kv_heads))]
+    """The oracle as it stands, timed on the host cores in a subprocess with BLAS pinned to one
+    thread per process: the headline workload on every core (one worker process per core, one
+    (b, h) pair each, whole context) and on one core, plus a single-core sample of every workload.
+    value = the headline decode throughput on all cores (GB/s of packed cache decoded)."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    code = ("import sys, json; sys.path.insert(0, %r); import bench, workloads as WL; "
-            "w = WL.WORKLOADS[%d]; a, d = bench._oracle_sample(w, %r); print(json.dumps([a, d]))"
-            % (ROOT, w.cfg_id, heads))
+    code = ("import sys, json; sys.path.insert(0, %r); import bench; print(json.dumps(bench.oracle_baseline_run()))"
+            % ROOT)
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True)
     if r.returncode != 0:
-        return {"value": None, "unit": "GB/s", "cores": 1, "kind": "oracle", "error": r.stderr[-400:]}
-    t_app, t_dec = json.loads(r.stdout.strip().splitlines()[-1])
-    import bit_kv_cache_block_gb300 as K
-    cfg = K.make_config(w.method, w.bits, 1, 1, w.group, w.n_blocks, w.dtype, w.pre_rope, w.rope_theta,
-                        w.outlier_frac, w.varn_iters, True, BENCH_LAYOUT)
-    per_head = K.kvq_decode_bytes(cfg, w.n_blocks)
-    nbytes = per_head * len(heads)
-    return {"value": round(nbytes / t_dec / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{len(heads)} of {w.batch * w.n_kv_heads} (batch, KV head) pairs, all {w.n_blocks} blocks; "
-                      f"decode {t_dec:.2f} s, append {t_app:.2f} s",
-            "append_tokens_per_s": round(len(heads) * w.n_blocks * 128 / t_app, 1),
-            "cpu": _cpu_model()}
+        return {"value": None, "unit": "GB/s", "cores": None, "kind": "oracle", "error": r.stderr[-400:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    ac = d["all_cores"]
+    return {"value": ac["decode_gbs"], "unit": "GB/s", "cores": ac["pairs"], "kind": "oracle",
+            "sample": f"{ac['pairs']} (batch, KV head) pairs of {WL.WORKLOADS[2].name}, all {ac['blocks']} blocks, "
+                      f"one worker process per core (decode {ac['decode_s']} s wall, append {ac['append_s']} s)",
+            "append_tokens_per_s": ac["append_tokens_per_s"], "one_core": d["one_core"],
+            "per_config_one_core": d["per_config"], "host_cores": d["cores"], "cpu": d["cpu"]}
 
 
 def _cpu_model():
@@ -604,30 +705,38 @@ def _cpu_model():
 
 
 def run_reference(args):
+    """The oracle as it stands, as the reference arm: one spawned process per host core (BLAS on one
+    thread each), one (batch, KV head) pair of the workload each; a step is one decode of every
+    pair, all started together, over a bounded sample of the context."""
     rank, world, local = _dist()
     if rank != 0:
         return None
+    for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[k] = "1"
     w = WL.WORKLOADS[args.config]
-    heads = [(0, 0)]
-    # bound the whole run to a few minutes of CPU work: fewer blocks per step for long runs
-    n_sample = w.n_blocks if args.steps + args.warmup <= 25 else \
-        max(16, w.n_blocks * 25 // (args.steps + args.warmup))
-    ws = w.scaled(ctx=128 * min(w.n_blocks, n_sample))
-    per = []
-    for i in range(args.warmup + args.steps):
-        t_app, t_dec = _oracle_sample(ws, heads, seed=i % 2)
-        if i >= args.warmup:
-            per.append(t_dec)
-    nbytes = _decode_bytes_per_head(ws)
+    # bound the run to a few minutes of CPU work at ~4 ms of oracle decode per block and core
+    n_sample = min(w.n_blocks, max(16, int(120.0 / (0.004 * (args.steps + args.warmup)))))
+    pool = OraclePool(args.config, n_sample, min(_host_cores(), w.batch * w.n_kv_heads))
+    try:
+        for i in range(args.warmup):
+            pool.step(i)
+        per = [pool.step(args.warmup + i) for i in range(args.steps)]
+    finally:
+        pool.close()
+    npairs = len(pool.pairs)
+    nbytes = npairs * _pair_bytes(w, n_sample)
     ms = 1e3 * statistics.mean(per)
     v = nbytes / (ms * 1e-3) / 1e9
+    sample = (f"decode of {npairs} (batch, KV head) pairs over {n_sample} of {w.n_blocks} blocks per step, "
+              f"one process per pair and core")
     return {"impl": "reference", "metric": "quantized decode-attn packed-KV GB/s (% of 8 TB/s HBM), us/step; append tokens/s",
             "value": round(v, 4), "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f64 (oracle)", "data": "synthetic (numpy, seeded)",
-            "config": {"workload": w.name, "sample": f"1 (batch, KV head) pair, {ws.n_blocks} blocks, per step"},
-            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": f"decode of 1 (batch, KV head) pair over {ws.n_blocks} blocks per step"},
+            "config": {"workload": w.name, "sample": sample},
+            "append_tokens_per_s": round(npairs * n_sample * 128 / pool.append_s, 1),
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": npairs, "kind": "oracle",
+                             "sample": sample, "host_cores": _host_cores(), "cpu": _cpu_model()},
             "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
