@@ -27,6 +27,8 @@
 // registers ([KVQ] §3.7 fused matvec kernels; [TQ] §5.2 dequantisation inside attention).
 #include "kvq_internal.cuh"
 
+#include <type_traits>
+
 namespace kvq {
 namespace mmadec {
 
@@ -54,11 +56,22 @@ struct Args {
 // different heads.
 constexpr int FRAG_COL = 68, QROW = D + 8;
 
-struct WarpSmem {
+struct WarpSmemQ {
   float q[GQ][QROW];          // queries of the current (b, h) (Hadamard domain for KVarN)
   uint32_t frag[8 * FRAG_COL];  // B columns staged for the score product, then the value product
   uint64_t bar[4];
 };
+// Absmax keys carry no per-channel scale, so q is read only while the fixed score operand of a
+// (b, h) is built: q and the staging area share their memory.
+struct WarpSmemU {
+  union {
+    float q[GQ][QROW];
+    uint32_t frag[8 * FRAG_COL];
+  };
+  uint64_t bar[4];
+};
+template <int METHOD>
+using WarpSmem = typename std::conditional<METHOD == KVQ_INT4, WarpSmemU, WarpSmemQ>::type;
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
@@ -69,23 +82,25 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Operand register `qr` of a packed word: two codes (positions qr and qr + n/2 of the word)
-// as fp16 subnormals.
+// Signed codes enter offset-binary: one xor of the whole word flips the top bit of every code
+// (int4: +8 per nibble; int8: +128 per byte), before the operands are masked out of it.
 template <int BITS, bool BIAS8>
+__device__ __forceinline__ uint32_t bias_word(uint32_t w) {
+  return BIAS8 ? (w ^ (BITS == 8 ? 0x80808080u : 0x88888888u)) : w;
+}
+template <bool BIAS8>
+__device__ __forceinline__ uint4 bias_words4(uint4 v) {
+  return BIAS8 ? make_uint4(v.x ^ 0x88888888u, v.y ^ 0x88888888u, v.z ^ 0x88888888u, v.w ^ 0x88888888u) : v;
+}
+
+// Operand register `qr` of a packed word (signed codes already biased by bias_word): two codes
+// (positions qr and qr + n/2 of the word) as fp16 subnormals. One mask each.
+template <int BITS>
 __device__ __forceinline__ uint32_t operand(uint32_t w, int qr) {
-  if (BITS == 8) {  // bytes 0, 2 (qr 0) or 1, 3 (qr 1); two's complement -> offset binary
-    uint32_t v = (qr ? (w >> 8) : w) & 0x00ff00ffu;
-    if (BIAS8) v ^= 0x00800080u;
-    return v;
-  }
-  if (BITS == 2) {
+  if (BITS == 8) return (qr ? (w >> 8) : w) & 0x00ff00ffu;  // bytes 0, 2 (qr 0) or 1, 3 (qr 1)
+  if (BITS == 2)
     return qr <= 4 ? (w & (0x00030003u << (2 * qr))) : ((w >> 10) & (0x00030003u << (2 * (qr - 5))));
-  } else {
-    const uint32_t m = (qr & 1) ? 0x00f000f0u : 0x000f000fu;
-    uint32_t v = (qr < 2 ? w : (w >> 8)) & m;
-    if (BIAS8) v ^= (qr & 1) ? 0x00800080u : 0x00080008u;
-    return v;
-  }
+  return (qr < 2 ? w : (w >> 8)) & ((qr & 1) ? 0x00f000f0u : 0x000f000fu);
 }
 
 // hi/lo fp16 split of x: hi = fp16(x), lo = fp16(x - hi).
@@ -153,9 +168,10 @@ __device__ __forceinline__ void tile_mma(float (&acc)[8][4], const uint32_t* cod
       for (int ks = 0; ks < 8; ++ks) {
 #pragma unroll
         for (int m = 0; m < 2; ++m) {
-          const uint32_t x0 = (&w0[m][ks >> 2].x)[ks & 3], x1 = (&w1[m][ks >> 2].x)[ks & 3];
-          mma16816(acc[2 * hm + m], operand<8, BIAS8>(x0, 0), operand<8, BIAS8>(x1, 0), operand<8, BIAS8>(x0, 1),
-                   operand<8, BIAS8>(x1, 1), b[2 * ks], b[2 * ks + 1]);
+          const uint32_t x0 = bias_word<8, BIAS8>((&w0[m][ks >> 2].x)[ks & 3]);
+          const uint32_t x1 = bias_word<8, BIAS8>((&w1[m][ks >> 2].x)[ks & 3]);
+          mma16816(acc[2 * hm + m], operand<8>(x0, 0), operand<8>(x1, 0), operand<8>(x0, 1), operand<8>(x1, 1),
+                   b[2 * ks], b[2 * ks + 1]);
         }
       }
     }
@@ -174,8 +190,8 @@ __device__ __forceinline__ void tile_mma(float (&acc)[8][4], const uint32_t* cod
       for (int mt = 0; mt < 8; ++mt) {
         if (mt < MT0 || mt >= MT1) continue;
         const uint32_t x0 = ks < 4 ? w0[mt].x : w0[mt].y, x1 = ks < 4 ? w1[mt].x : w1[mt].y;
-        mma16816(acc[mt], operand<2, BIAS8>(x0, qr), operand<2, BIAS8>(x1, qr), operand<2, BIAS8>(x0, qr + 1),
-                 operand<2, BIAS8>(x1, qr + 1), b[2 * ks], b[2 * ks + 1]);
+        mma16816(acc[mt], operand<2>(x0, qr), operand<2>(x1, qr), operand<2>(x0, qr + 1), operand<2>(x1, qr + 1),
+                 b[2 * ks], b[2 * ks + 1]);
       }
     }
   } else {
@@ -186,8 +202,8 @@ __device__ __forceinline__ void tile_mma(float (&acc)[8][4], const uint32_t* cod
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int mt = 4 * hm + m;
-        w0[m] = *reinterpret_cast<const uint4*>(codes + (16 * mt + gq) * 16 + 4 * tq);
-        w1[m] = *reinterpret_cast<const uint4*>(codes + (16 * mt + gq + 8) * 16 + 4 * tq);
+        w0[m] = bias_words4<BIAS8>(*reinterpret_cast<const uint4*>(codes + (16 * mt + gq) * 16 + 4 * tq));
+        w1[m] = bias_words4<BIAS8>(*reinterpret_cast<const uint4*>(codes + (16 * mt + gq + 8) * 16 + 4 * tq));
       }
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
@@ -197,10 +213,52 @@ __device__ __forceinline__ void tile_mma(float (&acc)[8][4], const uint32_t* cod
           const uint32_t* p0 = &w0[m].x;
           const uint32_t* p1 = &w1[m].x;
           const uint32_t x0 = p0[ks >> 1], x1 = p1[ks >> 1];
-          mma16816(acc[4 * hm + m], operand<4, BIAS8>(x0, qr), operand<4, BIAS8>(x1, qr),
-                   operand<4, BIAS8>(x0, qr + 1), operand<4, BIAS8>(x1, qr + 1), b[2 * ks], b[2 * ks + 1]);
+          mma16816(acc[4 * hm + m], operand<4>(x0, qr), operand<4>(x1, qr), operand<4>(x0, qr + 1),
+                   operand<4>(x1, qr + 1), b[2 * ks], b[2 * ks + 1]);
         }
       }
+    }
+  }
+}
+
+// The lane's code words of a 128-row tile of 2- or 4-bit codes (rows 16mt+gq and 16mt+gq+8 of every
+// m-tile), held in registers so that the shared-memory buffer can be handed back before the
+// products run.
+template <int BITS>
+struct TileWords {
+  uint32_t w[8][BITS == 2 ? 4 : 8];
+};
+
+template <int BITS, bool BIAS8>
+__device__ __forceinline__ void load_tile(TileWords<BITS>& t, const uint32_t* codes, int gq, int tq) {
+#pragma unroll
+  for (int mt = 0; mt < 8; ++mt) {
+    if (BITS == 2) {
+      const uint2 a = *reinterpret_cast<const uint2*>(codes + (16 * mt + gq) * 8 + 2 * tq);
+      const uint2 b = *reinterpret_cast<const uint2*>(codes + (16 * mt + gq + 8) * 8 + 2 * tq);
+      t.w[mt][0] = a.x; t.w[mt][1] = a.y; t.w[mt][2] = b.x; t.w[mt][3] = b.y;
+    } else {
+      const uint4 a = bias_words4<BIAS8>(*reinterpret_cast<const uint4*>(codes + (16 * mt + gq) * 16 + 4 * tq));
+      const uint4 b = bias_words4<BIAS8>(*reinterpret_cast<const uint4*>(codes + (16 * mt + gq + 8) * 16 + 4 * tq));
+      t.w[mt][0] = a.x; t.w[mt][1] = a.y; t.w[mt][2] = a.z; t.w[mt][3] = a.w;
+      t.w[mt][4] = b.x; t.w[mt][5] = b.y; t.w[mt][6] = b.z; t.w[mt][7] = b.w;
+    }
+  }
+}
+
+// acc[mt] += the tile's m-tile mt . B for mt in [MT0, MT1), from the words in registers (biased by
+// load_tile; the same operands as tile_mma reads from shared memory).
+template <int BITS, int MT0 = 0, int MT1 = 8>
+__device__ __forceinline__ void words_mma(float (&acc)[8][4], const TileWords<BITS>& t, const uint32_t (&b)[16]) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+    for (int mt = MT0; mt < MT1; ++mt) {
+      const int qr = BITS == 2 ? 2 * (ks & 3) : 2 * (ks & 1);
+      const int wi = BITS == 2 ? (ks >> 2) : (ks >> 1);
+      const uint32_t x0 = t.w[mt][wi], x1 = t.w[mt][(BITS == 2 ? 2 : 4) + wi];
+      mma16816(acc[mt], operand<BITS>(x0, qr), operand<BITS>(x1, qr), operand<BITS>(x0, qr + 1),
+               operand<BITS>(x1, qr + 1), b[2 * ks], b[2 * ks + 1]);
     }
   }
 }
@@ -298,13 +356,24 @@ __device__ __forceinline__ void load_frag(const uint32_t* frag, int lane, int G,
 // G64 (absmax only): every token has two scales, one per 64 channels. Scores run the key tile
 // twice, against q restricted to each half, and the value product runs m-tiles 0-3 (channels
 // 0..63) and 4-7 against probabilities scaled by the matching half's scales.
+// 4-bit codes go to registers as soon as their buffer lands, and the buffer is handed back at once,
+// so every buffer of the warp but the one being read stays in flight while it computes (8-bit
+// tiles, and 4-bit tiles with two scale sets, are too large to hold; 2-bit tiles measured no
+// faster this way and are read from shared memory).
+template <int BITS, bool G64>
+constexpr bool early_release() { return BITS == 4 && !G64; }
+// CTAs per SM the register budget must allow (the shared-memory ring allows as many).
+template <int BITS, int GT, bool G64>
+constexpr int min_ctas() { return !early_release<BITS, G64>() ? 1 : (BITS == 2 && GT == 1) ? 3 : 2; }
+
 template <int METHOD, int BITS, int GT, int NW, int NB, bool WHOLE, bool G64>
-__global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
+__global__ void __launch_bounds__(NW * 32, (min_ctas<BITS, GT, G64>())) decode_mma_kernel(Args a) {
   launch_dependents();  // the combine kernel may be scheduled once every CTA of this grid runs
   constexpr bool BIAS8 = METHOD == KVQ_INT4;          // signed codes enter biased by 8 (or 128)
   constexpr float BIASF = BITS == 8 ? 128.0f : 8.0f;
   constexpr int RP = 4 / GT;
   constexpr int NMT = 8 / RP;  // m-tiles (16 rows) a lane finishes
+  constexpr bool EARLY = early_release<BITS, G64>();
   extern __shared__ __align__(128) uint8_t smem_raw[];
   const Geo& g = a.g;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -317,7 +386,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
   const int halfv = (int)g.rec_bytes - halfk;          // V half
   const int hb = WHOLE ? (int)g.rec_bytes : (halfk > halfv ? halfk : halfv);  // bytes per buffer
   uint8_t* ring = smem_raw + (size_t)warp * NB * hb;
-  WarpSmem* sw = reinterpret_cast<WarpSmem*>(smem_raw + (size_t)NW * NB * hb) + warp;
+  WarpSmem<METHOD>* sw = reinterpret_cast<WarpSmem<METHOD>*>(smem_raw + (size_t)NW * NB * hb) + warp;
 
   const long long R = (long long)blockIdx.x * NW + warp;
   if (R >= a.n_ranges) return;  // the last CTA may carry warps beyond the range count
@@ -461,6 +530,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
         sumq = head_sum<GT>(sq);
         if (G64) sumq1 = head_sum<GT>(sq1);
         g0_fixed = range_exp(mx);
+        __syncwarp();  // every lane has read its q values: the staging area may be overwritten
         const float sc = exp2i(g0_fixed) * inv_f;
 #pragma unroll
         for (int k = 0; k < 2 * NMT; ++k) {
@@ -489,6 +559,17 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(kbuf + g.codes_off[0]);
     const uint16_t* km = reinterpret_cast<const uint16_t*>(kbuf + g.meta_off[0]);
 
+    // ---- per-token key metadata of the lane's tokens (int4: scales; KVarN: the token scale)
+    float ktok[2 * NMT], ktok1[2 * NMT];
+#pragma unroll
+    for (int j = 0; j < NMT; ++j)
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        const int tok = 16 * (rho + RP * j) + gq + 8 * hf;
+        ktok[2 * j + hf] = METHOD == KVQ_INT4 ? h2f(km[tok]) : METHOD == KVQ_VARN ? h2f(km[2 * T + tok]) : 0.0f;
+        ktok1[2 * j + hf] = G64 ? h2f(km[T + tok]) : 0.0f;
+      }
+
     // ---- B fragments of the score product: q * s_channel (RTN, KVarN)
     int g0 = g0_fixed;
     if (METHOD != KVQ_INT4) {
@@ -516,16 +597,55 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
       load_frag(sw->frag, lane, G, bk);
     }
 
+    // ---- the V half's metadata and codes (value scale and zero point of the lane's tokens;
+    // KVarN: s1 of the lane's channel rows), read as soon as the half is in shared memory
+    const uint8_t* vbuf = kbuf + halfk;
+    float vtok[2 * NMT], vtok1[2 * NMT], s1r[16];
+    TileWords<EARLY ? BITS : 2> kw, vw;
+    auto read_v = [&]() {
+      const uint16_t* vm = reinterpret_cast<const uint16_t*>(vbuf + (g.meta_off[1] - g.codes_off[1]));
+#pragma unroll
+      for (int j = 0; j < NMT; ++j)
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          const int tok = 16 * (rho + RP * j) + gq + 8 * hf;
+          vtok[2 * j + hf] = h2f(vm[tok]);
+          vtok1[2 * j + hf] = METHOD == KVQ_INT4 && !G64 ? 0.0f : h2f(vm[T + tok]);
+        }
+      if (METHOD == KVQ_VARN) {
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+          s1r[2 * mt] = h2f(vm[2 * T + 16 * mt + gq]);
+          s1r[2 * mt + 1] = h2f(vm[2 * T + 16 * mt + gq + 8]);
+        }
+      }
+      if (EARLY) load_tile<EARLY ? BITS : 2, BIAS8>(vw, reinterpret_cast<const uint32_t*>(vbuf), gq, tq);
+    };
+    if (EARLY) {  // take the K half (or the whole record) into registers and hand the buffer back
+      load_tile<EARLY ? BITS : 2, BIAS8>(kw, kc, gq, tq);
+      if (WHOLE) read_v();
+      __syncwarp();
+      if (lane == 0) {
+        fence_proxy_async();
+        issue_next();
+      }
+    }
+
     // ---- scores: S = K . Bq  (8 m-tiles of 16 tokens x 8 k-steps of 16 channels)
     float sc8[8][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt) sc8[mt][0] = sc8[mt][1] = sc8[mt][2] = sc8[mt][3] = 0.0f;
-    tile_mma<BITS, BIAS8>(sc8, kc, gq, tq, bk);
     float sc8b[8][4];  // G64: the scores of channels 64..127
     if (G64) {
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) sc8b[mt][0] = sc8b[mt][1] = sc8b[mt][2] = sc8b[mt][3] = 0.0f;
-      tile_mma<BITS, BIAS8>(sc8b, kc, gq, tq, bk1);
+    }
+    if constexpr (EARLY) {
+      words_mma<BITS>(sc8, kw, bk);
+      if (G64) words_mma<BITS>(sc8b, kw, bk1);
+    } else {
+      tile_mma<BITS, BIAS8>(sc8, kc, gq, tq, bk);
+      if (G64) tile_mma<BITS, BIAS8>(sc8b, kc, gq, tq, bk1);
     }
 
     // ---- finish the scores of the lane's tokens, online softmax (base 2)
@@ -534,41 +654,48 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
     float mloc = -INFINITY;
 #pragma unroll
     for (int j = 0; j < NMT; ++j) {
-      const int mt = rho + RP * j;
       float c4[4], d4[4];
       pick_tile<RP>(sc8, j, rho, c4);
       if (G64) pick_tile<RP>(sc8b, j, rho, d4);
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int tok = 16 * mt + gq + 8 * hf;
         float v = (c4[2 * hf] + c4[2 * hf + 1]) * ksc;
         if (METHOD == KVQ_INT4) {
-          v = (v - BIASF * sumq) * h2f(km[tok]);
-          if (G64) v += ((d4[2 * hf] + d4[2 * hf + 1]) * ksc - BIASF * sumq1) * h2f(km[T + tok]);
+          v = (v - BIASF * sumq) * ktok[2 * j + hf];
+          if (G64) v += ((d4[2 * hf] + d4[2 * hf + 1]) * ksc - BIASF * sumq1) * ktok1[2 * j + hf];
         } else {
           v += zk;
         }
-        if (METHOD == KVQ_VARN) v *= h2f(km[2 * T + tok]);
+        if (METHOD == KVQ_VARN) v *= ktok[2 * j + hf];
         v *= LOG2E_RSQRT_D;
         sv[2 * j + hf] = v;
         mloc = fmaxf(mloc, v);
       }
     }
-    const uint8_t* vbuf = kbuf + halfk;
-    if (!WHOLE) {  // the K half is consumed: refill its buffer, then wait for the V half
-      __syncwarp();
-      if (lane == 0) {
-        fence_proxy_async();
-        issue_next();
+    if (!WHOLE) {  // the K half is consumed: refill its buffer (unless done above), then wait for the V half
+      if (!EARLY) {
+        __syncwarp();
+        if (lane == 0) {
+          fence_proxy_async();
+          issue_next();
+        }
       }
       if (__any_sync(0xffffffffu, !wait_next(vbuf))) {
         ok = false;
         failed_at = 2 * i + 1;
         break;
       }
+      read_v();
+      if (EARLY) {
+        __syncwarp();
+        if (lane == 0) {
+          fence_proxy_async();
+          issue_next();
+        }
+      }
+    } else if (!EARLY) {
+      read_v();
     }
-    const uint32_t* vc = reinterpret_cast<const uint32_t*>(vbuf);
-    const uint16_t* vm = reinterpret_cast<const uint16_t*>(vbuf + (g.meta_off[1] - g.codes_off[1]));
 
     mloc = head_max<GT>(mloc);
     const float m_new = fmaxf(m_run, mloc);
@@ -577,19 +704,17 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
     float sv1[2 * NMT];  // G64: probabilities times the scales of channels 64..127
 #pragma unroll
     for (int j = 0; j < NMT; ++j) {
-      const int mt = rho + RP * j;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        const int tok = 16 * mt + gq + 8 * hf;
         const float p = exp2f(sv[2 * j + hf] - m_new);
         lsum += p;
-        const float pp = p * h2f(vm[tok]);  // per-token value scale folded into p
+        const float pp = p * vtok[2 * j + hf];  // per-token value scale folded into p
         sv[2 * j + hf] = pp;
         if (METHOD == KVQ_INT4) zsum_blk -= BIASF * pp;
-        else zsum_blk = fmaf(pp, h2f(vm[T + tok]), zsum_blk);
+        else zsum_blk = fmaf(pp, vtok1[2 * j + hf], zsum_blk);
         pmax = fmaxf(pmax, pp);
         if (G64) {
-          const float pp1 = p * h2f(vm[T + tok]);
+          const float pp1 = p * vtok1[2 * j + hf];
           sv1[2 * j + hf] = pp1;
           zsum1 -= BIASF * pp1;
           pmax = fmaxf(pmax, pp1);
@@ -623,6 +748,7 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
     }
 
     // ---- outputs: O = V . Bp  (8 m-tiles of 16 channels x 8 k-steps of 16 tokens)
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(vbuf);
     if (METHOD != KVQ_VARN) {
       const float rs = alpha * exp2i(g1 - g1_cur);
 #pragma unroll
@@ -631,23 +757,33 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
       }
       zv = zv * alpha + zsum_blk;
       g1_cur = g1;
-      if (G64) {
-        zv1 = zv1 * alpha + zsum1;
-        tile_mma<BITS, BIAS8, 0, 4>(O, vc, gq, tq, bv);
-        tile_mma<BITS, BIAS8, 4, 8>(O, vc, gq, tq, bv1);
+      if constexpr (EARLY) {
+        if (G64) {
+          zv1 = zv1 * alpha + zsum1;
+          words_mma<BITS, 0, 4>(O, vw, bv);
+          words_mma<BITS, 4, 8>(O, vw, bv1);
+        } else {
+          words_mma<BITS>(O, vw, bv);
+        }
       } else {
-        tile_mma<BITS, BIAS8>(O, vc, gq, tq, bv);
+        if (G64) {
+          zv1 = zv1 * alpha + zsum1;
+          tile_mma<BITS, BIAS8, 0, 4>(O, vc, gq, tq, bv);
+          tile_mma<BITS, BIAS8, 4, 8>(O, vc, gq, tq, bv1);
+        } else {
+          tile_mma<BITS, BIAS8>(O, vc, gq, tq, bv);
+        }
       }
     } else {  // second scale s1 per channel: o_c += s1_c * (P.V_c + sum p' z)
       float acc[8][4];
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.0f;
-      tile_mma<BITS, BIAS8>(acc, vc, gq, tq, bv);
+      if constexpr (EARLY) words_mma<BITS>(acc, vw, bv);
+      else tile_mma<BITS, BIAS8>(acc, vc, gq, tq, bv);
       const float usc = exp2i(24 - g1);
 #pragma unroll
       for (int mt = 0; mt < 8; ++mt) {
-        const int r0 = 16 * mt + gq, r1 = r0 + 8;
-        const float s1a = h2f(vm[2 * T + r0]), s1b = h2f(vm[2 * T + r1]);
+        const float s1a = s1r[2 * mt], s1b = s1r[2 * mt + 1];
         O[mt][0] = O[mt][0] * alpha + (acc[mt][0] * usc + zsum_blk) * s1a;
         O[mt][1] = O[mt][1] * alpha + acc[mt][1] * usc * s1a;
         O[mt][2] = O[mt][2] * alpha + (acc[mt][2] * usc + zsum_blk) * s1b;
@@ -655,10 +791,12 @@ __global__ void __launch_bounds__(NW * 32, 1) decode_mma_kernel(Args a) {
       }
     }
 
-    __syncwarp();  // every lane is done with the record / V half: refill its buffer
-    if (lane == 0) {
-      fence_proxy_async();
-      issue_next();
+    if (!EARLY) {
+      __syncwarp();  // every lane is done with the record / V half: refill its buffer
+      if (lane == 0) {
+        fence_proxy_async();
+        issue_next();
+      }
     }
     if (++blk == a.nb) { blk = 0; ++u; }
   }
@@ -695,10 +833,16 @@ struct Plan {
 #define KVQ_MMA2_WHOLE_G1 0
 #endif
 #ifndef KVQ_MMA4_NW
-#define KVQ_MMA4_NW 5
+#define KVQ_MMA4_NW 4  // 2 CTAs per SM: 2 warps per scheduler, registers for a whole tile of words
+#endif
+#ifndef KVQ_MMA4G64_NW
+#define KVQ_MMA4G64_NW 5
 #endif
 #ifndef KVQ_MMA4_NB
 #define KVQ_MMA4_NB 2
+#endif
+#ifndef KVQ_MMA4_INT4_NB
+#define KVQ_MMA4_INT4_NB 2  // 3 fit beside the smaller warp state; measured the same (208 vs 211 us)
 #endif
 #ifndef KVQ_MMA4_WHOLE
 #define KVQ_MMA4_WHOLE 0
@@ -713,8 +857,10 @@ struct Plan {
 
 template <int METHOD, int BITS, int GT, bool G64>
 Plan plan_for() {
-  constexpr int NW = BITS == 2 ? KVQ_MMA2_NW : BITS == 4 ? KVQ_MMA4_NW : KVQ_MMA8_NW;
-  constexpr int NB = BITS == 2 ? KVQ_MMA2_NB : BITS == 4 ? KVQ_MMA4_NB : KVQ_MMA8_NB;
+  constexpr int NW = BITS == 2 ? KVQ_MMA2_NW : BITS == 4 ? (G64 ? KVQ_MMA4G64_NW : KVQ_MMA4_NW) : KVQ_MMA8_NW;
+  constexpr int NB = BITS == 2 ? KVQ_MMA2_NB
+                     : BITS == 4 ? ((METHOD == KVQ_INT4 && !G64) ? KVQ_MMA4_INT4_NB : KVQ_MMA4_NB)
+                                 : KVQ_MMA8_NB;
   // one query head (GT 1, four replicas of its columns): a long stream of light records runs
   // best from K/V half buffers; several heads per record: whole records
   constexpr bool WH = BITS == 2 ? (GT == 1 ? KVQ_MMA2_WHOLE_G1 : KVQ_MMA2_WHOLE) : BITS == 4 ? KVQ_MMA4_WHOLE : false;
@@ -745,7 +891,8 @@ Plan get_plan(const Geo& g) {
 size_t smem_bytes(const Geo& g, const Plan& p) {
   const uint64_t hk = g.codes_off[1], hv = g.rec_bytes - hk;
   const uint64_t hb = p.whole ? g.rec_bytes : (hk > hv ? hk : hv);
-  return (size_t)p.nw * p.ns * hb + (size_t)p.nw * sizeof(WarpSmem);
+  const size_t ws = g.method == KVQ_INT4 ? sizeof(WarpSmemU) : sizeof(WarpSmemQ);
+  return (size_t)p.nw * p.ns * hb + (size_t)p.nw * ws;
 }
 
 }  // namespace mmadec
