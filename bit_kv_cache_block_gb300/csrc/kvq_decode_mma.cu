@@ -363,8 +363,13 @@ __device__ __forceinline__ void load_frag(const uint32_t* frag, int lane, int G,
 template <int BITS, bool G64>
 constexpr bool early_release() { return BITS == 4 && !G64; }
 // CTAs per SM the register budget must allow (the shared-memory ring allows as many).
+#ifndef KVQ_MMA2_G1_MINB
+#define KVQ_MMA2_G1_MINB 1
+#endif
 template <int BITS, int GT, bool G64>
-constexpr int min_ctas() { return !early_release<BITS, G64>() ? 1 : (BITS == 2 && GT == 1) ? 3 : 2; }
+constexpr int min_ctas() {
+  return early_release<BITS, G64>() ? 2 : (BITS == 2 && GT == 1) ? KVQ_MMA2_G1_MINB : 1;
+}
 
 template <int METHOD, int BITS, int GT, int NW, int NB, bool WHOLE, bool G64>
 __global__ void __launch_bounds__(NW * 32, (min_ctas<BITS, GT, G64>())) decode_mma_kernel(Args a) {
@@ -816,6 +821,7 @@ struct Plan {
   void (*fn)(Args);
   int nw, ns;  // warps per CTA, buffers per warp
   bool whole;  // buffers hold whole records (else K and V halves)
+  int ws;      // bytes of per-warp state after the rings
 };
 
 // Warps per CTA and half-record buffers per warp (compile-time tuning; the defaults are the
@@ -825,6 +831,9 @@ struct Plan {
 #endif
 #ifndef KVQ_MMA2_NB
 #define KVQ_MMA2_NB 2
+#endif
+#ifndef KVQ_MMA2_G1_NW
+#define KVQ_MMA2_G1_NW KVQ_MMA2_NW
 #endif
 #ifndef KVQ_MMA2_WHOLE
 #define KVQ_MMA2_WHOLE 1
@@ -857,14 +866,16 @@ struct Plan {
 
 template <int METHOD, int BITS, int GT, bool G64>
 Plan plan_for() {
-  constexpr int NW = BITS == 2 ? KVQ_MMA2_NW : BITS == 4 ? (G64 ? KVQ_MMA4G64_NW : KVQ_MMA4_NW) : KVQ_MMA8_NW;
+  constexpr int NW = BITS == 2 ? (GT == 1 ? KVQ_MMA2_G1_NW : KVQ_MMA2_NW)
+                     : BITS == 4 ? (G64 ? KVQ_MMA4G64_NW : KVQ_MMA4_NW) : KVQ_MMA8_NW;
   constexpr int NB = BITS == 2 ? KVQ_MMA2_NB
                      : BITS == 4 ? ((METHOD == KVQ_INT4 && !G64) ? KVQ_MMA4_INT4_NB : KVQ_MMA4_NB)
                                  : KVQ_MMA8_NB;
   // one query head (GT 1, four replicas of its columns): a long stream of light records runs
   // best from K/V half buffers; several heads per record: whole records
   constexpr bool WH = BITS == 2 ? (GT == 1 ? KVQ_MMA2_WHOLE_G1 : KVQ_MMA2_WHOLE) : BITS == 4 ? KVQ_MMA4_WHOLE : false;
-  return Plan{decode_mma_kernel<METHOD, BITS, GT, NW, NB, WH, G64>, NW, NB, WH};
+  constexpr int WS = METHOD == KVQ_INT4 ? (int)sizeof(WarpSmemU) : (int)sizeof(WarpSmemQ);
+  return Plan{decode_mma_kernel<METHOD, BITS, GT, NW, NB, WH, G64>, NW, NB, WH, WS};
 }
 
 template <int METHOD, int BITS, bool G64 = false>
@@ -891,8 +902,7 @@ Plan get_plan(const Geo& g) {
 size_t smem_bytes(const Geo& g, const Plan& p) {
   const uint64_t hk = g.codes_off[1], hv = g.rec_bytes - hk;
   const uint64_t hb = p.whole ? g.rec_bytes : (hk > hv ? hk : hv);
-  const size_t ws = g.method == KVQ_INT4 ? sizeof(WarpSmemU) : sizeof(WarpSmemQ);
-  return (size_t)p.nw * p.ns * hb + (size_t)p.nw * ws;
+  return (size_t)p.nw * p.ns * hb + (size_t)p.nw * p.ws;
 }
 
 }  // namespace mmadec

@@ -161,6 +161,14 @@ DECODE_CASES = [
     ("nuq3_norope_gqa", WL.WORKLOADS[2], dict(pre_rope=False, batch=2, n_kv_heads=2, n_q_heads=4, ctx=3 * 128), [9]),
     ("varn2_gqa", WL.WORKLOADS[3], dict(batch=2, n_kv_heads=2, n_q_heads=8, ctx=4 * 128), [0, 100]),
     ("varn2_g16", WL.WORKLOADS[3], dict(batch=1, n_kv_heads=1, n_q_heads=16, ctx=2 * 128), [1]),
+    # one and two query heads per KV head with 2-bit codes: the e4m3 tensor-core kernel (K/V halves
+    # for one head, whole records for two); heavy-tailed keys with outlier channels stress the
+    # per-channel scale range its operand splits must carry
+    ("varn2_mha", WL.WORKLOADS[3], dict(batch=1, n_kv_heads=3, n_q_heads=3, ctx=4 * 128), [0, 33]),
+    ("varn2_g2", WL.WORKLOADS[3], dict(batch=2, n_kv_heads=2, n_q_heads=4, ctx=3 * 128), [5]),
+    ("rtn2_g2", WL.WORKLOADS[5], dict(batch=2, n_kv_heads=3, n_q_heads=6, ctx=5 * 128), [0, 17]),
+    ("rtn2_mha_heavy_keys", WL.WORKLOADS[3], dict(method="rtn", batch=1, n_kv_heads=2, n_q_heads=2, ctx=6 * 128),
+     [0, 9]),
     ("int8_bf16", WL.WORKLOADS[4], dict(bits=8, batch=2, n_kv_heads=2, n_q_heads=8, ctx=5 * 128), [0, 64]),
     ("int8_g64_f16", WL.WORKLOADS[4], dict(bits=8, scale_group=64, dtype="f16", batch=1, n_kv_heads=3, n_q_heads=3,
                                            ctx=4 * 128), [127]),
