@@ -49,7 +49,8 @@ struct CombineArgs {
   long long tail_bh;    // elements between the tail rows of consecutive (b, h)
   long long tail_tok;   // elements between consecutive tokens of a tail row
   int n_blocks;
-  int n_split;          // partial rows per (b, query head)
+  int n_split;          // partial rows per (b, query head) in the workspace
+  int tail_ws;          // 1: the decode kernel attended the fp tail into the last of those rows
   long long ranges;     // > 0: partials come from the range-split tensor-core decode
   int per_range;        // partial rows per range and (b, query head)
   long long total;      // B * H * n_blocks
@@ -445,7 +446,7 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
     Lt = 1.0f;
     Ot = in_bits_to_f32(ks[D + c], g.in_bf16);
   }
-  if (a.n_tail > 0) {  // the fp residual tail (< 128 tokens)
+  if (a.n_tail > 0 && !a.tail_ws) {  // the fp residual tail (< 128 tokens)
     const int nt = a.n_tail;
     const uint16_t* tk = a.tail_k + ((uint64_t)b * g.H + h) * a.tail_bh;
     const uint16_t* tv = a.tail_v + ((uint64_t)b * g.H + h) * a.tail_bh;
@@ -539,13 +540,23 @@ __global__ void __launch_bounds__(CB_THREADS) combine_kernel(CombineArgs a) {
     return;
   }
   const uint64_t row0 = ((uint64_t)b * g.Hq + hq) * a.n_split;
+  const int range_rows = a.n_split - (a.ranges > 0 && a.tail_ws ? 1 : 0);
   int n_part = a.n_split;
   if (a.ranges > 0) {  // the ranges that hold blocks of this (b, h)
     const long long u = (long long)b * g.H + h;
     const long long r0 = ((u * a.n_blocks + 1) * a.ranges - 1) / a.total;
     const long long r1 = (((u + 1) * a.n_blocks) * a.ranges - 1) / a.total;
     n_part = (int)(r1 - r0 + 1) * a.per_range;
-    if (n_part > a.n_split) n_part = a.n_split;
+    if (n_part > range_rows) n_part = range_rows;
+  }
+  if (a.tail_ws) {  // the tail's softmax state, attended by the decode kernel, joins the sink's
+    const uint64_t tr = row0 + (uint64_t)(a.n_split - 1);
+    const float m2 = a.ws_m[tr], l2 = a.ws_l[tr], o2 = a.ws_o[tr * D + c];
+    const float Mn = fmaxf(Mt, m2);
+    const float f1 = exp2f(Mt - Mn), f2 = exp2f(m2 - Mn);
+    Lt = Lt * f1 + l2 * f2;
+    Ot = Ot * f1 + o2 * f2;
+    Mt = Mn;
   }
 
   // ---- merge the partials in one pass: group grp takes partials grp, grp+4, ..., eight of them
@@ -655,8 +666,10 @@ long long kvq_mma_ranges(const kvq::Geo& g);
 long long kvq_nuq_ranges(const kvq::Geo& g);
 int kvq_nuq_parts_per_range();
 cudaError_t kvq_launch_decode_nuq(const kvq::Geo& g, const uint8_t* base, const float* codebook, const uint16_t* q,
-                                  int n_blocks, long long ranges, long long slots, float* ws_m, float* ws_l,
-                                  float* ws_o, int* status, cudaStream_t st);
+                                  int n_blocks, long long ranges, long long slots, long long rows_ph, float* ws_m,
+                                  float* ws_l, float* ws_o, int* status, const uint16_t* tail_k,
+                                  const uint16_t* tail_v, int n_tail, long long tail_bh, long long tail_tok,
+                                  cudaStream_t st);
 long long kvq_mma_slots(const kvq::Geo& g, int n_blocks, long long ranges);
 cudaError_t kvq_launch_decode_mma(const kvq::Geo& g, const uint8_t* base, const uint16_t* q, int n_blocks,
                                   long long ranges, long long slots, float* ws_m, float* ws_l, float* ws_o,
@@ -670,13 +683,14 @@ struct DecodePlan {
   long long ranges;  // > 0: tensor-core decode over this many ranges (warps, or CTAs for nuq)
   long long rows;    // partial rows per (b, query head)
   bool nuq;          // the 3-bit nuq pre-RoPE decode
-  long long slots;   // range slots per (b, query head) (rows = slots * per_range)
+  long long slots;   // range slots per (b, query head) (rows = slots * per_range [+ 1])
   int per_range;     // partial rows one range writes per (b, query head)
+  bool tail_row;     // the last row of each (b, query head) holds the tail (the nuq decode's idle warps)
 };
 
 DecodePlan plan_decode(const kvq::Geo& g, int n_blocks, int v1_splits) {
-  DecodePlan p{0, v1_splits, false, v1_splits, 1};
-  if (n_blocks <= 0) return DecodePlan{0, 0, false, 0, 1};
+  DecodePlan p{0, v1_splits, false, v1_splits, 1, false};
+  if (n_blocks <= 0) return DecodePlan{0, 0, false, 0, 1, false};
   long long ranges = kvq_nuq_ranges(g);
   p.nuq = ranges > 0;
   if (!p.nuq) ranges = kvq_mma_ranges(g);
@@ -686,7 +700,8 @@ DecodePlan plan_decode(const kvq::Geo& g, int n_blocks, int v1_splits) {
     p.ranges = ranges;
     p.slots = kvq_mma_slots(g, n_blocks, ranges);
     p.per_range = p.nuq ? kvq_nuq_parts_per_range() : 1;
-    p.rows = p.slots * p.per_range;
+    p.tail_row = p.nuq;
+    p.rows = p.slots * p.per_range + (p.tail_row ? 1 : 0);
   }
   return p;
 }
@@ -705,8 +720,8 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
   if (n_blocks > 0) {
     cudaError_t e;
     if (plan.ranges > 0 && plan.nuq) {
-      e = kvq_launch_decode_nuq(g, base, codebook, q, n_blocks, plan.ranges, plan.slots, ws_m, ws_l, ws_o, status,
-                                st);
+      e = kvq_launch_decode_nuq(g, base, codebook, q, n_blocks, plan.ranges, plan.slots, plan.rows, ws_m, ws_l, ws_o,
+                                status, tail_k, tail_v, n_tail, tail_bh, tail_tok, st);
     } else if (plan.ranges > 0) {
       e = kvq_launch_decode_mma(g, base, q, n_blocks, plan.ranges, plan.slots, ws_m, ws_l, ws_o, status, hadamard,
                                 st);
@@ -728,6 +743,7 @@ cudaError_t kvq_launch_decode(const kvq::Geo& g, const uint8_t* base, const floa
   c.tail_bh = tail_bh;
   c.tail_tok = tail_tok;
   c.n_blocks = n_blocks; c.n_split = (int)plan.rows; c.ranges = plan.ranges; c.per_range = plan.per_range;
+  c.tail_ws = (plan.tail_row && n_tail > 0) ? 1 : 0;
   c.total = (long long)g.B * g.H * n_blocks;
   c.ws_m = ws_m; c.ws_l = ws_l; c.ws_o = ws_o; c.out = out; c.hadamard = hadamard; c.status = status;
   cudaLaunchConfig_t lc = {};

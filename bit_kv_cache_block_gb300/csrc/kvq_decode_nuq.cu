@@ -68,10 +68,16 @@ struct Args {
   long long total;        // B * H * nb
   int n_ranges;           // CTAs in the grid
   int n_slots;            // range slots per (b, query head)
+  int rows_ph;            // partial rows per (b, query head): n_slots * NW range rows, then the tail row
   float* ws_m;
   float* ws_l;
   float* ws_o;
   int* status;
+  const uint16_t* tail_k;  // fp tail (the call's inputs), attended by the idle warps
+  const uint16_t* tail_v;
+  int n_tail;
+  long long tail_bh;       // elements between the tail rows of consecutive (b, h)
+  long long tail_tok;      // elements between consecutive tokens of a tail row
 };
 
 // Per-stage operands the aux warps prepare for the consumer warps.
@@ -194,6 +200,16 @@ __device__ __forceinline__ void regs_dec() {
   asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(R) : "memory");
 }
 
+#ifndef KVQ_NUQ_HELPER_SUSPEND
+#define KVQ_NUQ_HELPER_SUSPEND 1  // measured 89.7 vs 91.1 us per decode, 1.6% fewer instructions
+#endif
+// Waits of the warps that run ahead of the consumers (producer, aux): a sleeping probe loop, or
+// (KVQ_NUQ_HELPER_SUSPEND) the barrier's own suspending wait. Both bounded.
+__device__ __forceinline__ bool helper_wait(uint64_t* bar, uint32_t parity, int* status, long long max_cycles) {
+  if (KVQ_NUQ_HELPER_SUSPEND) return mbar_wait_bounded(bar, parity, status, max_cycles);
+  return mbar_wait_backoff(bar, parity, status, max_cycles);
+}
+
 // Producer warp: copies block p of the range into stage p % NBS once the consumer warps have
 // released the stage's previous block (NW arrivals on empty). A block's two copies (K half; V
 // half with the CSR) go out as one instruction from two lanes, and the lane pair rotates over
@@ -213,7 +229,7 @@ __device__ void producer(const Args& a, Smem* sm, uint8_t* ring, long long x0, i
   for (int p = 0; p < n; ++p) {
     const int s = p % NBS;
     if (p >= NBS) {
-      const bool got = mbar_wait_backoff(&sm->empty[s], (uint32_t)(((p / NBS) - 1) & 1), a.status, g.wait_cycles);
+      const bool got = helper_wait(&sm->empty[s], (uint32_t)(((p / NBS) - 1) & 1), a.status, g.wait_cycles);
       if (__any_sync(0xffffffffu, !got)) break;
     }
     const int set = 2 * (p & 15), part = lane - set;  // lanes set, set+1 copy this block
@@ -285,7 +301,7 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
       while (nb2 >= a.nb) nb2 -= a.nb;
       if (p + 2 < n) cs_next = __ldg(rope_blk + (size_t)nb2 * 64 + j);
     }
-    const bool got = mbar_wait_backoff(&sm->rec_full[s], (uint32_t)((p / NBS) & 1), a.status, g.wait_cycles);
+    const bool got = helper_wait(&sm->rec_full[s], (uint32_t)((p / NBS) & 1), a.status, g.wait_cycles);
     if (bar_or_group(grp, !got)) break;  // the consumers time out on their own waits
     const uint8_t* st = ring + (size_t)s * sb;
     Ops& op = sm->op[s];
@@ -756,7 +772,7 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
       const long long b = u / g.H, h = u - b * g.H;
       const long long slot = R - range_of(u * a.nb, a.total, a.n_ranges);
       if (slot >= 0 && slot < a.n_slots) {
-        const uint64_t row = (((uint64_t)(b * g.Hq + h)) * a.n_slots + slot) * NW + warp;
+        const uint64_t row = ((uint64_t)(b * g.Hq + h)) * a.rows_ph + (uint64_t)slot * NW + warp;
         if (tq == 0) {
 #pragma unroll
           for (int mt = 0; mt < 8; ++mt) {
@@ -775,6 +791,110 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
     i = iend;
     blk = 0;
     ++u;
+  }
+}
+
+// The idle warps (IDLE of them per CTA): attention over the fp tail, the n_tail < 128 tokens past the
+// cached blocks (positions n0 + t, n0 = nb * 128), one warp per (b, query head), written as the
+// last partial row (m, l, o) of that head for the combine to merge with the cached part. The keys
+// are stored before RoPE like the cache's: the score is (R(n0)^T q) . (R(t) k_t), the in-block
+// angles from the cache's table. Lane l holds channel pairs l and l + 32. It reads only the call's
+// inputs and the angle tables, so it runs beside the ring without waiting on it.
+constexpr int IDLE = NTHREADS / 32 - PRODUCER_WARP - 1;
+constexpr int TCH = 6;  // tail tokens per chunk (the idle warps run with 88 registers)
+__device__ void tail_warp(const Args& a, int wi, int lane) {
+  const Geo& g = a.g;
+  const int nt = a.n_tail;
+  if (nt <= 0) return;
+  const int n_heads = g.B * g.Hq;
+  const float2* rope_blk = reinterpret_cast<const float2*>(a.base + g.rope_off);
+  const float2* rope_loc = rope_blk + (size_t)(g.max_blocks + 1) * 64;
+  for (int hidx = (int)blockIdx.x * IDLE + wi; hidx < n_heads; hidx += a.n_ranges * IDLE) {
+    const int b = hidx / g.Hq, h = hidx - b * g.Hq;  // one query head per KV head
+    const uint16_t* qp = a.q + (uint64_t)hidx * D;
+    float q0[2][2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int pr = lane + 32 * k;
+      const float x0 = load_in(qp + 2 * pr, g.in_bf16), x1 = load_in(qp + 2 * pr + 1, g.in_bf16);
+      const float2 cs = __ldg(rope_blk + (size_t)a.nb * 64 + pr);
+      q0[k][0] = cs.x * x0 + cs.y * x1;
+      q0[k][1] = -cs.y * x0 + cs.x * x1;
+    }
+    const uint16_t* tk = a.tail_k + ((uint64_t)b * g.H + h) * a.tail_bh;
+    const uint16_t* tv = a.tail_v + ((uint64_t)b * g.H + h) * a.tail_bh;
+    float m = -INFINITY, l = 0.0f, o[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    // TCH tokens at a time, every load of a chunk issued before any is used (tokens past the
+    // tail read the last one again and get probability 0)
+    for (int t0 = 0; t0 < nt; t0 += TCH) {
+      uint32_t kw[TCH][2];
+      float2 cs[TCH][2];
+#pragma unroll
+      for (int i = 0; i < TCH; ++i) {
+        const int t = min(t0 + i, nt - 1);
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int pr = lane + 32 * k;
+          kw[i][k] = __ldg(reinterpret_cast<const unsigned int*>(tk + (uint64_t)t * a.tail_tok + 2 * pr));
+          cs[i][k] = __ldg(rope_loc + (size_t)t * 64 + pr);
+        }
+      }
+      float sc[TCH];
+#pragma unroll
+      for (int i = 0; i < TCH; ++i) {
+        float acc = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const float k0 = in_bits_to_f32((uint16_t)(kw[i][k] & 0xffffu), g.in_bf16);
+          const float k1 = in_bits_to_f32((uint16_t)(kw[i][k] >> 16), g.in_bf16);
+          acc = fmaf(q0[k][0], cs[i][k].x * k0 - cs[i][k].y * k1, fmaf(q0[k][1], cs[i][k].y * k0 + cs[i][k].x * k1, acc));
+        }
+        sc[i] = acc;
+      }
+      uint32_t vw[TCH][2];
+#pragma unroll
+      for (int i = 0; i < TCH; ++i) {
+        const int t = min(t0 + i, nt - 1);
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          vw[i][k] = __ldg(reinterpret_cast<const unsigned int*>(tv + (uint64_t)t * a.tail_tok + 2 * (lane + 32 * k)));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1)
+#pragma unroll
+        for (int i = 0; i < TCH; ++i) sc[i] += __shfl_xor_sync(0xffffffffu, sc[i], off);
+      float cm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < TCH; ++i) {  // the same values in every lane
+        sc[i] = t0 + i < nt ? sc[i] * LOG2E_RSQRT_D : -INFINITY;
+        cm = fmaxf(cm, sc[i]);
+      }
+      if (cm > m) {
+        const float al = exp2f(m - cm);
+        l *= al;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) o[k] *= al;
+        m = cm;
+      }
+#pragma unroll
+      for (int i = 0; i < TCH; ++i) {
+        const float pt = exp2f(sc[i] - m);
+        l += pt;
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          o[2 * k] = fmaf(pt, in_bits_to_f32((uint16_t)(vw[i][k] & 0xffffu), g.in_bf16), o[2 * k]);
+          o[2 * k + 1] = fmaf(pt, in_bits_to_f32((uint16_t)(vw[i][k] >> 16), g.in_bf16), o[2 * k + 1]);
+        }
+      }
+    }
+    const uint64_t row = (uint64_t)hidx * a.rows_ph + (uint64_t)(a.rows_ph - 1);
+#pragma unroll
+    for (int k = 0; k < 2; ++k)
+      *reinterpret_cast<float2*>(a.ws_o + row * D + 2 * (lane + 32 * k)) = make_float2(o[2 * k], o[2 * k + 1]);
+    if (lane == 0) {
+      a.ws_m[row] = m;
+      a.ws_l[row] = l;
+    }
   }
 }
 
@@ -815,6 +935,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
     regs_dec<REGS_OTHER>();
     if (warp < PRODUCER_WARP) aux_warps<NBS, CSC>(a, sm, ring, rows, rows_stride, x0, n, tid - NW * 32);
     else if (warp == PRODUCER_WARP) producer<NBS>(a, sm, ring, x0, n, lane);
+    else tail_warp(a, warp - PRODUCER_WARP - 1, lane);
   }
 }
 
@@ -879,10 +1000,13 @@ long long kvq_nuq_ranges(const kvq::Geo& g) {
 // Partial rows each range writes per (b, query head): one per consumer warp.
 int kvq_nuq_parts_per_range() { return kvq::nuqdec::NW; }
 
-// slots: range slots per (b, query head); the workspace holds slots * NW partial rows each.
+// slots: range slots per (b, query head); the workspace holds, per (b, query head), slots * NW
+// partial rows of the cached blocks and then one row for the fp tail (rows_ph in all).
 cudaError_t kvq_launch_decode_nuq(const kvq::Geo& g, const uint8_t* base, const float* codebook, const uint16_t* q,
-                                  int n_blocks, long long ranges, long long slots, float* ws_m, float* ws_l,
-                                  float* ws_o, int* status, cudaStream_t st) {
+                                  int n_blocks, long long ranges, long long slots, long long rows_ph, float* ws_m,
+                                  float* ws_l, float* ws_o, int* status, const uint16_t* tail_k,
+                                  const uint16_t* tail_v, int n_tail, long long tail_bh, long long tail_tok,
+                                  cudaStream_t st) {
   using namespace kvq::nuqdec;
   const size_t smem = smem_bytes(g);
   auto fn = g.v_csc ? decode_nuq_kernel<NB, true> : decode_nuq_kernel<NB, false>;
@@ -892,6 +1016,8 @@ cudaError_t kvq_launch_decode_nuq(const kvq::Geo& g, const uint8_t* base, const 
   a.g = g; a.base = base; a.codebook = codebook; a.q = q; a.nb = n_blocks;
   a.total = (long long)g.B * g.H * n_blocks; a.n_ranges = (int)ranges; a.n_slots = (int)slots;
   a.ws_m = ws_m; a.ws_l = ws_l; a.ws_o = ws_o; a.status = status;
+  a.rows_ph = (int)rows_ph;
+  a.tail_k = tail_k; a.tail_v = tail_v; a.n_tail = n_tail; a.tail_bh = tail_bh; a.tail_tok = tail_tok;
   fn<<<(int)ranges, NTHREADS, smem, st>>>(a);
   return cudaGetLastError();
 }
