@@ -40,20 +40,20 @@ DECODES_PER_STEP = 128
 BENCH_LAYOUT = "mma"
 
 # DRAM traffic of the decode kernel per block record (dram__bytes_read.sum + dram__bytes_write.sum
-# of ncu captures of three launches, divided by the records one launch reads), by workload. A
+# of an ncu capture of one launch, divided by the records that launch reads), by workload. A
 # launch reads every record once, so the traffic of a full launch is this figure times its
 # records. Each entry holds the sources it was measured on (sha256 of the kernel file and the
 # shared header); once they change the traffic reads null until a new capture replaces it.
 # Captures and commands: profiles/dram_traffic_decode_kernels.md.
 PROFILED_TRAFFIC = {
-    2: {"bytes_per_record": 14870.6, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
-        "sha256_16": "339632d5d3b9c159", "capture": "same workload at L = 16384 (4096 records)"},
-    3: {"bytes_per_record": 9791.8, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "2c3fc1268b83079d", "capture": "full workload (8192 records)"},
-    4: {"bytes_per_record": 17071.1, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "2c3fc1268b83079d", "capture": "same workload at L = 4096 (8192 records)"},
-    5: {"bytes_per_record": 9288.4, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
-        "sha256_16": "2c3fc1268b83079d", "capture": "same workload at L = 65536 (16384 records)"},
+    2: {"bytes_per_record": 14882.0, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
+        "sha256_16": "cdc9bad174a1e259", "capture": "same workload at L = 16384 (4096 records)"},
+    3: {"bytes_per_record": 9955.2, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "26b1444736ac01df", "capture": "full workload (8192 records)"},
+    4: {"bytes_per_record": 17039.0, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "26b1444736ac01df", "capture": "same workload at L = 16384 (32768 records)"},
+    5: {"bytes_per_record": 9318.0, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
+        "sha256_16": "26b1444736ac01df", "capture": "same workload at L = 131072 (32768 records)"},
 }
 
 

@@ -81,7 +81,11 @@ typedef enum { KVQ_F16 = 0, KVQ_BF16 = 1 } kvq_dtype;
  *   KVQ_LAYOUT_MMA : the tensor-core decode's format: 2- and 4-bit value tiles hold one row per
  *                    channel; 3-bit tiles are bit planes in matrix-fragment order, 48 bytes per
  *                    128 codes ([KVQ] §9.3 byte count). The tensor-core decodes need this layout;
- *                    with KVQ_LAYOUT_ROWS every decode runs on the CUDA cores. */
+ *                    with KVQ_LAYOUT_ROWS every decode runs on the CUDA cores (~12 instructions
+ *                    per element, several times slower). KVQ_LAYOUT_ROWS stays the default (0)
+ *                    because it is the pages' byte layout; a caller who wants decode speed creates
+ *                    its caches with KVQ_LAYOUT_MMA. Of the nuq caches only 3-bit ones with
+ *                    pre-RoPE keys and one query head per KV head have a tensor-core decode. */
 typedef enum { KVQ_LAYOUT_ROWS = 0, KVQ_LAYOUT_MMA = 1 } kvq_code_layout;
 
 /* Cache configuration. All fields are read by kvq_layout / kvq_cache_init. */
