@@ -13,7 +13,10 @@
 //   8 consumer warps  : warp w owns tokens 16w..16w+15 of every block and keeps its own
 //                       flash-decode state (running max, sum, output), written as its own
 //                       partial (m, l, o[128]) at the end of each (b, h) segment; the combine
-//                       kernel merges the partials.
+//                       kernel merges the partials. They publish each block's probabilities;
+//   2 value-outlier warps: add the value outliers weighted by those probabilities into the
+//                       consumers' outlier vectors, off the consumers' dependency chain;
+//   1 tail warp       : attends the fp tail of the call (one warp per (b, head) over the grid).
 // The consumer warpgroups run with 168 registers per thread, the others with 88 (setmaxnreg).
 //
 // Keys ([KVQ] §3.2 pre-RoPE quantisation, Algorithm 1 dequantisation, worked example step 5):
@@ -30,7 +33,7 @@
 // Values ([KVQ] §3.7 value matvec): O[channel] = sum_t p_t s_t C[q] + sum_t p_t zp_t + outliers,
 // one m16n8k16 per 16 channels x the warp's 16 tokens with B = p*s in high/low fp16 columns; the
 // value outliers add p_t * v per channel in token order (a fixed sequence of fp32 additions, the
-// same for CSR and CSC value tiles).
+// same for CSR and CSC value tiles), by the value-outlier warps.
 // Softmax in base 2 with the running max per warp (rescaling only when the max grows).
 #include "kvq_internal.cuh"
 
@@ -43,6 +46,10 @@ constexpr int NW = 8;               // consumer warps (16 tokens of each block p
 constexpr int NAUX = 128;           // aux threads: two groups that take alternate blocks
 constexpr int AUX_GROUP = 64;       // threads of one aux group: one per channel pair, two tokens each
 constexpr int PRODUCER_WARP = NW + NAUX / 32;  // issues the bulk copies
+constexpr int TAIL_WARP = PRODUCER_WARP + 1;     // attends the fp tail
+constexpr int VOUT_WARP = TAIL_WARP + 1;         // first of the warps that add the value outliers
+constexpr int NVOUT = 2;
+static_assert(VOUT_WARP + NVOUT == 512 / 32, "warp roles fill the CTA");
 constexpr int NTHREADS = 512;       // 4 warpgroups: consumers (2), aux, producer
 // Register split (setmaxnreg): launched at 65536 / 512 = 128 per thread; the consumer warpgroups
 // take 168 and the others give back down to 88 (2 x 128 x 168 + 2 x 128 x 88 = 65536).
@@ -96,10 +103,14 @@ struct Smem {
   float2 rope_b[16][64];     // (cos, sin) of b * theta_i, b = 0..15 (fine): t = 16a + b
   float qb[2][D];            // per aux group: q rotated back by the block's start angle
   float outv[NW][D + 32];    // value outliers weighted by p, per consumer warp (+ a slot per lane)
-  int own[NW][D + 32];       // per consumer warp and channel: the lowest lane holding an entry of it (32: none)
+  int own[NW][D + 32];       // owner table per (consumer warp, channel) for the value-outlier batches (32: none)
+  float pub[NB][T];          // per stage: each token's probability p (relative to its warp's reference)
+  float alw[NB][NW];         // per stage and consumer warp: the factor its reference moved by (1: none)
   uint64_t rec_full[NB];     // record landed (bulk copies)
   uint64_t ops_full[NB];     // score operands, key-outlier terms and outlier tags ready (AUX_GROUP arrivals)
-  uint64_t empty[NB];        // the consumer warps are done with the stage (NW arrivals)
+  uint64_t empty[NB];        // the stage is free again (NW consumer + NVOUT value-outlier warp arrivals)
+  uint64_t p_full[NB];       // the block's probabilities are published (NW arrivals)
+  uint64_t vdone[NB];        // the block's value outliers are in outv (NVOUT arrivals)
   // followed by NB x rows_stride bytes, per stage: the token of each key outlier [round16(n)], the
   // run index of each value outlier [round16(n)] (token for CSR value tiles, channel for CSC ones)
   // and, for CSC value tiles, the permutation grouping the value entries by consumer warp (uint16
@@ -534,12 +545,15 @@ __device__ __forceinline__ void value_outlier_span(uint32_t sa, uint32_t rw, con
   }
 }
 
-// Entry k of the span for this lane (k >= e1: none): its channel c (D + lane when there is none,
-// a slot of the lane's own past the channels) and x = p_t * v for its token t (p from the token's
-// owner lane).
+// Entry k of [E0, E1) of a block's value outliers (k >= e1: none) for the value-outlier warps:
+// the offsets of its outv / owner-table slot (consumer warp t / 16 of its token t, its channel;
+// a lane without an entry gets a scratch slot of its own) and x = p_t * v with p read from the
+// probabilities the consumer warps published for the stage (pubs); scratch: the lane's own slot
+// offset. CSC value tiles take their
+// entries in the order the aux warps grouped them by consumer warp.
 template <bool CSC>
-__device__ __forceinline__ void value_outlier_load(uint32_t sa, uint32_t rw, const Geo& g, int k, int e1, float p0,
-                                                   float p1, int lane, int& c, float& x) {
+__device__ __forceinline__ void value_outlier_entry(uint32_t sa, uint32_t rw, const Geo& g, int k, int e1,
+                                                    uint32_t pubs, uint32_t scratch, uint32_t& slot, float& x) {
   const int n_out = g.n_out;
   const bool valid = k < e1;
   const int kk = valid ? k : 0;
@@ -554,55 +568,90 @@ __device__ __forceinline__ void value_outlier_load(uint32_t sa, uint32_t rw, con
     ch = (int)lds_u8(idx + kk);
   }
   const float v = h2f((uint16_t)lds_u16(csr + 2 * e));
-  const int src = 4 * (t & 7);
-  const float pa = __shfl_sync(0xffffffffu, p0, src), pb = __shfl_sync(0xffffffffu, p1, src);
-  c = valid ? (ch & (D - 1)) : D + lane;
-  x = ((t & 8) ? pb : pa) * v;
+  t &= T - 1;
+  slot = valid ? 4u * (uint32_t)((t >> 4) * (D + 32) + (ch & (D - 1))) : scratch;
+  x = lds_f32(pubs + 4 * (uint32_t)t) * v;
 }
 
-// Adds one batch of the span's entries (one per lane; c = D + lane for a lane without one) to the
-// warp's outv. The lanes post their ids to the warp's owner table at their channel (a shared-memory
-// atomic minimum) and read it back: the lowest lane of each channel adds its entry, with no
-// branch (a lane without an entry updates a slot of its own), and resets the slot. Returns the
-// other lanes (a channel hit twice or more in the batch), which the caller adds one after another
-// in lane order (value_outlier_rest) before the next batch. Within a channel the lanes' entries
-// are in token order (CSR: (token, channel) order; CSC: (channel, token) order), so every
-// channel's sum is the same sequence of fp32 additions, in token order, for both value-outlier
-// layouts and whatever the thread timing.
-__device__ __forceinline__ uint32_t value_outlier_batch(uint32_t outv, uint32_t own, int c, float x, int lane) {
-  const uint32_t slot = own + 4 * c;
-  asm volatile("red.shared.min.s32 [%0], %1;" ::"r"(slot), "r"(lane));
-  __syncwarp();
-  int o;
-  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(o) : "r"(slot));
-  const bool first = o == lane;  // always for a lane without an entry (its own slot)
-  const uint32_t addr = outv + 4 * (first ? c : D + lane);
-  sts_f32(addr, lds_f32(addr) + x);
-  __syncwarp();
-  asm volatile("st.shared.s32 [%0], %1;" ::"r"(slot), "r"(32));
-  return __ballot_sync(0xffffffffu, !first);
-}
+// The first token a consumer lane's probabilities belong to: 16w + gq (and that + 8).
+__device__ __forceinline__ int t0_of(int warp, int lane) { return 16 * warp + (lane >> 2); }
 
-// The left-over entries of a batch, one after another in lane order.
-__device__ __forceinline__ void value_outlier_rest(uint32_t outv, uint32_t rest, int c, float x, int lane) {
-  for (uint32_t m = rest; m; m &= m - 1) {
+// Value-outlier warps (NVOUT of them): for every block of the range, once the consumer warps have
+// published its probabilities, they add the block's value outliers (x = p_t * v per entry) to the
+// outv of the consumer warp that owns each token, in the consumers' place. Warp VOUT_WARP + i takes
+// the entries of consumer warps 4i..4i+3 (a contiguous run of entries), 32 entries per batch,
+// blocks in order. In a batch the lanes post their ids to the owner table at their (consumer warp,
+// channel) slot (a shared-memory atomic minimum) and read it back: the lowest lane of each slot
+// adds its entry with no branch (a lane without an entry updates a scratch slot of its own) and
+// resets the slot; the others (a slot hit twice or more) follow one after another in lane order.
+// Within a slot the lanes' entries are in token order (CSR: (token, channel) order; CSC: grouped by
+// consumer warp, then (channel, token) order), so every channel's sum is the same sequence of fp32
+// additions, in token order, for both value-outlier layouts and whatever the thread timing.
+// A consumer warp's reference move at block j reaches its outv first (scaled by the published
+// factor), so outv stays relative to the consumer's current reference. A consumer reads its outv
+// at the end of a segment after vdone of the segment's last block. These warps hold each stage
+// until they are done with it (arrivals on empty).
+template <int NBS, bool CSC>
+__device__ void vout_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows, int rows_stride, int n, int wi,
+                           int lane) {
+  const Geo& g = a.g;
+  const int n_out = g.n_out;
+  const uint32_t sb = stage_bytes(g);
+  const uint32_t ring_sa = smem_u32(ring), rows_sa = smem_u32(rows);
+  const uint32_t vtag_ofs = (uint32_t)round16((uint64_t)n_out);
+  const uint32_t outv0 = smem_u32(&sm->outv[0][0]), own0 = smem_u32(&sm->own[0][0]);
+  constexpr int WPV = NW / NVOUT;  // consumer warps per value-outlier warp
+  // a slot of this lane's own past the channels of its first consumer warp (lanes without an entry)
+  const uint32_t scratch = 4u * (uint32_t)(WPV * wi * (D + 32) + D + lane);
+  for (int i = 0; i < n; ++i) {
+    const int s = i % NBS;
+    const bool got = helper_wait(&sm->p_full[s], (uint32_t)((i / NBS) & 1), a.status, g.wait_cycles);
+    if (__any_sync(0xffffffffu, !got)) return;  // the consumers time out on their own waits
+    const uint32_t sa = ring_sa + (uint32_t)s * sb;
+    const uint32_t rw = rows_sa + (uint32_t)s * (uint32_t)rows_stride + vtag_ofs;
+    const uint32_t pubs = smem_u32(&sm->pub[s][0]);
+#pragma unroll
+    for (int k = 0; k < WPV; ++k) {  // reference moves first
+      const int w = WPV * wi + k;
+      const float al = sm->alw[s][w];
+      if (al != 1.0f) {  // warp-uniform
+        const uint32_t outv = outv0 + 4u * (uint32_t)(w * (D + 32));
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t o = outv + 4 * (lane + 32 * q);
+          sts_f32(o, lds_f32(o) * al);
+        }
+      }
+    }
     __syncwarp();
-    if (lane == __ffs(m) - 1) sts_f32(outv + 4 * c, lds_f32(outv + 4 * c) + x);
-  }
-  __syncwarp();
-}
-
-// Entries past the span's first 32: whole batches of 32, each finished (first lanes, then the rest
-// in lane order) before the next.
-template <bool CSC>
-__device__ __forceinline__ void value_outlier_more(uint32_t sa, uint32_t rw, uint32_t outv, uint32_t own, const Geo& g,
-                                                   int e0, int e1, float p0, float p1, int lane) {
-  for (int kb = e0 + 32; kb < e1; kb += 32) {
-    int c;
-    float x;
-    value_outlier_load<CSC>(sa, rw, g, kb + lane, e1, p0, p1, lane, c, x);
-    const uint32_t rest = value_outlier_batch(outv, own, c, x, lane);
-    if (rest) value_outlier_rest(outv, rest, c, x, lane);
+    int e0, e1, d0, d1;
+    value_outlier_span<CSC>(sa, rw, g, WPV * wi, e0, d0);
+    value_outlier_span<CSC>(sa, rw, g, WPV * wi + WPV - 1, d1, e1);
+    for (int kb = e0; kb < e1; kb += 32) {  // batches of 32, each finished before the next
+      uint32_t slot;
+      float x;
+      value_outlier_entry<CSC>(sa, rw, g, kb + lane, e1, pubs, scratch, slot, x);
+      const uint32_t os = own0 + slot, vs = outv0 + slot;
+      asm volatile("red.shared.min.s32 [%0], %1;" ::"r"(os), "r"(lane));
+      __syncwarp();
+      int o;
+      asm volatile("ld.shared.s32 %0, [%1];" : "=r"(o) : "r"(os));
+      const bool first = o == lane;  // always for a lane without an entry (its own slot)
+      const uint32_t addr = first ? vs : outv0 + scratch;
+      sts_f32(addr, lds_f32(addr) + x);
+      __syncwarp();
+      asm volatile("st.shared.s32 [%0], %1;" ::"r"(os), "r"(32));
+      const uint32_t rest = __ballot_sync(0xffffffffu, !first);
+      for (uint32_t m = rest; m; m &= m - 1) {  // a slot hit twice or more: in lane order
+        __syncwarp();
+        if (lane == __ffs(m) - 1) sts_f32(vs, lds_f32(vs) + x);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) {
+      mbar_arrive(&sm->vdone[s]);
+      mbar_arrive(&sm->empty[s]);
+    }
   }
 }
 
@@ -633,7 +682,9 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
   // shared-window addresses: stage bases and the lane's fixed offsets in a stage / operand block
   const uint32_t ring_sa = smem_u32(ring), ops_sa = smem_u32(&sm->op[0]);
   const uint32_t rows_sa = smem_u32(rows);
-  const uint32_t outv = smem_u32(&sm->outv[warp][0]), own = smem_u32(&sm->own[warp][0]);
+  const uint32_t outv = smem_u32(&sm->outv[warp][0]);
+  const uint32_t pub0 = smem_u32(&sm->pub[0][t0_of(warp, lane)]), alw0 = smem_u32(&sm->alw[0][warp]);
+  float alf = 1.0f;  // the factor the warp's reference moved by in this block
   const uint32_t vtag_ofs = (uint32_t)round16((uint64_t)g.n_out);
   const uint32_t kofs = g.codes_off[0] + warp * 768 + lane * 24, vofs = g.codes_off[1] + warp * 768 + lane * 24;
   const uint32_t vmofs = g.meta_off[1] + 2 * t0;
@@ -723,44 +774,32 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
         }
         l_w *= al;
         z_w *= al;
-        __syncwarp();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const uint32_t o = outv + 4 * (lane + 32 * k);
-          sts_f32(o, lds_f32(o) * al);
-        }
-        __syncwarp();
+        alf = al;
         m_w = mloc;
       }
       const float p0 = fast_exp2(sv0 - m_w), p1 = fast_exp2(sv1 - m_w);
       l_w += p0 + p1;
-      // value outliers: the first 32 entries of the warp's span as one branch-free batch placed
-      // with the tensor-core work; what is left (channels hit twice or more, entries past the
-      // first 32) after it, on warp-uniform paths
-      const uint32_t rw = rows_sa + (uint32_t)s * (uint32_t)rows_stride + vtag_ofs;
-      uint32_t rest = 0;
-      int c1 = D + lane;
-      float x1 = 0.0f;
-      bool more_batches = false;
-      if (vout) {
-        int e0, e1;
-        value_outlier_span<CSC>(sa, rw, g, warp, e0, e1);
-        value_outlier_load<CSC>(sa, rw, g, e0 + lane, e1, p0, p1, lane, c1, x1);
-        rest = value_outlier_batch(outv, own, c1, x1, lane);
-        more_batches = e1 - e0 > 32;
+      if (vout) {  // publish the block's probabilities and reference move for the value-outlier warps
+        if (tq == 0) {
+          sts_f32(pub0 + (uint32_t)s * (T * 4), p0);
+          sts_f32(pub0 + (uint32_t)s * (T * 4) + 32, p1);
+        }
+        if (lane == 0) sts_f32(alw0 + (uint32_t)s * (NW * 4), alf);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm->p_full[s]);
+        alf = 1.0f;
       }
       block_values(sa + vofs, sa + vmofs, src_a, xsel, ysel, p0, p1, tl0, tl1, th0, th1, z_w, acc);
-      if (rest) value_outlier_rest(outv, rest, c1, x1, lane);
-      if (more_batches) {
-        int e0, e1;
-        value_outlier_span<CSC>(sa, rw, g, warp, e0, e1);
-        value_outlier_more<CSC>(sa, rw, outv, own, g, e0, e1, p0, p1, lane);
-      }
       release(s);
       sv0 = nv0;
       sv1 = nv1;
     }
-    // the segment's partial row
+    // the segment's partial row (its value outliers are in outv once vdone of its last block passed)
+    if (vout) {
+      const int jl = iend - 1;
+      const bool got = mbar_wait_bounded(&sm->vdone[jl % NBS], (uint32_t)((jl / NBS) & 1), a.status, g.wait_cycles);
+      if (__any_sync(0xffffffffu, !got)) return;
+    }
     {
       float lt = l_w, zt = z_w;  // replicated over tq: reduce over gq only
 #pragma unroll
@@ -800,7 +839,7 @@ __device__ void consumer(const Args& a, Smem* sm, const uint8_t* ring, const uin
 // are stored before RoPE like the cache's: the score is (R(n0)^T q) . (R(t) k_t), the in-block
 // angles from the cache's table. Lane l holds channel pairs l and l + 32. It reads only the call's
 // inputs and the angle tables, so it runs beside the ring without waiting on it.
-constexpr int IDLE = NTHREADS / 32 - PRODUCER_WARP - 1;
+constexpr int IDLE = 1;  // warps per CTA that attend the tail
 constexpr int TCH = 6;  // tail tokens per chunk (the idle warps run with 88 registers)
 __device__ void tail_warp(const Args& a, int wi, int lane) {
   const Geo& g = a.g;
@@ -923,7 +962,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
     for (int s = 0; s < NBS; ++s) {
       mbar_init(&sm->rec_full[s], 1);
       mbar_init(&sm->ops_full[s], AUX_GROUP);
-      mbar_init(&sm->empty[s], NW);
+      mbar_init(&sm->empty[s], NW + (a.g.n_out > 0 ? NVOUT : 0));
+      mbar_init(&sm->p_full[s], NW);
+      mbar_init(&sm->vdone[s], NVOUT);
     }
     fence_mbar_init();
   }
@@ -935,7 +976,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
     regs_dec<REGS_OTHER>();
     if (warp < PRODUCER_WARP) aux_warps<NBS, CSC>(a, sm, ring, rows, rows_stride, x0, n, tid - NW * 32);
     else if (warp == PRODUCER_WARP) producer<NBS>(a, sm, ring, x0, n, lane);
-    else tail_warp(a, warp - PRODUCER_WARP - 1, lane);
+    else if (warp == TAIL_WARP) tail_warp(a, 0, lane);
+    else if (a.g.n_out > 0) vout_warps<NBS, CSC>(a, sm, ring, rows, rows_stride, n, warp - VOUT_WARP, lane);
   }
 }
 
