@@ -47,7 +47,7 @@ BENCH_LAYOUT = "mma"
 # Captures and commands: profiles/dram_traffic_decode_kernels.md.
 PROFILED_TRAFFIC = {
     2: {"bytes_per_record": 14882.0, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
-        "sha256_16": "cdc9bad174a1e259", "capture": "same workload at L = 16384 (4096 records)"},
+        "sha256_16": "6dd94604caffb0d1", "capture": "same workload at L = 16384 (4096 records)"},
     3: {"bytes_per_record": 9955.2, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
         "sha256_16": "26b1444736ac01df", "capture": "full workload (8192 records)"},
     4: {"bytes_per_record": 17039.0, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),

@@ -157,6 +157,8 @@ DECODE_CASES = [
     ("nuq3_rope", WL.WORKLOADS[2], dict(batch=1, n_kv_heads=3, n_q_heads=3, ctx=6 * 128), [0, 1, 127]),
     ("nuq3_rope_ragged_ranges", WL.WORKLOADS[2], dict(batch=3, n_kv_heads=5, n_q_heads=5, ctx=37 * 128), [0, 77]),
     ("nuq3_rope_5pct", WL.WORKLOADS[2], dict(outlier_frac=0.05, batch=1, n_kv_heads=2, n_q_heads=2, ctx=9 * 128), [3]),
+    # more (b, head) pairs than the nuq decode has CTAs: its tail warps loop over heads
+    ("nuq3_rope_160_heads", WL.WORKLOADS[2], dict(batch=10, n_kv_heads=16, n_q_heads=16, ctx=2 * 128), [0, 50, 127]),
     ("nuq3_rope_no_outliers", WL.WORKLOADS[2], dict(outlier_frac=0.0, batch=2, n_kv_heads=2, n_q_heads=2, ctx=4 * 128), [0]),
     ("nuq3_norope_gqa", WL.WORKLOADS[2], dict(pre_rope=False, batch=2, n_kv_heads=2, n_q_heads=4, ctx=3 * 128), [9]),
     ("varn2_gqa", WL.WORKLOADS[3], dict(batch=2, n_kv_heads=2, n_q_heads=8, ctx=4 * 128), [0, 100]),
