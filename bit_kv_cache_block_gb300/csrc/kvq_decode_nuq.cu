@@ -350,6 +350,8 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
       }
       bar_group(grp);  // q_b and the key tags visible
       if (CSC) {  // group the value entries by consumer warp (16 tokens each): count, offsets, scatter
+        // (the scatter keeps each group in the tile's (channel, token) order, which the value-outlier
+        // sums rely on to run in token order per channel)
         const uint8_t* vtok = st + g.csr_off[1] + 2 * n_out + 2 * (T + 1);  // token of each entry
         uint16_t* perm = reinterpret_cast<uint16_t*>(vtag + tag_bytes);
         uint16_t* off = reinterpret_cast<uint16_t*>(vtag + csc_off_of(n_out));
@@ -366,7 +368,19 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
           off[8] = (uint16_t)acc;
         }
         bar_group(grp);
-        for (int e = j; e < n_v; e += 64) perm[atomicAdd(&gcnt[8 + ((vtok[e] >> 4) & 7)], 1)] = (uint16_t)e;
+        if (j < 32) {  // one warp scatters in entry order, so each group keeps the tile's order
+          for (int eb = 0; eb < n_v; eb += 32) {
+            const int e = eb + j;
+            const bool valid = e < n_v;
+            const int w = valid ? ((vtok[e] >> 4) & 7) : 8 + j;  // lanes past the end: keys of their own
+            const uint32_t m = __match_any_sync(0xffffffffu, w);
+            const int rank = __popc(m & ((1u << j) - 1u));       // earlier entries of the same group
+            if (valid) perm[gcnt[8 + w] + rank] = (uint16_t)e;
+            __syncwarp();
+            if (valid && rank == 0) gcnt[8 + w] += __popc(m);
+            __syncwarp();
+          }
+        }
       }
       const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
       const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
