@@ -361,3 +361,18 @@ def test_calibrated_keys_and_sink_layout_and_checks(K):
     assert lib.kvq_calibrate_keys(C.byref(cache), C.c_void_p(0x1008), 64, None) == L.KVQ_ERR_ALIGNMENT
     cache.cfg = mk()
     assert lib.kvq_calibrate_keys(C.byref(cache), k, 64, None) == L.KVQ_ERR_INVALID_ARG        # no key_calib
+
+
+def test_nuq_decode_workspace_holds_the_tail_row(K):
+    """The 3-bit nuq pre-RoPE decode (tensor-core format) keeps, per (batch, query head), one
+    partial row per consumer warp and range slot plus one row for the fp tail its idle warps
+    attend. Without a device the plan assumes a 152-SM part with one CTA per SM."""
+    w = WL.WORKLOADS[2]
+    cfg = K.make_config(w.method, w.bits, w.batch, w.n_kv_heads, w.n_q_heads, w.n_blocks, w.dtype, w.pre_rope,
+                        w.rope_theta, w.outlier_frac, layout="mma")
+    for nb in (1, 3, 200, w.n_blocks):
+        total = w.batch * w.n_kv_heads * nb
+        ranges = min(152, total)
+        slots = min((nb - 1) * ranges // total + 2, nb)
+        rows = w.batch * w.n_q_heads * (slots * 8 + 1)   # 8 consumer warps per range, + the tail row
+        assert K.kvq_decode_workspace_bytes(cfg, nb) == 4 * (2 * rows + 4 + rows * 128), nb
