@@ -46,8 +46,8 @@ BENCH_LAYOUT = "mma"
 # shared header); once they change the traffic reads null until a new capture replaces it.
 # Captures and commands: profiles/dram_traffic_decode_kernels.md.
 PROFILED_TRAFFIC = {
-    2: {"bytes_per_record": 14880.5, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
-        "sha256_16": "6181951015155688", "capture": "same workload at L = 16384 (4096 records)"},
+    2: {"bytes_per_record": 14879.5, "sources": ("kvq_decode_nuq.cu", "kvq_internal.cuh"),
+        "sha256_16": "1ed2f05845bc2c91", "capture": "same workload at L = 16384 (4096 records)"},
     3: {"bytes_per_record": 9955.2, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),
         "sha256_16": "26b1444736ac01df", "capture": "full workload (8192 records)"},
     4: {"bytes_per_record": 17039.0, "sources": ("kvq_decode_mma.cu", "kvq_internal.cuh"),

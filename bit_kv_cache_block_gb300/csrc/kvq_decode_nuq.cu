@@ -111,11 +111,9 @@ struct Smem {
   uint64_t empty[NB];        // the stage is free again (NW consumer + NVOUT value-outlier warp arrivals)
   uint64_t p_full[NB];       // the block's probabilities are published (NW arrivals)
   uint64_t vdone[NB];        // the block's value outliers are in outv (NVOUT arrivals)
-  // followed by NB x rows_stride bytes, per stage: the token of each key outlier [round16(n)], the
-  // run index of each value outlier [round16(n)] (token for CSR value tiles, channel for CSC ones)
-  // and, for CSC value tiles, the permutation grouping the value entries by consumer warp (uint16
-  // [n], 16-byte padded) and the 9 group offsets (uint16, 32 bytes); then per aux group round16(n)
-  // floats (the score term of each key outlier) and, for CSC value tiles, 16 int counters
+  // followed by NB x rows_stride bytes, per stage: the token of each key outlier [round16(n)] and the
+  // run index of each value outlier [round16(n)] (token for CSR value tiles, channel for CSC ones);
+  // then per aux group round16(n) floats (the score term of each key outlier)
 };
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -191,15 +189,9 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 // Per-stage outlier area (after the ring and Smem): the token tag of each key outlier
-// [round16(n)], the run index of each value outlier [round16(n)] (token for CSR value tiles,
-// channel for CSC ones), and for CSC value tiles the permutation grouping the value entries by
-// consumer warp (uint16 [n], 16-byte padded) followed by the 9 group offsets (uint16, 32 bytes).
-__host__ __device__ inline int csc_off_of(int n_out) {  // from the value tags to the offsets
-  return (int)round16((uint64_t)n_out) + (int)round16(2 * (uint64_t)n_out);
-}
-__host__ __device__ inline int rows_stride_of(int n_out, bool csc) {
-  return 2 * (int)round16((uint64_t)n_out) + (csc ? (int)round16(2 * (uint64_t)n_out) + 32 : 0);
-}
+// [round16(n)] and the run index of each value outlier [round16(n)] (its token for CSR value tiles,
+// its channel for CSC ones).
+__host__ __device__ inline int rows_stride_of(int n_out) { return 2 * (int)round16((uint64_t)n_out); }
 
 // (the memory clobber keeps loads of the role code below the register split)
 template <uint32_t R>
@@ -273,7 +265,7 @@ __device__ void producer(const Args& a, Smem* sm, uint8_t* ring, long long x0, i
 // computes the score terms of the key-outlier entries e = j, j + 64, ...
 //     v * (R(t)^T q_b)_c    (entry e = (t, c, v) of the CSR)
 // and, after a group barrier, the sum sk[t] of each of its two tokens' terms in entry order.
-// The consumers add p_t * v for the value outliers.
+// The value-outlier warps add p_t * v for the value outliers, with the tags written here.
 template <int NBS, bool CSC>
 __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows, int rows_stride, long long x0,
                           int n, int ax) {
@@ -296,9 +288,6 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
   float2 cs_next = grp < n ? __ldg(rope_blk + (size_t)blk * 64 + j) : make_float2(1.0f, 0.0f);
   float* qb = sm->qb[grp];
   float* kterm = reinterpret_cast<float*>(rows + (size_t)NBS * rows_stride) + grp * tag_bytes;  // per group
-  // CSC value tiles: per group, entries per consumer warp [8] and the scatter cursors [8]
-  int* gcnt = reinterpret_cast<int*>(reinterpret_cast<float*>(rows + (size_t)NBS * rows_stride) + 2 * tag_bytes) +
-              grp * 16;
   const int tA = j, tB = j + 64;
   for (int p = grp; p < n; p += 2) {
     if (u != cur_u) {
@@ -346,42 +335,8 @@ __device__ void aux_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows,
         for (int e = kb0; e < kb1; ++e) ktag[e] = (uint8_t)tB;
         for (int e = va0; e < va1; ++e) vtag[e] = (uint8_t)tA;
         for (int e = vb0; e < vb1; ++e) vtag[e] = (uint8_t)tB;
-        if (CSC && j < 16) gcnt[j] = 0;
       }
       bar_group(grp);  // q_b and the key tags visible
-      if (CSC) {  // group the value entries by consumer warp (16 tokens each): count, offsets, scatter
-        // (the scatter keeps each group in the tile's (channel, token) order, which the value-outlier
-        // sums rely on to run in token order per channel)
-        const uint8_t* vtok = st + g.csr_off[1] + 2 * n_out + 2 * (T + 1);  // token of each entry
-        uint16_t* perm = reinterpret_cast<uint16_t*>(vtag + tag_bytes);
-        uint16_t* off = reinterpret_cast<uint16_t*>(vtag + csc_off_of(n_out));
-        const int n_v = min((int)rpv[T], n_out);
-        for (int e = j; e < n_v; e += 64) atomicAdd(&gcnt[(vtok[e] >> 4) & 7], 1);
-        bar_group(grp);
-        if (j == 0) {
-          int acc = 0;
-          for (int w = 0; w < 8; ++w) {
-            off[w] = (uint16_t)acc;
-            gcnt[8 + w] = acc;
-            acc += gcnt[w];
-          }
-          off[8] = (uint16_t)acc;
-        }
-        bar_group(grp);
-        if (j < 32) {  // one warp scatters in entry order, so each group keeps the tile's order
-          for (int eb = 0; eb < n_v; eb += 32) {
-            const int e = eb + j;
-            const bool valid = e < n_v;
-            const int w = valid ? ((vtok[e] >> 4) & 7) : 8 + j;  // lanes past the end: keys of their own
-            const uint32_t m = __match_any_sync(0xffffffffu, w);
-            const int rank = __popc(m & ((1u << j) - 1u));       // earlier entries of the same group
-            if (valid) perm[gcnt[8 + w] + rank] = (uint16_t)e;
-            __syncwarp();
-            if (valid && rank == 0) gcnt[8 + w] += __popc(m);
-            __syncwarp();
-          }
-        }
-      }
       const uint16_t* val = reinterpret_cast<const uint16_t*>(csr);
       const uint8_t* col = csr + 2 * n_out + 2 * (T + 1);
       const int n_k = min((int)rp[T], n_out);
@@ -541,50 +496,42 @@ __device__ __forceinline__ void block_values(uint32_t va, uint32_t vma, int src_
   }
 }
 
-// Value outliers of a consumer warp's tokens in one block: the span [e0, e1) of its entries. rw:
-// the stage's value-outlier area written by the aux warps: each entry's pointer-run index (the
-// token for CSR tiles, the channel for CSC tiles), then for CSC tiles a permutation of the
-// entries that groups them by consumer warp (16 tokens each) and the 9 group offsets.
-template <bool CSC>
-__device__ __forceinline__ void value_outlier_span(uint32_t sa, uint32_t rw, const Geo& g, int warp, int& e0, int& e1) {
+// CSR value tiles: the span [e0, e1) of the entries of consumer warp `warp`'s tokens (16w..16w+15)
+// in one block, from the tile's row pointers.
+__device__ __forceinline__ void value_outlier_span(uint32_t sa, const Geo& g, int warp, int& e0, int& e1) {
   const int n_out = g.n_out;
-  if (CSC) {
-    const uint32_t off = rw + (uint32_t)csc_off_of(n_out);
-    e0 = (int)lds_u16(off + 2 * warp);
-    e1 = (int)lds_u16(off + 2 * warp + 2);
-  } else {
-    const uint32_t rp = sa + g.csr_off[1] + 2 * n_out;
-    e0 = min((int)lds_u16(rp + 32 * warp), n_out);
-    e1 = min((int)lds_u16(rp + 32 * warp + 32), n_out);
-  }
+  const uint32_t rp = sa + g.csr_off[1] + 2 * n_out;
+  e0 = min((int)lds_u16(rp + 32 * warp), n_out);
+  e1 = min((int)lds_u16(rp + 32 * warp + 32), n_out);
 }
 
-// Entry k of [E0, E1) of a block's value outliers (k >= e1: none) for the value-outlier warps:
-// the offsets of its outv / owner-table slot (consumer warp t / 16 of its token t, its channel;
-// a lane without an entry gets a scratch slot of its own) and x = p_t * v with p read from the
-// probabilities the consumer warps published for the stage (pubs); scratch: the lane's own slot
-// offset. CSC value tiles take their
-// entries in the order the aux warps grouped them by consumer warp.
+// Entry k of [e0, e1) of a block's value outliers (k >= e1: none) for value-outlier warp `half`
+// (consumer warps 4 half .. 4 half + 3, tokens 64 half .. 64 half + 63): the offset of its outv /
+// owner-table slot (consumer warp t / 16 of its token t, its channel; a lane without an entry gets
+// a scratch slot of its own, `scratch`) and x = p_t * v with p read from the probabilities the
+// consumer warps published for the stage (pubs). rw: the stage's run index of each entry, written
+// by the aux warps (CSR: its token; CSC: its channel). CSR tiles give each warp a contiguous run of
+// entries; a CSC tile is read whole, in its (channel, token) order, by both warps, each keeping
+// the entries of its own tokens.
 template <bool CSC>
-__device__ __forceinline__ void value_outlier_entry(uint32_t sa, uint32_t rw, const Geo& g, int k, int e1,
+__device__ __forceinline__ void value_outlier_entry(uint32_t sa, uint32_t rw, const Geo& g, int k, int e1, int half,
                                                     uint32_t pubs, uint32_t scratch, uint32_t& slot, float& x) {
   const int n_out = g.n_out;
-  const bool valid = k < e1;
-  const int kk = valid ? k : 0;
+  const int kk = k < e1 ? k : 0;
   const uint32_t csr = sa + g.csr_off[1], idx = csr + 2 * n_out + 2 * (T + 1);  // idx: CSR channel, CSC token
-  int e = kk, t, ch;
+  int t, ch;
   if (CSC) {
-    e = min((int)lds_u16(rw + (uint32_t)round16((uint64_t)n_out) + 2 * kk), n_out - 1);
-    t = (int)lds_u8(idx + e);
-    ch = (int)lds_u8(rw + e);
+    t = (int)lds_u8(idx + kk);
+    ch = (int)lds_u8(rw + kk);
   } else {
     t = (int)lds_u8(rw + kk);
     ch = (int)lds_u8(idx + kk);
   }
-  const float v = h2f((uint16_t)lds_u16(csr + 2 * e));
+  const float v = h2f((uint16_t)lds_u16(csr + 2 * kk));
   t &= T - 1;
+  const bool valid = k < e1 && (!CSC || (t >> 6) == half);
   slot = valid ? 4u * (uint32_t)((t >> 4) * (D + 32) + (ch & (D - 1))) : scratch;
-  x = lds_f32(pubs + 4 * (uint32_t)t) * v;
+  x = lds_f32(pubs + 4 * (uint32_t)t) * v;  // (lanes without an entry of their own add into scratch)
 }
 
 // The first token a consumer lane's probabilities belong to: 16w + gq (and that + 8).
@@ -593,14 +540,14 @@ __device__ __forceinline__ int t0_of(int warp, int lane) { return 16 * warp + (l
 // Value-outlier warps (NVOUT of them): for every block of the range, once the consumer warps have
 // published its probabilities, they add the block's value outliers (x = p_t * v per entry) to the
 // outv of the consumer warp that owns each token, in the consumers' place. Warp VOUT_WARP + i takes
-// the entries of consumer warps 4i..4i+3 (a contiguous run of entries), 32 entries per batch,
-// blocks in order. In a batch the lanes post their ids to the owner table at their (consumer warp,
+// the entries of consumer warps 4i..4i+3 (tokens 64i..64i+63: a contiguous run of a CSR tile; a
+// CSC tile is read whole, keeping those tokens), 32 entries per batch, blocks in order. In a batch the lanes post their ids to the owner table at their (consumer warp,
 // channel) slot (a shared-memory atomic minimum) and read it back: the lowest lane of each slot
 // adds its entry with no branch (a lane without an entry updates a scratch slot of its own) and
 // resets the slot; the others (a slot hit twice or more) follow one after another in lane order.
-// Within a slot the lanes' entries are in token order (CSR: (token, channel) order; CSC: grouped by
-// consumer warp, then (channel, token) order), so every channel's sum is the same sequence of fp32
-// additions, in token order, for both value-outlier layouts and whatever the thread timing.
+// Within a slot the lanes' entries are in token order (CSR: (token, channel) order; CSC: (channel,
+// token) order), so every channel's sum is the same sequence of fp32 additions, in token order, for
+// both value-outlier layouts and whatever the thread timing.
 // A consumer warp's reference move at block j reaches its outv first (scaled by the published
 // factor), so outv stays relative to the consumer's current reference. A consumer reads its outv
 // at the end of a segment after vdone of the segment's last block. These warps hold each stage
@@ -638,13 +585,19 @@ __device__ void vout_warps(const Args& a, Smem* sm, uint8_t* ring, uint8_t* rows
       }
     }
     __syncwarp();
-    int e0, e1, d0, d1;
-    value_outlier_span<CSC>(sa, rw, g, WPV * wi, e0, d0);
-    value_outlier_span<CSC>(sa, rw, g, WPV * wi + WPV - 1, d1, e1);
+    int e0, e1;
+    if (CSC) {  // the whole tile, in column order
+      e0 = 0;
+      e1 = min((int)lds_u16(sa + g.csr_off[1] + 2 * n_out + 2 * T), n_out);
+    } else {    // the run of consumer warps WPV wi .. WPV wi + WPV - 1
+      int d0, d1;
+      value_outlier_span(sa, g, WPV * wi, e0, d0);
+      value_outlier_span(sa, g, WPV * wi + WPV - 1, d1, e1);
+    }
     for (int kb = e0; kb < e1; kb += 32) {  // batches of 32, each finished before the next
       uint32_t slot;
       float x;
-      value_outlier_entry<CSC>(sa, rw, g, kb + lane, e1, pubs, scratch, slot, x);
+      value_outlier_entry<CSC>(sa, rw, g, kb + lane, e1, wi, pubs, scratch, slot, x);
       const uint32_t os = own0 + slot, vs = outv0 + slot;
       asm volatile("red.shared.min.s32 [%0], %1;" ::"r"(os), "r"(lane));
       __syncwarp();
@@ -959,7 +912,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
   uint8_t* ring = smem_raw;
   Smem* sm = reinterpret_cast<Smem*>(smem_raw + (size_t)NBS * stage_bytes(a.g));
   uint8_t* rows = reinterpret_cast<uint8_t*>(sm + 1);
-  const int rows_stride = rows_stride_of(a.g.n_out, CSC);
+  const int rows_stride = rows_stride_of(a.g.n_out);
   const long long R = blockIdx.x;
   if (R >= a.n_ranges) return;
   const long long x0 = R * a.total / a.n_ranges, x1 = (R + 1) * a.total / a.n_ranges;
@@ -996,8 +949,8 @@ __global__ void __launch_bounds__(NTHREADS, 1) decode_nuq_kernel(Args a) {
 }
 
 size_t smem_bytes(const Geo& g) {
-  return (size_t)NB * (size_t)g.rec_bytes + sizeof(Smem) + (size_t)NB * rows_stride_of(g.n_out, g.v_csc) +
-         2 * sizeof(float) * round16((uint64_t)g.n_out) + (g.v_csc ? 2 * 16 * sizeof(int) : 0);
+  return (size_t)NB * (size_t)g.rec_bytes + sizeof(Smem) + (size_t)NB * rows_stride_of(g.n_out) +
+         2 * sizeof(float) * round16((uint64_t)g.n_out);
 }
 
 }  // namespace nuqdec
