@@ -366,12 +366,9 @@ constexpr bool early_release() { return BITS == 4 && !G64; }
 #ifndef KVQ_MMA2_G1_MINB
 #define KVQ_MMA2_G1_MINB 1
 #endif
-#ifndef KVQ_MMA2_MINB
-#define KVQ_MMA2_MINB 1
-#endif
 template <int BITS, int GT, bool G64>
 constexpr int min_ctas() {
-  return early_release<BITS, G64>() ? 2 : BITS == 2 ? (GT == 1 ? KVQ_MMA2_G1_MINB : KVQ_MMA2_MINB) : 1;
+  return early_release<BITS, G64>() ? 2 : (BITS == 2 && GT == 1) ? KVQ_MMA2_G1_MINB : 1;
 }
 
 template <int METHOD, int BITS, int GT, int NW, int NB, bool WHOLE, bool G64>
